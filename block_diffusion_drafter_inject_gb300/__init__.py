@@ -1,0 +1,25 @@
+"""GB300-native DFlash 2 draft cycle: a C-ABI CUDA library (sm_103a) and its binding.
+
+    inject_context  target hidden states -> per-layer paged draft KV
+    draft_block     one non-causal drafter pass over a block, per-position top-k
+    select_path     low-rank bilinear Viterbi over the candidate lattice
+    accept_greedy   longest prefix matching the target's argmax + bonus token
+"""
+
+from . import _lib  # noqa: F401
+from ._lib import DFlashError, lib  # noqa: F401
+from .api import (  # noqa: F401
+    DeviceWeights,
+    DraftCycle,
+    PagedKV,
+    Workspace,
+    accept_greedy,
+    clear_device_status,
+    draft_block,
+    inject_context,
+    launch_count,
+    make_config,
+    read_device_status,
+    select_path,
+    workspace_bytes,
+)

@@ -1,0 +1,185 @@
+"""Python binding of the DFlash C ABI: argument marshalling only.
+
+Device memory comes from PyTorch (weights, paged KV, workspace, outputs); every
+step of the draft cycle runs in the library's CUDA kernels, launched on the
+current PyTorch stream.  The names follow include/dflash.h:
+inject_context, draft_block, select_path, accept_greedy."""
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import check, lib
+
+_DT = {"f32": _lib.F32, "bf16": _lib.BF16}
+_TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def make_config(cfg):
+    """dflash_config from a dimension dict (the presets' keys)."""
+    c = _lib.Config()
+    for name, _ in _lib.Config._fields_:
+        if name == "dtype":
+            c.dtype = _DT[cfg["dtype"]]
+        elif name == "mask_token_id":
+            c.mask_token_id = int(cfg.get("mask_token_id", cfg["vocab"] - 1))
+        else:
+            setattr(c, name, type(getattr(c, name))(cfg[name]))
+    return c
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+class DeviceWeights:
+    """Drafter weights resident on the GPU and the dflash_weights struct that points at them."""
+
+    def __init__(self, cfg, tensors):
+        self.cfg = cfg
+        self.t = tensors
+        w = _lib.Weights()
+        for n in ("fc_norm", "fc", "embed", "lm_head", "final_norm", "sel_pu", "sel_pv"):
+            setattr(w, n, tensors[n].data_ptr())
+        for l in range(cfg["n_layers"]):
+            L = w.layer[l]
+            p = f"layers.{l}."
+            for n in ("attn_norm", "mlp_norm", "wqkv", "wo", "q_norm", "k_norm", "w_gate_up",
+                      "w_down"):
+                setattr(L, n, tensors[p + n].data_ptr())
+            for i in range(4):
+                L.conv_w[i] = tensors[p + f"conv_w.{i}"].data_ptr()
+                L.conv_base[i] = tensors[p + f"conv_base.{i}"].data_ptr()
+        self.struct = w
+
+    @classmethod
+    def from_host(cls, cfg, host, device="cuda"):
+        """Upload float32 host arrays (holding storage-dtype values) in the config dtype."""
+        dt = _TORCH_DT[cfg["dtype"]]
+        t = {}
+        for name, arr in host.items():
+            t[name] = torch.from_numpy(arr).to(dt).to(device).contiguous()
+        return cls(cfg, t)
+
+
+class PagedKV:
+    """Per-layer paged K and V caches [L][num_pages][Hkv][page_size][d] and a page table."""
+
+    def __init__(self, cfg, page_table, num_pages, device="cuda"):
+        dt = _TORCH_DT[cfg["dtype"]]
+        shape = (cfg["n_layers"], int(num_pages), cfg["n_kv_heads"], cfg["page_size"],
+                 cfg["head_dim"])
+        self.k = torch.zeros(shape, dtype=dt, device=device)
+        self.v = torch.zeros(shape, dtype=dt, device=device)
+        self.page_table = torch.as_tensor(page_table, dtype=torch.int32).to(device).contiguous()
+        s = _lib.KV()
+        s.k = self.k.data_ptr()
+        s.v = self.v.data_ptr()
+        s.page_table = self.page_table.data_ptr()
+        s.num_pages = int(num_pages)
+        s.max_pages_per_req = int(self.page_table.shape[1])
+        s.num_rows = int(self.page_table.shape[0])
+        self.struct = s
+
+
+def workspace_bytes(cfg, B, K, max_inject_tokens):
+    c = make_config(cfg)
+    n = lib().dflash_workspace_bytes(ctypes.byref(c), B, K, max_inject_tokens)
+    if n == 0:
+        raise ValueError("invalid configuration or sizes for dflash_workspace_bytes")
+    return n
+
+
+class Workspace:
+    """Zero-filled device scratch for up to B requests of block K and max_inject_tokens."""
+
+    def __init__(self, cfg, B, K, max_inject_tokens, device="cuda"):
+        self.nbytes = workspace_bytes(cfg, B, K, max_inject_tokens)
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+
+def inject_context(cfg, W, kv, hidden, req, pos, ws, stream=None):
+    c = make_config(cfg)
+    check(lib().dflash_inject_context(ctypes.byref(c), ctypes.byref(W.struct),
+                                      ctypes.byref(kv.struct), _ptr(hidden), _ptr(req), _ptr(pos),
+                                      int(hidden.shape[0]), ws.ptr, ws.nbytes, _stream(stream)),
+          "dflash_inject_context")
+
+
+def draft_block(cfg, W, kv, anchor, ctx_len, K, ws, topk_ids, topk_logp, logits=None,
+                stream=None):
+    c = make_config(cfg)
+    check(lib().dflash_draft_block(ctypes.byref(c), ctypes.byref(W.struct),
+                                   ctypes.byref(kv.struct), _ptr(anchor), _ptr(ctx_len),
+                                   int(anchor.shape[0]), int(K), _ptr(topk_ids), _ptr(topk_logp),
+                                   _ptr(logits), ws.ptr, ws.nbytes, _stream(stream)),
+          "dflash_draft_block")
+
+
+def select_path(cfg, W, anchor, topk_ids, topk_logp, K, ws, path, score, stream=None):
+    c = make_config(cfg)
+    check(lib().dflash_select_path(ctypes.byref(c), ctypes.byref(W.struct), _ptr(anchor),
+                                   _ptr(topk_ids), _ptr(topk_logp), int(anchor.shape[0]), int(K),
+                                   _ptr(path), _ptr(score), ws.ptr, ws.nbytes, _stream(stream)),
+          "dflash_select_path")
+
+
+def accept_greedy(path, target_logits, ws, accept_len, tokens, stream=None):
+    B, K, V = target_logits.shape
+    dt = _lib.F32 if target_logits.dtype == torch.float32 else _lib.BF16
+    check(lib().dflash_accept_greedy(_ptr(path), _ptr(target_logits), dt, B, K, V,
+                                     _ptr(accept_len), _ptr(tokens), ws.ptr, ws.nbytes,
+                                     _stream(stream)),
+          "dflash_accept_greedy")
+
+
+def read_device_status(ws, stream=None):
+    r = lib().dflash_read_device_status(ws.ptr, _stream(stream))
+    if r < 0:
+        check(r, "dflash_read_device_status")
+    return r
+
+
+def clear_device_status(ws, stream=None):
+    check(lib().dflash_clear_device_status(ws.ptr, _stream(stream)), "dflash_clear_device_status")
+
+
+def launch_count(reset=False):
+    return int(lib().dflash_launch_count(1 if reset else 0))
+
+
+class DraftCycle:
+    """Buffers and calls of one draft cycle (inject -> draft -> select -> accept) for B
+    requests of block K; the shape a serving loop would hold on to."""
+
+    def __init__(self, cfg, W, kv, B, K, max_inject_tokens, device="cuda"):
+        self.cfg, self.W, self.kv, self.B, self.K = cfg, W, kv, B, K
+        self.ws = Workspace(cfg, B, K, max_inject_tokens, device)
+        k = cfg["top_k"]
+        i32 = dict(dtype=torch.int32, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.topk_ids = torch.zeros((B, K - 1, k), **i32)
+        self.topk_logp = torch.zeros((B, K - 1, k), **f32)
+        self.path = torch.zeros((B, K - 1), **i32)
+        self.score = torch.zeros((B,), **f32)
+        self.accept_len = torch.zeros((B,), **i32)
+        self.tokens = torch.zeros((B, K), **i32)
+
+    def run(self, hidden, req, pos, anchor, ctx_len, target_logits, logits=None, stream=None):
+        if hidden is not None and hidden.shape[0] > 0:
+            inject_context(self.cfg, self.W, self.kv, hidden, req, pos, self.ws, stream)
+        draft_block(self.cfg, self.W, self.kv, anchor, ctx_len, self.K, self.ws, self.topk_ids,
+                    self.topk_logp, logits, stream)
+        select_path(self.cfg, self.W, anchor, self.topk_ids, self.topk_logp, self.K, self.ws,
+                    self.path, self.score, stream)
+        accept_greedy(self.path, target_logits, self.ws, self.accept_len, self.tokens, stream)

@@ -1,0 +1,462 @@
+// C ABI of the DFlash 2 draft cycle: argument checks, workspace layout and the
+// kernel sequence of each call.
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "attention.cuh"
+#include "gemm.cuh"
+#include "head.cuh"
+#include "pointwise.cuh"
+
+namespace dflh {
+
+// ---------------------------------------------------------------------------
+// device, launch counter, PDL switch
+// ---------------------------------------------------------------------------
+static thread_local int64_t g_launches = 0;
+void count_launch() { ++g_launches; }
+
+bool pdl_enabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char *e = getenv("DFLASH_PDL");
+    v = (e && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
+
+const Dev *device() {
+  static Dev devs[64];
+  static std::mutex mu;
+  int id = -1;
+  if (cudaGetDevice(&id) != cudaSuccess || id < 0 || id >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> g(mu);
+  Dev &d = devs[id];
+  if (d.id < 0) {
+    cudaDeviceProp p;
+    if (cudaGetDeviceProperties(&p, id) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    d.num_sms = p.multiProcessorCount;
+    d.max_smem_optin = (int)p.sharedMemPerBlockOptin;
+    d.cc_major = p.major;
+    d.cc_minor = p.minor;
+    d.id = id;
+  }
+  if (d.cc_major != 10 || d.cc_minor != 3) return nullptr;  // built for sm_103a only
+  return &d;
+}
+
+static int sm_count_or_default() {
+  int id = -1, n = 0;
+  if (cudaGetDevice(&id) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, id) == cudaSuccess && n > 0)
+    return n;
+  cudaGetLastError();
+  return 152;
+}
+
+// ---------------------------------------------------------------------------
+// argument checks
+// ---------------------------------------------------------------------------
+static int check_cfg(const dflash_config *c) {
+  if (!c) return DFLASH_ERR_NULL;
+  if (c->dtype != DFLASH_F32 && c->dtype != DFLASH_BF16) return DFLASH_ERR_DTYPE;
+  const bool ok =
+      c->d_model > 0 && c->d_model % 64 == 0 && c->n_layers >= 1 &&
+      c->n_layers <= DFLASH_MAX_LAYERS && c->n_kv_heads >= 1 && c->n_q_heads >= c->n_kv_heads &&
+      c->n_q_heads % c->n_kv_heads == 0 && (c->head_dim == 64 || c->head_dim == 128) &&
+      (c->n_q_heads * c->head_dim) % 64 == 0 && c->d_ff > 0 && c->d_ff % 64 == 0 &&
+      c->vocab >= 2 && c->n_taps >= 1 && c->d_target >= 1 &&
+      ((long)c->n_taps * c->d_target) % 64 == 0 && c->window >= 1 && c->page_size >= 1 &&
+      c->top_k >= 1 && c->top_k <= DFLASH_MAX_TOPK && c->top_k <= c->vocab &&
+      c->sel_rank >= 16 && c->sel_rank % 16 == 0 && c->sel_rank <= 1024 &&
+      c->top_k * c->sel_rank <= 16384 && c->conv_group >= 1 && c->d_model % c->conv_group == 0 &&
+      c->mask_token_id >= 0 && c->mask_token_id < c->vocab && c->rms_eps >= 0.f &&
+      c->rope_theta >= 0.f;
+  return ok ? DFLASH_OK : DFLASH_ERR_DIMS;
+}
+
+static bool a16(const void *p) { return ((uintptr_t)p & 15) == 0; }
+
+static int check_weights(const dflash_config *c, const dflash_weights *w, bool draft) {
+  if (!w) return DFLASH_ERR_NULL;
+  if (!w->fc_norm || !w->fc) return DFLASH_ERR_NULL;
+  if (!a16(w->fc)) return DFLASH_ERR_ALIGN;
+  for (int l = 0; l < c->n_layers; ++l) {
+    const dflash_layer_weights &L = w->layer[l];
+    if (!L.wqkv || !L.k_norm) return DFLASH_ERR_NULL;
+    if (!a16(L.wqkv)) return DFLASH_ERR_ALIGN;
+    if (!draft) continue;
+    if (!L.attn_norm || !L.mlp_norm || !L.wo || !L.q_norm || !L.w_gate_up || !L.w_down)
+      return DFLASH_ERR_NULL;
+    if (!a16(L.wo) || !a16(L.w_gate_up) || !a16(L.w_down)) return DFLASH_ERR_ALIGN;
+    for (int i = 0; i < 4; ++i) {
+      if (!L.conv_w[i] || !L.conv_base[i]) return DFLASH_ERR_NULL;
+      if (!a16(L.conv_w[i])) return DFLASH_ERR_ALIGN;
+    }
+  }
+  if (draft) {
+    if (!w->embed || !w->lm_head || !w->final_norm) return DFLASH_ERR_NULL;
+    if (!a16(w->lm_head) || !a16(w->embed)) return DFLASH_ERR_ALIGN;
+  }
+  return DFLASH_OK;
+}
+
+static int check_kv(const dflash_config *c, const dflash_kv *kv) {
+  (void)c;
+  if (!kv || !kv->k || !kv->v || !kv->page_table) return DFLASH_ERR_NULL;
+  if (kv->num_pages < 1 || kv->max_pages_per_req < 1 || kv->num_rows < 1) return DFLASH_ERR_DIMS;
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+struct Layout {
+  size_t status, x, un, ub, rf, rb, qb, kb, vb, ob, hb, zf, logits, part, gpart, attn, topk;
+  size_t selrows, upart, vpart, argmax, gn, cb, ipart, kvpart;
+  size_t total;
+  int S_gate, S_qkv, S_o, S_gu, S_down, S_sel;
+  AttnPlan ap;
+};
+
+static size_t max_partial(int N_out, int K_in, int Nmax, int sms) {
+  // the split count depends on the token count; take the largest buffer over
+  // token counts at the token-tile boundaries up to Nmax
+  size_t best = 0;
+  auto eval = [&](int n) {
+    if (n < 1 || n > Nmax) return;
+    size_t v = (size_t)gemm_splits(N_out, n, K_in, sms) * n * N_out;
+    if (v > best) best = v;
+  };
+  for (int n = 16; n <= 256; n *= 2) eval(n);
+  for (int n = 512; n <= Nmax; n += 256) eval(n);
+  for (int n = 1; n <= 16; ++n) eval(n);
+  eval(Nmax);
+  return best;
+}
+
+static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *L) {
+  const int sms = sm_count_or_default();
+  const size_t es = c->dtype == DFLASH_BF16 ? 2 : 4;
+  const int D = c->d_model, F = c->d_ff, V = c->vocab, dh = c->head_dim;
+  const int Hq = c->n_q_heads, Hkv = c->n_kv_heads, k = c->top_k, r = c->sel_rank;
+  const int GW = 2 * D / c->conv_group;
+  const int QKVW = (Hq + 2 * Hkv) * dh;
+  const int TIN = c->n_taps * c->d_target;
+  const int T = B * K, TL = B * (K - 1), R = 1 + (K - 1) * k, TR = B * R;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += (bytes + 255) & ~(size_t)255;
+    return o;
+  };
+  L->status = take(256);
+  L->S_gate = gemm_splits(GW, T, D, sms);
+  L->S_qkv = gemm_splits(QKVW, T, D, sms);
+  L->S_o = gemm_splits(D, T, Hq * dh, sms);
+  L->S_gu = gemm_splits(2 * F, T, D, sms);
+  L->S_down = gemm_splits(D, T, F, sms);
+  L->S_sel = gemm_splits(r, TR, D, sms);
+  L->ap = attn_plan(B, K, Hq, Hkv, dh, c->window, sms);
+  L->x = take((size_t)T * D * 4);
+  L->un = take((size_t)T * D * es);
+  L->ub = take((size_t)T * D * es);
+  L->rf = take((size_t)T * D * 4);
+  L->rb = take((size_t)T * D * es);
+  L->qb = take((size_t)T * Hq * dh * es);
+  L->kb = take((size_t)T * Hkv * dh * es);
+  L->vb = take((size_t)T * Hkv * dh * es);
+  L->ob = take((size_t)T * Hq * dh * es);
+  L->hb = take((size_t)T * F * es);
+  L->zf = take((size_t)TL * D * es);
+  L->logits = take((size_t)TL * V * 4);
+  size_t pf = 0;
+  pf = std::max(pf, (size_t)L->S_qkv * T * QKVW);
+  pf = std::max(pf, (size_t)L->S_o * T * D);
+  pf = std::max(pf, (size_t)L->S_gu * T * 2 * F);
+  pf = std::max(pf, (size_t)L->S_down * T * D);
+  L->part = take(pf * 4);
+  L->gpart = take((size_t)L->S_gate * T * GW * 4);
+  L->attn = take(L->ap.part_floats * 4);
+  L->topk = take((size_t)TL * topk_chunks(V) * (2 * k + 2) * 4);
+  L->selrows = take((size_t)TR * D * es);
+  L->upart = take((size_t)L->S_sel * TR * r * 4);
+  L->vpart = take((size_t)L->S_sel * TR * r * 4);
+  L->argmax = take((size_t)T * argmax_chunks(V) * 2 * 4);
+  const int N = Nmax > 0 ? Nmax : 1;
+  L->gn = take((size_t)N * TIN * es);
+  L->cb = take((size_t)N * D * es);
+  L->ipart = take(max_partial(D, TIN, N, sms) * 4);
+  L->kvpart = take(max_partial(2 * Hkv * dh, D, N, sms) * (size_t)c->n_layers * 4);
+  L->total = off;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// the calls
+// ---------------------------------------------------------------------------
+#define TRY(e)                           \
+  do {                                   \
+    int rc_ = (e);                       \
+    if (rc_ != DFLASH_OK) return rc_;    \
+  } while (0)
+
+template <typename S>
+static int run_inject(const dflash_config &c, const dflash_weights &w, const dflash_kv &kv,
+                      const void *hidden, const int32_t *req, const int32_t *pos, int N,
+                      uint8_t *ws, const Layout &L, cudaStream_t st) {
+  const int sms = device()->num_sms;
+  const int D = c.d_model, Hq = c.n_q_heads, Hkv = c.n_kv_heads, dh = c.head_dim;
+  const int TIN = c.n_taps * c.d_target, W2 = 2 * Hkv * dh;
+  int *err = (int *)(ws + L.status);
+  S *gn = (S *)(ws + L.gn);
+  S *cb = (S *)(ws + L.cb);
+  float *ipart = (float *)(ws + L.ipart);
+  float *kvpart = (float *)(ws + L.kvpart);
+  TRY(launch_rows_norm<S>((const S *)hidden, N, TIN, (const S *)w.fc_norm, c.rms_eps, gn, st));
+  const int S_fc = gemm_splits(D, N, TIN, sms);
+  TRY(gemm_xwT(c.dtype, w.fc, D, TIN, gn, N, ipart, D, S_fc, err, st));
+  TRY(launch_reduce<S>(ipart, S_fc, N, D, nullptr, cb, st));
+  const int S_kv = gemm_splits(W2, N, D, sms);
+  LayerPtrs kn;
+  memset(&kn, 0, sizeof(kn));
+  for (int l = 0; l < c.n_layers; ++l) {
+    const S *wkv = (const S *)w.layer[l].wqkv + (size_t)Hq * dh * D;  // [Wk; Wv] rows
+    TRY(gemm_xwT(c.dtype, wkv, W2, D, cb, N, kvpart + (size_t)l * S_kv * N * W2, W2, S_kv, err,
+                 st));
+    kn.p[l] = w.layer[l].k_norm;
+  }
+  TRY(launch_inject_store<S>(kvpart, S_kv, N, c.n_layers, Hkv, dh, kn, req, pos, kv.page_table,
+                             kv.num_rows, kv.max_pages_per_req, kv.num_pages, c.page_size,
+                             c.rope_theta, c.rms_eps, (S *)kv.k, (S *)kv.v, err, st));
+  return DFLASH_OK;
+}
+
+template <typename S>
+static int run_draft(const dflash_config &c, const dflash_weights &w, const dflash_kv &kv,
+                     const int32_t *anchor, const int32_t *ctx_len, int B, int K, int32_t *ids,
+                     float *logp, float *logits_opt, uint8_t *ws, const Layout &L,
+                     cudaStream_t st) {
+  const int D = c.d_model, F = c.d_ff, V = c.vocab, dh = c.head_dim;
+  const int Hq = c.n_q_heads, Hkv = c.n_kv_heads, g = c.conv_group;
+  const int GW = 2 * D / g, QKVW = (Hq + 2 * Hkv) * dh;
+  const int T = B * K, dt = c.dtype;
+  const float eps = c.rms_eps;
+  int *err = (int *)(ws + L.status);
+  float *x = (float *)(ws + L.x);
+  S *un = (S *)(ws + L.un), *ub = (S *)(ws + L.ub), *rb = (S *)(ws + L.rb);
+  float *rf = (float *)(ws + L.rf);
+  S *qb = (S *)(ws + L.qb), *kb = (S *)(ws + L.kb), *vb = (S *)(ws + L.vb);
+  S *ob = (S *)(ws + L.ob), *hb = (S *)(ws + L.hb), *zf = (S *)(ws + L.zf);
+  float *logits = logits_opt ? logits_opt : (float *)(ws + L.logits);
+  float *part = (float *)(ws + L.part), *gpart = (float *)(ws + L.gpart);
+  float *attnp = (float *)(ws + L.attn), *topkp = (float *)(ws + L.topk);
+
+  TRY(launch_embed_norm<S>((const S *)w.embed, anchor, c.mask_token_id, V, B, K, D,
+                           (const S *)w.layer[0].attn_norm, eps, x, un, err, st));
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights &lw = w.layer[l];
+    const bool last = l + 1 == c.n_layers;
+    // attention sublayer: conv -> QKV -> norm/RoPE -> block attention -> O -> conv, residual
+    TRY(gemm_xwT(dt, lw.conv_w[0], GW, D, un, T, gpart, GW, L.S_gate, err, st));
+    TRY(launch_conv_pre<S>(un, gpart, L.S_gate, T, K, D, g, (const S *)lw.conv_base[0], ub, st));
+    TRY(gemm_xwT(dt, lw.wqkv, QKVW, D, ub, T, part, QKVW, L.S_qkv, err, st));
+    TRY(launch_qkv_post<S>(part, L.S_qkv, T, K, Hq, Hkv, dh, (const S *)lw.q_norm,
+                           (const S *)lw.k_norm, ctx_len, c.rope_theta, eps, qb, kb, vb, st));
+    TRY(launch_block_attention<S>(L.ap, qb, kb, vb, (const S *)kv.k, (const S *)kv.v, l,
+                                  kv.page_table, kv.max_pages_per_req, kv.num_pages, c.page_size,
+                                  ctx_len, B, K, Hq, Hkv, dh, c.window, attnp, ob, err, st));
+    TRY(gemm_xwT(dt, lw.wo, D, Hq * dh, ob, T, part, D, L.S_o, err, st));
+    TRY(launch_reduce<S>(part, L.S_o, T, D, rf, rb, st));
+    TRY(gemm_xwT(dt, lw.conv_w[1], GW, D, rb, T, gpart, GW, L.S_gate, err, st));
+    TRY(launch_conv_post_norm<S>(rf, gpart, L.S_gate, T, K, D, g, (const S *)lw.conv_base[1], x,
+                                 (const S *)lw.mlp_norm, eps, un, (S *)nullptr, st));
+    // MLP sublayer: conv -> gate/up -> SwiGLU -> down -> conv, residual
+    TRY(gemm_xwT(dt, lw.conv_w[2], GW, D, un, T, gpart, GW, L.S_gate, err, st));
+    TRY(launch_conv_pre<S>(un, gpart, L.S_gate, T, K, D, g, (const S *)lw.conv_base[2], ub, st));
+    TRY(gemm_xwT(dt, lw.w_gate_up, 2 * F, D, ub, T, part, 2 * F, L.S_gu, err, st));
+    TRY(launch_swiglu<S>(part, L.S_gu, T, F, hb, st));
+    TRY(gemm_xwT(dt, lw.w_down, D, F, hb, T, part, D, L.S_down, err, st));
+    TRY(launch_reduce<S>(part, L.S_down, T, D, rf, rb, st));
+    TRY(gemm_xwT(dt, lw.conv_w[3], GW, D, rb, T, gpart, GW, L.S_gate, err, st));
+    TRY(launch_conv_post_norm<S>(
+        rf, gpart, L.S_gate, T, K, D, g, (const S *)lw.conv_base[3], x,
+        (const S *)(last ? w.final_norm : w.layer[l + 1].attn_norm), eps, un, last ? zf : (S *)nullptr,
+        st));
+  }
+  const int TL = B * (K - 1);
+  TRY(gemm_xwT(dt, w.lm_head, V, D, zf, TL, logits, V, 1, err, st));
+  TRY(launch_topk(logits, TL, V, c.top_k, topkp, ids, logp, st));
+  return DFLASH_OK;
+}
+
+template <typename S>
+static int run_select(const dflash_config &c, const dflash_weights &w, const int32_t *anchor,
+                      const int32_t *ids, const float *logp, int B, int K, int32_t *path,
+                      float *score, uint8_t *ws, const Layout &L, cudaStream_t st) {
+  const int D = c.d_model, k = c.top_k, r = c.sel_rank;
+  const int TR = B * (1 + (K - 1) * k);
+  int *err = (int *)(ws + L.status);
+  S *rows = (S *)(ws + L.selrows);
+  float *up = (float *)(ws + L.upart), *vp = (float *)(ws + L.vpart);
+  TRY(launch_sel_gather<S>((const S *)w.embed, anchor, ids, B, K, k, c.vocab, D, rows, err, st));
+  TRY(gemm_xwT(c.dtype, w.sel_pu, r, D, rows, TR, up, r, L.S_sel, err, st));
+  TRY(gemm_xwT(c.dtype, w.sel_pv, r, D, rows, TR, vp, r, L.S_sel, err, st));
+  TRY(launch_viterbi(up, vp, L.S_sel, L.S_sel, ids, logp, B, K, k, r, path, score, st));
+  return DFLASH_OK;
+}
+
+}  // namespace dflh
+
+using namespace dflh;
+
+extern "C" {
+
+size_t dflash_workspace_bytes(const dflash_config *cfg, int32_t B, int32_t K,
+                              int32_t max_inject_tokens) {
+  if (check_cfg(cfg) != DFLASH_OK) return 0;
+  if (B < 1 || K < 2 || K > DFLASH_MAX_BLOCK || max_inject_tokens < 0) return 0;
+  Layout L;
+  if (!make_layout(cfg, B, K, max_inject_tokens, &L)) return 0;
+  return L.total;
+}
+
+int dflash_inject_context(const dflash_config *cfg, const dflash_weights *w, const dflash_kv *kv,
+                          const void *target_hidden, const int32_t *req, const int32_t *pos,
+                          int32_t N, void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_cfg(cfg);
+  if (rc != DFLASH_OK) return rc;
+  if (N < 0) return DFLASH_ERR_DIMS;
+  if (N == 0) return DFLASH_OK;
+  if (!target_hidden || !req || !pos || !ws) return DFLASH_ERR_NULL;
+  if ((rc = check_weights(cfg, w, false)) != DFLASH_OK) return rc;
+  if ((rc = check_kv(cfg, kv)) != DFLASH_OK) return rc;
+  if (!a16(ws)) return DFLASH_ERR_ALIGN;
+  Layout L;
+  make_layout(cfg, 1, 2, N, &L);
+  if (ws_bytes < L.total) return DFLASH_ERR_WORKSPACE;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cfg->dtype == DFLASH_BF16)
+    return run_inject<dfl::bf16>(*cfg, *w, *kv, target_hidden, req, pos, N, (uint8_t *)ws, L, st);
+  return run_inject<float>(*cfg, *w, *kv, target_hidden, req, pos, N, (uint8_t *)ws, L, st);
+}
+
+int dflash_draft_block(const dflash_config *cfg, const dflash_weights *w, const dflash_kv *kv,
+                       const int32_t *anchor, const int32_t *ctx_len, int32_t B, int32_t K,
+                       int32_t *topk_ids, float *topk_logp, float *logits_opt, void *ws,
+                       size_t ws_bytes, void *stream) {
+  int rc = check_cfg(cfg);
+  if (rc != DFLASH_OK) return rc;
+  if (B < 0 || K < 2 || K > DFLASH_MAX_BLOCK) return DFLASH_ERR_BLOCK;
+  if (B == 0) return DFLASH_OK;
+  if (!anchor || !ctx_len || !topk_ids || !topk_logp || !ws) return DFLASH_ERR_NULL;
+  if ((rc = check_weights(cfg, w, true)) != DFLASH_OK) return rc;
+  if ((rc = check_kv(cfg, kv)) != DFLASH_OK) return rc;
+  if (!a16(ws)) return DFLASH_ERR_ALIGN;
+  Layout L;
+  make_layout(cfg, B, K, 0, &L);
+  if (ws_bytes < L.total) return DFLASH_ERR_WORKSPACE;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cfg->dtype == DFLASH_BF16)
+    return run_draft<dfl::bf16>(*cfg, *w, *kv, anchor, ctx_len, B, K, topk_ids, topk_logp,
+                                logits_opt, (uint8_t *)ws, L, st);
+  return run_draft<float>(*cfg, *w, *kv, anchor, ctx_len, B, K, topk_ids, topk_logp, logits_opt,
+                          (uint8_t *)ws, L, st);
+}
+
+int dflash_select_path(const dflash_config *cfg, const dflash_weights *w, const int32_t *anchor,
+                       const int32_t *topk_ids, const float *topk_logp, int32_t B, int32_t K,
+                       int32_t *path, float *path_score, void *ws, size_t ws_bytes,
+                       void *stream) {
+  int rc = check_cfg(cfg);
+  if (rc != DFLASH_OK) return rc;
+  if (B < 0 || K < 2 || K > DFLASH_MAX_BLOCK) return DFLASH_ERR_BLOCK;
+  if (B == 0) return DFLASH_OK;
+  if (!w || !anchor || !topk_ids || !topk_logp || !path || !path_score || !ws)
+    return DFLASH_ERR_NULL;
+  if (!w->embed || !w->sel_pu || !w->sel_pv) return DFLASH_ERR_NULL;
+  if (!a16(w->sel_pu) || !a16(w->sel_pv) || !a16(w->embed) || !a16(ws)) return DFLASH_ERR_ALIGN;
+  Layout L;
+  make_layout(cfg, B, K, 0, &L);
+  if (ws_bytes < L.total) return DFLASH_ERR_WORKSPACE;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cfg->dtype == DFLASH_BF16)
+    return run_select<dfl::bf16>(*cfg, *w, anchor, topk_ids, topk_logp, B, K, path, path_score,
+                                 (uint8_t *)ws, L, st);
+  return run_select<float>(*cfg, *w, anchor, topk_ids, topk_logp, B, K, path, path_score,
+                           (uint8_t *)ws, L, st);
+}
+
+int dflash_accept_greedy(const int32_t *path, const void *target_logits, int32_t logits_dtype,
+                         int32_t B, int32_t K, int32_t V, int32_t *accept_len, int32_t *tokens,
+                         void *ws, size_t ws_bytes, void *stream) {
+  if (logits_dtype != DFLASH_F32 && logits_dtype != DFLASH_BF16) return DFLASH_ERR_DTYPE;
+  if (B < 0 || K < 2 || K > DFLASH_MAX_BLOCK) return DFLASH_ERR_BLOCK;
+  if (V < 1) return DFLASH_ERR_DIMS;
+  if (B == 0) return DFLASH_OK;
+  if (!path || !target_logits || !accept_len || !tokens || !ws) return DFLASH_ERR_NULL;
+  if (!a16(ws)) return DFLASH_ERR_ALIGN;
+  // status word + argmax partials
+  const size_t need = 256 + (((size_t)B * K * argmax_chunks(V) * 2 * 4 + 255) & ~(size_t)255);
+  if (ws_bytes < need) return DFLASH_ERR_WORKSPACE;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  return launch_accept(path, target_logits, logits_dtype, B, K, V, (float *)((uint8_t *)ws + 256),
+                       accept_len, tokens, (cudaStream_t)stream);
+}
+
+int dflash_read_device_status(const void *ws, void *stream) {
+  if (!ws) return DFLASH_ERR_NULL;
+  int h = 0;
+  if (cudaMemcpyAsync(&h, ws, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  return h;
+}
+
+int dflash_clear_device_status(void *ws, void *stream) {
+  if (!ws) return DFLASH_ERR_NULL;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), (cudaStream_t)stream) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  return DFLASH_OK;
+}
+
+const char *dflash_status_string(int code) {
+  switch (code) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_NULL: return "a required pointer is NULL";
+    case DFLASH_ERR_DIMS: return "a dimension breaks the shape rules";
+    case DFLASH_ERR_BLOCK: return "block size K outside 2..32 or negative batch";
+    case DFLASH_ERR_WORKSPACE: return "workspace smaller than dflash_workspace_bytes";
+    case DFLASH_ERR_DTYPE: return "unsupported dtype";
+    case DFLASH_ERR_CUDA: return "a CUDA call failed";
+    case DFLASH_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case DFLASH_ERR_DEVICE: return "no usable sm_103 device";
+    case DFLASH_DEV_TOKEN_RANGE: return "device: token id out of range";
+    case DFLASH_DEV_PAGE_RANGE: return "device: page id out of range";
+    case DFLASH_DEV_POS_RANGE: return "device: position beyond the page table";
+    case DFLASH_DEV_TIMEOUT: return "device: bounded wait expired";
+    case DFLASH_DEV_REQ_RANGE: return "device: request row out of range";
+    default: return "unknown status";
+  }
+}
+
+int64_t dflash_launch_count(int reset) {
+  int64_t v = g_launches;
+  if (reset) g_launches = 0;
+  return v;
+}
+
+}  // extern "C"

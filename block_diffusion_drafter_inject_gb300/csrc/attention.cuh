@@ -1,0 +1,26 @@
+// Non-causal block attention over the paged context window plus the block.
+#pragma once
+#include "common.cuh"
+
+namespace dflh {
+
+struct AttnPlan {
+  int qg;        // query rows per CTA (64)
+  int nqg;       // query groups per (request, kv head)
+  int kps;       // keys per split (multiple of 64)
+  int nsplit;    // splits per (request, kv head, query group) at the largest key count
+  size_t part_floats;  // partial O + (m, l) floats
+};
+
+AttnPlan attn_plan(int B, int K, int Hq, int Hkv, int dh, int window, int num_sms);
+
+// o[r, h*dh + :] for r = b*K + i, from q [B*K, Hq, dh], block k/v [B*K, Hkv, dh]
+// and layer `layer` of the paged caches.
+template <typename S>
+int launch_block_attention(const AttnPlan &pl, const S *qb, const S *kb, const S *vb,
+                           const S *kc, const S *vc, int layer, const int32_t *page_table,
+                           int max_pages, int num_pages, int page_size, const int32_t *ctx_len,
+                           int B, int K, int Hq, int Hkv, int dh, int window, float *part, S *ob,
+                           int *err, cudaStream_t st);
+
+}  // namespace dflh

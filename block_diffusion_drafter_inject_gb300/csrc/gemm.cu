@@ -1,0 +1,435 @@
+// Projection GEMMs.
+//
+// bf16 path: one persistent, warp-specialised kernel per shape class.
+//   warp 0     TMA producer: weight tile [128 rows x 64] and activation tile
+//              [BN rows x 64] per stage, 128-byte swizzle, into a ring of stages
+//   warp 1     tensor-memory allocator and tcgen05.mma issuer (M=128, N=BN, K=16
+//              per instruction), fp32 accumulators in tensor memory, double
+//              buffered so the epilogue of one work unit overlaps the next unit
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, coalesced fp32 stores
+// The weight matrix is the M operand ("swap AB"): at draft batch sizes the token
+// count is 8..256, so weights stream through the M dimension and tokens fill N.
+// A work unit is (weight tile, token tile, K slice); the CTA's pipeline runs on
+// across units without draining.  Weight tiles are loaded with an evict-first
+// L2 hint (each is read once per pass); activation tiles with evict-last.
+//
+// fp32 path (the float32 configuration): a shared-memory tiled CUDA-core GEMM.
+#include <mutex>
+#include <unordered_map>
+
+#include "gemm.cuh"
+
+namespace dfl {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kGemmThreads = 192;
+
+struct GemmParams {
+  float *out;
+  int ld;
+  int N_out, T;
+  int kb_per_split;
+  int S, m_tiles, t_tiles, num_units;
+  int *err;
+};
+
+template <int BN>
+struct GemmShape {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN <= 16 ? 11 : BN <= 32 ? 10 : BN <= 64 ? 8 : BN <= 128 ? 6 : 4;
+  static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+__device__ __forceinline__ void unit_coords(int u, const GemmParams &p, int &m_tile, int &t_tile,
+                                            int &split) {
+  // weight tile fastest: CTAs working at the same time share activation tiles in L2
+  m_tile = u % p.m_tiles;
+  int r = u / p.m_tiles;
+  split = r % p.S;
+  t_tile = r / p.S;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+              GemmParams p) {
+  using SH = GemmShape<BN>;
+  constexpr int STAGES = SH::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t *full = (uint64_t *)(smem + STAGES * SH::STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = (uint32_t *)(drain + 1);
+  volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    tc_alloc(tmem_slot, SH::TMEM_COLS);
+    tc_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t last_phase[STAGES];
+      bool issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = false, last_phase[s] = 0;
+      // Weights do not depend on the previous kernel: prefetch the first
+      // stages' weight tiles before waiting for it, then add activations.
+      int pre = 0;
+      {
+        int cnt = 0;
+        for (int u = blockIdx.x; u < p.num_units && cnt < STAGES; u += gridDim.x) {
+          int m_tile, t_tile, split;
+          unit_coords(u, p, m_tile, t_tile, split);
+          for (int kb = 0; kb < p.kb_per_split && cnt < STAGES; ++kb, ++cnt) {
+            mbar_expect_tx(&full[cnt], SH::STAGE_BYTES);
+            tma_load_2d(smem + cnt * SH::STAGE_BYTES, &tmW, &full[cnt],
+                        (split * p.kb_per_split + kb) * BK, m_tile * BM, pol_w);
+          }
+        }
+        pre = cnt;
+      }
+      pdl_wait();
+      bool ok = true;
+      int n = 0;  // fill counter across units
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        int m_tile, t_tile, split;
+        unit_coords(u, p, m_tile, t_tile, split);
+        for (int kb = 0; kb < p.kb_per_split; ++kb, ++n) {
+          uint8_t *sa = smem + stage * SH::STAGE_BYTES;
+          const int kx = (split * p.kb_per_split + kb) * BK;
+          if (n < pre) {
+            tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, t_tile * BN, pol_x);
+          } else {
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&full[stage], SH::STAGE_BYTES);
+            tma_load_2d(sa, &tmW, &full[stage], kx, m_tile * BM, pol_w);
+            tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, t_tile * BN, pol_x);
+          }
+          issued[stage] = true;
+          last_phase[stage] = phase;
+          if (++stage == STAGES) stage = 0, phase ^= 1;
+        }
+      }
+      if (!ok) {
+        // give up: let the copies already issued land before shared memory is released
+        volatile int dummy = 0;
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) mbar_wait(&full[s], last_phase[s], (volatile int *)&dummy);
+      }
+    }
+  } else if (warp == 1) {
+    pdl_wait();
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < p.kb_per_split; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * SH::STAGE_BYTES);
+          const uint64_t adesc = sdesc_k_sw128(sa);
+          const uint64_t bdesc = sdesc_k_sw128(sa + SH::A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // advance 16 bf16 = 32 bytes along K inside the swizzled row
+            tc_mma_bf16(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc,
+                        (kb | k) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) stage = 0, phase ^= 1;
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        if (++acc == 2) acc = 0, acc_phase ^= 1;
+      }
+      if (!ok) {
+        // drain: wait (bounded) until the MMAs issued so far have finished
+        volatile int dummy = 0;
+        tc_commit(drain);
+        (void)mbar_wait(drain, 0, (volatile int *)&dummy);
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5 ----------------
+    pdl_wait();
+    const int quarter = warp & 3;  // tensor-memory lanes this warp may read
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+      int m_tile, t_tile, split;
+      unit_coords(u, p, m_tile, t_tile, split);
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
+      tc_fence_after();
+      const int n = m_tile * BM + quarter * 32 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      float *outp = p.out + (size_t)split * p.T * p.ld + n;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 16) {
+        float v[16];
+        tc_ld16(taddr + c, v);
+        const int t0 = t_tile * BN + c;
+        if (n < p.N_out) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (t0 + j < p.T) outp[(size_t)(t0 + j) * p.ld] = v[j];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) acc = 0, acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) set_err(p.err, DFLASH_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tc_dealloc(tmem_base, SH::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// fp32 CUDA-core GEMM (float32 configuration)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_gemm_f32(const float *__restrict__ W,
+                                                  const float *__restrict__ X,
+                                                  float *__restrict__ out, int ld, int N, int T,
+                                                  int K, int kps) {
+  __shared__ float Ws[64][33];
+  __shared__ float Xs[32][33];
+  pdl_launch();
+  pdl_wait();
+  const int n0 = blockIdx.x * 64, t0 = blockIdx.y * 32, s = blockIdx.z;
+  const int tn = threadIdx.x & 15, tt = threadIdx.x >> 4;  // 16 x 16 threads
+  float acc[4][2] = {};
+  const int kbeg = s * kps, kend = kbeg + kps;
+  for (int k0 = kbeg; k0 < kend; k0 += 32) {
+    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+      int r = i >> 5, c = i & 31;
+      Ws[r][c] = (n0 + r < N) ? W[(size_t)(n0 + r) * K + k0 + c] : 0.f;
+    }
+    for (int i = threadIdx.x; i < 32 * 32; i += 256) {
+      int r = i >> 5, c = i & 31;
+      Xs[r][c] = (t0 + r < T) ? X[(size_t)(t0 + r) * K + k0 + c] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int c = 0; c < 32; ++c) {
+      float x0 = Xs[tt * 2][c], x1 = Xs[tt * 2 + 1][c];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float w = Ws[tn * 4 + i][c];
+        acc[i][0] = fmaf(w, x0, acc[i][0]);
+        acc[i][1] = fmaf(w, x1, acc[i][1]);
+      }
+    }
+    __syncthreads();
+  }
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 2; ++j) {
+      int n = n0 + tn * 4 + i, t = t0 + tt * 2 + j;
+      if (n < N && t < T) out[((size_t)s * T + t) * ld + n] = acc[i][j];
+    }
+}
+
+}  // namespace dfl
+
+// ===========================================================================
+// host
+// ===========================================================================
+namespace dflh {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  });
+  return fn;
+}
+
+struct MapKey {
+  uintptr_t ptr;
+  uint64_t rows, cols;
+  uint32_t box_rows;
+  int dev;
+  bool operator==(const MapKey &o) const {
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && box_rows == o.box_rows &&
+           dev == o.dev;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey &k) const {
+    size_t h = (size_t)k.ptr * 0x9E3779B97F4A7C15ull;
+    h ^= (k.rows * 1315423911ull) ^ (k.cols << 20) ^ ((size_t)k.box_rows << 40) ^ (size_t)k.dev;
+    return h;
+  }
+};
+
+// Tensor map of a row-major bf16 matrix [rows, cols]; box = 64 columns x box_rows rows.
+static bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows, int dev) {
+  static std::mutex mu;
+  static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+  MapKey key{(uintptr_t)ptr, rows, cols, box_rows, dev};
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second;
+      return true;
+    }
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> g(mu);
+  if (cache.size() > 8192) cache.clear();
+  cache[key] = *out;
+  return true;
+}
+
+static int token_tile(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
+
+int gemm_splits(int N_out, int T, int K_in, int num_sms) {
+  const int kb = K_in / dfl::BK;
+  const int m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
+  const int bn = token_tile(T);
+  const int t_tiles = (T + bn - 1) / bn;
+  const long base = (long)m_tiles * t_tiles;
+  int best = 1;
+  for (int S = 1; S <= kb; ++S) {
+    if (kb % S) continue;
+    if (S > 1 && (size_t)S * T * N_out > kMaxPartialFloats) break;
+    if (S > 1 && kb / S < 2) break;
+    best = S;
+    if (base * S >= num_sms) break;
+  }
+  return best;
+}
+
+template <int BN>
+static int launch_tc(const void *W, int N_out, int K_in, const void *X, int T, float *out, int ld,
+                     int S, int *err, cudaStream_t st, const Dev *d) {
+  using SH = dfl::GemmShape<BN>;
+  static int attr_set_dev[64] = {0};
+  if (d->id < 64 && !attr_set_dev[d->id]) {
+    if (cudaFuncSetAttribute(dfl::k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SH::SMEM_BYTES) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_set_dev[d->id] = 1;
+  }
+  CUtensorMap mw, mx;
+  if (!bf16_map(&mw, W, (uint64_t)N_out, (uint64_t)K_in, dfl::BM, d->id)) return DFLASH_ERR_CUDA;
+  if (!bf16_map(&mx, X, (uint64_t)T, (uint64_t)K_in, BN, d->id)) return DFLASH_ERR_CUDA;
+  dfl::GemmParams p;
+  p.out = out;
+  p.ld = ld;
+  p.N_out = N_out;
+  p.T = T;
+  p.S = S;
+  p.kb_per_split = K_in / dfl::BK / S;
+  p.m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
+  p.t_tiles = (T + BN - 1) / BN;
+  p.num_units = p.m_tiles * p.t_tiles * S;
+  p.err = err;
+  const int grid = p.num_units < d->num_sms ? p.num_units : d->num_sms;
+  DFL_CHECK_LAUNCH(launch(dfl::k_gemm_tc<BN>, dim3(grid), dim3(dfl::kGemmThreads),
+                          (size_t)SH::SMEM_BYTES, st, mw, mx, p));
+  return DFLASH_OK;
+}
+
+int gemm_xwT(int dtype, const void *W, int N_out, int K_in, const void *X, int T, float *out,
+             int ld, int S, int *err, cudaStream_t st) {
+  if (T <= 0 || N_out <= 0) return DFLASH_OK;
+  const Dev *d = device();
+  if (!d) return DFLASH_ERR_DEVICE;
+  if (K_in % 64 || S < 1 || (K_in / 64) % S) return DFLASH_ERR_DIMS;
+  if (dtype == DFLASH_F32) {
+    dim3 grid((N_out + 63) / 64, (T + 31) / 32, S);
+    DFL_CHECK_LAUNCH(launch(dfl::k_gemm_f32, grid, dim3(256), 0, st, (const float *)W,
+                            (const float *)X, out, ld, N_out, T, K_in, K_in / S));
+    return DFLASH_OK;
+  }
+  if ((uintptr_t)W % 16 || (uintptr_t)X % 16) return DFLASH_ERR_ALIGN;
+  switch (token_tile(T)) {
+    case 16: return launch_tc<16>(W, N_out, K_in, X, T, out, ld, S, err, st, d);
+    case 32: return launch_tc<32>(W, N_out, K_in, X, T, out, ld, S, err, st, d);
+    case 64: return launch_tc<64>(W, N_out, K_in, X, T, out, ld, S, err, st, d);
+    case 128: return launch_tc<128>(W, N_out, K_in, X, T, out, ld, S, err, st, d);
+    default: return launch_tc<256>(W, N_out, K_in, X, T, out, ld, S, err, st, d);
+  }
+}
+
+}  // namespace dflh

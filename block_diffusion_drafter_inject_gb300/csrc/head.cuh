@@ -1,0 +1,29 @@
+// Per-position top-k + logsumexp, candidate-path selector, greedy acceptance.
+#pragma once
+#include "common.cuh"
+
+namespace dflh {
+
+constexpr int kTopkChunk = 4096;
+
+inline int topk_chunks(int V) { return (V + kTopkChunk - 1) / kTopkChunk; }
+
+// partials: rows * chunks * (2*k + 2) floats
+int launch_topk(const float *logits, int rows, int V, int k, float *partial, int32_t *ids,
+                float *logp, cudaStream_t st);
+
+template <typename S>
+int launch_sel_gather(const S *E, const int32_t *anchor, const int32_t *topk_ids, int B, int K,
+                      int k, int V, int D, S *rows, int *err, cudaStream_t st);
+
+int launch_viterbi(const float *upart, const float *vpart, int nsplit_u, int nsplit_v,
+                   const int32_t *topk_ids, const float *topk_logp, int B, int K, int k, int r,
+                   int32_t *path, float *score, cudaStream_t st);
+
+constexpr int kArgmaxChunk = 8192;
+inline int argmax_chunks(int V) { return (V + kArgmaxChunk - 1) / kArgmaxChunk; }
+// partial: B*K*chunks*2 words
+int launch_accept(const int32_t *path, const void *logits, int dtype, int B, int K, int V,
+                  float *partial, int32_t *accept_len, int32_t *tokens, cudaStream_t st);
+
+}  // namespace dflh

@@ -1,0 +1,220 @@
+/*
+ * dflash.h - C ABI of the DFlash 2 draft cycle on one GPU (sm_103a).
+ *
+ * One draft cycle, as the serving sequence on the DFlash 2 Architecture page
+ * ("One Cycle, Step by Step") orders it:
+ *   1. dflash_inject_context   target hidden states -> every draft layer's K/V cache
+ *   2. dflash_draft_block      one non-causal drafter pass over a block of K slots,
+ *                              per-position top-k candidates
+ *   3. dflash_select_path      one coherent candidate path (Viterbi over the lattice)
+ *   4. dflash_accept_greedy    longest prefix that matches the target's argmax + bonus
+ *
+ * Conventions shared by every call
+ *  - Every buffer belongs to the caller.  The library never allocates, frees or
+ *    synchronises device memory, except dflash_read_device_status, which waits
+ *    for the stream.  All pointers named "device" are device addresses.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL =
+ *    the legacy default stream) and may be captured in a CUDA graph.
+ *  - Return value: DFLASH_OK (0) or a negative DFLASH_ERR_* code for errors the
+ *    host can see (NULL pointer, bad dimension, block size out of range,
+ *    workspace too small, misaligned pointer, launch failure).  Nothing is
+ *    launched when a host check fails.
+ *  - Data-dependent errors (token id >= vocab, page id out of the pool, a
+ *    position beyond the page table, a bounded wait that expired) are found on
+ *    the device: the value is clamped, a bit is OR-ed into the sticky status
+ *    word at the start of the workspace, and the call continues.  Read it with
+ *    dflash_read_device_status.  Kernels never trap or assert.
+ *  - Weights are row-major [out, in] (the nn.Linear layout), in the dtype of
+ *    the config (norm gains and conv base kernels too).  Pointers passed to
+ *    tensor-memory-accelerator loads (fc, wqkv, wo, w_gate_up, w_down, conv_w,
+ *    lm_head, sel_pu, sel_pv, the workspace) must be 16-byte aligned.
+ *  - The workspace must be zero-filled once before its first use (the status
+ *    word lives at offset 0); after that it may be reused by any call of the
+ *    same or smaller shape.  Calls that share a workspace must not overlap.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFLASH_MAX_LAYERS 16
+#define DFLASH_MAX_BLOCK 32   /* K, block slots (anchor + K-1 masks)            */
+#define DFLASH_MAX_TOPK 32    /* candidates kept per position                   */
+
+/* storage dtypes */
+#define DFLASH_F32 0
+#define DFLASH_BF16 1
+
+/* host-side status codes */
+#define DFLASH_OK 0
+#define DFLASH_ERR_NULL (-1)       /* a required pointer is NULL                */
+#define DFLASH_ERR_DIMS (-2)       /* a dimension breaks the shape rules        */
+#define DFLASH_ERR_BLOCK (-3)      /* K outside 2..DFLASH_MAX_BLOCK, or B < 0   */
+#define DFLASH_ERR_WORKSPACE (-4)  /* ws_bytes below dflash_workspace_bytes     */
+#define DFLASH_ERR_DTYPE (-5)      /* unsupported dtype                         */
+#define DFLASH_ERR_CUDA (-6)       /* a CUDA runtime/driver call failed         */
+#define DFLASH_ERR_ALIGN (-7)      /* a pointer is not 16-byte aligned          */
+#define DFLASH_ERR_DEVICE (-8)     /* no usable sm_103 device                   */
+
+/* device-side sticky status bits (dflash_read_device_status) */
+#define DFLASH_DEV_TOKEN_RANGE 1   /* a token id was outside [0, vocab)         */
+#define DFLASH_DEV_PAGE_RANGE 2    /* a page id was outside [0, num_pages)      */
+#define DFLASH_DEV_POS_RANGE 4     /* a position fell outside the page table    */
+#define DFLASH_DEV_TIMEOUT 8       /* a bounded on-chip wait expired            */
+#define DFLASH_DEV_REQ_RANGE 16    /* an inject request row was out of range    */
+
+/* Drafter dimensions.  Shape rules (checked by every call):
+ *   d_model, d_ff, n_taps*d_target, n_q_heads*head_dim multiples of 64;
+ *   head_dim 64 or 128; n_q_heads a multiple of n_kv_heads;
+ *   d_model a multiple of conv_group; 1 <= top_k <= 32, top_k <= vocab;
+ *   sel_rank a multiple of 16 and <= 1024; window >= 1; page_size >= 1;
+ *   1 <= n_layers <= DFLASH_MAX_LAYERS; 0 <= mask_token_id < vocab.         */
+typedef struct dflash_config {
+  int32_t d_model;      /* D, draft width                                   */
+  int32_t n_layers;     /* L                                                */
+  int32_t n_q_heads;    /* Hq                                               */
+  int32_t n_kv_heads;   /* Hkv                                              */
+  int32_t head_dim;     /* d                                                */
+  int32_t d_ff;         /* F, SwiGLU width                                  */
+  int32_t vocab;        /* V                                                */
+  int32_t n_taps;       /* tapped target layers                             */
+  int32_t d_target;     /* target width per tap                             */
+  int32_t window;       /* context keys read per pass (sliding window)      */
+  int32_t page_size;    /* tokens per KV page                               */
+  int32_t top_k;        /* candidates per position                          */
+  int32_t sel_rank;     /* selector rank r                                  */
+  int32_t conv_group;   /* channels sharing one conv gate correction        */
+  int32_t mask_token_id;
+  int32_t dtype;        /* DFLASH_F32 or DFLASH_BF16                        */
+  float rms_eps;        /* RMSNorm epsilon                                  */
+  float rope_theta;     /* RoPE base; 0 disables RoPE                       */
+} dflash_config;
+
+/* One draft layer.  All device pointers, dtype of the config. */
+typedef struct dflash_layer_weights {
+  const void *attn_norm;   /* [D]   pre-attention RMSNorm gain                      */
+  const void *mlp_norm;    /* [D]   pre-MLP RMSNorm gain                            */
+  const void *wqkv;        /* [(Hq+2Hkv)*d, D] rows = [Wq; Wk; Wv]                  */
+  const void *wo;          /* [D, Hq*d]                                             */
+  const void *q_norm;      /* [d]   per-head RMSNorm gain on q                      */
+  const void *k_norm;      /* [d]   per-head RMSNorm gain on k (block and injected) */
+  const void *w_gate_up;   /* [2F, D] rows = [Wgate; Wup]                           */
+  const void *w_down;      /* [D, F]                                                */
+  const void *conv_w[4];   /* [2D/conv_group, D] gate linear [G_a; G_b] of the four
+                              two-tap convs: 0 before attention, 1 after attention,
+                              2 before the MLP, 3 after the MLP                     */
+  const void *conv_base[4];/* [2D] base kernels [base_a; base_b] of the same convs  */
+} dflash_layer_weights;
+
+typedef struct dflash_weights {
+  const void *fc_norm;     /* [n_taps*d_target] RMSNorm gain on the concatenated taps */
+  const void *fc;          /* [D, n_taps*d_target] injection projection              */
+  const void *embed;       /* [V, D] token embeddings                                 */
+  const void *lm_head;     /* [V, D]                                                  */
+  const void *final_norm;  /* [D]                                                     */
+  const void *sel_pu;      /* [r, D] selector projection of the predecessor token     */
+  const void *sel_pv;      /* [r, D] selector projection of the successor token       */
+  dflash_layer_weights layer[DFLASH_MAX_LAYERS];
+} dflash_weights;
+
+/* Paged per-layer draft KV cache.
+ * k, v: device, each [L][num_pages][Hkv][page_size][d] in the config dtype.
+ * page_table: device int32 [num_rows][max_pages_per_req]; row b serves request
+ *   b of a draft call and request row req[n] of an inject call; absolute
+ *   position p of that request lives in page page_table[row][p / page_size],
+ *   slot p % page_size.                                                        */
+typedef struct dflash_kv {
+  void *k;
+  void *v;
+  const int32_t *page_table;
+  int32_t num_pages;
+  int32_t max_pages_per_req;
+  int32_t num_rows;
+} dflash_kv;
+
+/* Bytes of workspace needed by every call below for up to B requests, block
+ * size K and up to max_inject_tokens tokens per inject call.  Returns 0 when
+ * the config or sizes are invalid. */
+size_t dflash_workspace_bytes(const dflash_config *cfg, int32_t B, int32_t K,
+                              int32_t max_inject_tokens);
+
+/* Target-KV injection (KV-injection post, "Persistent Conditioning Through
+ * Target KV Injection"; Architecture page, Component Breakdown, "KV injection
+ * path", and "Internals Worth Knowing": immediate projection into draft KV,
+ * norm + RoPE post-processing).  For each token n:
+ *   c = W_fc RMSNorm_{fc_norm}(target_hidden[n])
+ *   for every layer l: K = RoPE(pos[n], RMSNorm_{k_norm,l}(W_k,l c)) per head,
+ *                      V = W_v,l c
+ * stored at request row req[n], absolute position pos[n].
+ *   target_hidden  device [N, n_taps*d_target], config dtype, row-major
+ *   req, pos       device int32 [N]
+ *   N              0 (no-op) .. max_inject_tokens of the workspace            */
+int dflash_inject_context(const dflash_config *cfg, const dflash_weights *w,
+                          const dflash_kv *kv, const void *target_hidden,
+                          const int32_t *req, const int32_t *pos, int32_t N,
+                          void *ws, size_t ws_bytes, void *stream);
+
+/* One drafter pass over B blocks of K slots (Architecture page, Component
+ * Breakdown: block attention mask, 5-layer backbone with sliding window,
+ * shared lm_head, top-16; "Problem 2": two-tap dynamic convs).  Slot 0 of
+ * request b holds anchor[b] at absolute position ctx_len[b]; slots 1..K-1
+ * hold mask_token_id at positions ctx_len[b]+i.  Attention keys = the last
+ * min(window, ctx_len[b]) injected positions plus all K block slots (no mask
+ * inside the block).  Block K/V are not written to the cache.
+ *   anchor, ctx_len  device int32 [B]
+ *   topk_ids         device int32 [B, K-1, top_k]   out, larger logit first
+ *   topk_logp        device f32   [B, K-1, top_k]   out, logit - logsumexp
+ *   logits_opt       device f32   [B, K-1, V] out, or NULL                     */
+int dflash_draft_block(const dflash_config *cfg, const dflash_weights *w,
+                       const dflash_kv *kv, const int32_t *anchor,
+                       const int32_t *ctx_len, int32_t B, int32_t K,
+                       int32_t *topk_ids, float *topk_logp, float *logits_opt,
+                       void *ws, size_t ws_bytes, void *stream);
+
+/* Candidate-path selector (Architecture page, "Problem 1", eq. S_t, in the
+ * low-rank form (P_u e_a).(P_v e_b) with e = embedding rows, walked by
+ * max-sum Viterbi from the anchor):
+ *   delta_1(j) = logp_1(j) + u(anchor).v(c_1j)
+ *   delta_t(j) = logp_t(j) + max_i [delta_{t-1}(i) + u(c_{t-1,i}).v(c_tj)]
+ * Ties go to the lower candidate rank.
+ *   anchor      device int32 [B]
+ *   topk_ids    device int32 [B, K-1, top_k];  topk_logp device f32 [B, K-1, top_k]
+ *   path        device int32 [B, K-1] out;     path_score device f32 [B] out     */
+int dflash_select_path(const dflash_config *cfg, const dflash_weights *w,
+                       const int32_t *anchor, const int32_t *topk_ids,
+                       const float *topk_logp, int32_t B, int32_t K,
+                       int32_t *path, float *path_score, void *ws, size_t ws_bytes,
+                       void *stream);
+
+/* Greedy acceptance (Architecture page, "Speculative Decoding Context" and
+ * "One Cycle, Step by Step"): row i of the target logits predicts the token
+ * after slot i; draft token path[i] (slot i+1) is accepted while it equals
+ * argmax(target_logits[b, i]) (lower id on ties).  With m accepted drafts,
+ *   accept_len[b] = m + 1,  tokens[b] = path[0..m-1], argmax(row m), -1 ...
+ *   path           device int32 [B, K-1]
+ *   target_logits  device [B, K, V] f32 (logits_dtype DFLASH_F32) or bf16     */
+int dflash_accept_greedy(const int32_t *path, const void *target_logits,
+                         int32_t logits_dtype, int32_t B, int32_t K, int32_t V,
+                         int32_t *accept_len, int32_t *tokens, void *ws,
+                         size_t ws_bytes, void *stream);
+
+/* Waits for `stream`, then returns the sticky device status bits (>= 0) of
+ * the workspace, or a negative DFLASH_ERR_* code. */
+int dflash_read_device_status(const void *ws, void *stream);
+/* Clears the sticky device status word (asynchronous). */
+int dflash_clear_device_status(void *ws, void *stream);
+/* Static description of a status code (host or device bit). */
+const char *dflash_status_string(int code);
+/* Number of kernels the library launched on this thread since the last reset
+ * (a counter kept by the host code; for measurement). */
+int64_t dflash_launch_count(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

@@ -1,0 +1,103 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs.
+
+Tolerances (written here, derived from the storage contract): logits within
+2e-2 of the row maximum for bf16 storage, 1e-3 for the float32 configuration;
+top-k ids, selected paths and accepted lengths bit-exact wherever the oracle's
+decision margin exceeds 1e-2."""
+
+import numpy as np
+import pytest
+
+import oracle
+from _cases import Case, rowmax_rel, topk_compare
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+TOL = {"bf16": 2e-2, "f32": 1e-3}
+KV_TOL = {"bf16": 1.6e-2, "f32": 1e-4}
+
+CASES = [
+    # name, B, K, ctx lengths
+    ("tiny", 1, 8, [64]),
+    ("tiny_bf16", 1, 8, [64]),
+    ("tiny_bf16", 3, 8, [5, 90, 64]),
+    ("small", 2, 16, [130, 7]),
+    ("small_gqa", 2, 8, [200, 129]),
+    ("tiny_bf16", 1, 32, [1]),
+    ("small", 1, 2, [96]),
+]
+
+
+@pytest.fixture(scope="module", params=CASES, ids=lambda c: f"{c[0]}-B{c[1]}-K{c[2]}")
+def case(request):
+    name, B, K, ctx = request.param
+    c = Case(name, B, K, ctx, seed=len(ctx) + K).device()
+    c.g = c.run_device()
+    return c
+
+
+def test_device_status_clean(case):
+    assert case.g["status"] == 0
+
+
+def test_inject_kv_matches_oracle(case):
+    ok, ov = case.oracle()["ck"], case.oracle()["cv"]
+    gk, gv = case.gpu_kv_dense()
+    tol = KV_TOL[case.cfg["dtype"]]
+    for b in range(case.B):
+        for l in range(case.cfg["n_layers"]):
+            if case.ctx[b] == 0:
+                continue
+            assert rowmax_rel(gk[b][l], ok[b][l]) < tol, (b, l)
+            assert rowmax_rel(gv[b][l], ov[b][l]) < tol, (b, l)
+
+
+def test_logits_within_tolerance(case):
+    o = case.oracle()
+    err = rowmax_rel(case.g["logits"], o["logits"])
+    assert err < TOL[case.cfg["dtype"]], err
+
+
+def test_topk_bitexact_above_margin(case):
+    o = case.oracle()
+    compared, bad = topk_compare(case.g["ids"], o["logits"], o["ids"], case.cfg["top_k"])
+    assert compared > 0
+    assert bad == 0, f"{bad} of {compared} ranks differ"
+    # log-probabilities at matching ids
+    same = case.g["ids"] == o["ids"]
+    assert np.max(np.abs(case.g["logp"] - o["logp"])[same]) < 5e-2
+
+
+def test_select_path_on_oracle_candidates(case):
+    """The selector alone: the oracle's candidates in, path out."""
+    import block_diffusion_drafter_inject_gb300 as dfl
+    o = case.oracle()
+    ids = torch.from_numpy(o["ids"]).cuda()
+    logp = torch.from_numpy(o["logp"].astype(np.float32)).cuda()
+    path = torch.zeros((case.B, case.K - 1), dtype=torch.int32, device="cuda")
+    score = torch.zeros((case.B,), dtype=torch.float32, device="cuda")
+    dfl.select_path(case.cfg, case.Wd, case.d_anchor, ids, logp, case.K, case.cyc.ws, path, score)
+    torch.cuda.synchronize()
+    path, score = path.cpu().numpy(), score.cpu().numpy()
+    for b in range(case.B):
+        if o["margin"][b] > 1e-2:
+            assert list(path[b]) == list(o["path"][b]), b
+        assert abs(score[b] - o["score"][b]) < 1e-3 * max(1.0, abs(o["score"][b])), b
+
+
+def test_end_to_end_path_and_accept(case):
+    o = case.oracle()
+    g = case.g
+    for b in range(case.B):
+        same_lattice = np.array_equal(g["ids"][b], o["ids"][b])
+        if same_lattice and o["margin"][b] > 1e-2:
+            assert list(g["path"][b]) == list(o["path"][b]), b
+    # acceptance on the device's own path equals the oracle's rule on that path
+    acc, toks = oracle.accept_greedy(g["path"], case.target)
+    np.testing.assert_array_equal(g["acc"], acc)
+    np.testing.assert_array_equal(g["toks"], toks)
