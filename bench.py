@@ -1,0 +1,481 @@
+"""Benchmark of the DFlash 2 draft cycle on one GB300 (replicas across GPUs).
+
+Headline workload: the full-size drafter (5 layers, width 4096, vocab 151936),
+one request, block K=8, 2048 context tokens with a 1024-token window.  One
+step = one draft cycle: inject K target-hidden rows (the most accepted tokens a
+cycle can add) -> drafter pass + top-16 -> Viterbi selector -> greedy accept.
+value = draft cycles per second over all ranks (each GPU runs its own replica).
+
+Also reported: the draft pass alone (draft_block + select_path) at B=1 and at
+B=32 (ragged contexts in [512, 8192], paged 64-token pages), each as a
+fraction of the HBM roofline for its algorithmic bytes; the roofline of the
+dominant kernel (the tcgen05 projection GEMM) over the pass's GEMM shapes;
+an end-to-end figure through the C ABI with host buffers; and the CPU oracle
+timed on a bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-b32]
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "draft cycles/s (full-size DFlash 2 drafter, B=1, block 8)"
+UNIT = "cycles/s"
+WORKLOAD = "full drafter: D 4096, 5 layers, 32q/8kv x 128, SwiGLU 14336, vocab 151936; B=1, K=8, context 2048, window 1024, top-16, selector rank 256"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d["bf16_tflops_sustained"]), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ------------------------------------------------------------------ workload shapes
+
+def weight_bytes(cfg):
+    es = 2 if cfg["dtype"] == "bf16" else 4
+    return {n: int(np.prod(s)) * es for n, s, _ in synth.weight_names(cfg)}
+
+
+def pass_bytes(cfg, B, K, ctx):
+    """Algorithmic bytes of one draft pass (draft_block + select_path): every weight
+    the pass multiplies by, once; the window's context K/V; embedding rows gathered."""
+    wb = weight_bytes(cfg)
+    es = 2
+    D, k = cfg["d_model"], cfg["top_k"]
+    w = sum(v for n, v in wb.items() if n not in ("fc", "fc_norm", "embed"))
+    kv = 0
+    per_tok = cfg["n_layers"] * 2 * cfg["n_kv_heads"] * cfg["head_dim"] * es
+    for c in ctx:
+        kv += min(cfg["window"], int(c)) * per_tok
+    gathers = B * (K + 1 + (K - 1) * k) * D * es
+    return w + kv + gathers
+
+
+def pass_gemms(cfg, B, K):
+    """(N_out, K_in, T, weight name) of every projection GEMM of one draft pass."""
+    D, F, V = cfg["d_model"], cfg["d_ff"], cfg["vocab"]
+    Hq, Hkv, dh = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    GW = 2 * D // cfg["conv_group"]
+    T = B * K
+    out = []
+    for l in range(cfg["n_layers"]):
+        p = f"layers.{l}."
+        out += [(GW, D, T, p + "conv_w.0"), ((Hq + 2 * Hkv) * dh, D, T, p + "wqkv"),
+                (D, Hq * dh, T, p + "wo"), (GW, D, T, p + "conv_w.1"), (GW, D, T, p + "conv_w.2"),
+                (2 * F, D, T, p + "w_gate_up"), (D, F, T, p + "w_down"), (GW, D, T, p + "conv_w.3")]
+    out.append((V, D, B * (K - 1), "lm_head"))
+    R = 1 + (K - 1) * cfg["top_k"]
+    out += [(cfg["sel_rank"], D, B * R, "sel_pu"), (cfg["sel_rank"], D, B * R, "sel_pv")]
+    return out
+
+
+def window_layout(ctx, K, P, W, seed):
+    """Page table holding only the pages a pass touches: positions [ctx-W, ctx+K)."""
+    B = len(ctx)
+    maxp = max((int(c) + K + P - 1) // P for c in ctx)
+    need = []
+    for c in ctx:
+        lo = max(0, int(c) - W)
+        need.append(list(range(lo // P, (int(c) + K - 1) // P + 1)))
+    total = sum(len(n) for n in need)
+    perm = synth.stream(seed, "page_perm").permutation(total)
+    table = np.full((B, maxp), -1, dtype=np.int32)
+    o = 0
+    for b, pages in enumerate(need):
+        for pi in pages:
+            table[b, pi] = perm[o]
+            o += 1
+    return table, total
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+                 "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, gpu_index):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9 or f[0] != str(gpu_index):
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def event_time(torch, fn, steps, warmup, barrier=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return s.elapsed_time(e) / steps   # ms per step
+
+
+def capture(torch, fn):
+    fn()                                   # first call sets kernel attributes
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def setup_workload(torch, dfl, cfg, Wd, B, K, ctx, seed, max_inject):
+    """Paged KV holding the injected window of every request; device inputs of a cycle."""
+    P, Wn = cfg["page_size"], cfg["window"]
+    table, npages = window_layout(ctx, K, P, Wn, seed)
+    kv = dfl.PagedKV(cfg, table, npages, "cuda")
+    cyc = dfl.DraftCycle(cfg, Wd, kv, B, K, max_inject, "cuda")
+    # prefill: inject each request's window (synthetic hidden states), in chunks
+    req = np.concatenate([np.full(min(Wn, int(c)), b, np.int32) for b, c in enumerate(ctx)])
+    pos = np.concatenate([np.arange(max(0, int(c) - Wn), int(c), dtype=np.int32) for c in ctx])
+    hid = synth.make_hiddens(cfg, len(req), seed=seed, name="prefill_hiddens")
+    for o in range(0, len(req), max_inject):
+        sl = slice(o, o + max_inject)
+        dfl.inject_context(cfg, Wd, kv, torch.from_numpy(hid[sl]).to(torch.bfloat16).cuda(),
+                           torch.from_numpy(req[sl]).cuda(), torch.from_numpy(pos[sl]).cuda(),
+                           cyc.ws)
+    torch.cuda.synchronize()
+    # per-cycle inputs: re-inject the last K context rows of every request
+    creq = np.repeat(np.arange(B, dtype=np.int32), K)
+    cpos = np.concatenate([np.arange(int(c) - K, int(c), dtype=np.int32) for c in ctx])
+    ch = synth.make_hiddens(cfg, B * K, seed=seed, name="cycle_hiddens")
+    inp = dict(
+        hidden=torch.from_numpy(ch).to(torch.bfloat16).cuda(),
+        req=torch.from_numpy(creq).cuda(), pos=torch.from_numpy(cpos).cuda(),
+        anchor=torch.from_numpy(synth.make_anchors(cfg, B, seed=seed)).cuda(),
+        ctx=torch.from_numpy(np.asarray(ctx, np.int32)).cuda(),
+        target=torch.from_numpy(synth.make_target_logits(cfg, B, K, seed=seed)).cuda())
+    return kv, cyc, inp
+
+
+def run_gpu(args, rank, world, barrier, allmax):
+    import torch
+    import block_diffusion_drafter_inject_gb300 as dfl
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    cfg = synth.preset("full")
+    pk = peaks()
+    t0 = time.time()
+    Wh = synth.make_weights(cfg, seed=0)
+    Wd = dfl.DeviceWeights.from_host(cfg, Wh, "cuda")
+    setup_s = time.time() - t0
+
+    # ---------------- headline: B=1, K=8, ctx 2048
+    B, K, ctx = 1, 8, [2048]
+    kv, cyc, inp = setup_workload(torch, dfl, cfg, Wd, B, K, ctx, 0, 1024)
+
+    def cycle():
+        cyc.run(inp["hidden"], inp["req"], inp["pos"], inp["anchor"], inp["ctx"], inp["target"])
+
+    def dpass():
+        dfl.draft_block(cfg, Wd, kv, inp["anchor"], inp["ctx"], K, cyc.ws, cyc.topk_ids,
+                        cyc.topk_logp)
+        dfl.select_path(cfg, Wd, inp["anchor"], cyc.topk_ids, cyc.topk_logp, K, cyc.ws, cyc.path,
+                        cyc.score)
+
+    dfl.launch_count(reset=True)
+    cycle()
+    torch.cuda.synchronize()
+    launches_per_cycle = dfl.launch_count(reset=True)
+    status = dfl.read_device_status(cyc.ws)
+    g_cycle = capture(torch, cycle)
+    g_pass = capture(torch, dpass)
+
+    gpu_name = torch.cuda.get_device_name(dev)
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    with Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) as clk:
+        ms_cycle = event_time(torch, g_cycle.replay, args.steps, args.warmup, barrier)
+        ms_pass = event_time(torch, g_pass.replay, args.steps, args.warmup)
+    ms_cycle = allmax(ms_cycle)
+    clocks = clk.summary(dev)
+
+    # ---------------- dominant kernel: the projection GEMM at the pass's shapes
+    gem = pass_gemms(cfg, B, K)
+    xs = {}
+    outs = {}
+    gem_bytes = 0
+    for (N, Kin, T, name) in gem:
+        key = (T, Kin)
+        if key not in xs:
+            xs[key] = torch.randn((T, Kin), device="cuda").to(torch.bfloat16)
+        S = dfl.linear_splits(N, T, Kin)
+        outs[(N, Kin, T)] = (torch.empty((S, T, N), device="cuda", dtype=torch.float32), S)
+        gem_bytes += N * Kin * 2 + T * Kin * 2 + T * N * 4
+
+    def gemms():
+        for (N, Kin, T, name) in gem:
+            o, S = outs[(N, Kin, T)]
+            dfl.linear(Wd.t[name], xs[(T, Kin)], o, S)
+
+    g_gemm = capture(torch, gemms)
+    ms_gemm = event_time(torch, g_gemm.replay, args.steps, args.warmup)
+    gemm_gbs = gem_bytes / (ms_gemm * 1e-3) / 1e9
+
+    # ---------------- e2e through the C ABI with host buffers
+    pin = {k: v.cpu().pin_memory() for k, v in inp.items()}
+    out_acc = torch.empty_like(cyc.accept_len, device="cpu").pin_memory()
+    out_tok = torch.empty_like(cyc.tokens, device="cpu").pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = out_acc.numel() * 4 + out_tok.numel() * 4
+
+    def e2e_step():
+        for k in inp:
+            inp[k].copy_(pin[k], non_blocking=True)
+        g_cycle.replay()
+        out_acc.copy_(cyc.accept_len, non_blocking=True)
+        out_tok.copy_(cyc.tokens, non_blocking=True)
+
+    ms_e2e = allmax(event_time(torch, e2e_step, args.steps, args.warmup, barrier))
+
+    pb1 = pass_bytes(cfg, B, K, ctx)
+    res = {
+        "metric": METRIC, "value": world * 1e3 / ms_cycle, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_cycle,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) target hiddens, N(0,3) target logits)",
+        "config": {"workload": WORKLOAD, "B": B, "K": K, "ctx": ctx[0], "window": cfg["window"],
+                   "cycle": "inject K rows + draft_block + select_path + accept_greedy, one CUDA graph",
+                   "l2": "inputs larger than L2: 3.5 GB of weights streamed per step, no flush",
+                   "parallelism": f"replicas x{world}"},
+        "draft_pass_us": ms_pass * 1e3,
+        "draft_pass_bytes": pb1,
+        "draft_pass_hbm_frac": pb1 / (ms_pass * 1e-3) / 1e9 / pk["hbm"],
+        "roofline": {"kernel": "k_gemm_tc (tcgen05 projection GEMM, all shapes of one B=1 pass)",
+                     "bound": "hbm", "achieved": gemm_gbs, "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": gemm_gbs / pk["hbm"], "traffic": None,
+                     "algorithmic_bytes_per_pass": gem_bytes, "us_per_pass": ms_gemm * 1e3,
+                     "peak_source": pk["src"]},
+        "e2e": {"value": world * 1e3 / ms_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_cycle * args.steps,
+        "launches_per_cycle": launches_per_cycle,
+        "clocks": clocks,
+        "gpu": gpu_name,
+        "device_status": status,
+        "setup_s": round(setup_s, 1),
+    }
+
+    # ---------------- B=32 draft pass (ragged contexts, paged)
+    if not args.no_b32:
+        del g_cycle, g_pass, g_gemm
+        B2 = 32
+        ctx2 = synth.make_ctx_lens(B2, 512, 8192, seed=1).tolist()
+        kv2, cyc2, inp2 = setup_workload(torch, dfl, cfg, Wd, B2, K, ctx2, 1, 4096)
+
+        def dpass2():
+            dfl.draft_block(cfg, Wd, kv2, inp2["anchor"], inp2["ctx"], K, cyc2.ws, cyc2.topk_ids,
+                            cyc2.topk_logp)
+            dfl.select_path(cfg, Wd, inp2["anchor"], cyc2.topk_ids, cyc2.topk_logp, K, cyc2.ws,
+                            cyc2.path, cyc2.score)
+
+        def cycle2():
+            cyc2.run(inp2["hidden"], inp2["req"], inp2["pos"], inp2["anchor"], inp2["ctx"],
+                     inp2["target"])
+
+        gp2 = capture(torch, dpass2)
+        gc2 = capture(torch, cycle2)
+        ms_p2 = event_time(torch, gp2.replay, max(5, args.steps // 2), args.warmup)
+        ms_c2 = event_time(torch, gc2.replay, max(5, args.steps // 2), args.warmup)
+        pb2 = pass_bytes(cfg, B2, K, ctx2)
+        fl2 = sum(2.0 * N * Kin * T for (N, Kin, T, _) in pass_gemms(cfg, B2, K))
+        t_hbm = pb2 / (pk["hbm"] * 1e9)
+        t_tc = fl2 / (pk["bf16_sus"] * 1e12)
+        res["b32"] = {"draft_pass_us": ms_p2 * 1e3, "cycle_us": ms_c2 * 1e3,
+                      "cycles_per_s": 1e3 / ms_c2, "pass_bytes": pb2, "pass_gemm_flops": fl2,
+                      "hbm_floor_us": t_hbm * 1e6, "tensor_floor_us": t_tc * 1e6,
+                      "frac_of_tighter_roofline": max(t_hbm, t_tc) / (ms_p2 * 1e-3),
+                      "ctx_range": [min(ctx2), max(ctx2)]}
+    return res, Wh
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(cfg, Wh, K=8, ctx=2048, reps=1, seed=0):
+    """Time the unmodified oracle on a bounded sample of the headline cycle: layer 0
+    of the drafter, 1/L of the lm_head's vocabulary rows, the per-cycle injection
+    through that layer, the selector and greedy accept.  Returns (seconds per
+    sample, fraction of one cycle's weight parameters the sample touches)."""
+    import oracle
+    L = cfg["n_layers"]
+    Vs = cfg["vocab"] // L
+    scfg = dict(cfg, n_layers=1, vocab=Vs, mask_token_id=Vs - 1)
+    Ws = {k: v for k, v in Wh.items() if not k.startswith("layers.") or k.startswith("layers.0.")}
+    Ws["lm_head"] = Wh["lm_head"][:Vs]
+    g = synth.stream(seed, "oracle_ctx")
+    n = min(ctx, cfg["window"])
+    shape = (ctx, cfg["n_kv_heads"], cfg["head_dim"])
+    ck = np.zeros(shape, np.float32)
+    cv = np.zeros(shape, np.float32)
+    ck[ctx - n:] = g.standard_normal((n,) + shape[1:], dtype=np.float32)
+    cv[ctx - n:] = g.standard_normal((n,) + shape[1:], dtype=np.float32)
+    hid = synth.make_hiddens(cfg, K, seed=seed, name="cycle_hiddens")
+    anchor = synth.make_anchors(scfg, 1, seed=seed)
+    target = synth.make_target_logits(cfg, 1, K, seed=seed)
+    times = []
+    for _ in range(reps):
+        t = time.perf_counter()
+        oracle.inject_context(scfg, Ws, hid, np.arange(ctx - K, ctx), "bf16")
+        d = oracle.draft_block(scfg, Ws, [[ck]], [[cv]], anchor, [ctx], K, "bf16")
+        path, _ = oracle.select_path(scfg, Ws, anchor, d["ids"], d["logp"])
+        oracle.accept_greedy(path, target)
+        times.append(time.perf_counter() - t)
+    full = sum(int(np.prod(s)) for n, s, _ in synth.weight_names(cfg) if n != "embed")
+    samp = sum(int(np.prod(s)) for n, s, _ in synth.weight_names(scfg) if n != "embed")
+    return float(np.median(times)), samp / full
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(Wh, cfg):
+    t, frac = oracle_sample(cfg, Wh, reps=3)
+    return {"value": frac / t, "unit": UNIT, "cores": cores(), "kind": "oracle",
+            "sample": f"oracle (NumPy float64) on layer 0 + 1/{cfg['n_layers']} of the lm_head rows "
+                      f"+ per-cycle inject + selector + accept of the B=1 K=8 cycle; "
+                      f"{t:.2f} s per sample (median of 3), sample = {frac:.3f} of the cycle's "
+                      f"weight parameters, value = fraction / seconds"}
+
+
+def run_reference(args):
+    """The oracle as it stands on the host cores, on this workload's metric."""
+    cfg = synth.preset("full")
+    Wh = synth.make_weights(cfg, seed=0)
+    for _ in range(args.warmup):
+        oracle_sample(cfg, Wh, reps=1)
+    ts, frac = [], None
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        t, frac = oracle_sample(cfg, Wh, reps=1)
+        ts.append(t)
+    total = time.perf_counter() - t0
+    sec_per_cycle = (total / args.steps) / frac
+    v = 1.0 / sec_per_cycle
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "B": 1, "K": 8, "ctx": 2048},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                             "sample": f"each step: oracle on layer 0 + 1/5 of lm_head rows + "
+                                       f"inject + select + accept = {frac:.3f} of a cycle's weights"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-b32", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            args.steps = max(1, min(args.steps, 20))
+            args.warmup = min(args.warmup, 1)
+            print(json.dumps(run_reference(args)))
+        return
+
+    barrier = None
+    allmax = lambda x: x  # noqa: E731
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+
+        def barrier():
+            dist.barrier()
+
+        def allmax(x):
+            t = torch.tensor([x], device="cuda", dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+
+    res, Wh = run_gpu(args, rank, world, barrier, allmax)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(Wh, synth.preset("full"))
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

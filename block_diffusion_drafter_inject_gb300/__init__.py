@@ -18,6 +18,8 @@ from .api import (  # noqa: F401
     draft_block,
     inject_context,
     launch_count,
+    linear,
+    linear_splits,
     make_config,
     read_device_status,
     select_path,

@@ -60,6 +60,8 @@ EXPORTS = {
                                           vp, i32, i32, vp, vp, vp, ctypes.c_size_t, vp]),
     "dflash_accept_greedy": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                             ctypes.c_size_t, vp]),
+    "dflash_linear": (ctypes.c_int, [i32, vp, i32, i32, vp, i32, i32, vp, vp]),
+    "dflash_linear_splits": (ctypes.c_int32, [i32, i32, i32]),
     "dflash_read_device_status": (ctypes.c_int, [vp, vp]),
     "dflash_clear_device_status": (ctypes.c_int, [vp, vp]),
     "dflash_status_string": (ctypes.c_char_p, [ctypes.c_int]),

@@ -143,6 +143,19 @@ def accept_greedy(path, target_logits, ws, accept_len, tokens, stream=None):
           "dflash_accept_greedy")
 
 
+def linear_splits(N_out, T, K_in):
+    return int(lib().dflash_linear_splits(N_out, T, K_in))
+
+
+def linear(W, X, out, splits, stream=None):
+    """out[s] (s < splits) = slice s of X @ W.T; W [N_out, K_in], X [T, K_in] (same dtype)."""
+    N, Kin = W.shape
+    T = X.shape[0]
+    dt = _lib.F32 if W.dtype == torch.float32 else _lib.BF16
+    check(lib().dflash_linear(dt, _ptr(W), N, Kin, _ptr(X), T, int(splits), _ptr(out),
+                              _stream(stream)), "dflash_linear")
+
+
 def read_device_status(ws, stream=None):
     r = lib().dflash_read_device_status(ws.ptr, _stream(stream))
     if r < 0:

@@ -106,6 +106,8 @@ static int check_weights(const dflash_config *c, const dflash_weights *w, bool d
   if (draft) {
     if (!w->embed || !w->lm_head || !w->final_norm) return DFLASH_ERR_NULL;
     if (!a16(w->lm_head) || !a16(w->embed)) return DFLASH_ERR_ALIGN;
+    for (int l = 0; l < c->n_layers; ++l)
+      if (!a16(w->layer[l].attn_norm)) return DFLASH_ERR_ALIGN;
   }
   return DFLASH_OK;
 }
@@ -235,9 +237,10 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
                  st));
     kn.p[l] = w.layer[l].k_norm;
   }
+  const RopeTable rope = rope_table(c.rope_theta, dh);
   TRY(launch_inject_store<S>(kvpart, S_kv, N, c.n_layers, Hkv, dh, kn, req, pos, kv.page_table,
-                             kv.num_rows, kv.max_pages_per_req, kv.num_pages, c.page_size,
-                             c.rope_theta, c.rms_eps, (S *)kv.k, (S *)kv.v, err, st));
+                             kv.num_rows, kv.max_pages_per_req, kv.num_pages, c.page_size, rope,
+                             c.rms_eps, (S *)kv.k, (S *)kv.v, err, st));
   return DFLASH_OK;
 }
 
@@ -260,6 +263,7 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   float *logits = logits_opt ? logits_opt : (float *)(ws + L.logits);
   float *part = (float *)(ws + L.part), *gpart = (float *)(ws + L.gpart);
   float *attnp = (float *)(ws + L.attn), *topkp = (float *)(ws + L.topk);
+  const RopeTable rope = rope_table(c.rope_theta, dh);
 
   TRY(launch_embed_norm<S>((const S *)w.embed, anchor, c.mask_token_id, V, B, K, D,
                            (const S *)w.layer[0].attn_norm, eps, x, un, err, st));
@@ -271,7 +275,7 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     TRY(launch_conv_pre<S>(un, gpart, L.S_gate, T, K, D, g, (const S *)lw.conv_base[0], ub, st));
     TRY(gemm_xwT(dt, lw.wqkv, QKVW, D, ub, T, part, QKVW, L.S_qkv, err, st));
     TRY(launch_qkv_post<S>(part, L.S_qkv, T, K, Hq, Hkv, dh, (const S *)lw.q_norm,
-                           (const S *)lw.k_norm, ctx_len, c.rope_theta, eps, qb, kb, vb, st));
+                           (const S *)lw.k_norm, ctx_len, rope, eps, qb, kb, vb, st));
     TRY(launch_block_attention<S>(L.ap, qb, kb, vb, (const S *)kv.k, (const S *)kv.v, l,
                                   kv.page_table, kv.max_pages_per_req, kv.num_pages, c.page_size,
                                   ctx_len, B, K, Hq, Hkv, dh, c.window, attnp, ob, err, st));
@@ -311,7 +315,15 @@ static int run_select(const dflash_config &c, const dflash_weights &w, const int
   TRY(launch_sel_gather<S>((const S *)w.embed, anchor, ids, B, K, k, c.vocab, D, rows, err, st));
   TRY(gemm_xwT(c.dtype, w.sel_pu, r, D, rows, TR, up, r, L.S_sel, err, st));
   TRY(gemm_xwT(c.dtype, w.sel_pv, r, D, rows, TR, vp, r, L.S_sel, err, st));
-  TRY(launch_viterbi(up, vp, L.S_sel, L.S_sel, ids, logp, B, K, k, r, path, score, st));
+  int ns = L.S_sel;
+  if (ns > 1) {
+    // sum the K slices in place (slice 0 receives the sum) with many CTAs, so the
+    // one-CTA-per-request Viterbi kernel reads each projection once
+    TRY(launch_reduce<S>(up, ns, TR, r, up, (S *)nullptr, st));
+    TRY(launch_reduce<S>(vp, ns, TR, r, vp, (S *)nullptr, st));
+    ns = 1;
+  }
+  TRY(launch_viterbi(up, vp, ns, ns, ids, logp, B, K, k, r, path, score, st));
   return DFLASH_OK;
 }
 
@@ -338,6 +350,7 @@ int dflash_inject_context(const dflash_config *cfg, const dflash_weights *w, con
   if (N < 0) return DFLASH_ERR_DIMS;
   if (N == 0) return DFLASH_OK;
   if (!target_hidden || !req || !pos || !ws) return DFLASH_ERR_NULL;
+  if (!a16(target_hidden) || !a16(w->fc_norm)) return DFLASH_ERR_ALIGN;
   if ((rc = check_weights(cfg, w, false)) != DFLASH_OK) return rc;
   if ((rc = check_kv(cfg, kv)) != DFLASH_OK) return rc;
   if (!a16(ws)) return DFLASH_ERR_ALIGN;
@@ -414,6 +427,23 @@ int dflash_accept_greedy(const int32_t *path, const void *target_logits, int32_t
   if (!device()) return DFLASH_ERR_DEVICE;
   return launch_accept(path, target_logits, logits_dtype, B, K, V, (float *)((uint8_t *)ws + 256),
                        accept_len, tokens, (cudaStream_t)stream);
+}
+
+int dflash_linear(int32_t dtype, const void *W, int32_t N_out, int32_t K_in, const void *X,
+                  int32_t T, int32_t splits, float *out, void *stream) {
+  if (dtype != DFLASH_F32 && dtype != DFLASH_BF16) return DFLASH_ERR_DTYPE;
+  if (N_out < 1 || T < 0 || K_in < 64 || K_in % 64) return DFLASH_ERR_DIMS;
+  if (splits < 1 || (K_in / 64) % splits) return DFLASH_ERR_DIMS;
+  if (T == 0) return DFLASH_OK;
+  if (!W || !X || !out) return DFLASH_ERR_NULL;
+  if (!a16(W) || !a16(X)) return DFLASH_ERR_ALIGN;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  return gemm_xwT(dtype, W, N_out, K_in, X, T, out, N_out, splits, nullptr, (cudaStream_t)stream);
+}
+
+int32_t dflash_linear_splits(int32_t N_out, int32_t T, int32_t K_in) {
+  if (N_out < 1 || T < 1 || K_in < 64 || K_in % 64) return 0;
+  return gemm_splits(N_out, T, K_in, sm_count_or_default());
 }
 
 int dflash_read_device_status(const void *ws, void *stream) {

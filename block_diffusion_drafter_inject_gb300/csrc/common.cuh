@@ -25,6 +25,29 @@ __device__ __forceinline__ float rnd(float v, const bf16 *) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
+// 8 consecutive elements (16-byte aligned for bf16, 32-byte for float)
+__device__ __forceinline__ void load8(const bf16 *p, float *v) {
+  uint4 u = *(const uint4 *)p;
+  const bf16 *h = (const bf16 *)&u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __bfloat162float(h[i]);
+}
+__device__ __forceinline__ void load8(const float *p, float *v) {
+  float4 a = ((const float4 *)p)[0], b = ((const float4 *)p)[1];
+  v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+}
+__device__ __forceinline__ void store8(bf16 *p, const float *v) {
+  uint4 u;
+  bf16 *h = (bf16 *)&u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = __float2bfloat16_rn(v[i]);
+  *(uint4 *)p = u;
+}
+__device__ __forceinline__ void store8(float *p, const float *v) {
+  ((float4 *)p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  ((float4 *)p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
 __device__ __forceinline__ void set_err(int *err, int bit) {
   if (err) atomicOr(err, bit);
 }

@@ -363,18 +363,31 @@ static bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t 
 static int token_tile(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
 
 int gemm_splits(int N_out, int T, int K_in, int num_sms) {
+  // Pick the K split that best fills whole waves of one CTA per SM, among
+  // splits that keep >= 2 k-blocks per unit and the partial buffer under its
+  // cap; prefer fewer splits when the fill is about equal.
   const int kb = K_in / dfl::BK;
   const int m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
   const int bn = token_tile(T);
   const int t_tiles = (T + bn - 1) / bn;
   const long base = (long)m_tiles * t_tiles;
   int best = 1;
+  double best_score = -1.0;
   for (int S = 1; S <= kb; ++S) {
     if (kb % S) continue;
     if (S > 1 && (size_t)S * T * N_out > kMaxPartialFloats) break;
     if (S > 1 && kb / S < 2) break;
-    best = S;
-    if (base * S >= num_sms) break;
+    const long units = base * S;
+    const long waves = (units + num_sms - 1) / num_sms;
+    const double fill = (double)units / (double)(waves * num_sms);
+    // partial slices: written once and read once by the consumer, relative to
+    // the weight bytes; mostly L2 traffic while the slices stay small
+    const double part_bytes = 8.0 * S * T * (double)N_out;
+    const double alpha = part_bytes <= 32e6 ? 0.25 : 1.0;
+    const double extra = S > 1 ? alpha * part_bytes / (2.0 * N_out * (double)K_in) : 0.0;
+    const double score = fill / (1.0 + extra) - 0.002 * S / kb;
+    if (score > best_score + 1e-9) best_score = score, best = S;
+    if (units >= 8L * num_sms) break;  // many waves: fill no longer matters
   }
   return best;
 }

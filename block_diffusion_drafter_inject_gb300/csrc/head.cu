@@ -268,38 +268,34 @@ __global__ void __launch_bounds__(256) k_argmax_partial(const L *__restrict__ lo
   }
 }
 
-// per request: argmax of each row, then the longest matching prefix
-__global__ void k_accept(const int32_t *__restrict__ path, const float *__restrict__ partial,
-                         int B, int K, int nch, int32_t *__restrict__ accept_len,
-                         int32_t *__restrict__ tokens) {
+// per request: argmax of each row (one warp per row), then the longest matching prefix
+__global__ void __launch_bounds__(1024) k_accept(const int32_t *__restrict__ path,
+                                                 const float *__restrict__ partial, int B, int K,
+                                                 int nch, int32_t *__restrict__ accept_len,
+                                                 int32_t *__restrict__ tokens) {
+  __shared__ int tgt[DFLASH_MAX_BLOCK];
   pdl_launch();
   pdl_wait();
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= B) return;
-  int m = 0;
-  bool run = true;
-  for (int i = 0; i < K; ++i) {
-    const float *p = partial + (size_t)(b * K + i) * nch * 2;
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int c = 0; c < nch; ++c) {
+  const int b = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (w < K) {
+    const float *p = partial + (size_t)(b * K + w) * nch * 2;
+    VI best{-INFINITY, 0x7fffffff};
+    for (int c = lane; c < nch; c += 32) {
       const float v = p[2 * c];
       const int id = __float_as_int(p[2 * c + 1]);
-      if (better(v, id, bv, bi)) bv = v, bi = id;
+      if (better(v, id, best.v, best.i)) best.v = v, best.i = id;
     }
-    if (run) {
-      if (i < K - 1 && path[(size_t)b * (K - 1) + i] == bi) {
-        tokens[(size_t)b * K + i] = bi;
-        ++m;
-      } else {
-        tokens[(size_t)b * K + i] = bi;  // bonus token
-        run = false;
-      }
-    } else {
-      tokens[(size_t)b * K + i] = -1;
-    }
+    best = warp_best(best);
+    if (lane == 0) tgt[w] = best.i;
   }
-  accept_len[b] = m + 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int m = 0;
+    while (m < K - 1 && path[(size_t)b * (K - 1) + m] == tgt[m]) ++m;
+    for (int i = 0; i < K; ++i)
+      tokens[(size_t)b * K + i] = i < m ? tgt[i] : i == m ? tgt[m] : -1;
+    accept_len[b] = m + 1;
+  }
 }
 
 }  // namespace dfl
@@ -361,7 +357,7 @@ int launch_accept(const int32_t *path, const void *logits, int dtype, int B, int
     DFL_CHECK_LAUNCH(launch(dfl::k_argmax_partial<dfl::bf16>, dim3(nch, B * K), dim3(256), 0, st,
                             (const dfl::bf16 *)logits, V, partial));
   }
-  DFL_CHECK_LAUNCH(launch(dfl::k_accept, dim3((B + 127) / 128), dim3(128), 0, st,
+  DFL_CHECK_LAUNCH(launch(dfl::k_accept, dim3(B), dim3(32 * K), 0, st,
                           (const int32_t *)path, (const float *)partial, B, K, nch, accept_len,
                           tokens));
   return DFLASH_OK;

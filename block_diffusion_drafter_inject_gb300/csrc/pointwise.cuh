@@ -9,6 +9,13 @@ struct LayerPtrs {
   const void *p[DFLASH_MAX_LAYERS];
 };
 
+// RoPE frequencies theta^(-2i/d), i < d/2, computed once on the host in fp64.
+struct RopeTable {
+  double inv_freq[64];
+  int enabled;
+};
+RopeTable rope_table(float theta, int head_dim);
+
 template <typename S>
 int launch_embed_norm(const S *E, const int32_t *anchor, int mask_id, int V, int B, int K, int D,
                       const S *gain, float eps, float *x, S *un, int *err, cudaStream_t st);
@@ -29,13 +36,13 @@ template <typename S>
 int launch_swiglu(const float *part, int nsplit, int rows, int F, S *hb, cudaStream_t st);
 template <typename S>
 int launch_qkv_post(const float *part, int nsplit, int rows, int K, int Hq, int Hkv, int dh,
-                    const S *qn, const S *kn, const int32_t *ctx_len, float theta, float eps,
-                    S *qb, S *kb, S *vb, cudaStream_t st);
+                    const S *qn, const S *kn, const int32_t *ctx_len, const RopeTable &rope,
+                    float eps, S *qb, S *kb, S *vb, cudaStream_t st);
 template <typename S>
 int launch_inject_store(const float *kvpart, int nsplit, int N, int L, int Hkv, int dh,
                         LayerPtrs knorm, const int32_t *req, const int32_t *pos,
                         const int32_t *page_table, int num_rows, int max_pages, int num_pages,
-                        int page_size, float theta, float eps, S *kc, S *vc, int *err,
+                        int page_size, const RopeTable &rope, float eps, S *kc, S *vc, int *err,
                         cudaStream_t st);
 
 }  // namespace dflh

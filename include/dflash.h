@@ -203,6 +203,22 @@ int dflash_accept_greedy(const int32_t *path, const void *target_logits,
                          int32_t *accept_len, int32_t *tokens, void *ws,
                          size_t ws_bytes, void *stream);
 
+/* The projection GEMM every call above is built on (the drafter's dense
+ * layers: nn.Linear without bias).  Slice s of `out` receives
+ *   out[s][t][n] = sum over the s-th of `splits` equal K ranges of X[t][k] W[n][k]
+ * so Y = X W^T = sum_s out[s].  bf16 operands run on the tcgen05 tensor cores
+ * fed by TMA; f32 operands on CUDA cores.
+ *   dtype   DFLASH_BF16 or DFLASH_F32 (both W and X)
+ *   W       device [N_out, K_in] row-major, 16-byte aligned
+ *   X       device [T, K_in] row-major, 16-byte aligned
+ *   splits  >= 1 and dividing K_in/64 (dflash_linear_splits gives the
+ *           library's own choice for the shape)
+ *   out     device f32 [splits, T, N_out]
+ * K_in must be a multiple of 64. */
+int dflash_linear(int32_t dtype, const void *W, int32_t N_out, int32_t K_in, const void *X,
+                  int32_t T, int32_t splits, float *out, void *stream);
+int32_t dflash_linear_splits(int32_t N_out, int32_t T, int32_t K_in);
+
 /* Waits for `stream`, then returns the sticky device status bits (>= 0) of
  * the workspace, or a negative DFLASH_ERR_* code. */
 int dflash_read_device_status(const void *ws, void *stream);

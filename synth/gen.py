@@ -22,9 +22,12 @@ def stream(base_seed, name, chunk=0):
 def f32_to_bf16_bits(x):
     """Round float32 values to the nearest bfloat16 (ties to even); returns uint16 bits."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    b = x.view(np.uint32).astype(np.uint64)
-    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
-    return b.astype(np.uint16)
+    b = x.view(np.uint32)
+    r = (b >> 16) & 1                       # finite values cannot overflow 32 bits here
+    r += 0x7FFF
+    r += b
+    r >>= 16
+    return r.astype(np.uint16)
 
 
 def bf16_bits_to_f32(bits):
