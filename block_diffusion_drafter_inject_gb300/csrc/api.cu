@@ -100,12 +100,13 @@ static int check_weights(const dflash_config *c, const dflash_weights *w, bool d
     if (!a16(L.wo) || !a16(L.w_gate_up) || !a16(L.w_down)) return DFLASH_ERR_ALIGN;
     for (int i = 0; i < 4; ++i) {
       if (!L.conv_w[i] || !L.conv_base[i]) return DFLASH_ERR_NULL;
-      if (!a16(L.conv_w[i])) return DFLASH_ERR_ALIGN;
+      if (!a16(L.conv_w[i]) || !a16(L.conv_base[i])) return DFLASH_ERR_ALIGN;
     }
+    if (!a16(L.mlp_norm)) return DFLASH_ERR_ALIGN;
   }
   if (draft) {
     if (!w->embed || !w->lm_head || !w->final_norm) return DFLASH_ERR_NULL;
-    if (!a16(w->lm_head) || !a16(w->embed)) return DFLASH_ERR_ALIGN;
+    if (!a16(w->lm_head) || !a16(w->embed) || !a16(w->final_norm)) return DFLASH_ERR_ALIGN;
     for (int l = 0; l < c->n_layers; ++l)
       if (!a16(w->layer[l].attn_norm)) return DFLASH_ERR_ALIGN;
   }
@@ -122,28 +123,30 @@ static int check_kv(const dflash_config *c, const dflash_kv *kv) {
 // ---------------------------------------------------------------------------
 // workspace layout
 // ---------------------------------------------------------------------------
+constexpr int kMaxReduceSplits = 16;      // slices a reduce-mode GEMM may use
+constexpr size_t kTicketInts = 1 << 14;   // tile tickets of one reduce-mode GEMM
+
 struct Layout {
-  size_t status, x, un, ub, rf, rb, qb, kb, vb, ob, hb, zf, logits, part, gpart, attn, topk;
-  size_t selrows, upart, vpart, argmax, gn, cb, ipart, kvpart;
+  size_t status, tickets, scratch;
+  size_t x, un, ub, rf, rb, gates, qkv, qb, kb, vb, ob, hb, zf, logits, attn, topk;
+  size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf;
   size_t total;
-  int S_gate, S_qkv, S_o, S_gu, S_down, S_sel;
+  int S_gate, S_qkv, S_o, S_gu, S_down, S_sel, S_lm;
   AttnPlan ap;
 };
 
-static size_t max_partial(int N_out, int K_in, int Nmax, int sms) {
-  // the split count depends on the token count; take the largest buffer over
-  // token counts at the token-tile boundaries up to Nmax
-  size_t best = 0;
-  auto eval = [&](int n) {
-    if (n < 1 || n > Nmax) return;
-    size_t v = (size_t)gemm_splits(N_out, n, K_in, sms) * n * N_out;
-    if (v > best) best = v;
-  };
-  for (int n = 16; n <= 256; n *= 2) eval(n);
-  for (int n = 512; n <= Nmax; n += 256) eval(n);
-  for (int n = 1; n <= 16; ++n) eval(n);
-  eval(Nmax);
-  return best;
+// K slices of a reduce-mode GEMM: the cost model's choice, capped so the slice
+// scratch and the tile tickets stay bounded; float32 storage uses one slice.
+static int reduce_splits(const dflash_config *c, int N_out, int T, int K_in, int mode, int sms) {
+  if (c->dtype == DFLASH_F32) return 1;
+  int S = gemm_splits(mode == GEMM_SWIGLU ? 2 * N_out : N_out, T, K_in, sms, kMaxReduceSplits);
+  if (gemm_tiles(N_out, T, mode) > kTicketInts) S = 1;
+  return S;
+}
+static size_t reduce_scratch(const dflash_config *c, int N_out, int T, int S, int mode) {
+  if (c->dtype == DFLASH_F32)
+    return (size_t)S * T * (mode == GEMM_SWIGLU ? 2 * N_out : N_out);
+  return gemm_scratch_floats(N_out, T, S, mode);
 }
 
 static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *L) {
@@ -155,25 +158,56 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   const int QKVW = (Hq + 2 * Hkv) * dh;
   const int TIN = c->n_taps * c->d_target;
   const int T = B * K, TL = B * (K - 1), R = 1 + (K - 1) * k, TR = B * R;
+  const int N = Nmax > 0 ? Nmax : 1;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
     off += (bytes + 255) & ~(size_t)255;
     return o;
   };
-  L->status = take(256);
-  L->S_gate = gemm_splits(GW, T, D, sms);
-  L->S_qkv = gemm_splits(QKVW, T, D, sms);
-  L->S_o = gemm_splits(D, T, Hq * dh, sms);
-  L->S_gu = gemm_splits(2 * F, T, D, sms);
-  L->S_down = gemm_splits(D, T, F, sms);
-  L->S_sel = gemm_splits(r, TR, D, sms);
+  L->S_gate = reduce_splits(c, GW, T, D, GEMM_REDUCE, sms);
+  L->S_qkv = reduce_splits(c, QKVW, T, D, GEMM_REDUCE, sms);
+  L->S_o = reduce_splits(c, D, T, Hq * dh, GEMM_REDUCE, sms);
+  L->S_gu = reduce_splits(c, F, T, D, GEMM_SWIGLU, sms);
+  L->S_down = reduce_splits(c, D, T, F, GEMM_REDUCE, sms);
+  L->S_sel = reduce_splits(c, r, TR, D, GEMM_REDUCE, sms);
+  L->S_lm = 1;
   L->ap = attn_plan(B, K, Hq, Hkv, dh, c->window, sms);
+  // slice scratch shared by every reduce-mode GEMM (they run one after another)
+  size_t sc = 0;
+  sc = std::max(sc, reduce_scratch(c, GW, T, L->S_gate, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, QKVW, T, L->S_qkv, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, D, T, L->S_o, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, F, T, L->S_gu, GEMM_SWIGLU));
+  sc = std::max(sc, reduce_scratch(c, D, T, L->S_down, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, r, TR, L->S_sel, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, V, TL, 1, GEMM_REDUCE));
+  // injection GEMMs: the split depends on the token count; take the largest
+  auto inj = [&](int n_out, int k_in) {
+    size_t best = 0;
+    auto eval = [&](int n) {
+      if (n < 1 || n > N) return;
+      const int S = reduce_splits(c, n_out, n, k_in, GEMM_REDUCE, sms);
+      best = std::max(best, reduce_scratch(c, n_out, n, S, GEMM_REDUCE));
+    };
+    for (int n = 1; n <= 16; ++n) eval(n);
+    for (int n = 32; n <= 256; n *= 2) eval(n);
+    for (int n = 512; n <= N; n += 256) eval(n);
+    eval(N);
+    return best;
+  };
+  sc = std::max(sc, inj(D, TIN));
+  sc = std::max(sc, inj(2 * Hkv * dh, D));
+  L->status = take(256);
+  L->tickets = take(kTicketInts * sizeof(int));
+  L->scratch = take(sc * 4);
   L->x = take((size_t)T * D * 4);
   L->un = take((size_t)T * D * es);
   L->ub = take((size_t)T * D * es);
   L->rf = take((size_t)T * D * 4);
   L->rb = take((size_t)T * D * es);
+  L->gates = take((size_t)T * GW * 4);
+  L->qkv = take((size_t)T * QKVW * 4);
   L->qb = take((size_t)T * Hq * dh * es);
   L->kb = take((size_t)T * Hkv * dh * es);
   L->vb = take((size_t)T * Hkv * dh * es);
@@ -181,24 +215,16 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->hb = take((size_t)T * F * es);
   L->zf = take((size_t)TL * D * es);
   L->logits = take((size_t)TL * V * 4);
-  size_t pf = 0;
-  pf = std::max(pf, (size_t)L->S_qkv * T * QKVW);
-  pf = std::max(pf, (size_t)L->S_o * T * D);
-  pf = std::max(pf, (size_t)L->S_gu * T * 2 * F);
-  pf = std::max(pf, (size_t)L->S_down * T * D);
-  L->part = take(pf * 4);
-  L->gpart = take((size_t)L->S_gate * T * GW * 4);
   L->attn = take(L->ap.part_floats * 4);
   L->topk = take((size_t)TL * topk_chunks(V) * (2 * k + 2) * 4);
   L->selrows = take((size_t)TR * D * es);
-  L->upart = take((size_t)L->S_sel * TR * r * 4);
-  L->vpart = take((size_t)L->S_sel * TR * r * 4);
+  L->U = take((size_t)TR * r * 4);
+  L->Vp = take((size_t)TR * r * 4);
+  L->pairs = take((size_t)B * (K - 1) * k * k * 4);
   L->argmax = take((size_t)T * argmax_chunks(V) * 2 * 4);
-  const int N = Nmax > 0 ? Nmax : 1;
   L->gn = take((size_t)N * TIN * es);
   L->cb = take((size_t)N * D * es);
-  L->ipart = take(max_partial(D, TIN, N, sms) * 4);
-  L->kvpart = take(max_partial(2 * Hkv * dh, D, N, sms) * (size_t)c->n_layers * 4);
+  L->kvf = take((size_t)N * 2 * Hkv * dh * c->n_layers * 4);
   L->total = off;
   return true;
 }
@@ -212,6 +238,29 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
     if (rc_ != DFLASH_OK) return rc_;    \
   } while (0)
 
+// One reduce-mode GEMM on the shared scratch and tickets of the workspace.
+static GemmCall reduce_call(const dflash_config &c, uint8_t *ws, const Layout &L, const void *W,
+                            int N_out, int K_in, const void *X, int T, int S, int mode,
+                            float *out_f32, int ld, void *out_s, int ldb) {
+  GemmCall g;
+  g.dtype = c.dtype;
+  g.W = W;
+  g.N_out = N_out;
+  g.K_in = K_in;
+  g.X = X;
+  g.T = T;
+  g.S = S;
+  g.mode = mode;
+  g.out = (float *)(ws + L.scratch);
+  g.out_f32 = out_f32;
+  g.ld = ld;
+  g.out_bf16 = out_s;
+  g.ldb = ldb;
+  g.counters = (int *)(ws + L.tickets);
+  g.err = (int *)(ws + L.status);
+  return g;
+}
+
 template <typename S>
 static int run_inject(const dflash_config &c, const dflash_weights &w, const dflash_kv &kv,
                       const void *hidden, const int32_t *req, const int32_t *pos, int N,
@@ -222,23 +271,23 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
   int *err = (int *)(ws + L.status);
   S *gn = (S *)(ws + L.gn);
   S *cb = (S *)(ws + L.cb);
-  float *ipart = (float *)(ws + L.ipart);
-  float *kvpart = (float *)(ws + L.kvpart);
+  float *kvf = (float *)(ws + L.kvf);
   TRY(launch_rows_norm<S>((const S *)hidden, N, TIN, (const S *)w.fc_norm, c.rms_eps, gn, st));
-  const int S_fc = gemm_splits(D, N, TIN, sms);
-  TRY(gemm_xwT(c.dtype, w.fc, D, TIN, gn, N, ipart, D, S_fc, err, st));
-  TRY(launch_reduce<S>(ipart, S_fc, N, D, nullptr, cb, st));
-  const int S_kv = gemm_splits(W2, N, D, sms);
+  const int S_fc = reduce_splits(&c, D, N, TIN, GEMM_REDUCE, sms);
+  TRY(gemm_run(reduce_call(c, ws, L, w.fc, D, TIN, gn, N, S_fc, GEMM_REDUCE, nullptr, D, cb, D),
+               st));
+  const int S_kv = reduce_splits(&c, W2, N, D, GEMM_REDUCE, sms);
   LayerPtrs kn;
   memset(&kn, 0, sizeof(kn));
   for (int l = 0; l < c.n_layers; ++l) {
     const S *wkv = (const S *)w.layer[l].wqkv + (size_t)Hq * dh * D;  // [Wk; Wv] rows
-    TRY(gemm_xwT(c.dtype, wkv, W2, D, cb, N, kvpart + (size_t)l * S_kv * N * W2, W2, S_kv, err,
+    TRY(gemm_run(reduce_call(c, ws, L, wkv, W2, D, cb, N, S_kv, GEMM_REDUCE,
+                             kvf + (size_t)l * N * W2, W2, nullptr, 0),
                  st));
     kn.p[l] = w.layer[l].k_norm;
   }
   const RopeTable rope = rope_table(c.rope_theta, dh);
-  TRY(launch_inject_store<S>(kvpart, S_kv, N, c.n_layers, Hkv, dh, kn, req, pos, kv.page_table,
+  TRY(launch_inject_store<S>(kvf, N, c.n_layers, Hkv, dh, kn, req, pos, kv.page_table,
                              kv.num_rows, kv.max_pages_per_req, kv.num_pages, c.page_size, rope,
                              c.rms_eps, (S *)kv.k, (S *)kv.v, err, st));
   return DFLASH_OK;
@@ -252,18 +301,21 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   const int D = c.d_model, F = c.d_ff, V = c.vocab, dh = c.head_dim;
   const int Hq = c.n_q_heads, Hkv = c.n_kv_heads, g = c.conv_group;
   const int GW = 2 * D / g, QKVW = (Hq + 2 * Hkv) * dh;
-  const int T = B * K, dt = c.dtype;
+  const int T = B * K;
   const float eps = c.rms_eps;
   int *err = (int *)(ws + L.status);
-  float *x = (float *)(ws + L.x);
+  float *x = (float *)(ws + L.x), *rf = (float *)(ws + L.rf);
+  float *gates = (float *)(ws + L.gates), *qkv = (float *)(ws + L.qkv);
   S *un = (S *)(ws + L.un), *ub = (S *)(ws + L.ub), *rb = (S *)(ws + L.rb);
-  float *rf = (float *)(ws + L.rf);
   S *qb = (S *)(ws + L.qb), *kb = (S *)(ws + L.kb), *vb = (S *)(ws + L.vb);
   S *ob = (S *)(ws + L.ob), *hb = (S *)(ws + L.hb), *zf = (S *)(ws + L.zf);
   float *logits = logits_opt ? logits_opt : (float *)(ws + L.logits);
-  float *part = (float *)(ws + L.part), *gpart = (float *)(ws + L.gpart);
   float *attnp = (float *)(ws + L.attn), *topkp = (float *)(ws + L.topk);
   const RopeTable rope = rope_table(c.rope_theta, dh);
+  auto gate_gemm = [&](const void *Wg, const S *X) {
+    return gemm_run(
+        reduce_call(c, ws, L, Wg, GW, D, X, T, L.S_gate, GEMM_REDUCE, gates, GW, nullptr, 0), st);
+  };
 
   TRY(launch_embed_norm<S>((const S *)w.embed, anchor, c.mask_token_id, V, B, K, D,
                            (const S *)w.layer[0].attn_norm, eps, x, un, err, st));
@@ -271,34 +323,38 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     const dflash_layer_weights &lw = w.layer[l];
     const bool last = l + 1 == c.n_layers;
     // attention sublayer: conv -> QKV -> norm/RoPE -> block attention -> O -> conv, residual
-    TRY(gemm_xwT(dt, lw.conv_w[0], GW, D, un, T, gpart, GW, L.S_gate, err, st));
-    TRY(launch_conv_pre<S>(un, gpart, L.S_gate, T, K, D, g, (const S *)lw.conv_base[0], ub, st));
-    TRY(gemm_xwT(dt, lw.wqkv, QKVW, D, ub, T, part, QKVW, L.S_qkv, err, st));
-    TRY(launch_qkv_post<S>(part, L.S_qkv, T, K, Hq, Hkv, dh, (const S *)lw.q_norm,
-                           (const S *)lw.k_norm, ctx_len, rope, eps, qb, kb, vb, st));
+    TRY(gate_gemm(lw.conv_w[0], un));
+    TRY(launch_conv_pre<S>(un, gates, T, K, D, g, (const S *)lw.conv_base[0], ub, st));
+    TRY(gemm_run(reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.S_qkv, GEMM_REDUCE, qkv, QKVW,
+                             nullptr, 0),
+                 st));
+    TRY(launch_qkv_post<S>(qkv, T, K, Hq, Hkv, dh, (const S *)lw.q_norm, (const S *)lw.k_norm,
+                           ctx_len, rope, eps, qb, kb, vb, st));
     TRY(launch_block_attention<S>(L.ap, qb, kb, vb, (const S *)kv.k, (const S *)kv.v, l,
                                   kv.page_table, kv.max_pages_per_req, kv.num_pages, c.page_size,
                                   ctx_len, B, K, Hq, Hkv, dh, c.window, attnp, ob, err, st));
-    TRY(gemm_xwT(dt, lw.wo, D, Hq * dh, ob, T, part, D, L.S_o, err, st));
-    TRY(launch_reduce<S>(part, L.S_o, T, D, rf, rb, st));
-    TRY(gemm_xwT(dt, lw.conv_w[1], GW, D, rb, T, gpart, GW, L.S_gate, err, st));
-    TRY(launch_conv_post_norm<S>(rf, gpart, L.S_gate, T, K, D, g, (const S *)lw.conv_base[1], x,
+    TRY(gemm_run(reduce_call(c, ws, L, lw.wo, D, Hq * dh, ob, T, L.S_o, GEMM_REDUCE, rf, D, rb, D),
+                 st));
+    TRY(gate_gemm(lw.conv_w[1], rb));
+    TRY(launch_conv_post_norm<S>(rf, gates, T, K, D, g, (const S *)lw.conv_base[1], x,
                                  (const S *)lw.mlp_norm, eps, un, (S *)nullptr, st));
-    // MLP sublayer: conv -> gate/up -> SwiGLU -> down -> conv, residual
-    TRY(gemm_xwT(dt, lw.conv_w[2], GW, D, un, T, gpart, GW, L.S_gate, err, st));
-    TRY(launch_conv_pre<S>(un, gpart, L.S_gate, T, K, D, g, (const S *)lw.conv_base[2], ub, st));
-    TRY(gemm_xwT(dt, lw.w_gate_up, 2 * F, D, ub, T, part, 2 * F, L.S_gu, err, st));
-    TRY(launch_swiglu<S>(part, L.S_gu, T, F, hb, st));
-    TRY(gemm_xwT(dt, lw.w_down, D, F, hb, T, part, D, L.S_down, err, st));
-    TRY(launch_reduce<S>(part, L.S_down, T, D, rf, rb, st));
-    TRY(gemm_xwT(dt, lw.conv_w[3], GW, D, rb, T, gpart, GW, L.S_gate, err, st));
+    // MLP sublayer: conv -> gate/up + SwiGLU -> down -> conv, residual
+    TRY(gate_gemm(lw.conv_w[2], un));
+    TRY(launch_conv_pre<S>(un, gates, T, K, D, g, (const S *)lw.conv_base[2], ub, st));
+    TRY(gemm_run(reduce_call(c, ws, L, lw.w_gate_up, F, D, ub, T, L.S_gu, GEMM_SWIGLU, nullptr, 0,
+                             hb, F),
+                 st));
+    TRY(gemm_run(reduce_call(c, ws, L, lw.w_down, D, F, hb, T, L.S_down, GEMM_REDUCE, rf, D, rb, D),
+                 st));
+    TRY(gate_gemm(lw.conv_w[3], rb));
     TRY(launch_conv_post_norm<S>(
-        rf, gpart, L.S_gate, T, K, D, g, (const S *)lw.conv_base[3], x,
+        rf, gates, T, K, D, g, (const S *)lw.conv_base[3], x,
         (const S *)(last ? w.final_norm : w.layer[l + 1].attn_norm), eps, un, last ? zf : (S *)nullptr,
         st));
   }
   const int TL = B * (K - 1);
-  TRY(gemm_xwT(dt, w.lm_head, V, D, zf, TL, logits, V, 1, err, st));
+  TRY(gemm_run(reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, 1, GEMM_REDUCE, logits, V, nullptr, 0),
+               st));
   TRY(launch_topk(logits, TL, V, c.top_k, topkp, ids, logp, st));
   return DFLASH_OK;
 }
@@ -311,19 +367,14 @@ static int run_select(const dflash_config &c, const dflash_weights &w, const int
   const int TR = B * (1 + (K - 1) * k);
   int *err = (int *)(ws + L.status);
   S *rows = (S *)(ws + L.selrows);
-  float *up = (float *)(ws + L.upart), *vp = (float *)(ws + L.vpart);
+  float *U = (float *)(ws + L.U), *Vp = (float *)(ws + L.Vp);
   TRY(launch_sel_gather<S>((const S *)w.embed, anchor, ids, B, K, k, c.vocab, D, rows, err, st));
-  TRY(gemm_xwT(c.dtype, w.sel_pu, r, D, rows, TR, up, r, L.S_sel, err, st));
-  TRY(gemm_xwT(c.dtype, w.sel_pv, r, D, rows, TR, vp, r, L.S_sel, err, st));
-  int ns = L.S_sel;
-  if (ns > 1) {
-    // sum the K slices in place (slice 0 receives the sum) with many CTAs, so the
-    // one-CTA-per-request Viterbi kernel reads each projection once
-    TRY(launch_reduce<S>(up, ns, TR, r, up, (S *)nullptr, st));
-    TRY(launch_reduce<S>(vp, ns, TR, r, vp, (S *)nullptr, st));
-    ns = 1;
-  }
-  TRY(launch_viterbi(up, vp, ns, ns, ids, logp, B, K, k, r, path, score, st));
+  TRY(gemm_run(reduce_call(c, ws, L, w.sel_pu, r, D, rows, TR, L.S_sel, GEMM_REDUCE, U, r, nullptr, 0),
+               st));
+  TRY(gemm_run(reduce_call(c, ws, L, w.sel_pv, r, D, rows, TR, L.S_sel, GEMM_REDUCE, Vp, r, nullptr,
+                           0),
+               st));
+  TRY(launch_viterbi(U, Vp, ids, logp, B, K, k, r, (float *)(ws + L.pairs), path, score, st));
   return DFLASH_OK;
 }
 

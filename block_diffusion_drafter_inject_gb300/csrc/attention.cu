@@ -417,8 +417,10 @@ __global__ void k_attn_combine(const float *__restrict__ part, const int32_t *__
   const int ns = (n_ctx + K + kps - 1) / kps;
   const size_t base0 = (((size_t)b * nqg + qgi) * Hkv + kvh) * nsplit;
   float M = -INFINITY;
+#pragma unroll 4
   for (int s = 0; s < ns; ++s) M = fmaxf(M, part[((base0 + s) * kQG + row) * (dh + 2)]);
   float L = 0.f, O = 0.f;
+#pragma unroll 4
   for (int s = 0; s < ns; ++s) {
     const float *po = part + ((base0 + s) * kQG + row) * (dh + 2);
     const float w = po[0] == -INFINITY ? 0.f : expf(po[0] - M);

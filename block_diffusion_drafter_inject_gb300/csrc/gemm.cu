@@ -13,7 +13,15 @@
 // across units without draining.  Weight tiles are loaded with an evict-first
 // L2 hint (each is read once per pass); activation tiles with evict-last.
 //
+// Split-K reduction happens inside the kernel: each unit of a split tile writes
+// its slice to scratch, then takes a ticket on the tile (one atomic, no
+// waiting); the CTA that takes the last ticket sums the S slices in slice
+// order (so the result does not depend on timing), resets the ticket and runs
+// the fused epilogue: fp32 and/or storage-dtype output, or SwiGLU, where each
+// weight tile holds 64 gate rows and the matching 64 up rows.
+//
 // fp32 path (the float32 configuration): a shared-memory tiled CUDA-core GEMM.
+#include <algorithm>
 #include <mutex>
 #include <unordered_map>
 
@@ -26,13 +34,21 @@ constexpr int BK = 64;
 constexpr int kGemmThreads = 192;
 
 struct GemmParams {
-  float *out;
+  float *out;  // GEMM_PARTIAL output / slice scratch
   int ld;
   int N_out, T;
   int kb_per_split;
   int S, m_tiles, t_tiles, num_units;
+  int mode;
+  float *out_f32;
+  bf16 *out_bf16;
+  int ldb;
+  int F;  // GEMM_SWIGLU: gate rows before the up rows
+  int *counters;
   int *err;
 };
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 template <int BN>
 struct GemmShape {
@@ -51,6 +67,56 @@ __device__ __forceinline__ void unit_coords(int u, const GemmParams &p, int &m_t
   int r = u / p.m_tiles;
   split = r % p.S;
   t_tile = r / p.S;
+}
+
+// Weight tile of unit m_tile: 128 consecutive rows, or for GEMM_SWIGLU the 64
+// gate rows [64m, 64m+64) followed by the 64 up rows [F+64m, F+64m+64).
+__device__ __forceinline__ void load_w(uint8_t *dst, const CUtensorMap *m, uint64_t *bar, int kx,
+                                       int m_tile, const GemmParams &p, uint64_t pol) {
+  if (p.mode == 2) {
+    tma_load_2d(dst, m, bar, kx, m_tile * 64, pol);
+    tma_load_2d(dst + 64 * BK * 2, m, bar, kx, p.F + m_tile * 64, pol);
+  } else {
+    tma_load_2d(dst, m, bar, kx, m_tile * BM, pol);
+  }
+}
+
+// Final values v[16] of row `row` (0..127) of tile m_tile, columns c0..c0+15.
+// All four epilogue warps call this in step (SwiGLU exchanges through xbuf).
+__device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int row, int c0,
+                                          const float *v, float *xbuf) {
+  if (p.mode == 1) {
+    const int n = m_tile * BM + row;
+    if (n < p.N_out) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int t = c0 + j;
+        if (t < p.T) {
+          if (p.out_f32) p.out_f32[(size_t)t * p.ld + n] = v[j];
+          if (p.out_bf16) p.out_bf16[(size_t)t * p.ldb + n] = __float2bfloat16_rn(v[j]);
+        }
+      }
+    }
+  } else {
+    // rows 64..127 hold the up projections of the features of rows 0..63
+    if (row >= 64) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) xbuf[(row - 64) * 17 + j] = v[j];
+    }
+    epi_bar();
+    if (row < 64) {
+      const int f = m_tile * 64 + row;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int t = c0 + j;
+        if (t < p.T) {
+          const float g = v[j], u = xbuf[row * 17 + j];
+          p.out_bf16[(size_t)t * p.ldb + f] = __float2bfloat16_rn(g / (1.f + expf(-g)) * u);
+        }
+      }
+    }
+    epi_bar();
+  }
 }
 
 template <int BN>
@@ -117,8 +183,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           unit_coords(u, p, m_tile, t_tile, split);
           for (int kb = 0; kb < p.kb_per_split && cnt < STAGES; ++kb, ++cnt) {
             mbar_expect_tx(&full[cnt], SH::STAGE_BYTES);
-            tma_load_2d(smem + cnt * SH::STAGE_BYTES, &tmW, &full[cnt],
-                        (split * p.kb_per_split + kb) * BK, m_tile * BM, pol_w);
+            load_w(smem + cnt * SH::STAGE_BYTES, &tmW, &full[cnt],
+                   (split * p.kb_per_split + kb) * BK, m_tile, p, pol_w);
           }
         }
         pre = cnt;
@@ -140,7 +206,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               break;
             }
             mbar_expect_tx(&full[stage], SH::STAGE_BYTES);
-            tma_load_2d(sa, &tmW, &full[stage], kx, m_tile * BM, pol_w);
+            load_w(sa, &tmW, &full[stage], kx, m_tile, p, pol_w);
             tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, t_tile * BN, pol_x);
           }
           issued[stage] = true;
@@ -204,7 +270,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ---------------- epilogue: warps 2..5 ----------------
     pdl_wait();
+    __shared__ float xbuf[64 * 17];
+    __shared__ int s_last;
     const int quarter = warp & 3;  // tensor-memory lanes this warp may read
+    const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
@@ -212,19 +281,75 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       unit_coords(u, p, m_tile, t_tile, split);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
       tc_fence_after();
-      const int n = m_tile * BM + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      float *outp = p.out + (size_t)split * p.T * p.ld + n;
+      const int tcol0 = t_tile * BN;
+      if (p.mode == 0) {
+        const int n = m_tile * BM + row;
+        float *outp = p.out + (size_t)split * p.T * p.ld + n;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 16) {
-        float v[16];
-        tc_ld16(taddr + c, v);
-        const int t0 = t_tile * BN + c;
-        if (n < p.N_out) {
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tc_ld16(taddr + c, v);
+          const int t0 = tcol0 + c;
+          if (n < p.N_out) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (t0 + j < p.T) outp[(size_t)(t0 + j) * p.ld] = v[j];
+            for (int j = 0; j < 16; ++j)
+              if (t0 + j < p.T) outp[(size_t)(t0 + j) * p.ld] = v[j];
+          }
         }
+      } else if (p.S == 1) {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          if (tcol0 + c >= p.T) break;  // uniform across the epilogue warps
+          float v[16];
+          tc_ld16(taddr + c, v);
+          epi_store(p, m_tile, row, tcol0 + c, v, xbuf);
+        }
+      } else {
+        // slice -> scratch (tile-contiguous, [column][row]), then a ticket
+        const size_t tile = (size_t)t_tile * p.m_tiles + m_tile;
+        const size_t tile_sz = (size_t)BM * BN;
+        const size_t slice_stride = (size_t)p.t_tiles * p.m_tiles * tile_sz;
+        float *mine = p.out + (size_t)split * slice_stride + tile * tile_sz + row;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          if (tcol0 + c >= p.T) break;
+          float v[16];
+          tc_ld16(taddr + c, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) mine[(size_t)(c + j) * BM] = v[j];
+        }
+        // the accumulator can go back to the MMA warp now
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        __threadfence();
+        epi_bar();
+        if (threadIdx.x == 64) {
+          const int old = atomicAdd(&p.counters[tile], 1);
+          s_last = old == p.S - 1;
+          if (s_last) p.counters[tile] = 0;
+        }
+        epi_bar();
+        if (s_last) {
+          __threadfence();
+          const float *base = p.out + tile * tile_sz + row;
+#pragma unroll 1
+          for (int c = 0; c < BN; c += 16) {
+            if (tcol0 + c >= p.T) break;
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            for (int q = 0; q < p.S; ++q) {
+              const float *src = base + (size_t)q * slice_stride + (size_t)c * BM;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (size_t)j * BM);
+            }
+            epi_store(p, m_tile, row, tcol0 + c, v, xbuf);
+          }
+        }
+        if (++acc == 2) acc = 0, acc_phase ^= 1;
+        continue;
       }
       tc_fence_before();
       __syncwarp();
@@ -284,6 +409,35 @@ __global__ void __launch_bounds__(256) k_gemm_f32(const float *__restrict__ W,
       int n = n0 + tn * 4 + i, t = t0 + tt * 2 + j;
       if (n < N && t < T) out[((size_t)s * T + t) * ld + n] = acc[i][j];
     }
+}
+
+// fp32 configuration: reduce the slices of k_gemm_f32 and apply the epilogue.
+// part: [S][T][ld_part]; mode 1 -> out_f32 / out (float storage); mode 2 -> SwiGLU.
+__global__ void __launch_bounds__(256) k_gemm_f32_finish(const float *__restrict__ part, int S,
+                                                         int T, int N_out, int ld_part, int mode,
+                                                         int F, float *__restrict__ out_f32,
+                                                         int ld, float *__restrict__ out_s,
+                                                         int ldb) {
+  pdl_launch();
+  pdl_wait();
+  const size_t n = (size_t)T * N_out;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / N_out), c = (int)(i % N_out);
+    if (mode == 1) {
+      float v = 0.f;
+      for (int k = 0; k < S; ++k) v += part[((size_t)k * T + t) * ld_part + c];
+      if (out_f32) out_f32[(size_t)t * ld + c] = v;
+      if (out_s) out_s[(size_t)t * ldb + c] = v;
+    } else {
+      float g = 0.f, u = 0.f;
+      for (int k = 0; k < S; ++k) {
+        g += part[((size_t)k * T + t) * ld_part + c];
+        u += part[((size_t)k * T + t) * ld_part + F + c];
+      }
+      out_s[(size_t)t * ldb + c] = g / (1.f + expf(-g)) * u;
+    }
+  }
 }
 
 }  // namespace dfl
@@ -362,39 +516,57 @@ static bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t 
 
 static int token_tile(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
 
-int gemm_splits(int N_out, int T, int K_in, int num_sms) {
-  // Pick the K split that best fills whole waves of one CTA per SM, among
-  // splits that keep >= 2 k-blocks per unit and the partial buffer under its
-  // cap; prefer fewer splits when the fill is about equal.
+// Cost model (microseconds) of one launch split S ways, fitted to sweeps on
+// GB300: one CTA streams about 60 GB/s from memory, the GPU about 6.5 TB/s,
+// and a CTA's tensor pipe does about 11 TFLOP/s.  Each wave of units costs the
+// slower of one unit's own time and the wave's share of memory bandwidth;
+// split slices add their write + read traffic.
+static double gemm_cost(int N_out, int T, int K_in, int S, int num_sms) {
   const int kb = K_in / dfl::BK;
-  const int m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
   const int bn = token_tile(T);
   const int t_tiles = (T + bn - 1) / bn;
-  const long base = (long)m_tiles * t_tiles;
+  const int m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
+  const double kbps = kb / S;
+  const double uA = 128.0 * 64 * 2 * kbps, uB = (double)bn * 64 * 2 * kbps;
+  const double t_unit = std::max((uA + uB) / 60e3, 2.0 * 128 * bn * 64 * kbps / 11e6) + 0.15;
+  const long U = (long)m_tiles * t_tiles * S;
+  double tot = 0.0;
+  for (long w = 0; w * num_sms < U; ++w) {
+    const long n = std::min<long>(num_sms, U - w * num_sms);
+    tot += std::max(t_unit, n * uA / 6.5e6);
+  }
+  if (S > 1) tot += (double)S * T * N_out * 8.0 / 8e6;
+  return tot;
+}
+
+int gemm_splits(int N_out, int T, int K_in, int num_sms, int max_S) {
+  const int kb = K_in / dfl::BK;
   int best = 1;
-  double best_score = -1.0;
-  for (int S = 1; S <= kb; ++S) {
+  double best_cost = 1e300;
+  for (int S = 1; S <= kb && S <= max_S; ++S) {
     if (kb % S) continue;
-    if (S > 1 && (size_t)S * T * N_out > kMaxPartialFloats) break;
     if (S > 1 && kb / S < 2) break;
-    const long units = base * S;
-    const long waves = (units + num_sms - 1) / num_sms;
-    const double fill = (double)units / (double)(waves * num_sms);
-    // partial slices: written once and read once by the consumer, relative to
-    // the weight bytes; mostly L2 traffic while the slices stay small
-    const double part_bytes = 8.0 * S * T * (double)N_out;
-    const double alpha = part_bytes <= 32e6 ? 0.25 : 1.0;
-    const double extra = S > 1 ? alpha * part_bytes / (2.0 * N_out * (double)K_in) : 0.0;
-    const double score = fill / (1.0 + extra) - 0.002 * S / kb;
-    if (score > best_score + 1e-9) best_score = score, best = S;
-    if (units >= 8L * num_sms) break;  // many waves: fill no longer matters
+    if (S > 1 && (size_t)S * T * N_out > kMaxPartialFloats) break;
+    const double c = gemm_cost(N_out, T, K_in, S, num_sms);
+    if (c < best_cost * 0.985) best_cost = c, best = S;
   }
   return best;
 }
 
+size_t gemm_tiles(int N_out, int T, int mode) {
+  const int bn = token_tile(T);
+  const int rows = mode == GEMM_SWIGLU ? 64 : dfl::BM;
+  return (size_t)((N_out + rows - 1) / rows) * ((T + bn - 1) / bn);
+}
+
+size_t gemm_scratch_floats(int N_out, int T, int S, int mode) {
+  if (mode == GEMM_PARTIAL) return (size_t)S * T * N_out;
+  if (S <= 1) return 0;
+  return (size_t)S * gemm_tiles(N_out, T, mode) * dfl::BM * token_tile(T);
+}
+
 template <int BN>
-static int launch_tc(const void *W, int N_out, int K_in, const void *X, int T, float *out, int ld,
-                     int S, int *err, cudaStream_t st, const Dev *d) {
+static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
   using SH = dfl::GemmShape<BN>;
   static int attr_set_dev[64] = {0};
   if (d->id < 64 && !attr_set_dev[d->id]) {
@@ -403,46 +575,84 @@ static int launch_tc(const void *W, int N_out, int K_in, const void *X, int T, f
       return DFLASH_ERR_CUDA;
     attr_set_dev[d->id] = 1;
   }
+  const bool swiglu = g.mode == GEMM_SWIGLU;
+  const int w_rows = swiglu ? 2 * g.N_out : g.N_out;
   CUtensorMap mw, mx;
-  if (!bf16_map(&mw, W, (uint64_t)N_out, (uint64_t)K_in, dfl::BM, d->id)) return DFLASH_ERR_CUDA;
-  if (!bf16_map(&mx, X, (uint64_t)T, (uint64_t)K_in, BN, d->id)) return DFLASH_ERR_CUDA;
+  if (!bf16_map(&mw, g.W, (uint64_t)w_rows, (uint64_t)g.K_in, swiglu ? 64 : dfl::BM, d->id))
+    return DFLASH_ERR_CUDA;
+  if (!bf16_map(&mx, g.X, (uint64_t)g.T, (uint64_t)g.K_in, BN, d->id)) return DFLASH_ERR_CUDA;
   dfl::GemmParams p;
-  p.out = out;
-  p.ld = ld;
-  p.N_out = N_out;
-  p.T = T;
-  p.S = S;
-  p.kb_per_split = K_in / dfl::BK / S;
-  p.m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
-  p.t_tiles = (T + BN - 1) / BN;
-  p.num_units = p.m_tiles * p.t_tiles * S;
-  p.err = err;
+  p.out = g.out;
+  p.ld = g.ld;
+  p.N_out = g.N_out;
+  p.T = g.T;
+  p.S = g.S;
+  p.kb_per_split = g.K_in / dfl::BK / g.S;
+  p.m_tiles = swiglu ? g.N_out / 64 : (g.N_out + dfl::BM - 1) / dfl::BM;
+  p.t_tiles = (g.T + BN - 1) / BN;
+  p.num_units = p.m_tiles * p.t_tiles * g.S;
+  p.mode = g.mode;
+  p.out_f32 = g.out_f32;
+  p.out_bf16 = (dfl::bf16 *)g.out_bf16;
+  p.ldb = g.ldb;
+  p.F = swiglu ? g.N_out : 0;
+  p.counters = g.counters;
+  p.err = g.err;
   const int grid = p.num_units < d->num_sms ? p.num_units : d->num_sms;
   DFL_CHECK_LAUNCH(launch(dfl::k_gemm_tc<BN>, dim3(grid), dim3(dfl::kGemmThreads),
                           (size_t)SH::SMEM_BYTES, st, mw, mx, p));
   return DFLASH_OK;
 }
 
-int gemm_xwT(int dtype, const void *W, int N_out, int K_in, const void *X, int T, float *out,
-             int ld, int S, int *err, cudaStream_t st) {
-  if (T <= 0 || N_out <= 0) return DFLASH_OK;
+int gemm_run(const GemmCall &g, cudaStream_t st) {
+  if (g.T <= 0 || g.N_out <= 0) return DFLASH_OK;
   const Dev *d = device();
   if (!d) return DFLASH_ERR_DEVICE;
-  if (K_in % 64 || S < 1 || (K_in / 64) % S) return DFLASH_ERR_DIMS;
-  if (dtype == DFLASH_F32) {
-    dim3 grid((N_out + 63) / 64, (T + 31) / 32, S);
-    DFL_CHECK_LAUNCH(launch(dfl::k_gemm_f32, grid, dim3(256), 0, st, (const float *)W,
-                            (const float *)X, out, ld, N_out, T, K_in, K_in / S));
+  if (g.K_in % 64 || g.S < 1 || (g.K_in / 64) % g.S) return DFLASH_ERR_DIMS;
+  if (g.mode == GEMM_SWIGLU && g.N_out % 64) return DFLASH_ERR_DIMS;
+  if (g.mode != GEMM_PARTIAL && g.S > 1 && (!g.counters || !g.out)) return DFLASH_ERR_NULL;
+  if (g.dtype == DFLASH_F32) {
+    // CUDA-core path: slices to scratch (or the output itself), then the epilogue
+    const int n_rows = g.mode == GEMM_SWIGLU ? 2 * g.N_out : g.N_out;
+    float *part = g.out;
+    const int ldp = g.mode == GEMM_PARTIAL ? g.ld : n_rows;
+    dim3 grid((n_rows + 63) / 64, (g.T + 31) / 32, g.S);
+    DFL_CHECK_LAUNCH(launch(dfl::k_gemm_f32, grid, dim3(256), 0, st, (const float *)g.W,
+                            (const float *)g.X, part, ldp, n_rows, g.T, g.K_in, g.K_in / g.S));
+    if (g.mode != GEMM_PARTIAL) {
+      const size_t n = (size_t)g.T * g.N_out;
+      const int blocks = (int)std::min<size_t>((n + 255) / 256, (size_t)d->num_sms * 8);
+      DFL_CHECK_LAUNCH(launch(dfl::k_gemm_f32_finish, dim3(blocks), dim3(256), 0, st,
+                              (const float *)part, g.S, g.T, g.N_out, ldp, g.mode, g.N_out,
+                              g.out_f32, g.ld, (float *)g.out_bf16, g.ldb));
+    }
     return DFLASH_OK;
   }
-  if ((uintptr_t)W % 16 || (uintptr_t)X % 16) return DFLASH_ERR_ALIGN;
-  switch (token_tile(T)) {
-    case 16: return launch_tc<16>(W, N_out, K_in, X, T, out, ld, S, err, st, d);
-    case 32: return launch_tc<32>(W, N_out, K_in, X, T, out, ld, S, err, st, d);
-    case 64: return launch_tc<64>(W, N_out, K_in, X, T, out, ld, S, err, st, d);
-    case 128: return launch_tc<128>(W, N_out, K_in, X, T, out, ld, S, err, st, d);
-    default: return launch_tc<256>(W, N_out, K_in, X, T, out, ld, S, err, st, d);
+  if ((uintptr_t)g.W % 16 || (uintptr_t)g.X % 16) return DFLASH_ERR_ALIGN;
+  switch (token_tile(g.T)) {
+    case 16: return launch_tc<16>(g, st, d);
+    case 32: return launch_tc<32>(g, st, d);
+    case 64: return launch_tc<64>(g, st, d);
+    case 128: return launch_tc<128>(g, st, d);
+    default: return launch_tc<256>(g, st, d);
   }
+}
+
+int gemm_xwT(int dtype, const void *W, int N_out, int K_in, const void *X, int T, float *out,
+             int ld, int S, int *err, cudaStream_t st) {
+  GemmCall g;
+  g.dtype = dtype;
+  g.W = W;
+  g.N_out = N_out;
+  g.K_in = K_in;
+  g.X = X;
+  g.T = T;
+  g.S = S;
+  g.mode = GEMM_PARTIAL;
+  g.out = out;
+  g.ld = ld;
+  g.err = err;
+  return gemm_run(g, st);
 }
 
 }  // namespace dflh

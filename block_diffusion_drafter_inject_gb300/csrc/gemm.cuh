@@ -9,12 +9,44 @@ namespace dflh {
 
 constexpr size_t kMaxPartialFloats = size_t(48) << 20;  // cap of one partial buffer
 
-// Number of K slices for a GEMM of this shape on `num_sms` SMs.
-int gemm_splits(int N_out, int T, int K_in, int num_sms);
+// Number of K slices for a GEMM of this shape on `num_sms` SMs (at most max_S).
+int gemm_splits(int N_out, int T, int K_in, int num_sms, int max_S = 1 << 20);
 
-// Launch one GEMM.  dtype selects the operand storage (DFLASH_BF16: tcgen05
-// tensor cores fed by TMA; DFLASH_F32: fp32 CUDA cores).  W and X must be
-// 16-byte aligned and K_in a multiple of 64.  Returns DFLASH_OK or an error.
+enum GemmMode {
+  GEMM_PARTIAL = 0,  // slice s -> out[(s*T + t)*ld + n]; the caller sums the slices
+  GEMM_REDUCE = 1,   // final Y -> out_f32[t*ld + n] and/or out_bf16[t*ldb + n]
+  GEMM_SWIGLU = 2,   // rows [Wg; Wu] of a 2F-row weight: out_bf16[t*ldb + f] = SiLU(g_f) u_f
+};
+
+struct GemmCall {
+  int dtype = DFLASH_BF16;
+  const void *W = nullptr;
+  int N_out = 0;       // output features (F for GEMM_SWIGLU)
+  int K_in = 0;
+  const void *X = nullptr;
+  int T = 0;
+  int S = 1;
+  int mode = GEMM_PARTIAL;
+  float *out = nullptr;       // GEMM_PARTIAL output, or the slice scratch of the other modes
+  int ld = 0;
+  float *out_f32 = nullptr;   // GEMM_REDUCE
+  void *out_bf16 = nullptr;   // GEMM_REDUCE / GEMM_SWIGLU (storage dtype)
+  int ldb = 0;
+  int *counters = nullptr;    // tile tickets, zero on entry and on exit (S > 1)
+  int *err = nullptr;
+};
+
+// Floats of slice scratch a reduce-mode GEMM needs (0 when S == 1).
+size_t gemm_scratch_floats(int N_out, int T, int S, int mode);
+// Tile tickets a reduce-mode GEMM needs.
+size_t gemm_tiles(int N_out, int T, int mode);
+
+// Launch one GEMM.  DFLASH_BF16 operands run on tcgen05 tensor cores fed by
+// TMA; DFLASH_F32 on fp32 CUDA cores.  W and X 16-byte aligned, K_in a
+// multiple of 64, S dividing K_in/64.  Returns DFLASH_OK or an error.
+int gemm_run(const GemmCall &g, cudaStream_t stream);
+
+// GEMM_PARTIAL convenience form
 int gemm_xwT(int dtype, const void *W, int N_out, int K_in, const void *X, int T, float *out,
              int ld, int S, int *err, cudaStream_t stream);
 

@@ -36,99 +36,125 @@ __device__ __forceinline__ VI block_best(VI a, float *redv, int *redi) {
   return warp_best(b);
 }
 
-// One chunk of one logit row: local max, sum of exp, local top-k.
+// One chunk (8 warps x 1024 logits) of one row: max, sum of exp and top-k.
+// Each warp selects its own top-k in registers (32 values per lane, k rounds
+// of a warp-wide best), then warp 0 merges the 8 warp lists.
 // partial layout per (row, chunk): [m, s, v_0..v_{k-1}, id_0..id_{k-1}]
 __global__ void __launch_bounds__(256) k_topk_partial(const float *__restrict__ logits, int V,
                                                       int k, float *__restrict__ partial) {
-  __shared__ float vals[dflh::kTopkChunk];
-  __shared__ float redv[32];
-  __shared__ int redi[32];
+  __shared__ float cv[8 * DFLASH_MAX_TOPK];
+  __shared__ int ci[8 * DFLASH_MAX_TOPK];
+  __shared__ float wm[8], wsum[8];
   pdl_launch();
   pdl_wait();
   const int chunk = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
-  const int c0 = chunk * dflh::kTopkChunk;
-  const int n = min(dflh::kTopkChunk, V - c0);
-  const float *z = logits + (size_t)row * V + c0;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int base = chunk * dflh::kTopkChunk + w * 1024;
+  const float *z = logits + (size_t)row * V;
+  float v[32];
   float mx = -INFINITY;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    float v = z[i];
-    vals[i] = v;
-    mx = fmaxf(mx, v);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const int id = base + j * 32 + lane;
+    v[j] = id < V ? z[id] : -INFINITY;
+    mx = fmaxf(mx, v[j]);
   }
   mx = warp_max(mx);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) redv[threadIdx.x >> 5] = mx;
-  __syncthreads();
-  mx = (threadIdx.x & 31) < (blockDim.x >> 5) ? redv[threadIdx.x & 31] : -INFINITY;
-  mx = warp_max(mx);
   float se = 0.f;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) se += expf(vals[i] - mx);
-  se = block_sum(se, redv);
-  float *out = partial + ((size_t)row * nch + chunk) * (2 * k + 2);
-  if (threadIdx.x == 0) out[0] = mx, out[1] = se;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) se += (v[j] == -INFINITY) ? 0.f : expf(v[j] - mx);
+  se = warp_sum(se);
+  if (lane == 0) wm[w] = mx, wsum[w] = se;
+  uint32_t taken = 0;
   for (int it = 0; it < k; ++it) {
     VI best{-INFINITY, 0x7fffffff};
-    for (int i = threadIdx.x; i < n; i += blockDim.x)
-      if (better(vals[i], c0 + i, best.v, best.i)) best.v = vals[i], best.i = c0 + i;
-    best = block_best(best, redv, redi);
-    if (threadIdx.x == 0) {
-      out[2 + it] = best.v;
-      out[2 + k + it] = __int_as_float(best.i);
-      if (best.i != 0x7fffffff) vals[best.i - c0] = -INFINITY;
+    int bj = -1;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int id = base + j * 32 + lane;
+      if (!((taken >> j) & 1u) && id < V && better(v[j], id, best.v, best.i))
+        best.v = v[j], best.i = id, bj = j;
     }
-    __syncthreads();
+    const VI win = warp_best(best);
+    if (bj >= 0 && best.i == win.i) taken |= 1u << bj;
+    if (lane == 0) cv[w * k + it] = win.v, ci[w * k + it] = win.i;
+  }
+  __syncthreads();
+  if (w != 0) return;
+  float *out = partial + ((size_t)row * nch + chunk) * (2 * k + 2);
+  float M = -INFINITY;
+  for (int q = 0; q < 8; ++q) M = fmaxf(M, wm[q]);
+  if (lane == 0) {
+    float S = 0.f;
+    for (int q = 0; q < 8; ++q) S += (wm[q] == -INFINITY) ? 0.f : wsum[q] * expf(wm[q] - M);
+    out[0] = M;
+    out[1] = S;
+  }
+  // merge 8 lists of k: lane holds candidates lane, lane + 32, ...
+  const int nc = 8 * k;
+  uint32_t tk = 0;
+  for (int it = 0; it < k; ++it) {
+    VI best{-INFINITY, 0x7fffffff};
+    int bq = -1;
+    for (int q = 0; q * 32 + lane < nc; ++q) {
+      const int e = q * 32 + lane;
+      if (!((tk >> q) & 1u) && better(cv[e], ci[e], best.v, best.i)) best.v = cv[e], best.i = ci[e], bq = q;
+    }
+    const VI win = warp_best(best);
+    if (bq >= 0 && best.i == win.i) tk |= 1u << bq;
+    if (lane == 0) {
+      out[2 + it] = win.v;
+      out[2 + k + it] = __int_as_float(win.i);
+    }
   }
 }
 
-// Merge the chunks of one row: top-k ids, logp = logit - logsumexp.
-__global__ void __launch_bounds__(256) k_topk_merge(const float *__restrict__ partial, int nch,
-                                                    int k, int32_t *__restrict__ ids,
+// Merge the chunks of one row (one warp per row): top-k ids and
+// logp = logit - logsumexp.  Candidates staged in shared memory.
+__global__ void __launch_bounds__(128) k_topk_merge(const float *__restrict__ partial, int rows,
+                                                    int nch, int k, int32_t *__restrict__ ids,
                                                     float *__restrict__ logp) {
-  extern __shared__ float cand[];  // [nch*k] values, then [nch*k] ids
-  __shared__ float redv[32];
-  __shared__ int redi[32];
+  extern __shared__ float cand[];  // per warp: [nch*k] values, [nch*k] ids, [nch*k] taken
   pdl_launch();
   pdl_wait();
-  const int row = blockIdx.x, n = nch * k;
-  int *cid = (int *)(cand + n);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + w;
+  const int n = nch * k;
+  float *cval = cand + (size_t)w * 3 * n;
+  int *cid = (int *)(cval + n);
+  int *ctk = cid + n;
+  if (row >= rows) return;
   const float *pr = partial + (size_t)row * nch * (2 * k + 2);
   float M = -INFINITY;
-  for (int c = threadIdx.x; c < nch; c += blockDim.x) M = fmaxf(M, pr[(size_t)c * (2 * k + 2)]);
+  for (int c = lane; c < nch; c += 32) M = fmaxf(M, pr[(size_t)c * (2 * k + 2)]);
   M = warp_max(M);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) redv[threadIdx.x >> 5] = M;
-  __syncthreads();
-  M = (threadIdx.x & 31) < (blockDim.x >> 5) ? redv[threadIdx.x & 31] : -INFINITY;
-  M = warp_max(M);
-  float s = 0.f;
-  for (int c = threadIdx.x; c < nch; c += blockDim.x) {
+  float S = 0.f;
+  for (int c = lane; c < nch; c += 32) {
     const float *p = pr + (size_t)c * (2 * k + 2);
-    s += p[1] * expf(p[0] - M);
+    S += p[0] == -INFINITY ? 0.f : p[1] * expf(p[0] - M);
   }
-  s = block_sum(s, redv);
-  const float lse = M + logf(s);
-  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+  S = warp_sum(S);
+  const float lse = M + logf(S);
+  for (int e = lane; e < n; e += 32) {
     const int c = e / k, j = e % k;
     const float *p = pr + (size_t)c * (2 * k + 2);
-    cand[e] = p[2 + j];
+    cval[e] = p[2 + j];
     cid[e] = __float_as_int(p[2 + k + j]);
+    ctk[e] = 0;
   }
-  __syncthreads();
+  __syncwarp();
   for (int it = 0; it < k; ++it) {
     VI best{-INFINITY, 0x7fffffff};
     int where = -1;
-    for (int e = threadIdx.x; e < n; e += blockDim.x)
-      if (better(cand[e], cid[e], best.v, best.i)) best.v = cand[e], best.i = cid[e], where = e;
-    VI b = block_best(best, redv, redi);
-    if (best.i == b.i && where >= 0 && cand[where] == b.v) {
-      cand[where] = -INFINITY;
-      cid[where] = 0x7fffffff;
+    for (int e = lane; e < n; e += 32)
+      if (!ctk[e] && better(cval[e], cid[e], best.v, best.i)) best.v = cval[e], best.i = cid[e], where = e;
+    const VI win = warp_best(best);
+    if (where >= 0 && best.i == win.i) ctk[where] = 1;
+    if (lane == 0) {
+      ids[(size_t)row * k + it] = win.i;
+      logp[(size_t)row * k + it] = win.v - lse;
     }
-    if (threadIdx.x == 0) {
-      ids[(size_t)row * k + it] = b.i;
-      logp[(size_t)row * k + it] = b.v - lse;
-    }
-    __syncthreads();
+    __syncwarp();
   }
 }
 
@@ -160,87 +186,90 @@ __global__ void __launch_bounds__(256) k_sel_gather(const S *__restrict__ E,
   }
 }
 
-// One CTA per request: max-sum Viterbi over the K-1 positions of k candidates.
-// u = P_u e and v = P_v e come from the selector GEMM slices (summed here).
-__global__ void __launch_bounds__(256) k_viterbi(const float *__restrict__ upart,
-                                                 const float *__restrict__ vpart, int nsu,
-                                                 int nsv, const int32_t *__restrict__ topk_ids,
-                                                 const float *__restrict__ topk_logp, int B, int K,
-                                                 int k, int r, int32_t *__restrict__ path,
-                                                 float *__restrict__ score) {
+// Pair scores of every adjacent candidate pair, all positions at once:
+//   pair[b][t][i][j] = u(pred_i) . v(c_tj),  pred = the anchor at t = 0, else c_{t-1}
+// u = P_u e and v = P_v e are rows of the (reduced) selector projections, r wide.
+// grid (K-1, B); shared: 2 * k * (r + 4) floats.
+__global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
+                                                   const float *__restrict__ Vp, int K, int k,
+                                                   int r, float *__restrict__ pair) {
   extern __shared__ float sm[];
-  const int LDR = r + 1;
-  float *su = sm;                     // [k][LDR] predecessors' u
-  float *sv = su + (size_t)k * LDR;   // [k][LDR] current candidates' v
-  float *pair = sv + (size_t)k * LDR; // [k][k]
-  float *delta = pair + k * k;        // [k]
-  int *bp = (int *)(delta + k);       // [(K-1)][k]
+  const int LDR = r + 4;
+  float *su = sm, *sv = sm + (size_t)k * LDR;
   pdl_launch();
   pdl_wait();
-  const int b = blockIdx.x;
+  const int t = blockIdx.x, b = blockIdx.y;
   const int R = 1 + (K - 1) * k;
-  const size_t rows = (size_t)B * R;
-  auto urow = [&](int j, int c) {
-    float s = 0.f;
-    for (int q = 0; q < nsu; ++q) s += upart[((size_t)q * rows + (size_t)b * R + j) * r + c];
-    return s;
-  };
-  auto vrow = [&](int j, int c) {
-    float s = 0.f;
-    for (int q = 0; q < nsv; ++q) s += vpart[((size_t)q * rows + (size_t)b * R + j) * r + c];
-    return s;
-  };
-  // predecessor of position 0: the anchor (row 0)
-  for (int c = threadIdx.x; c < r; c += blockDim.x) su[c] = urow(0, c);
-  int n_prev = 1;
+  const int np = t == 0 ? 1 : k;
+  const size_t ubase = (size_t)b * R + (t == 0 ? 0 : 1 + (size_t)(t - 1) * k);
+  const size_t vbase = (size_t)b * R + 1 + (size_t)t * k;
+  const int r4 = r / 4;
+  for (int e = threadIdx.x; e < np * r4; e += blockDim.x) {
+    const int i = e / r4, c = e % r4;
+    *(float4 *)(su + (size_t)i * LDR + 4 * c) = ((const float4 *)(U + (ubase + i) * r))[c];
+  }
+  for (int e = threadIdx.x; e < k * r4; e += blockDim.x) {
+    const int j = e / r4, c = e % r4;
+    *(float4 *)(sv + (size_t)j * LDR + 4 * c) = ((const float4 *)(Vp + (vbase + j) * r))[c];
+  }
+  __syncthreads();
+  // one warp per pair, lanes across the rank
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  float *out = pair + ((size_t)b * (K - 1) + t) * k * k;
+  for (int e = w; e < np * k; e += nw) {
+    const int i = e / k, j = e % k;
+    float d = 0.f;
+    for (int c = lane; c < r; c += 32) d = fmaf(su[(size_t)i * LDR + c], sv[(size_t)j * LDR + c], d);
+    d = warp_sum(d);
+    if (lane == 0) out[e] = d;
+  }
+}
+
+// One CTA per request: max-sum Viterbi over the K-1 positions of k candidates
+// on the precomputed pair scores.  Ties go to the lower candidate rank.
+__global__ void __launch_bounds__(32) k_viterbi(const float *__restrict__ pair,
+                                                const int32_t *__restrict__ topk_ids,
+                                                const float *__restrict__ topk_logp, int K, int k,
+                                                int32_t *__restrict__ path,
+                                                float *__restrict__ score) {
+  __shared__ float delta[DFLASH_MAX_TOPK];
+  __shared__ int bp[DFLASH_MAX_BLOCK][DFLASH_MAX_TOPK];
+  pdl_launch();
+  pdl_wait();
+  const int b = blockIdx.x, j = threadIdx.x;
   for (int t = 0; t < K - 1; ++t) {
-    for (int e = threadIdx.x; e < k * r; e += blockDim.x) {
-      const int j = e / r, c = e % r;
-      sv[j * LDR + c] = vrow(1 + t * k + j, c);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < n_prev * k; e += blockDim.x) {
-      const int i = e / k, j = e % k;
-      float d = 0.f;
-      for (int c = 0; c < r; ++c) d = fmaf(su[i * LDR + c], sv[j * LDR + c], d);
-      pair[i * k + j] = d;
-    }
-    __syncthreads();
+    const float *pr = pair + ((size_t)b * (K - 1) + t) * k * k;
     const float *lp = topk_logp + ((size_t)b * (K - 1) + t) * k;
     float nd = 0.f;
     int arg = 0;
-    if (threadIdx.x < k) {
-      const int j = threadIdx.x;
-      float best = -INFINITY;
-      for (int i = 0; i < n_prev; ++i) {
-        const float c = (t == 0 ? 0.f : delta[i]) + pair[i * k + j];
-        if (c > best) best = c, arg = i;  // strict: the lower rank keeps ties
+    if (j < k) {
+      if (t == 0) {
+        nd = lp[j] + pr[j];
+      } else {
+        float best = -INFINITY;
+        for (int i = 0; i < k; ++i) {
+          const float c = delta[i] + pr[i * k + j];
+          if (c > best) best = c, arg = i;  // strict: the lower rank keeps ties
+        }
+        nd = lp[j] + best;
       }
-      nd = lp[j] + best;
     }
-    __syncthreads();
-    if (threadIdx.x < k) {
-      delta[threadIdx.x] = nd;
-      bp[t * k + threadIdx.x] = arg;
+    __syncwarp();
+    if (j < k) {
+      delta[j] = nd;
+      bp[t][j] = arg;
     }
-    // the current candidates become the predecessors
-    if (t + 1 < K - 1)
-      for (int e = threadIdx.x; e < k * r; e += blockDim.x) {
-        const int j = e / r, c = e % r;
-        su[j * LDR + c] = urow(1 + t * k + j, c);
-      }
-    n_prev = k;
-    __syncthreads();
+    __syncwarp();
   }
-  if (threadIdx.x == 0) {
+  if (j == 0) {
     int best = 0;
-    for (int j = 1; j < k; ++j)
-      if (delta[j] > delta[best]) best = j;
+    for (int i = 1; i < k; ++i)
+      if (delta[i] > delta[best]) best = i;
     score[b] = delta[best];
-    int j = best;
+    int c = best;
     for (int t = K - 2; t >= 0; --t) {
-      path[(size_t)b * (K - 1) + t] = topk_ids[((size_t)b * (K - 1) + t) * k + j];
-      j = bp[t * k + j];
+      path[(size_t)b * (K - 1) + t] = topk_ids[((size_t)b * (K - 1) + t) * k + c];
+      c = bp[t][c];
     }
   }
 }
@@ -308,14 +337,14 @@ int launch_topk(const float *logits, int rows, int V, int k, float *partial, int
   const int nch = topk_chunks(V);
   DFL_CHECK_LAUNCH(launch(dfl::k_topk_partial, dim3(nch, rows), dim3(256), 0, st, logits, V, k,
                           partial));
-  const size_t smem = (size_t)nch * k * 2 * sizeof(float);
+  const size_t smem = 4 * 3 * (size_t)nch * k * sizeof(float);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(dfl::k_topk_merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return DFLASH_ERR_CUDA;
   }
-  DFL_CHECK_LAUNCH(launch(dfl::k_topk_merge, dim3(rows), dim3(256), smem, st,
-                          (const float *)partial, nch, k, ids, logp));
+  DFL_CHECK_LAUNCH(launch(dfl::k_topk_merge, dim3((rows + 3) / 4), dim3(128), smem, st,
+                          (const float *)partial, rows, nch, k, ids, logp));
   return DFLASH_OK;
 }
 
@@ -332,18 +361,19 @@ template int launch_sel_gather<float>(const float *, const int32_t *, const int3
 template int launch_sel_gather<dfl::bf16>(const dfl::bf16 *, const int32_t *, const int32_t *, int,
                                           int, int, int, int, dfl::bf16 *, int *, cudaStream_t);
 
-int launch_viterbi(const float *upart, const float *vpart, int nsu, int nsv,
-                   const int32_t *topk_ids, const float *topk_logp, int B, int K, int k, int r,
+int launch_viterbi(const float *U, const float *Vp, const int32_t *topk_ids,
+                   const float *topk_logp, int B, int K, int k, int r, float *pair,
                    int32_t *path, float *score, cudaStream_t st) {
-  const size_t smem = sizeof(float) * (2 * (size_t)k * (r + 1) + (size_t)k * k + k) +
-                      sizeof(int) * (size_t)(K - 1) * k;
+  const size_t smem = sizeof(float) * 2 * (size_t)k * (r + 4);
   if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(dfl::k_viterbi, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(dfl::k_sel_pairs, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return DFLASH_ERR_CUDA;
   }
-  DFL_CHECK_LAUNCH(launch(dfl::k_viterbi, dim3(B), dim3(256), smem, st, upart, vpart, nsu, nsv,
-                          topk_ids, topk_logp, B, K, k, r, path, score));
+  DFL_CHECK_LAUNCH(launch(dfl::k_sel_pairs, dim3(K - 1, B), dim3(256), smem, st, U, Vp, K, k, r,
+                          pair));
+  DFL_CHECK_LAUNCH(launch(dfl::k_viterbi, dim3(B), dim3(32), 0, st, (const float *)pair, topk_ids,
+                          topk_logp, K, k, path, score));
   return DFLASH_OK;
 }
 

@@ -4,7 +4,7 @@
 
 namespace dflh {
 
-constexpr int kTopkChunk = 4096;
+constexpr int kTopkChunk = 8192;  // logits per top-k CTA (8 warps x 1024)
 
 inline int topk_chunks(int V) { return (V + kTopkChunk - 1) / kTopkChunk; }
 
@@ -16,8 +16,10 @@ template <typename S>
 int launch_sel_gather(const S *E, const int32_t *anchor, const int32_t *topk_ids, int B, int K,
                       int k, int V, int D, S *rows, int *err, cudaStream_t st);
 
-int launch_viterbi(const float *upart, const float *vpart, int nsplit_u, int nsplit_v,
-                   const int32_t *topk_ids, const float *topk_logp, int B, int K, int k, int r,
+// U, Vp: reduced selector projections [B*R, r] fp32 (R = 1 + (K-1)*k rows per
+// request: anchor, then candidates by (position, rank)); pair: B*(K-1)*k*k scratch
+int launch_viterbi(const float *U, const float *Vp, const int32_t *topk_ids,
+                   const float *topk_logp, int B, int K, int k, int r, float *pair,
                    int32_t *path, float *score, cudaStream_t st);
 
 constexpr int kArgmaxChunk = 8192;

@@ -80,50 +80,40 @@ __global__ void __launch_bounds__(1024) k_rows_norm(const S *__restrict__ in, in
   }
 }
 
-// Gate corrections of row r for gate rows [j0, j0 + n) of each half (a and b):
-// the K slices of the gate GEMM summed in slice order into shared memory
-// (ga[j] for a, gb[j] for b).  One pass over the slices per gate row.
-__device__ __forceinline__ void gate_sums(const float *__restrict__ gpart, int nsplit, int rows,
-                                          int GW, int r, int j0, int n, float *ga, float *gb) {
-  const int half = GW / 2;
-  for (int e = threadIdx.x; e < 2 * n; e += blockDim.x) {
-    const int j = e < n ? j0 + e : half + j0 + (e - n);
-    const float *p = gpart + (size_t)r * GW + j;
-    float s = 0.f;
-    for (int k = 0; k < nsplit; ++k) s += p[(size_t)k * rows * GW];
-    if (e < n)
-      ga[e] = s;
-    else
-      gb[e - n] = s;
-  }
-  __syncthreads();
-}
-
-// Pre-sublayer conv: ub[r] = a(r) * un[r] + b(r) * un[r-1] (zero before slot 0).
-// grid (rows, channel chunks of `chunk`), dynamic shared: 2 * chunk/group floats.
+// Pre-sublayer conv: ub[r] = a(r) * un[r] + b(r) * un[r-1] (zero before slot 0),
+//   a_c(r) = sigmoid(base[c] + gate[r][c/g]),  b_c(r) = sigmoid(base[D+c] + gate[r][D/g + c/g])
+// gate: the conv's gate linear of row r, fp32 [rows, 2D/g].  grid (rows, D/chunk).
 template <typename S>
 __global__ void __launch_bounds__(256) k_conv_pre(const S *__restrict__ un,
-                                                  const float *__restrict__ gpart, int nsplit,
-                                                  int rows, int K, int D, int group, int chunk,
-                                                  const S *__restrict__ base,
+                                                  const float *__restrict__ gate, int K, int D,
+                                                  int group, int chunk, const S *__restrict__ base,
                                                   S *__restrict__ ub) {
-  extern __shared__ float gs[];
   pdl_launch();
   pdl_wait();
   const int r = blockIdx.x;
   const int c0 = blockIdx.y * chunk, c1 = min(D, c0 + chunk);
-  const int GW = 2 * D / group;
-  const int g0 = c0 / group, ng = (c1 - 1) / group - g0 + 1;
-  float *ga = gs, *gb = gs + ng;
-  gate_sums(gpart, nsplit, rows, GW, r, g0, ng, ga, gb);
+  const float *ga = gate + (size_t)r * (2 * D / group);
+  const float *gb = ga + D / group;
   const bool first = (r % K) == 0;
-  for (int c = c0 + threadIdx.x; c < c1; c += blockDim.x) {
-    const int g = c / group - g0;
-    const float a = sigmoidf_(ldf(base + c) + ga[g]);
-    const float bg = sigmoidf_(ldf(base + D + c) + gb[g]);
-    const float cur = ldf(un + (size_t)r * D + c);
-    const float prev = first ? 0.f : ldf(un + (size_t)(r - 1) * D + c);
-    stf(ub + (size_t)r * D + c, a * cur + bg * prev);
+  for (int c = c0 + threadIdx.x * 8; c < c1; c += blockDim.x * 8) {
+    float cur[8], prev[8], ba[8], bb[8], y[8];
+    load8(un + (size_t)r * D + c, cur);
+    if (first) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) prev[j] = 0.f;
+    } else {
+      load8(un + (size_t)(r - 1) * D + c, prev);
+    }
+    load8(base + c, ba);
+    load8(base + D + c, bb);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int g = (c + j) / group;
+      const float a = sigmoidf_(ba[j] + ga[g]);
+      const float b = sigmoidf_(bb[j] + gb[g]);
+      y[j] = a * cur[j] + b * prev[j];
+    }
+    store8(ub + (size_t)r * D + c, y);
   }
 }
 
@@ -131,79 +121,59 @@ __global__ void __launch_bounds__(256) k_conv_pre(const S *__restrict__ un,
 //   x[r] += a(r) * rf[r] + b(r) * rf[r-1];  un[r] = gain * x[r] / rms(x[r]).
 // With zf != nullptr (after the last layer) the normed rows of slots 1..K-1
 // are written compactly to zf[b*(K-1) + i-1] instead of un.
-// One CTA per row; dynamic shared: D + 2*D/group floats.
+// One CTA per row; dynamic shared: D floats.
 template <typename S>
-__global__ void __launch_bounds__(1024) k_conv_post_norm(
-    const float *__restrict__ rf, const float *__restrict__ gpart, int nsplit, int rows, int K,
-    int D, int group, const S *__restrict__ base, float *__restrict__ x,
-    const S *__restrict__ gain, float eps, S *__restrict__ un, S *__restrict__ zf) {
-  extern __shared__ float sm[];
+__global__ void __launch_bounds__(512) k_conv_post_norm(
+    const float *__restrict__ rf, const float *__restrict__ gate, int K, int D, int group,
+    const S *__restrict__ base, float *__restrict__ x, const S *__restrict__ gain, float eps,
+    S *__restrict__ un, S *__restrict__ zf) {
+  extern __shared__ float xrow[];
   __shared__ float red[32];
-  float *xrow = sm;
-  float *ga = sm + D, *gb = ga + D / group;
   pdl_launch();
   pdl_wait();
   const int r = blockIdx.x;
-  const int GW = 2 * D / group;
-  gate_sums(gpart, nsplit, rows, GW, r, 0, D / group, ga, gb);
+  const float *ga = gate + (size_t)r * (2 * D / group);
+  const float *gb = ga + D / group;
   const bool first = (r % K) == 0;
   float ss = 0.f;
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    const int g = c / group;
-    const float a = sigmoidf_(ldf(base + c) + ga[g]);
-    const float bg = sigmoidf_(ldf(base + D + c) + gb[g]);
-    const float cur = rf[(size_t)r * D + c];
-    const float prev = first ? 0.f : rf[(size_t)(r - 1) * D + c];
-    const float v = x[(size_t)r * D + c] + (a * cur + bg * prev);
-    x[(size_t)r * D + c] = v;
-    xrow[c] = v;
-    ss += v * v;
+  for (int c = threadIdx.x * 8; c < D; c += blockDim.x * 8) {
+    float cur[8], prev[8], ba[8], bb[8], xv[8];
+    load8(rf + (size_t)r * D + c, cur);
+    if (first) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) prev[j] = 0.f;
+    } else {
+      load8(rf + (size_t)(r - 1) * D + c, prev);
+    }
+    load8(base + c, ba);
+    load8(base + D + c, bb);
+    load8(x + (size_t)r * D + c, xv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int g = (c + j) / group;
+      const float a = sigmoidf_(ba[j] + ga[g]);
+      const float b = sigmoidf_(bb[j] + gb[g]);
+      xv[j] += a * cur[j] + b * prev[j];
+      xrow[c + j] = xv[j];
+      ss += xv[j] * xv[j];
+    }
+    store8(x + (size_t)r * D + c, xv);
   }
   const float inv = rsqrtf(block_sum(ss, red) / D + eps);
+  S *o;
   if (zf) {
     const int i = r % K, b = r / K;
     if (i == 0) return;
-    S *o = zf + ((size_t)b * (K - 1) + (i - 1)) * D;
-    for (int c = threadIdx.x; c < D; c += blockDim.x) stf(o + c, xrow[c] * inv * ldf(gain + c));
+    o = zf + ((size_t)b * (K - 1) + (i - 1)) * D;
   } else {
-    for (int c = threadIdx.x; c < D; c += blockDim.x)
-      stf(un + (size_t)r * D + c, xrow[c] * inv * ldf(gain + c));
+    o = un + (size_t)r * D;
   }
-}
-
-// rf = sum of slices (fp32, may be null); rb = rf rounded to storage
-template <typename S>
-__global__ void __launch_bounds__(256) k_reduce(const float *__restrict__ part, int nsplit,
-                                                size_t n, float *__restrict__ rf,
-                                                S *__restrict__ rb) {
-  pdl_launch();
-  pdl_wait();
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
-       i += (size_t)gridDim.x * blockDim.x) {
-    float s = 0.f;
-    for (int k = 0; k < nsplit; ++k) s += part[(size_t)k * n + i];
-    if (rf) rf[i] = s;
-    if (rb) stf(rb + i, s);
-  }
-}
-
-// hb[r][j] = SiLU(gate) * up with [gate | up] the two halves of the gate/up GEMM row
-template <typename S>
-__global__ void __launch_bounds__(256) k_swiglu(const float *__restrict__ part, int nsplit,
-                                                int rows, int F, S *__restrict__ hb) {
-  pdl_launch();
-  pdl_wait();
-  const size_t n = (size_t)rows * F;
-  const size_t slice = (size_t)rows * 2 * F;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const size_t r = i / F, j = i % F;
-    float g = 0.f, u = 0.f;
-    for (int k = 0; k < nsplit; ++k) {
-      g += part[k * slice + r * 2 * F + j];
-      u += part[k * slice + r * 2 * F + F + j];
-    }
-    stf(hb + i, g * sigmoidf_(g) * u);
+  for (int c = threadIdx.x * 8; c < D; c += blockDim.x * 8) {
+    float g[8], y[8];
+    load8(gain + c, g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[j] = xrow[c + j] * inv * g[j];
+    store8(o + c, y);
   }
 }
 
@@ -231,9 +201,10 @@ __device__ __forceinline__ void head_norm_rope(float &lo, float &hi, int i, int 
   }
 }
 
-// q, k, v of the block from the QKV GEMM slices.  grid (rows, Hq + 2*Hkv), block d/2.
+// q, k, v of the block from the QKV projection qkv [rows, (Hq+2Hkv)*d] (fp32).
+// grid (rows, Hq + 2*Hkv), block d/2.
 template <typename S>
-__global__ void k_qkv_post(const float *__restrict__ part, int nsplit, int rows, int K, int Hq,
+__global__ void k_qkv_post(const float *__restrict__ qkv, int rows, int K, int Hq,
                            int Hkv, int dh, const S *__restrict__ qn, const S *__restrict__ kn,
                            const int32_t *__restrict__ ctx_len, const dflh::RopeTable rope,
                            float eps, S *__restrict__ qb, S *__restrict__ kb,
@@ -243,14 +214,9 @@ __global__ void k_qkv_post(const float *__restrict__ part, int nsplit, int rows,
   pdl_wait();
   const int r = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = dh / 2;
   const int W = (Hq + 2 * Hkv) * dh;
-  const size_t slice = (size_t)rows * W;
   const size_t o = (size_t)r * W + (size_t)h * dh;
-  float lo = 0.f, hi = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < nsplit; ++k) {
-    lo += part[k * slice + o + i];
-    hi += part[k * slice + o + i + half];
-  }
+  float lo = qkv[o + i], hi = qkv[o + i + half];
+  (void)rows;
   if (h < Hq + Hkv) {
     const S *g = h < Hq ? qn : kn;
     const int pos = ctx_len[r / K] + (r % K);
@@ -266,10 +232,10 @@ __global__ void k_qkv_post(const float *__restrict__ part, int nsplit, int rows,
 }
 
 // Injection epilogue: K = RoPE(k_norm(.)), V as is, into the paged caches.
-// kvpart holds, per layer, nsplit slices of [N, 2*Hkv*d] (K heads then V heads).
+// kvf holds, per layer, the K/V projection [N, 2*Hkv*d] (K heads then V heads).
 // grid (N, L, 2*Hkv), block d/2.
 template <typename S>
-__global__ void k_inject_store(const float *__restrict__ kvpart, int nsplit, int N, int L, int Hkv,
+__global__ void k_inject_store(const float *__restrict__ kvf, int N, int L, int Hkv,
                                int dh, dflh::LayerPtrs knorm, const int32_t *__restrict__ req,
                                const int32_t *__restrict__ pos, const int32_t *__restrict__ table,
                                int num_rows, int max_pages, int num_pages, int P,
@@ -280,15 +246,8 @@ __global__ void k_inject_store(const float *__restrict__ kvpart, int nsplit, int
   pdl_wait();
   const int n = blockIdx.x, l = blockIdx.y, h = blockIdx.z, i = threadIdx.x, half = dh / 2;
   const int W = 2 * Hkv * dh;
-  const size_t slice = (size_t)N * W;
-  const size_t layer_off = (size_t)l * nsplit * slice;
-  const size_t o = (size_t)n * W + (size_t)h * dh;
-  float lo = 0.f, hi = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < nsplit; ++k) {
-    lo += kvpart[layer_off + k * slice + o + i];
-    hi += kvpart[layer_off + k * slice + o + i + half];
-  }
+  const size_t o = (size_t)l * N * W + (size_t)n * W + (size_t)h * dh;
+  float lo = kvf[o + i], hi = kvf[o + i + half];
   const int row = req[n], p = pos[n];
   bool ok = true;
   if (row < 0 || row >= num_rows) {
@@ -334,13 +293,6 @@ RopeTable rope_table(float theta, int head_dim) {
   return t;
 }
 
-static int grid_for(size_t n) {
-  const Dev *d = device();
-  size_t g = (n + 255) / 256;
-  size_t cap = (size_t)(d ? d->num_sms : 152) * 8;
-  return (int)(g < cap ? (g > 0 ? g : 1) : cap);
-}
-
 template <typename S>
 int launch_embed_norm(const S *E, const int32_t *anchor, int mask_id, int V, int B, int K, int D,
                       const S *gain, float eps, float *x, S *un, int *err, cudaStream_t st) {
@@ -358,64 +310,45 @@ int launch_rows_norm(const S *in, int rows, int cols, const S *gain, float eps, 
   return DFLASH_OK;
 }
 template <typename S>
-int launch_conv_pre(const S *un, const float *gpart, int nsplit, int rows, int K, int D,
-                    int group, const S *base, S *ub, cudaStream_t st) {
-  // channel chunks: a multiple of the group, about 1024 channels
-  int chunk = ((1024 + group - 1) / group) * group;
-  if (chunk > D) chunk = D;
-  const int nchunk = (D + chunk - 1) / chunk;
-  const size_t smem = 2 * (size_t)(chunk / group + 2) * sizeof(float);
-  DFL_CHECK_LAUNCH(launch(dfl::k_conv_pre<S>, dim3(rows, nchunk), dim3(256), smem, st, un, gpart,
-                          nsplit, rows, K, D, group, chunk, base, ub));
+int launch_conv_pre(const S *un, const float *gate, int rows, int K, int D, int group,
+                    const S *base, S *ub, cudaStream_t st) {
+  const int chunk = D >= 2048 ? 1024 : D;
+  DFL_CHECK_LAUNCH(launch(dfl::k_conv_pre<S>, dim3(rows, (D + chunk - 1) / chunk), dim3(128), 0,
+                          st, un, gate, K, D, group, chunk, base, ub));
   return DFLASH_OK;
 }
 template <typename S>
-int launch_conv_post_norm(const float *rf, const float *gpart, int nsplit, int rows, int K, int D,
-                          int group, const S *base, float *x, const S *gain, float eps, S *un,
-                          S *zf, cudaStream_t st) {
-  const size_t smem = ((size_t)D + 2 * (size_t)(D / group)) * sizeof(float);
+int launch_conv_post_norm(const float *rf, const float *gate, int rows, int K, int D, int group,
+                          const S *base, float *x, const S *gain, float eps, S *un, S *zf,
+                          cudaStream_t st) {
+  const size_t smem = (size_t)D * sizeof(float);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(dfl::k_conv_post_norm<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return DFLASH_ERR_CUDA;
   }
-  const int threads = D >= 4096 ? 1024 : D >= 1024 ? 512 : 256;
-  DFL_CHECK_LAUNCH(launch(dfl::k_conv_post_norm<S>, dim3(rows), dim3(threads), smem, st, rf,
-                          gpart, nsplit, rows, K, D, group, base, x, gain, eps, un, zf));
+  const int threads = D >= 4096 ? 512 : D >= 1024 ? 128 : 32;
+  DFL_CHECK_LAUNCH(launch(dfl::k_conv_post_norm<S>, dim3(rows), dim3(threads), smem, st, rf, gate,
+                          K, D, group, base, x, gain, eps, un, zf));
   return DFLASH_OK;
 }
 template <typename S>
-int launch_reduce(const float *part, int nsplit, int rows, int N, float *rf, S *rb,
-                  cudaStream_t st) {
-  const size_t n = (size_t)rows * N;
-  DFL_CHECK_LAUNCH(
-      launch(dfl::k_reduce<S>, dim3(grid_for(n)), dim3(256), 0, st, part, nsplit, n, rf, rb));
+int launch_qkv_post(const float *qkv, int rows, int K, int Hq, int Hkv, int dh, const S *qn,
+                    const S *kn, const int32_t *ctx_len, const RopeTable &rope, float eps, S *qb,
+                    S *kb, S *vb, cudaStream_t st) {
+  DFL_CHECK_LAUNCH(launch(dfl::k_qkv_post<S>, dim3(rows, Hq + 2 * Hkv), dim3(dh / 2), 0, st, qkv,
+                          rows, K, Hq, Hkv, dh, qn, kn, ctx_len, rope, eps, qb, kb, vb));
   return DFLASH_OK;
 }
 template <typename S>
-int launch_swiglu(const float *part, int nsplit, int rows, int F, S *hb, cudaStream_t st) {
-  const size_t n = (size_t)rows * F;
-  DFL_CHECK_LAUNCH(
-      launch(dfl::k_swiglu<S>, dim3(grid_for(n)), dim3(256), 0, st, part, nsplit, rows, F, hb));
-  return DFLASH_OK;
-}
-template <typename S>
-int launch_qkv_post(const float *part, int nsplit, int rows, int K, int Hq, int Hkv, int dh,
-                    const S *qn, const S *kn, const int32_t *ctx_len, const RopeTable &rope,
-                    float eps, S *qb, S *kb, S *vb, cudaStream_t st) {
-  DFL_CHECK_LAUNCH(launch(dfl::k_qkv_post<S>, dim3(rows, Hq + 2 * Hkv), dim3(dh / 2), 0, st, part,
-                          nsplit, rows, K, Hq, Hkv, dh, qn, kn, ctx_len, rope, eps, qb, kb, vb));
-  return DFLASH_OK;
-}
-template <typename S>
-int launch_inject_store(const float *kvpart, int nsplit, int N, int L, int Hkv, int dh,
-                        LayerPtrs knorm, const int32_t *req, const int32_t *pos,
-                        const int32_t *page_table, int num_rows, int max_pages, int num_pages,
-                        int page_size, const RopeTable &rope, float eps, S *kc, S *vc, int *err,
+int launch_inject_store(const float *kvf, int N, int L, int Hkv, int dh, LayerPtrs knorm,
+                        const int32_t *req, const int32_t *pos, const int32_t *page_table,
+                        int num_rows, int max_pages, int num_pages, int page_size,
+                        const RopeTable &rope, float eps, S *kc, S *vc, int *err,
                         cudaStream_t st) {
-  DFL_CHECK_LAUNCH(launch(dfl::k_inject_store<S>, dim3(N, L, 2 * Hkv), dim3(dh / 2), 0, st, kvpart,
-                          nsplit, N, L, Hkv, dh, knorm, req, pos, page_table, num_rows, max_pages,
-                          num_pages, page_size, rope, eps, kc, vc, err));
+  DFL_CHECK_LAUNCH(launch(dfl::k_inject_store<S>, dim3(N, L, 2 * Hkv), dim3(dh / 2), 0, st, kvf, N,
+                          L, Hkv, dh, knorm, req, pos, page_table, num_rows, max_pages, num_pages,
+                          page_size, rope, eps, kc, vc, err));
   return DFLASH_OK;
 }
 
@@ -423,17 +356,15 @@ int launch_inject_store(const float *kvpart, int nsplit, int N, int L, int Hkv, 
   template int launch_embed_norm<S>(const S *, const int32_t *, int, int, int, int, int, const S *, \
                                     float, float *, S *, int *, cudaStream_t);                   \
   template int launch_rows_norm<S>(const S *, int, int, const S *, float, S *, cudaStream_t);    \
-  template int launch_conv_pre<S>(const S *, const float *, int, int, int, int, int, const S *,  \
-                                  S *, cudaStream_t);                                            \
-  template int launch_conv_post_norm<S>(const float *, const float *, int, int, int, int, int,   \
+  template int launch_conv_pre<S>(const S *, const float *, int, int, int, int, const S *, S *,  \
+                                  cudaStream_t);                                                 \
+  template int launch_conv_post_norm<S>(const float *, const float *, int, int, int, int,        \
                                         const S *, float *, const S *, float, S *, S *,          \
                                         cudaStream_t);                                           \
-  template int launch_reduce<S>(const float *, int, int, int, float *, S *, cudaStream_t);       \
-  template int launch_swiglu<S>(const float *, int, int, int, S *, cudaStream_t);                \
-  template int launch_qkv_post<S>(const float *, int, int, int, int, int, int, const S *,        \
-                                  const S *, const int32_t *, const RopeTable &, float, S *, S *, \
-                                  S *, cudaStream_t);                                            \
-  template int launch_inject_store<S>(const float *, int, int, int, int, int, LayerPtrs,         \
+  template int launch_qkv_post<S>(const float *, int, int, int, int, int, const S *, const S *,  \
+                                  const int32_t *, const RopeTable &, float, S *, S *, S *,      \
+                                  cudaStream_t);                                                 \
+  template int launch_inject_store<S>(const float *, int, int, int, int, LayerPtrs,              \
                                       const int32_t *, const int32_t *, const int32_t *, int,    \
                                       int, int, int, const RopeTable &, float, S *, S *, int *,  \
                                       cudaStream_t);

@@ -22,27 +22,23 @@ int launch_embed_norm(const S *E, const int32_t *anchor, int mask_id, int V, int
 template <typename S>
 int launch_rows_norm(const S *in, int rows, int cols, const S *gain, float eps, S *out,
                      cudaStream_t st);
+// gate: the conv's gate linear, fp32 [rows, 2D/group]
 template <typename S>
-int launch_conv_pre(const S *un, const float *gpart, int nsplit, int rows, int K, int D,
-                    int group, const S *base, S *ub, cudaStream_t st);
+int launch_conv_pre(const S *un, const float *gate, int rows, int K, int D, int group,
+                    const S *base, S *ub, cudaStream_t st);
 template <typename S>
-int launch_conv_post_norm(const float *rf, const float *gpart, int nsplit, int rows, int K, int D,
-                          int group, const S *base, float *x, const S *gain, float eps, S *un,
-                          S *zf, cudaStream_t st);
+int launch_conv_post_norm(const float *rf, const float *gate, int rows, int K, int D, int group,
+                          const S *base, float *x, const S *gain, float eps, S *un, S *zf,
+                          cudaStream_t st);
 template <typename S>
-int launch_reduce(const float *part, int nsplit, int rows, int N, float *rf, S *rb,
-                  cudaStream_t st);
+int launch_qkv_post(const float *qkv, int rows, int K, int Hq, int Hkv, int dh, const S *qn,
+                    const S *kn, const int32_t *ctx_len, const RopeTable &rope, float eps, S *qb,
+                    S *kb, S *vb, cudaStream_t st);
 template <typename S>
-int launch_swiglu(const float *part, int nsplit, int rows, int F, S *hb, cudaStream_t st);
-template <typename S>
-int launch_qkv_post(const float *part, int nsplit, int rows, int K, int Hq, int Hkv, int dh,
-                    const S *qn, const S *kn, const int32_t *ctx_len, const RopeTable &rope,
-                    float eps, S *qb, S *kb, S *vb, cudaStream_t st);
-template <typename S>
-int launch_inject_store(const float *kvpart, int nsplit, int N, int L, int Hkv, int dh,
-                        LayerPtrs knorm, const int32_t *req, const int32_t *pos,
-                        const int32_t *page_table, int num_rows, int max_pages, int num_pages,
-                        int page_size, const RopeTable &rope, float eps, S *kc, S *vc, int *err,
+int launch_inject_store(const float *kvf, int N, int L, int Hkv, int dh, LayerPtrs knorm,
+                        const int32_t *req, const int32_t *pos, const int32_t *page_table,
+                        int num_rows, int max_pages, int num_pages, int page_size,
+                        const RopeTable &rope, float eps, S *kc, S *vc, int *err,
                         cudaStream_t st);
 
 }  // namespace dflh
