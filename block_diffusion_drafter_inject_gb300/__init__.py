@@ -14,6 +14,7 @@ from .api import (  # noqa: F401
     PagedKV,
     Workspace,
     accept_greedy,
+    accept_greedy_noalloc,
     clear_device_status,
     draft_block,
     inject_context,

@@ -143,6 +143,16 @@ def accept_greedy(path, target_logits, ws, accept_len, tokens, stream=None):
           "dflash_accept_greedy")
 
 
+def accept_greedy_noalloc(path, target_logits, accept_len, tokens, stream=None):
+    """dflash_accept_greedy without a workspace (fixed library-owned scratch;
+    B * K * ceil(V / 8192) <= 32768; overlapping calls race)."""
+    B, K, V = target_logits.shape
+    dt = _lib.F32 if target_logits.dtype == torch.float32 else _lib.BF16
+    check(lib().dflash_accept_greedy_noalloc(_ptr(path), _ptr(target_logits), dt, B, K, V,
+                                             _ptr(accept_len), _ptr(tokens), _stream(stream)),
+          "dflash_accept_greedy_noalloc")
+
+
 def linear_splits(N_out, T, K_in):
     return int(lib().dflash_linear_splits(N_out, T, K_in))
 

@@ -203,6 +203,28 @@ int dflash_accept_greedy(const int32_t *path, const void *target_logits,
                          int32_t *accept_len, int32_t *tokens, void *ws,
                          size_t ws_bytes, void *stream);
 
+/* Greedy acceptance for callers that cannot provide a workspace.  (The DFlash
+ * pages have no counterpart: this is a deployment variant of
+ * dflash_accept_greedy, with the same inputs, outputs and results.)
+ * Some callers cannot allocate device memory where acceptance runs: a runtime
+ * whose device memory is planned once at start-up and may not grow, a host
+ * binding without a device allocator, or code that must not call cudaMalloc
+ * at that point.  This entry point takes no workspace and allocates nothing:
+ * its scratch (argmax partials) is a fixed 256 KiB array in the library's own
+ * device memory, held by every GPU that loads the library until exit.
+ *   Limit: B * K * ceil(V / 8192) <= 32768, else DFLASH_ERR_WORKSPACE
+ *   (for V = 151936: B * K <= 1724).
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ *   Every call shares the one array: calls that overlap on the GPU (different
+ *   streams, or different host threads on one device) race and must be
+ *   serialised by the caller.  Each call writes every partial it reads, so no
+ *   clearing is needed between calls. */
+int dflash_accept_greedy_noalloc(const int32_t *path, const void *target_logits,
+                                 int32_t logits_dtype, int32_t B, int32_t K, int32_t V,
+                                 int32_t *accept_len, int32_t *tokens, void *stream);
+
 /* The projection GEMM every call above is built on (the drafter's dense
  * layers: nn.Linear without bias).  Slice s of `out` receives
  *   out[s][t][n] = sum over the s-th of `splits` equal K ranges of X[t][k] W[n][k]
