@@ -293,7 +293,7 @@ def run_gpu(args, rank, world, barrier, allmax):
 
     pb1 = pass_bytes(cfg, B, K, ctx)
     res = {
-        "metric": METRIC, "value": world * 1e3 / ms_cycle, "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": whole_job_value(world, ms_cycle), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_cycle,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) target hiddens, N(0,3) target logits)",
@@ -309,7 +309,7 @@ def run_gpu(args, rank, world, barrier, allmax):
                      "frac": gemm_gbs / pk["hbm"], "traffic": None,
                      "algorithmic_bytes_per_pass": gem_bytes, "us_per_pass": ms_gemm * 1e3,
                      "peak_source": pk["src"]},
-        "e2e": {"value": world * 1e3 / ms_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_value(world, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_cycle * args.steps,
         "launches_per_cycle": launches_per_cycle,
@@ -428,6 +428,40 @@ def run_reference(args):
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------------ replicas
+
+def replica_sync(world, device="cuda"):
+    """(barrier, allmax) over the ranks of an already-initialised process group.
+
+    Replicas share nothing on the data path: the only cross-rank traffic is
+    the barrier around the timed region and the max of the per-rank step
+    times (whole-job throughput = ranks x steps / slowest rank's time)."""
+    if world <= 1:
+        return None, (lambda x: x)
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        if device == "cuda":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl" if device == "cuda" else "gloo")
+
+    def barrier():
+        dist.barrier()
+
+    def allmax(x):
+        t = torch.tensor([float(x)], dtype=torch.float64,
+                         device=device if device == "cuda" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return barrier, allmax
+
+
+def whole_job_value(world, ms_per_step_max):
+    """Cycles per second over all replicas for the slowest rank's step time."""
+    return world * 1e3 / ms_per_step_max
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -451,22 +485,7 @@ def main():
             print(json.dumps(run_reference(args)))
         return
 
-    barrier = None
-    allmax = lambda x: x  # noqa: E731
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
-        dist.init_process_group("nccl")
-
-        def barrier():
-            dist.barrier()
-
-        def allmax(x):
-            t = torch.tensor([x], device="cuda", dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-
+    barrier, allmax = replica_sync(world, device="cuda")
     res, Wh = run_gpu(args, rank, world, barrier, allmax)
     if rank == 0:
         if not args.no_cpu_baseline:
