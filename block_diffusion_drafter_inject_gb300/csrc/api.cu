@@ -125,10 +125,15 @@ static int check_kv(const dflash_config *c, const dflash_kv *kv) {
 // ---------------------------------------------------------------------------
 constexpr int kMaxReduceSplits = 16;      // slices a reduce-mode GEMM may use
 constexpr size_t kTicketInts = 1 << 14;   // tile tickets of one reduce-mode GEMM
+constexpr size_t kTopkTicketInts = 1 << 14;  // row tickets of the top-k (B*(K-1) rows at most)
+// Fixed header of every workspace: status word, GEMM tile tickets, top-k row
+// tickets.  They must stay zero between calls; every other region is scratch
+// that a call fully writes before reading (acceptance's partials start here).
+constexpr size_t kHeaderBytes = 256 + kTicketInts * 4 + kTopkTicketInts * 4;
 
 struct Layout {
   size_t status, tickets, scratch;
-  size_t x, un, ub, rf, rb, gates, qkv, qb, kb, vb, ob, hb, zf, logits, attn, topk;
+  size_t x, un, ub, rf, rb, gates, qkv, qb, kb, vb, ob, hb, zf, logits, attn, topk, topk_tickets;
   size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf;
   size_t total;
   int S_gate, S_qkv, S_o, S_gu, S_down, S_sel, S_lm;
@@ -200,6 +205,7 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   sc = std::max(sc, inj(2 * Hkv * dh, D));
   L->status = take(256);
   L->tickets = take(kTicketInts * sizeof(int));
+  L->topk_tickets = take(kTopkTicketInts * sizeof(int));
   L->scratch = take(sc * 4);
   L->x = take((size_t)T * D * 4);
   L->un = take((size_t)T * D * es);
@@ -328,11 +334,20 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     TRY(gemm_run(reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.S_qkv, GEMM_REDUCE, qkv, QKVW,
                              nullptr, 0),
                  st));
-    TRY(launch_qkv_post<S>(qkv, T, K, Hq, Hkv, dh, (const S *)lw.q_norm, (const S *)lw.k_norm,
-                           ctx_len, rope, eps, qb, kb, vb, st));
-    TRY(launch_block_attention<S>(L.ap, qb, kb, vb, (const S *)kv.k, (const S *)kv.v, l,
-                                  kv.page_table, kv.max_pages_per_req, kv.num_pages, c.page_size,
-                                  ctx_len, B, K, Hq, Hkv, dh, c.window, attnp, ob, err, st));
+    if constexpr (sizeof(S) == 2) {
+      TRY(launch_attention_fused(L.ap, qkv, (const dfl::bf16 *)lw.q_norm,
+                                 (const dfl::bf16 *)lw.k_norm, rope, eps, (const dfl::bf16 *)kv.k,
+                                 (const dfl::bf16 *)kv.v, l, kv.page_table, kv.max_pages_per_req,
+                                 kv.num_pages, c.page_size, ctx_len, B, K, Hq, Hkv, dh, c.window,
+                                 (dfl::bf16 *)ob, err, st));
+    } else {
+      TRY(launch_qkv_post<S>(qkv, T, K, Hq, Hkv, dh, (const S *)lw.q_norm, (const S *)lw.k_norm,
+                             ctx_len, rope, eps, qb, kb, vb, st));
+      TRY(launch_block_attention<S>(L.ap, qb, kb, vb, (const S *)kv.k, (const S *)kv.v, l,
+                                    kv.page_table, kv.max_pages_per_req, kv.num_pages,
+                                    c.page_size, ctx_len, B, K, Hq, Hkv, dh, c.window, attnp, ob,
+                                    err, st));
+    }
     TRY(gemm_run(reduce_call(c, ws, L, lw.wo, D, Hq * dh, ob, T, L.S_o, GEMM_REDUCE, rf, D, rb, D),
                  st));
     TRY(gate_gemm(lw.conv_w[1], rb));
@@ -355,7 +370,7 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   const int TL = B * (K - 1);
   TRY(gemm_run(reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, 1, GEMM_REDUCE, logits, V, nullptr, 0),
                st));
-  TRY(launch_topk(logits, TL, V, c.top_k, topkp, ids, logp, st));
+  TRY(launch_topk(logits, TL, V, c.top_k, topkp, (int *)(ws + L.topk_tickets), ids, logp, st));
   return DFLASH_OK;
 }
 
@@ -423,6 +438,7 @@ int dflash_draft_block(const dflash_config *cfg, const dflash_weights *w, const 
   if (rc != DFLASH_OK) return rc;
   if (B < 0 || K < 2 || K > DFLASH_MAX_BLOCK) return DFLASH_ERR_BLOCK;
   if (B == 0) return DFLASH_OK;
+  if ((size_t)B * (K - 1) > kTopkTicketInts) return DFLASH_ERR_DIMS;
   if (!anchor || !ctx_len || !topk_ids || !topk_logp || !ws) return DFLASH_ERR_NULL;
   if ((rc = check_weights(cfg, w, true)) != DFLASH_OK) return rc;
   if ((rc = check_kv(cfg, kv)) != DFLASH_OK) return rc;
@@ -472,12 +488,13 @@ int dflash_accept_greedy(const int32_t *path, const void *target_logits, int32_t
   if (B == 0) return DFLASH_OK;
   if (!path || !target_logits || !accept_len || !tokens || !ws) return DFLASH_ERR_NULL;
   if (!a16(ws)) return DFLASH_ERR_ALIGN;
-  // status word + argmax partials
-  const size_t need = 256 + (((size_t)B * K * argmax_chunks(V) * 2 * 4 + 255) & ~(size_t)255);
+  // argmax partials after the fixed header (scratch shared with the other calls)
+  const size_t need = kHeaderBytes + (size_t)B * K * argmax_chunks(V) * 2 * 4;
   if (ws_bytes < need) return DFLASH_ERR_WORKSPACE;
   if (!device()) return DFLASH_ERR_DEVICE;
-  return launch_accept(path, target_logits, logits_dtype, B, K, V, (float *)((uint8_t *)ws + 256),
-                       accept_len, tokens, (cudaStream_t)stream);
+  return launch_accept(path, target_logits, logits_dtype, B, K, V,
+                       (float *)((uint8_t *)ws + kHeaderBytes), accept_len, tokens,
+                       (cudaStream_t)stream);
 }
 
 int dflash_linear(int32_t dtype, const void *W, int32_t N_out, int32_t K_in, const void *X,

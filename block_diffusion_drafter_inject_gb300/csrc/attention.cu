@@ -9,6 +9,7 @@
 #include <math.h>
 
 #include "attention.cuh"
+#include "pointwise.cuh"
 
 namespace dfl {
 
@@ -198,82 +199,203 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *(uint32_t *)&h;
 }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t local_addr, uint32_t rank) {
+  uint32_t ra;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_dsmem_v2(uint32_t local_addr, uint32_t rank, float a, float b) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(ra), "f"(a), "f"(b) : "memory");
+}
+__device__ __forceinline__ void st_dsmem(uint32_t local_addr, uint32_t rank, float a) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(a) : "memory");
+}
+
+// Up to R head rows of the fp32 QKV projection -> RMSNorm(gain) -> RoPE(pos)
+// -> bf16 into swizzled shared rows; one warp, lane holds d = lane + 32e.  All
+// global loads of the batch are issued before any arithmetic.
+//   src[q]: row q's projection (nullptr: write zeros); pos[q]: its position.
+template <int DH, int R>
+__device__ __forceinline__ void norm_rope_rows(const float *const *src, const int *pos,
+                                               const int *dst_row, int nrows, const bf16 *gain,
+                                               bool rope_on, const dflh::RopeTable &rope,
+                                               float eps, uint8_t *base, int RB, int lane) {
+  constexpr int E = DH / 32;
+  float v[R][E];
+#pragma unroll
+  for (int q = 0; q < R; ++q)
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      v[q][e] = (q < nrows && src[q]) ? src[q][lane + 32 * e] : 0.f;
+  float g[E];
+  if (gain) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) g[e] = __bfloat162float(gain[lane + 32 * e]);
+  }
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    if (q >= nrows) break;
+    if (gain && src[q]) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ss += v[q][e] * v[q][e];
+      ss = warp_sum(ss);
+      const float inv = rsqrtf(ss / DH + eps);
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[q][e] = v[q][e] * inv * g[e];
+      if (rope_on) {
+        const double two_pi = 6.283185307179586476925286766559;
+#pragma unroll
+        for (int e = 0; e < E / 2; ++e) {
+          const int i = lane + 32 * e;  // pairs (i, i + DH/2)
+          const double a = (double)pos[q] * rope.inv_freq[i];
+          const float ar = (float)(a - two_pi * floor(a * (1.0 / two_pi)));
+          float sn, cs;
+          sincosf(ar, &sn, &cs);
+          const float lo = v[q][e], hi = v[q][e + E / 2];
+          v[q][e] = lo * cs - hi * sn;
+          v[q][e + E / 2] = hi * cs + lo * sn;
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int d = lane + 32 * e;
+      *(bf16 *)(base + swz(dst_row[q], d >> 3, RB) + (d & 7) * 2) = __float2bfloat16_rn(v[q][e]);
+    }
+  }
+}
+
+struct AttnArgs {
+  const float *qkv;  // [B*K, (Hq + 2Hkv) * DH] fp32
+  const bf16 *q_norm, *k_norm;
+  const bf16 *kc, *vc;
+  size_t layer_off;
+  const int32_t *table;
+  int max_pages, num_pages, P;
+  const int32_t *ctx_len;
+  int K, Hq, Hkv, window, kps, nsplit, nqg;
+  float eps;
+  bf16 *ob;  // [B*K, Hq*DH]
+  int *err;
+};
+
+// grid (nsplit, Hkv, B*nqg), cluster (nsplit, 1, 1); block 128 (4 warps x 16 rows).
 template <int DH>
-__global__ void __launch_bounds__(128) k_attn_mma(
-    const bf16 *__restrict__ qb, const bf16 *__restrict__ kb, const bf16 *__restrict__ vb,
-    const bf16 *__restrict__ kc, const bf16 *__restrict__ vc, size_t layer_off,
-    const int32_t *__restrict__ table, int max_pages, int num_pages, int P,
-    const int32_t *__restrict__ ctx_len, int K, int Hq, int Hkv, int window, int kps, int nsplit,
-    int nqg, float *__restrict__ part, int *err) {
+__global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::RopeTable rope) {
   constexpr int CH = kCH;          // keys per tile
   constexpr int CHUNKS = DH / 8;   // 16-byte chunks per row
   constexpr int RB = DH * 2;       // bytes per row
   constexpr int TILE = CH * RB;    // bytes per K (or V) tile
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int s_valid[2][CH];
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK0 = sQ + kQG * RB;
-  const uint32_t sV0 = sK0 + 2 * TILE;
+  uint8_t *pQ = smem;
+  uint8_t *pK0 = smem + kQG * RB;
+  uint8_t *pV0 = pK0 + 2 * TILE;
+  uint8_t *pRecv = pV0 + 2 * TILE;  // [nsplit][per][DH + 2] fp32, written by the peers
+  const uint32_t sQ = smem_u32(pQ), sK0 = smem_u32(pK0), sV0 = smem_u32(pV0);
   pdl_launch();
   pdl_wait();
 
   const int split = blockIdx.x, kvh = blockIdx.y;
-  const int b = blockIdx.z / nqg, qgi = blockIdx.z % nqg;
-  const int grp = Hq / Hkv, QR = K * grp;
-  const int ctx = ctx_len[b];
-  const int n_ctx = ctx < window ? (ctx > 0 ? ctx : 0) : window;
-  const int lo = ctx - n_ctx, n_keys = n_ctx + K;
-  const int k_begin = split * kps;
-  if (k_begin >= n_keys) return;
-  const int k_end = min(n_keys, k_begin + kps);
-  const int ntiles = (k_end - k_begin + CH - 1) / CH;
+  const int b = blockIdx.z / A.nqg, qgi = blockIdx.z % A.nqg;
+  const int grp = A.Hq / A.Hkv, QR = A.K * grp;
+  const int QKVW = (A.Hq + 2 * A.Hkv) * DH;
+  const int ctx = A.ctx_len[b];
+  const int n_ctx = ctx < A.window ? (ctx > 0 ? ctx : 0) : A.window;
+  const int lo = ctx - n_ctx, n_keys = n_ctx + A.K;
+  const int k_begin = split * A.kps;
+  const int k_end = min(n_keys, k_begin + A.kps);
+  const int ntiles = k_begin < n_keys ? (k_end - k_begin + CH - 1) / CH : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool rope_on = rope.enabled != 0;
 
-  // query rows qr = i*grp + g of this group
-  for (int e = tid; e < kQG * CHUNKS; e += 128) {
-    const int qr = e / CHUNKS, c = e % CHUNKS;
-    const int qrg = qgi * kQG + qr;
-    const bf16 *src = qb;
-    int bytes = 0;
-    if (qrg < QR) {
-      const int i = qrg / grp, g = qrg % grp;
-      src = qb + ((size_t)(b * K + i) * Hq + kvh * grp + g) * DH + c * 8;
-      bytes = 16;
+  // queries: head norm + RoPE of the projection rows, qr = i*grp + g; warp w
+  // stages rows 16w .. 16w+15 in two batches of 8
+  for (int half = 0; half < 2; ++half) {
+    const float *src[8];
+    int pos[8], dst[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int row = warp * 16 + half * 8 + q, qrg = qgi * kQG + row;
+      dst[q] = row;
+      src[q] = nullptr;
+      pos[q] = 0;
+      if (qrg < QR) {
+        const int i = qrg / grp, g = qrg % grp;
+        src[q] = A.qkv + (size_t)(b * A.K + i) * QKVW + (size_t)(kvh * grp + g) * DH;
+        pos[q] = ctx + i;
+      }
     }
-    cp_async16(sQ + swz(qr, c, RB), src, bytes);
+    norm_rope_rows<DH, 8>(src, pos, dst, 8, A.q_norm, rope_on, rope, A.eps, pQ, RB, lane);
   }
   auto load_tile = [&](int t, int stage) {
     const int t0 = k_begin + t * CH;
     for (int e = tid; e < CH * CHUNKS; e += 128) {
       const int j = e / CHUNKS, c = e % CHUNKS;
       const int key = t0 + j;
-      const bf16 *srck = kc, *srcv = vc;
+      if (key >= n_ctx && key < k_end) continue;  // block slot: computed below
+      const bf16 *srck = A.kc, *srcv = A.vc;
       int ok = 0;
       if (key < k_end) {
-        if (key < n_ctx) {
-          const int p = lo + key, pi = p / P;
-          const int page = pi < max_pages ? table[(size_t)b * max_pages + pi] : -1;
-          if (page >= 0 && page < num_pages) {
-            const size_t off = layer_off + (((size_t)page * Hkv + kvh) * P + (p % P)) * DH + c * 8;
-            srck = kc + off;
-            srcv = vc + off;
-            ok = 1;
-          } else if (c == 0) {
-            set_err(err, pi < max_pages ? DFLASH_DEV_PAGE_RANGE : DFLASH_DEV_POS_RANGE);
-          }
-        } else {
-          const size_t off = ((size_t)(b * K + key - n_ctx) * Hkv + kvh) * DH + c * 8;
-          srck = kb + off;
-          srcv = vb + off;
+        const int p = lo + key, pi = p / A.P;
+        const int page = pi < A.max_pages ? A.table[(size_t)b * A.max_pages + pi] : -1;
+        if (page >= 0 && page < A.num_pages) {
+          const size_t off =
+              A.layer_off + (((size_t)page * A.Hkv + kvh) * A.P + (p % A.P)) * DH + c * 8;
+          srck = A.kc + off;
+          srcv = A.vc + off;
           ok = 1;
+        } else if (c == 0) {
+          set_err(A.err, pi < A.max_pages ? DFLASH_DEV_PAGE_RANGE : DFLASH_DEV_POS_RANGE);
         }
       }
       cp_async16(sK0 + stage * TILE + swz(j, c, RB), srck, ok ? 16 : 0);
       cp_async16(sV0 + stage * TILE + swz(j, c, RB), srcv, ok ? 16 : 0);
       if (c == 0) s_valid[stage][j] = ok;
     }
+    // block slots of this tile: k = RoPE(k_norm(.)), v as projected; warp w takes
+    // the block rows j = w, w+4, ... (batches of 4)
+    {
+      const int jb0 = max(0, n_ctx - t0), jb1 = min(CH, k_end - t0);  // block rows [jb0, jb1)
+      for (int j0 = jb0 + warp * 4; j0 < jb1; j0 += 16) {
+        const float *sk[4], *sv[4];
+        int pos[4], dst[4];
+        const int nr = min(4, jb1 - j0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = j0 + q, i = t0 + j - n_ctx;
+          dst[q] = j;
+          pos[q] = ctx + i;
+          const float *row = A.qkv + (size_t)(b * A.K + (q < nr ? i : 0)) * QKVW;
+          sk[q] = row + (size_t)(A.Hq + kvh) * DH;
+          sv[q] = row + (size_t)(A.Hq + A.Hkv + kvh) * DH;
+        }
+        norm_rope_rows<DH, 4>(sk, pos, dst, nr, A.k_norm, rope_on, rope, A.eps,
+                              pK0 + stage * TILE, RB, lane);
+        norm_rope_rows<DH, 4>(sv, pos, dst, nr, nullptr, false, rope, A.eps, pV0 + stage * TILE,
+                              RB, lane);
+        if (lane < nr) s_valid[stage][j0 + lane] = 1;
+      }
+    }
   };
-  load_tile(0, 0);
+  if (ntiles > 0) load_tile(0, 0);
   cp_async_commit();
 
   const bool active = qgi * kQG + warp * 16 < QR;
@@ -316,7 +438,6 @@ __global__ void __launch_bounds__(128) k_attn_mma(
           mma_bf16_16816(sc[2 * jp + 1], qf[kk], b2, b3);
         }
       }
-      // mask, scale, running max
       const int t0 = k_begin + t * CH;
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -340,19 +461,23 @@ __global__ void __launch_bounds__(128) k_attn_mma(
         m_run[h] = mnew;
       }
       float ls[2] = {0.f, 0.f};
-      uint32_t pa[CH / 16][4];
+      // probabilities as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)):
+      // two products with V keep P at ~16 significant bits
+      uint32_t pa[CH / 16][4], pl[CH / 16][4];
 #pragma unroll
       for (int j = 0; j < CH / 8; ++j) {
-        float p[4];
+        float p[4], r[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float mm = m_run[e >> 1];
           p[e] = (sc[j][e] == -INFINITY) ? 0.f : exp2f(sc[j][e] - mm);
           ls[e >> 1] += p[e];
+          r[e] = p[e] - __bfloat162float(__float2bfloat16_rn(p[e]));
         }
-        // scores of n-tile j become the A operand of P.V (keys 16*(j/2) ..)
         pa[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p[0], p[1]);
         pa[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p[2], p[3]);
+        pl[j >> 1][(j & 1) * 2 + 0] = pack_bf16(r[0], r[1]);
+        pl[j >> 1][(j & 1) * 2 + 1] = pack_bf16(r[2], r[3]);
       }
       l_run[0] = l_run[0] * alpha[0] + ls[0];
       l_run[1] = l_run[1] * alpha[1] + ls[1];
@@ -371,35 +496,69 @@ __global__ void __launch_bounds__(128) k_attn_mma(
           ldsm_x4_t(sV + swz(16 * kk + (mi & 1) * 8 + r8, 2 * np + (mi >> 1), RB), b0, b1, b2, b3);
           mma_bf16_16816(o[2 * np], pa[kk], b0, b1);
           mma_bf16_16816(o[2 * np + 1], pa[kk], b2, b3);
+          mma_bf16_16816(o[2 * np], pl[kk], b0, b1);
+          mma_bf16_16816(o[2 * np + 1], pl[kk], b2, b3);
         }
       }
     }
     __syncthreads();
   }
-  if (!active) return;
-  // quad-reduce the row sums and write this split's state
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // Combine through the cluster: query row `row` is finished by CTA
+  // owner = row / per.  Every CTA pushes its (m, l, o) of that row into the
+  // owner's receive buffer recv[split][row - owner*per][0..DH+1] with posted
+  // distributed-shared-memory stores; one cluster barrier; each owner then
+  // merges its rows from local shared memory.
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
   }
-  const float ln2 = 0.6931471805599453f;
+  const int nrows = min(kQG, QR - qgi * kQG);
+  const int per = (nrows + A.nsplit - 1) / A.nsplit;
+  const uint32_t recv = smem_u32(pRecv);
+  constexpr int RS = DH + 2;  // floats per received row
+  if (active) {
+    const float ln2 = 0.6931471805599453f;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int row = warp * 16 + g8 + 8 * h;
-    const size_t base = ((((size_t)b * nqg + qgi) * Hkv + kvh) * nsplit + split) * kQG + row;
-    float *po = part + base * (DH + 2);
-    if (t4 == 0) {
-      po[0] = m_run[h] == -INFINITY ? -INFINITY : m_run[h] * ln2;
-      po[1] = l_run[h];
-    }
+    for (int h = 0; h < 2; ++h) {
+      const int row = warp * 16 + g8 + 8 * h;
+      if (row < nrows) {
+        const int owner = row / per, lr = row - owner * per;
+        const uint32_t dst = recv + (uint32_t)(((split * per) + lr) * RS) * 4u;
+        if (t4 == 0) {
+          st_dsmem(dst, owner, m_run[h] == -INFINITY ? -INFINITY : m_run[h] * ln2);
+          st_dsmem(dst + 4, owner, l_run[h]);
+        }
 #pragma unroll
-    for (int n = 0; n < DH / 8; ++n) {
-      po[2 + 8 * n + 2 * t4] = o[n][2 * h];
-      po[2 + 8 * n + 2 * t4 + 1] = o[n][2 * h + 1];
+        for (int n = 0; n < DH / 8; ++n)
+          st_dsmem_v2(dst + (uint32_t)(2 + 8 * n + 2 * t4) * 4u, owner, o[n][2 * h],
+                      o[n][2 * h + 1]);
+      }
     }
   }
+  cluster_sync();
+  const int r0 = split * per, r1 = min(nrows, r0 + per);
+  const float *rv = (const float *)pRecv;
+  for (int e = tid; e < (r1 - r0) * DH; e += 128) {
+    const int lr = e / DH, d = e % DH;
+    float M = -INFINITY;
+    for (int q = 0; q < A.nsplit; ++q) M = fmaxf(M, rv[(q * per + lr) * RS]);
+    float L = 0.f, O = 0.f;
+    for (int q = 0; q < A.nsplit; ++q) {
+      const float *src = rv + (q * per + lr) * RS;
+      if (src[0] == -INFINITY) continue;
+      const float w = expf(src[0] - M);
+      L += w * src[1];
+      O += w * src[2 + d];
+    }
+    const int qrg = qgi * kQG + r0 + lr, i = qrg / grp, g = qrg % grp;
+    A.ob[((size_t)(b * A.K + i) * A.Hq + kvh * grp + g) * DH + d] = __float2bfloat16_rn(O / L);
+  }
 }
+
 
 // o[r][h*dh + d] = sum_s e^{m_s - M} O_s / sum_s e^{m_s - M} l_s.  grid (B*K, Hq), block dh.
 template <typename S>
@@ -441,9 +600,12 @@ AttnPlan attn_plan(int B, int K, int Hq, int Hkv, int dh, int window, int num_sm
   pl.nqg = (QR + dfl::kQG - 1) / dfl::kQG;
   const int n_keys = window + K;
   const long items = (long)B * Hkv * pl.nqg;
-  // smallest key split (multiple of 64) that still gives ~2 CTAs per SM
+  // smallest key split (multiple of 64) that still gives ~2 CTAs per SM, and at
+  // most 8 splits (the splits of one item form a thread-block cluster)
   int kps = dfl::kCH;
-  while ((long)items * ((n_keys + kps - 1) / kps) > 2L * num_sms && kps < n_keys) kps += dfl::kCH;
+  while (kps < n_keys && ((long)items * ((n_keys + kps - 1) / kps) > 2L * num_sms ||
+                          (n_keys + kps - 1) / kps > 8))
+    kps += dfl::kCH;
   pl.kps = kps;
   pl.nsplit = (n_keys + kps - 1) / kps;
   pl.part_floats = (size_t)B * pl.nqg * Hkv * pl.nsplit * dfl::kQG * (dh + 2);
@@ -455,38 +617,99 @@ static int launch_attn_dh(const AttnPlan &pl, const S *qb, const S *kb, const S 
                           const S *vc, int layer, const int32_t *table, int max_pages,
                           int num_pages, int P, const int32_t *ctx_len, int B, int K, int Hq,
                           int Hkv, int window, float *part, S *ob, int *err, cudaStream_t st) {
+  // float32 storage: CUDA-core split kernel + combine
   const size_t layer_off = (size_t)layer * num_pages * Hkv * P * DH;
-  if constexpr (sizeof(S) == 2) {
-    const size_t smem = (size_t)dfl::kQG * DH * 2 + 4 * (size_t)dfl::kCH * DH * 2;
-    static int attr_done = 0;
-    if (!attr_done) {
-      if (cudaFuncSetAttribute(dfl::k_attn_mma<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem) != cudaSuccess)
-        return DFLASH_ERR_CUDA;
-      attr_done = 1;
-    }
-    DFL_CHECK_LAUNCH(launch(dfl::k_attn_mma<DH>, dim3(pl.nsplit, Hkv, B * pl.nqg), dim3(128), smem,
-                            st, qb, kb, vb, kc, vc, layer_off, table, max_pages, num_pages, P,
-                            ctx_len, K, Hq, Hkv, window, pl.kps, pl.nsplit, pl.nqg, part, err));
-  } else {
-    constexpr int LD = DH + 1;
-    const size_t smem = sizeof(float) * ((size_t)dfl::kQG * LD + 2 * (size_t)dfl::kCH * LD +
-                                         (size_t)dfl::kQG * (dfl::kCH + 1));
-    static int attr_done = 0;
-    if (!attr_done) {
-      if (cudaFuncSetAttribute(dfl::k_attn_split<S, DH>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return DFLASH_ERR_CUDA;
-      attr_done = 1;
-    }
-    DFL_CHECK_LAUNCH(launch(dfl::k_attn_split<S, DH>, dim3(pl.nsplit, Hkv, B * pl.nqg), dim3(256),
-                            smem, st, qb, kb, vb, kc, vc, layer_off, table, max_pages, num_pages, P,
-                            ctx_len, K, Hq, Hkv, window, pl.kps, pl.nsplit, pl.nqg, part, err));
+  constexpr int LD = DH + 1;
+  const size_t smem = sizeof(float) * ((size_t)dfl::kQG * LD + 2 * (size_t)dfl::kCH * LD +
+                                       (size_t)dfl::kQG * (dfl::kCH + 1));
+  static int attr_done = 0;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(dfl::k_attn_split<S, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_done = 1;
   }
+  DFL_CHECK_LAUNCH(launch(dfl::k_attn_split<S, DH>, dim3(pl.nsplit, Hkv, B * pl.nqg), dim3(256),
+                          smem, st, qb, kb, vb, kc, vc, layer_off, table, max_pages, num_pages, P,
+                          ctx_len, K, Hq, Hkv, window, pl.kps, pl.nsplit, pl.nqg, part, err));
   DFL_CHECK_LAUNCH(launch(dfl::k_attn_combine<S>, dim3(B * K, Hq), dim3(DH), 0, st,
                           (const float *)part, ctx_len, K, Hq, Hkv, DH, window, pl.kps, pl.nsplit,
                           pl.nqg, ob));
   return DFLASH_OK;
+}
+
+template <int DH>
+static int launch_attn_fused(const AttnPlan &pl, const float *qkv, const dfl::bf16 *qn,
+                             const dfl::bf16 *kn, const RopeTable &rope, float eps,
+                             const dfl::bf16 *kc, const dfl::bf16 *vc, int layer,
+                             const int32_t *table, int max_pages, int num_pages, int P,
+                             const int32_t *ctx_len, int B, int K, int Hq, int Hkv, int window,
+                             dfl::bf16 *ob, int *err, cudaStream_t st) {
+  // Q, two K and two V tiles, and the receive buffer: nsplit * ceil(rows/nsplit)
+  // <= kQG + 8 rows of DH + 2 floats
+  const size_t smem = (size_t)dfl::kQG * DH * 2 + 4 * (size_t)dfl::kCH * DH * 2 +
+                      (size_t)(dfl::kQG + 8) * (DH + 2) * 4;
+  static int attr_done = 0;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(dfl::k_attn_mma<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_done = 1;
+  }
+  dfl::AttnArgs a;
+  a.qkv = qkv;
+  a.q_norm = qn;
+  a.k_norm = kn;
+  a.kc = kc;
+  a.vc = vc;
+  a.layer_off = (size_t)layer * num_pages * Hkv * P * DH;
+  a.table = table;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.P = P;
+  a.ctx_len = ctx_len;
+  a.K = K;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.window = window;
+  a.kps = pl.kps;
+  a.nsplit = pl.nsplit;
+  a.nqg = pl.nqg;
+  a.eps = eps;
+  a.ob = ob;
+  a.err = err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.nsplit, Hkv, B * pl.nqg);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pl.nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  count_launch();
+  DFL_CHECK_LAUNCH(cudaLaunchKernelEx(&cfg, dfl::k_attn_mma<DH>, a, rope));
+  return DFLASH_OK;
+}
+
+int launch_attention_fused(const AttnPlan &pl, const float *qkv, const dfl::bf16 *qn,
+                           const dfl::bf16 *kn, const RopeTable &rope, float eps,
+                           const dfl::bf16 *kc, const dfl::bf16 *vc, int layer,
+                           const int32_t *table, int max_pages, int num_pages, int P,
+                           const int32_t *ctx_len, int B, int K, int Hq, int Hkv, int dh,
+                           int window, dfl::bf16 *ob, int *err, cudaStream_t st) {
+  if (dh == 128)
+    return launch_attn_fused<128>(pl, qkv, qn, kn, rope, eps, kc, vc, layer, table, max_pages,
+                                  num_pages, P, ctx_len, B, K, Hq, Hkv, window, ob, err, st);
+  if (dh == 64)
+    return launch_attn_fused<64>(pl, qkv, qn, kn, rope, eps, kc, vc, layer, table, max_pages,
+                                 num_pages, P, ctx_len, B, K, Hq, Hkv, window, ob, err, st);
+  return DFLASH_ERR_DIMS;
 }
 
 template <typename S>

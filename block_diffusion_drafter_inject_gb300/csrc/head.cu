@@ -36,15 +36,63 @@ __device__ __forceinline__ VI block_best(VI a, float *redv, int *redi) {
   return warp_best(b);
 }
 
+// Merge the nch chunk partials of one row (one warp): top-k ids and
+// logp = logit - logsumexp.  cand: 3 * nch * k words of shared scratch.
+__device__ __forceinline__ void topk_merge_row(const float *__restrict__ pr, int nch, int k,
+                                               int32_t *__restrict__ ids,
+                                               float *__restrict__ logp, float *cand, int lane) {
+  const int n = nch * k;
+  float *cval = cand;
+  int *cid = (int *)(cval + n);
+  int *ctk = cid + n;
+  float M = -INFINITY;
+  for (int c = lane; c < nch; c += 32) M = fmaxf(M, __ldcg(pr + (size_t)c * (2 * k + 2)));
+  M = warp_max(M);
+  float S = 0.f;
+  for (int c = lane; c < nch; c += 32) {
+    const float *p = pr + (size_t)c * (2 * k + 2);
+    const float m = __ldcg(p);
+    S += m == -INFINITY ? 0.f : __ldcg(p + 1) * expf(m - M);
+  }
+  S = warp_sum(S);
+  const float lse = M + logf(S);
+  for (int e = lane; e < n; e += 32) {
+    const int c = e / k, j = e % k;
+    const float *p = pr + (size_t)c * (2 * k + 2);
+    cval[e] = __ldcg(p + 2 + j);
+    cid[e] = __float_as_int(__ldcg(p + 2 + k + j));
+    ctk[e] = 0;
+  }
+  __syncwarp();
+  for (int it = 0; it < k; ++it) {
+    VI best{-INFINITY, 0x7fffffff};
+    int where = -1;
+    for (int e = lane; e < n; e += 32)
+      if (!ctk[e] && better(cval[e], cid[e], best.v, best.i))
+        best.v = cval[e], best.i = cid[e], where = e;
+    const VI win = warp_best(best);
+    if (where >= 0 && best.i == win.i) ctk[where] = 1;
+    if (lane == 0) {
+      ids[it] = win.i;
+      logp[it] = win.v - lse;
+    }
+    __syncwarp();
+  }
+}
+
 // One chunk (8 warps x 1024 logits) of one row: max, sum of exp and top-k.
 // Each warp selects its own top-k in registers (32 values per lane, k rounds
-// of a warp-wide best), then warp 0 merges the 8 warp lists.
-// partial layout per (row, chunk): [m, s, v_0..v_{k-1}, id_0..id_{k-1}]
-__global__ void __launch_bounds__(256) k_topk_partial(const float *__restrict__ logits, int V,
-                                                      int k, float *__restrict__ partial) {
+// of a warp-wide best), then warp 0 merges the 8 warp lists and writes the
+// chunk's partial [m, s, v_0..v_{k-1}, id_0..id_{k-1}].  The CTA that finishes
+// a row's last chunk (a ticket per row, no waiting) merges the row.
+__global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int V, int k,
+                                              float *__restrict__ partial, int *tickets,
+                                              int32_t *__restrict__ ids,
+                                              float *__restrict__ logp) {
   __shared__ float cv[8 * DFLASH_MAX_TOPK];
   __shared__ int ci[8 * DFLASH_MAX_TOPK];
   __shared__ float wm[8], wsum[8];
+  extern __shared__ float cand[];
   pdl_launch();
   pdl_wait();
   const int chunk = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
@@ -98,7 +146,8 @@ __global__ void __launch_bounds__(256) k_topk_partial(const float *__restrict__ 
     int bq = -1;
     for (int q = 0; q * 32 + lane < nc; ++q) {
       const int e = q * 32 + lane;
-      if (!((tk >> q) & 1u) && better(cv[e], ci[e], best.v, best.i)) best.v = cv[e], best.i = ci[e], bq = q;
+      if (!((tk >> q) & 1u) && better(cv[e], ci[e], best.v, best.i))
+        best.v = cv[e], best.i = ci[e], bq = q;
     }
     const VI win = warp_best(best);
     if (bq >= 0 && best.i == win.i) tk |= 1u << bq;
@@ -107,55 +156,19 @@ __global__ void __launch_bounds__(256) k_topk_partial(const float *__restrict__ 
       out[2 + k + it] = __int_as_float(win.i);
     }
   }
-}
-
-// Merge the chunks of one row (one warp per row): top-k ids and
-// logp = logit - logsumexp.  Candidates staged in shared memory.
-__global__ void __launch_bounds__(128) k_topk_merge(const float *__restrict__ partial, int rows,
-                                                    int nch, int k, int32_t *__restrict__ ids,
-                                                    float *__restrict__ logp) {
-  extern __shared__ float cand[];  // per warp: [nch*k] values, [nch*k] ids, [nch*k] taken
-  pdl_launch();
-  pdl_wait();
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + w;
-  const int n = nch * k;
-  float *cval = cand + (size_t)w * 3 * n;
-  int *cid = (int *)(cval + n);
-  int *ctk = cid + n;
-  if (row >= rows) return;
-  const float *pr = partial + (size_t)row * nch * (2 * k + 2);
-  float M = -INFINITY;
-  for (int c = lane; c < nch; c += 32) M = fmaxf(M, pr[(size_t)c * (2 * k + 2)]);
-  M = warp_max(M);
-  float S = 0.f;
-  for (int c = lane; c < nch; c += 32) {
-    const float *p = pr + (size_t)c * (2 * k + 2);
-    S += p[0] == -INFINITY ? 0.f : p[1] * expf(p[0] - M);
-  }
-  S = warp_sum(S);
-  const float lse = M + logf(S);
-  for (int e = lane; e < n; e += 32) {
-    const int c = e / k, j = e % k;
-    const float *p = pr + (size_t)c * (2 * k + 2);
-    cval[e] = p[2 + j];
-    cid[e] = __float_as_int(p[2 + k + j]);
-    ctk[e] = 0;
-  }
+  // ticket: the last chunk of the row merges it
+  __threadfence();
   __syncwarp();
-  for (int it = 0; it < k; ++it) {
-    VI best{-INFINITY, 0x7fffffff};
-    int where = -1;
-    for (int e = lane; e < n; e += 32)
-      if (!ctk[e] && better(cval[e], cid[e], best.v, best.i)) best.v = cval[e], best.i = cid[e], where = e;
-    const VI win = warp_best(best);
-    if (where >= 0 && best.i == win.i) ctk[where] = 1;
-    if (lane == 0) {
-      ids[(size_t)row * k + it] = win.i;
-      logp[(size_t)row * k + it] = win.v - lse;
-    }
-    __syncwarp();
+  int last = 0;
+  if (lane == 0) {
+    last = atomicAdd(&tickets[row], 1) == nch - 1;
+    if (last) tickets[row] = 0;
   }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  topk_merge_row(partial + (size_t)row * nch * (2 * k + 2), nch, k, ids + (size_t)row * k,
+                 logp + (size_t)row * k, cand, lane);
 }
 
 // rows[b*R + j] = E[token j of request b]: j = 0 the anchor, j >= 1 the
@@ -188,13 +201,13 @@ __global__ void __launch_bounds__(256) k_sel_gather(const S *__restrict__ E,
 
 // Pair scores of every adjacent candidate pair, all positions at once:
 //   pair[b][t][i][j] = u(pred_i) . v(c_tj),  pred = the anchor at t = 0, else c_{t-1}
-// u = P_u e and v = P_v e are rows of the (reduced) selector projections, r wide.
-// grid (K-1, B); shared: 2 * k * (r + 4) floats.
+// u = P_u e and v = P_v e are rows of the selector projections, r wide.
+// grid (K-1, B): rows staged in shared memory, one thread per pair.
 __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
                                                    const float *__restrict__ Vp, int K, int k,
                                                    int r, float *__restrict__ pair) {
   extern __shared__ float sm[];
-  const int LDR = r + 4;
+  const int LDR = r + 1;  // odd row stride: the threads of a warp hit distinct banks
   float *su = sm, *sv = sm + (size_t)k * LDR;
   pdl_launch();
   pdl_wait();
@@ -204,54 +217,66 @@ __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
   const size_t ubase = (size_t)b * R + (t == 0 ? 0 : 1 + (size_t)(t - 1) * k);
   const size_t vbase = (size_t)b * R + 1 + (size_t)t * k;
   const int r4 = r / 4;
-  for (int e = threadIdx.x; e < np * r4; e += blockDim.x) {
-    const int i = e / r4, c = e % r4;
-    *(float4 *)(su + (size_t)i * LDR + 4 * c) = ((const float4 *)(U + (ubase + i) * r))[c];
-  }
-  for (int e = threadIdx.x; e < k * r4; e += blockDim.x) {
-    const int j = e / r4, c = e % r4;
-    *(float4 *)(sv + (size_t)j * LDR + 4 * c) = ((const float4 *)(Vp + (vbase + j) * r))[c];
+  for (int e = threadIdx.x; e < (np + k) * r4; e += blockDim.x) {
+    const int row = e / r4, c = e % r4;
+    const float4 q = row < np ? ((const float4 *)(U + (ubase + row) * r))[c]
+                              : ((const float4 *)(Vp + (vbase + row - np) * r))[c];
+    float *dst = (row < np ? su + (size_t)row * LDR : sv + (size_t)(row - np) * LDR) + 4 * c;
+    dst[0] = q.x, dst[1] = q.y, dst[2] = q.z, dst[3] = q.w;
   }
   __syncthreads();
-  // one warp per pair, lanes across the rank
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   float *out = pair + ((size_t)b * (K - 1) + t) * k * k;
-  for (int e = w; e < np * k; e += nw) {
+  for (int e = threadIdx.x; e < np * k; e += blockDim.x) {
     const int i = e / k, j = e % k;
-    float d = 0.f;
-    for (int c = lane; c < r; c += 32) d = fmaf(su[(size_t)i * LDR + c], sv[(size_t)j * LDR + c], d);
-    d = warp_sum(d);
-    if (lane == 0) out[e] = d;
+    const float *a = su + (size_t)i * LDR, *c = sv + (size_t)j * LDR;
+    float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+    for (int q = 0; q < r; q += 4) {
+      d0 = fmaf(a[q], c[q], d0);
+      d1 = fmaf(a[q + 1], c[q + 1], d1);
+      d2 = fmaf(a[q + 2], c[q + 2], d2);
+      d3 = fmaf(a[q + 3], c[q + 3], d3);
+    }
+    out[e] = (d0 + d1) + (d2 + d3);
   }
 }
 
 // One CTA per request: max-sum Viterbi over the K-1 positions of k candidates
-// on the precomputed pair scores.  Ties go to the lower candidate rank.
-__global__ void __launch_bounds__(32) k_viterbi(const float *__restrict__ pair,
-                                                const int32_t *__restrict__ topk_ids,
-                                                const float *__restrict__ topk_logp, int K, int k,
-                                                int32_t *__restrict__ path,
-                                                float *__restrict__ score) {
+// on the precomputed pair scores (staged in shared memory with one coalesced
+// load).  Ties go to the lower candidate rank.
+__global__ void __launch_bounds__(256) k_viterbi(const float *__restrict__ pair,
+                                                 const int32_t *__restrict__ topk_ids,
+                                                 const float *__restrict__ topk_logp, int K, int k,
+                                                 int32_t *__restrict__ path,
+                                                 float *__restrict__ score) {
+  extern __shared__ float sp[];  // [(K-1) * k * k] pair scores, then [(K-1) * k] logp
   __shared__ float delta[DFLASH_MAX_TOPK];
   __shared__ int bp[DFLASH_MAX_BLOCK][DFLASH_MAX_TOPK];
   pdl_launch();
   pdl_wait();
-  const int b = blockIdx.x, j = threadIdx.x;
+  const int b = blockIdx.x;
+  const int npair = (K - 1) * k * k, nlp = (K - 1) * k;
+  float *slp = sp + npair;
+  const float *pr = pair + (size_t)b * npair;
+  const float *lp = topk_logp + (size_t)b * nlp;
+  for (int e = threadIdx.x; e < npair; e += blockDim.x) sp[e] = pr[e];
+  for (int e = threadIdx.x; e < nlp; e += blockDim.x) slp[e] = lp[e];
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int j = threadIdx.x;
   for (int t = 0; t < K - 1; ++t) {
-    const float *pr = pair + ((size_t)b * (K - 1) + t) * k * k;
-    const float *lp = topk_logp + ((size_t)b * (K - 1) + t) * k;
+    const float *ps = sp + (size_t)t * k * k;
     float nd = 0.f;
     int arg = 0;
     if (j < k) {
       if (t == 0) {
-        nd = lp[j] + pr[j];
+        nd = slp[j] + ps[j];
       } else {
         float best = -INFINITY;
         for (int i = 0; i < k; ++i) {
-          const float c = delta[i] + pr[i * k + j];
+          const float c = delta[i] + ps[i * k + j];
           if (c > best) best = c, arg = i;  // strict: the lower rank keeps ties
         }
-        nd = lp[j] + best;
+        nd = slp[t * k + j] + best;
       }
     }
     __syncwarp();
@@ -331,20 +356,18 @@ __global__ void __launch_bounds__(1024) k_accept(const int32_t *__restrict__ pat
 
 namespace dflh {
 
-int launch_topk(const float *logits, int rows, int V, int k, float *partial, int32_t *ids,
-                float *logp, cudaStream_t st) {
+int launch_topk(const float *logits, int rows, int V, int k, float *partial, int *tickets,
+                int32_t *ids, float *logp, cudaStream_t st) {
   if (rows <= 0) return DFLASH_OK;
   const int nch = topk_chunks(V);
-  DFL_CHECK_LAUNCH(launch(dfl::k_topk_partial, dim3(nch, rows), dim3(256), 0, st, logits, V, k,
-                          partial));
-  const size_t smem = 4 * 3 * (size_t)nch * k * sizeof(float);
+  const size_t smem = 3 * (size_t)nch * k * sizeof(float);
   if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(dfl::k_topk_merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(dfl::k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return DFLASH_ERR_CUDA;
   }
-  DFL_CHECK_LAUNCH(launch(dfl::k_topk_merge, dim3((rows + 3) / 4), dim3(128), smem, st,
-                          (const float *)partial, rows, nch, k, ids, logp));
+  DFL_CHECK_LAUNCH(launch(dfl::k_topk, dim3(nch, rows), dim3(256), smem, st, logits, V, k, partial,
+                          tickets, ids, logp));
   return DFLASH_OK;
 }
 
@@ -364,7 +387,7 @@ template int launch_sel_gather<dfl::bf16>(const dfl::bf16 *, const int32_t *, co
 int launch_viterbi(const float *U, const float *Vp, const int32_t *topk_ids,
                    const float *topk_logp, int B, int K, int k, int r, float *pair,
                    int32_t *path, float *score, cudaStream_t st) {
-  const size_t smem = sizeof(float) * 2 * (size_t)k * (r + 4);
+  const size_t smem = sizeof(float) * 2 * (size_t)k * (r + 1);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(dfl::k_sel_pairs, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
@@ -372,8 +395,14 @@ int launch_viterbi(const float *U, const float *Vp, const int32_t *topk_ids,
   }
   DFL_CHECK_LAUNCH(launch(dfl::k_sel_pairs, dim3(K - 1, B), dim3(256), smem, st, U, Vp, K, k, r,
                           pair));
-  DFL_CHECK_LAUNCH(launch(dfl::k_viterbi, dim3(B), dim3(32), 0, st, (const float *)pair, topk_ids,
-                          topk_logp, K, k, path, score));
+  const size_t smem2 = sizeof(float) * ((size_t)(K - 1) * k * k + (size_t)(K - 1) * k);
+  if (smem2 > 48 * 1024) {
+    if (cudaFuncSetAttribute(dfl::k_viterbi, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem2) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+  }
+  DFL_CHECK_LAUNCH(launch(dfl::k_viterbi, dim3(B), dim3(256), smem2, st, (const float *)pair,
+                          topk_ids, topk_logp, K, k, path, score));
   return DFLASH_OK;
 }
 

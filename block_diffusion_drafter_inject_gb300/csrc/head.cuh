@@ -8,9 +8,9 @@ constexpr int kTopkChunk = 8192;  // logits per top-k CTA (8 warps x 1024)
 
 inline int topk_chunks(int V) { return (V + kTopkChunk - 1) / kTopkChunk; }
 
-// partials: rows * chunks * (2*k + 2) floats
-int launch_topk(const float *logits, int rows, int V, int k, float *partial, int32_t *ids,
-                float *logp, cudaStream_t st);
+// partials: rows * chunks * (2*k + 2) floats; tickets: rows ints, zero on entry and exit
+int launch_topk(const float *logits, int rows, int V, int k, float *partial, int *tickets,
+                int32_t *ids, float *logp, cudaStream_t st);
 
 template <typename S>
 int launch_sel_gather(const S *E, const int32_t *anchor, const int32_t *topk_ids, int B, int K,

@@ -131,3 +131,107 @@ def topk_compare(g_ids, o_logits, o_ids, k, margin=1e-2):
 
 def sets_equal(g_ids, o_ids):
     return np.array_equal(np.sort(g_ids, axis=-1), np.sort(o_ids, axis=-1))
+
+
+class FullCase:
+    """Full-size drafter case with window-only injection: for request b only the
+    positions [max(0, ctx-W), ctx) are injected (the only ones a pass reads),
+    on the device and in the oracle.  The oracle runs a subset of requests."""
+
+    _weights = {}
+
+    def __init__(self, B, K, ctx, seed=0, oracle_requests=None, sel_scale=0.3, wseed=0):
+        self.cfg = synth.preset("full")
+        self.B, self.K = B, K
+        self.ctx = np.asarray(ctx, dtype=np.int32)
+        self.seed = seed
+        key = (wseed, sel_scale)
+        if key not in FullCase._weights:
+            FullCase._weights.clear()
+            FullCase._weights[key] = synth.make_weights(self.cfg, seed=wseed, sel_scale=sel_scale)
+        self.W = FullCase._weights[key]
+        Wn, P = self.cfg["window"], self.cfg["page_size"]
+        self.lo = np.maximum(0, self.ctx - Wn)
+        self.req = np.concatenate([np.full(c - l, b, np.int32)
+                                   for b, (c, l) in enumerate(zip(self.ctx, self.lo))])
+        self.pos = np.concatenate([np.arange(l, c, dtype=np.int32) for c, l in zip(self.ctx, self.lo)])
+        self.hidden = synth.make_hiddens(self.cfg, len(self.req), seed=seed, name="window_hiddens")
+        self.anchor = synth.make_anchors(self.cfg, B, seed=seed)
+        # pages only for the positions a pass touches
+        maxp = int(max((c + K + P - 1) // P for c in self.ctx))
+        need = [list(range(l // P, (c + K - 1) // P + 1)) for c, l in zip(self.ctx, self.lo)]
+        total = sum(len(n) for n in need)
+        perm = synth.stream(seed, "page_perm").permutation(total)
+        self.table = np.full((B, maxp), -1, dtype=np.int32)
+        o = 0
+        for b, pages in enumerate(need):
+            for pi in pages:
+                self.table[b, pi] = perm[o]
+                o += 1
+        self.num_pages = total
+        self.oracle_requests = list(range(B)) if oracle_requests is None else list(oracle_requests)
+        self._o = None
+
+    def oracle(self):
+        if self._o is None:
+            cfg, L, K = self.cfg, self.cfg["n_layers"], self.K
+            res = {}
+            for b in self.oracle_requests:
+                sel = self.req == b
+                n_ctx = int(self.ctx[b])
+                k, v, _ = oracle.inject_context(cfg, self.W, self.hidden[sel], self.pos[sel], "bf16")
+                shape = (n_ctx, cfg["n_kv_heads"], cfg["head_dim"])
+                ck, cv = [], []
+                for l in range(L):
+                    a = np.zeros(shape)
+                    a[self.pos[sel]] = k[l]
+                    ck.append(a)
+                    a = np.zeros(shape)
+                    a[self.pos[sel]] = v[l]
+                    cv.append(a)
+                d = oracle.draft_block(cfg, self.W, [ck], [cv], self.anchor[b:b + 1], [n_ctx], K,
+                                       "bf16")
+                p, s, m = oracle.select_path(cfg, self.W, self.anchor[b:b + 1], d["ids"], d["logp"],
+                                             with_margin=True)
+                res[b] = dict(k=k, v=v, logits=d["logits"][0], ids=d["ids"][0], logp=d["logp"][0],
+                              path=p[0], score=s[0], margin=m[0])
+            self._o = res
+        return self._o
+
+    def device(self, max_inject=4096):
+        import torch
+        import block_diffusion_drafter_inject_gb300 as dfl
+        self.Wd = dfl.DeviceWeights.from_host(self.cfg, self.W, "cuda")
+        self.kv = dfl.PagedKV(self.cfg, self.table, self.num_pages, "cuda")
+        self.cyc = dfl.DraftCycle(self.cfg, self.Wd, self.kv, self.B, self.K, max_inject, "cuda")
+        hid = torch.from_numpy(self.hidden).to(torch.bfloat16).cuda()
+        req = torch.from_numpy(self.req).cuda()
+        pos = torch.from_numpy(self.pos).cuda()
+        for o in range(0, len(self.req), max_inject):
+            sl = slice(o, o + max_inject)
+            dfl.inject_context(self.cfg, self.Wd, self.kv, hid[sl], req[sl], pos[sl], self.cyc.ws)
+        self.d_anchor = torch.from_numpy(self.anchor).cuda()
+        self.d_ctx = torch.from_numpy(self.ctx).cuda()
+        self.d_logits = torch.zeros((self.B, self.K - 1, self.cfg["vocab"]), dtype=torch.float32,
+                                    device="cuda")
+        dfl.draft_block(self.cfg, self.Wd, self.kv, self.d_anchor, self.d_ctx, self.K, self.cyc.ws,
+                        self.cyc.topk_ids, self.cyc.topk_logp, self.d_logits)
+        dfl.select_path(self.cfg, self.Wd, self.d_anchor, self.cyc.topk_ids, self.cyc.topk_logp,
+                        self.K, self.cyc.ws, self.cyc.path, self.cyc.score)
+        torch.cuda.synchronize()
+        self.status = dfl.read_device_status(self.cyc.ws)
+        return self
+
+    def gpu_kv(self, b):
+        """Device K/V of request b at its injected positions: [L, n, Hkv, d]."""
+        P = self.cfg["page_size"]
+        sel = self.req == b
+        p = self.pos[sel]
+        pages = self.table[b, p // P]
+        import torch
+        pg = torch.from_numpy(pages.astype(np.int64)).cuda()
+        sl = torch.from_numpy((p % P).astype(np.int64)).cuda()
+        # [pages, P, L, Hkv, d] -> rows (page, slot) -> [L, n, Hkv, d]
+        k = self.kv.k.permute(1, 3, 0, 2, 4)[pg, sl].permute(1, 0, 2, 3)
+        v = self.kv.v.permute(1, 3, 0, 2, 4)[pg, sl].permute(1, 0, 2, 3)
+        return k.float().cpu().numpy(), v.float().cpu().numpy()

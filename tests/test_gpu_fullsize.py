@@ -1,0 +1,141 @@
+"""Parity at the full drafter size (width 4096, 5 layers, vocab 151936), in the
+launch configurations the benchmark uses: B=1 block 8 with 2048 context; B=1
+block 16 with 8192 context (target logits built from the oracle's path so every
+accepted length 1..16 occurs); B=32 ragged contexts in [512, 8192] on shuffled
+64-token pages (oracle on a subset of requests, which the pass treats
+independently); and a 4096-token injection sampled row by row.
+
+Tolerances: logits within 2e-2 of the row maximum and injected K/V within bf16
+resolution, as in test_gpu_parity.  Decisions: (a) bit-exact on identical
+inputs - the top-k equals a full sort of the device's own logits, the selector
+run on the oracle's candidates matches the oracle's path where its margin
+exceeds 1e-2, acceptance on given logits matches exactly; (b) against the
+oracle's own logits, top-k ranks are compared where the oracle's margin
+exceeds twice the bf16 contract's measured sensitivity at this width
+(tests/golden/contract_sensitivity.json: the oracle alone moves its logits by
+that much when its pre-rounding values move by 1e-6)."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _cases import FullCase, rowmax_rel, topk_compare
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+GOLD = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+BAND = 2.0 * json.load(open(os.path.join(GOLD, "contract_sensitivity.json")))["shift"]
+
+
+def _check_request(case, b, kv_rows=64):
+    import block_diffusion_drafter_inject_gb300 as dfl
+    o = case.oracle()[b]
+    k = case.cfg["top_k"]
+    gk, gv = case.gpu_kv(b)
+    rows = np.linspace(0, gk.shape[1] - 1, min(kv_rows, gk.shape[1])).astype(int)
+    assert rowmax_rel(gk[:, rows], o["k"][:, rows]) < 1.6e-2
+    assert rowmax_rel(gv[:, rows], o["v"][:, rows]) < 1.6e-2
+    g_logits = case.d_logits[b].double().cpu().numpy()
+    assert rowmax_rel(g_logits, o["logits"]) < 2e-2
+    g_ids = case.cyc.topk_ids[b].cpu().numpy()
+    g_logp = case.cyc.topk_logp[b].cpu().numpy().astype(np.float64)
+    # (a) exact: the device top-k is the top-k of its own logits
+    for t in range(g_logits.shape[0]):
+        ids, lp, _ = oracle.topk_logp(g_logits[t], k)
+        np.testing.assert_array_equal(g_ids[t], ids)
+        np.testing.assert_allclose(g_logp[t], lp, atol=2e-5)
+    # (b) against the oracle's logits, outside the contract's sensitivity band
+    compared, bad = topk_compare(g_ids, o["logits"], o["ids"], k, margin=BAND)
+    top = np.take_along_axis(g_logits - o["logits"], o["ids"].astype(np.int64), axis=1)
+    assert bad == 0, f"{bad} of {compared}; max |err| at the oracle top-{k}: {np.abs(top).max():.2e}"
+    # the selector on the oracle's candidates (no bf16 storage inside)
+    ids = torch.from_numpy(o["ids"][None].astype(np.int32)).cuda()
+    lp = torch.from_numpy(o["logp"][None].astype(np.float32)).cuda()
+    path = torch.zeros((1, case.K - 1), dtype=torch.int32, device="cuda")
+    score = torch.zeros((1,), dtype=torch.float32, device="cuda")
+    dfl.select_path(case.cfg, case.Wd, case.d_anchor[b:b + 1], ids, lp, case.K, case.cyc.ws,
+                    path, score)
+    torch.cuda.synchronize()
+    if o["margin"] > 1e-2:
+        assert list(path.cpu().numpy()[0]) == list(o["path"])
+    assert abs(float(score.cpu()[0]) - o["score"]) < 1e-3 * max(1.0, abs(o["score"]))
+    return o
+
+
+def test_full_b1_k8_ctx2048():
+    case = FullCase(1, 8, [2048], seed=0).device()
+    assert case.status == 0
+    _check_request(case, 0)
+
+
+def test_full_b1_k16_ctx8192_every_accept_length():
+    import block_diffusion_drafter_inject_gb300 as dfl
+    case = FullCase(1, 16, [8192], seed=1).device()
+    assert case.status == 0
+    o = _check_request(case, 0)
+    # target logits from the oracle's path: accept_len = L for L = 1..16
+    K, V = 16, case.cfg["vocab"]
+    base = synth.make_target_logits(case.cfg, K, K, seed=1)      # one row set per L
+    T = np.zeros((K, K, V), np.float32)
+    path = case.cyc.path.cpu().numpy()[0]
+    for L in range(1, K + 1):
+        t = base[L - 1].copy()
+        for i in range(L - 1):
+            t[i, path[i]] = t[i].max() + 5.0
+        if L < K:
+            t[L - 1, path[L - 1]] = t[L - 1].min()
+        T[L - 1] = t
+    acc_o, tok_o = oracle.accept_greedy(np.tile(path, (K, 1)), T)
+    np.testing.assert_array_equal(acc_o, np.arange(1, K + 1))
+    acc = torch.zeros(K, dtype=torch.int32, device="cuda")
+    tok = torch.zeros((K, K), dtype=torch.int32, device="cuda")
+    ws = dfl.Workspace(case.cfg, K, K, 1)
+    dfl.accept_greedy(torch.from_numpy(np.tile(path, (K, 1))).cuda(), torch.from_numpy(T).cuda(),
+                      ws, acc, tok)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(acc.cpu().numpy(), acc_o)
+    np.testing.assert_array_equal(tok.cpu().numpy(), tok_o)
+    del o
+
+
+def test_full_b32_ragged_paged_subset():
+    ctx = synth.make_ctx_lens(32, 512, 8192, seed=2)
+    case = FullCase(32, 8, ctx, seed=2, oracle_requests=[0, 19]).device()
+    assert case.status == 0
+    for b in (0, 19):
+        _check_request(case, b)
+
+
+def test_full_inject_4096_rows_sampled():
+    import block_diffusion_drafter_inject_gb300 as dfl
+    cfg = synth.preset("full")
+    W = FullCase(1, 8, [64], seed=0).W                         # shared full weights
+    N = 4096
+    h = synth.make_hiddens(cfg, N, seed=3, name="inject_hiddens")
+    P = cfg["page_size"]
+    table = np.arange(N // P, dtype=np.int32)[None, :]
+    Wd = dfl.DeviceWeights.from_host(cfg, W, "cuda")
+    kv = dfl.PagedKV(cfg, table, N // P, "cuda")
+    ws = dfl.Workspace(cfg, 1, 2, N)
+    dfl.inject_context(cfg, Wd, kv, torch.from_numpy(h).to(torch.bfloat16).cuda(),
+                       torch.zeros(N, dtype=torch.int32, device="cuda"),
+                       torch.arange(N, dtype=torch.int32, device="cuda"), ws)
+    torch.cuda.synchronize()
+    assert dfl.read_device_status(ws) == 0
+    rows = np.concatenate([np.random.default_rng(3).choice(N, 14, replace=False), [0, N - 1]])
+    k, v, _ = oracle.inject_context(cfg, W, h[rows], rows, "bf16")
+    pg = torch.from_numpy(rows // P).cuda()
+    sl = torch.from_numpy(rows % P).cuda()
+    gk = kv.k.permute(1, 3, 0, 2, 4)[pg, sl].permute(1, 0, 2, 3)      # [L, n, Hkv, d]
+    gv = kv.v.permute(1, 3, 0, 2, 4)[pg, sl].permute(1, 0, 2, 3)
+    assert rowmax_rel(gk.float().cpu().numpy(), k) < 1.6e-2
+    assert rowmax_rel(gv.float().cpu().numpy(), v) < 1.6e-2

@@ -73,6 +73,19 @@ def test_topk_bitexact_above_margin(case):
     assert np.max(np.abs(case.g["logp"] - o["logp"])[same]) < 5e-2
 
 
+def test_topk_exact_on_own_logits(case):
+    """The device top-k is exactly the top-k (larger logit, then lower id) of the
+    device's own logits, with logp = z - logsumexp(z)."""
+    k = case.cfg["top_k"]
+    z = case.g["logits"].reshape(-1, case.cfg["vocab"])
+    ids = case.g["ids"].reshape(-1, k)
+    lp = case.g["logp"].reshape(-1, k)
+    for r in range(z.shape[0]):
+        want, wlp, _ = oracle.topk_logp(z[r], k)
+        np.testing.assert_array_equal(ids[r], want)
+        np.testing.assert_allclose(lp[r], wlp, atol=2e-5)
+
+
 def test_select_path_on_oracle_candidates(case):
     """The selector alone: the oracle's candidates in, path out."""
     import block_diffusion_drafter_inject_gb300 as dfl
