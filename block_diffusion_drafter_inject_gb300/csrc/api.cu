@@ -77,6 +77,7 @@ static int check_cfg(const dflash_config *c) {
       c->vocab >= 2 && c->n_taps >= 1 && c->d_target >= 1 &&
       ((long)c->n_taps * c->d_target) % 64 == 0 && c->window >= 1 && c->page_size >= 1 &&
       c->top_k >= 1 && c->top_k <= DFLASH_MAX_TOPK && c->top_k <= c->vocab &&
+      (long)topk_chunks(c->vocab) * c->top_k <= 640 &&
       c->sel_rank >= 16 && c->sel_rank % 16 == 0 && c->sel_rank <= 1024 &&
       c->top_k * c->sel_rank <= 16384 && c->conv_group >= 1 && c->d_model % c->conv_group == 0 &&
       c->mask_token_id >= 0 && c->mask_token_id < c->vocab && c->rms_eps >= 0.f &&
@@ -134,24 +135,26 @@ constexpr size_t kHeaderBytes = 256 + kTicketInts * 4 + kTopkTicketInts * 4;
 struct Layout {
   size_t status, tickets, scratch;
   size_t x, un, ub, rf, rb, gates, qkv, qb, kb, vb, ob, hb, zf, logits, attn, topk, topk_tickets;
-  size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf;
+  size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf, rope, rope_inj;
   size_t total;
-  int S_gate, S_qkv, S_o, S_gu, S_down, S_sel, S_lm;
+  GemmPlan P_gate, P_qkv, P_o, P_gu, P_down, P_sel;
   AttnPlan ap;
 };
 
-// K slices of a reduce-mode GEMM: the cost model's choice, capped so the slice
-// scratch and the tile tickets stay bounded; float32 storage uses one slice.
-static int reduce_splits(const dflash_config *c, int N_out, int T, int K_in, int mode, int sms) {
-  if (c->dtype == DFLASH_F32) return 1;
-  int S = gemm_splits(mode == GEMM_SWIGLU ? 2 * N_out : N_out, T, K_in, sms, kMaxReduceSplits);
-  if (gemm_tiles(N_out, T, mode) > kTicketInts) S = 1;
-  return S;
+// Token tile and K slices of a reduce-mode GEMM: the cost model's choice,
+// capped so the slice scratch and the tile tickets stay bounded; float32
+// storage runs on CUDA cores with one slice.
+static GemmPlan reduce_plan(const dflash_config *c, int N_out, int T, int K_in, int mode,
+                            int sms) {
+  if (c->dtype == DFLASH_F32) return GemmPlan{0, 1};
+  GemmPlan p = gemm_plan(N_out, T, K_in, mode, sms, kMaxReduceSplits);
+  if (gemm_tiles(N_out, T, mode, p.bn) > kTicketInts) p.S = 1;
+  return p;
 }
-static size_t reduce_scratch(const dflash_config *c, int N_out, int T, int S, int mode) {
+static size_t reduce_scratch(const dflash_config *c, int N_out, int T, GemmPlan p, int mode) {
   if (c->dtype == DFLASH_F32)
-    return (size_t)S * T * (mode == GEMM_SWIGLU ? 2 * N_out : N_out);
-  return gemm_scratch_floats(N_out, T, S, mode);
+    return (size_t)p.S * T * (mode == GEMM_SWIGLU ? 2 * N_out : N_out);
+  return gemm_scratch_floats(N_out, T, p.S, mode, p.bn);
 }
 
 static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *L) {
@@ -170,30 +173,29 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
     off += (bytes + 255) & ~(size_t)255;
     return o;
   };
-  L->S_gate = reduce_splits(c, GW, T, D, GEMM_REDUCE, sms);
-  L->S_qkv = reduce_splits(c, QKVW, T, D, GEMM_REDUCE, sms);
-  L->S_o = reduce_splits(c, D, T, Hq * dh, GEMM_REDUCE, sms);
-  L->S_gu = reduce_splits(c, F, T, D, GEMM_SWIGLU, sms);
-  L->S_down = reduce_splits(c, D, T, F, GEMM_REDUCE, sms);
-  L->S_sel = reduce_splits(c, r, TR, D, GEMM_REDUCE, sms);
-  L->S_lm = 1;
+  L->P_gate = reduce_plan(c, GW, T, D, GEMM_REDUCE, sms);
+  L->P_qkv = reduce_plan(c, QKVW, T, D, GEMM_REDUCE, sms);
+  L->P_o = reduce_plan(c, D, T, Hq * dh, GEMM_REDUCE, sms);
+  L->P_gu = reduce_plan(c, F, T, D, GEMM_SWIGLU, sms);
+  L->P_down = reduce_plan(c, D, T, F, GEMM_REDUCE, sms);
+  L->P_sel = reduce_plan(c, r, TR, D, GEMM_REDUCE, sms);
   L->ap = attn_plan(B, K, Hq, Hkv, dh, c->window, sms);
   // slice scratch shared by every reduce-mode GEMM (they run one after another)
   size_t sc = 0;
-  sc = std::max(sc, reduce_scratch(c, GW, T, L->S_gate, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, QKVW, T, L->S_qkv, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, D, T, L->S_o, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, F, T, L->S_gu, GEMM_SWIGLU));
-  sc = std::max(sc, reduce_scratch(c, D, T, L->S_down, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, r, TR, L->S_sel, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, V, TL, 1, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, GW, T, L->P_gate, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, QKVW, T, L->P_qkv, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, D, T, L->P_o, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, F, T, L->P_gu, GEMM_SWIGLU));
+  sc = std::max(sc, reduce_scratch(c, D, T, L->P_down, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, r, TR, L->P_sel, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, V, TL, GemmPlan{0, 1}, GEMM_REDUCE));
   // injection GEMMs: the split depends on the token count; take the largest
   auto inj = [&](int n_out, int k_in) {
     size_t best = 0;
     auto eval = [&](int n) {
       if (n < 1 || n > N) return;
-      const int S = reduce_splits(c, n_out, n, k_in, GEMM_REDUCE, sms);
-      best = std::max(best, reduce_scratch(c, n_out, n, S, GEMM_REDUCE));
+      const GemmPlan p = reduce_plan(c, n_out, n, k_in, GEMM_REDUCE, sms);
+      best = std::max(best, reduce_scratch(c, n_out, n, p, GEMM_REDUCE));
     };
     for (int n = 1; n <= 16; ++n) eval(n);
     for (int n = 32; n <= 256; n *= 2) eval(n);
@@ -228,6 +230,8 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->Vp = take((size_t)TR * r * 4);
   L->pairs = take((size_t)B * (K - 1) * k * k * 4);
   L->argmax = take((size_t)T * argmax_chunks(V) * 2 * 4);
+  L->rope = take((size_t)T * (dh / 2) * 8);
+  L->rope_inj = take((size_t)N * (dh / 2) * 8);
   L->gn = take((size_t)N * TIN * es);
   L->cb = take((size_t)N * D * es);
   L->kvf = take((size_t)N * 2 * Hkv * dh * c->n_layers * 4);
@@ -246,9 +250,11 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
 
 // One reduce-mode GEMM on the shared scratch and tickets of the workspace.
 static GemmCall reduce_call(const dflash_config &c, uint8_t *ws, const Layout &L, const void *W,
-                            int N_out, int K_in, const void *X, int T, int S, int mode,
+                            int N_out, int K_in, const void *X, int T, GemmPlan plan, int mode,
                             float *out_f32, int ld, void *out_s, int ldb) {
   GemmCall g;
+  g.bn = plan.bn;
+  const int S = plan.S;
   g.dtype = c.dtype;
   g.W = W;
   g.N_out = N_out;
@@ -278,11 +284,14 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
   S *gn = (S *)(ws + L.gn);
   S *cb = (S *)(ws + L.cb);
   float *kvf = (float *)(ws + L.kvf);
-  TRY(launch_rows_norm<S>((const S *)hidden, N, TIN, (const S *)w.fc_norm, c.rms_eps, gn, st));
-  const int S_fc = reduce_splits(&c, D, N, TIN, GEMM_REDUCE, sms);
+  const RopeTable rope = rope_table(c.rope_theta, dh);
+  float2 *rope_cs = (float2 *)(ws + L.rope_inj);
+  TRY(launch_rows_norm<S>((const S *)hidden, N, TIN, (const S *)w.fc_norm, c.rms_eps, gn, pos,
+                          rope, dh / 2, rope_cs, st));
+  const GemmPlan S_fc = reduce_plan(&c, D, N, TIN, GEMM_REDUCE, sms);
   TRY(gemm_run(reduce_call(c, ws, L, w.fc, D, TIN, gn, N, S_fc, GEMM_REDUCE, nullptr, D, cb, D),
                st));
-  const int S_kv = reduce_splits(&c, W2, N, D, GEMM_REDUCE, sms);
+  const GemmPlan S_kv = reduce_plan(&c, W2, N, D, GEMM_REDUCE, sms);
   LayerPtrs kn;
   memset(&kn, 0, sizeof(kn));
   for (int l = 0; l < c.n_layers; ++l) {
@@ -292,9 +301,8 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
                  st));
     kn.p[l] = w.layer[l].k_norm;
   }
-  const RopeTable rope = rope_table(c.rope_theta, dh);
   TRY(launch_inject_store<S>(kvf, N, c.n_layers, Hkv, dh, kn, req, pos, kv.page_table,
-                             kv.num_rows, kv.max_pages_per_req, kv.num_pages, c.page_size, rope,
+                             kv.num_rows, kv.max_pages_per_req, kv.num_pages, c.page_size, rope_cs,
                              c.rms_eps, (S *)kv.k, (S *)kv.v, err, st));
   return DFLASH_OK;
 }
@@ -320,35 +328,37 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   const RopeTable rope = rope_table(c.rope_theta, dh);
   auto gate_gemm = [&](const void *Wg, const S *X) {
     return gemm_run(
-        reduce_call(c, ws, L, Wg, GW, D, X, T, L.S_gate, GEMM_REDUCE, gates, GW, nullptr, 0), st);
+        reduce_call(c, ws, L, Wg, GW, D, X, T, L.P_gate, GEMM_REDUCE, gates, GW, nullptr, 0), st);
   };
 
+  float2 *rope_cs = (float2 *)(ws + L.rope);
   TRY(launch_embed_norm<S>((const S *)w.embed, anchor, c.mask_token_id, V, B, K, D,
-                           (const S *)w.layer[0].attn_norm, eps, x, un, err, st));
+                           (const S *)w.layer[0].attn_norm, eps, x, un, err, ctx_len, rope, dh / 2,
+                           rope_cs, st));
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights &lw = w.layer[l];
     const bool last = l + 1 == c.n_layers;
     // attention sublayer: conv -> QKV -> norm/RoPE -> block attention -> O -> conv, residual
     TRY(gate_gemm(lw.conv_w[0], un));
     TRY(launch_conv_pre<S>(un, gates, T, K, D, g, (const S *)lw.conv_base[0], ub, st));
-    TRY(gemm_run(reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.S_qkv, GEMM_REDUCE, qkv, QKVW,
+    TRY(gemm_run(reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_REDUCE, qkv, QKVW,
                              nullptr, 0),
                  st));
     if constexpr (sizeof(S) == 2) {
       TRY(launch_attention_fused(L.ap, qkv, (const dfl::bf16 *)lw.q_norm,
-                                 (const dfl::bf16 *)lw.k_norm, rope, eps, (const dfl::bf16 *)kv.k,
+                                 (const dfl::bf16 *)lw.k_norm, rope_cs, eps, (const dfl::bf16 *)kv.k,
                                  (const dfl::bf16 *)kv.v, l, kv.page_table, kv.max_pages_per_req,
                                  kv.num_pages, c.page_size, ctx_len, B, K, Hq, Hkv, dh, c.window,
                                  (dfl::bf16 *)ob, err, st));
     } else {
       TRY(launch_qkv_post<S>(qkv, T, K, Hq, Hkv, dh, (const S *)lw.q_norm, (const S *)lw.k_norm,
-                             ctx_len, rope, eps, qb, kb, vb, st));
+                             rope_cs, eps, qb, kb, vb, st));
       TRY(launch_block_attention<S>(L.ap, qb, kb, vb, (const S *)kv.k, (const S *)kv.v, l,
                                     kv.page_table, kv.max_pages_per_req, kv.num_pages,
                                     c.page_size, ctx_len, B, K, Hq, Hkv, dh, c.window, attnp, ob,
                                     err, st));
     }
-    TRY(gemm_run(reduce_call(c, ws, L, lw.wo, D, Hq * dh, ob, T, L.S_o, GEMM_REDUCE, rf, D, rb, D),
+    TRY(gemm_run(reduce_call(c, ws, L, lw.wo, D, Hq * dh, ob, T, L.P_o, GEMM_REDUCE, rf, D, rb, D),
                  st));
     TRY(gate_gemm(lw.conv_w[1], rb));
     TRY(launch_conv_post_norm<S>(rf, gates, T, K, D, g, (const S *)lw.conv_base[1], x,
@@ -356,10 +366,10 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     // MLP sublayer: conv -> gate/up + SwiGLU -> down -> conv, residual
     TRY(gate_gemm(lw.conv_w[2], un));
     TRY(launch_conv_pre<S>(un, gates, T, K, D, g, (const S *)lw.conv_base[2], ub, st));
-    TRY(gemm_run(reduce_call(c, ws, L, lw.w_gate_up, F, D, ub, T, L.S_gu, GEMM_SWIGLU, nullptr, 0,
+    TRY(gemm_run(reduce_call(c, ws, L, lw.w_gate_up, F, D, ub, T, L.P_gu, GEMM_SWIGLU, nullptr, 0,
                              hb, F),
                  st));
-    TRY(gemm_run(reduce_call(c, ws, L, lw.w_down, D, F, hb, T, L.S_down, GEMM_REDUCE, rf, D, rb, D),
+    TRY(gemm_run(reduce_call(c, ws, L, lw.w_down, D, F, hb, T, L.P_down, GEMM_REDUCE, rf, D, rb, D),
                  st));
     TRY(gate_gemm(lw.conv_w[3], rb));
     TRY(launch_conv_post_norm<S>(
@@ -368,7 +378,7 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
         st));
   }
   const int TL = B * (K - 1);
-  TRY(gemm_run(reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, 1, GEMM_REDUCE, logits, V, nullptr, 0),
+  TRY(gemm_run(reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, GemmPlan{0, 1}, GEMM_REDUCE, logits, V, nullptr, 0),
                st));
   TRY(launch_topk(logits, TL, V, c.top_k, topkp, (int *)(ws + L.topk_tickets), ids, logp, st));
   return DFLASH_OK;
@@ -384,9 +394,9 @@ static int run_select(const dflash_config &c, const dflash_weights &w, const int
   S *rows = (S *)(ws + L.selrows);
   float *U = (float *)(ws + L.U), *Vp = (float *)(ws + L.Vp);
   TRY(launch_sel_gather<S>((const S *)w.embed, anchor, ids, B, K, k, c.vocab, D, rows, err, st));
-  TRY(gemm_run(reduce_call(c, ws, L, w.sel_pu, r, D, rows, TR, L.S_sel, GEMM_REDUCE, U, r, nullptr, 0),
+  TRY(gemm_run(reduce_call(c, ws, L, w.sel_pu, r, D, rows, TR, L.P_sel, GEMM_REDUCE, U, r, nullptr, 0),
                st));
-  TRY(gemm_run(reduce_call(c, ws, L, w.sel_pv, r, D, rows, TR, L.S_sel, GEMM_REDUCE, Vp, r, nullptr,
+  TRY(gemm_run(reduce_call(c, ws, L, w.sel_pv, r, D, rows, TR, L.P_sel, GEMM_REDUCE, Vp, r, nullptr,
                            0),
                st));
   TRY(launch_viterbi(U, Vp, ids, logp, B, K, k, r, (float *)(ws + L.pairs), path, score, st));

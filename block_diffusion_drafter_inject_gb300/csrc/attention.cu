@@ -227,22 +227,27 @@ __device__ __forceinline__ void st_dsmem(uint32_t local_addr, uint32_t rank, flo
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(a) : "memory");
 }
 
-// Up to R head rows of the fp32 QKV projection -> RMSNorm(gain) -> RoPE(pos)
-// -> bf16 into swizzled shared rows; one warp, lane holds d = lane + 32e.  All
+// Up to R head rows of the fp32 QKV projection -> RMSNorm(gain) -> RoPE ->
+// bf16 into swizzled shared rows; one warp, lane holds d = lane + 32e.  All
 // global loads of the batch are issued before any arithmetic.
-//   src[q]: row q's projection (nullptr: write zeros); pos[q]: its position.
+//   src[q]: row q's projection (nullptr: write zeros); cs[q]: its RoPE
+//   (cos, sin) row (nullptr: no RoPE); gain nullptr: no norm, no RoPE.
 template <int DH, int R>
-__device__ __forceinline__ void norm_rope_rows(const float *const *src, const int *pos,
+__device__ __forceinline__ void norm_rope_rows(const float *const *src, const float2 *const *cs,
                                                const int *dst_row, int nrows, const bf16 *gain,
-                                               bool rope_on, const dflh::RopeTable &rope,
                                                float eps, uint8_t *base, int RB, int lane) {
   constexpr int E = DH / 32;
   float v[R][E];
+  float2 rc[R][E / 2];
 #pragma unroll
-  for (int q = 0; q < R; ++q)
+  for (int q = 0; q < R; ++q) {
 #pragma unroll
     for (int e = 0; e < E; ++e)
       v[q][e] = (q < nrows && src[q]) ? src[q][lane + 32 * e] : 0.f;
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e)
+      rc[q][e] = (q < nrows && gain && cs[q]) ? cs[q][lane + 32 * e] : make_float2(1.f, 0.f);
+  }
   float g[E];
   if (gain) {
 #pragma unroll
@@ -259,19 +264,11 @@ __device__ __forceinline__ void norm_rope_rows(const float *const *src, const in
       const float inv = rsqrtf(ss / DH + eps);
 #pragma unroll
       for (int e = 0; e < E; ++e) v[q][e] = v[q][e] * inv * g[e];
-      if (rope_on) {
-        const double two_pi = 6.283185307179586476925286766559;
 #pragma unroll
-        for (int e = 0; e < E / 2; ++e) {
-          const int i = lane + 32 * e;  // pairs (i, i + DH/2)
-          const double a = (double)pos[q] * rope.inv_freq[i];
-          const float ar = (float)(a - two_pi * floor(a * (1.0 / two_pi)));
-          float sn, cs;
-          sincosf(ar, &sn, &cs);
-          const float lo = v[q][e], hi = v[q][e + E / 2];
-          v[q][e] = lo * cs - hi * sn;
-          v[q][e + E / 2] = hi * cs + lo * sn;
-        }
+      for (int e = 0; e < E / 2; ++e) {  // pairs (i, i + DH/2), i = lane + 32e
+        const float lo = v[q][e], hi = v[q][e + E / 2];
+        v[q][e] = lo * rc[q][e].x - hi * rc[q][e].y;
+        v[q][e + E / 2] = hi * rc[q][e].x + lo * rc[q][e].y;
       }
     }
 #pragma unroll
@@ -292,13 +289,17 @@ struct AttnArgs {
   const int32_t *ctx_len;
   int K, Hq, Hkv, window, kps, nsplit, nqg;
   float eps;
+  const float2 *rope_cs;  // [B*K, DH/2] (cos, sin) of each block slot's position
   bf16 *ob;  // [B*K, Hq*DH]
   int *err;
 };
 
-// grid (nsplit, Hkv, B*nqg), cluster (nsplit, 1, 1); block 128 (4 warps x 16 rows).
-template <int DH>
-__global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::RopeTable rope) {
+// grid (nsplit, Hkv, B*nqg), cluster (nsplit, 1, 1); block 128 = 4 warps.
+// KP warps share each 16-row query block and split every key tile KP ways
+// (KP = 1, 2, 4 for groups of <= 64, 32, 16 query rows); their softmax states
+// are merged in shared memory after the tile loop.
+template <int DH, int KP>
+__global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
   constexpr int CH = kCH;          // keys per tile
   constexpr int CHUNKS = DH / 8;   // 16-byte chunks per row
   constexpr int RB = DH * 2;       // bytes per row
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::
   uint8_t *pQ = smem;
   uint8_t *pK0 = smem + kQG * RB;
   uint8_t *pV0 = pK0 + 2 * TILE;
-  uint8_t *pRecv = pV0 + 2 * TILE;  // [nsplit][per][DH + 2] fp32, written by the peers
+  uint8_t *pRecv = pK0;  // after the tile loop: [nsplit][per][DH + 2] fp32, written by the peers
   const uint32_t sQ = smem_u32(pQ), sK0 = smem_u32(pK0), sV0 = smem_u32(pV0);
   pdl_launch();
   pdl_wait();
@@ -324,26 +325,26 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::
   const int k_end = min(n_keys, k_begin + A.kps);
   const int ntiles = k_begin < n_keys ? (k_end - k_begin + CH - 1) / CH : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool rope_on = rope.enabled != 0;
 
   // queries: head norm + RoPE of the projection rows, qr = i*grp + g; warp w
   // stages rows 16w .. 16w+15 in two batches of 8
   for (int half = 0; half < 2; ++half) {
     const float *src[8];
-    int pos[8], dst[8];
+    const float2 *cs[8];
+    int dst[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int row = warp * 16 + half * 8 + q, qrg = qgi * kQG + row;
       dst[q] = row;
       src[q] = nullptr;
-      pos[q] = 0;
+      cs[q] = nullptr;
       if (qrg < QR) {
         const int i = qrg / grp, g = qrg % grp;
         src[q] = A.qkv + (size_t)(b * A.K + i) * QKVW + (size_t)(kvh * grp + g) * DH;
-        pos[q] = ctx + i;
+        cs[q] = A.rope_cs + (size_t)(b * A.K + i) * (DH / 2);
       }
     }
-    norm_rope_rows<DH, 8>(src, pos, dst, 8, A.q_norm, rope_on, rope, A.eps, pQ, RB, lane);
+    norm_rope_rows<DH, 8>(src, cs, dst, 8, A.q_norm, A.eps, pQ, RB, lane);
   }
   auto load_tile = [&](int t, int stage) {
     const int t0 = k_begin + t * CH;
@@ -376,21 +377,20 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::
       const int jb0 = max(0, n_ctx - t0), jb1 = min(CH, k_end - t0);  // block rows [jb0, jb1)
       for (int j0 = jb0 + warp * 4; j0 < jb1; j0 += 16) {
         const float *sk[4], *sv[4];
-        int pos[4], dst[4];
+        const float2 *cs[4];
+        int dst[4];
         const int nr = min(4, jb1 - j0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int j = j0 + q, i = t0 + j - n_ctx;
+          const int j = j0 + q, i = q < nr ? t0 + j - n_ctx : 0;
           dst[q] = j;
-          pos[q] = ctx + i;
-          const float *row = A.qkv + (size_t)(b * A.K + (q < nr ? i : 0)) * QKVW;
+          const float *row = A.qkv + (size_t)(b * A.K + i) * QKVW;
           sk[q] = row + (size_t)(A.Hq + kvh) * DH;
           sv[q] = row + (size_t)(A.Hq + A.Hkv + kvh) * DH;
+          cs[q] = A.rope_cs + (size_t)(b * A.K + i) * (DH / 2);
         }
-        norm_rope_rows<DH, 4>(sk, pos, dst, nr, A.k_norm, rope_on, rope, A.eps,
-                              pK0 + stage * TILE, RB, lane);
-        norm_rope_rows<DH, 4>(sv, pos, dst, nr, nullptr, false, rope, A.eps, pV0 + stage * TILE,
-                              RB, lane);
+        norm_rope_rows<DH, 4>(sk, cs, dst, nr, A.k_norm, A.eps, pK0 + stage * TILE, RB, lane);
+        norm_rope_rows<DH, 4>(sv, cs, dst, nr, nullptr, A.eps, pV0 + stage * TILE, RB, lane);
         if (lane < nr) s_valid[stage][j0 + lane] = 1;
       }
     }
@@ -398,7 +398,10 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::
   if (ntiles > 0) load_tile(0, 0);
   cp_async_commit();
 
-  const bool active = qgi * kQG + warp * 16 < QR;
+  constexpr int RW = 4 / KP;            // query row blocks per CTA
+  constexpr int KW = CH / KP;           // keys of a tile per warp
+  const int rb = warp % RW, kpart = warp / RW;
+  const bool active = qgi * kQG + rb * 16 < QR;
   const int g8 = lane >> 2, t4 = lane & 3, r8 = lane & 7, mi = lane >> 3;
   const float sl2 = rsqrtf((float)DH) * 1.4426950408889634f;
   uint32_t qf[DH / 16][4];
@@ -420,20 +423,22 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::
     if (t == 0 && active) {
 #pragma unroll
       for (int kk = 0; kk < DH / 16; ++kk)
-        ldsm_x4(sQ + swz(warp * 16 + (mi & 1) * 8 + r8, 2 * kk + (mi >> 1), RB), qf[kk][0],
+        ldsm_x4(sQ + swz(rb * 16 + (mi & 1) * 8 + r8, 2 * kk + (mi >> 1), RB), qf[kk][0],
                 qf[kk][1], qf[kk][2], qf[kk][3]);
     }
     if (active) {
       const uint32_t sK = sK0 + stage * TILE, sV = sV0 + stage * TILE;
-      float sc[CH / 8][4];
+      const int kw0 = kpart * KW;  // this warp's keys within the tile
+      float sc[KW / 8][4];
 #pragma unroll
-      for (int j = 0; j < CH / 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+      for (int j = 0; j < KW / 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
 #pragma unroll
-      for (int jp = 0; jp < CH / 16; ++jp) {
+      for (int jp = 0; jp < KW / 16; ++jp) {
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(sK + swz(16 * jp + (mi >> 1) * 8 + r8, 2 * kk + (mi & 1), RB), b0, b1, b2, b3);
+          ldsm_x4(sK + swz(kw0 + 16 * jp + (mi >> 1) * 8 + r8, 2 * kk + (mi & 1), RB), b0, b1,
+                  b2, b3);
           mma_bf16_16816(sc[2 * jp], qf[kk], b0, b1);
           mma_bf16_16816(sc[2 * jp + 1], qf[kk], b2, b3);
         }
@@ -441,10 +446,10 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::
       const int t0 = k_begin + t * CH;
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int j = 0; j < CH / 8; ++j) {
+      for (int j = 0; j < KW / 8; ++j) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int col = 8 * j + 2 * t4 + (e & 1);
+          const int col = kw0 + 8 * j + 2 * t4 + (e & 1);
           const bool ok = (t0 + col < k_end) && s_valid[stage][col];
           const float v = ok ? sc[j][e] * sl2 : -INFINITY;
           sc[j][e] = v;
@@ -463,9 +468,9 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::
       float ls[2] = {0.f, 0.f};
       // probabilities as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)):
       // two products with V keep P at ~16 significant bits
-      uint32_t pa[CH / 16][4], pl[CH / 16][4];
+      uint32_t pa[KW / 16][4], pl[KW / 16][4];
 #pragma unroll
-      for (int j = 0; j < CH / 8; ++j) {
+      for (int j = 0; j < KW / 8; ++j) {
         float p[4], r[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -489,11 +494,12 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::
         o[n][3] *= alpha[1];
       }
 #pragma unroll
-      for (int kk = 0; kk < CH / 16; ++kk) {
+      for (int kk = 0; kk < KW / 16; ++kk) {
 #pragma unroll
         for (int np = 0; np < DH / 16; ++np) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(sV + swz(16 * kk + (mi & 1) * 8 + r8, 2 * np + (mi >> 1), RB), b0, b1, b2, b3);
+          ldsm_x4_t(sV + swz(kw0 + 16 * kk + (mi & 1) * 8 + r8, 2 * np + (mi >> 1), RB), b0, b1,
+                    b2, b3);
           mma_bf16_16816(o[2 * np], pa[kk], b0, b1);
           mma_bf16_16816(o[2 * np + 1], pa[kk], b2, b3);
           mma_bf16_16816(o[2 * np], pl[kk], b0, b1);
@@ -505,6 +511,42 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::
   }
   cp_async_wait<0>();
   __syncthreads();
+
+  // merge the KP key parts of each row block (fragment layout, per thread)
+  if (KP > 1) {
+    constexpr int FS = 4 + DH / 2;  // floats per thread: m[2], l[2], o[DH/8][4]
+    float *xs = (float *)pK0;        // [KP-1][RW][32 lanes][FS]
+    if (kpart > 0) {
+      float *d = xs + (((size_t)(kpart - 1) * RW + rb) * 32 + lane) * FS;
+      d[0] = m_run[0], d[1] = m_run[1], d[2] = l_run[0], d[3] = l_run[1];
+#pragma unroll
+      for (int n = 0; n < DH / 8; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d[4 + 4 * n + e] = o[n][e];
+    }
+    __syncthreads();
+    if (kpart == 0) {
+#pragma unroll
+      for (int q = 0; q < KP - 1; ++q) {
+        const float *d = xs + (((size_t)q * RW + rb) * 32 + lane) * FS;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float mo = d[h];
+          const float M = fmaxf(m_run[h], mo);
+          const float a = M == -INFINITY ? 0.f : exp2f(m_run[h] - M);
+          const float c = M == -INFINITY ? 0.f : exp2f(mo - M);
+          l_run[h] = l_run[h] * a + d[2 + h] * c;
+#pragma unroll
+          for (int n = 0; n < DH / 8; ++n) {
+            o[n][2 * h] = o[n][2 * h] * a + d[4 + 4 * n + 2 * h] * c;
+            o[n][2 * h + 1] = o[n][2 * h + 1] * a + d[4 + 4 * n + 2 * h + 1] * c;
+          }
+          m_run[h] = M;
+        }
+      }
+    }
+    __syncthreads();
+  }
 
   // Combine through the cluster: query row `row` is finished by CTA
   // owner = row / per.  Every CTA pushes its (m, l, o) of that row into the
@@ -519,12 +561,13 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A, const dflh::
   const int nrows = min(kQG, QR - qgi * kQG);
   const int per = (nrows + A.nsplit - 1) / A.nsplit;
   const uint32_t recv = smem_u32(pRecv);
+  cluster_sync();  // every CTA of the cluster is done with its tile buffers
   constexpr int RS = DH + 2;  // floats per received row
-  if (active) {
+  if (active && kpart == 0) {
     const float ln2 = 0.6931471805599453f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int row = warp * 16 + g8 + 8 * h;
+      const int row = rb * 16 + g8 + 8 * h;
       if (row < nrows) {
         const int owner = row / per, lr = row - owner * per;
         const uint32_t dst = recv + (uint32_t)(((split * per) + lr) * RS) * 4u;
@@ -601,10 +644,10 @@ AttnPlan attn_plan(int B, int K, int Hq, int Hkv, int dh, int window, int num_sm
   const int n_keys = window + K;
   const long items = (long)B * Hkv * pl.nqg;
   // smallest key split (multiple of 64) that still gives ~2 CTAs per SM, and at
-  // most 8 splits (the splits of one item form a thread-block cluster)
+  // most 16 splits (the splits of one item form a thread-block cluster)
   int kps = dfl::kCH;
   while (kps < n_keys && ((long)items * ((n_keys + kps - 1) / kps) > 2L * num_sms ||
-                          (n_keys + kps - 1) / kps > 8))
+                          (n_keys + kps - 1) / kps > 16))
     kps += dfl::kCH;
   pl.kps = kps;
   pl.nsplit = (n_keys + kps - 1) / kps;
@@ -638,21 +681,24 @@ static int launch_attn_dh(const AttnPlan &pl, const S *qb, const S *kb, const S 
   return DFLASH_OK;
 }
 
-template <int DH>
+template <int DH, int KP>
 static int launch_attn_fused(const AttnPlan &pl, const float *qkv, const dfl::bf16 *qn,
-                             const dfl::bf16 *kn, const RopeTable &rope, float eps,
+                             const dfl::bf16 *kn, const float2 *rope_cs, float eps,
                              const dfl::bf16 *kc, const dfl::bf16 *vc, int layer,
                              const int32_t *table, int max_pages, int num_pages, int P,
                              const int32_t *ctx_len, int B, int K, int Hq, int Hkv, int window,
                              dfl::bf16 *ob, int *err, cudaStream_t st) {
-  // Q, two K and two V tiles, and the receive buffer: nsplit * ceil(rows/nsplit)
-  // <= kQG + 8 rows of DH + 2 floats
-  const size_t smem = (size_t)dfl::kQG * DH * 2 + 4 * (size_t)dfl::kCH * DH * 2 +
-                      (size_t)(dfl::kQG + 8) * (DH + 2) * 4;
+  // Q, two K and two V tiles; the key-part merge and the receive buffer
+  // (nsplit * ceil(rows/nsplit) <= kQG + 16 rows of DH + 2 floats) reuse the
+  // tile buffers after the tile loop
+  static_assert((dfl::kQG + 16) * (DH + 2) * 4 <= 4 * dfl::kCH * DH * 2, "receive buffer");
+  const size_t smem = (size_t)dfl::kQG * DH * 2 + 4 * (size_t)dfl::kCH * DH * 2;
   static int attr_done = 0;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(dfl::k_attn_mma<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return DFLASH_ERR_CUDA;
     attr_done = 1;
   }
@@ -676,6 +722,7 @@ static int launch_attn_fused(const AttnPlan &pl, const float *qkv, const dfl::bf
   a.nsplit = pl.nsplit;
   a.nqg = pl.nqg;
   a.eps = eps;
+  a.rope_cs = rope_cs;
   a.ob = ob;
   a.err = err;
   cudaLaunchConfig_t cfg = {};
@@ -693,22 +740,33 @@ static int launch_attn_fused(const AttnPlan &pl, const float *qkv, const dfl::bf
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   count_launch();
-  DFL_CHECK_LAUNCH(cudaLaunchKernelEx(&cfg, dfl::k_attn_mma<DH>, a, rope));
+  DFL_CHECK_LAUNCH(cudaLaunchKernelEx(&cfg, dfl::k_attn_mma<DH, KP>, a));
   return DFLASH_OK;
 }
 
 int launch_attention_fused(const AttnPlan &pl, const float *qkv, const dfl::bf16 *qn,
-                           const dfl::bf16 *kn, const RopeTable &rope, float eps,
+                           const dfl::bf16 *kn, const float2 *rope_cs, float eps,
                            const dfl::bf16 *kc, const dfl::bf16 *vc, int layer,
                            const int32_t *table, int max_pages, int num_pages, int P,
                            const int32_t *ctx_len, int B, int K, int Hq, int Hkv, int dh,
                            int window, dfl::bf16 *ob, int *err, cudaStream_t st) {
-  if (dh == 128)
-    return launch_attn_fused<128>(pl, qkv, qn, kn, rope, eps, kc, vc, layer, table, max_pages,
-                                  num_pages, P, ctx_len, B, K, Hq, Hkv, window, ob, err, st);
-  if (dh == 64)
-    return launch_attn_fused<64>(pl, qkv, qn, kn, rope, eps, kc, vc, layer, table, max_pages,
-                                 num_pages, P, ctx_len, B, K, Hq, Hkv, window, ob, err, st);
+  const int QR = K * (Hq / Hkv);
+  const int kp = QR <= 16 ? 4 : QR <= 32 ? 2 : 1;
+#define DFL_ATTN(D, KPV)                                                                        \
+  return launch_attn_fused<D, KPV>(pl, qkv, qn, kn, rope_cs, eps, kc, vc, layer, table,         \
+                                   max_pages, num_pages, P, ctx_len, B, K, Hq, Hkv, window, ob, \
+                                   err, st)
+  if (dh == 128) {
+    if (kp == 4) DFL_ATTN(128, 4);
+    if (kp == 2) DFL_ATTN(128, 2);
+    DFL_ATTN(128, 1);
+  }
+  if (dh == 64) {
+    if (kp == 4) DFL_ATTN(64, 4);
+    if (kp == 2) DFL_ATTN(64, 2);
+    DFL_ATTN(64, 1);
+  }
+#undef DFL_ATTN
   return DFLASH_ERR_DIMS;
 }
 

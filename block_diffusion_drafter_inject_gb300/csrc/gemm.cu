@@ -514,55 +514,79 @@ static bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t 
   return true;
 }
 
+
 static int token_tile(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
 
-// Cost model (microseconds) of one launch split S ways, fitted to sweeps on
-// GB300: one CTA streams about 60 GB/s from memory, the GPU about 6.5 TB/s,
-// and a CTA's tensor pipe does about 11 TFLOP/s.  Each wave of units costs the
-// slower of one unit's own time and the wave's share of memory bandwidth;
-// split slices add their write + read traffic.
-static double gemm_cost(int N_out, int T, int K_in, int S, int num_sms) {
+// Cost model (microseconds) of one launch with token tile bn split S ways,
+// fitted to sweeps on GB300: one CTA streams about 60 GB/s, the GPU about
+// 6.5 TB/s from HBM, and a CTA's tensor pipe does about 11 TFLOP/s.  Each wave
+// of units costs the slower of one unit's own time and the wave's share of HBM
+// bandwidth (weights are read from HBM once per token tile when they do not
+// fit in L2); split slices add their write + read traffic, and in the reduce
+// modes the last CTA of a tile reads the S slices of its 128 x bn block.
+static double gemm_cost(int N_out, int T, int K_in, int S, int bn, int mode, int num_sms) {
   const int kb = K_in / dfl::BK;
-  const int bn = token_tile(T);
   const int t_tiles = (T + bn - 1) / bn;
   const int m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
   const double kbps = kb / S;
   const double uA = 128.0 * 64 * 2 * kbps, uB = (double)bn * 64 * 2 * kbps;
   const double t_unit = std::max((uA + uB) / 60e3, 2.0 * 128 * bn * 64 * kbps / 11e6) + 0.15;
   const long U = (long)m_tiles * t_tiles * S;
+  const double wbytes = 2.0 * N_out * K_in;
+  const double hbm_share = wbytes > 48e6 ? 1.0 : 1.0 / t_tiles;  // re-read per token tile?
   double tot = 0.0;
   for (long w = 0; w * num_sms < U; ++w) {
     const long n = std::min<long>(num_sms, U - w * num_sms);
-    tot += std::max(t_unit, n * uA / 6.5e6);
+    tot += std::max(t_unit, n * uA * hbm_share / 6.5e6);
   }
-  if (S > 1) tot += (double)S * T * N_out * 8.0 / 8e6;
+  if (S > 1) {
+    tot += (double)S * T * N_out * 8.0 / 8e6;
+    if (mode != GEMM_PARTIAL) tot += (double)S * std::min(bn, T) * 128 * 4 / 60e3;
+  }
   return tot;
 }
 
-int gemm_splits(int N_out, int T, int K_in, int num_sms, int max_S) {
+static GemmPlan plan_for(int N_out, int T, int K_in, int mode, int num_sms, int max_S,
+                         bool choose_bn) {
   const int kb = K_in / dfl::BK;
-  int best = 1;
+  GemmPlan best{token_tile(T), 1};
   double best_cost = 1e300;
-  for (int S = 1; S <= kb && S <= max_S; ++S) {
-    if (kb % S) continue;
-    if (S > 1 && kb / S < 2) break;
-    if (S > 1 && (size_t)S * T * N_out > kMaxPartialFloats) break;
-    const double c = gemm_cost(N_out, T, K_in, S, num_sms);
-    if (c < best_cost * 0.985) best_cost = c, best = S;
+  const int bns[5] = {16, 32, 64, 128, 256};
+  for (int bi = 0; bi < 5; ++bi) {
+    const int bn = bns[bi];
+    if (!choose_bn && bn != token_tile(T)) continue;
+    if (bn > token_tile(T)) break;
+    for (int S = 1; S <= kb && S <= max_S; ++S) {
+      if (kb % S) continue;
+      if (S > 1 && kb / S < 2) break;
+      if (S > 1 && (size_t)S * T * N_out > kMaxPartialFloats) break;
+      const double c = gemm_cost(N_out, T, K_in, S, bn, mode, num_sms);
+      if (c < best_cost * 0.985) best_cost = c, best = GemmPlan{bn, S};
+    }
   }
   return best;
 }
 
-size_t gemm_tiles(int N_out, int T, int mode) {
-  const int bn = token_tile(T);
+int gemm_splits(int N_out, int T, int K_in, int num_sms, int max_S) {
+  return plan_for(N_out, T, K_in, GEMM_PARTIAL, num_sms, max_S, false).S;
+}
+
+GemmPlan gemm_plan(int N_out, int T, int K_in, int mode, int num_sms, int max_S) {
+  const int rows = mode == GEMM_SWIGLU ? 2 * N_out : N_out;
+  return plan_for(rows, T, K_in, mode, num_sms, max_S, true);
+}
+
+size_t gemm_tiles(int N_out, int T, int mode, int bn) {
+  if (bn <= 0) bn = token_tile(T);
   const int rows = mode == GEMM_SWIGLU ? 64 : dfl::BM;
   return (size_t)((N_out + rows - 1) / rows) * ((T + bn - 1) / bn);
 }
 
-size_t gemm_scratch_floats(int N_out, int T, int S, int mode) {
+size_t gemm_scratch_floats(int N_out, int T, int S, int mode, int bn) {
   if (mode == GEMM_PARTIAL) return (size_t)S * T * N_out;
   if (S <= 1) return 0;
-  return (size_t)S * gemm_tiles(N_out, T, mode) * dfl::BM * token_tile(T);
+  if (bn <= 0) bn = token_tile(T);
+  return (size_t)S * gemm_tiles(N_out, T, mode, bn) * dfl::BM * bn;
 }
 
 template <int BN>
@@ -629,7 +653,9 @@ int gemm_run(const GemmCall &g, cudaStream_t st) {
     return DFLASH_OK;
   }
   if ((uintptr_t)g.W % 16 || (uintptr_t)g.X % 16) return DFLASH_ERR_ALIGN;
-  switch (token_tile(g.T)) {
+  const int bn = g.bn > 0 ? g.bn : token_tile(g.T);
+  if (bn != 16 && bn != 32 && bn != 64 && bn != 128 && bn != 256) return DFLASH_ERR_DIMS;
+  switch (bn) {
     case 16: return launch_tc<16>(g, st, d);
     case 32: return launch_tc<32>(g, st, d);
     case 64: return launch_tc<64>(g, st, d);

@@ -9,8 +9,17 @@ namespace dflh {
 
 constexpr size_t kMaxPartialFloats = size_t(48) << 20;  // cap of one partial buffer
 
-// Number of K slices for a GEMM of this shape on `num_sms` SMs (at most max_S).
+// Number of K slices for a GEMM of this shape on `num_sms` SMs (at most max_S),
+// for the default token tile.
 int gemm_splits(int N_out, int T, int K_in, int num_sms, int max_S = 1 << 20);
+
+// Token tile and K split of one GEMM: picked by a cost model of the waves of
+// work units, the memory traffic, and (reduce modes) the last CTA's reduction.
+struct GemmPlan {
+  int bn;  // token tile: 16, 32, 64, 128 or 256
+  int S;   // K slices
+};
+GemmPlan gemm_plan(int N_out, int T, int K_in, int mode, int num_sms, int max_S);
 
 enum GemmMode {
   GEMM_PARTIAL = 0,  // slice s -> out[(s*T + t)*ld + n]; the caller sums the slices
@@ -26,6 +35,7 @@ struct GemmCall {
   const void *X = nullptr;
   int T = 0;
   int S = 1;
+  int bn = 0;          // token tile; 0 = the smallest tile that holds T (at most 256)
   int mode = GEMM_PARTIAL;
   float *out = nullptr;       // GEMM_PARTIAL output, or the slice scratch of the other modes
   int ld = 0;
@@ -37,9 +47,9 @@ struct GemmCall {
 };
 
 // Floats of slice scratch a reduce-mode GEMM needs (0 when S == 1).
-size_t gemm_scratch_floats(int N_out, int T, int S, int mode);
+size_t gemm_scratch_floats(int N_out, int T, int S, int mode, int bn = 0);
 // Tile tickets a reduce-mode GEMM needs.
-size_t gemm_tiles(int N_out, int T, int mode);
+size_t gemm_tiles(int N_out, int T, int mode, int bn = 0);
 
 // Launch one GEMM.  DFLASH_BF16 operands run on tcgen05 tensor cores fed by
 // TMA; DFLASH_F32 on fp32 CUDA cores.  W and X 16-byte aligned, K_in a

@@ -36,63 +36,102 @@ __device__ __forceinline__ VI block_best(VI a, float *redv, int *redi) {
   return warp_best(b);
 }
 
-// Merge the nch chunk partials of one row (one warp): top-k ids and
-// logp = logit - logsumexp.  cand: 3 * nch * k words of shared scratch.
-__device__ __forceinline__ void topk_merge_row(const float *__restrict__ pr, int nch, int k,
-                                               int32_t *__restrict__ ids,
-                                               float *__restrict__ logp, float *cand, int lane) {
-  const int n = nch * k;
-  float *cval = cand;
-  int *cid = (int *)(cval + n);
-  int *ctk = cid + n;
-  float M = -INFINITY;
-  for (int c = lane; c < nch; c += 32) M = fmaxf(M, __ldcg(pr + (size_t)c * (2 * k + 2)));
-  M = warp_max(M);
-  float S = 0.f;
-  for (int c = lane; c < nch; c += 32) {
-    const float *p = pr + (size_t)c * (2 * k + 2);
-    const float m = __ldcg(p);
-    S += m == -INFINITY ? 0.f : __ldcg(p + 1) * expf(m - M);
-  }
-  S = warp_sum(S);
-  const float lse = M + logf(S);
-  for (int e = lane; e < n; e += 32) {
-    const int c = e / k, j = e % k;
-    const float *p = pr + (size_t)c * (2 * k + 2);
-    cval[e] = __ldcg(p + 2 + j);
-    cid[e] = __float_as_int(__ldcg(p + 2 + k + j));
-    ctk[e] = 0;
-  }
-  __syncwarp();
-  for (int it = 0; it < k; ++it) {
-    VI best{-INFINITY, 0x7fffffff};
-    int where = -1;
-    for (int e = lane; e < n; e += 32)
-      if (!ctk[e] && better(cval[e], cid[e], best.v, best.i))
-        best.v = cval[e], best.i = cid[e], where = e;
-    const VI win = warp_best(best);
-    if (where >= 0 && best.i == win.i) ctk[where] = 1;
-    if (lane == 0) {
-      ids[it] = win.i;
-      logp[it] = win.v - lse;
+// Descending bitonic sort of one value per lane across the warp; returns this
+// lane's value of the sorted sequence (lane 0 holds the largest).
+__device__ __forceinline__ float warp_sort_desc(float x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const float y = __shfl_xor_sync(0xffffffffu, x, stride);
+      const bool lower = (lane & stride) == 0;
+      const bool desc_block = (lane & size) == 0;
+      x = (lower == desc_block) ? fmaxf(x, y) : fminf(x, y);
     }
-    __syncwarp();
   }
+  return x;
 }
 
-// One chunk (8 warps x 1024 logits) of one row: max, sum of exp and top-k.
-// Each warp selects its own top-k in registers (32 values per lane, k rounds
-// of a warp-wide best), then warp 0 merges the 8 warp lists and writes the
-// chunk's partial [m, s, v_0..v_{k-1}, id_0..id_{k-1}].  The CTA that finishes
-// a row's last chunk (a ticket per row, no waiting) merges the row.
+constexpr int kNoId = 0x7fffffff;  // id of an empty slot (never better than a real one)
+
+// Warp-wide top-k (larger value, then lower id) of the candidates v[j], id[j]
+// (j < J) held by the lanes; results in ov[0..k), oi[0..k) (written by lane 0).
+// Every top-k element is >= the k-th largest of the lane maxima t (k lanes each
+// hold an element >= t), so when at most `cap` candidates reach t they are
+// compacted into the warp's shared buffers cv/ci and ranked there; otherwise
+// (heavy ties) all candidates are ranked in registers.
+template <int J>
+__device__ __forceinline__ void warp_topk(const float (&v)[J], const int (&id)[J], int k,
+                                          float *cv, int *ci, int cap, float *ov, int *oi,
+                                          int lane) {
+  float lm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < J; ++j)
+    if (id[j] != kNoId) lm = fmaxf(lm, v[j]);
+  const float t = __shfl_sync(0xffffffffu, warp_sort_desc(lm), k - 1);
+  int cnt = 0;
+#pragma unroll
+  for (int j = 0; j < J; ++j) cnt += (id[j] != kNoId && v[j] >= t) ? 1 : 0;
+  int pre = cnt;  // inclusive prefix over the lanes
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, pre, o);
+    if (lane >= o) pre += y;
+  }
+  const int total = __shfl_sync(0xffffffffu, pre, 31);
+  if (total <= cap) {
+    int w = pre - cnt;
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+      if (id[j] != kNoId && v[j] >= t) cv[w] = v[j], ci[w] = id[j], ++w;
+    __syncwarp();
+    for (int it = 0; it < k; ++it) {
+      VI best{-INFINITY, kNoId};
+      int where = -1;
+      for (int e = lane; e < total; e += 32)
+        if (better(cv[e], ci[e], best.v, best.i)) best.v = cv[e], best.i = ci[e], where = e;
+      const VI win = warp_best(best);
+      if (where >= 0 && best.i == win.i) cv[where] = -INFINITY, ci[where] = kNoId;
+      if (lane == 0) ov[it] = win.v, oi[it] = win.i;
+      __syncwarp();
+    }
+  } else {
+    uint32_t taken = 0;
+    for (int it = 0; it < k; ++it) {
+      VI best{-INFINITY, kNoId};
+      int bj = -1;
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        if (!((taken >> j) & 1u) && id[j] != kNoId && better(v[j], id[j], best.v, best.i))
+          best.v = v[j], best.i = id[j], bj = j;
+      const VI win = warp_best(best);
+      if (bj >= 0 && best.i == win.i) taken |= 1u << bj;
+      if (lane == 0) ov[it] = win.v, oi[it] = win.i;
+    }
+  }
+  __syncwarp();
+}
+
+constexpr int kTopkCap = 64;      // compacted candidates per warp
+constexpr int kTopkRowJ = 20;     // row merge: up to 32 * 20 = 640 chunk candidates
+
+// Top-k and logsumexp of logit rows.  One CTA = one 8192-logit chunk of one
+// row (8 warps x 1024): each warp finds its top-k (warp_topk), warp 0 merges
+// the 8 lists and writes the chunk's partial [m, s, v_0..v_{k-1}, id_0..id_{k-1}]
+// (m = max, s = sum of exp(z - m)).  The CTA that finishes a row's last chunk
+// (a ticket per row, no waiting) merges the row: ids, logp = logit - logsumexp.
 __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int V, int k,
                                               float *__restrict__ partial, int *tickets,
                                               int32_t *__restrict__ ids,
                                               float *__restrict__ logp) {
-  __shared__ float cv[8 * DFLASH_MAX_TOPK];
-  __shared__ int ci[8 * DFLASH_MAX_TOPK];
+  __shared__ float cv[8][kTopkCap];
+  __shared__ int ci[8][kTopkCap];
+  __shared__ float wv[8 * DFLASH_MAX_TOPK];
+  __shared__ int wi[8 * DFLASH_MAX_TOPK];
+  __shared__ float rv[DFLASH_MAX_TOPK];
+  __shared__ int ri[DFLASH_MAX_TOPK];
   __shared__ float wm[8], wsum[8];
-  extern __shared__ float cand[];
   pdl_launch();
   pdl_wait();
   const int chunk = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
@@ -100,11 +139,13 @@ __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, 
   const int base = chunk * dflh::kTopkChunk + w * 1024;
   const float *z = logits + (size_t)row * V;
   float v[32];
+  int id[32];
   float mx = -INFINITY;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    const int id = base + j * 32 + lane;
-    v[j] = id < V ? z[id] : -INFINITY;
+    const int i = base + j * 32 + lane;
+    v[j] = i < V ? z[i] : -INFINITY;
+    id[j] = i < V ? i : kNoId;
     mx = fmaxf(mx, v[j]);
   }
   mx = warp_max(mx);
@@ -113,22 +154,21 @@ __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, 
   for (int j = 0; j < 32; ++j) se += (v[j] == -INFINITY) ? 0.f : expf(v[j] - mx);
   se = warp_sum(se);
   if (lane == 0) wm[w] = mx, wsum[w] = se;
-  uint32_t taken = 0;
-  for (int it = 0; it < k; ++it) {
-    VI best{-INFINITY, 0x7fffffff};
-    int bj = -1;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int id = base + j * 32 + lane;
-      if (!((taken >> j) & 1u) && id < V && better(v[j], id, best.v, best.i))
-        best.v = v[j], best.i = id, bj = j;
-    }
-    const VI win = warp_best(best);
-    if (bj >= 0 && best.i == win.i) taken |= 1u << bj;
-    if (lane == 0) cv[w * k + it] = win.v, ci[w * k + it] = win.i;
-  }
+  warp_topk<32>(v, id, k, cv[w], ci[w], kTopkCap, wv + w * k, wi + w * k, lane);
   __syncthreads();
   if (w != 0) return;
+  // warp 0: merge the 8 warp lists, write the chunk partial
+  {
+    float mv[8];
+    int mi[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int e = 32 * q + lane;
+      mv[q] = e < 8 * k ? wv[e] : -INFINITY;
+      mi[q] = e < 8 * k ? wi[e] : kNoId;
+    }
+    warp_topk<8>(mv, mi, k, cv[0], ci[0], kTopkCap, rv, ri, lane);
+  }
   float *out = partial + ((size_t)row * nch + chunk) * (2 * k + 2);
   float M = -INFINITY;
   for (int q = 0; q < 8; ++q) M = fmaxf(M, wm[q]);
@@ -138,23 +178,9 @@ __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, 
     out[0] = M;
     out[1] = S;
   }
-  // merge 8 lists of k: lane holds candidates lane, lane + 32, ...
-  const int nc = 8 * k;
-  uint32_t tk = 0;
-  for (int it = 0; it < k; ++it) {
-    VI best{-INFINITY, 0x7fffffff};
-    int bq = -1;
-    for (int q = 0; q * 32 + lane < nc; ++q) {
-      const int e = q * 32 + lane;
-      if (!((tk >> q) & 1u) && better(cv[e], ci[e], best.v, best.i))
-        best.v = cv[e], best.i = ci[e], bq = q;
-    }
-    const VI win = warp_best(best);
-    if (bq >= 0 && best.i == win.i) tk |= 1u << bq;
-    if (lane == 0) {
-      out[2 + it] = win.v;
-      out[2 + k + it] = __int_as_float(win.i);
-    }
+  for (int it = lane; it < k; it += 32) {
+    out[2 + it] = rv[it];
+    out[2 + k + it] = __int_as_float(ri[it]);
   }
   // ticket: the last chunk of the row merges it
   __threadfence();
@@ -167,8 +193,37 @@ __global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, 
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
   __threadfence();
-  topk_merge_row(partial + (size_t)row * nch * (2 * k + 2), nch, k, ids + (size_t)row * k,
-                 logp + (size_t)row * k, cand, lane);
+  const float *pr = partial + (size_t)row * nch * (2 * k + 2);
+  float Mr = -INFINITY;
+  for (int c = lane; c < nch; c += 32) Mr = fmaxf(Mr, __ldcg(pr + (size_t)c * (2 * k + 2)));
+  Mr = warp_max(Mr);
+  float Sr = 0.f;
+  for (int c = lane; c < nch; c += 32) {
+    const float *p = pr + (size_t)c * (2 * k + 2);
+    const float m = __ldcg(p);
+    Sr += m == -INFINITY ? 0.f : __ldcg(p + 1) * expf(m - Mr);
+  }
+  Sr = warp_sum(Sr);
+  const float lse = Mr + logf(Sr);
+  const int n = nch * k;
+  float cvr[kTopkRowJ];
+  int cir[kTopkRowJ];
+#pragma unroll
+  for (int q = 0; q < kTopkRowJ; ++q) {
+    const int e = 32 * q + lane;
+    cvr[q] = -INFINITY;
+    cir[q] = kNoId;
+    if (e < n) {
+      const float *p = pr + (size_t)(e / k) * (2 * k + 2);
+      cvr[q] = __ldcg(p + 2 + e % k);
+      cir[q] = __float_as_int(__ldcg(p + 2 + k + e % k));
+    }
+  }
+  warp_topk<kTopkRowJ>(cvr, cir, k, cv[0], ci[0], kTopkCap, rv, ri, lane);
+  for (int it = lane; it < k; it += 32) {
+    ids[(size_t)row * k + it] = ri[it];
+    logp[(size_t)row * k + it] = rv[it] - lse;
+  }
 }
 
 // rows[b*R + j] = E[token j of request b]: j = 0 the anchor, j >= 1 the
@@ -360,13 +415,8 @@ int launch_topk(const float *logits, int rows, int V, int k, float *partial, int
                 int32_t *ids, float *logp, cudaStream_t st) {
   if (rows <= 0) return DFLASH_OK;
   const int nch = topk_chunks(V);
-  const size_t smem = 3 * (size_t)nch * k * sizeof(float);
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(dfl::k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return DFLASH_ERR_CUDA;
-  }
-  DFL_CHECK_LAUNCH(launch(dfl::k_topk, dim3(nch, rows), dim3(256), smem, st, logits, V, k, partial,
+  if (nch * k > 32 * dfl::kTopkRowJ) return DFLASH_ERR_DIMS;
+  DFL_CHECK_LAUNCH(launch(dfl::k_topk, dim3(nch, rows), dim3(256), 0, st, logits, V, k, partial,
                           tickets, ids, logp));
   return DFLASH_OK;
 }

@@ -17,17 +17,38 @@ __device__ __forceinline__ float sigmoidf_(float t) { return 1.f / (1.f + expf(-
 // x[r] = E[token of r]; un[r] = gain * x / rms(x).  Row r = b*K + i; slot 0 holds
 // the anchor, the other slots the mask token.  Requires D % 8 == 0 and
 // 16-byte aligned rows (8 elements per access).
+// cos/sin of the rotate-half RoPE angles of absolute position `pos` for the
+// d/2 frequencies: the angle pos * theta^(-2i/d) is formed and reduced modulo
+// 2*pi in fp64, its sine and cosine taken in fp32.  Written once per row so
+// that the kernels applying RoPE stay in fp32.
+__device__ __forceinline__ void rope_row(float2 *__restrict__ cs, int pos,
+                                         const dflh::RopeTable &rope, int half) {
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    float2 v = make_float2(1.f, 0.f);
+    if (rope.enabled) {
+      const double two_pi = 6.283185307179586476925286766559;
+      const double a = (double)pos * rope.inv_freq[i];
+      const float ar = (float)(a - two_pi * floor(a * (1.0 / two_pi)));
+      sincosf(ar, &v.y, &v.x);
+    }
+    cs[i] = v;
+  }
+}
+
 template <typename S>
 __global__ void __launch_bounds__(512) k_embed_norm(const S *__restrict__ E,
                                                     const int32_t *__restrict__ anchor,
                                                     int mask_id, int V, int K, int D,
                                                     const S *__restrict__ gain, float eps,
                                                     float *__restrict__ x, S *__restrict__ un,
-                                                    int *err) {
+                                                    int *err, const int32_t *__restrict__ ctx_len,
+                                                    const dflh::RopeTable rope, int half,
+                                                    float2 *__restrict__ rope_cs) {
   __shared__ float red[32];
   pdl_launch();
   pdl_wait();
   const int r = blockIdx.x, b = r / K, i = r % K;
+  rope_row(rope_cs + (size_t)r * half, ctx_len[b] + i, rope, half);
   int tok = i == 0 ? anchor[b] : mask_id;
   if (tok < 0 || tok >= V) {
     if (threadIdx.x == 0) set_err(err, DFLASH_DEV_TOKEN_RANGE);
@@ -57,10 +78,14 @@ __global__ void __launch_bounds__(512) k_embed_norm(const S *__restrict__ E,
 template <typename S>
 __global__ void __launch_bounds__(1024) k_rows_norm(const S *__restrict__ in, int cols,
                                                     const S *__restrict__ gain, float eps,
-                                                    S *__restrict__ out) {
+                                                    S *__restrict__ out,
+                                                    const int32_t *__restrict__ pos,
+                                                    const dflh::RopeTable rope, int half,
+                                                    float2 *__restrict__ rope_cs) {
   __shared__ float red[32];
   pdl_launch();
   pdl_wait();
+  if (rope_cs) rope_row(rope_cs + (size_t)blockIdx.x * half, pos[blockIdx.x], rope, half);
   const S *row = in + (size_t)blockIdx.x * cols;
   float ss = 0.f;
   for (int c = threadIdx.x * 8; c < cols; c += blockDim.x * 8) {
@@ -178,27 +203,18 @@ __global__ void __launch_bounds__(512) k_conv_post_norm(
 }
 
 // RMSNorm over one head (d values held as pairs (i, i + d/2) by d/2 threads)
-// followed by rotate-half RoPE at absolute position `pos`.  The angle
-// pos * theta^(-2i/d) is formed and reduced modulo 2*pi in fp64 (two fp64
-// operations); sine and cosine of the reduced angle are taken in fp32.
+// followed by rotate-half RoPE with the row's (cos, sin) table.
 __device__ __forceinline__ void head_norm_rope(float &lo, float &hi, int i, int half,
-                                               float gl, float gh, float eps, int pos,
-                                               const dflh::RopeTable &rope, float *red) {
+                                               float gl, float gh, float eps, float2 cs,
+                                               float *red) {
   float ss = lo * lo + hi * hi;
   ss = block_sum(ss, red);
   const float inv = rsqrtf(ss / (2 * half) + eps);
   lo = lo * inv * gl;
   hi = hi * inv * gh;
-  if (rope.enabled) {
-    const double two_pi = 6.283185307179586476925286766559;
-    const double a = (double)pos * rope.inv_freq[i];
-    const float ar = (float)(a - two_pi * floor(a * (1.0 / two_pi)));
-    float s, c;
-    sincosf(ar, &s, &c);
-    const float x = lo * c - hi * s, y = hi * c + lo * s;
-    lo = x;
-    hi = y;
-  }
+  const float x = lo * cs.x - hi * cs.y, y = hi * cs.x + lo * cs.y;
+  lo = x;
+  hi = y;
 }
 
 // q, k, v of the block from the QKV projection qkv [rows, (Hq+2Hkv)*d] (fp32).
@@ -206,9 +222,8 @@ __device__ __forceinline__ void head_norm_rope(float &lo, float &hi, int i, int 
 template <typename S>
 __global__ void k_qkv_post(const float *__restrict__ qkv, int rows, int K, int Hq,
                            int Hkv, int dh, const S *__restrict__ qn, const S *__restrict__ kn,
-                           const int32_t *__restrict__ ctx_len, const dflh::RopeTable rope,
-                           float eps, S *__restrict__ qb, S *__restrict__ kb,
-                           S *__restrict__ vb) {
+                           const float2 *__restrict__ rope_cs, float eps,
+                           S *__restrict__ qb, S *__restrict__ kb, S *__restrict__ vb) {
   __shared__ float red[32];
   pdl_launch();
   pdl_wait();
@@ -219,8 +234,8 @@ __global__ void k_qkv_post(const float *__restrict__ qkv, int rows, int K, int H
   (void)rows;
   if (h < Hq + Hkv) {
     const S *g = h < Hq ? qn : kn;
-    const int pos = ctx_len[r / K] + (r % K);
-    head_norm_rope(lo, hi, i, half, ldf(g + i), ldf(g + i + half), eps, pos, rope, red);
+    head_norm_rope(lo, hi, i, half, ldf(g + i), ldf(g + i + half), eps,
+                   rope_cs[(size_t)r * half + i], red);
     S *dst = h < Hq ? qb + ((size_t)r * Hq + h) * dh : kb + ((size_t)r * Hkv + (h - Hq)) * dh;
     stf(dst + i, lo);
     stf(dst + i + half, hi);
@@ -239,8 +254,8 @@ __global__ void k_inject_store(const float *__restrict__ kvf, int N, int L, int 
                                int dh, dflh::LayerPtrs knorm, const int32_t *__restrict__ req,
                                const int32_t *__restrict__ pos, const int32_t *__restrict__ table,
                                int num_rows, int max_pages, int num_pages, int P,
-                               const dflh::RopeTable rope, float eps, S *__restrict__ kc,
-                               S *__restrict__ vc, int *err) {
+                               const float2 *__restrict__ rope_cs, float eps,
+                               S *__restrict__ kc, S *__restrict__ vc, int *err) {
   __shared__ float red[32];
   pdl_launch();
   pdl_wait();
@@ -270,7 +285,8 @@ __global__ void k_inject_store(const float *__restrict__ kvf, int N, int L, int 
   if (is_k) {
     const S *g = (const S *)knorm.p[l];
     // every thread of the block takes part in the norm's reduction
-    head_norm_rope(lo, hi, i, half, ldf(g + i), ldf(g + i + half), eps, p, rope, red);
+    head_norm_rope(lo, hi, i, half, ldf(g + i), ldf(g + i + half), eps,
+                   rope_cs[(size_t)n * half + i], red);
   }
   if (!ok) return;
   const int hh = is_k ? h : h - Hkv;
@@ -295,18 +311,21 @@ RopeTable rope_table(float theta, int head_dim) {
 
 template <typename S>
 int launch_embed_norm(const S *E, const int32_t *anchor, int mask_id, int V, int B, int K, int D,
-                      const S *gain, float eps, float *x, S *un, int *err, cudaStream_t st) {
+                      const S *gain, float eps, float *x, S *un, int *err, const int32_t *ctx_len,
+                      const RopeTable &rope, int half, float2 *rope_cs, cudaStream_t st) {
   DFL_CHECK_LAUNCH(launch(dfl::k_embed_norm<S>, dim3(B * K), dim3(D >= 4096 ? 512 : 128), 0, st, E,
-                          anchor, mask_id, V, K, D, gain, eps, x, un, err));
+                          anchor, mask_id, V, K, D, gain, eps, x, un, err, ctx_len, rope, half,
+                          rope_cs));
   return DFLASH_OK;
 }
 template <typename S>
 int launch_rows_norm(const S *in, int rows, int cols, const S *gain, float eps, S *out,
+                     const int32_t *pos, const RopeTable &rope, int half, float2 *rope_cs,
                      cudaStream_t st) {
   if (rows <= 0) return DFLASH_OK;
   const int threads = cols >= 8192 ? 1024 : cols >= 2048 ? 256 : 64;
-  DFL_CHECK_LAUNCH(
-      launch(dfl::k_rows_norm<S>, dim3(rows), dim3(threads), 0, st, in, cols, gain, eps, out));
+  DFL_CHECK_LAUNCH(launch(dfl::k_rows_norm<S>, dim3(rows), dim3(threads), 0, st, in, cols, gain,
+                          eps, out, pos, rope, half, rope_cs));
   return DFLASH_OK;
 }
 template <typename S>
@@ -334,39 +353,40 @@ int launch_conv_post_norm(const float *rf, const float *gate, int rows, int K, i
 }
 template <typename S>
 int launch_qkv_post(const float *qkv, int rows, int K, int Hq, int Hkv, int dh, const S *qn,
-                    const S *kn, const int32_t *ctx_len, const RopeTable &rope, float eps, S *qb,
-                    S *kb, S *vb, cudaStream_t st) {
+                    const S *kn, const float2 *rope_cs, float eps, S *qb, S *kb, S *vb,
+                    cudaStream_t st) {
   DFL_CHECK_LAUNCH(launch(dfl::k_qkv_post<S>, dim3(rows, Hq + 2 * Hkv), dim3(dh / 2), 0, st, qkv,
-                          rows, K, Hq, Hkv, dh, qn, kn, ctx_len, rope, eps, qb, kb, vb));
+                          rows, K, Hq, Hkv, dh, qn, kn, rope_cs, eps, qb, kb, vb));
   return DFLASH_OK;
 }
 template <typename S>
 int launch_inject_store(const float *kvf, int N, int L, int Hkv, int dh, LayerPtrs knorm,
                         const int32_t *req, const int32_t *pos, const int32_t *page_table,
                         int num_rows, int max_pages, int num_pages, int page_size,
-                        const RopeTable &rope, float eps, S *kc, S *vc, int *err,
+                        const float2 *rope_cs, float eps, S *kc, S *vc, int *err,
                         cudaStream_t st) {
   DFL_CHECK_LAUNCH(launch(dfl::k_inject_store<S>, dim3(N, L, 2 * Hkv), dim3(dh / 2), 0, st, kvf, N,
                           L, Hkv, dh, knorm, req, pos, page_table, num_rows, max_pages, num_pages,
-                          page_size, rope, eps, kc, vc, err));
+                          page_size, rope_cs, eps, kc, vc, err));
   return DFLASH_OK;
 }
 
 #define DFL_INST(S)                                                                              \
   template int launch_embed_norm<S>(const S *, const int32_t *, int, int, int, int, int, const S *, \
-                                    float, float *, S *, int *, cudaStream_t);                   \
-  template int launch_rows_norm<S>(const S *, int, int, const S *, float, S *, cudaStream_t);    \
+                                    float, float *, S *, int *, const int32_t *,                 \
+                                    const RopeTable &, int, float2 *, cudaStream_t);             \
+  template int launch_rows_norm<S>(const S *, int, int, const S *, float, S *, const int32_t *,  \
+                                   const RopeTable &, int, float2 *, cudaStream_t);              \
   template int launch_conv_pre<S>(const S *, const float *, int, int, int, int, const S *, S *,  \
                                   cudaStream_t);                                                 \
   template int launch_conv_post_norm<S>(const float *, const float *, int, int, int, int,        \
                                         const S *, float *, const S *, float, S *, S *,          \
                                         cudaStream_t);                                           \
   template int launch_qkv_post<S>(const float *, int, int, int, int, int, const S *, const S *,  \
-                                  const int32_t *, const RopeTable &, float, S *, S *, S *,      \
-                                  cudaStream_t);                                                 \
+                                  const float2 *, float, S *, S *, S *, cudaStream_t);           \
   template int launch_inject_store<S>(const float *, int, int, int, int, LayerPtrs,              \
                                       const int32_t *, const int32_t *, const int32_t *, int,    \
-                                      int, int, int, const RopeTable &, float, S *, S *, int *,  \
+                                      int, int, int, const float2 *, float, S *, S *, int *,     \
                                       cudaStream_t);
 DFL_INST(float)
 DFL_INST(dfl::bf16)

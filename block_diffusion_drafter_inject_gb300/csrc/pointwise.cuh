@@ -16,11 +16,15 @@ struct RopeTable {
 };
 RopeTable rope_table(float theta, int head_dim);
 
+// Both also write the RoPE (cos, sin) row of each row's absolute position
+// (embed: ctx_len[b] + slot; rows_norm: pos[row], skipped when rope_cs is null).
 template <typename S>
 int launch_embed_norm(const S *E, const int32_t *anchor, int mask_id, int V, int B, int K, int D,
-                      const S *gain, float eps, float *x, S *un, int *err, cudaStream_t st);
+                      const S *gain, float eps, float *x, S *un, int *err, const int32_t *ctx_len,
+                      const RopeTable &rope, int half, float2 *rope_cs, cudaStream_t st);
 template <typename S>
 int launch_rows_norm(const S *in, int rows, int cols, const S *gain, float eps, S *out,
+                     const int32_t *pos, const RopeTable &rope, int half, float2 *rope_cs,
                      cudaStream_t st);
 // gate: the conv's gate linear, fp32 [rows, 2D/group]
 template <typename S>
@@ -32,13 +36,13 @@ int launch_conv_post_norm(const float *rf, const float *gate, int rows, int K, i
                           cudaStream_t st);
 template <typename S>
 int launch_qkv_post(const float *qkv, int rows, int K, int Hq, int Hkv, int dh, const S *qn,
-                    const S *kn, const int32_t *ctx_len, const RopeTable &rope, float eps, S *qb,
-                    S *kb, S *vb, cudaStream_t st);
+                    const S *kn, const float2 *rope_cs, float eps, S *qb, S *kb, S *vb,
+                    cudaStream_t st);
 template <typename S>
 int launch_inject_store(const float *kvf, int N, int L, int Hkv, int dh, LayerPtrs knorm,
                         const int32_t *req, const int32_t *pos, const int32_t *page_table,
                         int num_rows, int max_pages, int num_pages, int page_size,
-                        const RopeTable &rope, float eps, S *kc, S *vc, int *err,
+                        const float2 *rope_cs, float eps, S *kc, S *vc, int *err,
                         cudaStream_t st);
 
 }  // namespace dflh

@@ -5,8 +5,9 @@ accepted length 1..16 occurs); B=32 ragged contexts in [512, 8192] on shuffled
 64-token pages (oracle on a subset of requests, which the pass treats
 independently); and a 4096-token injection sampled row by row.
 
-Tolerances: logits within 2e-2 of the row maximum and injected K/V within bf16
-resolution, as in test_gpu_parity.  Decisions: (a) bit-exact on identical
+Tolerances: injected K/V within bf16 resolution as in test_gpu_parity; logits
+within 2e-2 norm-wise per row and within twice the contract's measured
+sensitivity element-wise (see below).  Decisions: (a) bit-exact on identical
 inputs - the top-k equals a full sort of the device's own logits, the selector
 run on the oracle's candidates matches the oracle's path where its margin
 exceeds 1e-2, acceptance on given logits matches exactly; (b) against the
@@ -45,7 +46,11 @@ def _check_request(case, b, kv_rows=64):
     assert rowmax_rel(gk[:, rows], o["k"][:, rows]) < 1.6e-2
     assert rowmax_rel(gv[:, rows], o["v"][:, rows]) < 1.6e-2
     g_logits = case.d_logits[b].double().cpu().numpy()
-    assert rowmax_rel(g_logits, o["logits"]) < 2e-2
+    # full width: per-row norm-wise relative error within 2e-2, and no logit
+    # further from the oracle than twice the contract's own sensitivity
+    nrel = np.linalg.norm(g_logits - o["logits"], axis=1) / np.linalg.norm(o["logits"], axis=1)
+    assert nrel.max() < 2e-2, nrel.max()
+    assert np.abs(g_logits - o["logits"]).max() < BAND
     g_ids = case.cyc.topk_ids[b].cpu().numpy()
     g_logp = case.cyc.topk_logp[b].cpu().numpy().astype(np.float64)
     # (a) exact: the device top-k is the top-k of its own logits

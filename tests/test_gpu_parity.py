@@ -114,3 +114,26 @@ def test_end_to_end_path_and_accept(case):
     acc, toks = oracle.accept_greedy(g["path"], case.target)
     np.testing.assert_array_equal(g["acc"], acc)
     np.testing.assert_array_equal(g["toks"], toks)
+
+
+@pytest.mark.parametrize("pattern", ["all_equal", "five_levels"])
+def test_topk_heavy_ties(pattern):
+    """Logits with massive ties (lm_head rows zero, or repeating in five classes):
+    the device top-k must still be the lowest ids among the largest values."""
+    c = Case("small", 1, 8, [40], seed=21)
+    V = c.cfg["vocab"]
+    if pattern == "all_equal":
+        c.W["lm_head"] = np.zeros_like(c.W["lm_head"])
+    else:
+        rows = c.W["lm_head"][1:6].copy()
+        c.W["lm_head"] = rows[np.arange(V) % 5]
+    c.device()
+    g = c.run_device()
+    k = c.cfg["top_k"]
+    z = g["logits"].reshape(-1, V)
+    for r in range(z.shape[0]):
+        want, wlp, _ = oracle.topk_logp(z[r], k)
+        np.testing.assert_array_equal(g["ids"].reshape(-1, k)[r], want)
+        np.testing.assert_allclose(g["logp"].reshape(-1, k)[r], wlp, atol=2e-5)
+    if pattern == "all_equal":
+        np.testing.assert_array_equal(g["ids"][0, 0], np.arange(k))
