@@ -148,13 +148,14 @@ static GemmPlan reduce_plan(const dflash_config *c, int N_out, int T, int K_in, 
                             int sms) {
   if (c->dtype == DFLASH_F32) return GemmPlan{0, 1};
   GemmPlan p = gemm_plan(N_out, T, K_in, mode, sms, kMaxReduceSplits);
-  if (gemm_tiles(N_out, T, mode, p.bn) > kTicketInts) p.S = 1;
+  if (gemm_tiles(N_out, T, mode, p.bn) > kTicketInts) p.S = 1, p.chunk = 0;
   return p;
 }
-static size_t reduce_scratch(const dflash_config *c, int N_out, int T, GemmPlan p, int mode) {
+static size_t reduce_scratch(const dflash_config *c, int N_out, int T, int K_in, GemmPlan p,
+                             int mode) {
   if (c->dtype == DFLASH_F32)
     return (size_t)p.S * T * (mode == GEMM_SWIGLU ? 2 * N_out : N_out);
-  return gemm_scratch_floats(N_out, T, p.S, mode, p.bn);
+  return gemm_scratch_floats(N_out, T, p.S, mode, p.bn, p.chunk, K_in);
 }
 
 static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *L) {
@@ -182,20 +183,20 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->ap = attn_plan(B, K, Hq, Hkv, dh, c->window, sms);
   // slice scratch shared by every reduce-mode GEMM (they run one after another)
   size_t sc = 0;
-  sc = std::max(sc, reduce_scratch(c, GW, T, L->P_gate, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, QKVW, T, L->P_qkv, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, D, T, L->P_o, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, F, T, L->P_gu, GEMM_SWIGLU));
-  sc = std::max(sc, reduce_scratch(c, D, T, L->P_down, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, r, TR, L->P_sel, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, V, TL, GemmPlan{0, 1}, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, GW, T, D, L->P_gate, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, QKVW, T, D, L->P_qkv, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, D, T, Hq * dh, L->P_o, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, F, T, D, L->P_gu, GEMM_SWIGLU));
+  sc = std::max(sc, reduce_scratch(c, D, T, F, L->P_down, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, r, TR, D, L->P_sel, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, V, TL, D, GemmPlan{0, 1}, GEMM_REDUCE));
   // injection GEMMs: the split depends on the token count; take the largest
   auto inj = [&](int n_out, int k_in) {
     size_t best = 0;
     auto eval = [&](int n) {
       if (n < 1 || n > N) return;
       const GemmPlan p = reduce_plan(c, n_out, n, k_in, GEMM_REDUCE, sms);
-      best = std::max(best, reduce_scratch(c, n_out, n, p, GEMM_REDUCE));
+      best = std::max(best, reduce_scratch(c, n_out, n, k_in, p, GEMM_REDUCE));
     };
     for (int n = 1; n <= 16; ++n) eval(n);
     for (int n = 32; n <= 256; n *= 2) eval(n);
@@ -262,6 +263,7 @@ static GemmCall reduce_call(const dflash_config &c, uint8_t *ws, const Layout &L
   g.X = X;
   g.T = T;
   g.S = S;
+  g.chunk = plan.chunk;
   g.mode = mode;
   g.out = (float *)(ws + L.scratch);
   g.out_f32 = out_f32;
@@ -331,16 +333,45 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
         reduce_call(c, ws, L, Wg, GW, D, X, T, L.P_gate, GEMM_REDUCE, gates, GW, nullptr, 0), st);
   };
 
+  // A few block rows: each conv is one launch with its gate linear fused (the
+  // pre-norm formed inside).  More rows: the gate linear is a tensor-core GEMM
+  // and the conv a row kernel.
+  const bool fused = gconv_fits(T, D, g, c.dtype);
+  auto conv_pre = [&](int l, int i, const void *gain) -> int {
+    const dflash_layer_weights &lw = w.layer[l];
+    if (fused)
+      return launch_gconv_pre<S>(x, T, K, D, g, (const S *)lw.conv_w[i],
+                                 (const S *)lw.conv_base[i], (const S *)gain, eps, ub, st);
+    int rc = gate_gemm(lw.conv_w[i], un);
+    if (rc != DFLASH_OK) return rc;
+    return launch_conv_pre<S>(un, gates, T, K, D, g, (const S *)lw.conv_base[i], ub, st);
+  };
+  // conv after a sublayer + residual; then the next pre-norm (row path) or,
+  // after the last layer, the final norm into zf
+  auto conv_post = [&](int l, int i, const void *next_gain, bool last) -> int {
+    const dflash_layer_weights &lw = w.layer[l];
+    int rc;
+    if (fused) {
+      rc = launch_gconv_post<S>(rf, rb, T, K, D, g, (const S *)lw.conv_w[i],
+                                (const S *)lw.conv_base[i], x, st);
+      if (rc != DFLASH_OK || !last) return rc;
+      return launch_final_norm<S>(x, B, K, D, (const S *)next_gain, eps, zf, st);
+    }
+    rc = gate_gemm(lw.conv_w[i], rb);
+    if (rc != DFLASH_OK) return rc;
+    return launch_conv_post_norm<S>(rf, gates, T, K, D, g, (const S *)lw.conv_base[i], x,
+                                    (const S *)next_gain, eps, un, last ? zf : (S *)nullptr, st);
+  };
+
   float2 *rope_cs = (float2 *)(ws + L.rope);
   TRY(launch_embed_norm<S>((const S *)w.embed, anchor, c.mask_token_id, V, B, K, D,
-                           (const S *)w.layer[0].attn_norm, eps, x, un, err, ctx_len, rope, dh / 2,
-                           rope_cs, st));
+                           (const S *)w.layer[0].attn_norm, eps, x, fused ? (S *)nullptr : un, err,
+                           ctx_len, rope, dh / 2, rope_cs, st));
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights &lw = w.layer[l];
     const bool last = l + 1 == c.n_layers;
     // attention sublayer: conv -> QKV -> norm/RoPE -> block attention -> O -> conv, residual
-    TRY(gate_gemm(lw.conv_w[0], un));
-    TRY(launch_conv_pre<S>(un, gates, T, K, D, g, (const S *)lw.conv_base[0], ub, st));
+    TRY(conv_pre(l, 0, lw.attn_norm));
     TRY(gemm_run(reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_REDUCE, qkv, QKVW,
                              nullptr, 0),
                  st));
@@ -360,22 +391,15 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     }
     TRY(gemm_run(reduce_call(c, ws, L, lw.wo, D, Hq * dh, ob, T, L.P_o, GEMM_REDUCE, rf, D, rb, D),
                  st));
-    TRY(gate_gemm(lw.conv_w[1], rb));
-    TRY(launch_conv_post_norm<S>(rf, gates, T, K, D, g, (const S *)lw.conv_base[1], x,
-                                 (const S *)lw.mlp_norm, eps, un, (S *)nullptr, st));
+    TRY(conv_post(l, 1, lw.mlp_norm, false));
     // MLP sublayer: conv -> gate/up + SwiGLU -> down -> conv, residual
-    TRY(gate_gemm(lw.conv_w[2], un));
-    TRY(launch_conv_pre<S>(un, gates, T, K, D, g, (const S *)lw.conv_base[2], ub, st));
+    TRY(conv_pre(l, 2, lw.mlp_norm));
     TRY(gemm_run(reduce_call(c, ws, L, lw.w_gate_up, F, D, ub, T, L.P_gu, GEMM_SWIGLU, nullptr, 0,
                              hb, F),
                  st));
     TRY(gemm_run(reduce_call(c, ws, L, lw.w_down, D, F, hb, T, L.P_down, GEMM_REDUCE, rf, D, rb, D),
                  st));
-    TRY(gate_gemm(lw.conv_w[3], rb));
-    TRY(launch_conv_post_norm<S>(
-        rf, gates, T, K, D, g, (const S *)lw.conv_base[3], x,
-        (const S *)(last ? w.final_norm : w.layer[l + 1].attn_norm), eps, un, last ? zf : (S *)nullptr,
-        st));
+    TRY(conv_post(l, 3, last ? w.final_norm : w.layer[l + 1].attn_norm, last));
   }
   const int TL = B * (K - 1);
   TRY(gemm_run(reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, GemmPlan{0, 1}, GEMM_REDUCE, logits, V, nullptr, 0),

@@ -46,6 +46,16 @@ struct GemmParams {
   int F;  // GEMM_SWIGLU: gate rows before the up rows
   int *counters;
   int *err;
+  // balanced schedule (chunk > 0, reduce modes): the k-block iterations of all
+  // tiles, tile after tile, are cut into equal chunks of `chunk`, one per CTA
+  int chunk, kb_total, total;
+  int nmax;  // slice slots per tile in the scratch
+};
+
+// One CTA's share of one tile: k-blocks [kb0, kb0 + nkb), slice `seg` of the
+// tile's `nseg` slices.
+struct Seg {
+  int m_tile, t_tile, kb0, nkb, seg, nseg;
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -67,6 +77,39 @@ __device__ __forceinline__ void unit_coords(int u, const GemmParams &p, int &m_t
   int r = u / p.m_tiles;
   split = r % p.S;
   t_tile = r / p.S;
+}
+
+// The i-th segment of this CTA; false when there is none.  Uniform schedule:
+// units blockIdx.x + i * gridDim.x, each one K slice of one tile.  Balanced
+// schedule: the CTA's chunk [blockIdx.x * chunk, + chunk) of the iteration
+// space cut at tile boundaries; a tile's slices come from consecutive CTAs.
+__device__ __forceinline__ bool get_seg(const GemmParams &p, int i, Seg &s) {
+  if (p.chunk == 0) {
+    const int u = blockIdx.x + i * gridDim.x;
+    if (u >= p.num_units) return false;
+    int split;
+    unit_coords(u, p, s.m_tile, s.t_tile, split);
+    s.kb0 = split * p.kb_per_split;
+    s.nkb = p.kb_per_split;
+    s.seg = split;
+    s.nseg = p.S;
+    return true;
+  }
+  const int pos0 = blockIdx.x * p.chunk;
+  const int end = min(pos0 + p.chunk, p.total);
+  const int tile = pos0 / p.kb_total + i;
+  const int start = i == 0 ? pos0 : tile * p.kb_total;
+  if (start >= end) return false;
+  const int stop = min(end, (tile + 1) * p.kb_total);
+  s.m_tile = tile % p.m_tiles;
+  s.t_tile = tile / p.m_tiles;
+  s.kb0 = start - tile * p.kb_total;
+  s.nkb = stop - start;
+  const int first = tile * p.kb_total / p.chunk;
+  const int last = ((tile + 1) * p.kb_total - 1) / p.chunk;
+  s.seg = blockIdx.x - first;
+  s.nseg = last - first + 1;
+  return true;
 }
 
 // Weight tile of unit m_tile: 128 consecutive rows, or for GEMM_SWIGLU the 64
@@ -178,36 +221,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int pre = 0;
       {
         int cnt = 0;
-        for (int u = blockIdx.x; u < p.num_units && cnt < STAGES; u += gridDim.x) {
-          int m_tile, t_tile, split;
-          unit_coords(u, p, m_tile, t_tile, split);
-          for (int kb = 0; kb < p.kb_per_split && cnt < STAGES; ++kb, ++cnt) {
+        Seg sg;
+        for (int i = 0; cnt < STAGES && get_seg(p, i, sg); ++i) {
+          for (int kb = 0; kb < sg.nkb && cnt < STAGES; ++kb, ++cnt) {
             mbar_expect_tx(&full[cnt], SH::STAGE_BYTES);
-            load_w(smem + cnt * SH::STAGE_BYTES, &tmW, &full[cnt],
-                   (split * p.kb_per_split + kb) * BK, m_tile, p, pol_w);
+            load_w(smem + cnt * SH::STAGE_BYTES, &tmW, &full[cnt], (sg.kb0 + kb) * BK, sg.m_tile,
+                   p, pol_w);
           }
         }
         pre = cnt;
       }
       pdl_wait();
       bool ok = true;
-      int n = 0;  // fill counter across units
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        int m_tile, t_tile, split;
-        unit_coords(u, p, m_tile, t_tile, split);
-        for (int kb = 0; kb < p.kb_per_split; ++kb, ++n) {
+      int n = 0;  // fill counter across segments
+      Seg sg;
+      for (int i = 0; ok && get_seg(p, i, sg); ++i) {
+        for (int kb = 0; kb < sg.nkb; ++kb, ++n) {
           uint8_t *sa = smem + stage * SH::STAGE_BYTES;
-          const int kx = (split * p.kb_per_split + kb) * BK;
+          const int kx = (sg.kb0 + kb) * BK;
           if (n < pre) {
-            tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, t_tile * BN, pol_x);
+            tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, sg.t_tile * BN, pol_x);
           } else {
             if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
               ok = false;
               break;
             }
             mbar_expect_tx(&full[stage], SH::STAGE_BYTES);
-            load_w(sa, &tmW, &full[stage], kx, m_tile, p, pol_w);
-            tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, t_tile * BN, pol_x);
+            load_w(sa, &tmW, &full[stage], kx, sg.m_tile, p, pol_w);
+            tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, sg.t_tile * BN, pol_x);
           }
           issued[stage] = true;
           last_phase[stage] = phase;
@@ -231,14 +272,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      Seg sg;
+      for (int i = 0; ok && get_seg(p, i, sg); ++i) {
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < p.kb_per_split; ++kb) {
+        for (int kb = 0; kb < sg.nkb; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -276,9 +318,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-      int m_tile, t_tile, split;
-      unit_coords(u, p, m_tile, t_tile, split);
+    Seg sg;
+    for (int i = 0; get_seg(p, i, sg); ++i) {
+      const int m_tile = sg.m_tile, t_tile = sg.t_tile, split = sg.seg;
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
@@ -297,7 +339,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               if (t0 + j < p.T) outp[(size_t)(t0 + j) * p.ld] = v[j];
           }
         }
-      } else if (p.S == 1) {
+      } else if (sg.nseg == 1) {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           if (tcol0 + c >= p.T) break;  // uniform across the epilogue warps
@@ -306,11 +348,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           epi_store(p, m_tile, row, tcol0 + c, v, xbuf);
         }
       } else {
-        // slice -> scratch (tile-contiguous, [column][row]), then a ticket
+        // slice -> scratch slot (tile, slice) ([column][row] inside), then a ticket
         const size_t tile = (size_t)t_tile * p.m_tiles + m_tile;
         const size_t tile_sz = (size_t)BM * BN;
-        const size_t slice_stride = (size_t)p.t_tiles * p.m_tiles * tile_sz;
-        float *mine = p.out + (size_t)split * slice_stride + tile * tile_sz + row;
+        float *mine = p.out + (tile * p.nmax + split) * tile_sz + row;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
           if (tcol0 + c >= p.T) break;
@@ -327,21 +368,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         epi_bar();
         if (threadIdx.x == 64) {
           const int old = atomicAdd(&p.counters[tile], 1);
-          s_last = old == p.S - 1;
+          s_last = old == sg.nseg - 1;
           if (s_last) p.counters[tile] = 0;
         }
         epi_bar();
         if (s_last) {
           __threadfence();
-          const float *base = p.out + tile * tile_sz + row;
+          const float *base = p.out + tile * p.nmax * tile_sz + row;
 #pragma unroll 1
           for (int c = 0; c < BN; c += 16) {
             if (tcol0 + c >= p.T) break;
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) v[j] = 0.f;
-            for (int q = 0; q < p.S; ++q) {
-              const float *src = base + (size_t)q * slice_stride + (size_t)c * BM;
+            for (int q = 0; q < sg.nseg; ++q) {
+              const float *src = base + (size_t)q * tile_sz + (size_t)c * BM;
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (size_t)j * BM);
             }
@@ -546,6 +587,38 @@ static double gemm_cost(int N_out, int T, int K_in, int S, int bn, int mode, int
   return tot;
 }
 
+int gemm_balanced_slots(int K_in, int chunk) {
+  const int kb = K_in / dfl::BK;
+  return chunk > 0 ? (kb + chunk - 1) / chunk + 1 : 1;
+}
+
+// Balanced schedule: every CTA streams `chunk` k-blocks (the iterations of all
+// tiles cut evenly over the SMs), so no wave is partly empty; tiles cut across
+// CTAs are reduced by their last CTA as in the split schedule.
+static double gemm_cost_balanced(int N_out, int T, int K_in, int bn, int num_sms, int *chunk_out) {
+  const int kb = K_in / dfl::BK;
+  const int t_tiles = (T + bn - 1) / bn;
+  const int m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
+  const long total = (long)m_tiles * t_tiles * kb;
+  const long chunk = (total + num_sms - 1) / num_sms;
+  *chunk_out = (int)chunk;
+  if (chunk < 2 || total > (1L << 30)) return 1e300;
+  const double per_kb = 128.0 * 64 * 2 + (double)bn * 64 * 2;
+  const int segs = (int)((chunk + kb - 1) / kb) + 1;
+  const double t_cta = std::max(chunk * per_kb / 60e3, 2.0 * 128 * bn * 64 * chunk / 11e6) +
+                       0.15 * segs;
+  const double wbytes = 2.0 * N_out * K_in;
+  const double hbm = wbytes * (wbytes > 48e6 ? t_tiles : 1) / 6.5e6;
+  double tot = std::max(t_cta, hbm);
+  if (chunk < kb || total % chunk) {  // cut tiles: slices written, then read by the last CTA
+    const int slots = gemm_balanced_slots(K_in, (int)chunk);
+    tot += (double)slots * std::min(bn, T) * 128 * 4 / 60e3;
+    tot += 2.0 * std::min<long>(num_sms, (long)m_tiles * t_tiles * slots) * 128 * std::min(bn, T) *
+           4 / 8e6;
+  }
+  return tot;
+}
+
 static GemmPlan plan_for(int N_out, int T, int K_in, int mode, int num_sms, int max_S,
                          bool choose_bn) {
   const int kb = K_in / dfl::BK;
@@ -562,6 +635,16 @@ static GemmPlan plan_for(int N_out, int T, int K_in, int mode, int num_sms, int 
       if (S > 1 && (size_t)S * T * N_out > kMaxPartialFloats) break;
       const double c = gemm_cost(N_out, T, K_in, S, bn, mode, num_sms);
       if (c < best_cost * 0.985) best_cost = c, best = GemmPlan{bn, S};
+    }
+    if (mode != GEMM_PARTIAL) {
+      int chunk = 0;
+      const double c = gemm_cost_balanced(N_out, T, K_in, bn, num_sms, &chunk);
+      const size_t fl = gemm_scratch_floats(mode == GEMM_SWIGLU ? N_out / 2 : N_out, T, 1, mode,
+                                            bn, chunk, K_in);
+      if (c < best_cost * 0.985 && fl <= kMaxPartialFloats) {
+        best_cost = c;
+        best = GemmPlan{bn, 1, chunk};
+      }
     }
   }
   return best;
@@ -582,11 +665,12 @@ size_t gemm_tiles(int N_out, int T, int mode, int bn) {
   return (size_t)((N_out + rows - 1) / rows) * ((T + bn - 1) / bn);
 }
 
-size_t gemm_scratch_floats(int N_out, int T, int S, int mode, int bn) {
+size_t gemm_scratch_floats(int N_out, int T, int S, int mode, int bn, int chunk, int K_in) {
   if (mode == GEMM_PARTIAL) return (size_t)S * T * N_out;
-  if (S <= 1) return 0;
   if (bn <= 0) bn = token_tile(T);
-  return (size_t)S * gemm_tiles(N_out, T, mode, bn) * dfl::BM * bn;
+  const size_t slots = chunk > 0 ? (size_t)gemm_balanced_slots(K_in, chunk) : (size_t)S;
+  if (slots <= 1) return 0;
+  return slots * gemm_tiles(N_out, T, mode, bn) * dfl::BM * bn;
 }
 
 template <int BN>
@@ -622,7 +706,22 @@ static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
   p.F = swiglu ? g.N_out : 0;
   p.counters = g.counters;
   p.err = g.err;
-  const int grid = p.num_units < d->num_sms ? p.num_units : d->num_sms;
+  p.chunk = 0;
+  p.kb_total = g.K_in / dfl::BK;
+  p.total = 0;
+  p.nmax = g.S;
+  int grid = p.num_units < d->num_sms ? p.num_units : d->num_sms;
+  if (g.chunk > 0) {
+    const long total = (long)p.m_tiles * p.t_tiles * p.kb_total;
+    if (total >= (1L << 30)) return DFLASH_ERR_DIMS;
+    p.chunk = g.chunk;
+    p.total = (int)total;
+    p.nmax = gemm_balanced_slots(g.K_in, g.chunk);
+    p.S = 1;
+    p.kb_per_split = p.kb_total;
+    p.num_units = p.m_tiles * p.t_tiles;
+    grid = (int)((total + g.chunk - 1) / g.chunk);
+  }
   DFL_CHECK_LAUNCH(launch(dfl::k_gemm_tc<BN>, dim3(grid), dim3(dfl::kGemmThreads),
                           (size_t)SH::SMEM_BYTES, st, mw, mx, p));
   return DFLASH_OK;
@@ -633,6 +732,8 @@ int gemm_run(const GemmCall &g, cudaStream_t st) {
   const Dev *d = device();
   if (!d) return DFLASH_ERR_DEVICE;
   if (g.K_in % 64 || g.S < 1 || (g.K_in / 64) % g.S) return DFLASH_ERR_DIMS;
+  if (g.chunk < 0 || (g.chunk > 0 && g.mode == GEMM_PARTIAL)) return DFLASH_ERR_DIMS;
+  if (g.chunk > 0 && (!g.counters || !g.out)) return DFLASH_ERR_NULL;
   if (g.mode == GEMM_SWIGLU && g.N_out % 64) return DFLASH_ERR_DIMS;
   if (g.mode != GEMM_PARTIAL && g.S > 1 && (!g.counters || !g.out)) return DFLASH_ERR_NULL;
   if (g.dtype == DFLASH_F32) {

@@ -16,8 +16,9 @@ int gemm_splits(int N_out, int T, int K_in, int num_sms, int max_S = 1 << 20);
 // Token tile and K split of one GEMM: picked by a cost model of the waves of
 // work units, the memory traffic, and (reduce modes) the last CTA's reduction.
 struct GemmPlan {
-  int bn;  // token tile: 16, 32, 64, 128 or 256
-  int S;   // K slices
+  int bn;         // token tile: 16, 32, 64, 128 or 256
+  int S;          // K slices (uniform schedule)
+  int chunk = 0;  // > 0: balanced schedule, k-block iterations per CTA (reduce modes)
 };
 GemmPlan gemm_plan(int N_out, int T, int K_in, int mode, int num_sms, int max_S);
 
@@ -35,6 +36,7 @@ struct GemmCall {
   const void *X = nullptr;
   int T = 0;
   int S = 1;
+  int chunk = 0;       // > 0: balanced schedule (reduce modes; S is then ignored)
   int bn = 0;          // token tile; 0 = the smallest tile that holds T (at most 256)
   int mode = GEMM_PARTIAL;
   float *out = nullptr;       // GEMM_PARTIAL output, or the slice scratch of the other modes
@@ -46,8 +48,11 @@ struct GemmCall {
   int *err = nullptr;
 };
 
-// Floats of slice scratch a reduce-mode GEMM needs (0 when S == 1).
-size_t gemm_scratch_floats(int N_out, int T, int S, int mode, int bn = 0);
+// Floats of slice scratch a reduce-mode GEMM needs (0 when S == 1 and chunk == 0).
+size_t gemm_scratch_floats(int N_out, int T, int S, int mode, int bn = 0, int chunk = 0,
+                           int K_in = 0);
+// Slice slots per tile of the balanced schedule.
+int gemm_balanced_slots(int K_in, int chunk);
 // Tile tickets a reduce-mode GEMM needs.
 size_t gemm_tiles(int N_out, int T, int mode, int bn = 0);
 

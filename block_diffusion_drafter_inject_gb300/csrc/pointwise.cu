@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(512) k_embed_norm(const S *__restrict__ E,
     for (int j = 0; j < 8; ++j) ss += v[j] * v[j];
   }
   const float inv = rsqrtf(block_sum(ss, red) / D + eps);
+  if (!un) return;
   for (int c = threadIdx.x * 8; c < D; c += blockDim.x * 8) {
     float v[8], g[8];
     load8(e + c, v);
@@ -296,6 +297,408 @@ __global__ void k_inject_store(const float *__restrict__ kvf, int N, int L, int 
   stf(dst + i + half, hi);
 }
 
+// ---------------------------------------------------------------------------
+// Two-tap conv with its gate linear fused, for a few block rows (T <= 16).
+//
+// The gate linear s = G u (G [2D/g, D]) is tiny next to the projections, and
+// at T <= 16 its cost is the latency of a GEMM launch plus its split-K
+// reduction.  Here one CTA owns NG channel groups: it stages its 2*NG gate
+// rows in shared memory before waiting for the producer, forms the T gate
+// pre-activations of those rows itself (fp32 dot products of full rows), and
+// applies the conv to its NG*g channels.  PRE also forms u = R(rmsnorm(x))
+// from the fp32 residual stream (sums of squares over the full rows, then
+// u = (x * inv) * gain rounded to storage).
+// ---------------------------------------------------------------------------
+
+// 8 consecutive storage elements, global -> shared, asynchronously (16-byte aligned)
+__device__ __forceinline__ void copy8_async(bf16 *d, const bf16 *s) {
+  cp_async16(smem_u32(d), s, 16);
+}
+__device__ __forceinline__ void copy8_async(float *d, const float *s) {
+  cp_async16(smem_u32(d), s, 16);
+  cp_async16(smem_u32(d + 4), s + 4, 16);
+}
+
+// Warp sum of N per-lane values by recursive halving (N a power of two): at
+// offset o = 16, 8, ... each lane keeps one half of its values and adds the
+// partner's copy of that half.  Afterwards lane L holds the totals of entries
+// rs_first<N>(L) .. + N/32 - 1 in v[0..) (N >= 32), or of entry rs_first<N>(L)
+// in v[0] (N < 32; the remaining offsets are summed as a butterfly).  The
+// order of additions is fixed, so the result is deterministic.
+template <int N>
+struct RS {
+  static constexpr int H = N >= 32 ? 5 : N >= 16 ? 4 : N >= 8 ? 3 : N >= 4 ? 2 : N >= 2 ? 1 : 0;
+};
+template <int N>
+__device__ __forceinline__ int rs_first(int lane) {
+  int idx = 0;
+#pragma unroll
+  for (int l = 0; l < RS<N>::H; ++l)
+    if (lane & (16 >> l)) idx += N >> (l + 1);
+  return idx;
+}
+template <int N>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
+#pragma unroll
+  for (int l = 0; l < RS<N>::H; ++l) {
+    const int o = 16 >> l;
+    const bool up = (lane & o) != 0;
+    const int h = N >> (l + 1);
+#pragma unroll
+    for (int j = 0; j < h; ++j) {
+      const float send = up ? v[j] : v[j + h];
+      const float keep = up ? v[j + h] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+#pragma unroll
+  for (int o = 16 >> RS<N>::H; o > 0; o >>= 1)
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+}
+
+constexpr int kGcMaxT = 16;
+
+template <typename S>
+struct GconvArgs {
+  int T, K, D, group;
+  const S *G;        // gate linear [2D/group, D]
+  const S *base;     // [2D]
+  const float *x;    // residual stream [T, D]: PRE reads it; POST adds the conv to it
+  float *xo;         // POST: the residual stream (same array as x)
+  const S *gain;     // PRE: pre-norm weight [D]
+  float eps;
+  S *ub;             // PRE: conv output [T, D]
+  const S *gin;      // POST: gate input R(r) [T, D]
+  const float *rf;   // POST: conv input r [T, D]
+};
+
+// grid (2D/g / (2*NG)), block 256; dynamic shared: (R2 + PRE) * D elements of S.
+template <typename S, int R2, bool PRE>
+__global__ void __launch_bounds__(256) k_gconv(const GconvArgs<S> A) {
+  constexpr int NG = R2 / 2, N = kGcMaxT * R2;
+  extern __shared__ __align__(16) uint8_t gc_smem[];
+  S *sG = (S *)gc_smem;   // [R2][D]: rows a_{j0..}, then b_{j0..}
+  S *sGain = sG + (size_t)R2 * A.D;
+  __shared__ float red[8][N];
+  __shared__ float s_s[N];   // gate pre-activations [t][R2]
+  __shared__ float s_inv[kGcMaxT];
+  pdl_launch();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int D = A.D, T = A.T, nv = D / 8, GW = D / A.group;
+  const int j0 = blockIdx.x * NG;
+  for (int e = tid; e < R2 * nv; e += blockDim.x) {
+    const int r = e / nv, v = e % nv;
+    const int grow = r < NG ? j0 + r : GW + j0 + (r - NG);
+    copy8_async(sG + (size_t)r * D + 8 * v, A.G + (size_t)grow * D + 8 * v);
+  }
+  if (PRE)
+    for (int v = tid; v < nv; v += blockDim.x) copy8_async(sGain + 8 * v, A.gain + 8 * v);
+  cp_async_commit();
+  pdl_wait();
+
+  if (PRE) {  // inverse RMS of every row
+    float ss[kGcMaxT];
+#pragma unroll
+    for (int t = 0; t < kGcMaxT; ++t) ss[t] = 0.f;
+    for (int v = tid; v < nv; v += blockDim.x) {
+#pragma unroll
+      for (int t = 0; t < kGcMaxT; ++t) {
+        if (t < T) {
+          float xv[8];
+          load8(A.x + (size_t)t * D + 8 * v, xv);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) ss[t] += xv[j] * xv[j];
+        }
+      }
+    }
+    warp_reduce_scatter<kGcMaxT>(ss, lane);
+    if ((lane & 1) == 0) red[warp][lane >> 1] = ss[0];
+    __syncthreads();
+    if (tid < kGcMaxT) {
+      float s = 0.f;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w][tid];
+      s_inv[tid] = rsqrtf(s / D + A.eps);
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // s_inv, the staged rows; red is reused below
+
+  float acc[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) acc[i] = 0.f;
+  for (int v = tid; v < nv; v += blockDim.x) {
+    float gw[R2][8], gn[8];
+#pragma unroll
+    for (int r = 0; r < R2; ++r) load8(sG + (size_t)r * D + 8 * v, gw[r]);
+    if (PRE) load8(sGain + 8 * v, gn);
+#pragma unroll
+    for (int t = 0; t < kGcMaxT; ++t) {
+      if (t < T) {
+        float u[8];
+        if (PRE) {
+          load8(A.x + (size_t)t * D + 8 * v, u);
+          const float inv = s_inv[t];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) u[j] = rnd(u[j] * inv * gn[j], (const S *)nullptr);
+        } else {
+          load8(A.gin + (size_t)t * D + 8 * v, u);
+        }
+#pragma unroll
+        for (int r = 0; r < R2; ++r)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[t * R2 + r] += u[j] * gw[r][j];
+      }
+    }
+  }
+  warp_reduce_scatter<N>(acc, lane);
+  {
+    const int f = rs_first<N>(lane);
+#pragma unroll
+    for (int m = 0; m < N / 32; ++m) red[warp][f + m] = acc[m];
+  }
+  __syncthreads();
+  if (tid < N) {
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w][tid];
+    s_s[tid] = s;
+  }
+  __syncthreads();
+
+  // the conv on this CTA's channels
+  const int c0 = j0 * A.group, nc = NG * A.group;
+  for (int e = tid; e < T * nc; e += blockDim.x) {
+    const int t = e / nc, c = c0 + e % nc, gl = c / A.group - j0;
+    const float a = sigmoidf_(ldf(A.base + c) + s_s[t * R2 + gl]);
+    const float b = sigmoidf_(ldf(A.base + D + c) + s_s[t * R2 + NG + gl]);
+    const bool first = (t % A.K) == 0;
+    const size_t o = (size_t)t * D + c;
+    if (PRE) {
+      const float g = ldf(sGain + c);
+      const float cur = rnd(A.x[o] * s_inv[t] * g, (const S *)nullptr);
+      const float prev = first ? 0.f : rnd(A.x[o - D] * s_inv[t - 1] * g, (const S *)nullptr);
+      stf(A.ub + o, a * cur + b * prev);
+    } else {
+      const float cur = A.rf[o], prev = first ? 0.f : A.rf[o - D];
+      A.xo[o] = A.x[o] + (a * cur + b * prev);
+    }
+  }
+}
+
+// bf16 storage: the same op on tensor cores, one thread-block cluster of C
+// CTAs per NGc (<= 8) channel groups.  CTA rank q takes the channel slice
+// [q*D/C, (q+1)*D/C) of the gate products: it stages its slice of the
+// cluster's 2*NGc gate rows (zero rows up to 16) and of the T input rows (zero
+// rows up to 16) in XOR-swizzled shared memory and runs mma.sync m16n8k16
+// (tokens x gate rows) over it.  The C partial 16x16 tiles (and, for PRE, the
+// C partial sums of squares of the rows) are read through distributed shared
+// memory and summed in rank order, so every CTA holds the same totals.  Rank
+// q then applies the conv to its W = NGc*g/C channels of the cluster's groups.
+// The slice is DS = D/C wide with DS/8 (a power of two, <= 128) 16-byte chunks.
+// Dynamic shared: 64 * DS bytes (+ 2 * DS for PRE's gain slice).
+template <bool PRE, int C>
+__global__ void __launch_bounds__(256) k_gconv_cl(const GconvArgs<bf16> A, int NGc) {
+  constexpr int MAXI = 8;  // PRE: input rows per thread (16 rows x DS/8 chunks / 256)
+  extern __shared__ __align__(128) uint8_t gc_sm[];
+  const int D = A.D, T = A.T, GW = D / A.group;
+  const int DS = D / C, nvs = DS / 8, RBs = DS * 2;
+  uint8_t *sG = gc_sm;                     // [16][DS], swizzled
+  uint8_t *sU = sG + 16 * RBs;             // [16][DS], swizzled
+  bf16 *sGain = (bf16 *)(sU + 16 * RBs);   // [DS] (PRE)
+  __shared__ float red[8][256];            // per-warp partial tiles [t][16]
+  __shared__ float s_part[256];            // this CTA's partial tile (read by the peers)
+  __shared__ float s_tot[256];             // the cluster's sums
+  __shared__ float s_ssw[4][16];
+  __shared__ float s_ssq[16];              // this CTA's partial sums of squares (read by peers)
+  __shared__ float s_inv[16];
+  pdl_launch();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q = (int)cluster_rank(), cl = blockIdx.x / C;
+  const int j0 = cl * NGc, R = 2 * NGc, d0 = q * DS;
+  const uint32_t uG = smem_u32(sG), uU = smem_u32(sU);
+  for (int e = tid; e < 16 * nvs; e += 256) {
+    const int r = e / nvs, v = e % nvs;
+    const bool ok = r < R;
+    const int grow = r < NGc ? j0 + r : GW + j0 + (r - NGc);
+    cp_async16(uG + swz(r, v, RBs),
+               ok ? (const void *)(A.G + (size_t)grow * D + d0 + 8 * v) : (const void *)A.G,
+               ok ? 16 : 0);
+  }
+  if (PRE)
+    for (int v = tid; v < nvs; v += 256) cp_async16(smem_u32(sGain + 8 * v), A.gain + d0 + 8 * v, 16);
+  cp_async_commit();
+  pdl_wait();
+
+  if (!PRE) {
+    for (int e = tid; e < 16 * nvs; e += 256) {
+      const int t = e / nvs, v = e % nvs;
+      const bool ok = t < T;
+      cp_async16(uU + swz(t, v, RBs),
+                 ok ? (const void *)(A.gin + (size_t)t * D + d0 + 8 * v) : (const void *)A.gin,
+                 ok ? 16 : 0);
+    }
+    cp_async_commit();
+  } else {
+    // this thread's chunk v of rows t0 + j * tstep (nvs divides 256)
+    const int v = tid % nvs, tstep = 256 / nvs, t0 = tid / nvs;
+    float xv[MAXI][8];
+    float ss[MAXI];
+#pragma unroll
+    for (int j = 0; j < MAXI; ++j) {
+      const int t = t0 + j * tstep;
+      if (t < T) {
+        load8(A.x + (size_t)t * D + d0 + 8 * v, xv[j]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xv[j][k] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < MAXI; ++j) {
+      ss[j] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ss[j] += xv[j][k] * xv[j][k];
+    }
+    // sum over the lanes that hold the same row (aligned groups of min(nvs, 32))
+    const int span = nvs < 32 ? nvs : 32;
+    for (int o = span >> 1; o > 0; o >>= 1)
+#pragma unroll
+      for (int j = 0; j < MAXI; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], o);
+    if (lane % span == 0)
+#pragma unroll
+      for (int j = 0; j < MAXI; ++j) {
+        const int t = t0 + j * tstep;
+        if (t < 16) s_ssw[v / span][t] = ss[j];
+      }
+    __syncthreads();
+    if (tid < 16) {
+      float a = 0.f;
+      for (int g = 0; g < (nvs + 31) / 32; ++g) a += s_ssw[g][tid];
+      s_ssq[tid] = a;
+    }
+    cluster_sync();  // partial sums of squares visible to the cluster
+    if (tid < 16) {
+      float a = 0.f;
+      for (int r = 0; r < C; ++r) a += ld_dsmem(smem_u32(&s_ssq[tid]), (uint32_t)r);
+      s_inv[tid] = rsqrtf(a / D + A.eps);
+    }
+    cp_async_wait<0>();  // the gain slice
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < MAXI; ++j) {
+      const int t = t0 + j * tstep;
+      if (t < 16) {
+        uint4 pk = make_uint4(0u, 0u, 0u, 0u);
+        if (t < T) {
+          float gn[8];
+          load8(sGain + 8 * v, gn);
+          const float inv = s_inv[t];
+          pk.x = pack_bf16(xv[j][0] * inv * gn[0], xv[j][1] * inv * gn[1]);
+          pk.y = pack_bf16(xv[j][2] * inv * gn[2], xv[j][3] * inv * gn[3]);
+          pk.z = pack_bf16(xv[j][4] * inv * gn[4], xv[j][5] * inv * gn[5]);
+          pk.w = pack_bf16(xv[j][6] * inv * gn[6], xv[j][7] * inv * gn[7]);
+        }
+        *(uint4 *)(sU + swz(t, v, RBs)) = pk;
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // partial s[t][r] over this slice: tokens are the mma rows, gate rows the columns
+  float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    const int r8 = lane & 7, mi = lane >> 3;
+    const int nks = DS / 16;
+    for (int ks = warp * 2; ks < nks; ks += 16) {
+      uint32_t a0[4], a1[4], b0[4], b1[4];
+      ldsm_x4(uU + swz((mi & 1) * 8 + r8, 2 * ks + (mi >> 1), RBs), a0[0], a0[1], a0[2], a0[3]);
+      ldsm_x4(uU + swz((mi & 1) * 8 + r8, 2 * ks + 2 + (mi >> 1), RBs), a1[0], a1[1], a1[2],
+              a1[3]);
+      ldsm_x4(uG + swz(r8, 2 * ks + mi, RBs), b0[0], b0[1], b0[2], b0[3]);
+      ldsm_x4(uG + swz(8 + r8, 2 * ks + mi, RBs), b1[0], b1[1], b1[2], b1[3]);
+      mma_bf16_16816(c0, a0, b0[0], b0[1]);
+      mma_bf16_16816(c0, a1, b0[2], b0[3]);
+      mma_bf16_16816(c1, a0, b1[0], b1[1]);
+      mma_bf16_16816(c1, a1, b1[2], b1[3]);
+    }
+  }
+  {
+    const int g8 = lane >> 2, t4 = lane & 3;
+    float *rw = red[warp];
+    rw[g8 * 16 + 2 * t4] = c0[0];
+    rw[g8 * 16 + 2 * t4 + 1] = c0[1];
+    rw[(g8 + 8) * 16 + 2 * t4] = c0[2];
+    rw[(g8 + 8) * 16 + 2 * t4 + 1] = c0[3];
+    rw[g8 * 16 + 8 + 2 * t4] = c1[0];
+    rw[g8 * 16 + 8 + 2 * t4 + 1] = c1[1];
+    rw[(g8 + 8) * 16 + 8 + 2 * t4] = c1[2];
+    rw[(g8 + 8) * 16 + 8 + 2 * t4 + 1] = c1[3];
+  }
+  __syncthreads();
+  {
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) a += red[w][tid];
+    s_part[tid] = a;
+  }
+  cluster_sync();  // partial tiles visible to the cluster
+  {
+    float a = 0.f;
+    for (int r = 0; r < C; ++r) a += ld_dsmem(smem_u32(&s_part[tid]), (uint32_t)r);
+    s_tot[tid] = a;
+  }
+  __syncthreads();
+
+  // the conv on this CTA's channels
+  const int W = NGc * A.group / C;
+  const int cb = j0 * A.group + q * W;
+  for (int e = tid; e < T * W; e += 256) {
+    const int t = e / W, ch = cb + e % W, gl = ch / A.group - j0;
+    const float a = sigmoidf_(ldf(A.base + ch) + s_tot[t * 16 + gl]);
+    const float b = sigmoidf_(ldf(A.base + D + ch) + s_tot[t * 16 + NGc + gl]);
+    const bool first = (t % A.K) == 0;
+    const size_t o = (size_t)t * D + ch;
+    if (PRE) {
+      const float g = ldf(A.gain + ch);
+      const float cur = rnd(A.x[o] * s_inv[t] * g, (const bf16 *)nullptr);
+      const float prev = first ? 0.f : rnd(A.x[o - D] * s_inv[t - 1] * g, (const bf16 *)nullptr);
+      stf(A.ub + o, a * cur + b * prev);
+    } else {
+      const float cur = A.rf[o], prev = first ? 0.f : A.rf[o - D];
+      A.xo[o] = A.x[o] + (a * cur + b * prev);
+    }
+  }
+  cluster_sync();  // the peers have read s_part (and s_ssq) before this CTA exits
+}
+
+// zf[b*(K-1) + i-1] = gain * x[b*K + i] / rms(x[b*K + i]) for slots i >= 1.
+template <typename S>
+__global__ void __launch_bounds__(512) k_final_norm(const float *__restrict__ x, int K, int D,
+                                                    const S *__restrict__ gain, float eps,
+                                                    S *__restrict__ zf) {
+  __shared__ float red[32];
+  pdl_launch();
+  pdl_wait();
+  const int o = blockIdx.x, b = o / (K - 1), i = o % (K - 1) + 1;
+  const float *row = x + ((size_t)b * K + i) * D;
+  float ss = 0.f;
+  for (int c = threadIdx.x * 8; c < D; c += blockDim.x * 8) {
+    float v[8];
+    load8(row + c, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += v[j] * v[j];
+  }
+  const float inv = rsqrtf(block_sum(ss, red) / D + eps);
+  for (int c = threadIdx.x * 8; c < D; c += blockDim.x * 8) {
+    float v[8], g[8];
+    load8(row + c, v);
+    load8(gain + c, g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = v[j] * inv * g[j];
+    store8(zf + (size_t)o * D + c, v);
+  }
+}
+
 }  // namespace dfl
 
 namespace dflh {
@@ -371,6 +774,126 @@ int launch_inject_store(const float *kvf, int N, int L, int Hkv, int dh, LayerPt
   return DFLASH_OK;
 }
 
+template <typename S, int R2, bool PRE>
+static int launch_gconv_t(const dfl::GconvArgs<S> &a, cudaStream_t st) {
+  const size_t smem = (size_t)(R2 + (PRE ? 1 : 0)) * a.D * sizeof(S);
+  static int attr_done = 0;
+  if (smem > 48 * 1024 && !attr_done) {
+    if (cudaFuncSetAttribute(dfl::k_gconv<S, R2, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_done = 1;
+  }
+  const int groups = a.D / a.group;
+  DFL_CHECK_LAUNCH(
+      launch(dfl::k_gconv<S, R2, PRE>, dim3(groups / (R2 / 2)), dim3(256), smem, st, a));
+  return DFLASH_OK;
+}
+
+// Cluster size C and groups per cluster NGc of the bf16 fused conv for width D
+// and group size g; false when the shape does not fit it.
+static bool gconv_cluster_shape(int D, int g, int *C, int *NGc) {
+  const int groups = D / g;
+  for (int c : {4, 8, 2}) {
+    if (D % (32 * c)) continue;
+    const int nvs = D / c / 8;
+    if (nvs > 128 || (nvs & (nvs - 1))) continue;
+    for (int n : {8, 4, 2, 1}) {
+      if (groups % n || (n * g) % c) continue;
+      *C = c;
+      *NGc = n;
+      return true;
+    }
+  }
+  return false;
+}
+
+template <bool PRE, int C>
+static int launch_gconv_cl_t(const dfl::GconvArgs<dfl::bf16> &a, int ngc, cudaStream_t st) {
+  const int DS = a.D / C;
+  const size_t smem = (size_t)64 * DS + (PRE ? (size_t)2 * DS : 0);
+  static int attr_done = 0;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(dfl::k_gconv_cl<PRE, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             66 * 1024 /* DS <= 1024 */) !=
+        cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_done = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.D / a.group / ngc) * C);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  count_launch();
+  DFL_CHECK_LAUNCH(cudaLaunchKernelEx(&cfg, dfl::k_gconv_cl<PRE, C>, a, ngc));
+  return DFLASH_OK;
+}
+
+template <bool PRE>
+static int launch_gconv_cl(const dfl::GconvArgs<dfl::bf16> &a, cudaStream_t st) {
+  int C = 0, ngc = 0;
+  if (!gconv_cluster_shape(a.D, a.group, &C, &ngc)) return DFLASH_ERR_DIMS;
+  if (C == 4) return launch_gconv_cl_t<PRE, 4>(a, ngc, st);
+  if (C == 8) return launch_gconv_cl_t<PRE, 8>(a, ngc, st);
+  return launch_gconv_cl_t<PRE, 2>(a, ngc, st);
+}
+
+template <typename S>
+static int launch_gconv(bool pre, const dfl::GconvArgs<S> &a, cudaStream_t st) {
+  if (!gconv_fits(a.T, a.D, a.group, sizeof(S) == 2 ? DFLASH_BF16 : DFLASH_F32))
+    return DFLASH_ERR_DIMS;
+  const int groups = a.D / a.group;
+  if constexpr (sizeof(S) == 2) {
+    return pre ? launch_gconv_cl<true>(a, st) : launch_gconv_cl<false>(a, st);
+  } else {
+    const bool two = groups % 2 == 0 && groups >= 256;  // two groups per CTA on wide models
+    if (pre) return two ? launch_gconv_t<S, 4, true>(a, st) : launch_gconv_t<S, 2, true>(a, st);
+    return two ? launch_gconv_t<S, 4, false>(a, st) : launch_gconv_t<S, 2, false>(a, st);
+  }
+}
+
+bool gconv_fits(int T, int D, int group, int dtype) {
+  if (T < 1 || T > kGconvMaxT) return false;
+  int C, ngc;
+  if (dtype == DFLASH_BF16) return gconv_cluster_shape(D, group, &C, &ngc);
+  return (size_t)5 * D * 4 <= 160 * 1024;
+}
+
+template <typename S>
+int launch_gconv_pre(const float *x, int T, int K, int D, int group, const S *G, const S *base,
+                     const S *gain, float eps, S *ub, cudaStream_t st) {
+  dfl::GconvArgs<S> a = {};
+  a.T = T, a.K = K, a.D = D, a.group = group, a.G = G, a.base = base;
+  a.x = x, a.gain = gain, a.eps = eps, a.ub = ub;
+  return launch_gconv<S>(true, a, st);
+}
+template <typename S>
+int launch_gconv_post(const float *rf, const S *gin, int T, int K, int D, int group, const S *G,
+                      const S *base, float *x, cudaStream_t st) {
+  dfl::GconvArgs<S> a = {};
+  a.T = T, a.K = K, a.D = D, a.group = group, a.G = G, a.base = base;
+  a.x = x, a.xo = x, a.gin = gin, a.rf = rf;
+  return launch_gconv<S>(false, a, st);
+}
+template <typename S>
+int launch_final_norm(const float *x, int B, int K, int D, const S *gain, float eps, S *zf,
+                      cudaStream_t st) {
+  DFL_CHECK_LAUNCH(launch(dfl::k_final_norm<S>, dim3(B * (K - 1)),
+                          dim3(D >= 4096 ? 512 : D >= 1024 ? 128 : 32), 0, st, x, K, D, gain, eps,
+                          zf));
+  return DFLASH_OK;
+}
+
 #define DFL_INST(S)                                                                              \
   template int launch_embed_norm<S>(const S *, const int32_t *, int, int, int, int, int, const S *, \
                                     float, float *, S *, int *, const int32_t *,                 \
@@ -387,7 +910,13 @@ int launch_inject_store(const float *kvf, int N, int L, int Hkv, int dh, LayerPt
   template int launch_inject_store<S>(const float *, int, int, int, int, LayerPtrs,              \
                                       const int32_t *, const int32_t *, const int32_t *, int,    \
                                       int, int, int, const float2 *, float, S *, S *, int *,     \
-                                      cudaStream_t);
+                                      cudaStream_t);                                             \
+  template int launch_gconv_pre<S>(const float *, int, int, int, int, const S *, const S *,      \
+                                   const S *, float, S *, cudaStream_t);                         \
+  template int launch_gconv_post<S>(const float *, const S *, int, int, int, int, const S *,     \
+                                    const S *, float *, cudaStream_t);                           \
+  template int launch_final_norm<S>(const float *, int, int, int, const S *, float, S *,         \
+                                    cudaStream_t);
 DFL_INST(float)
 DFL_INST(dfl::bf16)
 

@@ -34,6 +34,22 @@ template <typename S>
 int launch_conv_post_norm(const float *rf, const float *gate, int rows, int K, int D, int group,
                           const S *base, float *x, const S *gain, float eps, S *un, S *zf,
                           cudaStream_t st);
+// Two-tap conv with its gate linear fused, for T <= kGconvMaxT block rows
+// (one launch per conv).  PRE: ub = conv(u) with u = R(rmsnorm(x, gain)) formed
+// here from the fp32 residual x.  POST: x += conv(rf) with the gates of gin.
+constexpr int kGconvMaxT = 16;
+// whether the fused conv takes T rows of width D with channel groups of `group`
+bool gconv_fits(int T, int D, int group, int dtype);
+template <typename S>
+int launch_gconv_pre(const float *x, int T, int K, int D, int group, const S *G, const S *base,
+                     const S *gain, float eps, S *ub, cudaStream_t st);
+template <typename S>
+int launch_gconv_post(const float *rf, const S *gin, int T, int K, int D, int group, const S *G,
+                      const S *base, float *x, cudaStream_t st);
+// zf: RMSNorm of the rows of slots 1..K-1, written compactly [B*(K-1), D].
+template <typename S>
+int launch_final_norm(const float *x, int B, int K, int D, const S *gain, float eps, S *zf,
+                      cudaStream_t st);
 template <typename S>
 int launch_qkv_post(const float *qkv, int rows, int K, int Hq, int Hkv, int dh, const S *qn,
                     const S *kn, const float2 *rope_cs, float eps, S *qb, S *kb, S *vb,
