@@ -372,16 +372,26 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     const bool last = l + 1 == c.n_layers;
     // attention sublayer: conv -> QKV -> norm/RoPE -> block attention -> O -> conv, residual
     TRY(conv_pre(l, 0, lw.attn_norm));
-    TRY(gemm_run(reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_REDUCE, qkv, QKVW,
-                             nullptr, 0),
-                 st));
     if constexpr (sizeof(S) == 2) {
-      TRY(launch_attention_fused(L.ap, qkv, (const dfl::bf16 *)lw.q_norm,
-                                 (const dfl::bf16 *)lw.k_norm, rope_cs, eps, (const dfl::bf16 *)kv.k,
-                                 (const dfl::bf16 *)kv.v, l, kv.page_table, kv.max_pages_per_req,
-                                 kv.num_pages, c.page_size, ctx_len, B, K, Hq, Hkv, dh, c.window,
-                                 (dfl::bf16 *)ob, err, st));
+      // the projection's epilogue applies the q/k head norms and RoPE: bf16 q, k, v rows
+      dfl::bf16 *qkvb = (dfl::bf16 *)(ws + L.qkv);
+      GemmCall gq = reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_QKV, nullptr, 0,
+                                qkvb, QKVW);
+      gq.q_norm = lw.q_norm;
+      gq.k_norm = lw.k_norm;
+      gq.rope_cs = rope_cs;
+      gq.Hq = Hq;
+      gq.Hkv = Hkv;
+      gq.dh = dh;
+      gq.eps = eps;
+      TRY(gemm_run(gq, st));
+      TRY(launch_attention_fused(L.ap, qkvb, (const dfl::bf16 *)kv.k, (const dfl::bf16 *)kv.v, l,
+                                 kv.page_table, kv.max_pages_per_req, kv.num_pages, c.page_size,
+                                 ctx_len, B, K, Hq, Hkv, dh, c.window, (dfl::bf16 *)ob, err, st));
     } else {
+      TRY(gemm_run(reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_REDUCE, qkv, QKVW,
+                               nullptr, 0),
+                   st));
       TRY(launch_qkv_post<S>(qkv, T, K, Hq, Hkv, dh, (const S *)lw.q_norm, (const S *)lw.k_norm,
                              rope_cs, eps, qb, kb, vb, st));
       TRY(launch_block_attention<S>(L.ap, qb, kb, vb, (const S *)kv.k, (const S *)kv.v, l,

@@ -15,6 +15,11 @@ namespace dfl {
 
 constexpr int kQG = 64;   // query rows per CTA
 constexpr int kCH = 64;   // keys per shared-memory tile
+constexpr int kAttnStages = 3;  // K/V tile stages of the tensor-core kernel
+constexpr int kPageAhead = 3;   // tiles whose pages a loader thread holds ahead
+// receive buffer of the cluster combine: (kQG + 16) rows x (DH + 2) floats, DH <= 128;
+// the combine weights [rows][nsplit <= 16] follow it
+constexpr int kAttnRecvBytes = (64 + 16) * (128 + 2) * 4;
 
 template <typename S, int DH>
 __global__ void __launch_bounds__(256) k_attn_split(
@@ -160,69 +165,14 @@ __global__ void __launch_bounds__(256) k_attn_split(
 // a double-buffered, XOR-swizzled shared layout that ldmatrix reads without
 // bank conflicts.  Online softmax in base 2; partial state in natural units.
 // ---------------------------------------------------------------------------
-// Up to R head rows of the fp32 QKV projection -> RMSNorm(gain) -> RoPE ->
-// bf16 into swizzled shared rows; one warp, lane holds d = lane + 32e.  All
-// global loads of the batch are issued before any arithmetic.
-//   src[q]: row q's projection (nullptr: write zeros); cs[q]: its RoPE
-//   (cos, sin) row (nullptr: no RoPE); gain nullptr: no norm, no RoPE.
-template <int DH, int R>
-__device__ __forceinline__ void norm_rope_rows(const float *const *src, const float2 *const *cs,
-                                               const int *dst_row, int nrows, const bf16 *gain,
-                                               float eps, uint8_t *base, int RB, int lane) {
-  constexpr int E = DH / 32;
-  float v[R][E];
-  float2 rc[R][E / 2];
-#pragma unroll
-  for (int q = 0; q < R; ++q) {
-#pragma unroll
-    for (int e = 0; e < E; ++e)
-      v[q][e] = (q < nrows && src[q]) ? src[q][lane + 32 * e] : 0.f;
-#pragma unroll
-    for (int e = 0; e < E / 2; ++e)
-      rc[q][e] = (q < nrows && gain && cs[q]) ? cs[q][lane + 32 * e] : make_float2(1.f, 0.f);
-  }
-  float g[E];
-  if (gain) {
-#pragma unroll
-    for (int e = 0; e < E; ++e) g[e] = __bfloat162float(gain[lane + 32 * e]);
-  }
-#pragma unroll
-  for (int q = 0; q < R; ++q) {
-    if (q >= nrows) break;
-    if (gain && src[q]) {
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) ss += v[q][e] * v[q][e];
-      ss = warp_sum(ss);
-      const float inv = rsqrtf(ss / DH + eps);
-#pragma unroll
-      for (int e = 0; e < E; ++e) v[q][e] = v[q][e] * inv * g[e];
-#pragma unroll
-      for (int e = 0; e < E / 2; ++e) {  // pairs (i, i + DH/2), i = lane + 32e
-        const float lo = v[q][e], hi = v[q][e + E / 2];
-        v[q][e] = lo * rc[q][e].x - hi * rc[q][e].y;
-        v[q][e + E / 2] = hi * rc[q][e].x + lo * rc[q][e].y;
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      const int d = lane + 32 * e;
-      *(bf16 *)(base + swz(dst_row[q], d >> 3, RB) + (d & 7) * 2) = __float2bfloat16_rn(v[q][e]);
-    }
-  }
-}
-
 struct AttnArgs {
-  const float *qkv;  // [B*K, (Hq + 2Hkv) * DH] fp32
-  const bf16 *q_norm, *k_norm;
+  const bf16 *qkvb;  // [B*K, (Hq + 2Hkv) * DH]: q, k normed and rotated, v
   const bf16 *kc, *vc;
   size_t layer_off;
   const int32_t *table;
   int max_pages, num_pages, P;
   const int32_t *ctx_len;
   int K, Hq, Hkv, window, kps, nsplit, nqg;
-  float eps;
-  const float2 *rope_cs;  // [B*K, DH/2] (cos, sin) of each block slot's position
   bf16 *ob;  // [B*K, Hq*DH]
   int *err;
 };
@@ -237,13 +187,14 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
   constexpr int CHUNKS = DH / 8;   // 16-byte chunks per row
   constexpr int RB = DH * 2;       // bytes per row
   constexpr int TILE = CH * RB;    // bytes per K (or V) tile
+  constexpr int NST = kAttnStages; // tile stages in flight
+  constexpr int QROWS = 64 / KP;   // query rows staged (row blocks x 16)
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_valid[2][CH];
+  __shared__ int s_valid[NST][CH];
   uint8_t *pQ = smem;
-  uint8_t *pK0 = smem + kQG * RB;
-  uint8_t *pV0 = pK0 + 2 * TILE;
+  uint8_t *pK0 = smem + QROWS * RB;
   uint8_t *pRecv = pK0;  // after the tile loop: [nsplit][per][DH + 2] fp32, written by the peers
-  const uint32_t sQ = smem_u32(pQ), sK0 = smem_u32(pK0), sV0 = smem_u32(pV0);
+  const uint32_t sQ = smem_u32(pQ), sK0 = smem_u32(pK0), sV0 = sK0 + NST * TILE;
   pdl_launch();
   pdl_wait();
 
@@ -258,78 +209,70 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
   const int k_end = min(n_keys, k_begin + A.kps);
   const int ntiles = k_begin < n_keys ? (k_end - k_begin + CH - 1) / CH : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bf16 *blk = A.qkvb + (size_t)b * A.K * QKVW;  // this request's block rows
 
-  // queries: head norm + RoPE of the projection rows, qr = i*grp + g; warp w
-  // stages rows 16w .. 16w+15 in two batches of 8
-  for (int half = 0; half < 2; ++half) {
-    const float *src[8];
-    const float2 *cs[8];
-    int dst[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int row = warp * 16 + half * 8 + q, qrg = qgi * kQG + row;
-      dst[q] = row;
-      src[q] = nullptr;
-      cs[q] = nullptr;
-      if (qrg < QR) {
-        const int i = qrg / grp, g = qrg % grp;
-        src[q] = A.qkv + (size_t)(b * A.K + i) * QKVW + (size_t)(kvh * grp + g) * DH;
-        cs[q] = A.rope_cs + (size_t)(b * A.K + i) * (DH / 2);
-      }
-    }
-    norm_rope_rows<DH, 8>(src, cs, dst, 8, A.q_norm, A.eps, pQ, RB, lane);
-  }
-  auto load_tile = [&](int t, int stage) {
-    const int t0 = k_begin + t * CH;
-    for (int e = tid; e < CH * CHUNKS; e += 128) {
-      const int j = e / CHUNKS, c = e % CHUNKS;
-      const int key = t0 + j;
-      if (key >= n_ctx && key < k_end) continue;  // block slot: computed below
-      const bf16 *srck = A.kc, *srcv = A.vc;
-      int ok = 0;
-      if (key < k_end) {
-        const int p = lo + key, pi = p / A.P;
-        const int page = pi < A.max_pages ? A.table[(size_t)b * A.max_pages + pi] : -1;
-        if (page >= 0 && page < A.num_pages) {
-          const size_t off =
-              A.layer_off + (((size_t)page * A.Hkv + kvh) * A.P + (p % A.P)) * DH + c * 8;
-          srck = A.kc + off;
-          srcv = A.vc + off;
-          ok = 1;
-        } else if (c == 0) {
-          set_err(A.err, pi < A.max_pages ? DFLASH_DEV_PAGE_RANGE : DFLASH_DEV_POS_RANGE);
-        }
-      }
-      cp_async16(sK0 + stage * TILE + swz(j, c, RB), srck, ok ? 16 : 0);
-      cp_async16(sV0 + stage * TILE + swz(j, c, RB), srcv, ok ? 16 : 0);
-      if (c == 0) s_valid[stage][j] = ok;
-    }
-    // block slots of this tile: k = RoPE(k_norm(.)), v as projected; warp w takes
-    // the block rows j = w, w+4, ... (batches of 4)
-    {
-      const int jb0 = max(0, n_ctx - t0), jb1 = min(CH, k_end - t0);  // block rows [jb0, jb1)
-      for (int j0 = jb0 + warp * 4; j0 < jb1; j0 += 16) {
-        const float *sk[4], *sv[4];
-        const float2 *cs[4];
-        int dst[4];
-        const int nr = min(4, jb1 - j0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int j = j0 + q, i = q < nr ? t0 + j - n_ctx : 0;
-          dst[q] = j;
-          const float *row = A.qkv + (size_t)(b * A.K + i) * QKVW;
-          sk[q] = row + (size_t)(A.Hq + kvh) * DH;
-          sv[q] = row + (size_t)(A.Hq + A.Hkv + kvh) * DH;
-          cs[q] = A.rope_cs + (size_t)(b * A.K + i) * (DH / 2);
-        }
-        norm_rope_rows<DH, 4>(sk, cs, dst, nr, A.k_norm, A.eps, pK0 + stage * TILE, RB, lane);
-        norm_rope_rows<DH, 4>(sv, cs, dst, nr, nullptr, A.eps, pV0 + stage * TILE, RB, lane);
-        if (lane < nr) s_valid[stage][j0 + lane] = 1;
-      }
-    }
+  // Loader: thread tid copies key row jrow = tid / 2 of every tile, chunks
+  // [ch0, ch0 + CHUNKS/2) of its K and V rows: a context key from the paged
+  // cache, a block slot from the projection rows, nothing (zeros) past the end.
+  // The page of a context key is looked up kPageAhead tiles before the tile is
+  // loaded (a register pipeline), so table reads never sit in front of copies.
+  const int jrow = tid >> 1, ch0 = (tid & 1) * (CHUNKS / 2);
+  auto key_page = [&](int t) -> int {  // >= 0 page; -1 not a context key; < -1 error bit
+    const int key = k_begin + t * CH + jrow;
+    if (t >= ntiles || key >= k_end || key >= n_ctx) return -1;
+    const int pi = (lo + key) / A.P;
+    if (pi >= A.max_pages) return -DFLASH_DEV_POS_RANGE;
+    const int page = A.table[(size_t)b * A.max_pages + pi];
+    return (page >= 0 && page < A.num_pages) ? page : -DFLASH_DEV_PAGE_RANGE;
   };
-  if (ntiles > 0) load_tile(0, 0);
-  cp_async_commit();
+  auto load_tile = [&](int t, int stage, int page) {
+    const int key = k_begin + t * CH + jrow;
+    const bf16 *srck = A.kc, *srcv = A.vc;
+    int ok = 0;
+    if (key < k_end && key < n_ctx) {
+      if (page >= 0) {
+        const size_t off =
+            A.layer_off + (((size_t)page * A.Hkv + kvh) * A.P + ((lo + key) % A.P)) * DH;
+        srck = A.kc + off;
+        srcv = A.vc + off;
+        ok = 1;
+      } else if (ch0 == 0) {
+        set_err(A.err, -page);
+      }
+    } else if (key < k_end) {  // block slot i
+      const bf16 *row = blk + (size_t)(key - n_ctx) * QKVW;
+      srck = row + (size_t)(A.Hq + kvh) * DH;
+      srcv = row + (size_t)(A.Hq + A.Hkv + kvh) * DH;
+      ok = 1;
+    }
+#pragma unroll
+    for (int c = ch0; c < ch0 + CHUNKS / 2; ++c) {
+      cp_async16(sK0 + stage * TILE + swz(jrow, c, RB), srck + c * 8, ok ? 16 : 0);
+      cp_async16(sV0 + stage * TILE + swz(jrow, c, RB), srcv + c * 8, ok ? 16 : 0);
+    }
+    if (ch0 == 0) s_valid[stage][jrow] = ok;
+  };
+  static_assert(kPageAhead == 3 && NST == 3, "page pipeline below holds three tiles");
+  static_assert(DFLASH_DEV_PAGE_RANGE > 1 && DFLASH_DEV_POS_RANGE > 1, "error codes vs -1");
+  int pg0 = key_page(0), pg1 = key_page(1), pg2 = key_page(2);
+
+  // queries qr = i*grp + g of this group: projection rows, copied (zeros past QR)
+  for (int e = tid; e < QROWS * CHUNKS; e += 128) {
+    const int row = e / CHUNKS, c = e % CHUNKS, qrg = qgi * kQG + row;
+    const bool ok = qrg < QR;
+    const bf16 *src = ok ? blk + (size_t)(qrg / grp) * QKVW + (size_t)(kvh * grp + qrg % grp) * DH
+                         : A.qkvb;
+    cp_async16(sQ + swz(row, c, RB), src + c * 8, ok ? 16 : 0);
+  }
+  // the first NST-1 tiles in flight; one commit group per tile (empty past the end)
+#pragma unroll
+  for (int t = 0; t < NST - 1; ++t) {
+    if (t < ntiles) load_tile(t, t, t == 0 ? pg0 : pg1);
+    cp_async_commit();
+  }
+  pg0 = pg2;  // page of tile NST-1 = 2
+  pg1 = key_page(3);
+  pg2 = key_page(4);
 
   constexpr int RW = 4 / KP;            // query row blocks per CTA
   constexpr int KW = CH / KP;           // keys of a tile per warp
@@ -343,15 +286,20 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
   for (int n = 0; n < DH / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
+  int stage = 0;
   for (int t = 0; t < ntiles; ++t) {
-    const int stage = t & 1;
-    if (t + 1 < ntiles) {
-      load_tile(t + 1, stage ^ 1);
+    // tile t + NST - 1 into the stage tile t - 1 used (free since the loop's end barrier)
+    {
+      const int tn = t + NST - 1;
+      int sn = stage + NST - 1;
+      if (sn >= NST) sn -= NST;
+      if (tn < ntiles) load_tile(tn, sn, pg0);
       cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+      pg0 = pg1;
+      pg1 = pg2;
+      pg2 = key_page(t + NST + 2);
     }
+    cp_async_wait<NST - 1>();  // tile t has landed
     __syncthreads();
     if (t == 0 && active) {
 #pragma unroll
@@ -441,6 +389,7 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
       }
     }
     __syncthreads();
+    if (++stage == NST) stage = 0;
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -518,20 +467,28 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
   cluster_sync();
   const int r0 = split * per, r1 = min(nrows, r0 + per);
   const float *rv = (const float *)pRecv;
-  for (int e = tid; e < (r1 - r0) * DH; e += 128) {
-    const int lr = e / DH, d = e % DH;
+  // weights of the splits of each owned row: w_q = e^(m_q - M) / sum_q e^(m_q - M) l_q
+  float *wts = (float *)(pRecv + kAttnRecvBytes);  // [per][nsplit]
+  for (int lr = tid; lr < r1 - r0; lr += 128) {
     float M = -INFINITY;
     for (int q = 0; q < A.nsplit; ++q) M = fmaxf(M, rv[(q * per + lr) * RS]);
-    float L = 0.f, O = 0.f;
+    float L = 0.f;
     for (int q = 0; q < A.nsplit; ++q) {
-      const float *src = rv + (q * per + lr) * RS;
-      if (src[0] == -INFINITY) continue;
-      const float w = expf(src[0] - M);
-      L += w * src[1];
-      O += w * src[2 + d];
+      const float m = rv[(q * per + lr) * RS];
+      const float w = m == -INFINITY ? 0.f : expf(m - M);
+      wts[lr * A.nsplit + q] = w;
+      L += w * rv[(q * per + lr) * RS + 1];
     }
+    const float il = 1.f / L;
+    for (int q = 0; q < A.nsplit; ++q) wts[lr * A.nsplit + q] *= il;
+  }
+  __syncthreads();
+  for (int e = tid; e < (r1 - r0) * DH; e += 128) {
+    const int lr = e / DH, d = e % DH;
+    float O = 0.f;
+    for (int q = 0; q < A.nsplit; ++q) O += wts[lr * A.nsplit + q] * rv[(q * per + lr) * RS + 2 + d];
     const int qrg = qgi * kQG + r0 + lr, i = qrg / grp, g = qrg % grp;
-    A.ob[((size_t)(b * A.K + i) * A.Hq + kvh * grp + g) * DH + d] = __float2bfloat16_rn(O / L);
+    A.ob[((size_t)(b * A.K + i) * A.Hq + kvh * grp + g) * DH + d] = __float2bfloat16_rn(O);
   }
 }
 
@@ -615,17 +572,17 @@ static int launch_attn_dh(const AttnPlan &pl, const S *qb, const S *kb, const S 
 }
 
 template <int DH, int KP>
-static int launch_attn_fused(const AttnPlan &pl, const float *qkv, const dfl::bf16 *qn,
-                             const dfl::bf16 *kn, const float2 *rope_cs, float eps,
-                             const dfl::bf16 *kc, const dfl::bf16 *vc, int layer,
-                             const int32_t *table, int max_pages, int num_pages, int P,
-                             const int32_t *ctx_len, int B, int K, int Hq, int Hkv, int window,
-                             dfl::bf16 *ob, int *err, cudaStream_t st) {
-  // Q, two K and two V tiles; the key-part merge and the receive buffer
-  // (nsplit * ceil(rows/nsplit) <= kQG + 16 rows of DH + 2 floats) reuse the
-  // tile buffers after the tile loop
-  static_assert((dfl::kQG + 16) * (DH + 2) * 4 <= 4 * dfl::kCH * DH * 2, "receive buffer");
-  const size_t smem = (size_t)dfl::kQG * DH * 2 + 4 * (size_t)dfl::kCH * DH * 2;
+static int launch_attn_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl::bf16 *kc,
+                             const dfl::bf16 *vc, int layer, const int32_t *table, int max_pages,
+                             int num_pages, int P, const int32_t *ctx_len, int B, int K, int Hq,
+                             int Hkv, int window, dfl::bf16 *ob, int *err, cudaStream_t st) {
+  // Q and NST K and V tiles; the key-part merge, the receive buffer and the
+  // combine weights reuse the tile buffers after the tile loop
+  static_assert(dfl::kAttnRecvBytes + (dfl::kQG + 16) * 16 * 4 <=
+                    2 * dfl::kAttnStages * dfl::kCH * DH * 2,
+                "receive buffer and combine weights in the tile buffers");
+  const size_t smem =
+      (size_t)(64 / KP) * DH * 2 + 2 * (size_t)dfl::kAttnStages * dfl::kCH * DH * 2;
   static int attr_done = 0;
   if (!attr_done) {
     if (cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -636,9 +593,7 @@ static int launch_attn_fused(const AttnPlan &pl, const float *qkv, const dfl::bf
     attr_done = 1;
   }
   dfl::AttnArgs a;
-  a.qkv = qkv;
-  a.q_norm = qn;
-  a.k_norm = kn;
+  a.qkvb = qkvb;
   a.kc = kc;
   a.vc = vc;
   a.layer_off = (size_t)layer * num_pages * Hkv * P * DH;
@@ -654,8 +609,6 @@ static int launch_attn_fused(const AttnPlan &pl, const float *qkv, const dfl::bf
   a.kps = pl.kps;
   a.nsplit = pl.nsplit;
   a.nqg = pl.nqg;
-  a.eps = eps;
-  a.rope_cs = rope_cs;
   a.ob = ob;
   a.err = err;
   cudaLaunchConfig_t cfg = {};
@@ -677,18 +630,15 @@ static int launch_attn_fused(const AttnPlan &pl, const float *qkv, const dfl::bf
   return DFLASH_OK;
 }
 
-int launch_attention_fused(const AttnPlan &pl, const float *qkv, const dfl::bf16 *qn,
-                           const dfl::bf16 *kn, const float2 *rope_cs, float eps,
-                           const dfl::bf16 *kc, const dfl::bf16 *vc, int layer,
-                           const int32_t *table, int max_pages, int num_pages, int P,
-                           const int32_t *ctx_len, int B, int K, int Hq, int Hkv, int dh,
-                           int window, dfl::bf16 *ob, int *err, cudaStream_t st) {
+int launch_attention_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl::bf16 *kc,
+                           const dfl::bf16 *vc, int layer, const int32_t *table, int max_pages,
+                           int num_pages, int P, const int32_t *ctx_len, int B, int K, int Hq,
+                           int Hkv, int dh, int window, dfl::bf16 *ob, int *err, cudaStream_t st) {
   const int QR = K * (Hq / Hkv);
   const int kp = QR <= 16 ? 4 : QR <= 32 ? 2 : 1;
-#define DFL_ATTN(D, KPV)                                                                        \
-  return launch_attn_fused<D, KPV>(pl, qkv, qn, kn, rope_cs, eps, kc, vc, layer, table,         \
-                                   max_pages, num_pages, P, ctx_len, B, K, Hq, Hkv, window, ob, \
-                                   err, st)
+#define DFL_ATTN(D, KPV)                                                                      \
+  return launch_attn_fused<D, KPV>(pl, qkvb, kc, vc, layer, table, max_pages, num_pages, P,   \
+                                   ctx_len, B, K, Hq, Hkv, window, ob, err, st)
   if (dh == 128) {
     if (kp == 4) DFL_ATTN(128, 4);
     if (kp == 2) DFL_ATTN(128, 2);

@@ -23,15 +23,13 @@ int launch_block_attention(const AttnPlan &pl, const S *qb, const S *kb, const S
                            int B, int K, int Hq, int Hkv, int dh, int window, float *part, S *ob,
                            int *err, cudaStream_t st);
 
-// bf16 storage: one kernel per layer reads the fp32 QKV projection [B*K,
-// (Hq+2Hkv)*dh], applies the q/k head norms and RoPE while staging, attends, and
-// merges its key splits through the cluster's distributed shared memory into
-// o [B*K, Hq*dh].  rope_cs: [B*K, dh/2] (cos, sin) of each block slot.
-int launch_attention_fused(const AttnPlan &pl, const float *qkv, const dfl::bf16 *qn,
-                           const dfl::bf16 *kn, const float2 *rope_cs, float eps,
-                           const dfl::bf16 *kc, const dfl::bf16 *vc, int layer,
-                           const int32_t *table, int max_pages, int num_pages, int P,
-                           const int32_t *ctx_len, int B, int K, int Hq, int Hkv, int dh,
-                           int window, dfl::bf16 *ob, int *err, cudaStream_t st);
+// bf16 storage: one kernel per layer reads the block's q, k (head-normed and
+// rotated) and v rows from qkvb [B*K, (Hq+2Hkv)*dh] and the paged context
+// window, attends, and merges its key splits through the cluster's distributed
+// shared memory into o [B*K, Hq*dh].
+int launch_attention_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl::bf16 *kc,
+                           const dfl::bf16 *vc, int layer, const int32_t *table, int max_pages,
+                           int num_pages, int P, const int32_t *ctx_len, int B, int K, int Hq,
+                           int Hkv, int dh, int window, dfl::bf16 *ob, int *err, cudaStream_t st);
 
 }  // namespace dflh

@@ -63,6 +63,43 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Warp sum of N per-lane values by recursive halving (N a power of two): at
+// offset o = 16, 8, ... each lane keeps one half of its values and adds the
+// partner's copy of that half.  Afterwards lane L holds the totals of entries
+// rs_first<N>(L) .. + N/32 - 1 in v[0..) (N >= 32), or of entry rs_first<N>(L)
+// in v[0] (N < 32; the remaining offsets are summed as a butterfly).  The
+// order of additions is fixed, so the result is deterministic.
+template <int N>
+struct RS {
+  static constexpr int H = N >= 32 ? 5 : N >= 16 ? 4 : N >= 8 ? 3 : N >= 4 ? 2 : N >= 2 ? 1 : 0;
+};
+template <int N>
+__device__ __forceinline__ int rs_first(int lane) {
+  int idx = 0;
+#pragma unroll
+  for (int l = 0; l < RS<N>::H; ++l)
+    if (lane & (16 >> l)) idx += N >> (l + 1);
+  return idx;
+}
+template <int N>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
+#pragma unroll
+  for (int l = 0; l < RS<N>::H; ++l) {
+    const int o = 16 >> l;
+    const bool up = (lane & o) != 0;
+    const int h = N >> (l + 1);
+#pragma unroll
+    for (int j = 0; j < h; ++j) {
+      const float send = up ? v[j] : v[j + h];
+      const float keep = up ? v[j + h] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+#pragma unroll
+  for (int o = 16 >> RS<N>::H; o > 0; o >>= 1)
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+}
+
 // Sum over the block; `red` is shared scratch of >= 32 floats. All threads get the sum.
 __device__ __forceinline__ float block_sum(float v, float *red) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;

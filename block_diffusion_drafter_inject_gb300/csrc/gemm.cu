@@ -6,7 +6,9 @@
 //   warp 1     tensor-memory allocator and tcgen05.mma issuer (M=128, N=BN, K=16
 //              per instruction), fp32 accumulators in tensor memory, double
 //              buffered so the epilogue of one work unit overlaps the next unit
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, coalesced fp32 stores
+//   warps 2-9  epilogue, two groups of four (one warp per tensor-memory lane
+//              quarter each) on alternate 16-column chunks: tcgen05.ld of the
+//              accumulator, coalesced stores
 // The weight matrix is the M operand ("swap AB"): at draft batch sizes the token
 // count is 8..256, so weights stream through the M dimension and tokens fill N.
 // A work unit is (weight tile, token tile, K slice); the CTA's pipeline runs on
@@ -31,7 +33,8 @@ namespace dfl {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kGemmThreads = 192;
+constexpr int kEpiGroups = 2;                         // epilogue warp groups
+constexpr int kGemmThreads = 64 + kEpiGroups * 128;   // producer, MMA, epilogue warps
 
 struct GemmParams {
   float *out;  // GEMM_PARTIAL output / slice scratch
@@ -50,6 +53,11 @@ struct GemmParams {
   // tiles, tile after tile, are cut into equal chunks of `chunk`, one per CTA
   int chunk, kb_total, total;
   int nmax;  // slice slots per tile in the scratch
+  // GEMM_QKV: head RMSNorm (q and k heads) + rotate-half RoPE, bf16 out
+  const bf16 *q_norm, *k_norm;
+  const float2 *rope_cs;  // [T][dh/2] (cos, sin)
+  int Hq, Hkv, dh;
+  float eps;
 };
 
 // One CTA's share of one tile: k-blocks [kb0, kb0 + nkb), slice `seg` of the
@@ -58,7 +66,13 @@ struct Seg {
   int m_tile, t_tile, kb0, nkb, seg, nseg;
 };
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// named barriers: 1 + eg for epilogue group eg, 3 for all epilogue warps
+__device__ __forceinline__ void epi_bar(int eg) {
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + eg) : "memory");
+}
+__device__ __forceinline__ void epi_all_bar() {
+  asm volatile("bar.sync 3, %0;" ::"n"(kEpiGroups * 128) : "memory");
+}
 
 template <int BN>
 struct GemmShape {
@@ -70,13 +84,19 @@ struct GemmShape {
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
+// Tile index -> (weight tile, token tile): token tile fastest, so that the CTAs
+// holding the token tiles of one weight tile run together and the weight tile
+// is read from HBM once (the others hit L2); the activations are small enough
+// to stay in L2 throughout.
+__device__ __forceinline__ void tile_coords(int tile, const GemmParams &p, int &m_tile,
+                                            int &t_tile) {
+  t_tile = tile % p.t_tiles;
+  m_tile = tile / p.t_tiles;
+}
 __device__ __forceinline__ void unit_coords(int u, const GemmParams &p, int &m_tile, int &t_tile,
                                             int &split) {
-  // weight tile fastest: CTAs working at the same time share activation tiles in L2
-  m_tile = u % p.m_tiles;
-  int r = u / p.m_tiles;
-  split = r % p.S;
-  t_tile = r / p.S;
+  split = u % p.S;  // the slices of one tile are adjacent units
+  tile_coords(u / p.S, p, m_tile, t_tile);
 }
 
 // The i-th segment of this CTA; false when there is none.  Uniform schedule:
@@ -101,8 +121,7 @@ __device__ __forceinline__ bool get_seg(const GemmParams &p, int i, Seg &s) {
   const int start = i == 0 ? pos0 : tile * p.kb_total;
   if (start >= end) return false;
   const int stop = min(end, (tile + 1) * p.kb_total);
-  s.m_tile = tile % p.m_tiles;
-  s.t_tile = tile / p.m_tiles;
+  tile_coords(tile, p, s.m_tile, s.t_tile);
   s.kb0 = start - tile * p.kb_total;
   s.nkb = stop - start;
   const int first = tile * p.kb_total / p.chunk;
@@ -125,10 +144,55 @@ __device__ __forceinline__ void load_w(uint8_t *dst, const CUtensorMap *m, uint6
 }
 
 // Final values v[16] of row `row` (0..127) of tile m_tile, columns c0..c0+15.
-// All four epilogue warps call this in step (SwiGLU exchanges through xbuf).
+// The four warps of epilogue group eg call this in step (SwiGLU and the head
+// norm exchange through the group's xbuf [128][17] and xss [4][16]).
 __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int row, int c0,
-                                          const float *v, float *xbuf) {
-  if (p.mode == 1) {
+                                          float *v, float *xbuf, float *xss, int eg) {
+  if (p.mode == 3) {
+    // row n of the QKV projection: head h = n / dh, feature d = n % dh; a tile
+    // holds 128 / dh whole heads.  q and k heads: y = RMSNorm(x) * gain, then
+    // RoPE on the pairs (d, d + dh/2) with the token's (cos, sin); v heads as is.
+    const int lane = row & 31, quarter = row >> 5;
+    const int n = m_tile * BM + row, dh = p.dh, half = dh >> 1;
+    const int h = n / dh, d = n - h * dh;
+    const bool is_q = h < p.Hq, normed = h < p.Hq + p.Hkv;
+    float ss[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) ss[j] = v[j] * v[j];
+    warp_reduce_scatter<16>(ss, lane);  // lane L: token L >> 1 over this warp's 32 rows
+    if ((lane & 1) == 0) xss[quarter * 16 + (lane >> 1)] = ss[0];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) xbuf[row * 17 + j] = v[j];
+    epi_bar(eg);
+    if (normed && n < p.N_out) {
+      const bf16 *gain = is_q ? p.q_norm : p.k_norm;
+      const int w0 = (row - d) >> 5, nw = dh >> 5;  // the head's warps
+      const int pr = d < half ? row + half : row - half, di = d < half ? d : d - half;
+      const float g = __bfloat162float(gain[d]), gp = __bfloat162float(gain[d < half ? d + half : d - half]);
+      // every load of the chunk before its first store (stores may alias the table)
+      float2 cs[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        cs[j] = c0 + j < p.T ? __ldg(&p.rope_cs[(size_t)(c0 + j) * half + di]) : make_float2(1.f, 0.f);
+      float o[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float sq = 0.f;
+        for (int w = 0; w < nw; ++w) sq += xss[(w0 + w) * 16 + j];
+        const float inv = rsqrtf(sq / dh + p.eps);
+        const float x = v[j] * inv * g, y = xbuf[pr * 17 + j] * inv * gp;
+        o[j] = d < half ? x * cs[j].x - y * cs[j].y : x * cs[j].x + y * cs[j].y;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < p.T) p.out_bf16[(size_t)(c0 + j) * p.ldb + n] = __float2bfloat16_rn(o[j]);
+    } else if (n < p.N_out) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (c0 + j < p.T) p.out_bf16[(size_t)(c0 + j) * p.ldb + n] = __float2bfloat16_rn(v[j]);
+    }
+    epi_bar(eg);
+  } else if (p.mode == 1) {
     const int n = m_tile * BM + row;
     if (n < p.N_out) {
 #pragma unroll
@@ -146,7 +210,7 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
 #pragma unroll
       for (int j = 0; j < 16; ++j) xbuf[(row - 64) * 17 + j] = v[j];
     }
-    epi_bar();
+    epi_bar(eg);
     if (row < 64) {
       const int f = m_tile * 64 + row;
 #pragma unroll
@@ -158,7 +222,7 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
         }
       }
     }
-    epi_bar();
+    epi_bar(eg);
   }
 }
 
@@ -188,7 +252,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], 4 * kEpiGroups);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -262,6 +326,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (issued[s]) mbar_wait(&full[s], last_phase[s], (volatile int *)&dummy);
       }
     }
+    __syncwarp();  // lane 0 rejoins its warp before the block-wide barrier below
   } else if (warp == 1) {
     pdl_wait();
     if (lane == 0) {
@@ -309,13 +374,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         (void)mbar_wait(drain, 0, (volatile int *)&dummy);
       }
     }
+    __syncwarp();  // lane 0 rejoins its warp before the block-wide barrier below
   } else {
-    // ---------------- epilogue: warps 2..5 ----------------
+    // ---------------- epilogue: warps 2..9 ----------------
+    // two groups of four warps (each group covers the four tensor-memory lane
+    // quarters); group eg takes the 16-column chunks c = 16*eg + 32*i
     pdl_wait();
-    __shared__ float xbuf[64 * 17];
+    __shared__ float xbuf[kEpiGroups][128 * 17];
+    __shared__ float xss[kEpiGroups][4 * 16];
     __shared__ int s_last;
     const int quarter = warp & 3;  // tensor-memory lanes this warp may read
+    const int eg = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
+    float *gx = xbuf[eg], *gs = xss[eg];
     int acc = 0;
     uint32_t acc_phase = 0;
     Seg sg;
@@ -329,7 +400,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int n = m_tile * BM + row;
         float *outp = p.out + (size_t)split * p.T * p.ld + n;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
+        for (int c = 16 * eg; c < BN; c += 32) {
           float v[16];
           tc_ld16(taddr + c, v);
           const int t0 = tcol0 + c;
@@ -341,11 +412,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       } else if (sg.nseg == 1) {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
-          if (tcol0 + c >= p.T) break;  // uniform across the epilogue warps
+        for (int c = 16 * eg; c < BN; c += 32) {
+          if (tcol0 + c >= p.T) break;  // uniform across the group
           float v[16];
           tc_ld16(taddr + c, v);
-          epi_store(p, m_tile, row, tcol0 + c, v, xbuf);
+          epi_store(p, m_tile, row, tcol0 + c, v, gx, gs, eg);
         }
       } else {
         // slice -> scratch slot (tile, slice) ([column][row] inside), then a ticket
@@ -353,7 +424,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const size_t tile_sz = (size_t)BM * BN;
         float *mine = p.out + (tile * p.nmax + split) * tile_sz + row;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
+        for (int c = 16 * eg; c < BN; c += 32) {
           if (tcol0 + c >= p.T) break;
           float v[16];
           tc_ld16(taddr + c, v);
@@ -365,28 +436,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
         __threadfence();
-        epi_bar();
+        epi_all_bar();
         if (threadIdx.x == 64) {
           const int old = atomicAdd(&p.counters[tile], 1);
           s_last = old == sg.nseg - 1;
           if (s_last) p.counters[tile] = 0;
         }
-        epi_bar();
+        epi_all_bar();
         if (s_last) {
           __threadfence();
+          // sum the slices in slice order, CPI of the group's chunks per pass so
+          // that the loads of several chunks and slices are in flight together
+          constexpr int CPI = BN >= 128 ? 4 : BN >= 64 ? 2 : 1;
           const float *base = p.out + tile * p.nmax * tile_sz + row;
 #pragma unroll 1
-          for (int c = 0; c < BN; c += 16) {
+          for (int c = 16 * eg; c < BN; c += 32 * CPI) {
             if (tcol0 + c >= p.T) break;
-            float v[16];
+            float v[CPI][16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+            for (int k = 0; k < CPI; ++k)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[k][j] = 0.f;
+#pragma unroll 2
             for (int q = 0; q < sg.nseg; ++q) {
-              const float *src = base + (size_t)q * tile_sz + (size_t)c * BM;
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] += __ldcg(src + (size_t)j * BM);
+              for (int k = 0; k < CPI; ++k) {
+                const int cc = c + 32 * k;
+                if (cc < BN && tcol0 + cc < p.T) {
+                  const float *src = base + (size_t)q * tile_sz + (size_t)cc * BM;
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) v[k][j] += __ldcg(src + (size_t)j * BM);
+                }
+              }
             }
-            epi_store(p, m_tile, row, tcol0 + c, v, xbuf);
+#pragma unroll
+            for (int k = 0; k < CPI; ++k) {
+              const int cc = c + 32 * k;
+              if (cc < BN && tcol0 + cc < p.T)  // uniform across the group
+                epi_store(p, m_tile, row, tcol0 + cc, v[k], gx, gs, eg);
+            }
           }
         }
         if (++acc == 2) acc = 0, acc_phase ^= 1;
@@ -558,9 +646,31 @@ static bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t 
 
 static int token_tile(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
 
+// One k-block of one CTA (microseconds): the slowest of the weight tile from
+// HBM (~60 GB/s per CTA), both tiles through TMA (~110 GB/s per CTA, the
+// activation tile mostly from L2) and the tensor pipe (~11 TFLOP/s per CTA).
+static double stage_us(int bn) {
+  const double a = 128.0 * 64 * 2, b = (double)bn * 64 * 2;
+  return std::max(std::max(a / 60e3, (a + b) / 110e3), 2.0 * 128 * bn * 64 / 11e6);
+}
+
+// Epilogue of one tile (microseconds): per 16-column chunk a tensor-memory
+// load and the stores, plus the exchange of the SwiGLU / head-norm modes.
+static double epilogue_us(int bn, int T, int mode) {
+  const int chunks = (std::min(bn, T) + 15) / 16;
+  return chunks * (mode == GEMM_REDUCE ? 0.25 : 0.45);
+}
+// Tail of a split tile: the slice stores, the ticket, then the last CTA reads
+// the S slices (four 16-column chunks of all slices per round trip) and runs
+// the epilogue.  Fitted to per-CTA timestamps on GB300.
+static double reduce_tail_us(int bn, int T, int S, int mode) {
+  const int rounds = (std::min(bn, T) + 63) / 64;
+  return 1.5 + rounds * (1.0 + 0.15 * S) + epilogue_us(bn, T, mode);
+}
+
 // Cost model (microseconds) of one launch with token tile bn split S ways,
-// fitted to sweeps on GB300: one CTA streams about 60 GB/s, the GPU about
-// 6.5 TB/s from HBM, and a CTA's tensor pipe does about 11 TFLOP/s.  Each wave
+// fitted to sweeps and per-CTA timestamps on GB300: stage_us per k-block, the
+// GPU about 6.5 TB/s from HBM.  Each wave
 // of units costs the slower of one unit's own time and the wave's share of HBM
 // bandwidth (weights are read from HBM once per token tile when they do not
 // fit in L2); split slices add their write + read traffic, and in the reduce
@@ -570,8 +680,8 @@ static double gemm_cost(int N_out, int T, int K_in, int S, int bn, int mode, int
   const int t_tiles = (T + bn - 1) / bn;
   const int m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
   const double kbps = kb / S;
-  const double uA = 128.0 * 64 * 2 * kbps, uB = (double)bn * 64 * 2 * kbps;
-  const double t_unit = std::max((uA + uB) / 60e3, 2.0 * 128 * bn * 64 * kbps / 11e6) + 0.15;
+  const double uA = 128.0 * 64 * 2 * kbps;
+  const double t_unit = kbps * stage_us(bn) + 0.15;
   const long U = (long)m_tiles * t_tiles * S;
   const double wbytes = 2.0 * N_out * K_in;
   const double hbm_share = wbytes > 48e6 ? 1.0 : 1.0 / t_tiles;  // re-read per token tile?
@@ -582,7 +692,9 @@ static double gemm_cost(int N_out, int T, int K_in, int S, int bn, int mode, int
   }
   if (S > 1) {
     tot += (double)S * T * N_out * 8.0 / 8e6;
-    if (mode != GEMM_PARTIAL) tot += (double)S * std::min(bn, T) * 128 * 4 / 60e3;
+    if (mode != GEMM_PARTIAL) tot += reduce_tail_us(bn, T, S, mode);
+  } else if (mode != GEMM_PARTIAL) {
+    tot += epilogue_us(bn, T, mode);  // the last tile's epilogue is not overlapped
   }
   return tot;
 }
@@ -595,7 +707,8 @@ int gemm_balanced_slots(int K_in, int chunk) {
 // Balanced schedule: every CTA streams `chunk` k-blocks (the iterations of all
 // tiles cut evenly over the SMs), so no wave is partly empty; tiles cut across
 // CTAs are reduced by their last CTA as in the split schedule.
-static double gemm_cost_balanced(int N_out, int T, int K_in, int bn, int num_sms, int *chunk_out) {
+static double gemm_cost_balanced(int N_out, int T, int K_in, int bn, int mode, int num_sms,
+                                 int *chunk_out) {
   const int kb = K_in / dfl::BK;
   const int t_tiles = (T + bn - 1) / bn;
   const int m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
@@ -603,18 +716,18 @@ static double gemm_cost_balanced(int N_out, int T, int K_in, int bn, int num_sms
   const long chunk = (total + num_sms - 1) / num_sms;
   *chunk_out = (int)chunk;
   if (chunk < 2 || total > (1L << 30)) return 1e300;
-  const double per_kb = 128.0 * 64 * 2 + (double)bn * 64 * 2;
   const int segs = (int)((chunk + kb - 1) / kb) + 1;
-  const double t_cta = std::max(chunk * per_kb / 60e3, 2.0 * 128 * bn * 64 * chunk / 11e6) +
-                       0.15 * segs;
+  const double t_cta = chunk * stage_us(bn) + 0.15 * segs;
   const double wbytes = 2.0 * N_out * K_in;
   const double hbm = wbytes * (wbytes > 48e6 ? t_tiles : 1) / 6.5e6;
   double tot = std::max(t_cta, hbm);
   if (chunk < kb || total % chunk) {  // cut tiles: slices written, then read by the last CTA
     const int slots = gemm_balanced_slots(K_in, (int)chunk);
-    tot += (double)slots * std::min(bn, T) * 128 * 4 / 60e3;
+    tot += reduce_tail_us(bn, T, slots, mode);
     tot += 2.0 * std::min<long>(num_sms, (long)m_tiles * t_tiles * slots) * 128 * std::min(bn, T) *
            4 / 8e6;
+  } else {
+    tot += epilogue_us(bn, T, mode);
   }
   return tot;
 }
@@ -638,7 +751,7 @@ static GemmPlan plan_for(int N_out, int T, int K_in, int mode, int num_sms, int 
     }
     if (mode != GEMM_PARTIAL) {
       int chunk = 0;
-      const double c = gemm_cost_balanced(N_out, T, K_in, bn, num_sms, &chunk);
+      const double c = gemm_cost_balanced(N_out, T, K_in, bn, mode, num_sms, &chunk);
       const size_t fl = gemm_scratch_floats(mode == GEMM_SWIGLU ? N_out / 2 : N_out, T, 1, mode,
                                             bn, chunk, K_in);
       if (c < best_cost * 0.985 && fl <= kMaxPartialFloats) {
@@ -706,6 +819,13 @@ static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
   p.F = swiglu ? g.N_out : 0;
   p.counters = g.counters;
   p.err = g.err;
+  p.q_norm = (const dfl::bf16 *)g.q_norm;
+  p.k_norm = (const dfl::bf16 *)g.k_norm;
+  p.rope_cs = g.rope_cs;
+  p.Hq = g.Hq;
+  p.Hkv = g.Hkv;
+  p.dh = g.dh;
+  p.eps = g.eps;
   p.chunk = 0;
   p.kb_total = g.K_in / dfl::BK;
   p.total = 0;
@@ -735,6 +855,11 @@ int gemm_run(const GemmCall &g, cudaStream_t st) {
   if (g.chunk < 0 || (g.chunk > 0 && g.mode == GEMM_PARTIAL)) return DFLASH_ERR_DIMS;
   if (g.chunk > 0 && (!g.counters || !g.out)) return DFLASH_ERR_NULL;
   if (g.mode == GEMM_SWIGLU && g.N_out % 64) return DFLASH_ERR_DIMS;
+  if (g.mode == GEMM_QKV &&
+      (g.dtype != DFLASH_BF16 || (g.dh != 64 && g.dh != 128) ||
+       g.N_out != (g.Hq + 2 * g.Hkv) * g.dh || !g.q_norm || !g.k_norm || !g.rope_cs ||
+       !g.out_bf16))
+    return DFLASH_ERR_DIMS;
   if (g.mode != GEMM_PARTIAL && g.S > 1 && (!g.counters || !g.out)) return DFLASH_ERR_NULL;
   if (g.dtype == DFLASH_F32) {
     // CUDA-core path: slices to scratch (or the output itself), then the epilogue

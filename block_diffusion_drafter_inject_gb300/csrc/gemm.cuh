@@ -26,6 +26,7 @@ enum GemmMode {
   GEMM_PARTIAL = 0,  // slice s -> out[(s*T + t)*ld + n]; the caller sums the slices
   GEMM_REDUCE = 1,   // final Y -> out_f32[t*ld + n] and/or out_bf16[t*ldb + n]
   GEMM_SWIGLU = 2,   // rows [Wg; Wu] of a 2F-row weight: out_bf16[t*ldb + f] = SiLU(g_f) u_f
+  GEMM_QKV = 3,      // QKV projection -> bf16 q, k (head RMSNorm + RoPE) and v, out_bf16
 };
 
 struct GemmCall {
@@ -46,6 +47,11 @@ struct GemmCall {
   int ldb = 0;
   int *counters = nullptr;    // tile tickets, zero on entry and on exit (S > 1)
   int *err = nullptr;
+  // GEMM_QKV: head norm gains (bf16 [dh]), per-token RoPE (cos, sin) [T][dh/2]
+  const void *q_norm = nullptr, *k_norm = nullptr;
+  const float2 *rope_cs = nullptr;
+  int Hq = 0, Hkv = 0, dh = 0;
+  float eps = 0.f;
 };
 
 // Floats of slice scratch a reduce-mode GEMM needs (0 when S == 1 and chunk == 0).

@@ -55,6 +55,37 @@ __device__ __forceinline__ float warp_sort_desc(float x) {
 
 constexpr int kNoId = 0x7fffffff;  // id of an empty slot (never better than a real one)
 
+// Bitonic sort of 64 (value, id) pairs held two per lane, element e = 32*i + lane
+// in (v[i], id[i]); afterwards element 0 is the best (larger value, then lower id).
+__device__ __forceinline__ void warp_sort64(float (&v)[2], int (&id)[2], int lane) {
+#pragma unroll
+  for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j == 32) {  // partner is the lane's other element; element 0 is the lower one
+        const bool up = ((lane & k) == 0);  // k == 64 here: always the descending half
+        const bool swap = up ? better(v[1], id[1], v[0], id[0]) : better(v[0], id[0], v[1], id[1]);
+        if (swap) {
+          const float tv = v[0];
+          const int ti = id[0];
+          v[0] = v[1], id[0] = id[1], v[1] = tv, id[1] = ti;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int e = 32 * i + lane;
+          const float pv = __shfl_xor_sync(0xffffffffu, v[i], j);
+          const int pi = __shfl_xor_sync(0xffffffffu, id[i], j);
+          const bool lower = (e & j) == 0, up = (e & k) == 0;
+          // the lower element of a pair takes the better one in a descending run
+          const bool take = (lower == up) ? better(pv, pi, v[i], id[i]) : better(v[i], id[i], pv, pi);
+          if (take) v[i] = pv, id[i] = pi;
+        }
+      }
+    }
+  }
+}
+
 // Warp-wide top-k (larger value, then lower id) of the candidates v[j], id[j]
 // (j < J) held by the lanes; results in ov[0..k), oi[0..k) (written by lane 0).
 // Every top-k element is >= the k-th largest of the lane maxima t (k lanes each
@@ -86,16 +117,16 @@ __device__ __forceinline__ void warp_topk(const float (&v)[J], const int (&id)[J
     for (int j = 0; j < J; ++j)
       if (id[j] != kNoId && v[j] >= t) cv[w] = v[j], ci[w] = id[j], ++w;
     __syncwarp();
-    for (int it = 0; it < k; ++it) {
-      VI best{-INFINITY, kNoId};
-      int where = -1;
-      for (int e = lane; e < total; e += 32)
-        if (better(cv[e], ci[e], best.v, best.i)) best.v = cv[e], best.i = ci[e], where = e;
-      const VI win = warp_best(best);
-      if (where >= 0 && best.i == win.i) cv[where] = -INFINITY, ci[where] = kNoId;
-      if (lane == 0) ov[it] = win.v, oi[it] = win.i;
-      __syncwarp();
+    float sv[2];
+    int si[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int e = 32 * i + lane;
+      sv[i] = e < total ? cv[e] : -INFINITY;
+      si[i] = e < total ? ci[e] : kNoId;
     }
+    warp_sort64(sv, si, lane);
+    if (lane < k) ov[lane] = sv[0], oi[lane] = si[0];  // k <= 32
   } else {
     uint32_t taken = 0;
     for (int it = 0; it < k; ++it) {
@@ -113,7 +144,7 @@ __device__ __forceinline__ void warp_topk(const float (&v)[J], const int (&id)[J
   __syncwarp();
 }
 
-constexpr int kTopkCap = 64;      // compacted candidates per warp
+constexpr int kTopkCap = 64;      // compacted candidates per warp (one 64-element sort)
 constexpr int kTopkRowJ = 20;     // row merge: up to 32 * 20 = 640 chunk candidates
 
 // Top-k and logsumexp of logit rows.  One CTA = one 8192-logit chunk of one
