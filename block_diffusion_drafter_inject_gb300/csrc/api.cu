@@ -77,7 +77,7 @@ static int check_cfg(const dflash_config *c) {
       c->vocab >= 2 && c->n_taps >= 1 && c->d_target >= 1 &&
       ((long)c->n_taps * c->d_target) % 64 == 0 && c->window >= 1 && c->page_size >= 1 &&
       c->top_k >= 1 && c->top_k <= DFLASH_MAX_TOPK && c->top_k <= c->vocab &&
-      (long)topk_chunks(c->vocab) * c->top_k <= 640 &&
+      topk_tiles(c->vocab) <= kTopkMaxTiles &&
       c->sel_rank >= 16 && c->sel_rank % 16 == 0 && c->sel_rank <= 1024 &&
       c->top_k * c->sel_rank <= 16384 && c->conv_group >= 1 && c->d_model % c->conv_group == 0 &&
       c->mask_token_id >= 0 && c->mask_token_id < c->vocab && c->rms_eps >= 0.f &&
@@ -225,7 +225,7 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->zf = take((size_t)TL * D * es);
   L->logits = take((size_t)TL * V * 4);
   L->attn = take(L->ap.part_floats * 4);
-  L->topk = take((size_t)TL * topk_chunks(V) * (2 * k + 2) * 4);
+  L->topk = take((size_t)TL * topk_tiles(V) * sizeof(float2));
   L->selrows = take((size_t)TR * D * es);
   L->U = take((size_t)TR * r * 4);
   L->Vp = take((size_t)TR * r * 4);
@@ -412,9 +412,13 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     TRY(conv_post(l, 3, last ? w.final_norm : w.layer[l + 1].attn_norm, last));
   }
   const int TL = B * (K - 1);
-  TRY(gemm_run(reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, GemmPlan{0, 1}, GEMM_REDUCE, logits, V, nullptr, 0),
-               st));
-  TRY(launch_topk(logits, TL, V, c.top_k, topkp, (int *)(ws + L.topk_tickets), ids, logp, st));
+  // the lm_head's epilogue also writes each 128-entry vocab tile's (max, sum e^(z - max))
+  float2 *tstats = c.dtype == DFLASH_BF16 ? (float2 *)topkp : nullptr;
+  GemmCall gl = reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, GemmPlan{0, 1}, GEMM_REDUCE, logits,
+                            V, nullptr, 0);
+  gl.stats = tstats;
+  TRY(gemm_run(gl, st));
+  TRY(launch_topk(logits, tstats, TL, V, c.top_k, ids, logp, st));
   return DFLASH_OK;
 }
 

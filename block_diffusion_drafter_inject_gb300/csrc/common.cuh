@@ -63,7 +63,7 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Warp sum of N per-lane values by recursive halving (N a power of two): at
+// Warp max / sum of N per-lane values by recursive halving (N a power of two): at
 // offset o = 16, 8, ... each lane keeps one half of its values and adds the
 // partner's copy of that half.  Afterwards lane L holds the totals of entries
 // rs_first<N>(L) .. + N/32 - 1 in v[0..) (N >= 32), or of entry rs_first<N>(L)
@@ -81,6 +81,25 @@ __device__ __forceinline__ int rs_first(int lane) {
     if (lane & (16 >> l)) idx += N >> (l + 1);
   return idx;
 }
+template <int N>
+__device__ __forceinline__ void warp_reduce_scatter_max(float (&v)[N], int lane) {
+#pragma unroll
+  for (int l = 0; l < RS<N>::H; ++l) {
+    const int o = 16 >> l;
+    const bool up = (lane & o) != 0;
+    const int h = N >> (l + 1);
+#pragma unroll
+    for (int j = 0; j < h; ++j) {
+      const float send = up ? v[j] : v[j + h];
+      const float keep = up ? v[j + h] : v[j];
+      v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+    }
+  }
+#pragma unroll
+  for (int o = 16 >> RS<N>::H; o > 0; o >>= 1)
+    v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+}
+// the same with sums (see above)
 template <int N>
 __device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
 #pragma unroll
@@ -100,6 +119,16 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
     v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
 }
 
+// Max over the block; `red` is shared scratch of >= 32 floats. All threads get the max.
+__device__ __forceinline__ float block_max(float v, float *red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  float t = (lane < nw) ? red[lane] : -INFINITY;
+  return warp_max(t);
+}
 // Sum over the block; `red` is shared scratch of >= 32 floats. All threads get the sum.
 __device__ __forceinline__ float block_sum(float v, float *red) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;

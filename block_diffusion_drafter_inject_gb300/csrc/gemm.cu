@@ -53,6 +53,8 @@ struct GemmParams {
   // tiles, tile after tile, are cut into equal chunks of `chunk`, one per CTA
   int chunk, kb_total, total;
   int nmax;  // slice slots per tile in the scratch
+  // GEMM_REDUCE: optional per-(token, weight tile) (max, sum e^(y - max)) [T][m_tiles]
+  float2 *stats;
   // GEMM_QKV: head RMSNorm (q and k heads) + rotate-half RoPE, bf16 out
   const bf16 *q_norm, *k_norm;
   const float2 *rope_cs;  // [T][dh/2] (cos, sin)
@@ -203,6 +205,31 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
           if (p.out_bf16) p.out_bf16[(size_t)t * p.ldb + n] = __float2bfloat16_rn(v[j]);
         }
       }
+    }
+    if (p.stats) {
+      // per token of the chunk, over the tile's rows: m = max, s = sum e^(y - m)
+      const int lane = row & 31, quarter = row >> 5;
+      const bool valid = n < p.N_out;
+      float w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = valid ? v[j] : -INFINITY;
+      warp_reduce_scatter_max<16>(w, lane);  // lane L: token L >> 1, this warp's rows
+      if ((lane & 1) == 0) xss[quarter * 16 + (lane >> 1)] = w[0];
+      epi_bar(eg);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float m = fmaxf(fmaxf(xss[j], xss[16 + j]), fmaxf(xss[32 + j], xss[48 + j]));
+        w[j] = valid ? expf(v[j] - m) : 0.f;
+      }
+      warp_reduce_scatter<16>(w, lane);
+      if ((lane & 1) == 0) xbuf[quarter * 16 + (lane >> 1)] = w[0];
+      epi_bar(eg);
+      if (row < 16 && c0 + row < p.T) {
+        const float m = fmaxf(fmaxf(xss[row], xss[16 + row]), fmaxf(xss[32 + row], xss[48 + row]));
+        const float sum = (xbuf[row] + xbuf[16 + row]) + (xbuf[32 + row] + xbuf[48 + row]);
+        p.stats[(size_t)(c0 + row) * p.m_tiles + m_tile] = make_float2(m, sum);
+      }
+      epi_bar(eg);  // xss / xbuf are rewritten by the next chunk
     }
   } else {
     // rows 64..127 hold the up projections of the features of rows 0..63
@@ -658,13 +685,14 @@ static double stage_us(int bn) {
 // load and the stores, plus the exchange of the SwiGLU / head-norm modes.
 static double epilogue_us(int bn, int T, int mode) {
   const int chunks = (std::min(bn, T) + 15) / 16;
-  return chunks * (mode == GEMM_REDUCE ? 0.25 : 0.45);
+  const int per_group = (chunks + dfl::kEpiGroups - 1) / dfl::kEpiGroups;
+  return per_group * (mode == GEMM_REDUCE ? 0.6 : 1.8);
 }
 // Tail of a split tile: the slice stores, the ticket, then the last CTA reads
-// the S slices (four 16-column chunks of all slices per round trip) and runs
-// the epilogue.  Fitted to per-CTA timestamps on GB300.
+// the S slices (per epilogue group four 16-column chunks of all slices per
+// round trip) and runs the epilogue.  Fitted to per-CTA timestamps on GB300.
 static double reduce_tail_us(int bn, int T, int S, int mode) {
-  const int rounds = (std::min(bn, T) + 63) / 64;
+  const int rounds = (std::min(bn, T) + 127) / 128;  // 4 chunks per group per round
   return 1.5 + rounds * (1.0 + 0.15 * S) + epilogue_us(bn, T, mode);
 }
 
@@ -722,8 +750,11 @@ static double gemm_cost_balanced(int N_out, int T, int K_in, int bn, int mode, i
   const double hbm = wbytes * (wbytes > 48e6 ? t_tiles : 1) / 6.5e6;
   double tot = std::max(t_cta, hbm);
   if (chunk < kb || total % chunk) {  // cut tiles: slices written, then read by the last CTA
+    // a cut tile's contributors finish at different points of their chunks: the
+    // last one's reduction starts late and overlaps nothing; with the SwiGLU and
+    // head-norm epilogues this measured about twice the reduction itself
     const int slots = gemm_balanced_slots(K_in, (int)chunk);
-    tot += reduce_tail_us(bn, T, slots, mode);
+    tot += (mode == GEMM_REDUCE ? 1.0 : 2.0) * reduce_tail_us(bn, T, slots, mode);
     tot += 2.0 * std::min<long>(num_sms, (long)m_tiles * t_tiles * slots) * 128 * std::min(bn, T) *
            4 / 8e6;
   } else {
@@ -819,6 +850,7 @@ static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
   p.F = swiglu ? g.N_out : 0;
   p.counters = g.counters;
   p.err = g.err;
+  p.stats = g.stats;
   p.q_norm = (const dfl::bf16 *)g.q_norm;
   p.k_norm = (const dfl::bf16 *)g.k_norm;
   p.rope_cs = g.rope_cs;
@@ -853,6 +885,7 @@ int gemm_run(const GemmCall &g, cudaStream_t st) {
   if (!d) return DFLASH_ERR_DEVICE;
   if (g.K_in % 64 || g.S < 1 || (g.K_in / 64) % g.S) return DFLASH_ERR_DIMS;
   if (g.chunk < 0 || (g.chunk > 0 && g.mode == GEMM_PARTIAL)) return DFLASH_ERR_DIMS;
+  if (g.stats && (g.mode != GEMM_REDUCE || g.dtype != DFLASH_BF16)) return DFLASH_ERR_DIMS;
   if (g.chunk > 0 && (!g.counters || !g.out)) return DFLASH_ERR_NULL;
   if (g.mode == GEMM_SWIGLU && g.N_out % 64) return DFLASH_ERR_DIMS;
   if (g.mode == GEMM_QKV &&

@@ -47,6 +47,9 @@ struct GemmCall {
   int ldb = 0;
   int *counters = nullptr;    // tile tickets, zero on entry and on exit (S > 1)
   int *err = nullptr;
+  // GEMM_REDUCE (bf16): per token t and 128-row weight tile i, (max, sum e^(y - max))
+  // of the tile's outputs -> stats[t * ceil(N_out/128) + i]
+  float2 *stats = nullptr;
   // GEMM_QKV: head norm gains (bf16 [dh]), per-token RoPE (cos, sin) [T][dh/2]
   const void *q_norm = nullptr, *k_norm = nullptr;
   const float2 *rope_cs = nullptr;

@@ -144,114 +144,193 @@ __device__ __forceinline__ void warp_topk(const float (&v)[J], const int (&id)[J
   __syncwarp();
 }
 
-constexpr int kTopkCap = 64;      // compacted candidates per warp (one 64-element sort)
-constexpr int kTopkRowJ = 20;     // row merge: up to 32 * 20 = 640 chunk candidates
+constexpr int kTopkCap = 64;       // compacted candidates per warp (one 64-element sort)
+constexpr int kTopkCandTiles = 64; // vocab tiles scanned on the direct path
+constexpr int kTopkCand = 512;     // candidates kept on the direct path
 
-// Top-k and logsumexp of logit rows.  One CTA = one 8192-logit chunk of one
-// row (8 warps x 1024): each warp finds its top-k (warp_topk), warp 0 merges
-// the 8 lists and writes the chunk's partial [m, s, v_0..v_{k-1}, id_0..id_{k-1}]
-// (m = max, s = sum of exp(z - m)).  The CTA that finishes a row's last chunk
-// (a ticket per row, no waiting) merges the row: ids, logp = logit - logsumexp.
-__global__ void __launch_bounds__(256) k_topk(const float *__restrict__ logits, int V, int k,
-                                              float *__restrict__ partial, int *tickets,
-                                              int32_t *__restrict__ ids,
-                                              float *__restrict__ logp) {
-  __shared__ float cv[8][kTopkCap];
-  __shared__ int ci[8][kTopkCap];
+// Top-k and logsumexp of logit rows, one CTA per row.  The row is cut into
+// 128-entry vocab tiles with (m_i, s_i) = (max, sum e^(z - m_i)) per tile,
+// given by the projection that wrote the logits (or formed here when
+// stats == nullptr); logsumexp = M + log sum_i s_i e^(m_i - M).  The k-th
+// largest tile maximum thr is a lower bound of the k-th largest logit (k tiles
+// each hold an entry >= thr), so every top-k entry lies in a tile with
+// m_i >= thr and is itself >= thr: those tiles are scanned and their entries
+// >= thr ranked (larger value, then lower id).  Rows whose ties defeat the
+// bounds (more than kTopkCandTiles tiles or kTopkCand entries at or above thr)
+// are ranked by a scan of the whole row instead.
+__global__ void __launch_bounds__(256) k_topk_rows(const float *__restrict__ logits,
+                                                   const float2 *__restrict__ stats, int V, int k,
+                                                   int32_t *__restrict__ ids,
+                                                   float *__restrict__ logp) {
+  extern __shared__ float tk_sm[];  // [nt] tile maxima, [nt] tile sums
+  __shared__ float cv[kTopkCand];
+  __shared__ int ci[kTopkCand];
+  __shared__ int ctile[kTopkCandTiles];
+  __shared__ float sc[8][kTopkCap];
+  __shared__ int sci[8][kTopkCap];
   __shared__ float wv[8 * DFLASH_MAX_TOPK];
   __shared__ int wi[8 * DFLASH_MAX_TOPK];
   __shared__ float rv[DFLASH_MAX_TOPK];
   __shared__ int ri[DFLASH_MAX_TOPK];
-  __shared__ float wm[8], wsum[8];
+  __shared__ float red[32];
+  __shared__ float s_thr;
+  __shared__ int n_tiles, n_cand;
   pdl_launch();
   pdl_wait();
-  const int chunk = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int base = chunk * dflh::kTopkChunk + w * 1024;
+  const int row = blockIdx.x, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int nt = (V + 127) / 128;
+  float *sm_m = tk_sm, *sm_s = tk_sm + nt;
   const float *z = logits + (size_t)row * V;
-  float v[32];
-  int id[32];
-  float mx = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int i = base + j * 32 + lane;
-    v[j] = i < V ? z[i] : -INFINITY;
-    id[j] = i < V ? i : kNoId;
-    mx = fmaxf(mx, v[j]);
+  if (tid == 0) n_tiles = 0, n_cand = 0;
+  for (int i = tid; i < nt; i += blockDim.x) {
+    float m, sum;
+    if (stats) {
+      const float2 st = stats[(size_t)row * nt + i];
+      m = st.x, sum = st.y;
+    } else {
+      const int e1 = min(V, 128 * i + 128);
+      m = -INFINITY, sum = 0.f;
+      for (int e = 128 * i; e < e1; ++e) m = fmaxf(m, z[e]);
+      for (int e = 128 * i; e < e1; ++e) sum += expf(z[e] - m);
+    }
+    sm_m[i] = m;
+    sm_s[i] = sum;
   }
-  mx = warp_max(mx);
-  float se = 0.f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j) se += (v[j] == -INFINITY) ? 0.f : expf(v[j] - mx);
-  se = warp_sum(se);
-  if (lane == 0) wm[w] = mx, wsum[w] = se;
-  warp_topk<32>(v, id, k, cv[w], ci[w], kTopkCap, wv + w * k, wi + w * k, lane);
   __syncthreads();
-  if (w != 0) return;
-  // warp 0: merge the 8 warp lists, write the chunk partial
-  {
-    float mv[8];
-    int mi[8];
+  float mm = -INFINITY;
+  for (int i = tid; i < nt; i += blockDim.x) mm = fmaxf(mm, sm_m[i]);
+  const float M = block_max(mm, red);
+  float ss = 0.f;
+  for (int i = tid; i < nt; i += blockDim.x) ss += sm_s[i] * expf(sm_m[i] - M);
+  const float lse = M + logf(block_sum(ss, red));
+
+  // threshold: the k-th largest tile maximum (warp 0)
+  if (w == 0) {
+    float lm = -INFINITY;
+    for (int i = lane; i < nt; i += 32) lm = fmaxf(lm, sm_m[i]);
+    const float t0 = __shfl_sync(0xffffffffu, warp_sort_desc(lm), k - 1);
+    int cnt = 0;
+    for (int i = lane; i < nt; i += 32) cnt += sm_m[i] >= t0 ? 1 : 0;
+    int pre = cnt;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int e = 32 * q + lane;
-      mv[q] = e < 8 * k ? wv[e] : -INFINITY;
-      mi[q] = e < 8 * k ? wi[e] : kNoId;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, pre, o);
+      if (lane >= o) pre += y;
     }
-    warp_topk<8>(mv, mi, k, cv[0], ci[0], kTopkCap, rv, ri, lane);
-  }
-  float *out = partial + ((size_t)row * nch + chunk) * (2 * k + 2);
-  float M = -INFINITY;
-  for (int q = 0; q < 8; ++q) M = fmaxf(M, wm[q]);
-  if (lane == 0) {
-    float S = 0.f;
-    for (int q = 0; q < 8; ++q) S += (wm[q] == -INFINITY) ? 0.f : wsum[q] * expf(wm[q] - M);
-    out[0] = M;
-    out[1] = S;
-  }
-  for (int it = lane; it < k; it += 32) {
-    out[2 + it] = rv[it];
-    out[2 + k + it] = __int_as_float(ri[it]);
-  }
-  // ticket: the last chunk of the row merges it
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  if (lane == 0) {
-    last = atomicAdd(&tickets[row], 1) == nch - 1;
-    if (last) tickets[row] = 0;
-  }
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
-  const float *pr = partial + (size_t)row * nch * (2 * k + 2);
-  float Mr = -INFINITY;
-  for (int c = lane; c < nch; c += 32) Mr = fmaxf(Mr, __ldcg(pr + (size_t)c * (2 * k + 2)));
-  Mr = warp_max(Mr);
-  float Sr = 0.f;
-  for (int c = lane; c < nch; c += 32) {
-    const float *p = pr + (size_t)c * (2 * k + 2);
-    const float m = __ldcg(p);
-    Sr += m == -INFINITY ? 0.f : __ldcg(p + 1) * expf(m - Mr);
-  }
-  Sr = warp_sum(Sr);
-  const float lse = Mr + logf(Sr);
-  const int n = nch * k;
-  float cvr[kTopkRowJ];
-  int cir[kTopkRowJ];
+    const int total = __shfl_sync(0xffffffffu, pre, 31);
+    float thr = t0;
+    if (total <= kTopkCap) {  // rank the maxima >= t0 exactly: thr = the k-th of them
+      int wpos = pre - cnt;
+      for (int i = lane; i < nt; i += 32)
+        if (sm_m[i] >= t0) sc[0][wpos++] = sm_m[i];
+      __syncwarp();
+      float sv[2];
+      int si[2];
 #pragma unroll
-  for (int q = 0; q < kTopkRowJ; ++q) {
-    const int e = 32 * q + lane;
-    cvr[q] = -INFINITY;
-    cir[q] = kNoId;
-    if (e < n) {
-      const float *p = pr + (size_t)(e / k) * (2 * k + 2);
-      cvr[q] = __ldcg(p + 2 + e % k);
-      cir[q] = __float_as_int(__ldcg(p + 2 + k + e % k));
+      for (int q = 0; q < 2; ++q) {
+        const int e = 32 * q + lane;
+        sv[q] = e < total ? sc[0][e] : -INFINITY;
+        si[q] = e < total ? e : kNoId;
+      }
+      warp_sort64(sv, si, lane);  // element k-1 is in half 0 (k <= 32)
+      thr = __shfl_sync(0xffffffffu, sv[0], k - 1);
     }
+    if (lane == 0) s_thr = thr;
   }
-  warp_topk<kTopkRowJ>(cvr, cir, k, cv[0], ci[0], kTopkCap, rv, ri, lane);
-  for (int it = lane; it < k; it += 32) {
+  __syncthreads();
+  const float thr = s_thr;
+  for (int i = tid; i < nt; i += blockDim.x)
+    if (sm_m[i] >= thr) {
+      const int pos = atomicAdd(&n_tiles, 1);
+      if (pos < kTopkCandTiles) ctile[pos] = i;
+    }
+  __syncthreads();
+  bool direct = n_tiles <= kTopkCandTiles;
+  if (direct) {
+    for (int q = w; q < n_tiles; q += 8) {
+      const int e0 = 128 * ctile[q];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int e = e0 + 32 * j + lane;
+        if (e < V) {
+          const float x = z[e];
+          if (x >= thr) {
+            const int pos = atomicAdd(&n_cand, 1);
+            if (pos < kTopkCand) cv[pos] = x, ci[pos] = e;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    direct = n_cand <= kTopkCand;
+  }
+  if (direct) {
+    if (w != 0) return;
+    const int n = n_cand;
+    if (n <= kTopkCap) {
+      float sv[2];
+      int si[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int e = 32 * q + lane;
+        sv[q] = e < n ? cv[e] : -INFINITY;
+        si[q] = e < n ? ci[e] : kNoId;
+      }
+      warp_sort64(sv, si, lane);
+      if (lane < k) {
+        ids[(size_t)row * k + lane] = si[0];
+        logp[(size_t)row * k + lane] = sv[0] - lse;
+      }
+    } else {
+      float v[kTopkCand / 32];
+      int id[kTopkCand / 32];
+#pragma unroll
+      for (int q = 0; q < kTopkCand / 32; ++q) {
+        const int e = 32 * q + lane;
+        v[q] = e < n ? cv[e] : -INFINITY;
+        id[q] = e < n ? ci[e] : kNoId;
+      }
+      warp_topk<kTopkCand / 32>(v, id, k, sc[0], sci[0], kTopkCap, rv, ri, lane);
+      for (int it = lane; it < k; it += 32) {
+        ids[(size_t)row * k + it] = ri[it];
+        logp[(size_t)row * k + it] = rv[it] - lse;
+      }
+    }
+    return;
+  }
+
+  // whole-row scan: 8192 entries per pass (8 warps x 1024); warp 0 merges the
+  // warps' lists with the running list
+  if (tid < k) rv[tid] = -INFINITY, ri[tid] = kNoId;
+  __syncthreads();
+  for (int base = 0; base < V; base += 8192) {
+    float v[32];
+    int id[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int e = base + w * 1024 + j * 32 + lane;
+      v[j] = e < V ? z[e] : -INFINITY;
+      id[j] = e < V ? e : kNoId;
+    }
+    warp_topk<32>(v, id, k, sc[w], sci[w], kTopkCap, wv + w * k, wi + w * k, lane);
+    __syncthreads();
+    if (w == 0) {
+      float mv[9];
+      int mi[9];
+#pragma unroll
+      for (int q = 0; q < 9; ++q) {
+        const int e = 32 * q + lane;
+        mv[q] = -INFINITY;
+        mi[q] = kNoId;
+        if (e < 8 * k) mv[q] = wv[e], mi[q] = wi[e];
+        else if (e < 9 * k) mv[q] = rv[e - 8 * k], mi[q] = ri[e - 8 * k];
+      }
+      __syncwarp();
+      warp_topk<9>(mv, mi, k, sc[0], sci[0], kTopkCap, rv, ri, lane);
+    }
+    __syncthreads();
+  }
+  for (int it = tid; it < k; it += blockDim.x) {
     ids[(size_t)row * k + it] = ri[it];
     logp[(size_t)row * k + it] = rv[it] - lse;
   }
@@ -442,13 +521,21 @@ __global__ void __launch_bounds__(1024) k_accept(const int32_t *__restrict__ pat
 
 namespace dflh {
 
-int launch_topk(const float *logits, int rows, int V, int k, float *partial, int *tickets,
-                int32_t *ids, float *logp, cudaStream_t st) {
+int launch_topk(const float *logits, const float2 *stats, int rows, int V, int k, int32_t *ids,
+                float *logp, cudaStream_t st) {
   if (rows <= 0) return DFLASH_OK;
-  const int nch = topk_chunks(V);
-  if (nch * k > 32 * dfl::kTopkRowJ) return DFLASH_ERR_DIMS;
-  DFL_CHECK_LAUNCH(launch(dfl::k_topk, dim3(nch, rows), dim3(256), 0, st, logits, V, k, partial,
-                          tickets, ids, logp));
+  const int nt = topk_tiles(V);
+  if (nt > kTopkMaxTiles || k < 1 || k > DFLASH_MAX_TOPK || k > V) return DFLASH_ERR_DIMS;
+  const size_t smem = (size_t)nt * 2 * sizeof(float);
+  static int attr_done = 0;
+  if (smem > 48 * 1024 && !attr_done) {
+    if (cudaFuncSetAttribute(dfl::k_topk_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kTopkMaxTiles * 2 * (int)sizeof(float)) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_done = 1;
+  }
+  DFL_CHECK_LAUNCH(
+      launch(dfl::k_topk_rows, dim3(rows), dim3(256), smem, st, logits, stats, V, k, ids, logp));
   return DFLASH_OK;
 }
 

@@ -4,13 +4,14 @@
 
 namespace dflh {
 
-constexpr int kTopkChunk = 8192;  // logits per top-k CTA (8 warps x 1024)
+// top-k works on 128-entry vocab tiles (the projection's weight tiles)
+constexpr int kTopkMaxTiles = 8192;  // vocab <= 8192 * 128
+inline int topk_tiles(int V) { return (V + 127) / 128; }
 
-inline int topk_chunks(int V) { return (V + kTopkChunk - 1) / kTopkChunk; }
-
-// partials: rows * chunks * (2*k + 2) floats; tickets: rows ints, zero on entry and exit
-int launch_topk(const float *logits, int rows, int V, int k, float *partial, int *tickets,
-                int32_t *ids, float *logp, cudaStream_t st);
+// ids / logp [rows][k]; stats: per row the (max, sum e^(z - max)) of each
+// 128-entry tile [rows][topk_tiles(V)], or nullptr (formed from the logits)
+int launch_topk(const float *logits, const float2 *stats, int rows, int V, int k, int32_t *ids,
+                float *logp, cudaStream_t st);
 
 template <typename S>
 int launch_sel_gather(const S *E, const int32_t *anchor, const int32_t *topk_ids, int B, int K,

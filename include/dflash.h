@@ -72,7 +72,7 @@ extern "C" {
  *   d_model, d_ff, n_taps*d_target, n_q_heads*head_dim multiples of 64;
  *   head_dim 64 or 128; n_q_heads a multiple of n_kv_heads;
  *   d_model a multiple of conv_group; 1 <= top_k <= 32, top_k <= vocab,
- *   ceil(vocab / 8192) * top_k <= 640 (e.g. vocab up to 327680 at top_k 16);
+ *   vocab <= 1048576 (8192 vocab tiles of 128 entries for the top-k);
  *   sel_rank a multiple of 16 and <= 1024; window >= 1; page_size >= 1;
  *   1 <= n_layers <= DFLASH_MAX_LAYERS; 0 <= mask_token_id < vocab.         */
 typedef struct dflash_config {
