@@ -126,7 +126,8 @@ static int check_kv(const dflash_config *c, const dflash_kv *kv) {
 // ---------------------------------------------------------------------------
 constexpr int kMaxReduceSplits = 16;      // slices a reduce-mode GEMM may use
 constexpr size_t kTicketInts = 1 << 14;   // tile tickets of one reduce-mode GEMM
-constexpr size_t kTopkTicketInts = 1 << 14;  // row tickets of the top-k (B*(K-1) rows at most)
+constexpr size_t kTopkTicketInts = 1 << 14;  // reserved header words (B*(K-1) rows at most)
+constexpr int kKvGroup = 8;  // layers per grouped K/V projection launch of injection
 // Fixed header of every workspace: status word, GEMM tile tickets, top-k row
 // tickets.  They must stay zero between calls; every other region is scratch
 // that a call fully writes before reading (acceptance's partials start here).
@@ -137,7 +138,7 @@ struct Layout {
   size_t x, un, ub, rf, rb, gates, qkv, qb, kb, vb, ob, hb, zf, logits, attn, topk, topk_tickets;
   size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf, rope, rope_inj;
   size_t total;
-  GemmPlan P_gate, P_qkv, P_o, P_gu, P_down, P_sel;
+  GemmPlan P_gate, P_qkv, P_o, P_gu, P_down, P_sel, P_sel2;
   AttnPlan ap;
 };
 
@@ -175,20 +176,23 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
     return o;
   };
   L->P_gate = reduce_plan(c, GW, T, D, GEMM_REDUCE, sms);
-  L->P_qkv = reduce_plan(c, QKVW, T, D, GEMM_REDUCE, sms);
+  L->P_qkv = reduce_plan(c, QKVW, T, D, c->dtype == DFLASH_BF16 ? GEMM_QKV : GEMM_REDUCE, sms);
   L->P_o = reduce_plan(c, D, T, Hq * dh, GEMM_REDUCE, sms);
   L->P_gu = reduce_plan(c, F, T, D, GEMM_SWIGLU, sms);
   L->P_down = reduce_plan(c, D, T, F, GEMM_REDUCE, sms);
   L->P_sel = reduce_plan(c, r, TR, D, GEMM_REDUCE, sms);
+  L->P_sel2 = reduce_plan(c, 2 * r, TR, D, GEMM_REDUCE, sms);
   L->ap = attn_plan(B, K, Hq, Hkv, dh, c->window, sms);
   // slice scratch shared by every reduce-mode GEMM (they run one after another)
   size_t sc = 0;
   sc = std::max(sc, reduce_scratch(c, GW, T, D, L->P_gate, GEMM_REDUCE));
-  sc = std::max(sc, reduce_scratch(c, QKVW, T, D, L->P_qkv, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, QKVW, T, D, L->P_qkv,
+                                    c->dtype == DFLASH_BF16 ? GEMM_QKV : GEMM_REDUCE));
   sc = std::max(sc, reduce_scratch(c, D, T, Hq * dh, L->P_o, GEMM_REDUCE));
   sc = std::max(sc, reduce_scratch(c, F, T, D, L->P_gu, GEMM_SWIGLU));
   sc = std::max(sc, reduce_scratch(c, D, T, F, L->P_down, GEMM_REDUCE));
   sc = std::max(sc, reduce_scratch(c, r, TR, D, L->P_sel, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, 2 * r, TR, D, L->P_sel2, GEMM_REDUCE));
   sc = std::max(sc, reduce_scratch(c, V, TL, D, GemmPlan{0, 1}, GEMM_REDUCE));
   // injection GEMMs: the split depends on the token count; take the largest
   auto inj = [&](int n_out, int k_in) {
@@ -206,6 +210,7 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   };
   sc = std::max(sc, inj(D, TIN));
   sc = std::max(sc, inj(2 * Hkv * dh, D));
+  sc = std::max(sc, inj(std::min(c->n_layers, kKvGroup) * 2 * Hkv * dh, D));
   L->status = take(256);
   L->tickets = take(kTicketInts * sizeof(int));
   L->topk_tickets = take(kTopkTicketInts * sizeof(int));
@@ -227,8 +232,8 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->attn = take(L->ap.part_floats * 4);
   L->topk = take((size_t)TL * topk_tiles(V) * sizeof(float2));
   L->selrows = take((size_t)TR * D * es);
-  L->U = take((size_t)TR * r * 4);
-  L->Vp = take((size_t)TR * r * 4);
+  L->U = take((size_t)TR * r * 4 * 2);  // U then Vp, back to back
+  L->Vp = L->U + (size_t)TR * r * 4;
   L->pairs = take((size_t)B * (K - 1) * k * k * 4);
   L->argmax = take((size_t)T * argmax_chunks(V) * 2 * 4);
   L->rope = take((size_t)T * (dh / 2) * 8);
@@ -293,16 +298,23 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
   const GemmPlan S_fc = reduce_plan(&c, D, N, TIN, GEMM_REDUCE, sms);
   TRY(gemm_run(reduce_call(c, ws, L, w.fc, D, TIN, gn, N, S_fc, GEMM_REDUCE, nullptr, D, cb, D),
                st));
-  const GemmPlan S_kv = reduce_plan(&c, W2, N, D, GEMM_REDUCE, sms);
+  // the [Wk; Wv] rows of every layer: one grouped launch per kKvGroup layers
+  // (layer l's projection -> kvf [l][N][W2])
   LayerPtrs kn;
   memset(&kn, 0, sizeof(kn));
-  for (int l = 0; l < c.n_layers; ++l) {
-    const S *wkv = (const S *)w.layer[l].wqkv + (size_t)Hq * dh * D;  // [Wk; Wv] rows
-    TRY(gemm_run(reduce_call(c, ws, L, wkv, W2, D, cb, N, S_kv, GEMM_REDUCE,
-                             kvf + (size_t)l * N * W2, W2, nullptr, 0),
-                 st));
-    kn.p[l] = w.layer[l].k_norm;
+  const bool grouped = c.dtype == DFLASH_BF16 && W2 % 128 == 0;
+  const int per = grouped ? kKvGroup : 1;
+  for (int l0 = 0; l0 < c.n_layers; l0 += per) {
+    const int ng = std::min(per, c.n_layers - l0);
+    const GemmPlan S_kv = reduce_plan(&c, ng * W2, N, D, GEMM_REDUCE, sms);
+    GemmCall g = reduce_call(c, ws, L, (const S *)w.layer[l0].wqkv + (size_t)Hq * dh * D, W2, D,
+                             cb, N, S_kv, GEMM_REDUCE, kvf + (size_t)l0 * N * W2, W2, nullptr, 0);
+    g.groups = ng;
+    g.ostride = (size_t)N * W2;
+    for (int j = 1; j < ng; ++j) g.Wg[j] = (const S *)w.layer[l0 + j].wqkv + (size_t)Hq * dh * D;
+    TRY(gemm_run(g, st));
   }
+  for (int l = 0; l < c.n_layers; ++l) kn.p[l] = w.layer[l].k_norm;
   TRY(launch_inject_store<S>(kvf, N, c.n_layers, Hkv, dh, kn, req, pos, kv.page_table,
                              kv.num_rows, kv.max_pages_per_req, kv.num_pages, c.page_size, rope_cs,
                              c.rms_eps, (S *)kv.k, (S *)kv.v, err, st));
@@ -432,11 +444,22 @@ static int run_select(const dflash_config &c, const dflash_weights &w, const int
   S *rows = (S *)(ws + L.selrows);
   float *U = (float *)(ws + L.U), *Vp = (float *)(ws + L.Vp);
   TRY(launch_sel_gather<S>((const S *)w.embed, anchor, ids, B, K, k, c.vocab, D, rows, err, st));
-  TRY(gemm_run(reduce_call(c, ws, L, w.sel_pu, r, D, rows, TR, L.P_sel, GEMM_REDUCE, U, r, nullptr, 0),
-               st));
-  TRY(gemm_run(reduce_call(c, ws, L, w.sel_pv, r, D, rows, TR, L.P_sel, GEMM_REDUCE, Vp, r, nullptr,
-                           0),
-               st));
+  if (c.dtype == DFLASH_BF16 && r % 128 == 0) {
+    // both projections in one grouped launch (Vp follows U in the workspace)
+    GemmCall g = reduce_call(c, ws, L, w.sel_pu, r, D, rows, TR, L.P_sel2, GEMM_REDUCE, U, r,
+                             nullptr, 0);
+    g.groups = 2;
+    g.Wg[1] = w.sel_pv;
+    g.ostride = (size_t)TR * r;
+    TRY(gemm_run(g, st));
+  } else {
+    TRY(gemm_run(reduce_call(c, ws, L, w.sel_pu, r, D, rows, TR, L.P_sel, GEMM_REDUCE, U, r,
+                             nullptr, 0),
+                 st));
+    TRY(gemm_run(reduce_call(c, ws, L, w.sel_pv, r, D, rows, TR, L.P_sel, GEMM_REDUCE, Vp, r,
+                             nullptr, 0),
+                 st));
+  }
   TRY(launch_viterbi(U, Vp, ids, logp, B, K, k, r, (float *)(ws + L.pairs), path, score, st));
   return DFLASH_OK;
 }

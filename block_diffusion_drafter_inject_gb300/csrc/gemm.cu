@@ -23,6 +23,8 @@
 // weight tile holds 64 gate rows and the matching 64 up rows.
 //
 // fp32 path (the float32 configuration): a shared-memory tiled CUDA-core GEMM.
+#include <string.h>
+
 #include <algorithm>
 #include <mutex>
 #include <unordered_map>
@@ -53,6 +55,10 @@ struct GemmParams {
   // tiles, tile after tile, are cut into equal chunks of `chunk`, one per CTA
   int chunk, kb_total, total;
   int nmax;  // slice slots per tile in the scratch
+  // grouped weights (GEMM_REDUCE): weight tile m belongs to group m / mtg; group g's
+  // outputs start at out_f32 + g * ostride; N_out is the rows of one group
+  int mtg;
+  size_t ostride;
   // GEMM_REDUCE: optional per-(token, weight tile) (max, sum e^(y - max)) [T][m_tiles]
   float2 *stats;
   // GEMM_QKV: head RMSNorm (q and k heads) + rotate-half RoPE, bf16 out
@@ -133,15 +139,22 @@ __device__ __forceinline__ bool get_seg(const GemmParams &p, int i, Seg &s) {
   return true;
 }
 
-// Weight tile of unit m_tile: 128 consecutive rows, or for GEMM_SWIGLU the 64
-// gate rows [64m, 64m+64) followed by the 64 up rows [F+64m, F+64m+64).
-__device__ __forceinline__ void load_w(uint8_t *dst, const CUtensorMap *m, uint64_t *bar, int kx,
+constexpr int kMaxGroups = 8;
+struct WMaps {
+  CUtensorMap m[kMaxGroups];
+};
+
+// Weight tile of unit m_tile: 128 consecutive rows of its group's matrix, or for
+// GEMM_SWIGLU the 64 gate rows [64m, 64m+64) followed by the 64 up rows
+// [F+64m, F+64m+64).
+__device__ __forceinline__ void load_w(uint8_t *dst, const WMaps &maps, uint64_t *bar, int kx,
                                        int m_tile, const GemmParams &p, uint64_t pol) {
   if (p.mode == 2) {
-    tma_load_2d(dst, m, bar, kx, m_tile * 64, pol);
-    tma_load_2d(dst + 64 * BK * 2, m, bar, kx, p.F + m_tile * 64, pol);
+    tma_load_2d(dst, &maps.m[0], bar, kx, m_tile * 64, pol);
+    tma_load_2d(dst + 64 * BK * 2, &maps.m[0], bar, kx, p.F + m_tile * 64, pol);
   } else {
-    tma_load_2d(dst, m, bar, kx, m_tile * BM, pol);
+    const int g = m_tile / p.mtg;
+    tma_load_2d(dst, &maps.m[g], bar, kx, (m_tile - g * p.mtg) * BM, pol);
   }
 }
 
@@ -195,13 +208,15 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
     }
     epi_bar(eg);
   } else if (p.mode == 1) {
-    const int n = m_tile * BM + row;
+    const int grp = m_tile / p.mtg;
+    const int n = (m_tile - grp * p.mtg) * BM + row;  // row within the group
     if (n < p.N_out) {
+      float *of = p.out_f32 ? p.out_f32 + grp * p.ostride : nullptr;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const int t = c0 + j;
         if (t < p.T) {
-          if (p.out_f32) p.out_f32[(size_t)t * p.ld + n] = v[j];
+          if (of) of[(size_t)t * p.ld + n] = v[j];
           if (p.out_bf16) p.out_bf16[(size_t)t * p.ldb + n] = __float2bfloat16_rn(v[j]);
         }
       }
@@ -255,7 +270,7 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
 
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+    k_gemm_tc(const __grid_constant__ WMaps tmW, const __grid_constant__ CUtensorMap tmX,
               GemmParams p) {
   using SH = GemmShape<BN>;
   constexpr int STAGES = SH::STAGES;
@@ -284,7 +299,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
-    tma_prefetch_desc(&tmW);
+    for (int g = 0; g * p.mtg < p.m_tiles && g < kMaxGroups; ++g) tma_prefetch_desc(&tmW.m[g]);
     tma_prefetch_desc(&tmX);
   }
   if (warp == 1) {
@@ -316,7 +331,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int i = 0; cnt < STAGES && get_seg(p, i, sg); ++i) {
           for (int kb = 0; kb < sg.nkb && cnt < STAGES; ++kb, ++cnt) {
             mbar_expect_tx(&full[cnt], SH::STAGE_BYTES);
-            load_w(smem + cnt * SH::STAGE_BYTES, &tmW, &full[cnt], (sg.kb0 + kb) * BK, sg.m_tile,
+            load_w(smem + cnt * SH::STAGE_BYTES, tmW, &full[cnt], (sg.kb0 + kb) * BK, sg.m_tile,
                    p, pol_w);
           }
         }
@@ -338,7 +353,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               break;
             }
             mbar_expect_tx(&full[stage], SH::STAGE_BYTES);
-            load_w(sa, &tmW, &full[stage], kx, sg.m_tile, p, pol_w);
+            load_w(sa, tmW, &full[stage], kx, sg.m_tile, p, pol_w);
             tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, sg.t_tile * BN, pol_x);
           }
           issued[stage] = true;
@@ -674,11 +689,12 @@ static bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t 
 static int token_tile(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
 
 // One k-block of one CTA (microseconds): the slowest of the weight tile from
-// HBM (~60 GB/s per CTA), both tiles through TMA (~110 GB/s per CTA, the
-// activation tile mostly from L2) and the tensor pipe (~11 TFLOP/s per CTA).
+// HBM (~46 GB/s per CTA, measured with per-CTA timestamps), both tiles through
+// TMA (~110 GB/s per CTA, the activation tile mostly from L2) and the tensor
+// pipe (~11 TFLOP/s per CTA).
 static double stage_us(int bn) {
   const double a = 128.0 * 64 * 2, b = (double)bn * 64 * 2;
-  return std::max(std::max(a / 60e3, (a + b) / 110e3), 2.0 * 128 * bn * 64 / 11e6);
+  return std::max(std::max(a / 46e3, (a + b) / 110e3), 2.0 * 128 * bn * 64 / 11e6);
 }
 
 // Epilogue of one tile (microseconds): per 16-column chunk a tensor-memory
@@ -693,7 +709,7 @@ static double epilogue_us(int bn, int T, int mode) {
 // round trip) and runs the epilogue.  Fitted to per-CTA timestamps on GB300.
 static double reduce_tail_us(int bn, int T, int S, int mode) {
   const int rounds = (std::min(bn, T) + 127) / 128;  // 4 chunks per group per round
-  return 1.5 + rounds * (1.0 + 0.15 * S) + epilogue_us(bn, T, mode);
+  return 1.5 + 0.5 * S + rounds * (1.0 + 0.15 * S) + epilogue_us(bn, T, mode);
 }
 
 // Cost model (microseconds) of one launch with token tile bn split S ways,
@@ -752,9 +768,11 @@ static double gemm_cost_balanced(int N_out, int T, int K_in, int bn, int mode, i
   if (chunk < kb || total % chunk) {  // cut tiles: slices written, then read by the last CTA
     // a cut tile's contributors finish at different points of their chunks: the
     // last one's reduction starts late and overlaps nothing; with the SwiGLU and
-    // head-norm epilogues this measured about twice the reduction itself
+    // head-norm epilogues over several column chunks this measured about twice
+    // the reduction itself
     const int slots = gemm_balanced_slots(K_in, (int)chunk);
-    tot += (mode == GEMM_REDUCE ? 1.0 : 2.0) * reduce_tail_us(bn, T, slots, mode);
+    const bool heavy = mode != GEMM_REDUCE && std::min(bn, T) > 16;  // several epilogue chunks
+    tot += (heavy ? 2.0 : 1.0) * reduce_tail_us(bn, T, slots, mode);
     tot += 2.0 * std::min<long>(num_sms, (long)m_tiles * t_tiles * slots) * 128 * std::min(bn, T) *
            4 / 8e6;
   } else {
@@ -829,9 +847,13 @@ static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
   }
   const bool swiglu = g.mode == GEMM_SWIGLU;
   const int w_rows = swiglu ? 2 * g.N_out : g.N_out;
-  CUtensorMap mw, mx;
-  if (!bf16_map(&mw, g.W, (uint64_t)w_rows, (uint64_t)g.K_in, swiglu ? 64 : dfl::BM, d->id))
-    return DFLASH_ERR_CUDA;
+  dfl::WMaps mw;
+  CUtensorMap mx;
+  memset(&mw, 0, sizeof(mw));
+  for (int gi = 0; gi < g.groups; ++gi)
+    if (!bf16_map(&mw.m[gi], gi == 0 ? g.W : g.Wg[gi], (uint64_t)w_rows, (uint64_t)g.K_in,
+                  swiglu ? 64 : dfl::BM, d->id))
+      return DFLASH_ERR_CUDA;
   if (!bf16_map(&mx, g.X, (uint64_t)g.T, (uint64_t)g.K_in, BN, d->id)) return DFLASH_ERR_CUDA;
   dfl::GemmParams p;
   p.out = g.out;
@@ -840,7 +862,9 @@ static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
   p.T = g.T;
   p.S = g.S;
   p.kb_per_split = g.K_in / dfl::BK / g.S;
-  p.m_tiles = swiglu ? g.N_out / 64 : (g.N_out + dfl::BM - 1) / dfl::BM;
+  p.mtg = swiglu ? g.N_out / 64 : (g.N_out + dfl::BM - 1) / dfl::BM;
+  p.m_tiles = p.mtg * g.groups;
+  p.ostride = g.ostride;
   p.t_tiles = (g.T + BN - 1) / BN;
   p.num_units = p.m_tiles * p.t_tiles * g.S;
   p.mode = g.mode;
@@ -886,6 +910,14 @@ int gemm_run(const GemmCall &g, cudaStream_t st) {
   if (g.K_in % 64 || g.S < 1 || (g.K_in / 64) % g.S) return DFLASH_ERR_DIMS;
   if (g.chunk < 0 || (g.chunk > 0 && g.mode == GEMM_PARTIAL)) return DFLASH_ERR_DIMS;
   if (g.stats && (g.mode != GEMM_REDUCE || g.dtype != DFLASH_BF16)) return DFLASH_ERR_DIMS;
+  if (g.groups < 1 || g.groups > dfl::kMaxGroups) return DFLASH_ERR_DIMS;
+  if (g.groups > 1) {
+    if (g.mode != GEMM_REDUCE || g.dtype != DFLASH_BF16 || g.N_out % dfl::BM || g.out_bf16 ||
+        g.stats || !g.out_f32)
+      return DFLASH_ERR_DIMS;
+    for (int gi = 1; gi < g.groups; ++gi)
+      if (!g.Wg[gi] || (uintptr_t)g.Wg[gi] % 16) return DFLASH_ERR_ALIGN;
+  }
   if (g.chunk > 0 && (!g.counters || !g.out)) return DFLASH_ERR_NULL;
   if (g.mode == GEMM_SWIGLU && g.N_out % 64) return DFLASH_ERR_DIMS;
   if (g.mode == GEMM_QKV &&

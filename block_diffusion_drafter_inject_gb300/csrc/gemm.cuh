@@ -47,6 +47,12 @@ struct GemmCall {
   int ldb = 0;
   int *counters = nullptr;    // tile tickets, zero on entry and on exit (S > 1)
   int *err = nullptr;
+  // GEMM_REDUCE (bf16) with groups > 1: one launch over `groups` weight matrices of
+  // N_out rows each (N_out a multiple of 128, W = group 0, Wg[g] the others, all with
+  // the same X); group g writes out_f32 + g * ostride
+  int groups = 1;
+  const void *Wg[8] = {};
+  size_t ostride = 0;
   // GEMM_REDUCE (bf16): per token t and 128-row weight tile i, (max, sum e^(y - max))
   // of the tile's outputs -> stats[t * ceil(N_out/128) + i]
   float2 *stats = nullptr;

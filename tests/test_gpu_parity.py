@@ -30,6 +30,8 @@ CASES = [
     ("small_gqa", 2, 8, [200, 129]),
     ("tiny_bf16", 1, 32, [1]),
     ("small", 1, 2, [96]),
+    ("tiny_bf16", 9, 8, [70, 3, 64, 0, 200, 17, 64, 65, 9]),   # two 64-row conv tiles
+    ("tiny_bf16", 2, 12, [40, 77]),                            # K does not divide 64
 ]
 
 
