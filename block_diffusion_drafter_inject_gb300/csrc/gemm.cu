@@ -189,11 +189,13 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         cs[j] = c0 + j < p.T ? __ldg(&p.rope_cs[(size_t)(c0 + j) * half + di]) : make_float2(1.f, 0.f);
+      // the head's sum of squares per token: nw = 2 or 4 warp partials
+      const float *s0 = xss + w0 * 16;
       float o[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        float sq = 0.f;
-        for (int w = 0; w < nw; ++w) sq += xss[(w0 + w) * 16 + j];
+        float sq = s0[j] + s0[16 + j];
+        if (nw == 4) sq += s0[32 + j] + s0[48 + j];
         const float inv = rsqrtf(sq / dh + p.eps);
         const float x = v[j] * inv * g, y = xbuf[pr * 17 + j] * inv * gp;
         o[j] = d < half ? x * cs[j].x - y * cs[j].y : x * cs[j].x + y * cs[j].y;
