@@ -8,6 +8,8 @@
 // writes it out; the combine kernel merges the splits in order.
 #include <math.h>
 
+#include <algorithm>
+
 #include "attention.cuh"
 #include "pointwise.cuh"
 
@@ -46,9 +48,9 @@ __global__ void __launch_bounds__(256) k_attn_split(
   const int n_ctx = ctx < window ? (ctx > 0 ? ctx : 0) : window;
   const int lo = ctx - n_ctx;
   const int n_keys = n_ctx + K;
-  const int k_begin = split * kps;
+  const int k_begin = split * kps;  // the last split takes every key after it
   if (k_begin >= n_keys) return;
-  const int k_end = min(n_keys, k_begin + kps);
+  const int k_end = split == nsplit - 1 ? n_keys : min(n_keys, k_begin + kps);
   const float scale = rsqrtf((float)DH);
 
   // query rows of this group: qr = i*grp + g -> slot i, q head kvh*grp + g
@@ -205,8 +207,8 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
   const int ctx = A.ctx_len[b];
   const int n_ctx = ctx < A.window ? (ctx > 0 ? ctx : 0) : A.window;
   const int lo = ctx - n_ctx, n_keys = n_ctx + A.K;
-  const int k_begin = split * A.kps;
-  const int k_end = min(n_keys, k_begin + A.kps);
+  const int k_begin = split * A.kps;  // the last split takes every key after it
+  const int k_end = split == A.nsplit - 1 ? n_keys : min(n_keys, k_begin + A.kps);
   const int ntiles = k_begin < n_keys ? (k_end - k_begin + CH - 1) / CH : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bf16 *blk = A.qkvb + (size_t)b * A.K * QKVW;  // this request's block rows
@@ -506,7 +508,7 @@ __global__ void k_attn_combine(const float *__restrict__ part, const int32_t *__
   const int qr = i * grp + g, qgi = qr / kQG, row = qr % kQG;
   const int ctx = ctx_len[b];
   const int n_ctx = ctx < window ? (ctx > 0 ? ctx : 0) : window;
-  const int ns = (n_ctx + K + kps - 1) / kps;
+  const int ns = min(nsplit, (n_ctx + K + kps - 1) / kps);  // the last split holds the rest
   const size_t base0 = (((size_t)b * nqg + qgi) * Hkv + kvh) * nsplit;
   float M = -INFINITY;
 #pragma unroll 4
@@ -533,14 +535,14 @@ AttnPlan attn_plan(int B, int K, int Hq, int Hkv, int dh, int window, int num_sm
   pl.nqg = (QR + dfl::kQG - 1) / dfl::kQG;
   const int n_keys = window + K;
   const long items = (long)B * Hkv * pl.nqg;
-  // smallest key split (multiple of 64) that still gives ~2 CTAs per SM, and at
-  // most 16 splits (the splits of one item form a thread-block cluster)
+  // smallest key split (multiple of 64) that still gives ~2 CTAs per SM; at
+  // most 16 splits (the splits of one item form a thread-block cluster), the
+  // last one taking the keys left over
   int kps = dfl::kCH;
-  while (kps < n_keys && ((long)items * ((n_keys + kps - 1) / kps) > 2L * num_sms ||
-                          (n_keys + kps - 1) / kps > 16))
+  while (kps < n_keys && (long)items * std::min(16, (n_keys + kps - 1) / kps) > 2L * num_sms)
     kps += dfl::kCH;
   pl.kps = kps;
-  pl.nsplit = (n_keys + kps - 1) / kps;
+  pl.nsplit = std::min(16, (n_keys + kps - 1) / kps);
   pl.part_floats = (size_t)B * pl.nqg * Hkv * pl.nsplit * dfl::kQG * (dh + 2);
   return pl;
 }

@@ -139,3 +139,15 @@ def test_topk_heavy_ties(pattern):
         np.testing.assert_allclose(g["logp"].reshape(-1, k)[r], wlp, atol=2e-5)
     if pattern == "all_equal":
         np.testing.assert_array_equal(g["ids"][0, 0], np.arange(k))
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_bf16"])
+def test_long_window_last_split_takes_the_rest(name):
+    """A window of more than 16 key tiles: the attention's key splits are capped
+    at 16 (one thread-block cluster) and the last split takes every remaining
+    key; logits still match the oracle."""
+    c = Case(name, 1, 8, [1300], seed=5, window=1200).device()
+    g = c.run_device()
+    assert g["status"] == 0
+    err = rowmax_rel(g["logits"], c.oracle()["logits"])
+    assert err < TOL[c.cfg["dtype"]], err
