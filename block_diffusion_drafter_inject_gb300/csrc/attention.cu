@@ -443,6 +443,23 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
   }
   const int nrows = min(kQG, QR - qgi * kQG);
+  if (A.nsplit == 1) {  // one split: the rows are final here, o / l straight to bf16
+    if (active && kpart == 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = rb * 16 + g8 + 8 * h;
+        if (row < nrows) {
+          const int qrg = qgi * kQG + row, i = qrg / grp, g = qrg % grp;
+          bf16 *dst = A.ob + ((size_t)(b * A.K + i) * A.Hq + kvh * grp + g) * DH + 2 * t4;
+          const float il = 1.f / l_run[h];
+#pragma unroll
+          for (int n = 0; n < DH / 8; ++n)
+            *(uint32_t *)(dst + 8 * n) = pack_bf16(o[n][2 * h] * il, o[n][2 * h + 1] * il);
+        }
+      }
+    }
+    return;
+  }
   const int per = (nrows + A.nsplit - 1) / A.nsplit;
   const uint32_t recv = smem_u32(pRecv);
   cluster_sync();  // every CTA of the cluster is done with its tile buffers
