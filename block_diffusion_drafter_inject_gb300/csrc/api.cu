@@ -398,7 +398,8 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
       gq.eps = eps;
       TRY(gemm_run(gq, st));
       TRY(launch_attention_fused(L.ap, qkvb, (const dfl::bf16 *)kv.k, (const dfl::bf16 *)kv.v, l,
-                                 kv.page_table, kv.max_pages_per_req, kv.num_pages, c.page_size,
+                                 c.n_layers, kv.page_table, kv.max_pages_per_req, kv.num_pages,
+                                 c.page_size,
                                  ctx_len, B, K, Hq, Hkv, dh, c.window, (dfl::bf16 *)ob, err, st));
     } else {
       TRY(gemm_run(reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_REDUCE, qkv, QKVW,

@@ -7,10 +7,12 @@
 // keeps an online softmax (running max m, sum l, unnormalised output) and
 // writes it out; the combine kernel merges the splits in order.
 #include <math.h>
+#include <string.h>
 
 #include <algorithm>
 
 #include "attention.cuh"
+#include "gemm.cuh"
 #include "pointwise.cuh"
 
 namespace dfl {
@@ -167,10 +169,18 @@ __global__ void __launch_bounds__(256) k_attn_split(
 // a double-buffered, XOR-swizzled shared layout that ldmatrix reads without
 // bank conflicts.  Online softmax in base 2; partial state in natural units.
 // ---------------------------------------------------------------------------
+// K/V tile layout of the TMA loader: the tile's 64-column halves are separate
+// [64 rows][128 B] boxes, each with the 128-byte swizzle (16-byte chunk index
+// xor row % 8); chunk c of row r sits in half c / 8.
+__device__ __forceinline__ uint32_t swzt(int row, int chunk) {
+  return (uint32_t)((chunk >> 3) * 8192 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
 struct AttnArgs {
   const bf16 *qkvb;  // [B*K, (Hq + 2Hkv) * DH]: q, k normed and rotated, v
   const bf16 *kc, *vc;
   size_t layer_off;
+  int layer;
   const int32_t *table;
   int max_pages, num_pages, P;
   const int32_t *ctx_len;
@@ -183,20 +193,39 @@ struct AttnArgs {
 // KP warps share each 16-row query block and split every key tile KP ways
 // (KP = 1, 2, 4 for groups of <= 64, 32, 16 query rows); their softmax states
 // are merged in shared memory after the tile loop.
-template <int DH, int KP>
-__global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
+// TK (page size 64): the key tiles are the window's cache pages, each brought
+// in by TMA (two 64x64 boxes for K and for V per 128-wide head) by one thread
+// with an mbarrier per stage, then one tile of the block slots; rows outside
+// the window are masked and their V rows zeroed.  Otherwise every thread copies
+// 16-byte chunks of the tile's key rows with cp.async.
+template <int DH, int KP, bool TK>
+__global__ void __launch_bounds__(128)
+    k_attn_mma(const AttnArgs A, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV) {
   constexpr int CH = kCH;          // keys per tile
   constexpr int CHUNKS = DH / 8;   // 16-byte chunks per row
   constexpr int RB = DH * 2;       // bytes per row
   constexpr int TILE = CH * RB;    // bytes per K (or V) tile
   constexpr int NST = kAttnStages; // tile stages in flight
   constexpr int QROWS = 64 / KP;   // query rows staged (row blocks x 16)
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ int s_valid[NST][CH];
+  __shared__ __align__(8) uint64_t kvbar[NST];
+  __shared__ int s_tbase[NST], s_tok[NST];
+  __shared__ int s_abort;
   uint8_t *pQ = smem;
   uint8_t *pK0 = smem + QROWS * RB;
   uint8_t *pRecv = pK0;  // after the tile loop: [nsplit][per][DH + 2] fp32, written by the peers
   const uint32_t sQ = smem_u32(pQ), sK0 = smem_u32(pK0), sV0 = sK0 + NST * TILE;
+  if (TK && threadIdx.x == 0) {
+    for (int st = 0; st < NST; ++st) mbar_init(&kvbar[st], 1);
+    s_abort = 0;
+    mbar_fence_init();
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (TK) __syncthreads();  // barrier init visible to every thread
   pdl_launch();
   pdl_wait();
 
@@ -209,9 +238,16 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
   const int lo = ctx - n_ctx, n_keys = n_ctx + A.K;
   const int k_begin = split * A.kps;  // the last split takes every key after it
   const int k_end = split == A.nsplit - 1 ? n_keys : min(n_keys, k_begin + A.kps);
-  const int ntiles = k_begin < n_keys ? (k_end - k_begin + CH - 1) / CH : 0;
+  // TK: window pages [pgf, pgf + nct) then the block tile, kps / 64 tiles a split
+  const int pgf = lo / CH, nct = n_ctx > 0 ? (ctx - 1) / CH - pgf + 1 : 0;
+  const int t_begin = split * (A.kps / CH);
+  const int t_end = split == A.nsplit - 1 ? nct + 1 : min(nct + 1, t_begin + A.kps / CH);
+  const int ntiles = TK ? max(0, t_end - t_begin)
+                        : (k_begin < n_keys ? (k_end - k_begin + CH - 1) / CH : 0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bf16 *blk = A.qkvb + (size_t)b * A.K * QKVW;  // this request's block rows
+  uint64_t pol_kv = 0;
+  if (TK) pol_kv = l2_policy_evict_first();
 
   // Loader: thread tid copies key row jrow = tid / 2 of every tile, chunks
   // [ch0, ch0 + CHUNKS/2) of its K and V rows: a context key from the paged
@@ -227,7 +263,59 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
     const int page = A.table[(size_t)b * A.max_pages + pi];
     return (page >= 0 && page < A.num_pages) ? page : -DFLASH_DEV_PAGE_RANGE;
   };
+  // TK loader: one thread looks the page up and starts the boxes; the block
+  // tile's rows come from the projection rows by cp.async (zeros past K)
+  auto load_tile_tk = [&](int t, int stage) {
+    const int gt = t_begin + t;
+    if (gt < nct) {
+      if (tid == 0) {
+        const int pi = pgf + gt;
+        int page = -1;
+        if (pi < A.max_pages) {
+          page = A.table[(size_t)b * A.max_pages + pi];
+          if (page < 0 || page >= A.num_pages) {
+            set_err(A.err, DFLASH_DEV_PAGE_RANGE);
+            page = -1;
+          }
+        } else {
+          set_err(A.err, DFLASH_DEV_POS_RANGE);
+        }
+        s_tbase[stage] = pi * CH;
+        s_tok[stage] = page >= 0;
+        if (page >= 0) {
+          mbar_expect_tx(&kvbar[stage], 2 * TILE);
+          const int y = (int)((((size_t)A.layer * A.num_pages + page) * A.Hkv + kvh) * CH);
+#pragma unroll
+          for (int hh = 0; hh < DH / 64; ++hh) {
+            tma_load_2d(pK0 + stage * TILE + hh * 8192, &tmK, &kvbar[stage], 64 * hh, y, pol_kv);
+            tma_load_2d(pK0 + NST * TILE + stage * TILE + hh * 8192, &tmV, &kvbar[stage], 64 * hh,
+                        y, pol_kv);
+          }
+        } else {
+          mbar_arrive(&kvbar[stage]);
+        }
+      }
+    } else {
+      const bool ok = jrow < A.K;
+      const bf16 *row = blk + (size_t)(ok ? jrow : 0) * QKVW;
+      const bf16 *srck = row + (size_t)(A.Hq + kvh) * DH, *srcv = row + (size_t)(A.Hq + A.Hkv + kvh) * DH;
+#pragma unroll
+      for (int c = ch0; c < ch0 + CHUNKS / 2; ++c) {
+        cp_async16(sK0 + stage * TILE + swzt(jrow, c), srck + c * 8, ok ? 16 : 0);
+        cp_async16(sV0 + stage * TILE + swzt(jrow, c), srcv + c * 8, ok ? 16 : 0);
+      }
+      if (tid == 0) {
+        s_tbase[stage] = -1;
+        s_tok[stage] = 1;
+        mbar_arrive(&kvbar[stage]);
+      }
+    }
+  };
   auto load_tile = [&](int t, int stage, int page) {
+    if constexpr (TK) {
+      load_tile_tk(t, stage);
+      return;
+    }
     const int key = k_begin + t * CH + jrow;
     const bf16 *srck = A.kc, *srcv = A.vc;
     int ok = 0;
@@ -256,7 +344,7 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
   };
   static_assert(kPageAhead == 3 && NST == 3, "page pipeline below holds three tiles");
   static_assert(DFLASH_DEV_PAGE_RANGE > 1 && DFLASH_DEV_POS_RANGE > 1, "error codes vs -1");
-  int pg0 = key_page(0), pg1 = key_page(1), pg2 = key_page(2);
+  int pg0 = TK ? 0 : key_page(0), pg1 = TK ? 0 : key_page(1), pg2 = TK ? 0 : key_page(2);
 
   // queries qr = i*grp + g of this group: projection rows, copied (zeros past QR)
   for (int e = tid; e < QROWS * CHUNKS; e += 128) {
@@ -273,8 +361,8 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
     cp_async_commit();
   }
   pg0 = pg2;  // page of tile NST-1 = 2
-  pg1 = key_page(3);
-  pg2 = key_page(4);
+  pg1 = TK ? 0 : key_page(3);
+  pg2 = TK ? 0 : key_page(4);
 
   constexpr int RW = 4 / KP;            // query row blocks per CTA
   constexpr int KW = CH / KP;           // keys of a tile per warp
@@ -299,9 +387,24 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
       cp_async_commit();
       pg0 = pg1;
       pg1 = pg2;
-      pg2 = key_page(t + NST + 2);
+      pg2 = TK ? 0 : key_page(t + NST + 2);
     }
-    cp_async_wait<NST - 1>();  // tile t has landed
+    cp_async_wait<NST - 1>();  // tile t has landed (cp.async part)
+    if constexpr (TK) {
+      // the TMA part; then zero the V rows outside the window (a page's other
+      // rows may hold anything, and 0 * NaN would reach the output)
+      if (!mbar_wait(&kvbar[stage], (uint32_t)((t / NST) & 1), &s_abort) && tid == 0)
+        set_err(A.err, DFLASH_DEV_TIMEOUT);
+      const int base = s_tbase[stage];
+      if (base >= 0 && tid < CH) {
+        const int pos = base + tid;
+        if (!(s_tok[stage] && pos >= lo && pos < ctx)) {
+#pragma unroll
+          for (int c = 0; c < CHUNKS; ++c)
+            *(uint4 *)(pK0 + NST * TILE + stage * TILE + swzt(tid, c)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
     __syncthreads();
     if (t == 0 && active) {
 #pragma unroll
@@ -320,8 +423,8 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(sK + swz(kw0 + 16 * jp + (mi >> 1) * 8 + r8, 2 * kk + (mi & 1), RB), b0, b1,
-                  b2, b3);
+          const int kr = kw0 + 16 * jp + (mi >> 1) * 8 + r8, kc = 2 * kk + (mi & 1);
+          ldsm_x4(sK + (TK ? swzt(kr, kc) : swz(kr, kc, RB)), b0, b1, b2, b3);
           mma_bf16_16816(sc[2 * jp], qf[kk], b0, b1);
           mma_bf16_16816(sc[2 * jp + 1], qf[kk], b2, b3);
         }
@@ -333,7 +436,13 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int col = kw0 + 8 * j + 2 * t4 + (e & 1);
-          const bool ok = (t0 + col < k_end) && s_valid[stage][col];
+          bool ok;
+          if constexpr (TK) {
+            const int base = s_tbase[stage];
+            ok = base >= 0 ? (s_tok[stage] && base + col >= lo && base + col < ctx) : col < A.K;
+          } else {
+            ok = (t0 + col < k_end) && s_valid[stage][col];
+          }
           const float v = ok ? sc[j][e] * sl2 : -INFINITY;
           sc[j][e] = v;
           mx[e >> 1] = fmaxf(mx[e >> 1], v);
@@ -381,8 +490,8 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
 #pragma unroll
         for (int np = 0; np < DH / 16; ++np) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(sV + swz(kw0 + 16 * kk + (mi & 1) * 8 + r8, 2 * np + (mi >> 1), RB), b0, b1,
-                    b2, b3);
+          const int vr = kw0 + 16 * kk + (mi & 1) * 8 + r8, vc = 2 * np + (mi >> 1);
+          ldsm_x4_t(sV + (TK ? swzt(vr, vc) : swz(vr, vc, RB)), b0, b1, b2, b3);
           mma_bf16_16816(o[2 * np], pa[kk], b0, b1);
           mma_bf16_16816(o[2 * np + 1], pa[kk], b2, b3);
           mma_bf16_16816(o[2 * np], pl[kk], b0, b1);
@@ -390,6 +499,7 @@ __global__ void __launch_bounds__(128) k_attn_mma(const AttnArgs A) {
         }
       }
     }
+    if (TK) fence_proxy_async();  // this stage's generic writes before its next TMA fill
     __syncthreads();
     if (++stage == NST) stage = 0;
   }
@@ -590,32 +700,58 @@ static int launch_attn_dh(const AttnPlan &pl, const S *qb, const S *kb, const S 
   return DFLASH_OK;
 }
 
-template <int DH, int KP>
-static int launch_attn_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl::bf16 *kc,
-                             const dfl::bf16 *vc, int layer, const int32_t *table, int max_pages,
-                             int num_pages, int P, const int32_t *ctx_len, int B, int K, int Hq,
-                             int Hkv, int window, dfl::bf16 *ob, int *err, cudaStream_t st) {
-  // Q and NST K and V tiles; the key-part merge, the receive buffer and the
-  // combine weights reuse the tile buffers after the tile loop
+template <int DH, int KP, bool TK>
+static int launch_attn_fused(const AttnPlan &pl, const dfl::AttnArgs &a, int B,
+                             const CUtensorMap &mk, const CUtensorMap &mv, cudaStream_t st) {
+  // Q and NST K and V tiles (1 KB of alignment slack); the key-part merge, the
+  // receive buffer and the combine weights reuse the tile buffers afterwards
   static_assert(dfl::kAttnRecvBytes + (dfl::kQG + 16) * 16 * 4 <=
                     2 * dfl::kAttnStages * dfl::kCH * DH * 2,
                 "receive buffer and combine weights in the tile buffers");
   const size_t smem =
-      (size_t)(64 / KP) * DH * 2 + 2 * (size_t)dfl::kAttnStages * dfl::kCH * DH * 2;
+      1024 + (size_t)(64 / KP) * DH * 2 + 2 * (size_t)dfl::kAttnStages * dfl::kCH * DH * 2;
   static int attr_done = 0;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess ||
-        cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP>,
+    if (cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP, TK>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP, TK>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return DFLASH_ERR_CUDA;
     attr_done = 1;
   }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.nsplit, a.Hkv, B * pl.nqg);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pl.nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  count_launch();
+  DFL_CHECK_LAUNCH(cudaLaunchKernelEx(&cfg, dfl::k_attn_mma<DH, KP, TK>, a, mk, mv));
+  return DFLASH_OK;
+}
+
+int launch_attention_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl::bf16 *kc,
+                           const dfl::bf16 *vc, int layer, int n_layers, const int32_t *table,
+                           int max_pages, int num_pages, int P, const int32_t *ctx_len, int B,
+                           int K, int Hq, int Hkv, int dh, int window, dfl::bf16 *ob, int *err,
+                           cudaStream_t st) {
+  const Dev *d = device();
+  if (!d) return DFLASH_ERR_DEVICE;
   dfl::AttnArgs a;
   a.qkvb = qkvb;
   a.kc = kc;
   a.vc = vc;
-  a.layer_off = (size_t)layer * num_pages * Hkv * P * DH;
+  a.layer_off = (size_t)layer * num_pages * Hkv * P * dh;
+  a.layer = layer;
   a.table = table;
   a.max_pages = max_pages;
   a.num_pages = num_pages;
@@ -630,34 +766,20 @@ static int launch_attn_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const df
   a.nqg = pl.nqg;
   a.ob = ob;
   a.err = err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.nsplit, Hkv, B * pl.nqg);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = pl.nsplit;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl_enabled() ? 2 : 1;
-  count_launch();
-  DFL_CHECK_LAUNCH(cudaLaunchKernelEx(&cfg, dfl::k_attn_mma<DH, KP>, a));
-  return DFLASH_OK;
-}
-
-int launch_attention_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl::bf16 *kc,
-                           const dfl::bf16 *vc, int layer, const int32_t *table, int max_pages,
-                           int num_pages, int P, const int32_t *ctx_len, int B, int K, int Hq,
-                           int Hkv, int dh, int window, dfl::bf16 *ob, int *err, cudaStream_t st) {
+  // pages of 64 positions: whole pages are loaded by TMA from the caches viewed
+  // as [n_layers * num_pages * Hkv * 64, dh] matrices
+  CUtensorMap mk, mv;
+  memset(&mk, 0, sizeof(mk));
+  memset(&mv, 0, sizeof(mv));
+  const uint64_t rows = (uint64_t)n_layers * num_pages * Hkv * 64;
+  const bool tk = P == dfl::kCH && rows < (1ull << 31) && (uintptr_t)kc % 16 == 0 &&
+                  (uintptr_t)vc % 16 == 0 && bf16_map(&mk, kc, rows, dh, 64, d->id) &&
+                  bf16_map(&mv, vc, rows, dh, 64, d->id);
   const int QR = K * (Hq / Hkv);
   const int kp = QR <= 16 ? 4 : QR <= 32 ? 2 : 1;
-#define DFL_ATTN(D, KPV)                                                                      \
-  return launch_attn_fused<D, KPV>(pl, qkvb, kc, vc, layer, table, max_pages, num_pages, P,   \
-                                   ctx_len, B, K, Hq, Hkv, window, ob, err, st)
+#define DFL_ATTN(D, KPV)                                                                   \
+  return tk ? launch_attn_fused<D, KPV, true>(pl, a, B, mk, mv, st)                        \
+            : launch_attn_fused<D, KPV, false>(pl, a, B, mk, mv, st)
   if (dh == 128) {
     if (kp == 4) DFL_ATTN(128, 4);
     if (kp == 2) DFL_ATTN(128, 2);

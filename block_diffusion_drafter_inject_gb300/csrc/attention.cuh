@@ -27,9 +27,12 @@ int launch_block_attention(const AttnPlan &pl, const S *qb, const S *kb, const S
 // rotated) and v rows from qkvb [B*K, (Hq+2Hkv)*dh] and the paged context
 // window, attends, and merges its key splits through the cluster's distributed
 // shared memory into o [B*K, Hq*dh].
+// Page size 64: whole cache pages are loaded by TMA (caches [n_layers][num_pages]
+// [Hkv][64][dh]); other page sizes copy 16-byte chunks per key row.
 int launch_attention_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl::bf16 *kc,
-                           const dfl::bf16 *vc, int layer, const int32_t *table, int max_pages,
-                           int num_pages, int P, const int32_t *ctx_len, int B, int K, int Hq,
-                           int Hkv, int dh, int window, dfl::bf16 *ob, int *err, cudaStream_t st);
+                           const dfl::bf16 *vc, int layer, int n_layers, const int32_t *table,
+                           int max_pages, int num_pages, int P, const int32_t *ctx_len, int B,
+                           int K, int Hq, int Hkv, int dh, int window, dfl::bf16 *ob, int *err,
+                           cudaStream_t st);
 
 }  // namespace dflh

@@ -237,6 +237,11 @@ __device__ __forceinline__ uint64_t globaltimer() {
 // a wait that has not finished after this long is treated as a fault
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// orders this thread's earlier generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses of the same locations
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }

@@ -658,8 +658,8 @@ struct MapKeyHash {
 };
 
 // Tensor map of a row-major bf16 matrix [rows, cols]; box = 64 columns x box_rows rows.
-static bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t cols,
-                     uint32_t box_rows, int dev) {
+bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t cols,
+              uint32_t box_rows, int dev) {
   static std::mutex mu;
   static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
   MapKey key{(uintptr_t)ptr, rows, cols, box_rows, dev};

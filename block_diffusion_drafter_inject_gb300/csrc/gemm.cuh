@@ -76,6 +76,11 @@ size_t gemm_tiles(int N_out, int T, int mode, int bn = 0);
 // multiple of 64, S dividing K_in/64.  Returns DFLASH_OK or an error.
 int gemm_run(const GemmCall &g, cudaStream_t stream);
 
+// Tensor map (cached) of a row-major bf16 matrix [rows, cols] (cols * 2 a multiple of
+// 16 bytes): boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t cols,
+              uint32_t box_rows, int dev);
+
 // GEMM_PARTIAL convenience form
 int gemm_xwT(int dtype, const void *W, int N_out, int K_in, const void *X, int T, float *out,
              int ld, int S, int *err, cudaStream_t stream);

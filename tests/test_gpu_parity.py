@@ -151,3 +151,13 @@ def test_long_window_last_split_takes_the_rest(name):
     assert g["status"] == 0
     err = rowmax_rel(g["logits"], c.oracle()["logits"])
     assert err < TOL[c.cfg["dtype"]], err
+
+
+def test_page_size_not_64():
+    """Pages of 16 positions: the attention copies key rows in 16-byte chunks
+    instead of whole pages; logits still match the oracle."""
+    c = Case("small", 2, 8, [150, 37], seed=6, page_size=16).device()
+    g = c.run_device()
+    assert g["status"] == 0
+    err = rowmax_rel(g["logits"], c.oracle()["logits"])
+    assert err < TOL["bf16"], err
