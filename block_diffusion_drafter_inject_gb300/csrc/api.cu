@@ -126,7 +126,7 @@ static int check_kv(const dflash_config *c, const dflash_kv *kv) {
 // ---------------------------------------------------------------------------
 constexpr int kMaxReduceSplits = 16;      // slices a reduce-mode GEMM may use
 constexpr size_t kTicketInts = 1 << 14;   // tile tickets of one reduce-mode GEMM
-constexpr size_t kTopkTicketInts = 1 << 14;  // reserved header words (B*(K-1) rows at most)
+constexpr size_t kTopkTicketInts = 1 << 14;  // selector tickets, one per request (B at most)
 constexpr int kKvGroup = 8;  // layers per grouped K/V projection launch of injection
 // Fixed header of every workspace: status word, GEMM tile tickets, top-k row
 // tickets.  They must stay zero between calls; every other region is scratch
@@ -461,7 +461,8 @@ static int run_select(const dflash_config &c, const dflash_weights &w, const int
                              nullptr, 0),
                  st));
   }
-  TRY(launch_viterbi(U, Vp, ids, logp, B, K, k, r, (float *)(ws + L.pairs), path, score, st));
+  TRY(launch_viterbi(U, Vp, ids, logp, B, K, k, r, (float *)(ws + L.pairs),
+                     (int *)(ws + L.topk_tickets), path, score, st));
   return DFLASH_OK;
 }
 
@@ -535,6 +536,7 @@ int dflash_select_path(const dflash_config *cfg, const dflash_weights *w, const 
   if (rc != DFLASH_OK) return rc;
   if (B < 0 || K < 2 || K > DFLASH_MAX_BLOCK) return DFLASH_ERR_BLOCK;
   if (B == 0) return DFLASH_OK;
+  if ((size_t)B > kTopkTicketInts) return DFLASH_ERR_DIMS;
   if (!w || !anchor || !topk_ids || !topk_logp || !path || !path_score || !ws)
     return DFLASH_ERR_NULL;
   if (!w->embed || !w->sel_pu || !w->sel_pv) return DFLASH_ERR_NULL;

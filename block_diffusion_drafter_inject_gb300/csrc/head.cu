@@ -4,6 +4,8 @@
 // lower index (token id, candidate rank).
 #include <math.h>
 
+#include <algorithm>
+
 #include "head.cuh"
 
 namespace dfl {
@@ -364,16 +366,26 @@ __global__ void __launch_bounds__(256) k_sel_gather(const S *__restrict__ E,
   }
 }
 
-// Pair scores of every adjacent candidate pair, all positions at once:
-//   pair[b][t][i][j] = u(pred_i) . v(c_tj),  pred = the anchor at t = 0, else c_{t-1}
-// u = P_u e and v = P_v e are rows of the selector projections, r wide.
-// grid (K-1, B): rows staged in shared memory, one thread per pair.
+// Pair scores and the Viterbi walk.  CTA (t, b) stages the rows of request b's
+// candidates at positions t and t+1 (U of position t, or of the anchor for
+// t = 0; Vp of position t+1) and writes pair[b][t][i][j] = U_i . Vp_j, then
+// takes a ticket on its request; the CTA that finishes the request's last
+// position (no waiting) walks max-sum Viterbi over the K-1 positions of k
+// candidates on all of them (staged in shared memory).  Ties go to the lower
+// candidate rank.  tickets: B ints, zero on entry and on exit.
 __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
                                                    const float *__restrict__ Vp, int K, int k,
-                                                   int r, float *__restrict__ pair) {
+                                                   int r, float *__restrict__ pair, int *tickets,
+                                                   const int32_t *__restrict__ topk_ids,
+                                                   const float *__restrict__ topk_logp,
+                                                   int32_t *__restrict__ path,
+                                                   float *__restrict__ score) {
   extern __shared__ float sm[];
   const int LDR = r + 1;  // odd row stride: the threads of a warp hit distinct banks
   float *su = sm, *sv = sm + (size_t)k * LDR;
+  __shared__ float delta[DFLASH_MAX_TOPK];
+  __shared__ int bp[DFLASH_MAX_BLOCK][DFLASH_MAX_TOPK];
+  __shared__ int s_last;
   pdl_launch();
   pdl_wait();
   const int t = blockIdx.x, b = blockIdx.y;
@@ -403,37 +415,31 @@ __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
     }
     out[e] = (d0 + d1) + (d2 + d3);
   }
-}
-
-// One CTA per request: max-sum Viterbi over the K-1 positions of k candidates
-// on the precomputed pair scores (staged in shared memory with one coalesced
-// load).  Ties go to the lower candidate rank.
-__global__ void __launch_bounds__(256) k_viterbi(const float *__restrict__ pair,
-                                                 const int32_t *__restrict__ topk_ids,
-                                                 const float *__restrict__ topk_logp, int K, int k,
-                                                 int32_t *__restrict__ path,
-                                                 float *__restrict__ score) {
-  extern __shared__ float sp[];  // [(K-1) * k * k] pair scores, then [(K-1) * k] logp
-  __shared__ float delta[DFLASH_MAX_TOPK];
-  __shared__ int bp[DFLASH_MAX_BLOCK][DFLASH_MAX_TOPK];
-  pdl_launch();
-  pdl_wait();
-  const int b = blockIdx.x;
+  // ticket: the last position of the request walks the lattice
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_last = atomicAdd(&tickets[b], 1) == K - 2;
+    if (s_last) tickets[b] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
   const int npair = (K - 1) * k * k, nlp = (K - 1) * k;
-  float *slp = sp + npair;
+  float *sp = sm, *slp = sm + npair;  // the staged rows are no longer needed
   const float *pr = pair + (size_t)b * npair;
   const float *lp = topk_logp + (size_t)b * nlp;
-  for (int e = threadIdx.x; e < npair; e += blockDim.x) sp[e] = pr[e];
+  for (int e = threadIdx.x; e < npair; e += blockDim.x) sp[e] = __ldcg(pr + e);
   for (int e = threadIdx.x; e < nlp; e += blockDim.x) slp[e] = lp[e];
   __syncthreads();
   if (threadIdx.x >= 32) return;
   const int j = threadIdx.x;
-  for (int t = 0; t < K - 1; ++t) {
-    const float *ps = sp + (size_t)t * k * k;
+  for (int tt = 0; tt < K - 1; ++tt) {
+    const float *ps = sp + (size_t)tt * k * k;
     float nd = 0.f;
     int arg = 0;
     if (j < k) {
-      if (t == 0) {
+      if (tt == 0) {
         nd = slp[j] + ps[j];
       } else {
         float best = -INFINITY;
@@ -441,13 +447,13 @@ __global__ void __launch_bounds__(256) k_viterbi(const float *__restrict__ pair,
           const float c = delta[i] + ps[i * k + j];
           if (c > best) best = c, arg = i;  // strict: the lower rank keeps ties
         }
-        nd = slp[t * k + j] + best;
+        nd = slp[tt * k + j] + best;
       }
     }
     __syncwarp();
     if (j < k) {
       delta[j] = nd;
-      bp[t][j] = arg;
+      bp[tt][j] = arg;
     }
     __syncwarp();
   }
@@ -457,9 +463,9 @@ __global__ void __launch_bounds__(256) k_viterbi(const float *__restrict__ pair,
       if (delta[i] > delta[best]) best = i;
     score[b] = delta[best];
     int c = best;
-    for (int t = K - 2; t >= 0; --t) {
-      path[(size_t)b * (K - 1) + t] = topk_ids[((size_t)b * (K - 1) + t) * k + c];
-      c = bp[t][c];
+    for (int tt = K - 2; tt >= 0; --tt) {
+      path[(size_t)b * (K - 1) + tt] = topk_ids[((size_t)b * (K - 1) + tt) * k + c];
+      c = bp[tt][c];
     }
   }
 }
@@ -553,24 +559,17 @@ template int launch_sel_gather<dfl::bf16>(const dfl::bf16 *, const int32_t *, co
                                           int, int, int, int, dfl::bf16 *, int *, cudaStream_t);
 
 int launch_viterbi(const float *U, const float *Vp, const int32_t *topk_ids,
-                   const float *topk_logp, int B, int K, int k, int r, float *pair,
+                   const float *topk_logp, int B, int K, int k, int r, float *pair, int *tickets,
                    int32_t *path, float *score, cudaStream_t st) {
-  const size_t smem = sizeof(float) * 2 * (size_t)k * (r + 1);
+  const size_t smem = sizeof(float) * std::max(2 * (size_t)k * (r + 1),
+                                               (size_t)(K - 1) * k * k + (size_t)(K - 1) * k);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(dfl::k_sel_pairs, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return DFLASH_ERR_CUDA;
   }
   DFL_CHECK_LAUNCH(launch(dfl::k_sel_pairs, dim3(K - 1, B), dim3(256), smem, st, U, Vp, K, k, r,
-                          pair));
-  const size_t smem2 = sizeof(float) * ((size_t)(K - 1) * k * k + (size_t)(K - 1) * k);
-  if (smem2 > 48 * 1024) {
-    if (cudaFuncSetAttribute(dfl::k_viterbi, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem2) != cudaSuccess)
-      return DFLASH_ERR_CUDA;
-  }
-  DFL_CHECK_LAUNCH(launch(dfl::k_viterbi, dim3(B), dim3(256), smem2, st, (const float *)pair,
-                          topk_ids, topk_logp, K, k, path, score));
+                          pair, tickets, topk_ids, topk_logp, path, score));
   return DFLASH_OK;
 }
 

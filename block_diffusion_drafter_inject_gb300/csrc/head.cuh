@@ -18,9 +18,10 @@ int launch_sel_gather(const S *E, const int32_t *anchor, const int32_t *topk_ids
                       int k, int V, int D, S *rows, int *err, cudaStream_t st);
 
 // U, Vp: reduced selector projections [B*R, r] fp32 (R = 1 + (K-1)*k rows per
-// request: anchor, then candidates by (position, rank)); pair: B*(K-1)*k*k scratch
+// request: anchor, then candidates by (position, rank)); pair: B*(K-1)*k*k scratch;
+// tickets: B ints, zero on entry and on exit
 int launch_viterbi(const float *U, const float *Vp, const int32_t *topk_ids,
-                   const float *topk_logp, int B, int K, int k, int r, float *pair,
+                   const float *topk_logp, int B, int K, int k, int r, float *pair, int *tickets,
                    int32_t *path, float *score, cudaStream_t st);
 
 constexpr int kArgmaxChunk = 8192;

@@ -182,7 +182,7 @@ int dflash_draft_block(const dflash_config *cfg, const dflash_weights *w,
  * max-sum Viterbi from the anchor):
  *   delta_1(j) = logp_1(j) + u(anchor).v(c_1j)
  *   delta_t(j) = logp_t(j) + max_i [delta_{t-1}(i) + u(c_{t-1,i}).v(c_tj)]
- * Ties go to the lower candidate rank.
+ * Ties go to the lower candidate rank.  B <= 16384 (else DFLASH_ERR_DIMS).
  *   anchor      device int32 [B]
  *   topk_ids    device int32 [B, K-1, top_k];  topk_logp device f32 [B, K-1, top_k]
  *   path        device int32 [B, K-1] out;     path_score device f32 [B] out     */
