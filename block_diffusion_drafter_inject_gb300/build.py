@@ -36,7 +36,9 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _fingerprint():
+def source_fingerprint():
+    """Hash of the kernel sources, headers and compile flags (machine-independent):
+    identifies the build a stored profile measurement belongs to."""
     h = hashlib.sha256()
     for d in (CSRC, INCLUDE):
         for f in sorted(os.listdir(d)):
@@ -44,8 +46,11 @@ def _fingerprint():
                 h.update(f.encode())
                 h.update(open(os.path.join(d, f), "rb").read())
     h.update(" ".join(ARCH + FLAGS).encode())
-    h.update(os.uname().machine.encode())
     return h.hexdigest()
+
+
+def _fingerprint():
+    return source_fingerprint() + "|" + os.uname().machine
 
 
 def build(force=False, verbose=False, extra_flags=()):
