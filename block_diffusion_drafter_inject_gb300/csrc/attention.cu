@@ -19,11 +19,9 @@ namespace dfl {
 
 constexpr int kQG = 64;   // query rows per CTA
 constexpr int kCH = 64;   // keys per shared-memory tile
-constexpr int kAttnStages = 3;  // K/V tile stages of the tensor-core kernel
+constexpr int kAttnStages = 3;  // K/V tile stages of the tensor-core kernel (one split)
+constexpr int kAttnPrePages = 32;  // context tiles per CTA whose pages are looked up early
 constexpr int kPageAhead = 3;   // tiles whose pages a loader thread holds ahead
-// receive buffer of the cluster combine: (kQG + 16) rows x (DH + 2) floats, DH <= 128;
-// the combine weights [rows][nsplit <= 16] follow it
-constexpr int kAttnRecvBytes = (64 + 16) * (128 + 2) * 4;
 
 template <typename S, int DH>
 __global__ void __launch_bounds__(256) k_attn_split(
@@ -198,7 +196,7 @@ struct AttnArgs {
 // with an mbarrier per stage, then one tile of the block slots; rows outside
 // the window are masked and their V rows zeroed.  Otherwise every thread copies
 // 16-byte chunks of the tile's key rows with cp.async.
-template <int DH, int KP, bool TK>
+template <int DH, int KP, bool TK, int NST>
 __global__ void __launch_bounds__(128)
     k_attn_mma(const AttnArgs A, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV) {
@@ -206,7 +204,6 @@ __global__ void __launch_bounds__(128)
   constexpr int CHUNKS = DH / 8;   // 16-byte chunks per row
   constexpr int RB = DH * 2;       // bytes per row
   constexpr int TILE = CH * RB;    // bytes per K (or V) tile
-  constexpr int NST = kAttnStages; // tile stages in flight
   constexpr int QROWS = 64 / KP;   // query rows staged (row blocks x 16)
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -214,20 +211,34 @@ __global__ void __launch_bounds__(128)
   __shared__ __align__(8) uint64_t kvbar[NST];
   __shared__ int s_tbase[NST], s_tok[NST];
   __shared__ int s_abort;
+  __shared__ int s_pg[kAttnPrePages];
+  __shared__ __align__(8) uint64_t cmbar;  // the peers' rows of this CTA have landed
   uint8_t *pQ = smem;
   uint8_t *pK0 = smem + QROWS * RB;
-  uint8_t *pRecv = pK0;  // after the tile loop: [nsplit][per][DH + 2] fp32, written by the peers
+  // receive buffer of the cluster combine, [nsplit][per][DH + 2] fp32 written by
+  // the peers, then the combine weights [per][nsplit]
+  uint8_t *pRecv = pK0 + 2 * NST * TILE;
   const uint32_t sQ = smem_u32(pQ), sK0 = smem_u32(pK0), sV0 = sK0 + NST * TILE;
-  if (TK && threadIdx.x == 0) {
-    for (int st = 0; st < NST; ++st) mbar_init(&kvbar[st], 1);
-    s_abort = 0;
-    mbar_fence_init();
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-  }
-  if (TK) __syncthreads();  // barrier init visible to every thread
   pdl_launch();
-  pdl_wait();
+  // rows of this CTA's query group and the share that this CTA finishes
+  const int QR0 = A.K * (A.Hq / A.Hkv), qg0 = blockIdx.z % A.nqg;
+  const int nrows = min(kQG, QR0 - qg0 * kQG);
+  const int per = (nrows + A.nsplit - 1) / A.nsplit;
+  const int r0 = blockIdx.x * per, r1 = min(nrows, r0 + per);
+  const bool clus = A.nsplit > 1;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    if (TK) {
+      for (int st = 0; st < NST; ++st) mbar_init(&kvbar[st], 1);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+    }
+    if (clus) {
+      mbar_init(&cmbar, 1);
+      mbar_expect_tx(&cmbar, (uint32_t)(A.nsplit * max(0, r1 - r0) * (DH + 4) * 4));
+    }
+    if (TK || clus) mbar_fence_init();
+  }
 
   const int split = blockIdx.x, kvh = blockIdx.y;
   const int b = blockIdx.z / A.nqg, qgi = blockIdx.z % A.nqg;
@@ -245,6 +256,37 @@ __global__ void __launch_bounds__(128)
   const int ntiles = TK ? max(0, t_end - t_begin)
                         : (k_begin < n_keys ? (k_end - k_begin + CH - 1) / CH : 0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // TK: the context lengths and the page table are inputs of the pass (no
+  // kernel of the pass writes them), so the pages of the first context tiles
+  // are looked up, one thread per tile, before waiting for the projection; the
+  // first NST - 1 context tiles are loaded right away (the caches are complete:
+  // the pass's first kernel lets no later kernel start before all earlier work
+  // has completed) and the next two are prefetched into L2
+  const int npre = TK ? min(max(0, min(t_end, nct) - t_begin), kAttnPrePages) : 0;
+  if (TK && tid < npre) {
+    const int pi = pgf + t_begin + tid;
+    int page = -1;
+    if (pi < A.max_pages) {
+      page = A.table[(size_t)b * A.max_pages + pi];
+      if (page < 0 || page >= A.num_pages) {
+        set_err(A.err, DFLASH_DEV_PAGE_RANGE);
+        page = -1;
+      }
+    } else {
+      set_err(A.err, DFLASH_DEV_POS_RANGE);
+    }
+    s_pg[tid] = page;
+    if (page >= 0 && tid >= NST - 1 && tid < NST + 1) {  // the tiles after the first ones
+      const int y = (int)((((size_t)A.layer * A.num_pages + page) * A.Hkv + kvh) * CH);
+#pragma unroll
+      for (int hh = 0; hh < DH / 64; ++hh) {
+        tma_prefetch_l2_2d(&tmK, 64 * hh, y);
+        tma_prefetch_l2_2d(&tmV, 64 * hh, y);
+      }
+    }
+  }
+  __syncthreads();  // barrier init and the looked-up pages visible to every thread
+  if (clus) cluster_arrive_relaxed();  // this CTA's receive mbarrier is initialised
   const bf16 *blk = A.qkvb + (size_t)b * A.K * QKVW;  // this request's block rows
   uint64_t pol_kv = 0;
   if (TK) pol_kv = l2_policy_evict_first();
@@ -271,7 +313,9 @@ __global__ void __launch_bounds__(128)
       if (tid == 0) {
         const int pi = pgf + gt;
         int page = -1;
-        if (pi < A.max_pages) {
+        if (t < npre) {
+          page = s_pg[t];  // looked up (and checked) before the wait
+        } else if (pi < A.max_pages) {
           page = A.table[(size_t)b * A.max_pages + pi];
           if (page < 0 || page >= A.num_pages) {
             set_err(A.err, DFLASH_DEV_PAGE_RANGE);
@@ -342,9 +386,15 @@ __global__ void __launch_bounds__(128)
     }
     if (ch0 == 0) s_valid[stage][jrow] = ok;
   };
-  static_assert(kPageAhead == 3 && NST == 3, "page pipeline below holds three tiles");
+  static_assert(TK || (kPageAhead == 3 && NST == 3), "page pipeline below holds three tiles");
   static_assert(DFLASH_DEV_PAGE_RANGE > 1 && DFLASH_DEV_POS_RANGE > 1, "error codes vs -1");
   int pg0 = TK ? 0 : key_page(0), pg1 = TK ? 0 : key_page(1), pg2 = TK ? 0 : key_page(2);
+  // TK: the context tiles among the first NST - 1 start loading now
+  if (TK)
+#pragma unroll
+    for (int t = 0; t < NST - 1; ++t)
+      if (t < ntiles && t_begin + t < nct) load_tile_tk(t, t);
+  pdl_wait();  // the projection rows (queries, block keys and values) are ready
 
   // queries qr = i*grp + g of this group: projection rows, copied (zeros past QR)
   for (int e = tid; e < QROWS * CHUNKS; e += 128) {
@@ -357,7 +407,7 @@ __global__ void __launch_bounds__(128)
   // the first NST-1 tiles in flight; one commit group per tile (empty past the end)
 #pragma unroll
   for (int t = 0; t < NST - 1; ++t) {
-    if (t < ntiles) load_tile(t, t, t == 0 ? pg0 : pg1);
+    if (t < ntiles && !(TK && t_begin + t < nct)) load_tile(t, t, t == 0 ? pg0 : pg1);
     cp_async_commit();
   }
   pg0 = pg2;  // page of tile NST-1 = 2
@@ -543,16 +593,20 @@ __global__ void __launch_bounds__(128)
   }
 
   // Combine through the cluster: query row `row` is finished by CTA
-  // owner = row / per.  Every CTA pushes its (m, l, o) of that row into the
-  // owner's receive buffer recv[split][row - owner*per][0..DH+1] with posted
-  // distributed-shared-memory stores; one cluster barrier; each owner then
-  // merges its rows from local shared memory.
+  // owner = row / per.  Every CTA stages its (m, l, o) rows in shared memory
+  // (m, l, 2 floats of padding, o: DH + 4 floats, a multiple of 16 bytes) and
+  // copies row `row` with one bulk copy into the owner's receive buffer
+  // recv[split][row - owner*per], counted in bytes on the owner's mbarrier;
+  // each owner waits for its bytes, then merges its rows from local shared
+  // memory.  The cluster barrier arrived at the start makes every receive
+  // mbarrier initialised before the first copy; the one arrived once a CTA's
+  // rows have landed keeps every CTA (and its staged rows) alive until all
+  // copies of the cluster have landed.
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
   }
-  const int nrows = min(kQG, QR - qgi * kQG);
   if (A.nsplit == 1) {  // one split: the rows are final here, o / l straight to bf16
     if (active && kpart == 0) {
 #pragma unroll
@@ -570,34 +624,39 @@ __global__ void __launch_bounds__(128)
     }
     return;
   }
-  const int per = (nrows + A.nsplit - 1) / A.nsplit;
   const uint32_t recv = smem_u32(pRecv);
-  cluster_sync();  // every CTA of the cluster is done with its tile buffers
-  constexpr int RS = DH + 2;  // floats per received row
+  constexpr int RS = DH + 4;  // floats per staged / received row
+  float *stg = (float *)pK0;  // staged rows [row][RS] (the tile buffers are free now)
   if (active && kpart == 0) {
     const float ln2 = 0.6931471805599453f;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = rb * 16 + g8 + 8 * h;
       if (row < nrows) {
-        const int owner = row / per, lr = row - owner * per;
-        const uint32_t dst = recv + (uint32_t)(((split * per) + lr) * RS) * 4u;
+        float *d = stg + row * RS;
         if (t4 == 0) {
-          st_dsmem(dst, owner, m_run[h] == -INFINITY ? -INFINITY : m_run[h] * ln2);
-          st_dsmem(dst + 4, owner, l_run[h]);
+          d[0] = m_run[h] == -INFINITY ? -INFINITY : m_run[h] * ln2;
+          d[1] = l_run[h];
         }
 #pragma unroll
         for (int n = 0; n < DH / 8; ++n)
-          st_dsmem_v2(dst + (uint32_t)(2 + 8 * n + 2 * t4) * 4u, owner, o[n][2 * h],
-                      o[n][2 * h + 1]);
+          *(float2 *)(d + 4 + 8 * n + 2 * t4) = make_float2(o[n][2 * h], o[n][2 * h + 1]);
       }
     }
   }
-  cluster_sync();
-  const int r0 = split * per, r1 = min(nrows, r0 + per);
+  fence_proxy_async();  // the staged rows, written by this thread, before the bulk copies
+  __syncthreads();
+  cluster_wait();  // every receive mbarrier of the cluster is initialised
+  if (tid < nrows) {
+    const int owner = tid / per, lr = tid - owner * per;
+    bulk_copy_to_peer(cluster_addr(recv + (uint32_t)((split * per + lr) * RS) * 4u, owner),
+                      smem_u32(stg + tid * RS), RS * 4, cluster_addr(smem_u32(&cmbar), owner));
+  }
+  if (!mbar_wait<true>(&cmbar, 0, &s_abort) && tid == 0) set_err(A.err, DFLASH_DEV_TIMEOUT);
+  cluster_arrive();  // this CTA's rows have landed
   const float *rv = (const float *)pRecv;
   // weights of the splits of each owned row: w_q = e^(m_q - M) / sum_q e^(m_q - M) l_q
-  float *wts = (float *)(pRecv + kAttnRecvBytes);  // [per][nsplit]
+  float *wts = (float *)(pRecv + (size_t)A.nsplit * per * RS * 4);  // [per][nsplit]
   for (int lr = tid; lr < r1 - r0; lr += 128) {
     float M = -INFINITY;
     for (int q = 0; q < A.nsplit; ++q) M = fmaxf(M, rv[(q * per + lr) * RS]);
@@ -615,10 +674,11 @@ __global__ void __launch_bounds__(128)
   for (int e = tid; e < (r1 - r0) * DH; e += 128) {
     const int lr = e / DH, d = e % DH;
     float O = 0.f;
-    for (int q = 0; q < A.nsplit; ++q) O += wts[lr * A.nsplit + q] * rv[(q * per + lr) * RS + 2 + d];
+    for (int q = 0; q < A.nsplit; ++q) O += wts[lr * A.nsplit + q] * rv[(q * per + lr) * RS + 4 + d];
     const int qrg = qgi * kQG + r0 + lr, i = qrg / grp, g = qrg % grp;
     A.ob[((size_t)(b * A.K + i) * A.Hq + kvh * grp + g) * DH + d] = __float2bfloat16_rn(O);
   }
+  cluster_wait();  // every CTA's rows have landed: no push is in flight into any of them
 }
 
 
@@ -700,25 +760,30 @@ static int launch_attn_dh(const AttnPlan &pl, const S *qb, const S *kb, const S 
   return DFLASH_OK;
 }
 
-template <int DH, int KP, bool TK>
+template <int DH, int KP, bool TK, int NST>
 static int launch_attn_fused(const AttnPlan &pl, const dfl::AttnArgs &a, int B,
                              const CUtensorMap &mk, const CUtensorMap &mv, cudaStream_t st) {
-  // Q and NST K and V tiles (1 KB of alignment slack); the key-part merge, the
-  // receive buffer and the combine weights reuse the tile buffers afterwards
-  static_assert(dfl::kAttnRecvBytes + (dfl::kQG + 16) * 16 * 4 <=
-                    2 * dfl::kAttnStages * dfl::kCH * DH * 2,
-                "receive buffer and combine weights in the tile buffers");
-  const size_t smem =
-      1024 + (size_t)(64 / KP) * DH * 2 + 2 * (size_t)dfl::kAttnStages * dfl::kCH * DH * 2;
-  static int attr_done = 0;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP, TK>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP, TK>,
+  // Q, NST K and V tiles (1 KB of alignment slack; the key-part merge reuses
+  // the tile buffers), then, with several splits, the receive buffer
+  // [nsplit][per][DH + 4] and the combine weights [per][nsplit]
+  const int QR = a.K * (a.Hq / a.Hkv);
+  const size_t per = (std::min(dfl::kQG, QR) + pl.nsplit - 1) / pl.nsplit;
+  const size_t recv = pl.nsplit > 1 ? pl.nsplit * per * (DH + 4) * 4 + pl.nsplit * per * 4 : 0;
+  const size_t smem = 1024 + (size_t)(64 / KP) * DH * 2 + 2 * (size_t)NST * dfl::kCH * DH * 2 +
+                      ((recv + 15) & ~(size_t)15);
+  static size_t attr_smem = 0;
+  static int attr_cluster = 0;
+  if (smem > attr_smem) {
+    if (cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP, TK, NST>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_smem = smem;
+  }
+  if (!attr_cluster) {
+    if (cudaFuncSetAttribute(dfl::k_attn_mma<DH, KP, TK, NST>,
                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return DFLASH_ERR_CUDA;
-    attr_done = 1;
+    attr_cluster = 1;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.nsplit, a.Hkv, B * pl.nqg);
@@ -735,7 +800,7 @@ static int launch_attn_fused(const AttnPlan &pl, const dfl::AttnArgs &a, int B,
   cfg.attrs = attr;
   cfg.numAttrs = pdl_enabled() ? 2 : 1;
   count_launch();
-  DFL_CHECK_LAUNCH(cudaLaunchKernelEx(&cfg, dfl::k_attn_mma<DH, KP, TK>, a, mk, mv));
+  DFL_CHECK_LAUNCH(cudaLaunchKernelEx(&cfg, dfl::k_attn_mma<DH, KP, TK, NST>, a, mk, mv));
   return DFLASH_OK;
 }
 
@@ -777,9 +842,12 @@ int launch_attention_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl:
                   bf16_map(&mv, vc, rows, dh, 64, d->id);
   const int QR = K * (Hq / Hkv);
   const int kp = QR <= 16 ? 4 : QR <= 32 ? 2 : 1;
+  // split launches (a cluster per item, a few tiles per CTA, plus the receive
+  // buffer) keep two tile stages so that two CTAs fit on an SM
 #define DFL_ATTN(D, KPV)                                                                   \
-  return tk ? launch_attn_fused<D, KPV, true>(pl, a, B, mk, mv, st)                        \
-            : launch_attn_fused<D, KPV, false>(pl, a, B, mk, mv, st)
+  return tk ? (pl.nsplit > 1 ? launch_attn_fused<D, KPV, true, 2>(pl, a, B, mk, mv, st)    \
+                             : launch_attn_fused<D, KPV, true, 3>(pl, a, B, mk, mv, st))   \
+            : launch_attn_fused<D, KPV, false, dfl::kAttnStages>(pl, a, B, mk, mv, st)
   if (dh == 128) {
     if (kp == 4) DFL_ATTN(128, 4);
     if (kp == 2) DFL_ATTN(128, 2);

@@ -45,7 +45,10 @@ __global__ void __launch_bounds__(512) k_embed_norm(const S *__restrict__ E,
                                                     const dflh::RopeTable rope, int half,
                                                     float2 *__restrict__ rope_cs) {
   __shared__ float red[32];
-  pdl_launch();
+  // The first kernel of a draft pass releases its dependents only when it
+  // completes (no early trigger): every later kernel of the pass therefore
+  // starts after all work queued before the pass (the injection of context
+  // K/V above all) has completed, and may read the caches before its own wait.
   pdl_wait();
   const int r = blockIdx.x, b = r / K, i = r % K;
   rope_row(rope_cs + (size_t)r * half, ctx_len[b] + i, rope, half);
