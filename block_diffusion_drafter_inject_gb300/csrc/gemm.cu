@@ -463,7 +463,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           epi_store(p, m_tile, row, tcol0 + c, v, gx, gs, eg);
         }
       } else {
-        // slice -> scratch slot (tile, slice) ([column][row] inside), then a ticket
+        // slice -> scratch slot (tile, slice) ([column][row] inside: every
+        // store of a warp writes 128 consecutive bytes), then a ticket
         const size_t tile = (size_t)t_tile * p.m_tiles + m_tile;
         const size_t tile_sz = (size_t)BM * BN;
         float *mine = p.out + (tile * p.nmax + split) * tile_sz + row;
@@ -479,18 +480,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
-        __threadfence();
+        // the ticket: the barrier orders every epilogue thread's slice stores
+        // before one thread's acquire-release atomic (cumulative at GPU scope);
+        // in the last CTA the second barrier orders the slice loads after it
         epi_all_bar();
         if (threadIdx.x == 64) {
-          const int old = atomicAdd(&p.counters[tile], 1);
+          const int old = atomic_add_acq_rel_gpu(&p.counters[tile], 1);
           s_last = old == sg.nseg - 1;
           if (s_last) p.counters[tile] = 0;
         }
         epi_all_bar();
         if (s_last) {
-          __threadfence();
-          // sum the slices in slice order, CPI of the group's chunks per pass so
-          // that the loads of several chunks and slices are in flight together
+          // sum the slices in slice order, CPI of the group's chunks per pass and
+          // QU slices per round, so that their loads are in flight together
           constexpr int CPI = BN >= 128 ? 4 : BN >= 64 ? 2 : 1;
           const float *base = p.out + tile * p.nmax * tile_sz + row;
 #pragma unroll 1
@@ -501,7 +503,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int k = 0; k < CPI; ++k)
 #pragma unroll
               for (int j = 0; j < 16; ++j) v[k][j] = 0.f;
-#pragma unroll 2
+#pragma unroll(CPI == 1 ? 4 : 2)
             for (int q = 0; q < sg.nseg; ++q) {
 #pragma unroll
               for (int k = 0; k < CPI; ++k) {
