@@ -54,16 +54,18 @@ def weight_bytes(cfg):
 
 def pass_bytes(cfg, B, K, ctx):
     """Algorithmic bytes of one draft pass (draft_block + select_path): every weight
-    the pass multiplies by, once; the window's context K/V; embedding rows gathered."""
+    the pass multiplies by, once; the window's context K/V; the block's embedding
+    rows; the selector's table rows (both projections) of the anchor and the
+    candidates."""
     wb = weight_bytes(cfg)
     es = 2
-    D, k = cfg["d_model"], cfg["top_k"]
-    w = sum(v for n, v in wb.items() if n not in ("fc", "fc_norm", "embed"))
+    D, k, r = cfg["d_model"], cfg["top_k"], cfg["sel_rank"]
+    w = sum(v for n, v in wb.items() if n not in ("fc", "fc_norm", "embed", "sel_pu", "sel_pv"))
     kv = 0
     per_tok = cfg["n_layers"] * 2 * cfg["n_kv_heads"] * cfg["head_dim"] * es
     for c in ctx:
         kv += min(cfg["window"], int(c)) * per_tok
-    gathers = B * (K + 1 + (K - 1) * k) * D * es
+    gathers = B * K * D * es + B * (1 + (K - 1) * k) * 2 * r * 4
     return w + kv + gathers
 
 
@@ -243,6 +245,11 @@ def run_gpu(args, rank, world, barrier, allmax):
     t0 = time.time()
     Wh = synth.make_weights(cfg, seed=0)
     Wd = dfl.DeviceWeights.from_host(cfg, Wh, "cuda")
+    # the selector's projections of every vocabulary row, formed once per weight set
+    tab_ws = dfl.Workspace(cfg, 1, 2, 1)
+    dfl.prepare_selector(cfg, Wd, tab_ws)
+    torch.cuda.synchronize()
+    del tab_ws
     setup_s = time.time() - t0
 
     # ---------------- headline: B=1, K=8, ctx 2048

@@ -22,6 +22,7 @@ from .api import (  # noqa: F401
     linear,
     linear_splits,
     make_config,
+    prepare_selector,
     read_device_status,
     select_path,
     workspace_bytes,

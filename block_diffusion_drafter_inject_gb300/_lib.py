@@ -40,7 +40,8 @@ class LayerWeights(ctypes.Structure):
 
 class Weights(ctypes.Structure):
     _fields_ = [("fc_norm", vp), ("fc", vp), ("embed", vp), ("lm_head", vp), ("final_norm", vp),
-                ("sel_pu", vp), ("sel_pv", vp), ("layer", LayerWeights * MAX_LAYERS)]
+                ("sel_pu", vp), ("sel_pv", vp), ("layer", LayerWeights * MAX_LAYERS),
+                ("sel_table", vp)]
 
 
 class KV(ctypes.Structure):
@@ -58,6 +59,8 @@ EXPORTS = {
                                           ctypes.c_size_t, vp]),
     "dflash_select_path": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, vp,
                                           vp, i32, i32, vp, vp, vp, ctypes.c_size_t, vp]),
+    "dflash_prepare_selector": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(Weights),
+                                               vp, vp, ctypes.c_size_t, vp]),
     "dflash_accept_greedy": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                             ctypes.c_size_t, vp]),
     "dflash_accept_greedy_noalloc": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp]),

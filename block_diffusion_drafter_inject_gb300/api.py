@@ -57,6 +57,7 @@ class DeviceWeights:
                 L.conv_w[i] = tensors[p + f"conv_w.{i}"].data_ptr()
                 L.conv_base[i] = tensors[p + f"conv_base.{i}"].data_ptr()
         self.struct = w
+        self.sel_table = None  # see prepare_selector
 
     @classmethod
     def from_host(cls, cfg, host, device="cuda"):
@@ -132,6 +133,21 @@ def select_path(cfg, W, anchor, topk_ids, topk_logp, K, ws, path, score, stream=
                                    _ptr(topk_ids), _ptr(topk_logp), int(anchor.shape[0]), int(K),
                                    _ptr(path), _ptr(score), ws.ptr, ws.nbytes, _stream(stream)),
           "dflash_select_path")
+
+
+def prepare_selector(cfg, W, ws, stream=None):
+    """Forms both selector projections of every vocabulary row once
+    (dflash_prepare_selector) and points W's weights struct at them, so that
+    select_path reads candidate rows from the table instead of projecting them."""
+    c = make_config(cfg)
+    table = torch.empty((2, cfg["vocab"], cfg["sel_rank"]), dtype=torch.float32,
+                        device=W.t["embed"].device)
+    check(lib().dflash_prepare_selector(ctypes.byref(c), ctypes.byref(W.struct), _ptr(table),
+                                        ws.ptr, ws.nbytes, _stream(stream)),
+          "dflash_prepare_selector")
+    W.sel_table = table
+    W.struct.sel_table = table.data_ptr()
+    return table
 
 
 def accept_greedy(path, target_logits, ws, accept_len, tokens, stream=None):

@@ -444,6 +444,12 @@ static int run_select(const dflash_config &c, const dflash_weights &w, const int
   int *err = (int *)(ws + L.status);
   S *rows = (S *)(ws + L.selrows);
   float *U = (float *)(ws + L.U), *Vp = (float *)(ws + L.Vp);
+  if (w.sel_table) {  // the projections of every vocabulary row, formed ahead
+    TRY(launch_viterbi(U, Vp, ids, logp, B, K, k, r, (float *)(ws + L.pairs),
+                       (int *)(ws + L.topk_tickets), path, score, w.sel_table, c.vocab, anchor,
+                       err, st));
+    return DFLASH_OK;
+  }
   TRY(launch_sel_gather<S>((const S *)w.embed, anchor, ids, B, K, k, c.vocab, D, rows, err, st));
   if (c.dtype == DFLASH_BF16 && r % 128 == 0) {
     // both projections in one grouped launch (Vp follows U in the workspace)
@@ -462,7 +468,8 @@ static int run_select(const dflash_config &c, const dflash_weights &w, const int
                  st));
   }
   TRY(launch_viterbi(U, Vp, ids, logp, B, K, k, r, (float *)(ws + L.pairs),
-                     (int *)(ws + L.topk_tickets), path, score, st));
+                     (int *)(ws + L.topk_tickets), path, score, nullptr, c.vocab, anchor, err,
+                     st));
   return DFLASH_OK;
 }
 
@@ -539,8 +546,11 @@ int dflash_select_path(const dflash_config *cfg, const dflash_weights *w, const 
   if ((size_t)B > kTopkTicketInts) return DFLASH_ERR_DIMS;
   if (!w || !anchor || !topk_ids || !topk_logp || !path || !path_score || !ws)
     return DFLASH_ERR_NULL;
-  if (!w->embed || !w->sel_pu || !w->sel_pv) return DFLASH_ERR_NULL;
-  if (!a16(w->sel_pu) || !a16(w->sel_pv) || !a16(w->embed) || !a16(ws)) return DFLASH_ERR_ALIGN;
+  if (!w->sel_table && (!w->embed || !w->sel_pu || !w->sel_pv)) return DFLASH_ERR_NULL;
+  if (w->sel_table ? !a16(w->sel_table)
+                   : (!a16(w->sel_pu) || !a16(w->sel_pv) || !a16(w->embed)))
+    return DFLASH_ERR_ALIGN;
+  if (!a16(ws)) return DFLASH_ERR_ALIGN;
   Layout L;
   make_layout(cfg, B, K, 0, &L);
   if (ws_bytes < L.total) return DFLASH_ERR_WORKSPACE;
@@ -551,6 +561,26 @@ int dflash_select_path(const dflash_config *cfg, const dflash_weights *w, const 
                                  (uint8_t *)ws, L, st);
   return run_select<float>(*cfg, *w, anchor, topk_ids, topk_logp, B, K, path, path_score,
                            (uint8_t *)ws, L, st);
+}
+
+int dflash_prepare_selector(const dflash_config *cfg, const dflash_weights *w, float *table,
+                            void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_cfg(cfg);
+  if (rc != DFLASH_OK) return rc;
+  if (!w || !table || !ws || !w->embed || !w->sel_pu || !w->sel_pv) return DFLASH_ERR_NULL;
+  if (!a16(table) || !a16(w->embed) || !a16(w->sel_pu) || !a16(w->sel_pv) || !a16(ws))
+    return DFLASH_ERR_ALIGN;
+  Layout L;
+  make_layout(cfg, 1, 2, 0, &L);
+  if (ws_bytes < L.status + 256) return DFLASH_ERR_WORKSPACE;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int V = cfg->vocab, D = cfg->d_model, r = cfg->sel_rank;
+  int *err = (int *)((uint8_t *)ws + L.status);
+  // one K slice each: the projections land directly in the table rows
+  TRY(gemm_xwT(cfg->dtype, w->sel_pu, r, D, w->embed, V, table, r, 1, err, st));
+  TRY(gemm_xwT(cfg->dtype, w->sel_pv, r, D, w->embed, V, table + (size_t)V * r, r, 1, err, st));
+  return DFLASH_OK;
 }
 
 int dflash_accept_greedy(const int32_t *path, const void *target_logits, int32_t logits_dtype,

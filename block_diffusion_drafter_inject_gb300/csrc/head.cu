@@ -379,7 +379,9 @@ __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
                                                    const int32_t *__restrict__ topk_ids,
                                                    const float *__restrict__ topk_logp,
                                                    int32_t *__restrict__ path,
-                                                   float *__restrict__ score) {
+                                                   float *__restrict__ score,
+                                                   const float *__restrict__ tab, int V,
+                                                   const int32_t *__restrict__ anchor, int *err) {
   extern __shared__ float sm[];
   const int LDR = r + 1;  // odd row stride: the threads of a warp hit distinct banks
   float *su = sm, *sv = sm + (size_t)k * LDR;
@@ -396,8 +398,21 @@ __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
   const int r4 = r / 4;
   for (int e = threadIdx.x; e < (np + k) * r4; e += blockDim.x) {
     const int row = e / r4, c = e % r4;
-    const float4 q = row < np ? ((const float4 *)(U + (ubase + row) * r))[c]
-                              : ((const float4 *)(Vp + (vbase + row - np) * r))[c];
+    const float *src;
+    if (tab) {
+      // the rows' tokens: the anchor or position t-1's candidates (P_u side),
+      // position t's candidates (P_v side); their projections from the table
+      int tok = row < np ? (t == 0 ? anchor[b] : topk_ids[((size_t)b * (K - 1) + t - 1) * k + row])
+                         : topk_ids[((size_t)b * (K - 1) + t) * k + (row - np)];
+      if (tok < 0 || tok >= V) {
+        if (c == 0) set_err(err, DFLASH_DEV_TOKEN_RANGE);
+        tok = tok < 0 ? 0 : V - 1;
+      }
+      src = tab + ((row < np ? 0 : (size_t)V) + (size_t)tok) * r;
+    } else {
+      src = row < np ? U + (ubase + row) * r : Vp + (vbase + row - np) * r;
+    }
+    const float4 q = ((const float4 *)src)[c];
     float *dst = (row < np ? su + (size_t)row * LDR : sv + (size_t)(row - np) * LDR) + 4 * c;
     dst[0] = q.x, dst[1] = q.y, dst[2] = q.z, dst[3] = q.w;
   }
@@ -560,7 +575,8 @@ template int launch_sel_gather<dfl::bf16>(const dfl::bf16 *, const int32_t *, co
 
 int launch_viterbi(const float *U, const float *Vp, const int32_t *topk_ids,
                    const float *topk_logp, int B, int K, int k, int r, float *pair, int *tickets,
-                   int32_t *path, float *score, cudaStream_t st) {
+                   int32_t *path, float *score, const float *tab, int V, const int32_t *anchor,
+                   int *err, cudaStream_t st) {
   const size_t smem = sizeof(float) * std::max(2 * (size_t)k * (r + 1),
                                                (size_t)(K - 1) * k * k + (size_t)(K - 1) * k);
   if (smem > 48 * 1024) {
@@ -569,7 +585,7 @@ int launch_viterbi(const float *U, const float *Vp, const int32_t *topk_ids,
       return DFLASH_ERR_CUDA;
   }
   DFL_CHECK_LAUNCH(launch(dfl::k_sel_pairs, dim3(K - 1, B), dim3(256), smem, st, U, Vp, K, k, r,
-                          pair, tickets, topk_ids, topk_logp, path, score));
+                          pair, tickets, topk_ids, topk_logp, path, score, tab, V, anchor, err));
   return DFLASH_OK;
 }
 

@@ -18,11 +18,14 @@ int launch_sel_gather(const S *E, const int32_t *anchor, const int32_t *topk_ids
                       int k, int V, int D, S *rows, int *err, cudaStream_t st);
 
 // U, Vp: reduced selector projections [B*R, r] fp32 (R = 1 + (K-1)*k rows per
-// request: anchor, then candidates by (position, rank)); pair: B*(K-1)*k*k scratch;
-// tickets: B ints, zero on entry and on exit
+// request: anchor, then candidates by (position, rank)); or, with tab non-null,
+// the projections of every vocabulary row [2][V][r] fp32, read by token (the
+// anchor and the candidates; tokens out of range raise a status bit in err and
+// are clamped).  pair: B*(K-1)*k*k scratch; tickets: B ints, zero on entry and on exit
 int launch_viterbi(const float *U, const float *Vp, const int32_t *topk_ids,
                    const float *topk_logp, int B, int K, int k, int r, float *pair, int *tickets,
-                   int32_t *path, float *score, cudaStream_t st);
+                   int32_t *path, float *score, const float *tab, int V, const int32_t *anchor,
+                   int *err, cudaStream_t st);
 
 constexpr int kArgmaxChunk = 8192;
 inline int argmax_chunks(int V) { return (V + kArgmaxChunk - 1) / kArgmaxChunk; }

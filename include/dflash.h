@@ -121,6 +121,10 @@ typedef struct dflash_weights {
   const void *sel_pu;      /* [r, D] selector projection of the predecessor token     */
   const void *sel_pv;      /* [r, D] selector projection of the successor token       */
   dflash_layer_weights layer[DFLASH_MAX_LAYERS];
+  /* optional: f32 [2][V][r] = (P_u e_v, P_v e_v) for every vocabulary row v, as
+   * written by dflash_prepare_selector; NULL: dflash_select_path gathers the
+   * candidates' embedding rows and projects them on every call */
+  const float *sel_table;
 } dflash_weights;
 
 /* Paged per-layer draft KV cache.
@@ -191,6 +195,18 @@ int dflash_select_path(const dflash_config *cfg, const dflash_weights *w,
                        const float *topk_logp, int32_t B, int32_t K,
                        int32_t *path, float *path_score, void *ws, size_t ws_bytes,
                        void *stream);
+
+/* Selector tables (Architecture page, "Problem 1": the pair score
+ * (P_u e_a).(P_v e_b) is bilinear in fixed projections of vocabulary rows, so
+ * both projections of every row can be formed once per weight set):
+ *   table[0][v][:] = P_u e_v,   table[1][v][:] = P_v e_v    (f32 [2][V][r])
+ * from w->embed, w->sel_pu, w->sel_pv, on `stream`.  The caller owns `table`
+ * (2*V*r floats, 16-byte aligned; 311 MB for V = 151936, r = 256) and then
+ * sets w->sel_table = table, after which dflash_select_path reads the
+ * candidates' rows from it instead of projecting them.  ws: any workspace of
+ * dflash_workspace_bytes (only its status word is used). */
+int dflash_prepare_selector(const dflash_config *cfg, const dflash_weights *w, float *table,
+                            void *ws, size_t ws_bytes, void *stream);
 
 /* Greedy acceptance (Architecture page, "Speculative Decoding Context" and
  * "One Cycle, Step by Step"): row i of the target logits predicts the token

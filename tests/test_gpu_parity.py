@@ -161,3 +161,45 @@ def test_page_size_not_64():
     assert g["status"] == 0
     err = rowmax_rel(g["logits"], c.oracle()["logits"])
     assert err < TOL["bf16"], err
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_bf16", "small"])
+def test_selector_table_is_the_projection_of_every_row(name):
+    """dflash_prepare_selector: table[0][v] = P_u e_v and table[1][v] = P_v e_v,
+    against the fp64 products of the same stored values (the projections the
+    oracle's selector forms), on sampled vocabulary rows including the ends."""
+    import block_diffusion_drafter_inject_gb300 as dfl
+    c = Case(name, 1, 8, [64], seed=11).device()
+    tab = dfl.prepare_selector(c.cfg, c.Wd, c.cyc.ws)
+    torch.cuda.synchronize()
+    assert dfl.read_device_status(c.cyc.ws) == 0
+    tab = tab.cpu().numpy().astype(np.float64)
+    V = c.cfg["vocab"]
+    rows = np.unique(np.concatenate([[0, 1, V - 2, V - 1], np.random.default_rng(3).integers(0, V, 64)]))
+    E = c.W["embed"][rows].astype(np.float64)
+    for side, P in ((0, c.W["sel_pu"]), (1, c.W["sel_pv"])):
+        want = E @ P.astype(np.float64).T
+        err = np.abs(tab[side][rows] - want).max() / np.abs(want).max()
+        assert err < (1e-5 if c.cfg["dtype"] == "f32" else 1e-4), (side, err)
+
+
+@pytest.mark.parametrize("B,K", [(1, 8), (3, 8), (2, 16)])
+def test_select_path_with_table_on_oracle_candidates(B, K):
+    """The selector reading candidate rows from the prepared table: the same
+    paths as the oracle wherever its margin exceeds 1e-2, scores within 1e-3."""
+    import block_diffusion_drafter_inject_gb300 as dfl
+    c = Case("small", B, K, [60 + 17 * b for b in range(B)], seed=4 + B).device()
+    dfl.prepare_selector(c.cfg, c.Wd, c.cyc.ws)
+    o = c.oracle()
+    ids = torch.from_numpy(o["ids"]).cuda()
+    logp = torch.from_numpy(o["logp"].astype(np.float32)).cuda()
+    path = torch.zeros((B, K - 1), dtype=torch.int32, device="cuda")
+    score = torch.zeros((B,), dtype=torch.float32, device="cuda")
+    dfl.select_path(c.cfg, c.Wd, c.d_anchor, ids, logp, K, c.cyc.ws, path, score)
+    torch.cuda.synchronize()
+    assert dfl.read_device_status(c.cyc.ws) == 0
+    path, score = path.cpu().numpy(), score.cpu().numpy()
+    for b in range(B):
+        if o["margin"][b] > 1e-2:
+            assert list(path[b]) == list(o["path"][b]), b
+        assert abs(score[b] - o["score"][b]) < 1e-3 * max(1.0, abs(o["score"][b])), b
