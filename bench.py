@@ -89,7 +89,8 @@ def stored_traffic(n_launches):
 def pass_gemms(cfg, B, K):
     """(N_out, K_in, T, weight name) of every projection GEMM of one draft pass.
     At 16 block rows or fewer (bf16) the conv gate linears run inside the fused
-    conv kernels, not as GEMMs."""
+    conv kernels, not as GEMMs; the selector reads its prepared table (no
+    projection GEMMs per pass)."""
     D, F, V = cfg["d_model"], cfg["d_ff"], cfg["vocab"]
     Hq, Hkv, dh = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
     GW = 2 * D // cfg["conv_group"]
@@ -103,8 +104,6 @@ def pass_gemms(cfg, B, K):
                 g[2], (2 * F, D, T, p + "w_gate_up"), (D, F, T, p + "w_down"), g[3]]
     out = [x for x in out if x is not None]
     out.append((V, D, B * (K - 1), "lm_head"))
-    R = 1 + (K - 1) * cfg["top_k"]
-    out += [(cfg["sel_rank"], D, B * R, "sel_pu"), (cfg["sel_rank"], D, B * R, "sel_pv")]
     return out
 
 

@@ -244,16 +244,6 @@ __device__ __forceinline__ float ld_dsmem(uint32_t local_addr, uint32_t rank) {
   return v;
 }
 
-__device__ __forceinline__ void st_dsmem_v2(uint32_t local_addr, uint32_t rank, float a, float b) {
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(ra), "f"(a), "f"(b) : "memory");
-}
-__device__ __forceinline__ void st_dsmem(uint32_t local_addr, uint32_t rank, float a) {
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(a) : "memory");
-}
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
