@@ -215,8 +215,9 @@ __global__ void __launch_bounds__(128)
   __shared__ __align__(8) uint64_t cmbar;  // the peers' rows of this CTA have landed
   uint8_t *pQ = smem;
   uint8_t *pK0 = smem + QROWS * RB;
-  // receive buffer of the cluster combine, [nsplit][per][DH + 2] fp32 written by
-  // the peers, then the combine weights [per][nsplit]
+  // receive buffer of the cluster combine, [nsplit][per][DH + 4] fp32 rows (m, l,
+  // two floats of padding, o) copied in by the peers, then the combine weights
+  // [per][nsplit]
   uint8_t *pRecv = pK0 + 2 * NST * TILE;
   const uint32_t sQ = smem_u32(pQ), sK0 = smem_u32(pK0), sV0 = sK0 + NST * TILE;
   pdl_launch();
