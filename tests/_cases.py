@@ -198,12 +198,16 @@ class FullCase:
             self._o = res
         return self._o
 
-    def device(self, max_inject=4096):
+    def device(self, max_inject=4096, sel_table=False):
+        """Upload, inject the windows, run draft_block and select_path; with
+        sel_table, the selector reads the prepared table of every row's projections."""
         import torch
         import block_diffusion_drafter_inject_gb300 as dfl
         self.Wd = dfl.DeviceWeights.from_host(self.cfg, self.W, "cuda")
         self.kv = dfl.PagedKV(self.cfg, self.table, self.num_pages, "cuda")
         self.cyc = dfl.DraftCycle(self.cfg, self.Wd, self.kv, self.B, self.K, max_inject, "cuda")
+        if sel_table:
+            dfl.prepare_selector(self.cfg, self.Wd, self.cyc.ws)
         hid = torch.from_numpy(self.hidden).to(torch.bfloat16).cuda()
         req = torch.from_numpy(self.req).cuda()
         pos = torch.from_numpy(self.pos).cuda()

@@ -1,5 +1,6 @@
 """Parity at the full drafter size (width 4096, 5 layers, vocab 151936), in the
-launch configurations the benchmark uses: B=1 block 8 with 2048 context; B=1
+launch configurations the benchmark uses: B=1 block 8 with 2048 context (and
+with 2100, a window that starts mid-page, on the prepared selector table); B=1
 block 16 with 8192 context (target logits built from the oracle's path so every
 accepted length 1..16 occurs); B=32 ragged contexts in [512, 8192] on shuffled
 64-token pages (oracle on a subset of requests, which the pass treats
@@ -78,6 +79,16 @@ def _check_request(case, b, kv_rows=64):
 
 def test_full_b1_k8_ctx2048():
     case = FullCase(1, 8, [2048], seed=0).device()
+    assert case.status == 0
+    _check_request(case, 0)
+
+
+def test_full_b1_unaligned_window_with_selector_table():
+    """Context 2100: the window starts mid-page, so it spans 17 cache pages and
+    the last of the 16 key splits takes three tiles (two context pages and the
+    block) through the split launch's two-stage ring; the selector reads the
+    prepared table of all 151936 rows' projections."""
+    case = FullCase(1, 8, [2100], seed=7).device(sel_table=True)
     assert case.status == 0
     _check_request(case, 0)
 
