@@ -285,7 +285,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 // the same with acquire at cluster scope: for data that other CTAs of the
-// cluster delivered with st.async
+// cluster delivered with bulk copies counted on this mbarrier
 __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

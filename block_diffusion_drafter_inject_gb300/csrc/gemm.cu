@@ -492,7 +492,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         epi_all_bar();
         if (s_last) {
           // sum the slices in slice order, CPI of the group's chunks per pass and
-          // QU slices per round, so that their loads are in flight together
+          // four slices (two for wider tiles) per round, so that their loads
+          // are in flight together
           constexpr int CPI = BN >= 128 ? 4 : BN >= 64 ? 2 : 1;
           const float *base = p.out + tile * p.nmax * tile_sz + row;
 #pragma unroll 1
