@@ -183,7 +183,8 @@ int dflash_draft_block(const dflash_config *cfg, const dflash_weights *w,
 
 /* Candidate-path selector (Architecture page, "Problem 1", eq. S_t, in the
  * low-rank form (P_u e_a).(P_v e_b) with e = embedding rows, walked by
- * max-sum Viterbi from the anchor):
+ * max-sum Viterbi from the anchor; the projections are read from
+ * w->sel_table when it is set, else formed from the gathered rows):
  *   delta_1(j) = logp_1(j) + u(anchor).v(c_1j)
  *   delta_t(j) = logp_t(j) + max_i [delta_{t-1}(i) + u(c_{t-1,i}).v(c_tj)]
  * Ties go to the lower candidate rank.  B <= 16384 (else DFLASH_ERR_DIMS).
