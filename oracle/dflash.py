@@ -394,7 +394,9 @@ def accept_greedy_request(path, T):
     bonus token); at temperature 0 the output equals the target's own greedy
     output (Model-card summary, "The idea").  Row i of T is the target's
     prediction for the token after block slot i; the draft token of slot i+1
-    is accepted while it equals that row's argmax (lower id on ties).
+    is accepted while it equals that row's argmax (lower id on ties; a NaN
+    counts as larger than every number, so a row's first NaN is its argmax,
+    which is numpy's argmax rule).
 
     Returns (accept_len in 1..K, tokens [K] with -1 after the bonus token)."""
     T = np.asarray(T)

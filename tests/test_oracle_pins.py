@@ -393,3 +393,47 @@ def test_draft_contract_rounding_stays_close():
     b = oracle.draft_block_request(cfg, W, ck, cv, 5, 40, 8, "bf16")["logits"]
     rel = np.max(np.abs(a - b), axis=1) / np.max(np.abs(a), axis=1)
     assert rel.max() < 2e-2 and rel.max() > 0
+
+
+# ---------------------------------------------------------------- one drafter layer, by hand
+
+def _sig(z):
+    return 1.0 / (1.0 + math.exp(-z))
+
+
+def _hand_layer_case(fx, case):
+    cfg = dict(fx["common"]["cfg"])
+    W = {k: np.array(v, dtype=np.float64) for k, v in fx["common"]["weights"].items()}
+    W.update({k: np.array(v, dtype=np.float64) for k, v in case["weights"].items()})
+    n = case.get("ctx_len", 0)
+    shape = (n, cfg["n_kv_heads"], cfg["head_dim"])
+    ck = [np.array(case["ctx_k"], dtype=np.float64).reshape(shape) if n else np.zeros(shape)]
+    cv = [np.array(case["ctx_v"], dtype=np.float64).reshape(shape) if n else np.zeros(shape)]
+    return cfg, W, ck, cv, n
+
+
+def test_draft_layer_hand_fixtures():
+    """One drafter layer on hand-worked 2-wide cases (tests/golden/draft_layer_hand.json):
+    SwiGLU takes the gate rows first and applies SiLU to them, the post-sublayer conv
+    sits inside the residual branch with its gate map reading the sublayer output,
+    and the pre-sublayer conv follows the RMSNorm."""
+    fx = json.load(open(os.path.join(GOLD, "draft_layer_hand.json")))
+    K, anchor = fx["common"]["K"], fx["common"]["anchor"]
+    for case in fx["cases"]:
+        cfg, W, ck, cv, n = _hand_layer_case(fx, case)
+        out = oracle.draft_block_request(cfg, W, ck, cv, anchor, n, K, contract="none")
+        want = np.array([[float(eval(e, {"s": _sig})) for e in row]
+                         for row in case["expected_hidden"]])
+        np.testing.assert_allclose(out["hidden"], want, rtol=1e-9, atol=1e-12,
+                                   err_msg=case["name"])
+
+
+def test_accept_argmax_orders_nan_above_numbers():
+    # numpy's argmax rule: the first NaN of a row is its argmax
+    nan = float("nan")
+    T = np.array([[1.0, nan, 5.0, nan], [0.0, 2.0, 2.0, -1.0], [nan, nan, nan, nan]])
+    assert [int(np.argmax(r)) for r in T] == [1, 1, 0]
+    n, toks = oracle.accept_greedy_request(np.array([1, 1]), T)
+    assert (n, list(toks)) == (3, [1, 1, 0])
+    n, toks = oracle.accept_greedy_request(np.array([2, 1]), T)
+    assert (n, list(toks)) == (1, [1, -1, -1])
