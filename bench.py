@@ -13,7 +13,8 @@ dominant kernel (the tcgen05 projection GEMM) over the pass's GEMM shapes;
 an end-to-end figure through the C ABI with host buffers; and the CPU oracle
 timed on a bounded sample of the same workload.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-b32]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--only b1,b32,inject] [--no-b32] [--no-inject] [--no-cpu-baseline]
 """
 
 import argparse
@@ -22,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -129,9 +131,13 @@ def window_layout(ctx, K, P, W, seed):
 # ------------------------------------------------------------------ clocks
 
 class Clocks:
-    def __init__(self, path):
-        self.path = path
+    """nvidia-smi clock and throttle-reason samples (every 200 ms) while the
+    block runs, kept in a temporary file that is removed afterwards."""
+
+    def __init__(self):
         self.proc = None
+        fd, self.path = tempfile.mkstemp(prefix="dflash_clocks_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
         try:
@@ -147,7 +153,14 @@ class Clocks:
         return self
 
     def __exit__(self, *a):
-        if self.proc:
+        self._stop()
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+
+    def _stop(self):
+        if self.proc and self.proc.poll() is None:
             self.proc.terminate()
             try:
                 self.proc.wait(5)
@@ -156,8 +169,10 @@ class Clocks:
             self.f.close()
 
     def summary(self, gpu_index):
+        """Median SM clock, max clock and throttle reasons seen so far (stops sampling)."""
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self._stop()
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
@@ -249,9 +264,19 @@ def run_gpu(args, rank, world, barrier, allmax):
     dfl.prepare_selector(cfg, Wd, tab_ws)
     torch.cuda.synchronize()
     del tab_ws
-    setup_s = time.time() - t0
+    res = {"gpu": torch.cuda.get_device_name(dev), "setup_s": round(time.time() - t0, 1)}
+    sections = args.sections
+    if "b1" in sections:
+        res.update(bench_b1(torch, dfl, cfg, Wd, pk, args, world, barrier, allmax, dev))
+    if "b32" in sections:
+        res["b32"] = bench_b32(torch, dfl, cfg, Wd, pk, args)
+    if "inject" in sections:
+        res["inject"] = bench_inject(torch, dfl, cfg, Wd, pk, args)
+    return res, Wh
 
-    # ---------------- headline: B=1, K=8, ctx 2048
+
+def bench_b1(torch, dfl, cfg, Wd, pk, args, world, barrier, allmax, dev):
+    """The headline: one draft cycle at B=1, K=8, context 2048 (one CUDA graph)."""
     B, K, ctx = 1, 8, [2048]
     kv, cyc, inp = setup_workload(torch, dfl, cfg, Wd, B, K, ctx, 0, 1024)
 
@@ -272,13 +297,13 @@ def run_gpu(args, rank, world, barrier, allmax):
     g_cycle = capture(torch, cycle)
     g_pass = capture(torch, dpass)
 
-    gpu_name = torch.cuda.get_device_name(dev)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    with Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")) as clk:
+    with Clocks() as clk:
         ms_cycle = event_time(torch, g_cycle.replay, args.steps, args.warmup, barrier)
+        torch.cuda.nvtx.range_push("b1_pass")  # lets a profiler select these launches
         ms_pass = event_time(torch, g_pass.replay, args.steps, args.warmup)
+        torch.cuda.nvtx.range_pop()
+        clocks = clk.summary(dev)
     ms_cycle = allmax(ms_cycle)
-    clocks = clk.summary(dev)
 
     # ---------------- dominant kernel: the projection GEMM at the pass's shapes
     gem = pass_gemms(cfg, B, K)
@@ -322,7 +347,7 @@ def run_gpu(args, rank, world, barrier, allmax):
     ms_e2e = allmax(event_time(torch, e2e_step, args.steps, args.warmup, barrier))
 
     pb1 = pass_bytes(cfg, B, K, ctx)
-    res = {
+    return {
         "metric": METRIC, "value": whole_job_value(world, ms_cycle), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_cycle,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -344,42 +369,100 @@ def run_gpu(args, rank, world, barrier, allmax):
         "gpu_launches": launches_per_cycle * args.steps,
         "launches_per_cycle": launches_per_cycle,
         "clocks": clocks,
-        "gpu": gpu_name,
         "device_status": status,
-        "setup_s": round(setup_s, 1),
     }
 
-    # ---------------- B=32 draft pass (ragged contexts, paged)
-    if not args.no_b32:
-        del g_cycle, g_pass, g_gemm
-        B2 = 32
-        ctx2 = synth.make_ctx_lens(B2, 512, 8192, seed=1).tolist()
-        kv2, cyc2, inp2 = setup_workload(torch, dfl, cfg, Wd, B2, K, ctx2, 1, 4096)
 
-        def dpass2():
-            dfl.draft_block(cfg, Wd, kv2, inp2["anchor"], inp2["ctx"], K, cyc2.ws, cyc2.topk_ids,
-                            cyc2.topk_logp)
-            dfl.select_path(cfg, Wd, inp2["anchor"], cyc2.topk_ids, cyc2.topk_logp, K, cyc2.ws,
-                            cyc2.path, cyc2.score)
+def bench_b32(torch, dfl, cfg, Wd, pk, args):
+    """The draft pass and cycle at B=32 (ragged contexts in [512, 8192], paged)."""
+    B2, K = 32, 8
+    ctx2 = synth.make_ctx_lens(B2, 512, 8192, seed=1).tolist()
+    kv2, cyc2, inp2 = setup_workload(torch, dfl, cfg, Wd, B2, K, ctx2, 1, 4096)
 
-        def cycle2():
-            cyc2.run(inp2["hidden"], inp2["req"], inp2["pos"], inp2["anchor"], inp2["ctx"],
-                     inp2["target"])
+    def dpass2():
+        dfl.draft_block(cfg, Wd, kv2, inp2["anchor"], inp2["ctx"], K, cyc2.ws, cyc2.topk_ids,
+                        cyc2.topk_logp)
+        dfl.select_path(cfg, Wd, inp2["anchor"], cyc2.topk_ids, cyc2.topk_logp, K, cyc2.ws,
+                        cyc2.path, cyc2.score)
 
-        gp2 = capture(torch, dpass2)
-        gc2 = capture(torch, cycle2)
-        ms_p2 = event_time(torch, gp2.replay, max(5, args.steps // 2), args.warmup)
-        ms_c2 = event_time(torch, gc2.replay, max(5, args.steps // 2), args.warmup)
-        pb2 = pass_bytes(cfg, B2, K, ctx2)
-        fl2 = sum(2.0 * N * Kin * T for (N, Kin, T, _) in pass_gemms(cfg, B2, K))
-        t_hbm = pb2 / (pk["hbm"] * 1e9)
-        t_tc = fl2 / (pk["bf16_sus"] * 1e12)
-        res["b32"] = {"draft_pass_us": ms_p2 * 1e3, "cycle_us": ms_c2 * 1e3,
-                      "cycles_per_s": 1e3 / ms_c2, "pass_bytes": pb2, "pass_gemm_flops": fl2,
-                      "hbm_floor_us": t_hbm * 1e6, "tensor_floor_us": t_tc * 1e6,
-                      "frac_of_tighter_roofline": max(t_hbm, t_tc) / (ms_p2 * 1e-3),
-                      "ctx_range": [min(ctx2), max(ctx2)]}
-    return res, Wh
+    def cycle2():
+        cyc2.run(inp2["hidden"], inp2["req"], inp2["pos"], inp2["anchor"], inp2["ctx"],
+                 inp2["target"])
+
+    gp2 = capture(torch, dpass2)
+    gc2 = capture(torch, cycle2)
+    torch.cuda.nvtx.range_push("b32_pass")  # lets a profiler select these launches
+    ms_p2 = event_time(torch, gp2.replay, max(5, args.steps // 2), args.warmup)
+    torch.cuda.nvtx.range_pop()
+    ms_c2 = event_time(torch, gc2.replay, max(5, args.steps // 2), args.warmup)
+    status = dfl.read_device_status(cyc2.ws)
+    pb2 = pass_bytes(cfg, B2, K, ctx2)
+    fl2 = sum(2.0 * N * Kin * T for (N, Kin, T, _) in pass_gemms(cfg, B2, K))
+    t_hbm = pb2 / (pk["hbm"] * 1e9)
+    t_tc = fl2 / (pk["bf16_sus"] * 1e12)
+    return {"draft_pass_us": ms_p2 * 1e3, "cycle_us": ms_c2 * 1e3,
+            "cycles_per_s": 1e3 / ms_c2, "pass_bytes": pb2, "pass_gemm_flops": fl2,
+            "hbm_floor_us": t_hbm * 1e6, "tensor_floor_us": t_tc * 1e6,
+            "frac_of_tighter_roofline": max(t_hbm, t_tc) / (ms_p2 * 1e-3),
+            "ctx_range": [min(ctx2), max(ctx2)], "device_status": status}
+
+
+def inject_flops(cfg, N):
+    """Multiply-add flops of injecting N target-hidden rows: the fc projection and
+    every layer's K and V projections."""
+    D, Hkv, dh = cfg["d_model"], cfg["n_kv_heads"], cfg["head_dim"]
+    TIN = cfg["n_taps"] * cfg["d_target"]
+    return 2.0 * N * (D * TIN + cfg["n_layers"] * 2 * Hkv * dh * D)
+
+
+def bench_inject(torch, dfl, cfg, Wd, pk, args):
+    """Context capture at scale: 8 requests each inject 4096 new target-hidden rows
+    (5 x 5120 bf16) into their paged draft KV in one call, then one block-16 draft
+    cycle runs for all 8 requests."""
+    B, K, n = 8, 16, 4096
+    N = B * n
+    P = cfg["page_size"]
+    TIN = cfg["n_taps"] * cfg["d_target"]
+    per = (n + K + P - 1) // P
+    table = np.arange(B * per, dtype=np.int32).reshape(B, per)
+    perm = synth.stream(5, "inject_page_perm").permutation(B * per).astype(np.int32)
+    table = perm[table]
+    kv = dfl.PagedKV(cfg, table, B * per, "cuda")
+    cyc = dfl.DraftCycle(cfg, Wd, kv, B, K, N, "cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    hid = torch.randn((N, TIN), device="cuda", generator=gen).to(torch.bfloat16)
+    req = torch.arange(B, dtype=torch.int32, device="cuda").repeat_interleave(n)
+    pos = torch.arange(n, dtype=torch.int32, device="cuda").repeat(B)
+    anchor = torch.from_numpy(synth.make_anchors(cfg, B, seed=5)).cuda()
+    ctx = torch.full((B,), n, dtype=torch.int32, device="cuda")
+    target = torch.from_numpy(synth.make_target_logits(cfg, B, K, seed=5)).cuda()
+
+    def inject():
+        dfl.inject_context(cfg, Wd, kv, hid, req, pos, cyc.ws)
+
+    def cycle():
+        cyc.run(None, None, None, anchor, ctx, target)
+
+    g_inj = capture(torch, inject)
+    g_cyc = capture(torch, cycle)
+    steps = max(3, min(args.steps, 20))
+    torch.cuda.nvtx.range_push("inject_32k")  # lets a profiler select these launches
+    ms_inj = event_time(torch, g_inj.replay, steps, args.warmup)
+    torch.cuda.nvtx.range_pop()
+    ms_cyc = event_time(torch, g_cyc.replay, max(5, args.steps // 2), args.warmup)
+    status = dfl.read_device_status(cyc.ws)
+    fl = inject_flops(cfg, N)
+    t_tc = fl / (pk["bf16_sus"] * 1e12)
+    cb = pass_bytes(cfg, B, K, [n] * B)
+    return {"workload": f"{B} requests x {n} injected rows ({cfg['n_taps']} x {cfg['d_target']} "
+                        f"bf16), then one block-{K} cycle for all {B}",
+            "rows": N, "inject_ms": ms_inj, "inject_tflops": fl / (ms_inj * 1e-3) / 1e12,
+            "inject_flops": fl, "tensor_floor_ms": t_tc * 1e3,
+            "frac_of_tensor_roofline": t_tc / (ms_inj * 1e-3), "peak_tflops": pk["bf16_sus"],
+            "peak_kind": "bf16 sustained (measured)",
+            "cycle_us": ms_cyc * 1e3, "cycle_pass_bytes": cb,
+            "cycle_hbm_frac": cb / (ms_cyc * 1e-3) / 1e9 / pk["hbm"], "device_status": status}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -494,19 +577,63 @@ def whole_job_value(world, ms_per_step_max):
 
 # ------------------------------------------------------------------ main
 
+def spawn_replicas(n, argv):
+    """Re-run this script under torch.distributed.run with n ranks on this node (one
+    replica per GPU) and return its exit status; rank 0 prints the JSON line."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node",
+           str(n), "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
+def replica_selftest(world, rank):
+    """CPU check of the replica plumbing (gloo): every rank joins, passes the
+    barrier and agrees on the max of the per-rank step times."""
+    barrier, allmax = replica_sync(world, device="cpu")
+    if barrier:
+        barrier()
+    worst = allmax(float(rank + 1))
+    if rank == 0:
+        print(json.dumps({"replica_selftest": True, "world": world, "max_step": worst,
+                          "value": whole_job_value(world, worst)}))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--only", default="",
+                    help="comma list of sections to run: b1 (headline), b32, inject")
     ap.add_argument("--no-b32", action="store_true")
+    ap.add_argument("--no-inject", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--replica-selftest", action="store_true",
+                    help="check the replica barrier / max on CPU (gloo) and exit")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    args.sections = set(x for x in args.only.split(",") if x) or {"b1", "b32", "inject"}
+    if args.no_b32:
+        args.sections.discard("b32")
+    if args.no_inject:
+        args.sections.discard("inject")
 
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(spawn_replicas(args.gpus, sys.argv[1:]))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+
+    if args.replica_selftest:
+        replica_selftest(world, rank)
+        return
 
     if args.impl == "reference":
         if rank == 0:
@@ -518,7 +645,7 @@ def main():
     barrier, allmax = replica_sync(world, device="cuda")
     res, Wh = run_gpu(args, rank, world, barrier, allmax)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and "b1" in args.sections:
             res["cpu_baseline"] = cpu_baseline(Wh, synth.preset("full"))
         print(json.dumps(res))
     if world > 1:

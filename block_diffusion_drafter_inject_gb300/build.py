@@ -36,16 +36,33 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def source_fingerprint():
-    """Hash of the kernel sources, headers and compile flags (machine-independent):
-    identifies the build a stored profile measurement belongs to."""
+def portable_flags(flags, root=ROOT):
+    """The compile flags with paths inside the checkout written relative to its
+    root, so that they do not depend on where the repository sits."""
+    out = []
+    for f in flags:
+        if os.path.isabs(f) and (f == root or f.startswith(root.rstrip(os.sep) + os.sep)):
+            f = os.path.relpath(f, root)
+        out.append(f)
+    return out
+
+
+def source_fingerprint(root=None):
+    """Hash of the kernel sources, headers and compile flags (independent of the
+    machine and of the checkout path): identifies the build a stored profile
+    measurement belongs to.  `root` reads the sources of another checkout."""
+    root = ROOT if root is None else root
+    csrc = os.path.join(root, os.path.relpath(CSRC, ROOT))
+    include = os.path.join(root, os.path.relpath(INCLUDE, ROOT))
+    flags = [os.path.join(root, os.path.relpath(f, ROOT)) if f in (CSRC, INCLUDE) else f
+             for f in FLAGS]
     h = hashlib.sha256()
-    for d in (CSRC, INCLUDE):
+    for d in (csrc, include):
         for f in sorted(os.listdir(d)):
             if f.endswith((".cu", ".cuh", ".h")):
                 h.update(f.encode())
                 h.update(open(os.path.join(d, f), "rb").read())
-    h.update(" ".join(ARCH + FLAGS).encode())
+    h.update(" ".join(ARCH + portable_flags(flags, root)).encode())
     return h.hexdigest()
 
 

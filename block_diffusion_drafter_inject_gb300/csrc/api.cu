@@ -345,6 +345,46 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
         reduce_call(c, ws, L, Wg, GW, D, X, T, L.P_gate, GEMM_REDUCE, gates, GW, nullptr, 0), st);
   };
 
+  // the projection GEMMs of the pass
+  const int TL = B * (K - 1);
+  // the lm_head's epilogue also writes each 128-entry vocab tile's (max, sum e^(z - max))
+  float2 *tstats = c.dtype == DFLASH_BF16 ? (float2 *)topkp : nullptr;
+  float2 *rope_cs = (float2 *)(ws + L.rope);
+  auto qkv_call = [&](int l) {
+    const dflash_layer_weights &lw = w.layer[l];
+    if (c.dtype != DFLASH_BF16)
+      return reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_REDUCE, qkv, QKVW,
+                         nullptr, 0);
+    // the projection's epilogue applies the q/k head norms and RoPE: bf16 q, k, v rows
+    GemmCall gq = reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_QKV, nullptr, 0,
+                              ws + L.qkv, QKVW);
+    gq.q_norm = lw.q_norm;
+    gq.k_norm = lw.k_norm;
+    gq.rope_cs = rope_cs;
+    gq.Hq = Hq;
+    gq.Hkv = Hkv;
+    gq.dh = dh;
+    gq.eps = eps;
+    return gq;
+  };
+  auto o_call = [&](int l) {
+    return reduce_call(c, ws, L, w.layer[l].wo, D, Hq * dh, ob, T, L.P_o, GEMM_REDUCE, rf, D, rb,
+                       D);
+  };
+  auto gu_call = [&](int l) {
+    return reduce_call(c, ws, L, w.layer[l].w_gate_up, F, D, ub, T, L.P_gu, GEMM_SWIGLU, nullptr,
+                       0, hb, F);
+  };
+  auto down_call = [&](int l) {
+    return reduce_call(c, ws, L, w.layer[l].w_down, D, F, hb, T, L.P_down, GEMM_REDUCE, rf, D, rb,
+                       D);
+  };
+  auto lm_call = [&]() {
+    GemmCall gl = reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, GemmPlan{0, 1}, GEMM_REDUCE,
+                              logits, V, nullptr, 0);
+    gl.stats = tstats;
+    return gl;
+  };
   // A few block rows: each conv is one launch with its gate linear fused (the
   // pre-norm formed inside).  More rows: the gate linear is a tensor-core GEMM
   // and the conv a row kernel.
@@ -375,7 +415,6 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
                                     (const S *)next_gain, eps, un, last ? zf : (S *)nullptr, st);
   };
 
-  float2 *rope_cs = (float2 *)(ws + L.rope);
   TRY(launch_embed_norm<S>((const S *)w.embed, anchor, c.mask_token_id, V, B, K, D,
                            (const S *)w.layer[0].attn_norm, eps, x, fused ? (S *)nullptr : un, err,
                            ctx_len, rope, dh / 2, rope_cs, st));
@@ -384,27 +423,13 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     const bool last = l + 1 == c.n_layers;
     // attention sublayer: conv -> QKV -> norm/RoPE -> block attention -> O -> conv, residual
     TRY(conv_pre(l, 0, lw.attn_norm));
+    TRY(gemm_run(qkv_call(l), st));
     if constexpr (sizeof(S) == 2) {
-      // the projection's epilogue applies the q/k head norms and RoPE: bf16 q, k, v rows
-      dfl::bf16 *qkvb = (dfl::bf16 *)(ws + L.qkv);
-      GemmCall gq = reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_QKV, nullptr, 0,
-                                qkvb, QKVW);
-      gq.q_norm = lw.q_norm;
-      gq.k_norm = lw.k_norm;
-      gq.rope_cs = rope_cs;
-      gq.Hq = Hq;
-      gq.Hkv = Hkv;
-      gq.dh = dh;
-      gq.eps = eps;
-      TRY(gemm_run(gq, st));
-      TRY(launch_attention_fused(L.ap, qkvb, (const dfl::bf16 *)kv.k, (const dfl::bf16 *)kv.v, l,
-                                 c.n_layers, kv.page_table, kv.max_pages_per_req, kv.num_pages,
-                                 c.page_size,
-                                 ctx_len, B, K, Hq, Hkv, dh, c.window, (dfl::bf16 *)ob, err, st));
+      TRY(launch_attention_fused(L.ap, (const dfl::bf16 *)(ws + L.qkv), (const dfl::bf16 *)kv.k,
+                                 (const dfl::bf16 *)kv.v, l, c.n_layers, kv.page_table,
+                                 kv.max_pages_per_req, kv.num_pages, c.page_size, ctx_len, B, K,
+                                 Hq, Hkv, dh, c.window, (dfl::bf16 *)ob, err, st));
     } else {
-      TRY(gemm_run(reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_REDUCE, qkv, QKVW,
-                               nullptr, 0),
-                   st));
       TRY(launch_qkv_post<S>(qkv, T, K, Hq, Hkv, dh, (const S *)lw.q_norm, (const S *)lw.k_norm,
                              rope_cs, eps, qb, kb, vb, st));
       TRY(launch_block_attention<S>(L.ap, qb, kb, vb, (const S *)kv.k, (const S *)kv.v, l,
@@ -412,25 +437,15 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
                                     c.page_size, ctx_len, B, K, Hq, Hkv, dh, c.window, attnp, ob,
                                     err, st));
     }
-    TRY(gemm_run(reduce_call(c, ws, L, lw.wo, D, Hq * dh, ob, T, L.P_o, GEMM_REDUCE, rf, D, rb, D),
-                 st));
+    TRY(gemm_run(o_call(l), st));
     TRY(conv_post(l, 1, lw.mlp_norm, false));
     // MLP sublayer: conv -> gate/up + SwiGLU -> down -> conv, residual
     TRY(conv_pre(l, 2, lw.mlp_norm));
-    TRY(gemm_run(reduce_call(c, ws, L, lw.w_gate_up, F, D, ub, T, L.P_gu, GEMM_SWIGLU, nullptr, 0,
-                             hb, F),
-                 st));
-    TRY(gemm_run(reduce_call(c, ws, L, lw.w_down, D, F, hb, T, L.P_down, GEMM_REDUCE, rf, D, rb, D),
-                 st));
+    TRY(gemm_run(gu_call(l), st));
+    TRY(gemm_run(down_call(l), st));
     TRY(conv_post(l, 3, last ? w.final_norm : w.layer[l + 1].attn_norm, last));
   }
-  const int TL = B * (K - 1);
-  // the lm_head's epilogue also writes each 128-entry vocab tile's (max, sum e^(z - max))
-  float2 *tstats = c.dtype == DFLASH_BF16 ? (float2 *)topkp : nullptr;
-  GemmCall gl = reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, GemmPlan{0, 1}, GEMM_REDUCE, logits,
-                            V, nullptr, 0);
-  gl.stats = tstats;
-  TRY(gemm_run(gl, st));
+  TRY(gemm_run(lm_call(), st));
   TRY(launch_topk(logits, tstats, TL, V, c.top_k, ids, logp, st));
   return DFLASH_OK;
 }

@@ -840,27 +840,9 @@ size_t gemm_scratch_floats(int N_out, int T, int S, int mode, int bn, int chunk,
   return slots * gemm_tiles(N_out, T, mode, bn) * dfl::BM * bn;
 }
 
-template <int BN>
-static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
-  using SH = dfl::GemmShape<BN>;
-  static int attr_set_dev[64] = {0};
-  if (d->id < 64 && !attr_set_dev[d->id]) {
-    if (cudaFuncSetAttribute(dfl::k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SH::SMEM_BYTES) != cudaSuccess)
-      return DFLASH_ERR_CUDA;
-    attr_set_dev[d->id] = 1;
-  }
+// Kernel parameters and grid of one launch with token tile BN.
+static int make_params(const GemmCall &g, int BN, int num_sms, dfl::GemmParams &p) {
   const bool swiglu = g.mode == GEMM_SWIGLU;
-  const int w_rows = swiglu ? 2 * g.N_out : g.N_out;
-  dfl::WMaps mw;
-  CUtensorMap mx;
-  memset(&mw, 0, sizeof(mw));
-  for (int gi = 0; gi < g.groups; ++gi)
-    if (!bf16_map(&mw.m[gi], gi == 0 ? g.W : g.Wg[gi], (uint64_t)w_rows, (uint64_t)g.K_in,
-                  swiglu ? 64 : dfl::BM, d->id))
-      return DFLASH_ERR_CUDA;
-  if (!bf16_map(&mx, g.X, (uint64_t)g.T, (uint64_t)g.K_in, BN, d->id)) return DFLASH_ERR_CUDA;
-  dfl::GemmParams p;
   p.out = g.out;
   p.ld = g.ld;
   p.N_out = g.N_out;
@@ -891,10 +873,10 @@ static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
   p.kb_total = g.K_in / dfl::BK;
   p.total = 0;
   p.nmax = g.S;
-  int grid = p.num_units < d->num_sms ? p.num_units : d->num_sms;
+  int grid = p.num_units < num_sms ? p.num_units : num_sms;
   if (g.chunk > 0) {
     const long total = (long)p.m_tiles * p.t_tiles * p.kb_total;
-    if (total >= (1L << 30)) return DFLASH_ERR_DIMS;
+    if (total >= (1L << 30)) return -1;
     p.chunk = g.chunk;
     p.total = (int)total;
     p.nmax = gemm_balanced_slots(g.K_in, g.chunk);
@@ -903,6 +885,32 @@ static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
     p.num_units = p.m_tiles * p.t_tiles;
     grid = (int)((total + g.chunk - 1) / g.chunk);
   }
+  return grid;
+}
+
+template <int BN>
+static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
+  using SH = dfl::GemmShape<BN>;
+  static int attr_set_dev[64] = {0};
+  if (d->id < 64 && !attr_set_dev[d->id]) {
+    if (cudaFuncSetAttribute(dfl::k_gemm_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SH::SMEM_BYTES) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_set_dev[d->id] = 1;
+  }
+  const bool swiglu = g.mode == GEMM_SWIGLU;
+  const int w_rows = swiglu ? 2 * g.N_out : g.N_out;
+  dfl::WMaps mw;
+  CUtensorMap mx;
+  memset(&mw, 0, sizeof(mw));
+  for (int gi = 0; gi < g.groups; ++gi)
+    if (!bf16_map(&mw.m[gi], gi == 0 ? g.W : g.Wg[gi], (uint64_t)w_rows, (uint64_t)g.K_in,
+                  swiglu ? 64 : dfl::BM, d->id))
+      return DFLASH_ERR_CUDA;
+  if (!bf16_map(&mx, g.X, (uint64_t)g.T, (uint64_t)g.K_in, BN, d->id)) return DFLASH_ERR_CUDA;
+  dfl::GemmParams p;
+  const int grid = make_params(g, BN, d->num_sms, p);
+  if (grid < 0) return DFLASH_ERR_DIMS;
   DFL_CHECK_LAUNCH(launch(dfl::k_gemm_tc<BN>, dim3(grid), dim3(dfl::kGemmThreads),
                           (size_t)SH::SMEM_BYTES, st, mw, mx, p));
   return DFLASH_OK;

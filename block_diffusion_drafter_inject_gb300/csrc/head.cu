@@ -17,25 +17,38 @@ struct VI {
 __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
   return v1 > v2 || (v1 == v2 && i1 < i2);
 }
+// The argmax of a target-logit row orders NaN above every number (the row's
+// first NaN wins, as numpy's argmax does), then by value, then by lower id.
+__device__ __forceinline__ bool better_nan_max(float v1, int i1, float v2, int i2) {
+  const bool n1 = v1 != v1, n2 = v2 != v2;
+  if (n1 || n2) return n1 && (!n2 || i1 < i2);
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+template <bool NAN_MAX = false>
+__device__ __forceinline__ bool pick(float v1, int i1, float v2, int i2) {
+  return NAN_MAX ? better_nan_max(v1, i1, v2, i2) : better(v1, i1, v2, i2);
+}
+template <bool NAN_MAX = false>
 __device__ __forceinline__ VI warp_best(VI a) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     float v = __shfl_xor_sync(0xffffffffu, a.v, o);
     int i = __shfl_xor_sync(0xffffffffu, a.i, o);
-    if (better(v, i, a.v, a.i)) a.v = v, a.i = i;
+    if (pick<NAN_MAX>(v, i, a.v, a.i)) a.v = v, a.i = i;
   }
   return a;
 }
 // best over the block; red: 2*32 words of shared scratch
+template <bool NAN_MAX = false>
 __device__ __forceinline__ VI block_best(VI a, float *redv, int *redi) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  a = warp_best(a);
+  a = warp_best<NAN_MAX>(a);
   __syncthreads();
   if (lane == 0) redv[wid] = a.v, redi[wid] = a.i;
   __syncthreads();
   VI b{-INFINITY, 0x7fffffff};
   if (lane < nw) b.v = redv[lane], b.i = redi[lane];
-  return warp_best(b);
+  return warp_best<NAN_MAX>(b);
 }
 
 // Descending bitonic sort of one value per lane across the warp; returns this
@@ -485,7 +498,8 @@ __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
   }
 }
 
-// argmax of one chunk of one target-logit row -> partial (value, id)
+// argmax of one chunk of one target-logit row -> partial (value, id); NaN ranks
+// above every number (better_nan_max)
 template <typename L>
 __global__ void __launch_bounds__(256) k_argmax_partial(const L *__restrict__ logits, int V,
                                                         float *__restrict__ partial) {
@@ -499,9 +513,9 @@ __global__ void __launch_bounds__(256) k_argmax_partial(const L *__restrict__ lo
   VI best{-INFINITY, 0x7fffffff};
   for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
     const float v = ldf(z + i);
-    if (better(v, i, best.v, best.i)) best.v = v, best.i = i;
+    if (better_nan_max(v, i, best.v, best.i)) best.v = v, best.i = i;
   }
-  best = block_best(best, redv, redi);
+  best = block_best<true>(best, redv, redi);
   if (threadIdx.x == 0) {
     partial[((size_t)row * nch + chunk) * 2] = best.v;
     partial[((size_t)row * nch + chunk) * 2 + 1] = __int_as_float(best.i);
@@ -523,9 +537,9 @@ __global__ void __launch_bounds__(1024) k_accept(const int32_t *__restrict__ pat
     for (int c = lane; c < nch; c += 32) {
       const float v = p[2 * c];
       const int id = __float_as_int(p[2 * c + 1]);
-      if (better(v, id, best.v, best.i)) best.v = v, best.i = id;
+      if (better_nan_max(v, id, best.v, best.i)) best.v = v, best.i = id;
     }
-    best = warp_best(best);
+    best = warp_best<true>(best);
     if (lane == 0) tgt[w] = best.i;
   }
   __syncthreads();

@@ -212,7 +212,8 @@ int dflash_prepare_selector(const dflash_config *cfg, const dflash_weights *w, f
 /* Greedy acceptance (Architecture page, "Speculative Decoding Context" and
  * "One Cycle, Step by Step"): row i of the target logits predicts the token
  * after slot i; draft token path[i] (slot i+1) is accepted while it equals
- * argmax(target_logits[b, i]) (lower id on ties).  With m accepted drafts,
+ * argmax(target_logits[b, i]) (lower id on ties; NaN counts as larger than
+ * every number, so a row's first NaN is its argmax).  With m accepted drafts,
  *   accept_len[b] = m + 1,  tokens[b] = path[0..m-1], argmax(row m), -1 ...
  *   path           device int32 [B, K-1]
  *   target_logits  device [B, K, V] f32 (logits_dtype DFLASH_F32) or bf16     */

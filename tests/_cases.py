@@ -56,6 +56,21 @@ class Case:
                            toks=toks, **d)
         return self._o
 
+    def oracle_pure_logits(self):
+        """The oracle's logits with no storage rounding anywhere (contract "none")."""
+        L = self.cfg["n_layers"]
+        ck, cv = [], []
+        o = 0
+        for b in range(self.B):
+            n = int(self.ctx[b])
+            k, v, _ = oracle.inject_context(self.cfg, self.W, self.hidden[o:o + n], np.arange(n),
+                                            "none")
+            ck.append([k[l] for l in range(L)])
+            cv.append([v[l] for l in range(L)])
+            o += n
+        return oracle.draft_block(self.cfg, self.W, ck, cv, self.anchor, self.ctx, self.K,
+                                  "none")["logits"]
+
     # ---------------------------------------------------------------- device
     def device(self):
         import torch
@@ -102,6 +117,22 @@ class Case:
             outk.append([k[l][pages, :, p % P, :] for l in range(self.cfg["n_layers"])])
             outv.append([v[l][pages, :, p % P, :] for l in range(self.cfg["n_layers"])])
         return outk, outv
+
+
+def exact_logits(cfg, W, hidden, pos, n_ctx, anchor, K):
+    """The oracle's logits of one request with no storage rounding anywhere
+    (contract "none"): its context rows `hidden` injected at positions `pos`."""
+    k, v, _ = oracle.inject_context(cfg, W, hidden, pos, "none")
+    shape = (n_ctx, cfg["n_kv_heads"], cfg["head_dim"])
+    ck, cv = [], []
+    for l in range(cfg["n_layers"]):
+        a = np.zeros(shape)
+        a[pos] = k[l]
+        ck.append(a)
+        a = np.zeros(shape)
+        a[pos] = v[l]
+        cv.append(a)
+    return oracle.draft_block(cfg, W, [ck], [cv], [anchor], [n_ctx], K, "none")["logits"][0]
 
 
 def rowmax_rel(g, o):
@@ -194,7 +225,9 @@ class FullCase:
                 p, s, m = oracle.select_path(cfg, self.W, self.anchor[b:b + 1], d["ids"], d["logp"],
                                              with_margin=True)
                 res[b] = dict(k=k, v=v, logits=d["logits"][0], ids=d["ids"][0], logp=d["logp"][0],
-                              path=p[0], score=s[0], margin=m[0])
+                              path=p[0], score=s[0], margin=m[0],
+                              logits_exact=exact_logits(cfg, self.W, self.hidden[sel],
+                                                        self.pos[sel], n_ctx, self.anchor[b], K))
             self._o = res
         return self._o
 

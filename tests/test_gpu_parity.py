@@ -2,14 +2,16 @@
 same seeded inputs.
 
 Tolerances (written here, derived from the storage contract): logits within
-2e-2 of the row maximum for bf16 storage, 1e-3 for the float32 configuration;
-top-k ids, selected paths and accepted lengths bit-exact wherever the oracle's
-decision margin exceeds 1e-2."""
+2e-2 of the row maximum for bf16 storage, 1e-3 for the float32 configuration,
+against both the oracle that rounds at the same storage points and the one
+that rounds nowhere; top-k ids, selected paths and accepted lengths bit-exact
+wherever the oracle's decision margin exceeds 1e-2."""
 
 import numpy as np
 import pytest
 
 import oracle
+import synth
 from _cases import Case, rowmax_rel, topk_compare
 
 pytestmark = pytest.mark.gpu
@@ -22,23 +24,33 @@ TOL = {"bf16": 2e-2, "f32": 1e-3}
 KV_TOL = {"bf16": 1.6e-2, "f32": 1e-4}
 
 CASES = [
-    # name, B, K, ctx lengths
-    ("tiny", 1, 8, [64]),
-    ("tiny_bf16", 1, 8, [64]),
-    ("tiny_bf16", 3, 8, [5, 90, 64]),
-    ("small", 2, 16, [130, 7]),
-    ("small_gqa", 2, 8, [200, 129]),
-    ("tiny_bf16", 1, 32, [1]),
-    ("small", 1, 2, [96]),
-    ("tiny_bf16", 9, 8, [70, 3, 64, 0, 200, 17, 64, 65, 9]),   # two 64-row conv tiles
-    ("tiny_bf16", 2, 12, [40, 77]),                            # K does not divide 64
+    # name, B, K, ctx lengths, preset overrides
+    ("tiny", 1, 8, [64], {}),
+    ("tiny_bf16", 1, 8, [64], {}),
+    ("tiny_bf16", 3, 8, [5, 90, 64], {}),
+    ("small", 2, 16, [130, 7], {}),
+    ("small_gqa", 2, 8, [200, 129], {}),
+    ("tiny_bf16", 1, 32, [1], {}),
+    ("small", 1, 2, [96], {}),
+    ("tiny_bf16", 9, 8, [70, 3, 64, 0, 200, 17, 64, 65, 9], {}),   # two 64-row conv tiles
+    ("tiny_bf16", 2, 12, [40, 77], {}),                            # K does not divide 64
+    # one channel per conv gate correction (a full 2D x D gate linear): the fused
+    # conv (8 rows), the GEMM + row-kernel conv (24 rows), the float32 conv
+    ("tiny_bf16", 1, 8, [64], {"conv_group": 1}),
+    ("tiny_bf16", 3, 8, [5, 90, 64], {"conv_group": 1}),
+    ("tiny", 1, 8, [64], {"conv_group": 1}),
 ]
 
 
-@pytest.fixture(scope="module", params=CASES, ids=lambda c: f"{c[0]}-B{c[1]}-K{c[2]}")
+def _case_id(c):
+    name, B, K, _, over = c
+    return f"{name}-B{B}-K{K}" + "".join(f"-{k}{v}" for k, v in over.items())
+
+
+@pytest.fixture(scope="module", params=CASES, ids=_case_id)
 def case(request):
-    name, B, K, ctx = request.param
-    c = Case(name, B, K, ctx, seed=len(ctx) + K).device()
+    name, B, K, ctx, over = request.param
+    c = Case(name, B, K, ctx, seed=len(ctx) + K, **over).device()
     c.g = c.run_device()
     return c
 
@@ -62,6 +74,13 @@ def test_inject_kv_matches_oracle(case):
 def test_logits_within_tolerance(case):
     o = case.oracle()
     err = rowmax_rel(case.g["logits"], o["logits"])
+    assert err < TOL[case.cfg["dtype"]], err
+
+
+def test_logits_within_tolerance_of_unrounded_oracle(case):
+    """The same tolerance against the oracle that keeps float64 at every storage
+    point (the device stores bf16 or float32 there)."""
+    err = rowmax_rel(case.g["logits"], case.oracle_pure_logits())
     assert err < TOL[case.cfg["dtype"]], err
 
 
@@ -203,3 +222,40 @@ def test_select_path_with_table_on_oracle_candidates(B, K):
         if o["margin"][b] > 1e-2:
             assert list(path[b]) == list(o["path"][b]), b
         assert abs(score[b] - o["score"][b]) < 1e-3 * max(1.0, abs(o["score"][b])), b
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("noalloc", [False, True])
+def test_accept_nan_rows(dtype, noalloc):
+    """Acceptance on target rows holding NaN: a row's first NaN is its argmax (NaN
+    ranks above every number), the rule of the oracle (numpy's argmax)."""
+    import block_diffusion_drafter_inject_gb300 as dfl
+    B, K, V = 3, 4, 20000
+    g = np.random.default_rng(7)
+    T = g.standard_normal((B, K, V)).astype(np.float32)
+    T[0, 0, 12345] = np.nan                 # a NaN beats the row's maximum
+    T[0, 1, :] = np.nan                     # all NaN: id 0
+    T[1, 0, 19999] = np.nan                 # NaN in the last chunk
+    T[1, 0, 9000] = np.nan                  # ... and an earlier one in another chunk
+    T[2, 2, 5] = np.inf                     # +inf is a number, NaN still wins
+    T[2, 2, 7] = np.nan
+    tt = torch.from_numpy(T).cuda()
+    if dtype == "bf16":
+        tt = tt.to(torch.bfloat16)
+        T = tt.float().cpu().numpy()
+    # paths that follow the argmax where it is defined by a NaN
+    path = np.stack([[int(np.argmax(T[b, i])) for i in range(K - 1)] for b in range(B)])
+    path[2, 2] = 0                          # request 2 stops at its third draft
+    want_acc, want_tok = oracle.accept_greedy(path.astype(np.int32), T)
+    acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    tok = torch.zeros((B, K), dtype=torch.int32, device="cuda")
+    d_path = torch.from_numpy(path.astype(np.int32)).cuda()
+    if noalloc:
+        dfl.accept_greedy_noalloc(d_path, tt, acc, tok)
+    else:
+        cfg = synth.preset("tiny_bf16")
+        dfl.accept_greedy(d_path, tt, dfl.Workspace(cfg, B, K, 1), acc, tok)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(acc.cpu().numpy(), want_acc)
+    np.testing.assert_array_equal(tok.cpu().numpy(), want_tok)
+    assert list(want_tok[0][:2]) == [12345, 0] and want_tok[1][0] == 9000
