@@ -66,6 +66,9 @@ struct GemmParams {
   const float2 *rope_cs;  // [T][dh/2] (cos, sin)
   int Hq, Hkv, dh;
   float eps;
+  // tile order: weight tile fastest (activations too large to re-read per
+  // weight tile) instead of token tile fastest
+  int m_fastest;
 };
 
 // One CTA's share of one tile: k-blocks [kb0, kb0 + nkb), slice `seg` of the
@@ -92,14 +95,21 @@ struct GemmShape {
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
-// Tile index -> (weight tile, token tile): token tile fastest, so that the CTAs
+// Tile index -> (weight tile, token tile).  Token tile fastest, so that the CTAs
 // holding the token tiles of one weight tile run together and the weight tile
-// is read from HBM once (the others hit L2); the activations are small enough
-// to stay in L2 throughout.
+// is read from HBM once (the others hit L2) while the activations stay in L2
+// throughout; or, when the activations are too large for that (bulk
+// injection), weight tile fastest, so that every activation tile is read from
+// HBM once and the weights, re-read once per wave of token tiles, come from L2.
 __device__ __forceinline__ void tile_coords(int tile, const GemmParams &p, int &m_tile,
                                             int &t_tile) {
-  t_tile = tile % p.t_tiles;
-  m_tile = tile / p.t_tiles;
+  if (p.m_fastest) {
+    m_tile = tile % p.m_tiles;
+    t_tile = tile / p.m_tiles;
+  } else {
+    t_tile = tile % p.t_tiles;
+    m_tile = tile / p.t_tiles;
+  }
 }
 __device__ __forceinline__ void unit_coords(int u, const GemmParams &p, int &m_tile, int &t_tile,
                                             int &split) {
@@ -840,6 +850,9 @@ size_t gemm_scratch_floats(int N_out, int T, int S, int mode, int bn, int chunk,
   return slots * gemm_tiles(N_out, T, mode, bn) * dfl::BM * bn;
 }
 
+// Activation bytes above which tiles are walked weight tile fastest.
+constexpr double kMFastestActBytes = 64e6;
+
 // Kernel parameters and grid of one launch with token tile BN.
 static int make_params(const GemmCall &g, int BN, int num_sms, dfl::GemmParams &p) {
   const bool swiglu = g.mode == GEMM_SWIGLU;
@@ -873,6 +886,7 @@ static int make_params(const GemmCall &g, int BN, int num_sms, dfl::GemmParams &
   p.kb_total = g.K_in / dfl::BK;
   p.total = 0;
   p.nmax = g.S;
+  p.m_fastest = (double)g.T * g.K_in * 2 > kMFastestActBytes ? 1 : 0;
   int grid = p.num_units < num_sms ? p.num_units : num_sms;
   if (g.chunk > 0) {
     const long total = (long)p.m_tiles * p.t_tiles * p.kb_total;
