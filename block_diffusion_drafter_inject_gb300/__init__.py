@@ -4,6 +4,8 @@
     draft_block     one non-causal drafter pass over a block, per-position top-k
     select_path     low-rank bilinear Viterbi over the candidate lattice
     accept_greedy   longest prefix matching the target's argmax + bonus token
+    sample_path     temperature-1 sampling walk over the same pair scores
+    accept_sample   lossless speculative rejection sampling against the target
 """
 
 from . import _lib  # noqa: F401
@@ -15,6 +17,7 @@ from .api import (  # noqa: F401
     Workspace,
     accept_greedy,
     accept_greedy_noalloc,
+    accept_sample,
     clear_device_status,
     draft_block,
     inject_context,
@@ -24,6 +27,7 @@ from .api import (  # noqa: F401
     make_config,
     prepare_selector,
     read_device_status,
+    sample_path,
     select_path,
     workspace_bytes,
 )

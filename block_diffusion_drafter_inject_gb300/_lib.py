@@ -64,6 +64,11 @@ EXPORTS = {
     "dflash_accept_greedy": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                             ctypes.c_size_t, vp]),
     "dflash_accept_greedy_noalloc": (ctypes.c_int, [vp, vp, i32, i32, i32, i32, vp, vp, vp]),
+    "dflash_sample_path": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp,
+                                          vp, vp, i32, i32, vp, vp, vp, vp, ctypes.c_size_t,
+                                          vp]),
+    "dflash_accept_sample": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
+                                            vp, ctypes.c_size_t, vp]),
     "dflash_linear": (ctypes.c_int, [i32, vp, i32, i32, vp, i32, i32, vp, vp]),
     "dflash_linear_splits": (ctypes.c_int32, [i32, i32, i32]),
     "dflash_read_device_status": (ctypes.c_int, [vp, vp]),

@@ -169,6 +169,30 @@ def accept_greedy_noalloc(path, target_logits, accept_len, tokens, stream=None):
           "dflash_accept_greedy_noalloc")
 
 
+def sample_path(cfg, W, anchor, topk_ids, topk_logp, K, uniforms, ws, path, path_q, stream=None):
+    """Temperature-1 sampling walk (dflash_sample_path): uniforms [B, K-1] f32 in
+    [0, 1); path [B, K-1] int32 and path_q [B, K-1, top_k] f32 out."""
+    c = make_config(cfg)
+    check(lib().dflash_sample_path(ctypes.byref(c), ctypes.byref(W.struct), _ptr(anchor),
+                                   _ptr(topk_ids), _ptr(topk_logp), int(anchor.shape[0]), int(K),
+                                   _ptr(uniforms), _ptr(path), _ptr(path_q), ws.ptr, ws.nbytes,
+                                   _stream(stream)),
+          "dflash_sample_path")
+
+
+def accept_sample(path, topk_ids, path_q, target_logits, uniforms, ws, accept_len, tokens,
+                  stream=None):
+    """Speculative rejection sampling (dflash_accept_sample): uniforms [B, K, 2] f32."""
+    B, K, V = target_logits.shape
+    k = topk_ids.shape[-1]
+    dt = _lib.F32 if target_logits.dtype == torch.float32 else _lib.BF16
+    check(lib().dflash_accept_sample(_ptr(path), _ptr(topk_ids), _ptr(path_q),
+                                     _ptr(target_logits), dt, B, K, V, k, _ptr(uniforms),
+                                     _ptr(accept_len), _ptr(tokens), ws.ptr, ws.nbytes,
+                                     _stream(stream)),
+          "dflash_accept_sample")
+
+
 def linear_splits(N_out, T, K_in):
     return int(lib().dflash_linear_splits(N_out, T, K_in))
 

@@ -242,6 +242,8 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->cb = take((size_t)N * D * es);
   L->kvf = take((size_t)N * 2 * Hkv * dh * c->n_layers * 4);
   L->total = off;
+  // acceptance keeps its scratch right after the fixed header
+  L->total = std::max(L->total, kHeaderBytes + accept_sample_floats(B, K, V) * 4);
   return true;
 }
 
@@ -450,21 +452,17 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   return DFLASH_OK;
 }
 
+// Both low-rank projections of the anchor and candidate rows (U then Vp in the
+// workspace) when the weights carry no prepared selector table.
 template <typename S>
-static int run_select(const dflash_config &c, const dflash_weights &w, const int32_t *anchor,
-                      const int32_t *ids, const float *logp, int B, int K, int32_t *path,
-                      float *score, uint8_t *ws, const Layout &L, cudaStream_t st) {
+static int sel_project(const dflash_config &c, const dflash_weights &w, const int32_t *anchor,
+                       const int32_t *ids, int B, int K, uint8_t *ws, const Layout &L,
+                       cudaStream_t st) {
   const int D = c.d_model, k = c.top_k, r = c.sel_rank;
   const int TR = B * (1 + (K - 1) * k);
   int *err = (int *)(ws + L.status);
   S *rows = (S *)(ws + L.selrows);
   float *U = (float *)(ws + L.U), *Vp = (float *)(ws + L.Vp);
-  if (w.sel_table) {  // the projections of every vocabulary row, formed ahead
-    TRY(launch_viterbi(U, Vp, ids, logp, B, K, k, r, (float *)(ws + L.pairs),
-                       (int *)(ws + L.topk_tickets), path, score, w.sel_table, c.vocab, anchor,
-                       err, st));
-    return DFLASH_OK;
-  }
   TRY(launch_sel_gather<S>((const S *)w.embed, anchor, ids, B, K, k, c.vocab, D, rows, err, st));
   if (c.dtype == DFLASH_BF16 && r % 128 == 0) {
     // both projections in one grouped launch (Vp follows U in the workspace)
@@ -482,9 +480,34 @@ static int run_select(const dflash_config &c, const dflash_weights &w, const int
                              nullptr, 0),
                  st));
   }
+  return DFLASH_OK;
+}
+
+template <typename S>
+static int run_select(const dflash_config &c, const dflash_weights &w, const int32_t *anchor,
+                      const int32_t *ids, const float *logp, int B, int K, int32_t *path,
+                      float *score, uint8_t *ws, const Layout &L, cudaStream_t st) {
+  const int k = c.top_k, r = c.sel_rank;
+  int *err = (int *)(ws + L.status);
+  float *U = (float *)(ws + L.U), *Vp = (float *)(ws + L.Vp);
+  // with a table the projections of every vocabulary row are read by token
+  if (!w.sel_table) TRY(sel_project<S>(c, w, anchor, ids, B, K, ws, L, st));
   TRY(launch_viterbi(U, Vp, ids, logp, B, K, k, r, (float *)(ws + L.pairs),
-                     (int *)(ws + L.topk_tickets), path, score, nullptr, c.vocab, anchor, err,
+                     (int *)(ws + L.topk_tickets), path, score, w.sel_table, c.vocab, anchor, err,
                      st));
+  return DFLASH_OK;
+}
+
+template <typename S>
+static int run_sample(const dflash_config &c, const dflash_weights &w, const int32_t *anchor,
+                      const int32_t *ids, const float *logp, int B, int K, const float *uniforms,
+                      int32_t *path, float *path_q, uint8_t *ws, const Layout &L,
+                      cudaStream_t st) {
+  int *err = (int *)(ws + L.status);
+  if (!w.sel_table) TRY(sel_project<S>(c, w, anchor, ids, B, K, ws, L, st));
+  TRY(launch_sample_walk((float *)(ws + L.U), (float *)(ws + L.Vp), ids, logp, B, K, c.top_k,
+                         c.sel_rank, w.sel_table, c.vocab, anchor, uniforms, path, path_q, err,
+                         st));
   return DFLASH_OK;
 }
 
@@ -578,6 +601,56 @@ int dflash_select_path(const dflash_config *cfg, const dflash_weights *w, const 
                            (uint8_t *)ws, L, st);
 }
 
+int dflash_sample_path(const dflash_config *cfg, const dflash_weights *w, const int32_t *anchor,
+                       const int32_t *topk_ids, const float *topk_logp, int32_t B, int32_t K,
+                       const float *uniforms, int32_t *path, float *path_q, void *ws,
+                       size_t ws_bytes, void *stream) {
+  int rc = check_cfg(cfg);
+  if (rc != DFLASH_OK) return rc;
+  if (B < 0 || K < 2 || K > DFLASH_MAX_BLOCK) return DFLASH_ERR_BLOCK;
+  if (B == 0) return DFLASH_OK;
+  if ((size_t)B > kTopkTicketInts) return DFLASH_ERR_DIMS;
+  if (!w || !anchor || !topk_ids || !topk_logp || !uniforms || !path || !path_q || !ws)
+    return DFLASH_ERR_NULL;
+  if (!w->sel_table && (!w->embed || !w->sel_pu || !w->sel_pv)) return DFLASH_ERR_NULL;
+  if (w->sel_table ? !a16(w->sel_table)
+                   : (!a16(w->sel_pu) || !a16(w->sel_pv) || !a16(w->embed)))
+    return DFLASH_ERR_ALIGN;
+  if (!a16(ws)) return DFLASH_ERR_ALIGN;
+  Layout L;
+  make_layout(cfg, B, K, 0, &L);
+  if (ws_bytes < L.total) return DFLASH_ERR_WORKSPACE;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cfg->dtype == DFLASH_BF16)
+    return run_sample<dfl::bf16>(*cfg, *w, anchor, topk_ids, topk_logp, B, K, uniforms, path,
+                                 path_q, (uint8_t *)ws, L, st);
+  return run_sample<float>(*cfg, *w, anchor, topk_ids, topk_logp, B, K, uniforms, path, path_q,
+                           (uint8_t *)ws, L, st);
+}
+
+int dflash_accept_sample(const int32_t *path, const int32_t *topk_ids, const float *path_q,
+                         const void *target_logits, int32_t logits_dtype, int32_t B, int32_t K,
+                         int32_t V, int32_t top_k, const float *uniforms, int32_t *accept_len,
+                         int32_t *tokens, void *ws, size_t ws_bytes, void *stream) {
+  if (logits_dtype != DFLASH_F32 && logits_dtype != DFLASH_BF16) return DFLASH_ERR_DTYPE;
+  if (B < 0 || K < 2 || K > DFLASH_MAX_BLOCK) return DFLASH_ERR_BLOCK;
+  if (V < 1 || top_k < 1 || top_k > DFLASH_MAX_TOPK) return DFLASH_ERR_DIMS;
+  if ((long)B * K > 65535) return DFLASH_ERR_DIMS;  // one grid row per target row
+  if (B == 0) return DFLASH_OK;
+  if (!path || !topk_ids || !path_q || !target_logits || !uniforms || !accept_len || !tokens ||
+      !ws)
+    return DFLASH_ERR_NULL;
+  if (!a16(ws)) return DFLASH_ERR_ALIGN;
+  // chunk statistics after the fixed header (scratch shared with the other calls)
+  const size_t need = kHeaderBytes + accept_sample_floats(B, K, V) * 4;
+  if (ws_bytes < need) return DFLASH_ERR_WORKSPACE;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  return launch_accept_sample(path, topk_ids, path_q, target_logits, logits_dtype, B, K, V, top_k,
+                              uniforms, (float *)((uint8_t *)ws + kHeaderBytes), accept_len,
+                              tokens, (cudaStream_t)stream);
+}
+
 int dflash_prepare_selector(const dflash_config *cfg, const dflash_weights *w, float *table,
                             void *ws, size_t ws_bytes, void *stream) {
   int rc = check_cfg(cfg);
@@ -603,7 +676,7 @@ int dflash_accept_greedy(const int32_t *path, const void *target_logits, int32_t
                          void *ws, size_t ws_bytes, void *stream) {
   if (logits_dtype != DFLASH_F32 && logits_dtype != DFLASH_BF16) return DFLASH_ERR_DTYPE;
   if (B < 0 || K < 2 || K > DFLASH_MAX_BLOCK) return DFLASH_ERR_BLOCK;
-  if (V < 1) return DFLASH_ERR_DIMS;
+  if (V < 1 || (long)B * K > 65535) return DFLASH_ERR_DIMS;  // one grid row per target row
   if (B == 0) return DFLASH_OK;
   if (!path || !target_logits || !accept_len || !tokens || !ws) return DFLASH_ERR_NULL;
   if (!a16(ws)) return DFLASH_ERR_ALIGN;

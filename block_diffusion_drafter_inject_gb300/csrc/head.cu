@@ -552,6 +552,289 @@ __global__ void __launch_bounds__(1024) k_accept(const int32_t *__restrict__ pat
   }
 }
 
+// ---------------------------------------------------------------------------
+// sampling walk and speculative rejection sampling
+// ---------------------------------------------------------------------------
+
+// Inverse-CDF draw (as the oracle's draw_index): the smallest j whose running
+// sum of w exceeds u * total, walking w[0..n) in order; the last positive
+// weight when rounding leaves none.
+__device__ __forceinline__ int draw_inv_cdf(const float *w, int n, float u, float total) {
+  const float target = u * total;
+  float c = 0.f;
+  int last = -1;
+  for (int j = 0; j < n; ++j) {
+    if (w[j] > 0.f) last = j;
+    c += w[j];
+    if (target < c && w[j] > 0.f) return j;
+  }
+  return last < 0 ? 0 : last;
+}
+
+// One CTA per request: the temperature-1 walk from the anchor.  Position t's
+// candidate j gets s_j = logp_t(j) + u(prev) . v(c_tj) with the projections
+// from the selector table (tab, by token) or from the gathered rows (U, Vp
+// [B*R][r], R = 1 + (K-1)*k: anchor first, then the candidates by position and
+// rank); q_t = softmax(s) is written out and one candidate is drawn with the
+// uniform uw[b][t].  prev = the token drawn at t-1 (the anchor at t = 0).
+__global__ void __launch_bounds__(256) k_sample_walk(
+    const float *__restrict__ U, const float *__restrict__ Vp, const int32_t *__restrict__ ids,
+    const float *__restrict__ logp, int K, int k, int r, const float *__restrict__ tab, int V,
+    const int32_t *__restrict__ anchor, const float *__restrict__ uw, int32_t *__restrict__ path,
+    float *__restrict__ pq, int *err) {
+  extern __shared__ float sw[];
+  float *up = sw;  // [r] projection of the predecessor
+  __shared__ float sc[DFLASH_MAX_TOPK];
+  __shared__ int s_tok, s_row;
+  pdl_launch();
+  pdl_wait();
+  const int b = blockIdx.x, T = K - 1, R = 1 + T * k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (threadIdx.x == 0) {
+    int a = anchor[b];
+    if (a < 0 || a >= V) {
+      set_err(err, DFLASH_DEV_TOKEN_RANGE);
+      a = a < 0 ? 0 : V - 1;
+    }
+    s_tok = a;
+    s_row = 0;
+  }
+  __syncthreads();
+  for (int t = 0; t < T; ++t) {
+    const float *usrc = tab ? tab + (size_t)s_tok * r : U + ((size_t)b * R + s_row) * r;
+    for (int i = threadIdx.x; i < r; i += blockDim.x) up[i] = usrc[i];
+    __syncthreads();
+    const size_t cb = ((size_t)b * T + t) * k;
+    for (int j = warp; j < k; j += nw) {
+      int c = ids[cb + j];
+      if (c < 0 || c >= V) {
+        if (lane == 0) set_err(err, DFLASH_DEV_TOKEN_RANGE);
+        c = c < 0 ? 0 : V - 1;
+      }
+      const float *vsrc = tab ? tab + ((size_t)V + c) * r : Vp + ((size_t)b * R + 1 + (size_t)t * k + j) * r;
+      float acc = 0.f;
+      for (int i = lane; i < r; i += 32) acc = fmaf(up[i], vsrc[i], acc);
+      acc = warp_sum(acc);
+      if (lane == 0) sc[j] = logp[cb + j] + acc;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = -INFINITY;
+      for (int j = 0; j < k; ++j) m = fmaxf(m, sc[j]);
+      float e[DFLASH_MAX_TOPK], tot = 0.f;
+      for (int j = 0; j < k; ++j) {
+        e[j] = expf(sc[j] - m);
+        tot += e[j];
+      }
+      for (int j = 0; j < k; ++j) pq[cb + j] = e[j] / tot;
+      const int jd = draw_inv_cdf(e, k, uw[(size_t)b * T + t], tot);
+      int c = ids[cb + jd];
+      c = c < 0 ? 0 : c >= V ? V - 1 : c;
+      path[(size_t)b * T + t] = c;
+      s_tok = c;
+      s_row = 1 + t * k + jd;
+    }
+    __syncthreads();
+  }
+}
+
+// (max, sum e^(z - max)) of one chunk of one target row -> part[row][chunk]
+template <typename L>
+__global__ void __launch_bounds__(256) k_row_chunk_stats(const L *__restrict__ logits, int V,
+                                                          float2 *__restrict__ part) {
+  __shared__ float red[32];
+  pdl_launch();
+  pdl_wait();
+  const int chunk = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
+  const int c0 = chunk * dflh::kArgmaxChunk, c1 = min(V, c0 + dflh::kArgmaxChunk);
+  const L *z = logits + (size_t)row * V;
+  float m = -INFINITY;
+  for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) m = fmaxf(m, ldf(z + i));
+  m = block_max(m, red);
+  float s = 0.f;
+  if (m > -INFINITY)
+    for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) s += expf(ldf(z + i) - m);
+  s = block_sum(s, red);
+  if (threadIdx.x == 0) part[(size_t)row * nch + chunk] = make_float2(m, s);
+}
+
+// The row's softmax normaliser from its chunk partials, in chunk order (every
+// caller forms exactly the same values).
+__device__ __forceinline__ float2 row_norm(const float2 *part, int nch) {
+  float M = -INFINITY;
+  for (int c = 0; c < nch; ++c) M = fmaxf(M, part[c].x);
+  float S = 0.f;
+  for (int c = 0; c < nch; ++c)
+    if (part[c].x > -INFINITY) S += part[c].y * expf(part[c].x - M);
+  return make_float2(M, S);
+}
+
+// Residual weight of token v in target row i of request b: max(0, p_i(v) -
+// q_i(v)) for draft rows (q from the proposal over the row's candidates),
+// p_i(v) for the last row (the bonus draw).
+struct RowQ {
+  int id[DFLASH_MAX_TOPK];
+  float q[DFLASH_MAX_TOPK];
+  int n;
+};
+__device__ __forceinline__ float resid_w(float z, float2 MS, int v, const RowQ &rq) {
+  const float p = MS.y > 0.f ? expf(z - MS.x) / MS.y : 0.f;
+  float q = 0.f;
+  for (int j = 0; j < rq.n; ++j)
+    if (rq.id[j] == v) q += rq.q[j];
+  return fmaxf(p - q, 0.f);
+}
+
+// Per (chunk, row): the row's residual weights summed over the chunk ->
+// rsum[row][chunk], and its target probabilities -> psum[row][chunk].
+template <typename L>
+__global__ void __launch_bounds__(256) k_resid_chunks(const L *__restrict__ logits, int V, int K,
+                                                       int k, const float2 *__restrict__ part,
+                                                       const int32_t *__restrict__ ids,
+                                                       const float *__restrict__ pq,
+                                                       float *__restrict__ rsum,
+                                                       float *__restrict__ psum) {
+  __shared__ float red[32];
+  __shared__ RowQ rq;
+  pdl_launch();
+  pdl_wait();
+  const int chunk = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
+  const int b = row / K, i = row % K;
+  if (threadIdx.x == 0) {
+    rq.n = i < K - 1 ? k : 0;
+    for (int j = 0; j < rq.n; ++j) {
+      rq.id[j] = ids[((size_t)b * (K - 1) + i) * k + j];
+      rq.q[j] = pq[((size_t)b * (K - 1) + i) * k + j];
+    }
+  }
+  __syncthreads();
+  const float2 MS = row_norm(part + (size_t)row * nch, nch);
+  const int c0 = chunk * dflh::kArgmaxChunk, c1 = min(V, c0 + dflh::kArgmaxChunk);
+  const L *z = logits + (size_t)row * V;
+  float rs = 0.f, ps = 0.f;
+  for (int v = c0 + threadIdx.x; v < c1; v += blockDim.x) {
+    const float zv = ldf(z + v);
+    ps += MS.y > 0.f ? expf(zv - MS.x) / MS.y : 0.f;
+    rs += resid_w(zv, MS, v, rq);
+  }
+  rs = block_sum(rs, red);
+  ps = block_sum(ps, red);
+  if (threadIdx.x == 0) {
+    rsum[(size_t)row * nch + chunk] = rs;
+    psum[(size_t)row * nch + chunk] = ps;
+  }
+}
+
+// One CTA per request: accept draft i while u0 q_i(x) < p_i(x); at the first
+// rejection draw the replacement from the residual max(0, p_i - q_i) (from p_i
+// when that is zero everywhere), else the bonus token from p_{K-1}; the draw
+// walks the chunk sums in order, then the chosen chunk's weights in token order.
+template <typename L>
+__global__ void __launch_bounds__(256) k_accept_sample(
+    const L *__restrict__ logits, int V, int K, int k, int nch, const int32_t *__restrict__ path,
+    const int32_t *__restrict__ ids, const float *__restrict__ pq,
+    const float2 *__restrict__ part, const float *__restrict__ rsum,
+    const float *__restrict__ psum, const float *__restrict__ uni,
+    int32_t *__restrict__ accept_len, int32_t *__restrict__ tokens) {
+  constexpr int NT = 256, PER = dflh::kArgmaxChunk / NT;  // 32 tokens per thread
+  __shared__ int s_stop, s_chunk, s_usep, s_tok;
+  __shared__ float s_target, s_pref[NT];
+  __shared__ RowQ rq;
+  pdl_launch();
+  pdl_wait();
+  const int b = blockIdx.x, tid = threadIdx.x;
+  if (tid == 0) {
+    int stop = K - 1;
+    for (int i = 0; i < K - 1; ++i) {
+      const size_t row = (size_t)b * K + i;
+      const float2 MS = row_norm(part + row * nch, nch);
+      const int x = path[(size_t)b * (K - 1) + i];
+      float qx = 0.f;
+      for (int j = 0; j < k; ++j)
+        if (ids[((size_t)b * (K - 1) + i) * k + j] == x) qx += pq[((size_t)b * (K - 1) + i) * k + j];
+      const float px = (x >= 0 && x < V && MS.y > 0.f)
+                           ? expf(ldf(logits + row * V + x) - MS.x) / MS.y : 0.f;
+      if (!(uni[row * 2] * qx < px)) {
+        stop = i;
+        break;
+      }
+    }
+    const size_t row = (size_t)b * K + stop;
+    rq.n = stop < K - 1 ? k : 0;
+    for (int j = 0; j < rq.n; ++j) {
+      rq.id[j] = ids[((size_t)b * (K - 1) + stop) * k + j];
+      rq.q[j] = pq[((size_t)b * (K - 1) + stop) * k + j];
+    }
+    float tot = 0.f;
+    for (int c = 0; c < nch; ++c) tot += rsum[row * nch + c];
+    const bool usep = !(tot > 0.f);
+    const float *cs = (usep ? psum : rsum) + row * nch;
+    if (usep) {
+      tot = 0.f;
+      for (int c = 0; c < nch; ++c) tot += cs[c];
+    }
+    float target = uni[row * 2 + 1] * tot, run = 0.f;
+    int ch = -1, lastpos = 0;
+    for (int c = 0; c < nch; ++c) {
+      if (cs[c] > 0.f) lastpos = c;
+      if (ch < 0 && target < run + cs[c] && cs[c] > 0.f) ch = c;
+      if (ch < 0) run += cs[c];
+    }
+    // rounding left the target past every chunk: the last positive weight
+    if (ch < 0) ch = lastpos, run = 0.f, target = 3.0e38f;
+    s_stop = stop;
+    s_chunk = ch;
+    s_usep = usep;
+    s_target = target - run;  // position inside the chunk
+    s_tok = -1;
+  }
+  __syncthreads();
+  const int stop = s_stop;
+  const size_t row = (size_t)b * K + stop;
+  const float2 MS = row_norm(part + row * nch, nch);
+  const L *z = logits + row * V;
+  const int c0 = s_chunk * dflh::kArgmaxChunk;
+  // this thread's run of PER consecutive tokens
+  float w[PER], own = 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int v = c0 + tid * PER + e;
+    float x = 0.f;
+    if (v < V) {
+      const float zv = ldf(z + v);
+      x = s_usep ? (MS.y > 0.f ? expf(zv - MS.x) / MS.y : 0.f) : resid_w(zv, MS, v, rq);
+    }
+    w[e] = x;
+    own += x;
+  }
+  s_pref[tid] = own;
+  __syncthreads();
+  if (tid == 0) {  // exclusive prefix over the threads, in order
+    float run = 0.f;
+    int hit = -1, lastpos = -1;
+    for (int t = 0; t < NT; ++t) {
+      const float o = s_pref[t];
+      if (o > 0.f) lastpos = t;
+      if (hit < 0 && s_target < run + o && o > 0.f) hit = t;
+      s_pref[t] = run;
+      run += o;
+    }
+    if (hit < 0) hit = lastpos < 0 ? 0 : lastpos, s_target = s_pref[hit] + 3.0e38f;
+    s_tok = hit;  // the thread holding the draw
+  }
+  __syncthreads();
+  if (tid == s_tok) {
+    const float tgt = s_target - s_pref[tid];
+    const int j = draw_inv_cdf(w, PER, 1.f, tgt > 0.f ? tgt : 0.f);
+    // draw_inv_cdf(w, n, 1, T) walks the running sum against T directly
+    int v = c0 + tid * PER + j;
+    v = v >= V ? V - 1 : v;
+    for (int i = 0; i < K; ++i)
+      tokens[(size_t)b * K + i] = i < stop ? path[(size_t)b * (K - 1) + i] : i == stop ? v : -1;
+    accept_len[b] = stop + 1;
+  }
+}
+
 }  // namespace dfl
 
 namespace dflh {
@@ -616,6 +899,51 @@ int launch_accept(const int32_t *path, const void *logits, int dtype, int B, int
   DFL_CHECK_LAUNCH(launch(dfl::k_accept, dim3(B), dim3(32 * K), 0, st,
                           (const int32_t *)path, (const float *)partial, B, K, nch, accept_len,
                           tokens));
+  return DFLASH_OK;
+}
+
+int launch_sample_walk(const float *U, const float *Vp, const int32_t *topk_ids,
+                       const float *topk_logp, int B, int K, int k, int r, const float *tab, int V,
+                       const int32_t *anchor, const float *uniforms, int32_t *path, float *path_q,
+                       int *err, cudaStream_t st) {
+  const size_t smem = sizeof(float) * (size_t)r;
+  DFL_CHECK_LAUNCH(launch(dfl::k_sample_walk, dim3(B), dim3(256), smem, st, U, Vp, topk_ids,
+                          topk_logp, K, k, r, tab, V, anchor, uniforms, path, path_q, err));
+  return DFLASH_OK;
+}
+
+size_t accept_sample_floats(int B, int K, int V) {
+  return (size_t)B * K * argmax_chunks(V) * 4;
+}
+
+int launch_accept_sample(const int32_t *path, const int32_t *topk_ids, const float *path_q,
+                         const void *logits, int dtype, int B, int K, int V, int k,
+                         const float *uniforms, float *scratch, int32_t *accept_len,
+                         int32_t *tokens, cudaStream_t st) {
+  const int nch = argmax_chunks(V);
+  const size_t rows = (size_t)B * K;
+  float2 *part = (float2 *)scratch;
+  float *rsum = scratch + rows * nch * 2, *psum = rsum + rows * nch;
+  if (dtype == DFLASH_F32) {
+    const float *z = (const float *)logits;
+    DFL_CHECK_LAUNCH(launch(dfl::k_row_chunk_stats<float>, dim3(nch, B * K), dim3(256), 0, st, z,
+                            V, part));
+    DFL_CHECK_LAUNCH(launch(dfl::k_resid_chunks<float>, dim3(nch, B * K), dim3(256), 0, st, z, V,
+                            K, k, (const float2 *)part, topk_ids, path_q, rsum, psum));
+    DFL_CHECK_LAUNCH(launch(dfl::k_accept_sample<float>, dim3(B), dim3(256), 0, st, z, V, K, k,
+                            nch, path, topk_ids, path_q, (const float2 *)part, (const float *)rsum,
+                            (const float *)psum, uniforms, accept_len, tokens));
+  } else {
+    const dfl::bf16 *z = (const dfl::bf16 *)logits;
+    DFL_CHECK_LAUNCH(launch(dfl::k_row_chunk_stats<dfl::bf16>, dim3(nch, B * K), dim3(256), 0, st,
+                            z, V, part));
+    DFL_CHECK_LAUNCH(launch(dfl::k_resid_chunks<dfl::bf16>, dim3(nch, B * K), dim3(256), 0, st, z,
+                            V, K, k, (const float2 *)part, topk_ids, path_q, rsum, psum));
+    DFL_CHECK_LAUNCH(launch(dfl::k_accept_sample<dfl::bf16>, dim3(B), dim3(256), 0, st, z, V, K,
+                            k, nch, path, topk_ids, path_q, (const float2 *)part,
+                            (const float *)rsum, (const float *)psum, uniforms, accept_len,
+                            tokens));
+  }
   return DFLASH_OK;
 }
 

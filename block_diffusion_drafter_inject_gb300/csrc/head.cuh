@@ -33,4 +33,20 @@ inline int argmax_chunks(int V) { return (V + kArgmaxChunk - 1) / kArgmaxChunk; 
 int launch_accept(const int32_t *path, const void *logits, int dtype, int B, int K, int V,
                   float *partial, int32_t *accept_len, int32_t *tokens, cudaStream_t st);
 
+// Temperature-1 sampling walk over the pair scores (projections as for
+// launch_viterbi); uniforms [B][K-1]; path [B][K-1]; path_q [B][K-1][k]: the
+// proposal over position t's candidates given the token drawn before it.
+int launch_sample_walk(const float *U, const float *Vp, const int32_t *topk_ids,
+                       const float *topk_logp, int B, int K, int k, int r, const float *tab, int V,
+                       const int32_t *anchor, const float *uniforms, int32_t *path, float *path_q,
+                       int *err, cudaStream_t st);
+
+// Speculative rejection sampling; uniforms [B][K][2]; scratch of
+// accept_sample_floats(B, K, V) floats.
+size_t accept_sample_floats(int B, int K, int V);
+int launch_accept_sample(const int32_t *path, const int32_t *topk_ids, const float *path_q,
+                         const void *logits, int dtype, int B, int K, int V, int k,
+                         const float *uniforms, float *scratch, int32_t *accept_len,
+                         int32_t *tokens, cudaStream_t st);
+
 }  // namespace dflh

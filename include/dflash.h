@@ -7,7 +7,9 @@
  *   2. dflash_draft_block      one non-causal drafter pass over a block of K slots,
  *                              per-position top-k candidates
  *   3. dflash_select_path      one coherent candidate path (Viterbi over the lattice)
+ *      dflash_sample_path      ... or a temperature-1 walk drawn from the same scores
  *   4. dflash_accept_greedy    longest prefix that matches the target's argmax + bonus
+ *      dflash_accept_sample    ... or lossless speculative rejection sampling
  *
  * Conventions shared by every call
  *  - Every buffer belongs to the caller.  The library never allocates, frees or
@@ -216,11 +218,58 @@ int dflash_prepare_selector(const dflash_config *cfg, const dflash_weights *w, f
  * every number, so a row's first NaN is its argmax).  With m accepted drafts,
  *   accept_len[b] = m + 1,  tokens[b] = path[0..m-1], argmax(row m), -1 ...
  *   path           device int32 [B, K-1]
- *   target_logits  device [B, K, V] f32 (logits_dtype DFLASH_F32) or bf16     */
+ *   target_logits  device [B, K, V] f32 (logits_dtype DFLASH_F32) or bf16
+ * B * K <= 65535 (else DFLASH_ERR_DIMS).                                      */
 int dflash_accept_greedy(const int32_t *path, const void *target_logits,
                          int32_t logits_dtype, int32_t B, int32_t K, int32_t V,
                          int32_t *accept_len, int32_t *tokens, void *ws,
                          size_t ws_bytes, void *stream);
+
+/* Temperature-1 sampling walk (Architecture page, "Problem 1": only the final
+ * walk over the precomputed pair scores is sequential, and sampling draws from
+ * the same scores as the greedy walk).  From the anchor, position t draws one
+ * of its top_k candidates with probability
+ *   q_t(j) = softmax_j( logp_t(j) + u(prev) . v(c_tj) ),   prev = token drawn at t-1,
+ * with u, v the selector projections (from w->sel_table when set, else formed
+ * from the gathered embedding rows) and the inverse CDF over candidate ranks
+ * (the smallest j whose running sum of q exceeds uniforms[b][t]).
+ *   anchor     device int32 [B]
+ *   topk_ids   device int32 [B, K-1, top_k];  topk_logp device f32 [B, K-1, top_k]
+ *   uniforms   device f32 [B, K-1], values in [0, 1) (the caller's random numbers)
+ *   path       device int32 [B, K-1] out: the drawn tokens
+ *   path_q     device f32 [B, K-1, top_k] out: q_t over position t's candidates
+ *              given the token drawn before it (the proposal dflash_accept_sample
+ *              needs).  Workspace and errors as for dflash_select_path. */
+int dflash_sample_path(const dflash_config *cfg, const dflash_weights *w, const int32_t *anchor,
+                       const int32_t *topk_ids, const float *topk_logp, int32_t B, int32_t K,
+                       const float *uniforms, int32_t *path, float *path_q, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* Lossless speculative rejection sampling (Architecture page, "Speculative
+ * Decoding Context": rejection sampling makes the scheme lossless; "Problem 1":
+ * it restores the exact target distribution).  Row i of the target logits
+ * gives p_i = softmax(row i) for the token after slot i.  Draft i (token
+ * x = path[b][i], proposed with q_i: path_q over the candidates topk_ids[b][i],
+ * zero for other tokens) is accepted while u0 * q_i(x) < p_i(x), with
+ * u0 = uniforms[b][i][0].  At the first rejection the replacement is drawn from
+ * max(0, p_i - q_i) with uniforms[b][i][1] and the block ends; when every draft
+ * is accepted a bonus token is drawn from p_{K-1} with uniforms[b][K-1][1].
+ * Draws take the smallest token id whose running sum (in id order) exceeds
+ * u times the total.  The committed tokens follow the target's distribution
+ * exactly, whatever the proposal.
+ *   path           device int32 [B, K-1];  topk_ids device int32 [B, K-1, top_k]
+ *   path_q         device f32 [B, K-1, top_k] (from dflash_sample_path)
+ *   target_logits  device [B, K, V] f32 (logits_dtype DFLASH_F32) or bf16
+ *   uniforms       device f32 [B, K, 2], values in [0, 1)
+ *   accept_len     device int32 [B] out: committed tokens, 1..K
+ *   tokens         device int32 [B, K] out: the committed tokens, then -1
+ * B * K <= 65535 (else DFLASH_ERR_DIMS).  ws: any workspace of
+ * dflash_workspace_bytes for these B and K (scratch after its fixed header:
+ * B*K*ceil(V/8192)*16 bytes). */
+int dflash_accept_sample(const int32_t *path, const int32_t *topk_ids, const float *path_q,
+                         const void *target_logits, int32_t logits_dtype, int32_t B, int32_t K,
+                         int32_t V, int32_t top_k, const float *uniforms, int32_t *accept_len,
+                         int32_t *tokens, void *ws, size_t ws_bytes, void *stream);
 
 /* Greedy acceptance for callers that cannot provide a workspace.  (The DFlash
  * pages have no counterpart: this is a deployment variant of

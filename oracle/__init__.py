@@ -28,4 +28,9 @@ from .dflash import (  # noqa: F401
     select_path_request,
     accept_greedy,
     accept_greedy_request,
+    draw_index,
+    sample_path,
+    sample_path_request,
+    accept_sample,
+    accept_sample_request,
 )

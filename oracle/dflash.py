@@ -418,3 +418,111 @@ def accept_greedy(path, T):
     for b in range(B):
         acc[b], toks[b] = accept_greedy_request(path[b], T[b])
     return acc, toks
+
+
+# ----------------------------------------------------------------------------
+# sampling walk and lossless rejection sampling
+# ----------------------------------------------------------------------------
+
+def draw_index(weights, u):
+    """Inverse-CDF draw from non-negative weights (not necessarily normalised)
+    with one uniform u in [0, 1): the smallest index j with u * W < C_j, where
+    C_j is the running sum of the weights in index order and W = C_last."""
+    w = np.asarray(weights, dtype=F64)
+    c = np.cumsum(w)
+    j = int(np.searchsorted(c, u * c[-1], side="right"))
+    return min(j, int(np.flatnonzero(w > 0)[-1]))
+
+
+def sample_path_request(E, Pu, Pv, anchor, ids, logp, u_walk):
+    """Temperature-1 sampling walk over the candidate lattice of one request.
+
+    Architecture page, "Problem 1 - Independent picks are incoherent": the
+    walk over the precomputed pair scores is the only sequential part, and
+    sampling draws from the same scores as the greedy walk.  From the anchor
+    (last verified token), position t draws its candidate j with probability
+        q_t(j) = softmax_j( logp_t(j) + (P_u e_a) . (P_v e_{c_tj}) )
+    where a is the token drawn at t-1 (the anchor at t = 1), by inverse CDF
+    over the candidate ranks with the uniform u_walk[t] (draw_index).
+    ids, logp [T, k]; u_walk [T].  Returns (path [T], q [T, k]): the drawn
+    tokens and, per position, the proposal distribution they were drawn from."""
+    E = np.asarray(E)
+    Pu = np.asarray(Pu, dtype=F64)
+    Pv = np.asarray(Pv, dtype=F64)
+    T, k = ids.shape
+    emb = lambda t: np.asarray(E[int(t)], dtype=F64)
+    prev = int(anchor)
+    path = np.zeros(T, dtype=np.int32)
+    q = np.zeros((T, k))
+    for t in range(T):
+        u_prev = Pu @ emb(prev)
+        s = np.array([float(logp[t][j]) + u_prev @ (Pv @ emb(ids[t][j])) for j in range(k)])
+        e = np.exp(s - s.max())
+        q[t] = e / e.sum()
+        j = draw_index(e, float(u_walk[t]))
+        path[t] = ids[t][j]
+        prev = int(path[t])
+    return path, q
+
+
+def accept_sample_request(path, cand_ids, q, T, u):
+    """Speculative rejection sampling of one request's drafted block (lossless).
+
+    Architecture page, "Speculative Decoding Context" (rejection sampling makes
+    the scheme lossless) and "Problem 1" (rejection sampling restores the
+    exact target distribution).  Row i of T is the target's logits for the
+    token after block slot i; p_i = softmax(T[i]) at temperature 1.  The draft
+    token x = path[i] came from the proposal q_i (q[i][j] for candidate
+    cand_ids[i][j], 0 for every other token).  For i = 0, 1, ...: x is accepted
+    when u[i, 0] * q_i(x) < p_i(x) (probability min(1, p/q)); at the first
+    rejection the replacement is drawn from max(0, p_i - q_i) with u[i, 1] and
+    the block ends; when every draft is accepted a bonus token is drawn from
+    p_{K-1} with u[K-1, 1].  Draws use draw_index over token ids.
+    path [K-1]; cand_ids, q [K-1, k]; T [K, V]; u [K, 2].
+    Returns (accept_len in 1..K, tokens [K], -1 after the last token)."""
+    T = np.asarray(T, dtype=F64)
+    K = T.shape[0]
+    tokens = np.full(K, -1, dtype=np.int32)
+
+    def probs(i):
+        z = T[i]
+        e = np.exp(z - z.max())
+        return e / e.sum()
+
+    for i in range(K - 1):
+        p = probs(i)
+        x = int(path[i])
+        qi = np.zeros_like(p)
+        for j, c in enumerate(cand_ids[i]):
+            qi[int(c)] += float(q[i][j])
+        if float(u[i][0]) * qi[x] < p[x]:
+            tokens[i] = x
+            continue
+        r = np.maximum(p - qi, 0.0)
+        # r sums to zero only if p = q, where no draft is ever rejected; p then
+        # stands in (a measure-zero case kept defined)
+        tokens[i] = draw_index(r if r.sum() > 0 else p, float(u[i][1]))
+        return i + 1, tokens
+    tokens[K - 1] = draw_index(probs(K - 1), float(u[K - 1][1]))
+    return K, tokens
+
+
+def sample_path(cfg, W, anchors, ids, logp, u_walk):
+    """Batch form: path [B, K-1], q [B, K-1, k]."""
+    B, T, k = ids.shape
+    path = np.zeros((B, T), dtype=np.int32)
+    q = np.zeros((B, T, k))
+    for b in range(B):
+        path[b], q[b] = sample_path_request(W["embed"], W["sel_pu"], W["sel_pv"], anchors[b],
+                                            ids[b], logp[b], u_walk[b])
+    return path, q
+
+
+def accept_sample(path, cand_ids, q, T, u):
+    """Batch form: accept_len [B], tokens [B, K]."""
+    B, K = T.shape[0], T.shape[1]
+    acc = np.zeros(B, dtype=np.int32)
+    toks = np.zeros((B, K), dtype=np.int32)
+    for b in range(B):
+        acc[b], toks[b] = accept_sample_request(path[b], cand_ids[b], q[b], T[b], u[b])
+    return acc, toks

@@ -172,6 +172,28 @@ def test_inject_select_accept_linear_host_checks(dfl):
     assert L.dflash_read_device_status(None, None) == -1
 
 
+def test_sampling_host_checks(dfl):
+    L = dfl.lib()
+    cfg = _cfg(dfl)
+    w = _fake_weights(dfl, cfg)
+    P = ctypes.c_void_p
+    a = P(1 << 24)
+    big = 1 << 30
+    assert L.dflash_sample_path(ctypes.byref(cfg), ctypes.byref(w), a, a, a, 0, 8, a, a, a, a,
+                                big, None) == 0                       # B = 0: no-op
+    assert L.dflash_sample_path(ctypes.byref(cfg), ctypes.byref(w), a, a, a, 1, 1, a, a, a, a,
+                                big, None) == -3                      # K < 2
+    assert L.dflash_sample_path(ctypes.byref(cfg), ctypes.byref(w), a, a, a, 1, 8, P(0), a, a, a,
+                                big, None) == -1                      # no uniforms
+    assert L.dflash_sample_path(ctypes.byref(cfg), ctypes.byref(w), a, a, a, 1, 8, a, a, a, a,
+                                16, None) == -4                       # workspace too small
+    assert L.dflash_accept_sample(a, a, a, a, 3, 1, 8, 100, 4, a, a, a, a, big, None) == -5
+    assert L.dflash_accept_sample(a, a, a, a, 0, 1, 40, 100, 4, a, a, a, a, big, None) == -3
+    assert L.dflash_accept_sample(a, a, a, a, 0, 1, 8, 100, 33, a, a, a, a, big, None) == -2
+    assert L.dflash_accept_sample(a, a, a, a, 0, 1, 8, 100, 4, P(0), a, a, a, big, None) == -1
+    assert L.dflash_accept_sample(a, a, a, a, 0, 1, 8, 100, 4, a, a, a, a, 16, None) == -4
+
+
 def test_launch_counter_resets(dfl):
     L = dfl.lib()
     L.dflash_launch_count(1)
