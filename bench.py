@@ -62,7 +62,8 @@ def pass_bytes(cfg, B, K, ctx):
     wb = weight_bytes(cfg)
     es = 2
     D, k, r = cfg["d_model"], cfg["top_k"], cfg["sel_rank"]
-    w = sum(v for n, v in wb.items() if n not in ("fc", "fc_norm", "embed", "sel_pu", "sel_pv"))
+    w = sum(v for n, v in wb.items()
+            if n not in ("fc", "fc_norm", "embed", "sel_pu", "sel_pv", "sel_gate"))
     kv = 0
     per_tok = cfg["n_layers"] * 2 * cfg["n_kv_heads"] * cfg["head_dim"] * es
     for c in ctx:
@@ -248,6 +249,41 @@ def setup_workload(torch, dfl, cfg, Wd, B, K, ctx, seed, max_inject):
     return kv, cyc, inp
 
 
+def inject_weight_names(cfg):
+    """The weights an inject call reads: fc and its norm, every layer's wqkv and k_norm."""
+    names = {"fc_norm", "fc"}
+    for l in range(cfg["n_layers"]):
+        names |= {f"layers.{l}.wqkv", f"layers.{l}.k_norm"}
+    return names
+
+
+def bench_inject_rows(torch, dfl, cfg, pk, args, N=4096):
+    """One inject call of N rows into one request's pages, with only the weights
+    injection reads on the device (about 1.2 GB in all): the small case on which
+    the injection's GEMMs are profiled."""
+    Wh = synth.make_weights(cfg, seed=0, names=inject_weight_names(cfg))
+    Wd = dfl.DeviceWeights.from_host(cfg, Wh, "cuda")
+    P = cfg["page_size"]
+    kv = dfl.PagedKV(cfg, np.arange(N // P, dtype=np.int32)[None, :], N // P, "cuda")
+    ws = dfl.Workspace(cfg, 1, 2, N)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(3)
+    hid = torch.randn((N, cfg["n_taps"] * cfg["d_target"]), device="cuda",
+                      generator=gen).to(torch.bfloat16)
+    req = torch.zeros(N, dtype=torch.int32, device="cuda")
+    pos = torch.arange(N, dtype=torch.int32, device="cuda")
+
+    def inject():
+        dfl.inject_context(cfg, Wd, kv, hid, req, pos, ws)
+
+    steps = max(3, min(args.steps, 20))
+    ms = event_time(torch, inject, steps, args.warmup)
+    fl = inject_flops(cfg, N)
+    return {"rows": N, "inject_ms": ms, "inject_tflops": fl / (ms * 1e-3) / 1e12,
+            "frac_of_tensor_roofline": fl / (pk["bf16_sus"] * 1e12) / (ms * 1e-3),
+            "device_status": dfl.read_device_status(ws)}
+
+
 def run_gpu(args, rank, world, barrier, allmax):
     import torch
     import block_diffusion_drafter_inject_gb300 as dfl
@@ -256,6 +292,8 @@ def run_gpu(args, rank, world, barrier, allmax):
     torch.cuda.set_device(dev)
     cfg = synth.preset("full")
     pk = peaks()
+    if args.sections == {"inject4k"}:
+        return {"inject4k": bench_inject_rows(torch, dfl, cfg, pk, args)}, None
     t0 = time.time()
     Wh = synth.make_weights(cfg, seed=0)
     Wd = dfl.DeviceWeights.from_host(cfg, Wh, "cuda")
@@ -496,8 +534,8 @@ def oracle_sample(cfg, Wh, K=8, ctx=2048, reps=1, seed=0):
         path, _ = oracle.select_path(scfg, Ws, anchor, d["ids"], d["logp"])
         oracle.accept_greedy(path, target)
         times.append(time.perf_counter() - t)
-    full = sum(int(np.prod(s)) for n, s, _ in synth.weight_names(cfg) if n != "embed")
-    samp = sum(int(np.prod(s)) for n, s, _ in synth.weight_names(scfg) if n != "embed")
+    full = sum(int(np.prod(s)) for n, s, _ in synth.weight_names(cfg) if n not in ("embed", "sel_gate"))
+    samp = sum(int(np.prod(s)) for n, s, _ in synth.weight_names(scfg) if n not in ("embed", "sel_gate"))
     return float(np.median(times)), samp / full
 
 
@@ -612,7 +650,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--only", default="",
-                    help="comma list of sections to run: b1 (headline), b32, inject")
+                    help="comma list of sections to run: b1 (headline), b32, inject; or "
+                         "inject4k alone (a 4096-row injection with only its weights loaded, "
+                         "the small profiling case)")
     ap.add_argument("--no-b32", action="store_true")
     ap.add_argument("--no-inject", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -645,7 +685,7 @@ def main():
     barrier, allmax = replica_sync(world, device="cuda")
     res, Wh = run_gpu(args, rank, world, barrier, allmax)
     if rank == 0:
-        if not args.no_cpu_baseline and "b1" in args.sections:
+        if not args.no_cpu_baseline and "b1" in args.sections and Wh is not None:
             res["cpu_baseline"] = cpu_baseline(Wh, synth.preset("full"))
         print(json.dumps(res))
     if world > 1:

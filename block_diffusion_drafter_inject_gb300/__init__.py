@@ -5,6 +5,7 @@
     select_path     low-rank bilinear Viterbi over the candidate lattice
     accept_greedy   longest prefix matching the target's argmax + bonus token
     sample_path     temperature-1 sampling walk over the same pair scores
+    select_greedy   the pages' context-gated pair scores, greedy best-successor walk
     accept_sample   lossless speculative rejection sampling against the target
 """
 
@@ -20,6 +21,7 @@ from .api import (  # noqa: F401
     accept_sample,
     clear_device_status,
     draft_block,
+    draft_hidden,
     inject_context,
     launch_count,
     linear,
@@ -28,6 +30,7 @@ from .api import (  # noqa: F401
     prepare_selector,
     read_device_status,
     sample_path,
+    select_greedy,
     select_path,
     workspace_bytes,
 )

@@ -41,7 +41,7 @@ class LayerWeights(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [("fc_norm", vp), ("fc", vp), ("embed", vp), ("lm_head", vp), ("final_norm", vp),
                 ("sel_pu", vp), ("sel_pv", vp), ("layer", LayerWeights * MAX_LAYERS),
-                ("sel_table", vp)]
+                ("sel_table", vp), ("sel_gate", vp)]
 
 
 class KV(ctypes.Structure):
@@ -67,10 +67,17 @@ EXPORTS = {
     "dflash_sample_path": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp,
                                           vp, vp, i32, i32, vp, vp, vp, vp, ctypes.c_size_t,
                                           vp]),
+    "dflash_select_greedy": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp,
+                                            vp, vp, vp, i32, i32, vp, vp, vp, ctypes.c_size_t,
+                                            vp]),
+    "dflash_draft_hidden": (ctypes.c_void_p, [ctypes.POINTER(Config), i32, i32, vp,
+                                              ctypes.c_size_t]),
     "dflash_accept_sample": (ctypes.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp,
                                             vp, ctypes.c_size_t, vp]),
     "dflash_linear": (ctypes.c_int, [i32, vp, i32, i32, vp, i32, i32, vp, vp]),
     "dflash_linear_splits": (ctypes.c_int32, [i32, i32, i32]),
+    "dflash_test_linear_wait": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp, ctypes.c_size_t,
+                                               ctypes.c_uint32, vp]),
     "dflash_read_device_status": (ctypes.c_int, [vp, vp]),
     "dflash_clear_device_status": (ctypes.c_int, [vp, vp]),
     "dflash_status_string": (ctypes.c_char_p, [ctypes.c_int]),

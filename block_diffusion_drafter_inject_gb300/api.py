@@ -39,23 +39,28 @@ def _ptr(t):
 
 
 class DeviceWeights:
-    """Drafter weights resident on the GPU and the dflash_weights struct that points at them."""
+    """Drafter weights resident on the GPU and the dflash_weights struct that points at
+    them (a weight missing from `tensors` is a NULL pointer: the calls that need it
+    refuse with DFLASH_ERR_NULL)."""
 
     def __init__(self, cfg, tensors):
         self.cfg = cfg
         self.t = tensors
         w = _lib.Weights()
+        ptr = lambda n: tensors[n].data_ptr() if n in tensors else None  # absent: NULL
         for n in ("fc_norm", "fc", "embed", "lm_head", "final_norm", "sel_pu", "sel_pv"):
-            setattr(w, n, tensors[n].data_ptr())
+            setattr(w, n, ptr(n))
         for l in range(cfg["n_layers"]):
             L = w.layer[l]
             p = f"layers.{l}."
             for n in ("attn_norm", "mlp_norm", "wqkv", "wo", "q_norm", "k_norm", "w_gate_up",
                       "w_down"):
-                setattr(L, n, tensors[p + n].data_ptr())
+                setattr(L, n, ptr(p + n))
             for i in range(4):
-                L.conv_w[i] = tensors[p + f"conv_w.{i}"].data_ptr()
-                L.conv_base[i] = tensors[p + f"conv_base.{i}"].data_ptr()
+                L.conv_w[i] = ptr(p + f"conv_w.{i}")
+                L.conv_base[i] = ptr(p + f"conv_base.{i}")
+        if "sel_gate" in tensors:
+            w.sel_gate = tensors["sel_gate"].data_ptr()
         self.struct = w
         self.sel_table = None  # see prepare_selector
 
@@ -178,6 +183,31 @@ def sample_path(cfg, W, anchor, topk_ids, topk_logp, K, uniforms, ws, path, path
                                    _ptr(uniforms), _ptr(path), _ptr(path_q), ws.ptr, ws.nbytes,
                                    _stream(stream)),
           "dflash_sample_path")
+
+
+def select_greedy(cfg, W, anchor, topk_ids, topk_logp, hidden, K, ws, path, score, stream=None):
+    """The pages' context-gated pair scores, walked greedily (dflash_select_greedy):
+    hidden [B, K-1, D] in the config dtype (e.g. draft_hidden after draft_block)."""
+    c = make_config(cfg)
+    check(lib().dflash_select_greedy(ctypes.byref(c), ctypes.byref(W.struct), _ptr(anchor),
+                                     _ptr(topk_ids), _ptr(topk_logp), _ptr(hidden),
+                                     int(anchor.shape[0]), int(K), _ptr(path), _ptr(score),
+                                     ws.ptr, ws.nbytes, _stream(stream)),
+          "dflash_select_greedy")
+
+
+def draft_hidden(cfg, B, K, ws):
+    """The final-normed hidden states [B, K-1, D] that the last draft_block left
+    in the workspace (a view of the workspace: valid until its next use)."""
+    c = make_config(cfg)
+    addr = lib().dflash_draft_hidden(ctypes.byref(c), int(B), int(K), ws.ptr, ws.nbytes)
+    if not addr:
+        raise ValueError("invalid arguments for dflash_draft_hidden")
+    es = 2 if cfg["dtype"] == "bf16" else 4
+    off = addr - ws.buf.data_ptr()
+    n = B * (K - 1) * cfg["d_model"]
+    view = ws.buf[off:off + n * es].view(_TORCH_DT[cfg["dtype"]])
+    return view.view(B, K - 1, cfg["d_model"])
 
 
 def accept_sample(path, topk_ids, path_q, target_logits, uniforms, ws, accept_len, tokens,

@@ -136,9 +136,9 @@ constexpr size_t kHeaderBytes = 256 + kTicketInts * 4 + kTopkTicketInts * 4;
 struct Layout {
   size_t status, tickets, scratch;
   size_t x, un, ub, rf, rb, gates, qkv, qb, kb, vb, ob, hb, zf, logits, attn, topk, topk_tickets;
-  size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf, rope, rope_inj;
+  size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf, rope, rope_inj, selgate;
   size_t total;
-  GemmPlan P_gate, P_qkv, P_o, P_gu, P_down, P_sel, P_sel2;
+  GemmPlan P_gate, P_qkv, P_o, P_gu, P_down, P_sel, P_sel2, P_hgate;
   AttnPlan ap;
 };
 
@@ -182,6 +182,7 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->P_down = reduce_plan(c, D, T, F, GEMM_REDUCE, sms);
   L->P_sel = reduce_plan(c, r, TR, D, GEMM_REDUCE, sms);
   L->P_sel2 = reduce_plan(c, 2 * r, TR, D, GEMM_REDUCE, sms);
+  L->P_hgate = reduce_plan(c, r, TL, D, GEMM_REDUCE, sms);
   L->ap = attn_plan(B, K, Hq, Hkv, dh, c->window, sms);
   // slice scratch shared by every reduce-mode GEMM (they run one after another)
   size_t sc = 0;
@@ -193,6 +194,7 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   sc = std::max(sc, reduce_scratch(c, D, T, F, L->P_down, GEMM_REDUCE));
   sc = std::max(sc, reduce_scratch(c, r, TR, D, L->P_sel, GEMM_REDUCE));
   sc = std::max(sc, reduce_scratch(c, 2 * r, TR, D, L->P_sel2, GEMM_REDUCE));
+  sc = std::max(sc, reduce_scratch(c, r, TL, D, L->P_hgate, GEMM_REDUCE));
   sc = std::max(sc, reduce_scratch(c, V, TL, D, GemmPlan{0, 1}, GEMM_REDUCE));
   // injection GEMMs: the split depends on the token count; take the largest
   auto inj = [&](int n_out, int k_in) {
@@ -238,6 +240,7 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->argmax = take((size_t)T * argmax_chunks(V) * 2 * 4);
   L->rope = take((size_t)T * (dh / 2) * 8);
   L->rope_inj = take((size_t)N * (dh / 2) * 8);
+  L->selgate = take((size_t)TL * r * 4);
   L->gn = take((size_t)N * TIN * es);
   L->cb = take((size_t)N * D * es);
   L->kvf = take((size_t)N * 2 * Hkv * dh * c->n_layers * 4);
@@ -511,6 +514,24 @@ static int run_sample(const dflash_config &c, const dflash_weights &w, const int
   return DFLASH_OK;
 }
 
+template <typename S>
+static int run_greedy(const dflash_config &c, const dflash_weights &w, const int32_t *anchor,
+                      const int32_t *ids, const float *logp, const void *hidden, int B, int K,
+                      int32_t *path, float *score, uint8_t *ws, const Layout &L,
+                      cudaStream_t st) {
+  const int D = c.d_model, r = c.sel_rank, TL = B * (K - 1);
+  int *err = (int *)(ws + L.status);
+  float *gate = (float *)(ws + L.selgate);
+  if (!w.sel_table) TRY(sel_project<S>(c, w, anchor, ids, B, K, ws, L, st));
+  // the context gate's pre-activations W_H h_t of every draft position
+  TRY(gemm_run(reduce_call(c, ws, L, w.sel_gate, r, D, hidden, TL, L.P_hgate, GEMM_REDUCE, gate,
+                           r, nullptr, 0),
+               st));
+  TRY(launch_greedy_walk((float *)(ws + L.U), (float *)(ws + L.Vp), ids, logp, B, K, c.top_k, r,
+                         w.sel_table, c.vocab, anchor, gate, path, score, err, st));
+  return DFLASH_OK;
+}
+
 }  // namespace dflh
 
 using namespace dflh;
@@ -629,6 +650,44 @@ int dflash_sample_path(const dflash_config *cfg, const dflash_weights *w, const 
                            (uint8_t *)ws, L, st);
 }
 
+int dflash_select_greedy(const dflash_config *cfg, const dflash_weights *w,
+                         const int32_t *anchor, const int32_t *topk_ids, const float *topk_logp,
+                         const void *hidden, int32_t B, int32_t K, int32_t *path,
+                         float *path_score, void *ws, size_t ws_bytes, void *stream) {
+  int rc = check_cfg(cfg);
+  if (rc != DFLASH_OK) return rc;
+  if (B < 0 || K < 2 || K > DFLASH_MAX_BLOCK) return DFLASH_ERR_BLOCK;
+  if (B == 0) return DFLASH_OK;
+  if ((size_t)B > kTopkTicketInts) return DFLASH_ERR_DIMS;
+  if (!w || !anchor || !topk_ids || !topk_logp || !hidden || !path || !path_score || !ws ||
+      !w->sel_gate)
+    return DFLASH_ERR_NULL;
+  if (!w->sel_table && (!w->embed || !w->sel_pu || !w->sel_pv)) return DFLASH_ERR_NULL;
+  if (w->sel_table ? !a16(w->sel_table)
+                   : (!a16(w->sel_pu) || !a16(w->sel_pv) || !a16(w->embed)))
+    return DFLASH_ERR_ALIGN;
+  if (!a16(w->sel_gate) || !a16(hidden) || !a16(ws)) return DFLASH_ERR_ALIGN;
+  Layout L;
+  make_layout(cfg, B, K, 0, &L);
+  if (ws_bytes < L.total) return DFLASH_ERR_WORKSPACE;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cfg->dtype == DFLASH_BF16)
+    return run_greedy<dfl::bf16>(*cfg, *w, anchor, topk_ids, topk_logp, hidden, B, K, path,
+                                 path_score, (uint8_t *)ws, L, st);
+  return run_greedy<float>(*cfg, *w, anchor, topk_ids, topk_logp, hidden, B, K, path, path_score,
+                           (uint8_t *)ws, L, st);
+}
+
+const void *dflash_draft_hidden(const dflash_config *cfg, int32_t B, int32_t K, const void *ws,
+                                size_t ws_bytes) {
+  if (check_cfg(cfg) != DFLASH_OK || !ws || B < 1 || K < 2 || K > DFLASH_MAX_BLOCK) return nullptr;
+  Layout L;
+  make_layout(cfg, B, K, 0, &L);
+  if (ws_bytes < L.total) return nullptr;
+  return (const uint8_t *)ws + L.zf;
+}
+
 int dflash_accept_sample(const int32_t *path, const int32_t *topk_ids, const float *path_q,
                          const void *target_logits, int32_t logits_dtype, int32_t B, int32_t K,
                          int32_t V, int32_t top_k, const float *uniforms, int32_t *accept_len,
@@ -699,6 +758,33 @@ int dflash_linear(int32_t dtype, const void *W, int32_t N_out, int32_t K_in, con
   if (!a16(W) || !a16(X)) return DFLASH_ERR_ALIGN;
   if (!device()) return DFLASH_ERR_DEVICE;
   return gemm_xwT(dtype, W, N_out, K_in, X, T, out, N_out, splits, nullptr, (cudaStream_t)stream);
+}
+
+int dflash_test_linear_wait(const void *W, int32_t N_out, int32_t K_in, const void *X, int32_t T,
+                            float *out, void *ws, size_t ws_bytes, uint32_t stall_wait_us,
+                            void *stream) {
+  if (N_out < 1 || T < 1 || K_in < 64 || K_in % 64) return DFLASH_ERR_DIMS;
+  if (!W || !X || !out || !ws) return DFLASH_ERR_NULL;
+  if (!a16(W) || !a16(X) || !a16(ws)) return DFLASH_ERR_ALIGN;
+  if (ws_bytes < 256) return DFLASH_ERR_WORKSPACE;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  GemmCall g;
+  g.dtype = DFLASH_BF16;
+  g.W = W;
+  g.N_out = N_out;
+  g.K_in = K_in;
+  g.X = X;
+  g.T = T;
+  g.S = 1;
+  g.mode = GEMM_PARTIAL;
+  g.out = out;
+  g.ld = N_out;
+  g.err = (int *)ws;  // the workspace's status word
+  if (stall_wait_us > 0) {
+    g.stall = 1;
+    g.wait_ns = (uint64_t)stall_wait_us * 1000ull;
+  }
+  return gemm_run(g, (cudaStream_t)stream);
 }
 
 int32_t dflash_linear_splits(int32_t N_out, int32_t T, int32_t K_in) {

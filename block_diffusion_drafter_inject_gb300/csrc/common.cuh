@@ -298,10 +298,11 @@ __device__ __forceinline__ bool mbar_try_wait_cl(uint64_t *bar, uint32_t parity)
   return ok != 0;
 }
 // Bounded wait on phase `parity` (CL: cluster-scope acquire).  Returns false
-// (and raises *abort) when the wait gives up, or when another role already
-// raised *abort.
+// (and raises *abort) when the wait gives up after limit_ns, or when another
+// role already raised *abort.
 template <bool CL = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   auto tw = [&]() { return CL ? mbar_try_wait_cl(bar, parity) : mbar_try_wait(bar, parity); };
   if (tw()) return true;
   const uint64_t t0 = globaltimer();
@@ -309,7 +310,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     if (tw()) return true;
     if ((it & 31) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }

@@ -69,6 +69,10 @@ struct GemmParams {
   // tile order: weight tile fastest (activations too large to re-read per
   // weight tile) instead of token tile fastest
   int m_fastest;
+  // limit of the pipeline's bounded waits; stall (failure-path test only): the
+  // MMA issuer first waits on a barrier that nothing arrives on
+  uint64_t wait_ns;
+  int stall;
 };
 
 // One CTA's share of one tile: k-blocks [kb0, kb0 + nkb), slice `seg` of the
@@ -293,7 +297,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 2;
   uint64_t *drain = tempty + 2;
-  uint32_t *tmem_slot = (uint32_t *)(drain + 1);
+  uint64_t *stallbar = drain + 1;
+  uint32_t *tmem_slot = (uint32_t *)(stallbar + 1);
   volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -309,6 +314,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&tempty[a], 4 * kEpiGroups);
     }
     mbar_init(drain, 1);
+    mbar_init(stallbar, 1);
     *abort_flag = 0;
     mbar_fence_init();
     for (int g = 0; g * p.mtg < p.m_tiles && g < kMaxGroups; ++g) tma_prefetch_desc(&tmW.m[g]);
@@ -360,7 +366,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (n < pre) {
             tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, sg.t_tile * BN, pol_x);
           } else {
-            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -373,8 +379,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (++stage == STAGES) stage = 0, phase ^= 1;
         }
       }
-      if (!ok) {
-        // give up: let the copies already issued land before shared memory is released
+      // every copy this warp issued has landed before shared memory is released
+      // (already so when the MMA issuer consumed them; not when a wait gave up)
+      {
         volatile int dummy = 0;
         for (int s = 0; s < STAGES; ++s)
           if (issued[s]) mbar_wait(&full[s], last_phase[s], (volatile int *)&dummy);
@@ -391,16 +398,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      if (p.stall && !mbar_wait(stallbar, 0, abort_flag, p.wait_ns)) ok = false;
       Seg sg;
       for (int i = 0; ok && get_seg(p, i, sg); ++i) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < sg.nkb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -446,7 +454,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     Seg sg;
     for (int i = 0; get_seg(p, i, sg); ++i) {
       const int m_tile = sg.m_tile, t_tile = sg.t_tile, split = sg.seg;
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) break;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.wait_ns)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       const int tcol0 = t_tile * BN;
@@ -887,6 +895,8 @@ static int make_params(const GemmCall &g, int BN, int num_sms, dfl::GemmParams &
   p.total = 0;
   p.nmax = g.S;
   p.m_fastest = (double)g.T * g.K_in * 2 > kMFastestActBytes ? 1 : 0;
+  p.wait_ns = g.wait_ns > 0 ? g.wait_ns : dfl::kWaitLimitNs;
+  p.stall = g.stall;
   int grid = p.num_units < num_sms ? p.num_units : num_sms;
   if (g.chunk > 0) {
     const long total = (long)p.m_tiles * p.t_tiles * p.kb_total;

@@ -61,6 +61,11 @@ struct GemmCall {
   const float2 *rope_cs = nullptr;
   int Hq = 0, Hkv = 0, dh = 0;
   float eps = 0.f;
+  // limit of the kernel's bounded waits (0: the default, kWaitLimitNs); stall
+  // (failure-path test only, bf16): the MMA issuer first waits on a barrier
+  // that nothing arrives on, so that the wait gives up
+  uint64_t wait_ns = 0;
+  int stall = 0;
 };
 
 // Floats of slice scratch a reduce-mode GEMM needs (0 when S == 1 and chunk == 0).

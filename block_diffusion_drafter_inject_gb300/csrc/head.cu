@@ -577,11 +577,16 @@ __device__ __forceinline__ int draw_inv_cdf(const float *w, int n, float u, floa
 // [B*R][r], R = 1 + (K-1)*k: anchor first, then the candidates by position and
 // rank); q_t = softmax(s) is written out and one candidate is drawn with the
 // uniform uw[b][t].  prev = the token drawn at t-1 (the anchor at t = 0).
+//
+// Greedy mode (uw == nullptr): the walk takes argmax_j s_j (the lower rank on
+// ties) and score[b] receives the summed chosen scores.  gate (optional,
+// [B*(K-1)][r] pre-activations): the predecessor's projection is multiplied by
+// sigmoid(gate row of position t) before the dot products (the context gate).
 __global__ void __launch_bounds__(256) k_sample_walk(
     const float *__restrict__ U, const float *__restrict__ Vp, const int32_t *__restrict__ ids,
     const float *__restrict__ logp, int K, int k, int r, const float *__restrict__ tab, int V,
     const int32_t *__restrict__ anchor, const float *__restrict__ uw, int32_t *__restrict__ path,
-    float *__restrict__ pq, int *err) {
+    float *__restrict__ pq, const float *__restrict__ gate, float *__restrict__ score, int *err) {
   extern __shared__ float sw[];
   float *up = sw;  // [r] projection of the predecessor
   __shared__ float sc[DFLASH_MAX_TOPK];
@@ -600,9 +605,12 @@ __global__ void __launch_bounds__(256) k_sample_walk(
     s_row = 0;
   }
   __syncthreads();
+  float total = 0.f;  // greedy: summed chosen scores (thread 0)
   for (int t = 0; t < T; ++t) {
     const float *usrc = tab ? tab + (size_t)s_tok * r : U + ((size_t)b * R + s_row) * r;
-    for (int i = threadIdx.x; i < r; i += blockDim.x) up[i] = usrc[i];
+    const float *grow = gate ? gate + ((size_t)b * T + t) * r : nullptr;
+    for (int i = threadIdx.x; i < r; i += blockDim.x)
+      up[i] = grow ? usrc[i] * (1.f / (1.f + expf(-grow[i]))) : usrc[i];
     __syncthreads();
     const size_t cb = ((size_t)b * T + t) * k;
     for (int j = warp; j < k; j += nw) {
@@ -619,15 +627,23 @@ __global__ void __launch_bounds__(256) k_sample_walk(
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      float m = -INFINITY;
-      for (int j = 0; j < k; ++j) m = fmaxf(m, sc[j]);
-      float e[DFLASH_MAX_TOPK], tot = 0.f;
-      for (int j = 0; j < k; ++j) {
-        e[j] = expf(sc[j] - m);
-        tot += e[j];
+      int jd = 0;
+      if (uw) {
+        float m = -INFINITY;
+        for (int j = 0; j < k; ++j) m = fmaxf(m, sc[j]);
+        float e[DFLASH_MAX_TOPK], tot = 0.f;
+        for (int j = 0; j < k; ++j) {
+          e[j] = expf(sc[j] - m);
+          tot += e[j];
+        }
+        for (int j = 0; j < k; ++j) pq[cb + j] = e[j] / tot;
+        jd = draw_inv_cdf(e, k, uw[(size_t)b * T + t], tot);
+      } else {
+        for (int j = 1; j < k; ++j)
+          if (sc[j] > sc[jd]) jd = j;
+        total += sc[jd];
+        if (t == T - 1) score[b] = total;
       }
-      for (int j = 0; j < k; ++j) pq[cb + j] = e[j] / tot;
-      const int jd = draw_inv_cdf(e, k, uw[(size_t)b * T + t], tot);
       int c = ids[cb + jd];
       c = c < 0 ? 0 : c >= V ? V - 1 : c;
       path[(size_t)b * T + t] = c;
@@ -908,7 +924,19 @@ int launch_sample_walk(const float *U, const float *Vp, const int32_t *topk_ids,
                        int *err, cudaStream_t st) {
   const size_t smem = sizeof(float) * (size_t)r;
   DFL_CHECK_LAUNCH(launch(dfl::k_sample_walk, dim3(B), dim3(256), smem, st, U, Vp, topk_ids,
-                          topk_logp, K, k, r, tab, V, anchor, uniforms, path, path_q, err));
+                          topk_logp, K, k, r, tab, V, anchor, uniforms, path, path_q,
+                          (const float *)nullptr, (float *)nullptr, err));
+  return DFLASH_OK;
+}
+
+int launch_greedy_walk(const float *U, const float *Vp, const int32_t *topk_ids,
+                       const float *topk_logp, int B, int K, int k, int r, const float *tab, int V,
+                       const int32_t *anchor, const float *gate, int32_t *path, float *score,
+                       int *err, cudaStream_t st) {
+  const size_t smem = sizeof(float) * (size_t)r;
+  DFL_CHECK_LAUNCH(launch(dfl::k_sample_walk, dim3(B), dim3(256), smem, st, U, Vp, topk_ids,
+                          topk_logp, K, k, r, tab, V, anchor, (const float *)nullptr, path,
+                          (float *)nullptr, gate, score, err));
   return DFLASH_OK;
 }
 

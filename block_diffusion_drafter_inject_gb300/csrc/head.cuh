@@ -41,6 +41,13 @@ int launch_sample_walk(const float *U, const float *Vp, const int32_t *topk_ids,
                        const int32_t *anchor, const float *uniforms, int32_t *path, float *path_q,
                        int *err, cudaStream_t st);
 
+// Greedy walk over the pair scores with the context gate: gate [B*(K-1)][r]
+// pre-activations (sigmoid applied here), or nullptr; score [B].
+int launch_greedy_walk(const float *U, const float *Vp, const int32_t *topk_ids,
+                       const float *topk_logp, int B, int K, int k, int r, const float *tab, int V,
+                       const int32_t *anchor, const float *gate, int32_t *path, float *score,
+                       int *err, cudaStream_t st);
+
 // Speculative rejection sampling; uniforms [B][K][2]; scratch of
 // accept_sample_floats(B, K, V) floats.
 size_t accept_sample_floats(int B, int K, int V);

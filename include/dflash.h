@@ -127,6 +127,9 @@ typedef struct dflash_weights {
    * written by dflash_prepare_selector; NULL: dflash_select_path gathers the
    * candidates' embedding rows and projects them on every call */
   const float *sel_table;
+  /* optional: [r, D] W_H of the context gate H(h) = sigmoid(W_H h) of the
+   * gated selector (dflash_select_greedy); unused by the other calls */
+  const void *sel_gate;
 } dflash_weights;
 
 /* Paged per-layer draft KV cache.
@@ -245,6 +248,32 @@ int dflash_sample_path(const dflash_config *cfg, const dflash_weights *w, const 
                        const float *uniforms, int32_t *path, float *path_q, void *ws,
                        size_t ws_bytes, void *stream);
 
+/* The pages' selector form with its greedy walk (Architecture page, "Problem
+ * 1", eq. S_t, and "greedy follows the best successor"):
+ *   S_t(a, b) = logp_t(b) + < (P_u e_a) * sigmoid(W_H h_t), P_v e_b >
+ * with h_t the drafter's final-normed hidden state of draft position t (the
+ * lm_head's input; dflash_draft_hidden gives the rows the last draft pass left
+ * in the workspace) and W_H = w->sel_gate; from the anchor each position takes
+ * the candidate of largest S_t given the token taken before it (the lower
+ * rank on ties).  logp in place of the raw logit shifts every S_t by the same
+ * amount per position, so the walk is the same.
+ *   hidden      device [B, K-1, D] in the config dtype, 16-byte aligned
+ *   path        device int32 [B, K-1] out;  path_score device f32 [B] out: sum
+ *               of the chosen S_t.  Other arguments, workspace and errors as
+ *               for dflash_select_path; w->sel_gate is required. */
+int dflash_select_greedy(const dflash_config *cfg, const dflash_weights *w,
+                         const int32_t *anchor, const int32_t *topk_ids, const float *topk_logp,
+                         const void *hidden, int32_t B, int32_t K, int32_t *path,
+                         float *path_score, void *ws, size_t ws_bytes, void *stream);
+
+/* Device address, inside `ws`, of the final-normed hidden states [B*(K-1), D]
+ * (config dtype; request b's draft position t at row b*(K-1) + t-1) that the
+ * last dflash_draft_block on this workspace wrote, valid until the next call
+ * that uses the workspace; NULL for invalid arguments.  Reads nothing on the
+ * device. */
+const void *dflash_draft_hidden(const dflash_config *cfg, int32_t B, int32_t K, const void *ws,
+                                size_t ws_bytes);
+
 /* Lossless speculative rejection sampling (Architecture page, "Speculative
  * Decoding Context": rejection sampling makes the scheme lossless; "Problem 1":
  * it restores the exact target distribution).  Row i of the target logits
@@ -308,6 +337,22 @@ int dflash_accept_greedy_noalloc(const int32_t *path, const void *target_logits,
 int dflash_linear(int32_t dtype, const void *W, int32_t N_out, int32_t K_in, const void *X,
                   int32_t T, int32_t splits, float *out, void *stream);
 int32_t dflash_linear_splits(int32_t N_out, int32_t T, int32_t K_in);
+
+/* Test hook for the failure-detection path of the projection GEMM (no
+ * counterpart in the pages).  Every on-chip wait of the GEMM is bounded: when
+ * one runs out, the kernel stops issuing, waits for the copies and matrix
+ * operations it already issued, frees its tensor memory, sets
+ * DFLASH_DEV_TIMEOUT in the status word and returns, leaving the context
+ * usable.  This call runs dflash_linear's GEMM (bf16, one K slice:
+ * out[t][n] = sum_k X[t][k] W[n][k]) with its status word at the start of
+ * `ws`.  With stall_wait_us > 0 the tensor-core issuer first waits on a
+ * barrier that nothing arrives on, with every wait of the launch limited to
+ * stall_wait_us microseconds, so that the give-up path runs and out is not
+ * written; with 0 it is an ordinary launch.  W [N_out, K_in], X [T, K_in]
+ * bf16, 16-byte aligned; out f32 [T, N_out]; ws at least 256 bytes, zeroed. */
+int dflash_test_linear_wait(const void *W, int32_t N_out, int32_t K_in, const void *X, int32_t T,
+                            float *out, void *ws, size_t ws_bytes, uint32_t stall_wait_us,
+                            void *stream);
 
 /* Waits for `stream`, then returns the sticky device status bits (>= 0) of
  * the workspace, or a negative DFLASH_ERR_* code. */

@@ -33,4 +33,7 @@ from .dflash import (  # noqa: F401
     sample_path_request,
     accept_sample,
     accept_sample_request,
+    context_gate,
+    select_greedy,
+    select_greedy_request,
 )

@@ -272,7 +272,7 @@ def draft_block_request(cfg, W, ctx_k, ctx_v, anchor, ctx_len, K, contract="bf16
     zf = R(rmsnorm(x[1:], W["final_norm"], eps))
     logits = zf @ np.asarray(W["lm_head"], dtype=F64).T
     del D
-    return dict(logits=logits, hidden=x)
+    return dict(logits=logits, hidden=x, zf=zf)
 
 
 def draft_block(cfg, W, ctx_k, ctx_v, anchors, ctx_lens, K, contract="bf16"):
@@ -280,7 +280,8 @@ def draft_block(cfg, W, ctx_k, ctx_v, anchors, ctx_lens, K, contract="bf16"):
 
     ctx_k[b][l], ctx_v[b][l]: dense injected K/V of request b.
     Returns dict(logits [B, K-1, V], ids [B, K-1, k], logp [B, K-1, k],
-    lse [B, K-1])."""
+    lse [B, K-1], zf [B, K-1, D]: the final-normed hidden states of slots
+    1..K-1, the input of the lm_head)."""
     B = len(anchors)
     k = cfg["top_k"]
     V = cfg["vocab"]
@@ -288,13 +289,15 @@ def draft_block(cfg, W, ctx_k, ctx_v, anchors, ctx_lens, K, contract="bf16"):
     ids = np.zeros((B, K - 1, k), dtype=np.int32)
     logp = np.zeros((B, K - 1, k))
     lse = np.zeros((B, K - 1))
+    zf = np.zeros((B, K - 1, cfg["d_model"]))
     for b in range(B):
         out = draft_block_request(cfg, W, ctx_k[b], ctx_v[b], anchors[b], int(ctx_lens[b]), K,
                                   contract)
         logits[b] = out["logits"]
+        zf[b] = out["zf"]
         for t in range(K - 1):
             ids[b, t], logp[b, t], lse[b, t] = topk_logp(logits[b, t], k)
-    return dict(logits=logits, ids=ids, logp=logp, lse=lse)
+    return dict(logits=logits, ids=ids, logp=logp, lse=lse, zf=zf)
 
 
 # ----------------------------------------------------------------------------
@@ -526,3 +529,70 @@ def accept_sample(path, cand_ids, q, T, u):
     for b in range(B):
         acc[b], toks[b] = accept_sample_request(path[b], cand_ids[b], q[b], T[b], u[b])
     return acc, toks
+
+
+# ----------------------------------------------------------------------------
+# the pages' selector form: context-gated pair scores, greedy walk
+# ----------------------------------------------------------------------------
+
+def context_gate(Wh, h):
+    """H(h_t) = sigmoid(W_H h_t): the context gate of eq. S_t (Architecture page,
+    "Problem 1": H(h_t) decides which parts of the predecessor match count).
+    The form of H is a reading of this build (the pages name only its role):
+    one linear map of the drafter's hidden state, then per-dimension sigmoid.
+    Wh [r, D]; h [T, D]  ->  [T, r]."""
+    return sigmoid(np.asarray(h, dtype=F64) @ np.asarray(Wh, dtype=F64).T)
+
+
+def select_greedy_request(E, Pu, Pv, Wh, h, anchor, ids, logp, with_margin=False,
+                          step_margins=False):
+    """Greedy walk over the context-gated pair scores of one request.
+
+    Architecture page, "Problem 1", eq. S_t:
+        S_t(a, b) = U_t(b) + < A(a) * H(h_t), B(b) >
+    with A(a) = P_u e_a, B(b) = P_v e_b (compact r-dim token embeddings), H the
+    context gate of the drafter hidden state h_t of position t (context_gate),
+    and U_t(b) the drafter's score of candidate b (the log-probability here:
+    it differs from the logit by a per-position constant, which moves neither
+    the walk nor the comparison of paths).  "Greedy follows the best
+    successor": from the anchor, position t takes argmax_b S_t(a_{t-1}, b) over
+    its candidates (ties: lower rank).  ids, logp [T, k]; h [T, D].  Returns
+    (path [T], score = sum of the chosen S_t) and, with with_margin, the
+    smallest gap between the chosen and the runner-up score over the steps
+    (with step_margins, the gap of every step [T] instead)."""
+    E = np.asarray(E)
+    Pu = np.asarray(Pu, dtype=F64)
+    Pv = np.asarray(Pv, dtype=F64)
+    T, k = ids.shape
+    g = context_gate(Wh, h)
+    emb = lambda t: np.asarray(E[int(t)], dtype=F64)
+    prev = int(anchor)
+    path = np.zeros(T, dtype=np.int32)
+    score, margin = 0.0, np.inf
+    gaps = np.full(T, np.inf)
+    for t in range(T):
+        ug = (Pu @ emb(prev)) * g[t]
+        s = np.array([float(logp[t][j]) + ug @ (Pv @ emb(ids[t][j])) for j in range(k)])
+        j = int(np.argmax(s))                      # first maximum = lowest rank
+        if k > 1:
+            gaps[t] = float(s[j] - np.max(np.delete(s, j)))
+            margin = min(margin, gaps[t])
+        path[t] = ids[t][j]
+        score += float(s[j])
+        prev = int(path[t])
+    if with_margin:
+        return path, score, (gaps if step_margins else margin)
+    return path, score
+
+
+def select_greedy(cfg, W, anchors, ids, logp, hidden):
+    """Batch form: hidden [B, K-1, D].  Returns path [B, K-1], score [B], margin [B]."""
+    B, T, _ = ids.shape
+    path = np.zeros((B, T), dtype=np.int32)
+    score = np.zeros(B)
+    margin = np.zeros(B)
+    for b in range(B):
+        path[b], score[b], margin[b] = select_greedy_request(
+            W["embed"], W["sel_pu"], W["sel_pv"], W["sel_gate"], hidden[b], anchors[b], ids[b],
+            logp[b], with_margin=True)
+    return path, score, margin

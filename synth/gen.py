@@ -81,6 +81,7 @@ def weight_names(cfg):
         ("final_norm", (D,), "gain"),
         ("sel_pu", (r, D), "sel"),
         ("sel_pv", (r, D), "sel"),
+        ("sel_gate", (r, D), "sel"),
     ]
     for l in range(cfg["n_layers"]):
         p = f"layers.{l}."

@@ -177,3 +177,52 @@ def test_accept_sample_is_lossless_on_device():
     assert stat <= chi2.ppf(1.0 - 1e-4, len(counts) - 1), stat
     a = acc.cpu().numpy()
     assert a.min() == 1 and len(set(a.tolist())) >= 3   # rejections and several accepted lengths
+
+
+@pytest.mark.parametrize("name,B,K,table", [("tiny_bf16", 3, 8, False), ("small", 2, 16, True),
+                                             ("tiny", 2, 8, False), ("small_gqa", 2, 8, True)])
+def test_select_greedy_matches_oracle(name, B, K, table):
+    """The context-gated greedy walk on the oracle's candidates and hidden states:
+    each path bit-exact up to its first step whose gap (best minus runner-up
+    score) is 1e-2 or less, and the score within 1e-3 where no step is."""
+    import block_diffusion_drafter_inject_gb300 as dfl
+    c = Case(name, B, K, [40 + 9 * b for b in range(B)], seed=60 + B + K).device()
+    if table:
+        dfl.prepare_selector(c.cfg, c.Wd, c.cyc.ws)
+    o = c.oracle()
+    path_o, score_o, margin_o = oracle.select_greedy(c.cfg, c.W, c.anchor, o["ids"], o["logp"],
+                                                     o["zf"])
+    dt = torch.bfloat16 if c.cfg["dtype"] == "bf16" else torch.float32
+    hidden = torch.from_numpy(o["zf"].astype(np.float32)).to(dt).cuda()
+    path = torch.zeros((B, K - 1), dtype=torch.int32, device="cuda")
+    score = torch.zeros(B, dtype=torch.float32, device="cuda")
+    dfl.select_greedy(c.cfg, c.Wd, c.d_anchor, torch.from_numpy(o["ids"]).cuda(),
+                      torch.from_numpy(o["logp"].astype(np.float32)).cuda(), hidden, K, c.cyc.ws,
+                      path, score)
+    torch.cuda.synchronize()
+    assert dfl.read_device_status(c.cyc.ws) == 0
+    path, score = path.cpu().numpy(), score.cpu().numpy()
+    compared = 0
+    for b in range(B):
+        _, _, gaps = oracle.select_greedy_request(
+            c.W["embed"], c.W["sel_pu"], c.W["sel_pv"], c.W["sel_gate"], o["zf"][b], c.anchor[b],
+            o["ids"][b], o["logp"][b], with_margin=True, step_margins=True)
+        for t in range(K - 1):
+            if gaps[t] <= 1e-2:
+                break                          # later steps follow another predecessor
+            assert path[b, t] == path_o[b, t], (b, t)
+            compared += 1
+        if np.all(gaps > 1e-2):
+            assert abs(score[b] - score_o[b]) < 1e-3 * max(1.0, abs(score_o[b])), b
+    assert compared >= B
+
+
+def test_draft_hidden_is_the_lm_head_input():
+    """dflash_draft_hidden: the final-normed rows the draft pass left in the
+    workspace match the oracle's (row-max relative, the logits' tolerance)."""
+    import block_diffusion_drafter_inject_gb300 as dfl
+    from _cases import rowmax_rel
+    c = Case("small", 2, 8, [70, 33], seed=12).device()
+    c.run_device()
+    h = dfl.draft_hidden(c.cfg, c.B, c.K, c.cyc.ws).float().cpu().numpy()
+    assert rowmax_rel(h, c.oracle()["zf"]) < 2e-2

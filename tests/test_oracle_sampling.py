@@ -198,3 +198,57 @@ def test_lossless_check_detects_a_biased_sampler(monkeypatch):
     p /= p.sum()
     assert not chi2_ok(counts[0], p)[0]
     monkeypatch.setattr(oracle, "accept_sample_request", orig)
+
+
+# ---------------------------------------------------------------- context-gated greedy selector
+
+def test_gated_greedy_hand_fixture():
+    import json
+    import os
+    fx = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "selector_gate_hand.json")))
+    path, score, margin = oracle.select_greedy_request(
+        np.array(fx["embed"]), np.array(fx["P_u"]), np.array(fx["P_v"]), np.array(fx["W_H"]),
+        np.array(fx["hidden"]), fx["anchor"], np.array(fx["ids"]), np.array(fx["logp"]),
+        with_margin=True)
+    assert list(path) == fx["expected_path"]
+    assert score == pytest.approx(fx["expected_score"], abs=1e-12)
+    assert margin == pytest.approx(fx["expected_margin"], abs=1e-12)
+
+
+def test_gated_greedy_single_step_equals_viterbi_with_open_gate():
+    """One draft position and a gate saturated open: the greedy step is the
+    best path, which the brute-force-pinned Viterbi finds."""
+    g = np.random.default_rng(8)
+    for trial in range(20):
+        E, Pu, Pv, ids, logp = _lattice(g, 1, 16, 40, D=6, r=4)
+        Wh = np.full((4, 6), 0.0)
+        Wh[:, 0] = 80.0
+        h = np.zeros((1, 6))
+        h[0, 0] = 1.0
+        pg, sg = oracle.select_greedy_request(E, Pu, Pv, Wh, h, 5, ids, logp)
+        pv, sv = oracle.select_path_request(E, Pu, Pv, 5, ids, logp)
+        assert list(pg) == list(pv) and sg == pytest.approx(sv, rel=1e-12, abs=1e-12)
+
+
+def test_gated_greedy_without_pair_term_is_per_position_argmax():
+    g = np.random.default_rng(9)
+    E, _, _, ids, logp = _lattice(g, 5, 8, 60, D=6, r=4)
+    Z = np.zeros((4, 6))
+    path, _ = oracle.select_greedy_request(E, Z, Z, g.standard_normal((4, 6)),
+                                           g.standard_normal((5, 6)), 3, ids, logp)
+    np.testing.assert_array_equal(path, [ids[t][int(np.argmax(logp[t]))] for t in range(5)])
+
+
+def test_gated_greedy_never_beats_viterbi_with_open_gate():
+    """Viterbi maximises the summed pair scores; the greedy walk's total can only
+    match or trail it (gate saturated open, so both score the same function)."""
+    g = np.random.default_rng(10)
+    for trial in range(20):
+        E, Pu, Pv, ids, logp = _lattice(g, 4, 4, 30, D=6, r=4)
+        Wh = np.zeros((4, 6))
+        Wh[:, 0] = 80.0
+        h = np.zeros((4, 6))
+        h[:, 0] = 1.0
+        _, sg = oracle.select_greedy_request(E, Pu, Pv, Wh, h, 1, ids, logp)
+        _, sv = oracle.select_path_request(E, Pu, Pv, 1, ids, logp)
+        assert sg <= sv + 1e-12
