@@ -274,6 +274,7 @@ static GemmCall reduce_call(const dflash_config &c, uint8_t *ws, const Layout &L
   g.T = T;
   g.S = S;
   g.chunk = plan.chunk;
+  g.pair = plan.pair;
   g.mode = mode;
   g.out = (float *)(ws + L.scratch);
   g.out_f32 = out_f32;

@@ -236,6 +236,12 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, ui
       "r"(src), "r"(bytes), "r"(mbar)
       : "memory");
 }
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t local_addr, uint32_t rank) {
+  uint32_t ra, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
 __device__ __forceinline__ float ld_dsmem(uint32_t local_addr, uint32_t rank) {
   uint32_t ra;
   float v;
@@ -393,6 +399,60 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
           smem_u32(bar))
       : "memory");
 }
+// ---- two-SM tensor-core tiles (a CTA pair of a 2-CTA cluster) ----
+// Tensor memory of the pair: one warp of each CTA allocates, relinquishes and
+// frees together, and both get the same columns.
+__device__ __forceinline__ void tc2_alloc(uint32_t *slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc2_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc2_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// D (+)= A * B^T over the pair, issued by one thread of the even CTA: A's rows
+// 0..M/2-1 come from that CTA's shared memory and rows M/2..M-1 from its
+// peer's (same offsets); B's N columns likewise half from each; each CTA's
+// tensor memory receives its M/2 rows of D.
+__device__ __forceinline__ void tc2_mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once the pair
+// MMAs issued so far by this thread have completed
+__device__ __forceinline__ void tc2_commit_mc(uint64_t *bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+// 2-D tiled TMA load into this CTA's shared memory whose completion is counted
+// on an mbarrier of either CTA of the pair (given by its cluster address)
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m, uint32_t mbar_cl,
+                                                 int x, int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(mbar_cl), "l"(policy)
+      : "memory");
+}
+// arrive (release at cluster scope) on an mbarrier given by its cluster address
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 // 32 lanes x 16 consecutive fp32 columns of tensor memory
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float *v) {
   uint32_t r[16];

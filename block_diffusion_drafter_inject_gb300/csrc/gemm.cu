@@ -73,6 +73,8 @@ struct GemmParams {
   // MMA issuer first waits on a barrier that nothing arrives on
   uint64_t wait_ns;
   int stall;
+  // two-SM tiles (k_gemm_tc2): work units are over pairs of weight tiles
+  int pair;
 };
 
 // One CTA's share of one tile: k-blocks [kb0, kb0 + nkb), slice `seg` of the
@@ -562,6 +564,355 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Two-SM tiles for wide token tiles
+// ---------------------------------------------------------------------------
+// A cluster of two CTAs on two SMs computes a 256-row x 256-token tile with
+// tcgen05.mma.cta_group::2: CTA rank r holds weight tile 2*mp + r (its 128
+// rows) and the r-th 128 tokens of the token tile in shared memory, each MMA
+// reads A and B halves from both CTAs, and each CTA's tensor memory receives
+// its 128 rows x 256 tokens.  Per SM a k-block then moves 32 KB for 4.2 MFLOP
+// (a one-SM 128 x 256 tile moves 48 KB), so six stages fit where four did.
+//   warp 0     TMA producer of this CTA's halves; both CTAs' loads of a stage
+//              complete on the even CTA's full barrier (TMA with cta_group::2),
+//              which the even producer arms for both CTAs' bytes
+//   warp 1     even CTA: waits for full stages, issues the pair MMAs and commits
+//              them to both CTAs' empty / tfull barriers (odd CTA: idle)
+//   warps 2-9  epilogue of this CTA's rows, as in k_gemm_tc; they release an
+//              accumulator on the even CTA's tempty barrier
+// The two CTAs walk the same units (pair tile, token tile, K slice) in lockstep.
+// Before leaving, the even CTA waits (bounded) on its full barriers for the
+// last stage each CTA issued, so that no copy into either CTA is in flight.
+constexpr int kPairBN = 256;
+struct PairShape {
+  static constexpr int A_BYTES = BM * BK * 2;             // this CTA's 128 weight rows
+  static constexpr int B_BYTES = (kPairBN / 2) * BK * 2;  // this CTA's 128 tokens
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = 6;
+  static constexpr int TMEM_COLS = 2 * kPairBN;  // two accumulators of 256 columns
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 512 /*barriers*/;
+};
+
+// The i-th unit of this CTA's pair (uniform schedule over pair tiles).
+__device__ __forceinline__ bool get_seg_pair(const GemmParams &p, int i, uint32_t rank, Seg &s) {
+  const int u = (int)(blockIdx.x >> 1) + i * (int)(gridDim.x >> 1);
+  if (u >= p.num_units) return false;
+  const int split = u % p.S, tile = u / p.S, mpairs = p.m_tiles >> 1;
+  int mp, t;
+  if (p.m_fastest) {
+    mp = tile % mpairs;
+    t = tile / mpairs;
+  } else {
+    t = tile % p.t_tiles;
+    mp = tile / p.t_tiles;
+  }
+  s.m_tile = 2 * mp + (int)rank;
+  s.t_tile = t;
+  s.kb0 = split * p.kb_per_split;
+  s.nkb = p.kb_per_split;
+  s.seg = split;
+  s.nseg = p.S;
+  return true;
+}
+
+// load_w with the completion counted on the even CTA's barrier (cluster address)
+__device__ __forceinline__ void load_w_pair(uint8_t *dst, const WMaps &maps, uint32_t bar_cl,
+                                            int kx, int m_tile, const GemmParams &p,
+                                            uint64_t pol) {
+  if (p.mode == 2) {
+    tma_load_2d_pair(dst, &maps.m[0], bar_cl, kx, m_tile * 64, pol);
+    tma_load_2d_pair(dst + 64 * BK * 2, &maps.m[0], bar_cl, kx, p.F + m_tile * 64, pol);
+  } else {
+    const int g = m_tile / p.mtg;
+    tma_load_2d_pair(dst, &maps.m[g], bar_cl, kx, (m_tile - g * p.mtg) * BM, pol);
+  }
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_gemm_tc2(const __grid_constant__ WMaps tmW, const __grid_constant__ CUtensorMap tmX,
+               GemmParams p) {
+  using SH = PairShape;
+  constexpr int STAGES = SH::STAGES, BN = kPairBN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t *full = (uint64_t *)(smem + STAGES * SH::STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *drain = tempty + 2;
+  uint32_t *tmem_slot = (uint32_t *)(drain + 1);
+  volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool even = rank == 0;
+  // the producer's issue record (per stage: issued, last phase), read by the even
+  // CTA before the pair leaves
+  __shared__ uint32_t s_issued[STAGES], s_lphase[STAGES];
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);  // the even CTA's: armed by its producer for both CTAs' bytes
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * 4 * kEpiGroups);  // the epilogue warps of both CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+    for (int g = 0; g * p.mtg < p.m_tiles && g < kMaxGroups; ++g) tma_prefetch_desc(&tmW.m[g]);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) {
+    tc2_alloc(tmem_slot, SH::TMEM_COLS);
+    tc2_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers and tensor memory exist before any traffic between them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_launch();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (this CTA's halves) ----------------
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      const int xrow = (int)rank * (BN / 2);
+      const uint32_t full0 = cluster_addr(smem_u32(&full[0]), 0);  // the even CTA's
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t last_phase[STAGES];
+      bool issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = false, last_phase[s] = 0;
+      int pre = 0;
+      {
+        int cnt = 0;
+        Seg sg;
+        for (int i = 0; cnt < STAGES && get_seg_pair(p, i, rank, sg); ++i) {
+          for (int kb = 0; kb < sg.nkb && cnt < STAGES; ++kb, ++cnt) {
+            if (even) mbar_expect_tx(&full[cnt], 2 * SH::STAGE_BYTES);
+            load_w_pair(smem + cnt * SH::STAGE_BYTES, tmW, full0 + (uint32_t)(cnt * 8),
+                        (sg.kb0 + kb) * BK, sg.m_tile, p, pol_w);
+          }
+        }
+        pre = cnt;
+      }
+      pdl_wait();
+      bool ok = true;
+      int n = 0;
+      Seg sg;
+      for (int i = 0; ok && get_seg_pair(p, i, rank, sg); ++i) {
+        for (int kb = 0; kb < sg.nkb; ++kb, ++n) {
+          uint8_t *sa = smem + stage * SH::STAGE_BYTES;
+          const int kx = (sg.kb0 + kb) * BK;
+          const uint32_t fb = full0 + (uint32_t)(stage * 8);
+          if (n < pre) {
+            tma_load_2d_pair(sa + SH::A_BYTES, &tmX, fb, kx, sg.t_tile * BN + xrow, pol_x);
+          } else {
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+            if (even) mbar_expect_tx(&full[stage], 2 * SH::STAGE_BYTES);
+            load_w_pair(sa, tmW, fb, kx, sg.m_tile, p, pol_w);
+            tma_load_2d_pair(sa + SH::A_BYTES, &tmX, fb, kx, sg.t_tile * BN + xrow, pol_x);
+          }
+          issued[stage] = true;
+          last_phase[stage] = phase;
+          if (++stage == STAGES) stage = 0, phase ^= 1;
+        }
+      }
+      for (int s = 0; s < STAGES; ++s) s_issued[s] = issued[s] ? 1u : 0u, s_lphase[s] = last_phase[s];
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    pdl_wait();
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      Seg sg;
+      if (even) {
+        // ---------------- pair MMA issuer ----------------
+        constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool any = false;
+        for (int i = 0; ok && get_seg_pair(p, i, rank, sg); ++i) {
+          if (!mbar_wait<true>(&tempty[acc], acc_phase ^ 1, abort_flag, p.wait_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+          for (int kb = 0; kb < sg.nkb; ++kb) {
+            if (!mbar_wait<true>(&full[stage], phase, abort_flag, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * SH::STAGE_BYTES);
+            const uint64_t adesc = sdesc_k_sw128(sa);
+            const uint64_t bdesc = sdesc_k_sw128(sa + SH::A_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              tc2_mma_bf16(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc,
+                           (kb | k) != 0);
+            any = true;
+            tc2_commit_mc(&empty[stage], 0x3);
+            if (++stage == STAGES) stage = 0, phase ^= 1;
+          }
+          if (!ok) break;
+          tc2_commit_mc(&tfull[acc], 0x3);
+          if (++acc == 2) acc = 0, acc_phase ^= 1;
+        }
+        if (!ok && any) {
+          // drain: wait (bounded) until the pair MMAs issued so far have finished
+          volatile int dummy = 0;
+          tc2_commit_mc(drain, 0x1);
+          (void)mbar_wait(drain, 0, (volatile int *)&dummy);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: warps 2..9 (this CTA's 128 rows) ----------------
+    pdl_wait();
+    __shared__ float xbuf[kEpiGroups][128 * 17];
+    __shared__ float xss[kEpiGroups][4 * 16];
+    __shared__ int s_last;
+    const int quarter = warp & 3;
+    const int eg = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    float *gx = xbuf[eg], *gs = xss[eg];
+    // where this CTA's warps release an accumulator: the even CTA's tempty
+    const uint32_t te0 = cluster_addr(smem_u32(&tempty[0]), 0);
+    auto release = [&](int a) {
+      if (even)
+        mbar_arrive(&tempty[a]);
+      else
+        mbar_arrive_cluster(te0 + (uint32_t)(a * sizeof(uint64_t)));
+    };
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    Seg sg;
+    for (int i = 0; get_seg_pair(p, i, rank, sg); ++i) {
+      const int m_tile = sg.m_tile, t_tile = sg.t_tile, split = sg.seg;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.wait_ns)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      const int tcol0 = t_tile * BN;
+      if (p.mode == 0) {
+        const int n = m_tile * BM + row;
+        float *outp = p.out + (size_t)split * p.T * p.ld + n;
+#pragma unroll 1
+        for (int c = 16 * eg; c < BN; c += 32) {
+          float v[16];
+          tc_ld16(taddr + c, v);
+          const int t0 = tcol0 + c;
+          if (n < p.N_out) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (t0 + j < p.T) outp[(size_t)(t0 + j) * p.ld] = v[j];
+          }
+        }
+      } else if (sg.nseg == 1) {
+#pragma unroll 1
+        for (int c = 16 * eg; c < BN; c += 32) {
+          if (tcol0 + c >= p.T) break;
+          float v[16];
+          tc_ld16(taddr + c, v);
+          epi_store(p, m_tile, row, tcol0 + c, v, gx, gs, eg);
+        }
+      } else {
+        const size_t tile = (size_t)t_tile * p.m_tiles + m_tile;
+        const size_t tile_sz = (size_t)BM * BN;
+        float *mine = p.out + (tile * p.nmax + split) * tile_sz + row;
+#pragma unroll 1
+        for (int c = 16 * eg; c < BN; c += 32) {
+          if (tcol0 + c >= p.T) break;
+          float v[16];
+          tc_ld16(taddr + c, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) mine[(size_t)(c + j) * BM] = v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release(acc);
+        epi_all_bar();
+        if (threadIdx.x == 64) {
+          const int old = atomic_add_acq_rel_gpu(&p.counters[tile], 1);
+          s_last = old == sg.nseg - 1;
+          if (s_last) p.counters[tile] = 0;
+        }
+        epi_all_bar();
+        if (s_last) {
+          constexpr int CPI = 4;
+          const float *base = p.out + tile * p.nmax * tile_sz + row;
+#pragma unroll 1
+          for (int c = 16 * eg; c < BN; c += 32 * CPI) {
+            if (tcol0 + c >= p.T) break;
+            float v[CPI][16];
+#pragma unroll
+            for (int k = 0; k < CPI; ++k)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[k][j] = 0.f;
+#pragma unroll 2
+            for (int q = 0; q < sg.nseg; ++q) {
+#pragma unroll
+              for (int k = 0; k < CPI; ++k) {
+                const int cc = c + 32 * k;
+                if (cc < BN && tcol0 + cc < p.T) {
+                  const float *src = base + (size_t)q * tile_sz + (size_t)cc * BM;
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) v[k][j] += __ldcg(src + (size_t)j * BM);
+                }
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < CPI; ++k) {
+              const int cc = c + 32 * k;
+              if (cc < BN && tcol0 + cc < p.T) epi_store(p, m_tile, row, tcol0 + cc, v[k], gx, gs, eg);
+            }
+          }
+        }
+        if (++acc == 2) acc = 0, acc_phase ^= 1;
+        continue;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) release(acc);
+      if (++acc == 2) acc = 0, acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs have stopped issuing; their issue records are visible
+  if (even && threadIdx.x == 0) {
+    // every copy either CTA issued has landed (already so unless a wait gave up)
+    volatile int dummy = 0;
+    for (int c = 0; c < 2; ++c)
+      for (int s = 0; s < STAGES; ++s) {
+        const uint32_t iss = c == 0 ? s_issued[s] : ld_dsmem_u32(smem_u32(&s_issued[s]), 1);
+        const uint32_t ph = c == 0 ? s_lphase[s] : ld_dsmem_u32(smem_u32(&s_lphase[s]), 1);
+        if (iss) (void)mbar_wait<true>(&full[s], ph, (volatile int *)&dummy);
+      }
+  }
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair may still use its memory or barriers
+  if (threadIdx.x == 0 && *abort_flag) set_err(p.err, DFLASH_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tc2_dealloc(tmem_base, SH::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // fp32 CUDA-core GEMM (float32 configuration)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_gemm_f32(const float *__restrict__ W,
@@ -841,6 +1192,10 @@ int gemm_splits(int N_out, int T, int K_in, int num_sms, int max_S) {
 
 GemmPlan gemm_plan(int N_out, int T, int K_in, int mode, int num_sms, int max_S) {
   const int rows = mode == GEMM_SWIGLU ? 2 * N_out : N_out;
+  const int mt = mode == GEMM_SWIGLU ? N_out / 64 : (N_out + dfl::BM - 1) / dfl::BM;
+  // many tokens: two-SM tiles (a call whose weight groups do not pair up falls
+  // back to one-SM 256-token tiles with the same single slice)
+  if (mode != GEMM_PARTIAL && T >= kPairMinTokens && mt % 2 == 0) return GemmPlan{256, 1, 0, 1};
   return plan_for(rows, T, K_in, mode, num_sms, max_S, true);
 }
 
@@ -897,6 +1252,7 @@ static int make_params(const GemmCall &g, int BN, int num_sms, dfl::GemmParams &
   p.m_fastest = (double)g.T * g.K_in * 2 > kMFastestActBytes ? 1 : 0;
   p.wait_ns = g.wait_ns > 0 ? g.wait_ns : dfl::kWaitLimitNs;
   p.stall = g.stall;
+  p.pair = 0;
   int grid = p.num_units < num_sms ? p.num_units : num_sms;
   if (g.chunk > 0) {
     const long total = (long)p.m_tiles * p.t_tiles * p.kb_total;
@@ -940,6 +1296,60 @@ static int launch_tc(const GemmCall &g, cudaStream_t st, const Dev *d) {
   return DFLASH_OK;
 }
 
+// Two-SM tiles: a uniform schedule over pairs of weight tiles, 256-token tiles,
+// launched as clusters of two CTAs.
+static int launch_tc2(const GemmCall &g, cudaStream_t st, const Dev *d) {
+  using SH = dfl::PairShape;
+  static int attr_set_dev[64] = {0};
+  if (d->id < 64 && !attr_set_dev[d->id]) {
+    if (cudaFuncSetAttribute(dfl::k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SH::SMEM_BYTES) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_set_dev[d->id] = 1;
+  }
+  const bool swiglu = g.mode == GEMM_SWIGLU;
+  const int w_rows = swiglu ? 2 * g.N_out : g.N_out;
+  dfl::WMaps mw;
+  CUtensorMap mx;
+  memset(&mw, 0, sizeof(mw));
+  for (int gi = 0; gi < g.groups; ++gi)
+    if (!bf16_map(&mw.m[gi], gi == 0 ? g.W : g.Wg[gi], (uint64_t)w_rows, (uint64_t)g.K_in,
+                  swiglu ? 64 : dfl::BM, d->id))
+      return DFLASH_ERR_CUDA;
+  if (!bf16_map(&mx, g.X, (uint64_t)g.T, (uint64_t)g.K_in, dfl::kPairBN / 2, d->id))
+    return DFLASH_ERR_CUDA;
+  dfl::GemmParams p;
+  if (make_params(g, dfl::kPairBN, d->num_sms, p) < 0) return DFLASH_ERR_DIMS;
+  p.pair = 1;
+  p.num_units = (p.m_tiles / 2) * p.t_tiles * p.S;
+  const int clusters = std::min(p.num_units, d->num_sms / 2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(dfl::kGemmThreads);
+  cfg.dynamicSmemBytes = SH::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 2 : 1;
+  count_launch();
+  DFL_CHECK_LAUNCH(cudaLaunchKernelEx(&cfg, dfl::k_gemm_tc2, mw, mx, p));
+  return DFLASH_OK;
+}
+
+// Whether a call can run on two-SM tiles: bf16, uniform schedule, and weight
+// tiles that pair up inside every weight group.
+static bool pair_ok(const GemmCall &g) {
+  if (g.dtype != DFLASH_BF16 || g.chunk != 0 || g.stall) return false;
+  const int mtg = g.mode == GEMM_SWIGLU ? g.N_out / 64 : (g.N_out + dfl::BM - 1) / dfl::BM;
+  return mtg % 2 == 0;
+}
+
 int gemm_run(const GemmCall &g, cudaStream_t st) {
   if (g.T <= 0 || g.N_out <= 0) return DFLASH_OK;
   const Dev *d = device();
@@ -981,7 +1391,8 @@ int gemm_run(const GemmCall &g, cudaStream_t st) {
     return DFLASH_OK;
   }
   if ((uintptr_t)g.W % 16 || (uintptr_t)g.X % 16) return DFLASH_ERR_ALIGN;
-  const int bn = g.bn > 0 ? g.bn : token_tile(g.T);
+  if (g.pair && pair_ok(g)) return launch_tc2(g, st, d);
+  const int bn = g.pair ? 256 : g.bn > 0 ? g.bn : token_tile(g.T);
   if (bn != 16 && bn != 32 && bn != 64 && bn != 128 && bn != 256) return DFLASH_ERR_DIMS;
   switch (bn) {
     case 16: return launch_tc<16>(g, st, d);

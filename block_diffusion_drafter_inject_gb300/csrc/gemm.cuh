@@ -19,7 +19,12 @@ struct GemmPlan {
   int bn;         // token tile: 16, 32, 64, 128 or 256
   int S;          // K slices (uniform schedule)
   int chunk = 0;  // > 0: balanced schedule, k-block iterations per CTA (reduce modes)
+  int pair = 0;   // two-SM 256 x 256 tiles (k_gemm_tc2), one K slice
 };
+// Token count from which the reduce modes run on two-SM tiles (bulk injection):
+// there a one-SM CTA is bound by its operand bytes per flop, while at draft
+// batch sizes the pair tiles gain nothing.
+constexpr int kPairMinTokens = 2048;
 GemmPlan gemm_plan(int N_out, int T, int K_in, int mode, int num_sms, int max_S);
 
 enum GemmMode {
@@ -66,6 +71,9 @@ struct GemmCall {
   // that nothing arrives on, so that the wait gives up
   uint64_t wait_ns = 0;
   int stall = 0;
+  // two-SM tiles (bf16, uniform schedule, an even number of weight tiles per
+  // group): clusters of two CTAs compute 256-row x 256-token tiles
+  int pair = 0;
 };
 
 // Floats of slice scratch a reduce-mode GEMM needs (0 when S == 1 and chunk == 0).

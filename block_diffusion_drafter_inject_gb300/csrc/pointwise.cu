@@ -254,50 +254,72 @@ __global__ void k_qkv_post(const float *__restrict__ qkv, int rows, int K, int H
 // kvf holds, per layer, the K/V projection [N, 2*Hkv*d] (K heads then V heads).
 // grid (N, L, 2*Hkv), block d/2.
 template <typename S>
-__global__ void k_inject_store(const float *__restrict__ kvf, int N, int L, int Hkv,
-                               int dh, dflh::LayerPtrs knorm, const int32_t *__restrict__ req,
-                               const int32_t *__restrict__ pos, const int32_t *__restrict__ table,
-                               int num_rows, int max_pages, int num_pages, int P,
-                               const float2 *__restrict__ rope_cs, float eps,
-                               S *__restrict__ kc, S *__restrict__ vc, int *err) {
-  __shared__ float red[32];
+__global__ void __launch_bounds__(256) k_inject_store(
+    const float *__restrict__ kvf, int N, int L, int Hkv, int dh, dflh::LayerPtrs knorm,
+    const int32_t *__restrict__ req, const int32_t *__restrict__ pos,
+    const int32_t *__restrict__ table, int num_rows, int max_pages, int num_pages, int P,
+    const float2 *__restrict__ rope_cs, float eps, S *__restrict__ kc, S *__restrict__ vc,
+    int *err) {
   pdl_launch();
   pdl_wait();
-  const int n = blockIdx.x, l = blockIdx.y, h = blockIdx.z, i = threadIdx.x, half = dh / 2;
-  const int W = 2 * Hkv * dh;
-  const size_t o = (size_t)l * N * W + (size_t)n * W + (size_t)h * dh;
-  float lo = kvf[o + i], hi = kvf[o + i + half];
+  // one CTA per (token, layer); one warp per head, lanes on the pairs (i, i + dh/2)
+  const int n = blockIdx.x, l = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = dh / 2, W = 2 * Hkv * dh, nw = blockDim.x >> 5;
   const int row = req[n], p = pos[n];
-  bool ok = true;
-  if (row < 0 || row >= num_rows) {
-    if (i == 0 && l == 0 && h == 0) set_err(err, DFLASH_DEV_REQ_RANGE);
-    ok = false;
-  }
   int page = -1;
-  if (ok && (p < 0 || p / P >= max_pages)) {
-    if (i == 0 && l == 0 && h == 0) set_err(err, DFLASH_DEV_POS_RANGE);
-    ok = false;
+  if (row < 0 || row >= num_rows) {
+    if (threadIdx.x == 0 && l == 0) set_err(err, DFLASH_DEV_REQ_RANGE);
+    return;
   }
-  if (ok) {
-    page = table[(size_t)row * max_pages + p / P];
-    if (page < 0 || page >= num_pages) {
-      if (i == 0 && l == 0 && h == 0) set_err(err, DFLASH_DEV_PAGE_RANGE);
-      ok = false;
+  if (p < 0 || p / P >= max_pages) {
+    if (threadIdx.x == 0 && l == 0) set_err(err, DFLASH_DEV_POS_RANGE);
+    return;
+  }
+  page = table[(size_t)row * max_pages + p / P];
+  if (page < 0 || page >= num_pages) {
+    if (threadIdx.x == 0 && l == 0) set_err(err, DFLASH_DEV_PAGE_RANGE);
+    return;
+  }
+  const float *src = kvf + (size_t)l * N * W + (size_t)n * W;
+  const S *g = (const S *)knorm.p[l];
+  for (int h = warp; h < 2 * Hkv; h += nw) {
+    const bool is_k = h < Hkv;
+    const float *hs = src + (size_t)h * dh;
+    float lo[2], hi[2];  // dh <= 128: at most two pairs per lane
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int i = lane + 32 * j;
+      lo[j] = i < half ? hs[i] : 0.f;
+      hi[j] = i < half ? hs[i + half] : 0.f;
+      ss += lo[j] * lo[j] + hi[j] * hi[j];
+    }
+    if (is_k) {
+      // per-head RMSNorm, then rotate-half RoPE at the token's position
+      const float inv = rsqrtf(warp_sum(ss) / dh + eps);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int i = lane + 32 * j;
+        if (i < half) {
+          const float a = lo[j] * inv * ldf(g + i), b = hi[j] * inv * ldf(g + i + half);
+          const float2 cs = rope_cs[(size_t)n * half + i];
+          lo[j] = a * cs.x - b * cs.y;
+          hi[j] = b * cs.x + a * cs.y;
+        }
+      }
+    }
+    const int hh = is_k ? h : h - Hkv;
+    S *dst = (is_k ? kc : vc) +
+             ((((size_t)l * num_pages + page) * Hkv + hh) * P + (p % P)) * (size_t)dh;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int i = lane + 32 * j;
+      if (i < half) {
+        stf(dst + i, lo[j]);
+        stf(dst + i + half, hi[j]);
+      }
     }
   }
-  const bool is_k = h < Hkv;
-  if (is_k) {
-    const S *g = (const S *)knorm.p[l];
-    // every thread of the block takes part in the norm's reduction
-    head_norm_rope(lo, hi, i, half, ldf(g + i), ldf(g + i + half), eps,
-                   rope_cs[(size_t)n * half + i], red);
-  }
-  if (!ok) return;
-  const int hh = is_k ? h : h - Hkv;
-  S *dst = (is_k ? kc : vc) +
-           ((((size_t)l * num_pages + page) * Hkv + hh) * P + (p % P)) * (size_t)dh;
-  stf(dst + i, lo);
-  stf(dst + i + half, hi);
 }
 
 // ---------------------------------------------------------------------------
@@ -734,8 +756,8 @@ int launch_inject_store(const float *kvf, int N, int L, int Hkv, int dh, LayerPt
                         int num_rows, int max_pages, int num_pages, int page_size,
                         const float2 *rope_cs, float eps, S *kc, S *vc, int *err,
                         cudaStream_t st) {
-  DFL_CHECK_LAUNCH(launch(dfl::k_inject_store<S>, dim3(N, L, 2 * Hkv), dim3(dh / 2), 0, st, kvf, N,
-                          L, Hkv, dh, knorm, req, pos, page_table, num_rows, max_pages, num_pages,
+  DFL_CHECK_LAUNCH(launch(dfl::k_inject_store<S>, dim3(N, L), dim3(256), 0, st, kvf, N, L, Hkv,
+                          dh, knorm, req, pos, page_table, num_rows, max_pages, num_pages,
                           page_size, rope_cs, eps, kc, vc, err));
   return DFLASH_OK;
 }
