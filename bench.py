@@ -321,6 +321,10 @@ def bench_b1(torch, dfl, cfg, Wd, pk, args, world, barrier, allmax, dev):
     def cycle():
         cyc.run(inp["hidden"], inp["req"], inp["pos"], inp["anchor"], inp["ctx"], inp["target"])
 
+    def cycle_two_calls():
+        cyc.run(inp["hidden"], inp["req"], inp["pos"], inp["anchor"], inp["ctx"], inp["target"],
+                fused=False)
+
     def dpass():
         dfl.draft_block(cfg, Wd, kv, inp["anchor"], inp["ctx"], K, cyc.ws, cyc.topk_ids,
                         cyc.topk_logp)
@@ -333,6 +337,7 @@ def bench_b1(torch, dfl, cfg, Wd, pk, args, world, barrier, allmax, dev):
     launches_per_cycle = dfl.launch_count(reset=True)
     status = dfl.read_device_status(cyc.ws)
     g_cycle = capture(torch, cycle)
+    g_two = capture(torch, cycle_two_calls)
     g_pass = capture(torch, dpass)
 
     with Clocks() as clk:
@@ -340,6 +345,7 @@ def bench_b1(torch, dfl, cfg, Wd, pk, args, world, barrier, allmax, dev):
         torch.cuda.nvtx.range_push("b1_pass")  # lets a profiler select these launches
         ms_pass = event_time(torch, g_pass.replay, args.steps, args.warmup)
         torch.cuda.nvtx.range_pop()
+        ms_two = event_time(torch, g_two.replay, args.steps, args.warmup)
         clocks = clk.summary(dev)
     ms_cycle = allmax(ms_cycle)
 
@@ -391,10 +397,12 @@ def bench_b1(torch, dfl, cfg, Wd, pk, args, world, barrier, allmax, dev):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) target hiddens, N(0,3) target logits)",
         "config": {"workload": WORKLOAD, "B": B, "K": K, "ctx": ctx[0], "window": cfg["window"],
-                   "cycle": "inject K rows + draft_block + select_path + accept_greedy, one CUDA graph",
+                   "cycle": "draft_block_inject (K new context rows injected inside the pass) + "
+                            "select_path + accept_greedy, one CUDA graph",
                    "l2": "inputs larger than L2: 3.5 GB of weights streamed per step, no flush",
                    "parallelism": f"replicas x{world}"},
         "draft_pass_us": ms_pass * 1e3,
+        "cycle_two_calls_us": ms_two * 1e3,
         "draft_pass_bytes": pb1,
         "draft_pass_hbm_frac": pb1 / (ms_pass * 1e-3) / 1e9 / pk["hbm"],
         "roofline": {"kernel": "k_gemm_tc (tcgen05 projection GEMM, all shapes of one B=1 pass)",
@@ -423,22 +431,25 @@ def bench_b32(torch, dfl, cfg, Wd, pk, args):
         dfl.select_path(cfg, Wd, inp2["anchor"], cyc2.topk_ids, cyc2.topk_logp, K, cyc2.ws,
                         cyc2.path, cyc2.score)
 
-    def cycle2():
+    def cycle2(fused=True):
         cyc2.run(inp2["hidden"], inp2["req"], inp2["pos"], inp2["anchor"], inp2["ctx"],
-                 inp2["target"])
+                 inp2["target"], fused=fused)
 
     gp2 = capture(torch, dpass2)
     gc2 = capture(torch, cycle2)
+    gt2 = capture(torch, lambda: cycle2(False))
     torch.cuda.nvtx.range_push("b32_pass")  # lets a profiler select these launches
     ms_p2 = event_time(torch, gp2.replay, max(5, args.steps // 2), args.warmup)
     torch.cuda.nvtx.range_pop()
     ms_c2 = event_time(torch, gc2.replay, max(5, args.steps // 2), args.warmup)
+    ms_t2 = event_time(torch, gt2.replay, max(5, args.steps // 2), args.warmup)
     status = dfl.read_device_status(cyc2.ws)
     pb2 = pass_bytes(cfg, B2, K, ctx2)
     fl2 = sum(2.0 * N * Kin * T for (N, Kin, T, _) in pass_gemms(cfg, B2, K))
     t_hbm = pb2 / (pk["hbm"] * 1e9)
     t_tc = fl2 / (pk["bf16_sus"] * 1e12)
     return {"draft_pass_us": ms_p2 * 1e3, "cycle_us": ms_c2 * 1e3,
+            "cycle_two_calls_us": ms_t2 * 1e3,
             "cycles_per_s": 1e3 / ms_c2, "pass_bytes": pb2, "pass_gemm_flops": fl2,
             "hbm_floor_us": t_hbm * 1e6, "tensor_floor_us": t_tc * 1e6,
             "frac_of_tighter_roofline": max(t_hbm, t_tc) / (ms_p2 * 1e-3),

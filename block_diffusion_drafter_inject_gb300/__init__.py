@@ -2,6 +2,7 @@
 
     inject_context  target hidden states -> per-layer paged draft KV
     draft_block     one non-causal drafter pass over a block, per-position top-k
+    draft_block_inject  inject_context + draft_block in one pass (K/V weights read once)
     select_path     low-rank bilinear Viterbi over the candidate lattice
     accept_greedy   longest prefix matching the target's argmax + bonus token
     sample_path     temperature-1 sampling walk over the same pair scores
@@ -10,7 +11,15 @@
 """
 
 from . import _lib  # noqa: F401
-from ._lib import DFlashError, lib  # noqa: F401
+from ._lib import (  # noqa: F401
+    DEV_PAGE_RANGE,
+    DEV_POS_RANGE,
+    DEV_REQ_RANGE,
+    DEV_TIMEOUT,
+    DEV_TOKEN_RANGE,
+    DFlashError,
+    lib,
+)
 from .api import (  # noqa: F401
     DeviceWeights,
     DraftCycle,
@@ -21,6 +30,7 @@ from .api import (  # noqa: F401
     accept_sample,
     clear_device_status,
     draft_block,
+    draft_block_inject,
     draft_hidden,
     inject_context,
     launch_count,

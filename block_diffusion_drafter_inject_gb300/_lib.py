@@ -57,6 +57,9 @@ EXPORTS = {
     "dflash_draft_block": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(Weights),
                                           ctypes.POINTER(KV), vp, vp, i32, i32, vp, vp, vp, vp,
                                           ctypes.c_size_t, vp]),
+    "dflash_draft_block_inject": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(Weights),
+                                                 ctypes.POINTER(KV), vp, vp, vp, i32, vp, vp, i32,
+                                                 i32, vp, vp, vp, vp, ctypes.c_size_t, vp]),
     "dflash_select_path": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(Weights), vp, vp,
                                           vp, i32, i32, vp, vp, vp, ctypes.c_size_t, vp]),
     "dflash_prepare_selector": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(Weights),

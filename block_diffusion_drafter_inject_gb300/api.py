@@ -132,6 +132,21 @@ def draft_block(cfg, W, kv, anchor, ctx_len, K, ws, topk_ids, topk_logp, logits=
           "dflash_draft_block")
 
 
+def draft_block_inject(cfg, W, kv, hidden, req, pos, anchor, ctx_len, K, ws, topk_ids,
+                       topk_logp, logits=None, stream=None):
+    """inject_context followed by draft_block, in one pass (dflash_draft_block_inject):
+    the new rows' K/V come out of each layer's QKV projection."""
+    c = make_config(cfg)
+    n = 0 if hidden is None else int(hidden.shape[0])
+    check(lib().dflash_draft_block_inject(ctypes.byref(c), ctypes.byref(W.struct),
+                                          ctypes.byref(kv.struct), _ptr(hidden), _ptr(req),
+                                          _ptr(pos), n, _ptr(anchor), _ptr(ctx_len),
+                                          int(anchor.shape[0]), int(K), _ptr(topk_ids),
+                                          _ptr(topk_logp), _ptr(logits), ws.ptr, ws.nbytes,
+                                          _stream(stream)),
+          "dflash_draft_block_inject")
+
+
 def select_path(cfg, W, anchor, topk_ids, topk_logp, K, ws, path, score, stream=None):
     c = make_config(cfg)
     check(lib().dflash_select_path(ctypes.byref(c), ctypes.byref(W.struct), _ptr(anchor),
@@ -268,11 +283,18 @@ class DraftCycle:
         self.accept_len = torch.zeros((B,), **i32)
         self.tokens = torch.zeros((B, K), **i32)
 
-    def run(self, hidden, req, pos, anchor, ctx_len, target_logits, logits=None, stream=None):
-        if hidden is not None and hidden.shape[0] > 0:
-            inject_context(self.cfg, self.W, self.kv, hidden, req, pos, self.ws, stream)
-        draft_block(self.cfg, self.W, self.kv, anchor, ctx_len, self.K, self.ws, self.topk_ids,
-                    self.topk_logp, logits, stream)
+    def run(self, hidden, req, pos, anchor, ctx_len, target_logits, logits=None, stream=None,
+            fused=True):
+        """One cycle.  fused: the injection rides in the draft pass
+        (draft_block_inject); else inject_context then draft_block."""
+        if fused:
+            draft_block_inject(self.cfg, self.W, self.kv, hidden, req, pos, anchor, ctx_len,
+                               self.K, self.ws, self.topk_ids, self.topk_logp, logits, stream)
+        else:
+            if hidden is not None and hidden.shape[0] > 0:
+                inject_context(self.cfg, self.W, self.kv, hidden, req, pos, self.ws, stream)
+            draft_block(self.cfg, self.W, self.kv, anchor, ctx_len, self.K, self.ws,
+                        self.topk_ids, self.topk_logp, logits, stream)
         select_path(self.cfg, self.W, anchor, self.topk_ids, self.topk_logp, self.K, self.ws,
                     self.path, self.score, stream)
         accept_greedy(self.path, target_logits, self.ws, self.accept_len, self.tokens, stream)

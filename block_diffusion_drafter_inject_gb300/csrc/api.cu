@@ -136,8 +136,8 @@ constexpr size_t kHeaderBytes = 256 + kTicketInts * 4 + kTopkTicketInts * 4;
 struct Layout {
   size_t status, tickets, scratch;
   size_t x, un, ub, rf, rb, gates, qkv, qb, kb, vb, ob, hb, zf, logits, attn, topk, topk_tickets;
-  size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf, rope, rope_inj, selgate;
-  size_t total;
+  size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf, rope, rope_inj, selgate, slots;
+  size_t total, sc_floats;
   GemmPlan P_gate, P_qkv, P_o, P_gu, P_down, P_sel, P_sel2, P_hgate;
   AttnPlan ap;
 };
@@ -157,6 +157,16 @@ static size_t reduce_scratch(const dflash_config *c, int N_out, int T, int K_in,
   if (c->dtype == DFLASH_F32)
     return (size_t)p.S * T * (mode == GEMM_SWIGLU ? 2 * N_out : N_out);
   return gemm_scratch_floats(N_out, T, p.S, mode, p.bn, p.chunk, K_in);
+}
+
+// The QKV projection over T block rows and n injected rows: the token tiles of
+// the injected rows alone skip the q weight tiles, so the plan for T + n tokens
+// is kept only when its token tile is no larger than the block's own plan's
+// (larger tiles give fewer, longer work units); else the block's plan.
+static GemmPlan fused_qkv_plan(const dflash_config *c, int QKVW, int T, int n, int D, int sms) {
+  const GemmPlan pt = reduce_plan(c, QKVW, T, D, GEMM_QKV, sms);
+  const GemmPlan pn = reduce_plan(c, QKVW, T + n, D, GEMM_QKV, sms);
+  return pn.bn <= pt.bn || pn.pair ? pn : pt;
 }
 
 static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *L) {
@@ -213,13 +223,27 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   sc = std::max(sc, inj(D, TIN));
   sc = std::max(sc, inj(2 * Hkv * dh, D));
   sc = std::max(sc, inj(std::min(c->n_layers, kKvGroup) * 2 * Hkv * dh, D));
+  if (Nmax > 0 && c->dtype == DFLASH_BF16) {
+    // the pass with injected rows: each layer's QKV GEMM over the block rows and
+    // up to Nmax context rows
+    auto eval = [&](int n) {
+      if (n < 1 || n > Nmax) return;
+      const GemmPlan p = fused_qkv_plan(c, QKVW, T, n, D, sms);
+      sc = std::max(sc, reduce_scratch(c, QKVW, T + n, D, p, GEMM_QKV));
+    };
+    for (int n = 1; n <= 16; ++n) eval(n);
+    for (int n = 32; n <= 256; n *= 2) eval(n);
+    for (int n = 512; n <= Nmax; n += 256) eval(n);
+    eval(Nmax);
+  }
+  L->sc_floats = sc;
+  // buffers whose place does not depend on the injection capacity first (a
+  // draft pass and dflash_draft_hidden agree on them whatever Nmax was)
   L->status = take(256);
   L->tickets = take(kTicketInts * sizeof(int));
   L->topk_tickets = take(kTopkTicketInts * sizeof(int));
-  L->scratch = take(sc * 4);
   L->x = take((size_t)T * D * 4);
   L->un = take((size_t)T * D * es);
-  L->ub = take((size_t)T * D * es);
   L->rf = take((size_t)T * D * 4);
   L->rb = take((size_t)T * D * es);
   L->gates = take((size_t)T * GW * 4);
@@ -238,16 +262,30 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->Vp = L->U + (size_t)TR * r * 4;
   L->pairs = take((size_t)B * (K - 1) * k * k * 4);
   L->argmax = take((size_t)T * argmax_chunks(V) * 2 * 4);
-  L->rope = take((size_t)T * (dh / 2) * 8);
-  L->rope_inj = take((size_t)N * (dh / 2) * 8);
   L->selgate = take((size_t)TL * r * 4);
+  // then the ones sized by it: the QKV operand and the RoPE table hold the block
+  // rows followed by up to N injected rows
+  L->rope = take((size_t)(T + N) * (dh / 2) * 8);
+  L->ub = take((size_t)(T + N) * D * es);
+  L->rope_inj = take((size_t)N * (dh / 2) * 8);
+  L->slots = take((size_t)N * 8);
   L->gn = take((size_t)N * TIN * es);
   L->cb = take((size_t)N * D * es);
   L->kvf = take((size_t)N * 2 * Hkv * dh * c->n_layers * 4);
+  L->scratch = take(sc * 4);
   L->total = off;
   // acceptance keeps its scratch right after the fixed header
   L->total = std::max(L->total, kHeaderBytes + accept_sample_floats(B, K, V) * 4);
   return true;
+}
+
+// A plan chosen at call time for a token count the layout sampled around: one
+// K slice when its slice scratch would not fit the workspace's.
+static GemmPlan fit_plan(const dflash_config &c, const Layout &L, int N_out, int T, int K_in,
+                         int mode, GemmPlan p) {
+  if (c.dtype == DFLASH_BF16 && reduce_scratch(&c, N_out, T, K_in, p, mode) > L.sc_floats)
+    p.S = 1, p.chunk = 0;
+  return p;
 }
 
 // ---------------------------------------------------------------------------
@@ -301,7 +339,8 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
   float2 *rope_cs = (float2 *)(ws + L.rope_inj);
   TRY(launch_rows_norm<S>((const S *)hidden, N, TIN, (const S *)w.fc_norm, c.rms_eps, gn, pos,
                           rope, dh / 2, rope_cs, st));
-  const GemmPlan S_fc = reduce_plan(&c, D, N, TIN, GEMM_REDUCE, sms);
+  const GemmPlan S_fc =
+      fit_plan(c, L, D, N, TIN, GEMM_REDUCE, reduce_plan(&c, D, N, TIN, GEMM_REDUCE, sms));
   TRY(gemm_run(reduce_call(c, ws, L, w.fc, D, TIN, gn, N, S_fc, GEMM_REDUCE, nullptr, D, cb, D),
                st));
   // the [Wk; Wv] rows of every layer: one grouped launch per kKvGroup layers
@@ -312,7 +351,8 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
   const int per = grouped ? kKvGroup : 1;
   for (int l0 = 0; l0 < c.n_layers; l0 += per) {
     const int ng = std::min(per, c.n_layers - l0);
-    const GemmPlan S_kv = reduce_plan(&c, ng * W2, N, D, GEMM_REDUCE, sms);
+    const GemmPlan S_kv = fit_plan(c, L, ng * W2, N, D, GEMM_REDUCE,
+                                   reduce_plan(&c, ng * W2, N, D, GEMM_REDUCE, sms));
     GemmCall g = reduce_call(c, ws, L, (const S *)w.layer[l0].wqkv + (size_t)Hq * dh * D, W2, D,
                              cb, N, S_kv, GEMM_REDUCE, kvf + (size_t)l0 * N * W2, W2, nullptr, 0);
     g.groups = ng;
@@ -327,11 +367,18 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
   return DFLASH_OK;
 }
 
+// Injected context rows carried by one draft pass (N = 0: none).
+struct InjectRows {
+  const void *hidden = nullptr;
+  const int32_t *req = nullptr, *pos = nullptr;
+  int N = 0;
+};
+
 template <typename S>
 static int run_draft(const dflash_config &c, const dflash_weights &w, const dflash_kv &kv,
                      const int32_t *anchor, const int32_t *ctx_len, int B, int K, int32_t *ids,
                      float *logp, float *logits_opt, uint8_t *ws, const Layout &L,
-                     cudaStream_t st) {
+                     cudaStream_t st, const InjectRows &inj = InjectRows()) {
   const int D = c.d_model, F = c.d_ff, V = c.vocab, dh = c.head_dim;
   const int Hq = c.n_q_heads, Hkv = c.n_kv_heads, g = c.conv_group;
   const int GW = 2 * D / g, QKVW = (Hq + 2 * Hkv) * dh;
@@ -356,13 +403,35 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   // the lm_head's epilogue also writes each 128-entry vocab tile's (max, sum e^(z - max))
   float2 *tstats = c.dtype == DFLASH_BF16 ? (float2 *)topkp : nullptr;
   float2 *rope_cs = (float2 *)(ws + L.rope);
+  // injected context rows (bf16): their fc outputs follow the block rows in the
+  // QKV operand, so each layer's QKV GEMM also forms their K/V and stores them
+  const int N = c.dtype == DFLASH_BF16 ? inj.N : 0;
+  const int Tq = T + N;
+  // each injected row's place in a layer's cache, found (and checked) once
+  CacheSlots slots;
+  if (N > 0) {
+    slots.req = inj.req;
+    slots.table = kv.page_table;
+    slots.max_pages = kv.max_pages_per_req;
+    slots.num_rows = kv.num_rows;
+    slots.num_pages = kv.num_pages;
+    slots.P = c.page_size;
+    slots.Hkv = Hkv;
+    slots.dh = dh;
+    slots.slot = (long long *)(ws + L.slots);
+    slots.err = err;
+  }
+  const GemmPlan P_qkv =
+      N > 0 ? fit_plan(c, L, QKVW, Tq, D, GEMM_QKV,
+                       fused_qkv_plan(&c, QKVW, T, N, D, device()->num_sms))
+            : L.P_qkv;
   auto qkv_call = [&](int l) {
     const dflash_layer_weights &lw = w.layer[l];
     if (c.dtype != DFLASH_BF16)
       return reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_REDUCE, qkv, QKVW,
                          nullptr, 0);
     // the projection's epilogue applies the q/k head norms and RoPE: bf16 q, k, v rows
-    GemmCall gq = reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, T, L.P_qkv, GEMM_QKV, nullptr, 0,
+    GemmCall gq = reduce_call(c, ws, L, lw.wqkv, QKVW, D, ub, Tq, P_qkv, GEMM_QKV, nullptr, 0,
                               ws + L.qkv, QKVW);
     gq.q_norm = lw.q_norm;
     gq.k_norm = lw.k_norm;
@@ -371,6 +440,15 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     gq.Hkv = Hkv;
     gq.dh = dh;
     gq.eps = eps;
+    if (N > 0) {
+      gq.T0 = T;
+      gq.ctx_slot = slots.slot;
+      gq.layer_elems = (size_t)kv.num_pages * Hkv * c.page_size * dh;
+      gq.page_size = c.page_size;
+      gq.layer = l;
+      gq.kc = kv.k;
+      gq.vc = kv.v;
+    }
     return gq;
   };
   auto o_call = [&](int l) {
@@ -421,6 +499,19 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
                                     (const S *)next_gain, eps, un, last ? zf : (S *)nullptr, st);
   };
 
+  if (N > 0) {
+    // the injection's RMSNorm over the taps and fc to width D, into rows T.. of
+    // the QKV operand (their RoPE rows after the block's)
+    const int TIN = c.n_taps * c.d_target;
+    S *gn = (S *)(ws + L.gn);
+    TRY(launch_rows_norm<S>((const S *)inj.hidden, N, TIN, (const S *)w.fc_norm, eps, gn, inj.pos,
+                            rope, dh / 2, rope_cs + (size_t)T * (dh / 2), st, slots));
+    const GemmPlan pf = fit_plan(c, L, D, N, TIN, GEMM_REDUCE,
+                                 reduce_plan(&c, D, N, TIN, GEMM_REDUCE, device()->num_sms));
+    TRY(gemm_run(reduce_call(c, ws, L, w.fc, D, TIN, gn, N, pf, GEMM_REDUCE, nullptr, D,
+                             ub + (size_t)T * D, D),
+                 st));
+  }
   TRY(launch_embed_norm<S>((const S *)w.embed, anchor, c.mask_token_id, V, B, K, D,
                            (const S *)w.layer[0].attn_norm, eps, x, fused ? (S *)nullptr : un, err,
                            ctx_len, rope, dh / 2, rope_cs, st));
@@ -434,7 +525,8 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
       TRY(launch_attention_fused(L.ap, (const dfl::bf16 *)(ws + L.qkv), (const dfl::bf16 *)kv.k,
                                  (const dfl::bf16 *)kv.v, l, c.n_layers, kv.page_table,
                                  kv.max_pages_per_req, kv.num_pages, c.page_size, ctx_len, B, K,
-                                 Hq, Hkv, dh, c.window, (dfl::bf16 *)ob, err, st));
+                                 Hq, Hkv, dh, c.window, (dfl::bf16 *)ob, err, st, inj.req,
+                                 inj.pos, N));
     } else {
       TRY(launch_qkv_post<S>(qkv, T, K, Hq, Hkv, dh, (const S *)lw.q_norm, (const S *)lw.k_norm,
                              rope_cs, eps, qb, kb, vb, st));
@@ -593,6 +685,53 @@ int dflash_draft_block(const dflash_config *cfg, const dflash_weights *w, const 
                                 logits_opt, (uint8_t *)ws, L, st);
   return run_draft<float>(*cfg, *w, *kv, anchor, ctx_len, B, K, topk_ids, topk_logp, logits_opt,
                           (uint8_t *)ws, L, st);
+}
+
+int dflash_draft_block_inject(const dflash_config *cfg, const dflash_weights *w,
+                              const dflash_kv *kv, const void *target_hidden, const int32_t *req,
+                              const int32_t *pos, int32_t N, const int32_t *anchor,
+                              const int32_t *ctx_len, int32_t B, int32_t K, int32_t *topk_ids,
+                              float *topk_logp, float *logits_opt, void *ws, size_t ws_bytes,
+                              void *stream) {
+  int rc = check_cfg(cfg);
+  if (rc != DFLASH_OK) return rc;
+  if (N < 0) return DFLASH_ERR_DIMS;
+  if (B < 0 || K < 2 || K > DFLASH_MAX_BLOCK) return DFLASH_ERR_BLOCK;
+  if (N > 0 && B == 0)
+    return dflash_inject_context(cfg, w, kv, target_hidden, req, pos, N, ws, ws_bytes, stream);
+  if (B == 0) return DFLASH_OK;
+  if ((size_t)B * (K - 1) > kTopkTicketInts) return DFLASH_ERR_DIMS;
+  if (!anchor || !ctx_len || !topk_ids || !topk_logp || !ws) return DFLASH_ERR_NULL;
+  if (N > 0 && (!target_hidden || !req || !pos)) return DFLASH_ERR_NULL;
+  if (N > 0 && (!a16(target_hidden) || !a16(w->fc_norm))) return DFLASH_ERR_ALIGN;
+  if (N > 0 && (rc = check_weights(cfg, w, false)) != DFLASH_OK) return rc;
+  if ((rc = check_weights(cfg, w, true)) != DFLASH_OK) return rc;
+  if ((rc = check_kv(cfg, kv)) != DFLASH_OK) return rc;
+  if (!a16(ws)) return DFLASH_ERR_ALIGN;
+  Layout L;
+  make_layout(cfg, B, K, N, &L);
+  if (ws_bytes < L.total) return DFLASH_ERR_WORKSPACE;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cfg->dtype == DFLASH_BF16) {
+    InjectRows inj;
+    inj.hidden = target_hidden;
+    inj.req = req;
+    inj.pos = pos;
+    inj.N = N;
+    return run_draft<dfl::bf16>(*cfg, *w, *kv, anchor, ctx_len, B, K, topk_ids, topk_logp,
+                                logits_opt, (uint8_t *)ws, L, st, inj);
+  }
+  // float32 storage: the injection, then the pass
+  if (N > 0) {
+    Layout Li;
+    make_layout(cfg, 1, 2, N, &Li);
+    TRY(run_inject<float>(*cfg, *w, *kv, target_hidden, req, pos, N, (uint8_t *)ws, Li, st));
+  }
+  Layout Ld;
+  make_layout(cfg, B, K, 0, &Ld);
+  return run_draft<float>(*cfg, *w, *kv, anchor, ctx_len, B, K, topk_ids, topk_logp, logits_opt,
+                          (uint8_t *)ws, Ld, st);
 }
 
 int dflash_select_path(const dflash_config *cfg, const dflash_weights *w, const int32_t *anchor,

@@ -185,7 +185,16 @@ struct AttnArgs {
   int K, Hq, Hkv, window, kps, nsplit, nqg;
   bf16 *ob;  // [B*K, Hq*DH]
   int *err;
+  // context rows the pass itself injects (request row, position), written into
+  // this layer's cache by the projection before it: no tile holding one of them
+  // is read before the grid-dependency wait
+  const int32_t *inj_req, *inj_pos;
+  int inj_n;
 };
+
+// Injected rows scanned per CTA for the lowest position of its request; above
+// this many, no context tile is loaded before the wait.
+constexpr int kAttnScanMax = 1024;
 
 // grid (nsplit, Hkv, B*nqg), cluster (nsplit, 1, 1); block 128 = 4 warps.
 // KP warps share each 16-row query block and split every key tile KP ways
@@ -264,6 +273,20 @@ __global__ void __launch_bounds__(128)
   // the pass's first kernel lets no later kernel start before all earlier work
   // has completed) and the next two are prefetched into L2
   const int npre = TK ? min(max(0, min(t_end, nct) - t_begin), kAttnPrePages) : 0;
+  // the lowest position of this request that the pass injects (rows written by
+  // this layer's projection): tiles loaded before the wait must end below it
+  __shared__ int s_fresh[4];
+  if (TK) {
+    int f = INT_MAX;
+    if (A.inj_n > kAttnScanMax) {
+      f = INT_MIN;
+    } else {
+      for (int i = tid; i < A.inj_n; i += 128)
+        if (__ldg(A.inj_req + i) == b) f = min(f, __ldg(A.inj_pos + i));
+    }
+    f = __reduce_min_sync(0xffffffffu, f);
+    if (lane == 0) s_fresh[warp] = f;
+  }
   if (TK && tid < npre) {
     const int pi = pgf + t_begin + tid;
     int page = -1;
@@ -289,6 +312,13 @@ __global__ void __launch_bounds__(128)
   __syncthreads();  // barrier init and the looked-up pages visible to every thread
   if (clus) cluster_arrive_relaxed();  // this CTA's receive mbarrier is initialised
   const bf16 *blk = A.qkvb + (size_t)b * A.K * QKVW;  // this request's block rows
+  const int fresh = TK ? min(min(s_fresh[0], s_fresh[1]), min(s_fresh[2], s_fresh[3])) : INT_MAX;
+  // context tile t of this split may start before the wait: its cache rows are
+  // complete when the pass began (it ends below every position injected now)
+  auto early = [&](int t) {
+    return TK && t < ntiles && t_begin + t < nct &&
+           (long long)(pgf + t_begin + t + 1) * CH <= (long long)fresh;
+  };
   uint64_t pol_kv = 0;
   if (TK) pol_kv = l2_policy_evict_first();
 
@@ -394,7 +424,7 @@ __global__ void __launch_bounds__(128)
   if (TK)
 #pragma unroll
     for (int t = 0; t < NST - 1; ++t)
-      if (t < ntiles && t_begin + t < nct) load_tile_tk(t, t);
+      if (early(t)) load_tile_tk(t, t);
   pdl_wait();  // the projection rows (queries, block keys and values) are ready
 
   // queries qr = i*grp + g of this group: projection rows, copied (zeros past QR)
@@ -408,7 +438,7 @@ __global__ void __launch_bounds__(128)
   // the first NST-1 tiles in flight; one commit group per tile (empty past the end)
 #pragma unroll
   for (int t = 0; t < NST - 1; ++t) {
-    if (t < ntiles && !(TK && t_begin + t < nct)) load_tile(t, t, t == 0 ? pg0 : pg1);
+    if (t < ntiles && !early(t)) load_tile(t, t, t == 0 ? pg0 : pg1);
     cp_async_commit();
   }
   pg0 = pg2;  // page of tile NST-1 = 2
@@ -809,7 +839,8 @@ int launch_attention_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl:
                            const dfl::bf16 *vc, int layer, int n_layers, const int32_t *table,
                            int max_pages, int num_pages, int P, const int32_t *ctx_len, int B,
                            int K, int Hq, int Hkv, int dh, int window, dfl::bf16 *ob, int *err,
-                           cudaStream_t st) {
+                           cudaStream_t st, const int32_t *inj_req, const int32_t *inj_pos,
+                           int inj_n) {
   const Dev *d = device();
   if (!d) return DFLASH_ERR_DEVICE;
   dfl::AttnArgs a;
@@ -832,6 +863,9 @@ int launch_attention_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl:
   a.nqg = pl.nqg;
   a.ob = ob;
   a.err = err;
+  a.inj_req = inj_req;
+  a.inj_pos = inj_pos;
+  a.inj_n = inj_req && inj_pos ? inj_n : 0;
   // pages of 64 positions: whole pages are loaded by TMA from the caches viewed
   // as [n_layers * num_pages * Hkv * 64, dh] matrices
   CUtensorMap mk, mv;

@@ -28,11 +28,14 @@ int launch_block_attention(const AttnPlan &pl, const S *qb, const S *kb, const S
 // window, attends, and merges its key splits through the cluster's distributed
 // shared memory into o [B*K, Hq*dh].
 // Page size 64: whole cache pages are loaded by TMA (caches [n_layers][num_pages]
-// [Hkv][64][dh]); other page sizes copy 16-byte chunks per key row.
+// [Hkv][64][dh]); other page sizes copy 16-byte chunks per key row.  The first
+// context pages are loaded before the wait on the projection unless they hold
+// one of the inj_n rows (inj_req, inj_pos) that the pass itself injects.
 int launch_attention_fused(const AttnPlan &pl, const dfl::bf16 *qkvb, const dfl::bf16 *kc,
                            const dfl::bf16 *vc, int layer, int n_layers, const int32_t *table,
                            int max_pages, int num_pages, int P, const int32_t *ctx_len, int B,
                            int K, int Hq, int Hkv, int dh, int window, dfl::bf16 *ob, int *err,
-                           cudaStream_t st);
+                           cudaStream_t st, const int32_t *inj_req = nullptr,
+                           const int32_t *inj_pos = nullptr, int inj_n = 0);
 
 }  // namespace dflh

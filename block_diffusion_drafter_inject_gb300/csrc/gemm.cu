@@ -66,6 +66,15 @@ struct GemmParams {
   const float2 *rope_cs;  // [T][dh/2] (cos, sin)
   int Hq, Hkv, dh;
   float eps;
+  // tokens [T0, T) are injected context rows: k/v heads to the paged cache
+  int T0;
+  // token tiles from tb on hold context rows only: they skip the first mq weight
+  // tiles (q heads only), tiles enumerated as [m_tiles x tb] then [m_tiles - mq
+  // x t_tiles - tb]; tb = t_tiles when nothing is skipped
+  int tb, mq;
+  const long long *ctx_slot;  // per context row: offset in a layer's cache, or -1
+  bf16 *kc, *vc;  // this layer's caches
+  int P;
   // tile order: weight tile fastest (activations too large to re-read per
   // weight tile) instead of token tile fastest
   int m_fastest;
@@ -109,6 +118,18 @@ struct GemmShape {
 // HBM once and the weights, re-read once per wave of token tiles, come from L2.
 __device__ __forceinline__ void tile_coords(int tile, const GemmParams &p, int &m_tile,
                                             int &t_tile) {
+  if (p.tb < p.t_tiles) {
+    const int a = p.m_tiles * p.tb;
+    if (tile < a) {
+      t_tile = tile % p.tb;
+      m_tile = tile / p.tb;
+    } else {
+      const int r = tile - a, nt = p.t_tiles - p.tb;
+      t_tile = p.tb + r % nt;
+      m_tile = p.mq + r / nt;
+    }
+    return;
+  }
   if (p.m_fastest) {
     m_tile = tile % p.m_tiles;
     t_tile = tile / p.m_tiles;
@@ -216,13 +237,36 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
         const float x = v[j] * inv * g, y = xbuf[pr * 17 + j] * inv * gp;
         o[j] = d < half ? x * cs[j].x - y * cs[j].y : x * cs[j].x + y * cs[j].y;
       }
+      if (c0 + 16 <= p.T0) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (c0 + j < p.T) p.out_bf16[(size_t)(c0 + j) * p.ldb + n] = __float2bfloat16_rn(o[j]);
+        for (int j = 0; j < 16; ++j)
+          p.out_bf16[(size_t)(c0 + j) * p.ldb + n] = __float2bfloat16_rn(o[j]);
+      } else {
+        // injected context rows: k heads to this layer's cache, q heads dropped
+        const size_t hoff = (size_t)(h - p.Hq) * p.P * dh + d;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int t = c0 + j;
+          if (t < p.T0) {
+            p.out_bf16[(size_t)t * p.ldb + n] = __float2bfloat16_rn(o[j]);
+          } else if (t < p.T && !is_q) {
+            const long long s = __ldg(p.ctx_slot + (t - p.T0));
+            if (s >= 0) p.kc[s + hoff] = __float2bfloat16_rn(o[j]);
+          }
+        }
+      }
     } else if (n < p.N_out) {
+      const size_t hoff = (size_t)(h - p.Hq - p.Hkv) * p.P * dh + d;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (c0 + j < p.T) p.out_bf16[(size_t)(c0 + j) * p.ldb + n] = __float2bfloat16_rn(v[j]);
+      for (int j = 0; j < 16; ++j) {
+        const int t = c0 + j;
+        if (t < p.T0) {
+          p.out_bf16[(size_t)t * p.ldb + n] = __float2bfloat16_rn(v[j]);
+        } else if (t < p.T) {
+          const long long s = __ldg(p.ctx_slot + (t - p.T0));
+          if (s >= 0) p.vc[s + hoff] = __float2bfloat16_rn(v[j]);
+        }
+      }
     }
     epi_bar(eg);
   } else if (p.mode == 1) {
@@ -1229,7 +1273,15 @@ static int make_params(const GemmCall &g, int BN, int num_sms, dfl::GemmParams &
   p.m_tiles = p.mtg * g.groups;
   p.ostride = g.ostride;
   p.t_tiles = (g.T + BN - 1) / BN;
-  p.num_units = p.m_tiles * p.t_tiles * g.S;
+  p.tb = p.t_tiles;
+  p.mq = 0;
+  if (g.mode == GEMM_QKV && g.T0 > 0 && g.T0 < g.T && !g.pair) {
+    // token tiles of injected context rows alone need only the k and v weight tiles
+    p.tb = (g.T0 + BN - 1) / BN;
+    p.mq = g.Hq * g.dh / dfl::BM;
+  }
+  const int tiles = p.m_tiles * p.tb + (p.m_tiles - p.mq) * (p.t_tiles - p.tb);
+  p.num_units = tiles * g.S;
   p.mode = g.mode;
   p.out_f32 = g.out_f32;
   p.out_bf16 = (dfl::bf16 *)g.out_bf16;
@@ -1245,6 +1297,11 @@ static int make_params(const GemmCall &g, int BN, int num_sms, dfl::GemmParams &
   p.Hkv = g.Hkv;
   p.dh = g.dh;
   p.eps = g.eps;
+  p.T0 = g.T0 > 0 ? g.T0 : g.T;
+  p.ctx_slot = g.ctx_slot;
+  p.P = g.page_size;
+  p.kc = g.kc ? (dfl::bf16 *)g.kc + (size_t)g.layer * g.layer_elems : nullptr;
+  p.vc = g.vc ? (dfl::bf16 *)g.vc + (size_t)g.layer * g.layer_elems : nullptr;
   p.chunk = 0;
   p.kb_total = g.K_in / dfl::BK;
   p.total = 0;
@@ -1255,14 +1312,14 @@ static int make_params(const GemmCall &g, int BN, int num_sms, dfl::GemmParams &
   p.pair = 0;
   int grid = p.num_units < num_sms ? p.num_units : num_sms;
   if (g.chunk > 0) {
-    const long total = (long)p.m_tiles * p.t_tiles * p.kb_total;
+    const long total = (long)tiles * p.kb_total;
     if (total >= (1L << 30)) return -1;
     p.chunk = g.chunk;
     p.total = (int)total;
     p.nmax = gemm_balanced_slots(g.K_in, g.chunk);
     p.S = 1;
     p.kb_per_split = p.kb_total;
-    p.num_units = p.m_tiles * p.t_tiles;
+    p.num_units = tiles;
     grid = (int)((total + g.chunk - 1) / g.chunk);
   }
   return grid;
@@ -1371,6 +1428,10 @@ int gemm_run(const GemmCall &g, cudaStream_t st) {
       (g.dtype != DFLASH_BF16 || (g.dh != 64 && g.dh != 128) ||
        g.N_out != (g.Hq + 2 * g.Hkv) * g.dh || !g.q_norm || !g.k_norm || !g.rope_cs ||
        !g.out_bf16))
+    return DFLASH_ERR_DIMS;
+  if (g.T0 < 0 || g.T0 > g.T) return DFLASH_ERR_DIMS;
+  if (g.T0 > 0 && g.T0 < g.T &&
+      (g.mode != GEMM_QKV || !g.ctx_slot || !g.kc || !g.vc || g.page_size < 1 || g.layer < 0))
     return DFLASH_ERR_DIMS;
   if (g.mode != GEMM_PARTIAL && g.S > 1 && (!g.counters || !g.out)) return DFLASH_ERR_NULL;
   if (g.dtype == DFLASH_F32) {

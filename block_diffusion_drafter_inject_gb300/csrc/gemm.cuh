@@ -66,6 +66,16 @@ struct GemmCall {
   const float2 *rope_cs = nullptr;
   int Hq = 0, Hkv = 0, dh = 0;
   float eps = 0.f;
+  // GEMM_QKV with injected context rows: tokens t >= T0 (0: none) are context
+  // rows whose k and v heads go to layer `layer` of the paged caches [L][page]
+  // [Hkv][page_size][dh] (layer_elems elements a layer) at element offset
+  // ctx_slot[t - T0] + head * page_size * dh + feature (rows with a negative
+  // slot are skipped); their q heads are dropped.
+  int T0 = 0;
+  const long long *ctx_slot = nullptr;
+  size_t layer_elems = 0;
+  int page_size = 0, layer = 0;
+  void *kc = nullptr, *vc = nullptr;
   // limit of the kernel's bounded waits (0: the default, kWaitLimitNs); stall
   // (failure-path test only, bf16): the MMA issuer first waits on a barrier
   // that nothing arrives on, so that the wait gives up

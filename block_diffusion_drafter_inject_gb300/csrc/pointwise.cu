@@ -85,11 +85,28 @@ __global__ void __launch_bounds__(1024) k_rows_norm(const S *__restrict__ in, in
                                                     S *__restrict__ out,
                                                     const int32_t *__restrict__ pos,
                                                     const dflh::RopeTable rope, int half,
-                                                    float2 *__restrict__ rope_cs) {
+                                                    float2 *__restrict__ rope_cs,
+                                                    const dflh::CacheSlots cs) {
   __shared__ float red[32];
   pdl_launch();
   pdl_wait();
   if (rope_cs) rope_row(rope_cs + (size_t)blockIdx.x * half, pos[blockIdx.x], rope, half);
+  if (cs.slot && threadIdx.x == 0) {
+    const int row = cs.req[blockIdx.x], p = pos[blockIdx.x];
+    long long s = -1;
+    if (row < 0 || row >= cs.num_rows) {
+      set_err(cs.err, DFLASH_DEV_REQ_RANGE);
+    } else if (p < 0 || p / cs.P >= cs.max_pages) {
+      set_err(cs.err, DFLASH_DEV_POS_RANGE);
+    } else {
+      const int page = cs.table[(size_t)row * cs.max_pages + p / cs.P];
+      if (page < 0 || page >= cs.num_pages)
+        set_err(cs.err, DFLASH_DEV_PAGE_RANGE);
+      else
+        s = ((long long)page * cs.Hkv * cs.P + p % cs.P) * cs.dh;
+    }
+    cs.slot[blockIdx.x] = s;
+  }
   const S *row = in + (size_t)blockIdx.x * cols;
   float ss = 0.f;
   for (int c = threadIdx.x * 8; c < cols; c += blockDim.x * 8) {
@@ -712,11 +729,11 @@ int launch_embed_norm(const S *E, const int32_t *anchor, int mask_id, int V, int
 template <typename S>
 int launch_rows_norm(const S *in, int rows, int cols, const S *gain, float eps, S *out,
                      const int32_t *pos, const RopeTable &rope, int half, float2 *rope_cs,
-                     cudaStream_t st) {
+                     cudaStream_t st, const CacheSlots &slots) {
   if (rows <= 0) return DFLASH_OK;
   const int threads = cols >= 8192 ? 1024 : cols >= 2048 ? 256 : 64;
   DFL_CHECK_LAUNCH(launch(dfl::k_rows_norm<S>, dim3(rows), dim3(threads), 0, st, in, cols, gain,
-                          eps, out, pos, rope, half, rope_cs));
+                          eps, out, pos, rope, half, rope_cs, slots));
   return DFLASH_OK;
 }
 template <typename S>
@@ -887,7 +904,8 @@ int launch_final_norm(const float *x, int B, int K, int D, const S *gain, float 
                                     float, float *, S *, int *, const int32_t *,                 \
                                     const RopeTable &, int, float2 *, cudaStream_t);             \
   template int launch_rows_norm<S>(const S *, int, int, const S *, float, S *, const int32_t *,  \
-                                   const RopeTable &, int, float2 *, cudaStream_t);              \
+                                   const RopeTable &, int, float2 *, cudaStream_t,               \
+                                   const CacheSlots &);                                          \
   template int launch_conv_pre<S>(const S *, const float *, int, int, int, int, const S *, S *,  \
                                   cudaStream_t);                                                 \
   template int launch_conv_post_norm<S>(const float *, const float *, int, int, int, int,        \

@@ -22,10 +22,20 @@ template <typename S>
 int launch_embed_norm(const S *E, const int32_t *anchor, int mask_id, int V, int B, int K, int D,
                       const S *gain, float eps, float *x, S *un, int *err, const int32_t *ctx_len,
                       const RopeTable &rope, int half, float2 *rope_cs, cudaStream_t st);
+// Cache place of each injected row (rows_norm, optional): slot[n] = element
+// offset of (page, position within the page) for head 0, feature 0 inside one
+// layer of the caches [L][num_pages][Hkv][P][dh], or -1 (and a status bit) when
+// req[n], pos[n] or the page fails the checks.
+struct CacheSlots {
+  const int32_t *req = nullptr, *table = nullptr;
+  int max_pages = 0, num_rows = 0, num_pages = 0, P = 0, Hkv = 0, dh = 0;
+  long long *slot = nullptr;
+  int *err = nullptr;
+};
 template <typename S>
 int launch_rows_norm(const S *in, int rows, int cols, const S *gain, float eps, S *out,
                      const int32_t *pos, const RopeTable &rope, int half, float2 *rope_cs,
-                     cudaStream_t st);
+                     cudaStream_t st, const CacheSlots &slots = CacheSlots());
 // gate: the conv's gate linear, fp32 [rows, 2D/group]
 template <typename S>
 int launch_conv_pre(const S *un, const float *gate, int rows, int K, int D, int group,

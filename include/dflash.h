@@ -6,6 +6,8 @@
  *   1. dflash_inject_context   target hidden states -> every draft layer's K/V cache
  *   2. dflash_draft_block      one non-causal drafter pass over a block of K slots,
  *                              per-position top-k candidates
+ *      dflash_draft_block_inject   1 and 2 in one pass (each layer's K/V
+ *                              weights read once)
  *   3. dflash_select_path      one coherent candidate path (Viterbi over the lattice)
  *      dflash_sample_path      ... or a temperature-1 walk drawn from the same scores
  *   4. dflash_accept_greedy    longest prefix that matches the target's argmax + bonus
@@ -185,6 +187,31 @@ int dflash_draft_block(const dflash_config *cfg, const dflash_weights *w,
                        const int32_t *ctx_len, int32_t B, int32_t K,
                        int32_t *topk_ids, float *topk_logp, float *logits_opt,
                        void *ws, size_t ws_bytes, void *stream);
+
+/* Injection and drafter pass in one call: the same results as
+ * dflash_inject_context(target_hidden, req, pos, N) followed by
+ * dflash_draft_block(anchor, ctx_len, B, K), with the new rows' K/V
+ * projections done inside each layer's QKV projection of the pass, so that
+ * every layer's K/V weights are read once per cycle instead of twice
+ * (Architecture page, "Internals Worth Knowing": the accepted tokens'
+ * target features are projected into draft KV right away, and the serving
+ * loop overlaps that with the next draft).  Layer l's injected K/V are
+ * written just before layer l's block attention reads the window, so rows
+ * at positions below ctx_len[b] are attended in this same pass.
+ *   target_hidden, req, pos, N   as dflash_inject_context (N <= the
+ *                                workspace's max_inject_tokens; N = 0: the
+ *                                pass alone); (req, pos) pairs must differ
+ *   anchor .. logits_opt          as dflash_draft_block
+ * B = 0 with N > 0 is the injection alone.  float32 storage runs the two
+ * calls in sequence.  Device-side checks of req, pos and pages as
+ * dflash_inject_context (the row is skipped, a status bit set).          */
+int dflash_draft_block_inject(const dflash_config *cfg, const dflash_weights *w,
+                              const dflash_kv *kv, const void *target_hidden,
+                              const int32_t *req, const int32_t *pos, int32_t N,
+                              const int32_t *anchor, const int32_t *ctx_len,
+                              int32_t B, int32_t K, int32_t *topk_ids,
+                              float *topk_logp, float *logits_opt, void *ws,
+                              size_t ws_bytes, void *stream);
 
 /* Candidate-path selector (Architecture page, "Problem 1", eq. S_t, in the
  * low-rank form (P_u e_a).(P_v e_b) with e = embedding rows, walked by

@@ -91,12 +91,26 @@ class Case:
         self.d_logits = torch.zeros((self.B, self.K - 1, V), dtype=torch.float32, device=dev)
         return self
 
-    def run_device(self):
+    def run_device(self, fused=True, tail=None):
+        """One cycle on the device.  fused: the injection rides in the draft pass
+        (draft_block_inject), else inject_context then draft_block.  tail[b]: only
+        the last tail[b] context rows of request b go through the cycle call; the
+        rest are injected before it (a prefill)."""
         import torch
-        self.cyc.run(self.d_hidden, self.d_req, self.d_pos, self.d_anchor, self.d_ctx,
-                     self.d_target, logits=self.d_logits)
-        torch.cuda.synchronize()
         import block_diffusion_drafter_inject_gb300 as dfl
+        hid, req, pos = self.d_hidden, self.d_req, self.d_pos
+        if tail is not None:
+            late = np.concatenate([self.pos[self.req == b] >= int(self.ctx[b]) - int(tail[b])
+                                   for b in range(self.B)])
+            early = torch.from_numpy(np.nonzero(~late)[0]).cuda()
+            if len(early):
+                dfl.inject_context(self.cfg, self.Wd, self.kv, hid[early], req[early],
+                                   pos[early], self.cyc.ws)
+            idx = torch.from_numpy(np.nonzero(late)[0]).cuda()
+            hid, req, pos = hid[idx], req[idx], pos[idx]
+        self.cyc.run(hid, req, pos, self.d_anchor, self.d_ctx, self.d_target,
+                     logits=self.d_logits, fused=fused)
+        torch.cuda.synchronize()
         status = dfl.read_device_status(self.cyc.ws)
         c = self.cyc
         return dict(ids=c.topk_ids.cpu().numpy(), logp=c.topk_logp.cpu().numpy(),
@@ -231,28 +245,45 @@ class FullCase:
             self._o = res
         return self._o
 
-    def device(self, max_inject=4096, sel_table=False):
+    def device(self, max_inject=4096, sel_table=False, tail=None):
         """Upload, inject the windows, run draft_block and select_path; with
-        sel_table, the selector reads the prepared table of every row's projections."""
+        sel_table, the selector reads the prepared table of every row's projections.
+        tail[b]: the last tail[b] window rows of request b are injected by the pass
+        itself (draft_block_inject) instead of beforehand."""
         import torch
         import block_diffusion_drafter_inject_gb300 as dfl
+        self.Wd = None
         self.Wd = dfl.DeviceWeights.from_host(self.cfg, self.W, "cuda")
         self.kv = dfl.PagedKV(self.cfg, self.table, self.num_pages, "cuda")
         self.cyc = dfl.DraftCycle(self.cfg, self.Wd, self.kv, self.B, self.K, max_inject, "cuda")
         if sel_table:
             dfl.prepare_selector(self.cfg, self.Wd, self.cyc.ws)
-        hid = torch.from_numpy(self.hidden).to(torch.bfloat16).cuda()
-        req = torch.from_numpy(self.req).cuda()
-        pos = torch.from_numpy(self.pos).cuda()
-        for o in range(0, len(self.req), max_inject):
+        late = np.zeros(len(self.req), bool)
+        if tail is not None:
+            late = self.pos >= self.ctx[self.req] - np.asarray(tail)[self.req]
+        early = np.nonzero(~late)[0]
+        hid = torch.from_numpy(self.hidden[early]).to(torch.bfloat16).cuda()
+        req = torch.from_numpy(self.req[early]).cuda()
+        pos = torch.from_numpy(self.pos[early]).cuda()
+        for o in range(0, len(early), max_inject):
             sl = slice(o, o + max_inject)
             dfl.inject_context(self.cfg, self.Wd, self.kv, hid[sl], req[sl], pos[sl], self.cyc.ws)
         self.d_anchor = torch.from_numpy(self.anchor).cuda()
         self.d_ctx = torch.from_numpy(self.ctx).cuda()
         self.d_logits = torch.zeros((self.B, self.K - 1, self.cfg["vocab"]), dtype=torch.float32,
                                     device="cuda")
-        dfl.draft_block(self.cfg, self.Wd, self.kv, self.d_anchor, self.d_ctx, self.K, self.cyc.ws,
-                        self.cyc.topk_ids, self.cyc.topk_logp, self.d_logits)
+        if tail is None:
+            dfl.draft_block(self.cfg, self.Wd, self.kv, self.d_anchor, self.d_ctx, self.K,
+                            self.cyc.ws, self.cyc.topk_ids, self.cyc.topk_logp, self.d_logits)
+        else:
+            lt = np.nonzero(late)[0]
+            self.n_fused = len(lt)
+            dfl.draft_block_inject(
+                self.cfg, self.Wd, self.kv,
+                torch.from_numpy(self.hidden[lt]).to(torch.bfloat16).cuda(),
+                torch.from_numpy(self.req[lt]).cuda(), torch.from_numpy(self.pos[lt]).cuda(),
+                self.d_anchor, self.d_ctx, self.K, self.cyc.ws, self.cyc.topk_ids,
+                self.cyc.topk_logp, self.d_logits)
         dfl.select_path(self.cfg, self.Wd, self.d_anchor, self.cyc.topk_ids, self.cyc.topk_logp,
                         self.K, self.cyc.ws, self.cyc.path, self.cyc.score)
         torch.cuda.synchronize()

@@ -141,6 +141,31 @@ def test_draft_block_host_checks(dfl):
     assert call(cfg=c3) == -5
 
 
+def test_draft_block_inject_host_checks(dfl):
+    L = dfl.lib()
+    cfg = _cfg(dfl)
+    w = _fake_weights(dfl, cfg)
+    kv = _fake_kv(dfl)
+    P = ctypes.c_void_p
+    a = P(1 << 24)
+    need = L.dflash_workspace_bytes(ctypes.byref(cfg), 2, 8, 4)
+
+    def call(N=4, hid=a, B=2, K=8, nbytes=need, ws=a):
+        return L.dflash_draft_block_inject(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(kv),
+                                           hid, a, a, N, a, a, B, K, a, a, None, ws, nbytes, None)
+
+    assert call(N=-1) == -2
+    assert call(K=1) == -3
+    assert call(B=0, N=0) == 0                  # nothing to do
+    assert call(hid=P(0)) == -1                 # rows without hidden states
+    assert call(hid=P((1 << 24) + 2)) == -7     # misaligned hidden states
+    assert call(N=5) == -4                      # more rows than the workspace holds
+    assert call(nbytes=need - 1) == -4
+    assert call(ws=P((1 << 24) + 4)) == -7
+    # the workspace of a larger injection capacity holds the pass with rows
+    assert L.dflash_workspace_bytes(ctypes.byref(cfg), 2, 8, 64) >= need
+
+
 def test_inject_select_accept_linear_host_checks(dfl):
     L = dfl.lib()
     cfg = _cfg(dfl)

@@ -103,6 +103,10 @@ def test_full_b1_k8_ctx2048():
     case = FullCase(1, 8, [2048], seed=0).device()
     assert case.status == 0
     _check_request(case, 0)
+    # the serving cycle: the last 8 context rows injected by the pass itself
+    case.device(tail=[8])
+    assert case.status == 0 and case.n_fused == 8
+    _check_request(case, 0)
 
 
 def test_full_b1_unaligned_window_with_selector_table():
@@ -152,6 +156,14 @@ def test_full_b32_ragged_paged_subset():
     assert len(reqs) == 4
     case = FullCase(32, 8, ctx, seed=2, oracle_requests=reqs).device()
     assert case.status == 0
+    for b in reqs:
+        _check_request(case, b)
+    # the same requests with the last 0..8 rows of each injected by the pass itself
+    tail = synth.stream(2, "fused_tail").integers(0, 9, 32)
+    tail[reqs[0]] = 0
+    tail[reqs[1]] = 8
+    case.device(tail=tail)
+    assert case.status == 0 and case.n_fused == int(tail.sum())
     for b in reqs:
         _check_request(case, b)
 

@@ -47,11 +47,24 @@ def _case_id(c):
     return f"{name}-B{B}-K{K}" + "".join(f"-{k}{v}" for k, v in over.items())
 
 
-@pytest.fixture(scope="module", params=CASES, ids=_case_id)
+_made = {}
+
+
+# Every case runs the cycle both ways: the injection inside the draft pass
+# (draft_block_inject: each layer's QKV projection also forms the injected rows'
+# K/V) and as two calls (inject_context, then draft_block).  The oracle is the
+# same for both.
+@pytest.fixture(scope="module", params=[(c, f) for c in CASES for f in (True, False)],
+                ids=lambda p: _case_id(p[0]) + ("-fused" if p[1] else "-two_calls"))
 def case(request):
-    name, B, K, ctx, over = request.param
-    c = Case(name, B, K, ctx, seed=len(ctx) + K, **over).device()
-    c.g = c.run_device()
+    spec, fused = request.param
+    name, B, K, ctx, over = spec
+    key = _case_id(spec)
+    if key not in _made:
+        _made.clear()
+        _made[key] = Case(name, B, K, ctx, seed=len(ctx) + K, **over)
+    c = _made[key].device()
+    c.g = c.run_device(fused=fused)
     return c
 
 
@@ -259,3 +272,59 @@ def test_accept_nan_rows(dtype, noalloc):
     np.testing.assert_array_equal(acc.cpu().numpy(), want_acc)
     np.testing.assert_array_equal(tok.cpu().numpy(), want_tok)
     assert list(want_tok[0][:2]) == [12345, 0] and want_tok[1][0] == 9000
+
+
+@pytest.mark.parametrize("name,ctx,tail", [
+    ("tiny_bf16", [70, 5, 130], [7, 0, 3]),
+    ("small_gqa", [200, 129], [1, 8]),
+    ("tiny_bf16", [40, 64, 9, 100], [8, 8, 8, 8]),
+    ("tiny", [64, 33], [8, 2]),     # float32 storage: the two calls in sequence
+])
+def test_fused_tail_after_prefill(name, ctx, tail):
+    """The serving cycle: each request's context up to its last tail[b] rows is
+    injected beforehand and those last rows by the draft pass itself
+    (draft_block_inject, the rows' K/V formed in each layer's QKV projection and
+    attended in the same pass).  Cache rows, logits and top-k as the oracle's,
+    which injects every row and then drafts."""
+    c = Case(name, len(ctx), 8, ctx, seed=31).device()
+    g = c.run_device(fused=True, tail=tail)
+    assert g["status"] == 0
+    o = c.oracle()
+    gk, gv = c.gpu_kv_dense()
+    tol = KV_TOL[c.cfg["dtype"]]
+    for b in range(c.B):
+        for l in range(c.cfg["n_layers"]):
+            assert rowmax_rel(gk[b][l], o["ck"][b][l]) < tol, (b, l)
+            assert rowmax_rel(gv[b][l], o["cv"][b][l]) < tol, (b, l)
+    err = rowmax_rel(g["logits"], o["logits"])
+    assert err < TOL[c.cfg["dtype"]], err
+    compared, bad = topk_compare(g["ids"], o["logits"], o["ids"], c.cfg["top_k"])
+    assert compared > 0 and bad == 0, (compared, bad)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_injected_rows_failing_device_checks_are_skipped(fused):
+    """Rows whose request row, position or page fails the device checks set their
+    status bits and are skipped; the rest of the cycle is unaffected (logits as the
+    oracle's on the valid context)."""
+    import block_diffusion_drafter_inject_gb300 as dfl
+    c = Case("tiny_bf16", 2, 8, [40, 200], seed=9).device()
+    dfl.inject_context(c.cfg, c.Wd, c.kv, c.d_hidden, c.d_req, c.d_pos, c.cyc.ws)
+    P = c.cfg["page_size"]
+    assert c.table[0, 1] == -1 and c.table.shape[1] == 4
+    # request row 2 of 2; position beyond request 0's 4-page table; page entry -1
+    req = torch.tensor([2, 0, 0], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([10, 4 * P + 3, P + 36], dtype=torch.int32, device="cuda")
+    hid = c.d_hidden[:3].clone()
+    if fused:
+        dfl.draft_block_inject(c.cfg, c.Wd, c.kv, hid, req, pos, c.d_anchor, c.d_ctx, c.K,
+                               c.cyc.ws, c.cyc.topk_ids, c.cyc.topk_logp, c.d_logits)
+    else:
+        dfl.inject_context(c.cfg, c.Wd, c.kv, hid, req, pos, c.cyc.ws)
+        dfl.draft_block(c.cfg, c.Wd, c.kv, c.d_anchor, c.d_ctx, c.K, c.cyc.ws, c.cyc.topk_ids,
+                        c.cyc.topk_logp, c.d_logits)
+    torch.cuda.synchronize()
+    want = dfl.DEV_REQ_RANGE | dfl.DEV_POS_RANGE | dfl.DEV_PAGE_RANGE
+    assert dfl.read_device_status(c.cyc.ws) == want
+    err = rowmax_rel(c.d_logits.cpu().numpy(), c.oracle()["logits"])
+    assert err < TOL["bf16"], err
