@@ -16,6 +16,8 @@ unpinned for the composition; each step is pinned separately.
 from .dflash import (  # noqa: F401
     round_bf16,
     storage_round,
+    dequantize_affine,
+    quantized_weights,
     rmsnorm,
     rope,
     conv_two_tap,

@@ -39,6 +39,33 @@ def storage_round(x, contract):
 
 
 # ----------------------------------------------------------------------------
+# 4-bit drafter weights
+# ----------------------------------------------------------------------------
+
+def dequantize_affine(q, scale, bias, group):
+    """Weights of a drafter kept in 4 bits (README mirror, MLX section: the
+    example runs target and draft with 4-bit weights through a quantized matmul).
+    Each row of an [N, K] matrix is cut into groups of `group` consecutive input
+    features, each with its own scale s and bias b; the weight the product uses is
+    s*q + b rounded once to bfloat16, q in 0..15.
+
+    q [N, K] integers; scale, bias [N, K/group].  Returns [N, K] float64."""
+    q = np.asarray(q, dtype=F64)
+    s = np.repeat(np.asarray(scale, dtype=F64), group, axis=1)
+    b = np.repeat(np.asarray(bias, dtype=F64), group, axis=1)
+    return round_bf16(s * q + b)
+
+
+def quantized_weights(W, Q, group=64):
+    """The weight set W with every matrix named in Q (name -> (q, scale, bias))
+    replaced by its dequantized values; the rest of the drafter is unchanged."""
+    out = dict(W)
+    for name, (q, s, b) in Q.items():
+        out[name] = dequantize_affine(q, s, b, group)
+    return out
+
+
+# ----------------------------------------------------------------------------
 # building blocks
 # ----------------------------------------------------------------------------
 

@@ -21,6 +21,8 @@ from .gen import (  # noqa: F401
     bf16_bits_to_f32,
     f32_to_bf16_bits,
     make_weights,
+    make_q4_weights,
+    q4_names,
     make_hiddens,
     make_anchors,
     make_target_logits,

@@ -122,6 +122,54 @@ def make_weights(cfg, seed=0, sel_scale=0.02, base_scale=1.0, w_scale=0.02, name
     return W
 
 
+def q4_names(cfg):
+    """The matrices a 4-bit drafter keeps in 4 bits: the injection fc, every layer's
+    QKV, O, gate/up and down projections, and the lm_head."""
+    out = ["fc", "lm_head"]
+    for l in range(cfg["n_layers"]):
+        out += [f"layers.{l}.{n}" for n in ("wqkv", "wo", "w_gate_up", "w_down")]
+    return out
+
+
+def _uniform_u4(base_seed, name, shape, threads=None):
+    """Integers uniform on 0..15 (uint8), drawn in fixed chunks."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint8)
+    nchunks = (n + CHUNK - 1) // CHUNK
+
+    def fill(c):
+        lo, hi = c * CHUNK, min(n, (c + 1) * CHUNK)
+        out[lo:hi] = stream(base_seed, name, c).integers(0, 16, hi - lo, dtype=np.uint8)
+
+    if nchunks == 1:
+        fill(0)
+    else:
+        with ThreadPoolExecutor(threads or min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(nchunks)))
+    return out.reshape(shape)
+
+
+def make_q4_weights(cfg, seed=0, group=64, names=None):
+    """4-bit weights of the matrices in q4_names: name -> (q, scale, bias) with q
+    [N, K] uint8 uniform on 0..15 and, per group of `group` input features of a
+    row, scale uniform on [0.002, 0.006] and bias -7.5*scale + N(0, 0.002), both
+    bf16 values (float32 arrays), so the weights s*q + b spread over about
+    +-0.03 around zero (std ~0.018, like the N(0, 0.02) bf16 weights)."""
+    shapes = {n: sh for n, sh, _ in weight_names(cfg)}
+    Q = {}
+    for name in q4_names(cfg):
+        if names is not None and name not in names:
+            continue
+        N, K = shapes[name]
+        q = _uniform_u4(seed, name + ".q", (N, K))
+        g = stream(seed, name + ".scale")
+        sc = _to_storage(g.uniform(0.002, 0.006, (N, K // group)).astype(np.float32), "bf16")
+        nb = stream(seed, name + ".bias").standard_normal((N, K // group), dtype=np.float32)
+        bias = _to_storage(np.float32(-7.5) * sc + np.float32(0.002) * nb, "bf16")
+        Q[name] = (q, sc, bias)
+    return Q
+
+
 def make_hiddens(cfg, N, seed=0, name="hiddens"):
     """Concatenated target hidden states of the tapped layers, [N, n_taps*d_target], N(0,1)."""
     return _normal(seed, name, (N, cfg["n_taps"] * cfg["d_target"]), 0.0, 1.0, cfg["dtype"])

@@ -437,3 +437,58 @@ def test_accept_argmax_orders_nan_above_numbers():
     assert (n, list(toks)) == (3, [1, 1, 0])
     n, toks = oracle.accept_greedy_request(np.array([2, 1]), T)
     assert (n, list(toks)) == (1, [1, -1, -1])
+
+
+# ---------------------------------------------------------------- 4-bit weights
+
+def test_dequantize_hand_fixture():
+    """s*q + b rounded once to bf16, one (s, b) per group of 64 input features of
+    a row: hand-worked values, including two rounding cases and two ties."""
+    fx = json.load(open(os.path.join(GOLD, "q4_hand.json")))
+    g = fx["group"]
+    s = np.asarray(fx["scale"])
+    b = np.asarray(fx["bias"])
+    q = np.zeros((s.shape[0], s.shape[1] * g), np.int64)
+    for r, c, qq, _, _ in fx["entries"]:
+        q[r, c] = qq
+    w = oracle.dequantize_affine(q, s, b, g)
+    for r, c, qq, want, note in fx["entries"]:
+        assert w[r, c] == want, (r, c, qq, w[r, c], note)
+    # every other weight is its group's bias (q = 0; the biases are bf16 values)
+    rest = q == 0
+    want_rest = np.repeat(b, g, axis=1)
+    np.testing.assert_array_equal(w[rest], want_rest[rest])
+
+
+def test_dequantized_product_factors_through_groups():
+    """With power-of-two scales and small integer biases every step is exact, so
+    x @ W^T must equal the group-factored sum  sum_g [s_g sum_k x_k q_k + b_g sum_k x_k]
+    written out with loops: pins which axis the groups run along."""
+    rng = np.random.default_rng(5)
+    N, K, g = 3, 256, 64
+    q = rng.integers(0, 16, (N, K))
+    s = 2.0 ** rng.integers(-6, -2, (N, K // g))
+    b = rng.integers(-4, 4, (N, K // g)).astype(np.float64)
+    x = rng.integers(-8, 8, (2, K)).astype(np.float64)
+    y = x @ oracle.dequantize_affine(q, s, b, g).T
+    want = np.zeros((2, N))
+    for t in range(2):
+        for n in range(N):
+            for j in range(K // g):
+                ks = range(j * g, (j + 1) * g)
+                want[t, n] += s[n, j] * sum(x[t, k] * q[n, k] for k in ks) + b[n, j] * sum(x[t, k] for k in ks)
+    np.testing.assert_array_equal(y, want)
+
+
+def test_quantized_weights_replace_only_named_matrices():
+    cfg = synth.preset("tiny_bf16")
+    W = synth.make_weights(cfg, seed=1)
+    Q = synth.make_q4_weights(cfg, seed=1)
+    Wq = oracle.quantized_weights(W, Q)
+    for name in W:
+        if name in Q:
+            q, s, b = Q[name]
+            assert Wq[name].shape == W[name].shape
+            np.testing.assert_array_equal(Wq[name], oracle.dequantize_affine(q, s, b, 64))
+        else:
+            assert Wq[name] is W[name]
