@@ -35,8 +35,10 @@ from .api import (  # noqa: F401
     inject_context,
     launch_count,
     linear,
+    linear_q4,
     linear_splits,
     make_config,
+    pack_q4,
     prepare_selector,
     read_device_status,
     sample_path,

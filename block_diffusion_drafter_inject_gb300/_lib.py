@@ -29,19 +29,29 @@ class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "d_model", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "d_ff", "vocab",
         "n_taps", "d_target", "window", "page_size", "top_k", "sel_rank", "conv_group",
-        "mask_token_id", "dtype")] + [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+        "mask_token_id", "dtype")] + [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+                                      ("weight_bits", ctypes.c_int32)]
+
+
+class Q4(ctypes.Structure):
+    _fields_ = [("codes", vp), ("sb", vp)]
+
+
+# the matrices a 4-bit drafter keeps in 4 bits
+Q4_LAYER = ("wqkv", "wo", "w_gate_up", "w_down")
+Q4_TOP = ("fc", "lm_head")
 
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [("attn_norm", vp), ("mlp_norm", vp), ("wqkv", vp), ("wo", vp), ("q_norm", vp),
                 ("k_norm", vp), ("w_gate_up", vp), ("w_down", vp), ("conv_w", vp * 4),
-                ("conv_base", vp * 4)]
+                ("conv_base", vp * 4)] + [(n + "_q4", Q4) for n in Q4_LAYER]
 
 
 class Weights(ctypes.Structure):
     _fields_ = [("fc_norm", vp), ("fc", vp), ("embed", vp), ("lm_head", vp), ("final_norm", vp),
                 ("sel_pu", vp), ("sel_pv", vp), ("layer", LayerWeights * MAX_LAYERS),
-                ("sel_table", vp), ("sel_gate", vp)]
+                ("sel_table", vp), ("sel_gate", vp)] + [(n + "_q4", Q4) for n in Q4_TOP]
 
 
 class KV(ctypes.Structure):
@@ -79,6 +89,7 @@ EXPORTS = {
                                             vp, ctypes.c_size_t, vp]),
     "dflash_linear": (ctypes.c_int, [i32, vp, i32, i32, vp, i32, i32, vp, vp]),
     "dflash_linear_splits": (ctypes.c_int32, [i32, i32, i32]),
+    "dflash_linear_q4": (ctypes.c_int, [Q4, i32, i32, vp, i32, i32, vp, vp]),
     "dflash_test_linear_wait": (ctypes.c_int, [vp, i32, i32, vp, i32, vp, vp, ctypes.c_size_t,
                                                ctypes.c_uint32, vp]),
     "dflash_read_device_status": (ctypes.c_int, [vp, vp]),

@@ -24,6 +24,8 @@ def make_config(cfg):
             c.dtype = _DT[cfg["dtype"]]
         elif name == "mask_token_id":
             c.mask_token_id = int(cfg.get("mask_token_id", cfg["vocab"] - 1))
+        elif name == "weight_bits":
+            c.weight_bits = int(cfg.get("weight_bits", 0))
         else:
             setattr(c, name, type(getattr(c, name))(cfg[name]))
     return c
@@ -61,17 +63,58 @@ class DeviceWeights:
                 L.conv_base[i] = ptr(p + f"conv_base.{i}")
         if "sel_gate" in tensors:
             w.sel_gate = tensors["sel_gate"].data_ptr()
+        # 4-bit matrices: tensors NAME.codes and NAME.sb (see pack_q4)
+        q4 = lambda q, n: (setattr(q, "codes", ptr(n + ".codes")), setattr(q, "sb", ptr(n + ".sb")))
+        for n in _lib.Q4_TOP:
+            q4(getattr(w, n + "_q4"), n)
+        for l in range(cfg["n_layers"]):
+            for n in _lib.Q4_LAYER:
+                q4(getattr(w.layer[l], n + "_q4"), f"layers.{l}.{n}")
         self.struct = w
         self.sel_table = None  # see prepare_selector
 
     @classmethod
-    def from_host(cls, cfg, host, device="cuda"):
-        """Upload float32 host arrays (holding storage-dtype values) in the config dtype."""
+    def from_host(cls, cfg, host, device="cuda", q4=None):
+        """Upload float32 host arrays (holding storage-dtype values) in the config dtype.
+        q4: name -> (codes q [N, K] 0..15, scale [N, K/64], bias [N, K/64]) of the
+        matrices kept in 4 bits (their storage-dtype arrays in `host` are skipped)."""
         dt = _TORCH_DT[cfg["dtype"]]
         t = {}
         for name, arr in host.items():
+            if q4 is not None and name in q4:
+                continue
             t[name] = torch.from_numpy(arr).to(dt).to(device).contiguous()
+        for name, (q, sc, bias) in (q4 or {}).items():
+            codes, sb = pack_q4(q, sc, bias)
+            t[name + ".codes"] = codes.to(device)
+            t[name + ".sb"] = sb.to(device)
         return cls(cfg, t)
+
+
+def pack_q4(q, scale, bias):
+    """The C ABI's 4-bit layout of one matrix: codes [N, K/2] uint8 with the nibbles
+    of input features 8j..8j+7 in the order 8j, 8j+2, 8j+4, 8j+6, 8j+1, 8j+3, 8j+5,
+    8j+7 from the least significant of their 32-bit word, and (scale, bias) words
+    [K/64, N] int32 (bf16 scale bits low, bf16 bias bits high)."""
+    q = torch.as_tensor(q).to(torch.uint8)
+    N, K = q.shape
+    g = q.reshape(N, K // 8, 8)
+    lo = g[:, :, [0, 4, 1, 5]]
+    hi = g[:, :, [2, 6, 3, 7]]
+    codes = (lo | (hi << 4)).reshape(N, K // 2).contiguous()
+    bits = lambda a: torch.as_tensor(a).to(torch.bfloat16).view(torch.int16).to(torch.int32) & 0xFFFF
+    sb = (bits(scale) | (bits(bias) << 16)).t().contiguous()
+    return codes, sb
+
+
+def linear_q4(codes, sb, X, out, splits=1, stream=None):
+    """dflash_linear_q4: out[s] = the s-th K slice of X W^T with W in 4 bits."""
+    N_out, K2 = codes.shape
+    w = _lib.Q4()
+    w.codes = codes.data_ptr()
+    w.sb = sb.data_ptr()
+    check(lib().dflash_linear_q4(w, int(N_out), int(2 * K2), _ptr(X), int(X.shape[0]),
+                                 int(splits), _ptr(out), _stream(stream)), "dflash_linear_q4")
 
 
 class PagedKV:

@@ -82,23 +82,41 @@ static int check_cfg(const dflash_config *c) {
       c->top_k * c->sel_rank <= 16384 && c->conv_group >= 1 && c->d_model % c->conv_group == 0 &&
       c->mask_token_id >= 0 && c->mask_token_id < c->vocab && c->rms_eps >= 0.f &&
       c->rope_theta >= 0.f;
-  return ok ? DFLASH_OK : DFLASH_ERR_DIMS;
+  if (!ok) return DFLASH_ERR_DIMS;
+  if (c->weight_bits != 0 && c->weight_bits != 4) return DFLASH_ERR_DTYPE;
+  if (c->weight_bits == 4 && c->dtype != DFLASH_BF16) return DFLASH_ERR_DTYPE;
+  if (c->weight_bits == 4 && c->vocab % 4) return DFLASH_ERR_DIMS;  // (scale, bias) rows
+  return DFLASH_OK;
 }
 
 static bool a16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 
+// A projection: its storage-dtype matrix, or with 4-bit weights its codes and
+// (scale, bias) words.
+static int check_proj(const dflash_config *c, const void *w, const dflash_q4 &q) {
+  if (c->weight_bits == 4) {
+    if (!q.codes || !q.sb) return DFLASH_ERR_NULL;
+    return a16(q.codes) && a16(q.sb) ? DFLASH_OK : DFLASH_ERR_ALIGN;
+  }
+  if (!w) return DFLASH_ERR_NULL;
+  return a16(w) ? DFLASH_OK : DFLASH_ERR_ALIGN;
+}
+
 static int check_weights(const dflash_config *c, const dflash_weights *w, bool draft) {
   if (!w) return DFLASH_ERR_NULL;
-  if (!w->fc_norm || !w->fc) return DFLASH_ERR_NULL;
-  if (!a16(w->fc)) return DFLASH_ERR_ALIGN;
+  if (!w->fc_norm) return DFLASH_ERR_NULL;
+  int rc;
+  if ((rc = check_proj(c, w->fc, w->fc_q4)) != DFLASH_OK) return rc;
   for (int l = 0; l < c->n_layers; ++l) {
     const dflash_layer_weights &L = w->layer[l];
-    if (!L.wqkv || !L.k_norm) return DFLASH_ERR_NULL;
-    if (!a16(L.wqkv)) return DFLASH_ERR_ALIGN;
+    if (!L.k_norm) return DFLASH_ERR_NULL;
+    if ((rc = check_proj(c, L.wqkv, L.wqkv_q4)) != DFLASH_OK) return rc;
     if (!draft) continue;
-    if (!L.attn_norm || !L.mlp_norm || !L.wo || !L.q_norm || !L.w_gate_up || !L.w_down)
-      return DFLASH_ERR_NULL;
-    if (!a16(L.wo) || !a16(L.w_gate_up) || !a16(L.w_down)) return DFLASH_ERR_ALIGN;
+    if (!L.attn_norm || !L.mlp_norm || !L.q_norm) return DFLASH_ERR_NULL;
+    if ((rc = check_proj(c, L.wo, L.wo_q4)) != DFLASH_OK ||
+        (rc = check_proj(c, L.w_gate_up, L.w_gate_up_q4)) != DFLASH_OK ||
+        (rc = check_proj(c, L.w_down, L.w_down_q4)) != DFLASH_OK)
+      return rc;
     for (int i = 0; i < 4; ++i) {
       if (!L.conv_w[i] || !L.conv_base[i]) return DFLASH_ERR_NULL;
       if (!a16(L.conv_w[i]) || !a16(L.conv_base[i])) return DFLASH_ERR_ALIGN;
@@ -106,8 +124,9 @@ static int check_weights(const dflash_config *c, const dflash_weights *w, bool d
     if (!a16(L.mlp_norm)) return DFLASH_ERR_ALIGN;
   }
   if (draft) {
-    if (!w->embed || !w->lm_head || !w->final_norm) return DFLASH_ERR_NULL;
-    if (!a16(w->lm_head) || !a16(w->embed) || !a16(w->final_norm)) return DFLASH_ERR_ALIGN;
+    if (!w->embed || !w->final_norm) return DFLASH_ERR_NULL;
+    if ((rc = check_proj(c, w->lm_head, w->lm_head_q4)) != DFLASH_OK) return rc;
+    if (!a16(w->embed) || !a16(w->final_norm)) return DFLASH_ERR_ALIGN;
     for (int l = 0; l < c->n_layers; ++l)
       if (!a16(w->layer[l].attn_norm)) return DFLASH_ERR_ALIGN;
   }
@@ -279,6 +298,16 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   return true;
 }
 
+// The call reads weight matrix rows [row0, row0 + its rows) of a 4-bit matrix
+// with `rows` rows and K_in input features.
+static GemmCall with_q4(GemmCall g, const dflash_q4 &q, int rows, int K_in, int row0 = 0) {
+  g.Wq = (const uint8_t *)q.codes + (size_t)row0 * (K_in / 2);
+  g.Wsb = q.sb;
+  g.sb_rows = rows;
+  g.q_row0 = row0;
+  return g;
+}
+
 // A plan chosen at call time for a token count the layout sampled around: one
 // K slice when its slice scratch would not fit the workspace's.
 static GemmPlan fit_plan(const dflash_config &c, const Layout &L, int N_out, int T, int K_in,
@@ -341,13 +370,15 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
                           rope, dh / 2, rope_cs, st));
   const GemmPlan S_fc =
       fit_plan(c, L, D, N, TIN, GEMM_REDUCE, reduce_plan(&c, D, N, TIN, GEMM_REDUCE, sms));
-  TRY(gemm_run(reduce_call(c, ws, L, w.fc, D, TIN, gn, N, S_fc, GEMM_REDUCE, nullptr, D, cb, D),
-               st));
+  const bool q4 = c.weight_bits == 4;
+  GemmCall gf = reduce_call(c, ws, L, w.fc, D, TIN, gn, N, S_fc, GEMM_REDUCE, nullptr, D, cb, D);
+  if (q4) gf = with_q4(gf, w.fc_q4, D, TIN);
+  TRY(gemm_run(gf, st));
   // the [Wk; Wv] rows of every layer: one grouped launch per kKvGroup layers
   // (layer l's projection -> kvf [l][N][W2])
   LayerPtrs kn;
   memset(&kn, 0, sizeof(kn));
-  const bool grouped = c.dtype == DFLASH_BF16 && W2 % 128 == 0;
+  const bool grouped = c.dtype == DFLASH_BF16 && W2 % 128 == 0 && !q4;
   const int per = grouped ? kKvGroup : 1;
   for (int l0 = 0; l0 < c.n_layers; l0 += per) {
     const int ng = std::min(per, c.n_layers - l0);
@@ -358,6 +389,7 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
     g.groups = ng;
     g.ostride = (size_t)N * W2;
     for (int j = 1; j < ng; ++j) g.Wg[j] = (const S *)w.layer[l0 + j].wqkv + (size_t)Hq * dh * D;
+    if (q4) g = with_q4(g, w.layer[l0].wqkv_q4, (Hq + 2 * Hkv) * dh, D, Hq * dh);
     TRY(gemm_run(g, st));
   }
   for (int l = 0; l < c.n_layers; ++l) kn.p[l] = w.layer[l].k_norm;
@@ -407,6 +439,7 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   // QKV operand, so each layer's QKV GEMM also forms their K/V and stores them
   const int N = c.dtype == DFLASH_BF16 ? inj.N : 0;
   const int Tq = T + N;
+  const bool q4 = c.weight_bits == 4;
   // each injected row's place in a layer's cache, found (and checked) once
   CacheSlots slots;
   if (N > 0) {
@@ -440,6 +473,7 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     gq.Hkv = Hkv;
     gq.dh = dh;
     gq.eps = eps;
+    if (q4) gq = with_q4(gq, lw.wqkv_q4, QKVW, D);
     if (N > 0) {
       gq.T0 = T;
       gq.ctx_slot = slots.slot;
@@ -452,22 +486,25 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     return gq;
   };
   auto o_call = [&](int l) {
-    return reduce_call(c, ws, L, w.layer[l].wo, D, Hq * dh, ob, T, L.P_o, GEMM_REDUCE, rf, D, rb,
-                       D);
+    GemmCall g = reduce_call(c, ws, L, w.layer[l].wo, D, Hq * dh, ob, T, L.P_o, GEMM_REDUCE, rf,
+                             D, rb, D);
+    return q4 ? with_q4(g, w.layer[l].wo_q4, D, Hq * dh) : g;
   };
   auto gu_call = [&](int l) {
-    return reduce_call(c, ws, L, w.layer[l].w_gate_up, F, D, ub, T, L.P_gu, GEMM_SWIGLU, nullptr,
-                       0, hb, F);
+    GemmCall g = reduce_call(c, ws, L, w.layer[l].w_gate_up, F, D, ub, T, L.P_gu, GEMM_SWIGLU,
+                             nullptr, 0, hb, F);
+    return q4 ? with_q4(g, w.layer[l].w_gate_up_q4, 2 * F, D) : g;
   };
   auto down_call = [&](int l) {
-    return reduce_call(c, ws, L, w.layer[l].w_down, D, F, hb, T, L.P_down, GEMM_REDUCE, rf, D, rb,
-                       D);
+    GemmCall g = reduce_call(c, ws, L, w.layer[l].w_down, D, F, hb, T, L.P_down, GEMM_REDUCE, rf,
+                             D, rb, D);
+    return q4 ? with_q4(g, w.layer[l].w_down_q4, D, F) : g;
   };
   auto lm_call = [&]() {
     GemmCall gl = reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, GemmPlan{0, 1}, GEMM_REDUCE,
                               logits, V, nullptr, 0);
     gl.stats = tstats;
-    return gl;
+    return q4 ? with_q4(gl, w.lm_head_q4, V, D) : gl;
   };
   // A few block rows: each conv is one launch with its gate linear fused (the
   // pre-norm formed inside).  More rows: the gate linear is a tensor-core GEMM
@@ -508,9 +545,10 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
                             rope, dh / 2, rope_cs + (size_t)T * (dh / 2), st, slots));
     const GemmPlan pf = fit_plan(c, L, D, N, TIN, GEMM_REDUCE,
                                  reduce_plan(&c, D, N, TIN, GEMM_REDUCE, device()->num_sms));
-    TRY(gemm_run(reduce_call(c, ws, L, w.fc, D, TIN, gn, N, pf, GEMM_REDUCE, nullptr, D,
-                             ub + (size_t)T * D, D),
-                 st));
+    GemmCall gf =
+        reduce_call(c, ws, L, w.fc, D, TIN, gn, N, pf, GEMM_REDUCE, nullptr, D, ub + (size_t)T * D, D);
+    if (q4) gf = with_q4(gf, w.fc_q4, D, TIN);
+    TRY(gemm_run(gf, st));
   }
   TRY(launch_embed_norm<S>((const S *)w.embed, anchor, c.mask_token_id, V, B, K, D,
                            (const S *)w.layer[0].attn_norm, eps, x, fused ? (S *)nullptr : un, err,
@@ -898,6 +936,28 @@ int dflash_linear(int32_t dtype, const void *W, int32_t N_out, int32_t K_in, con
   if (!a16(W) || !a16(X)) return DFLASH_ERR_ALIGN;
   if (!device()) return DFLASH_ERR_DEVICE;
   return gemm_xwT(dtype, W, N_out, K_in, X, T, out, N_out, splits, nullptr, (cudaStream_t)stream);
+}
+
+int dflash_linear_q4(dflash_q4 W, int32_t N_out, int32_t K_in, const void *X, int32_t T,
+                     int32_t splits, float *out, void *stream) {
+  if (N_out < 4 || N_out % 4 || T < 0 || K_in < 64 || K_in % 64) return DFLASH_ERR_DIMS;
+  if (splits < 1 || (K_in / 64) % splits) return DFLASH_ERR_DIMS;
+  if (T == 0) return DFLASH_OK;
+  if (!W.codes || !W.sb || !X || !out) return DFLASH_ERR_NULL;
+  if (!a16(W.codes) || !a16(W.sb) || !a16(X)) return DFLASH_ERR_ALIGN;
+  if (!device()) return DFLASH_ERR_DEVICE;
+  GemmCall g;
+  g.dtype = DFLASH_BF16;
+  g.N_out = N_out;
+  g.K_in = K_in;
+  g.X = X;
+  g.T = T;
+  g.S = splits;
+  g.mode = GEMM_PARTIAL;
+  g.out = out;
+  g.ld = N_out;
+  g = with_q4(g, W, N_out, K_in);
+  return gemm_run(g, (cudaStream_t)stream);
 }
 
 int dflash_test_linear_wait(const void *W, int32_t N_out, int32_t K_in, const void *X, int32_t T,

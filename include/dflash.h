@@ -98,7 +98,27 @@ typedef struct dflash_config {
   int32_t dtype;        /* DFLASH_F32 or DFLASH_BF16                        */
   float rms_eps;        /* RMSNorm epsilon                                  */
   float rope_theta;     /* RoPE base; 0 disables RoPE                       */
+  int32_t weight_bits;  /* 0: every weight in the storage dtype; 4: the
+                           projections fc, wqkv, wo, w_gate_up, w_down and
+                           lm_head in the 4-bit format below (bf16 storage) */
 } dflash_config;
+
+/* 4-bit weights (README mirror, MLX section: the drafter runs with 4-bit
+ * weights).  A matrix W [N, K] (K a multiple of 64) is kept as 4-bit codes q
+ * and, per row and group of 64 consecutive input features, a bf16 scale s and
+ * bias b; the products use w = bf16(s*q + b) (s*q + b rounded once, to
+ * nearest even), activations stay bf16.
+ *   codes  device [N][K/2] bytes, 16-byte aligned.  The 32-bit little-endian
+ *          word holding input features 8j..8j+7 of a row keeps their codes,
+ *          from the least significant nibble up, in the order 8j, 8j+2, 8j+4,
+ *          8j+6, 8j+1, 8j+3, 8j+5, 8j+7.
+ *   sb     device [K/64][N] 32-bit words, 16-byte aligned, N % 4 == 0: word
+ *          (g, n) holds the bf16 scale of row n, group g in its low 16 bits and
+ *          the bf16 bias in its high 16 bits.                              */
+typedef struct dflash_q4 {
+  const void *codes;
+  const void *sb;
+} dflash_q4;
 
 /* One draft layer.  All device pointers, dtype of the config. */
 typedef struct dflash_layer_weights {
@@ -114,6 +134,9 @@ typedef struct dflash_layer_weights {
                               two-tap convs: 0 before attention, 1 after attention,
                               2 before the MLP, 3 after the MLP                     */
   const void *conv_base[4];/* [2D] base kernels [base_a; base_b] of the same convs  */
+  /* weight_bits == 4: the 4-bit forms of wqkv, wo, w_gate_up and w_down (their
+   * storage-dtype pointers above are then unused and may be NULL) */
+  dflash_q4 wqkv_q4, wo_q4, w_gate_up_q4, w_down_q4;
 } dflash_layer_weights;
 
 typedef struct dflash_weights {
@@ -132,6 +155,9 @@ typedef struct dflash_weights {
   /* optional: [r, D] W_H of the context gate H(h) = sigmoid(W_H h) of the
    * gated selector (dflash_select_greedy); unused by the other calls */
   const void *sel_gate;
+  /* weight_bits == 4: the 4-bit forms of fc and lm_head (fc and lm_head above
+   * then unused) */
+  dflash_q4 fc_q4, lm_head_q4;
 } dflash_weights;
 
 /* Paged per-layer draft KV cache.
@@ -363,6 +389,13 @@ int dflash_accept_greedy_noalloc(const int32_t *path, const void *target_logits,
  * K_in must be a multiple of 64. */
 int dflash_linear(int32_t dtype, const void *W, int32_t N_out, int32_t K_in, const void *X,
                   int32_t T, int32_t splits, float *out, void *stream);
+/* The same product with W in the 4-bit format (w = bf16(s*q + b)) and bf16 X:
+ * tensor-core GEMM whose weight tiles are dequantized in shared memory.
+ *   W       codes / (scale, bias) words of W [N_out, K_in]; N_out % 4 == 0,
+ *           K_in a multiple of 64
+ *   X, splits, out   as dflash_linear                                       */
+int dflash_linear_q4(dflash_q4 W, int32_t N_out, int32_t K_in, const void *X, int32_t T,
+                     int32_t splits, float *out, void *stream);
 int32_t dflash_linear_splits(int32_t N_out, int32_t T, int32_t K_in);
 
 /* Test hook for the failure-detection path of the projection GEMM (no

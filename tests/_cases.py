@@ -17,6 +17,11 @@ class Case:
         self.ctx = np.asarray(ctx, dtype=np.int32)
         self.seed = seed
         self.W = synth.make_weights(self.cfg, seed=seed, sel_scale=sel_scale)
+        # 4-bit drafter: the device gets the codes, the oracle the weights they stand for
+        self.Q = None
+        if self.cfg.get("weight_bits", 0) == 4:
+            self.Q = synth.make_q4_weights(self.cfg, seed=seed)
+            self.W = oracle.quantized_weights(self.W, self.Q)
         self.contract = self.cfg["dtype"]
         ntot = int(self.ctx.sum())
         self.hidden = synth.make_hiddens(self.cfg, max(ntot, 1), seed=seed)[:ntot]
@@ -76,7 +81,7 @@ class Case:
         import torch
         import block_diffusion_drafter_inject_gb300 as dfl
         dev = "cuda"
-        self.Wd = dfl.DeviceWeights.from_host(self.cfg, self.W, dev)
+        self.Wd = dfl.DeviceWeights.from_host(self.cfg, self.W, dev, q4=self.Q)
         self.kv = dfl.PagedKV(self.cfg, self.table, self.num_pages, dev)
         dt = torch.bfloat16 if self.cfg["dtype"] == "bf16" else torch.float32
         self.d_hidden = torch.from_numpy(self.hidden).to(dt).to(dev)

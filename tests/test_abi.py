@@ -223,3 +223,80 @@ def test_launch_counter_resets(dfl):
     L = dfl.lib()
     L.dflash_launch_count(1)
     assert L.dflash_launch_count(0) == 0
+
+
+def test_q4_host_checks(dfl):
+    """4-bit weights: the config's weight_bits (0 or 4, bf16 storage only), the
+    codes / (scale, bias) pointers of every projection, dflash_linear_q4's shape
+    rules; all refused before any launch."""
+    L = dfl.lib()
+    P = ctypes.c_void_p
+    a = P(1 << 24)
+    kv = _fake_kv(dfl)
+    need = 1 << 40
+
+    def draft(cfg, w):
+        return L.dflash_draft_block(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(kv), a, a,
+                                    2, 8, a, a, None, a, need, None)
+
+    cfg = _cfg(dfl, weight_bits=3)
+    assert draft(cfg, _fake_weights(dfl, cfg)) == -5
+    cfg = _cfg(dfl, weight_bits=4, dtype=0)                 # float32 storage
+    assert draft(cfg, _fake_weights(dfl, cfg)) == -5
+    cfg = _cfg(dfl, weight_bits=4)
+    w = _fake_weights(dfl, cfg)                             # storage-dtype pointers only
+    assert draft(cfg, w) == -1
+    base = 1 << 26
+    for n in dfl._lib.Q4_TOP:
+        q = getattr(w, n + "_q4")
+        q.codes, q.sb = base, base + 4096
+        base += 8192
+    for l in range(cfg.n_layers):
+        for n in dfl._lib.Q4_LAYER:
+            q = getattr(w.layer[l], n + "_q4")
+            q.codes, q.sb = base, base + 4096
+            base += 8192
+    w.layer[1].w_down_q4.sb = base + 8                      # misaligned
+    assert draft(cfg, w) == -7
+    w.layer[1].w_down_q4.sb = base
+    w.layer[0].wo_q4.codes = 0
+    assert draft(cfg, w) == -1
+    # the 4-bit product
+    q = dfl._lib.Q4()
+    q.codes, q.sb = 1 << 24, 1 << 25
+    assert L.dflash_linear_q4(q, 130, 512, a, 8, 1, a, None) == -2     # rows % 4
+    assert L.dflash_linear_q4(q, 128, 500, a, 8, 1, a, None) == -2     # K % 64
+    assert L.dflash_linear_q4(q, 128, 512, a, 8, 3, a, None) == -2     # splits must divide
+    assert L.dflash_linear_q4(q, 128, 512, a, 0, 1, a, None) == 0      # no tokens
+    assert L.dflash_linear_q4(q, 128, 512, P(0), 8, 1, a, None) == -1
+    q.sb = (1 << 25) + 4
+    assert L.dflash_linear_q4(q, 128, 512, a, 8, 1, a, None) == -7
+
+
+def test_pack_q4_layout(dfl):
+    """The binding's 4-bit packing follows the header: in the word of input features
+    8j..8j+7, (word >> 4i) & 0xF and (word >> (16 + 4i)) & 0xF are the codes of
+    features 8j+2i and 8j+2i+1; the (scale, bias) words are group-major."""
+    import numpy as np
+    import torch
+    g = np.random.default_rng(0)
+    N, K = 6, 128
+    q = g.integers(0, 16, (N, K)).astype(np.uint8)
+    s = torch.tensor(g.uniform(0.001, 1.0, (N, K // 64)), dtype=torch.float32).to(torch.bfloat16)
+    b = torch.tensor(g.standard_normal((N, K // 64)), dtype=torch.float32).to(torch.bfloat16)
+    codes, sb = dfl.pack_q4(q, s.float().numpy(), b.float().numpy())
+    assert codes.shape == (N, K // 2) and sb.shape == (K // 64, N)
+    words = codes.numpy().view("<u4")
+    for n in range(N):
+        for j in range(K // 8):
+            w = int(words[n, j])
+            for i in range(4):
+                assert (w >> (4 * i)) & 15 == q[n, 8 * j + 2 * i]
+                assert (w >> (16 + 4 * i)) & 15 == q[n, 8 * j + 2 * i + 1]
+    sbits = s.view(torch.int16).numpy().astype(np.uint16)
+    bbits = b.view(torch.int16).numpy().astype(np.uint16)
+    sbw = sb.numpy().view("<u4")
+    for n in range(N):
+        for grp in range(K // 64):
+            assert sbw[grp, n] & 0xFFFF == sbits[n, grp]
+            assert sbw[grp, n] >> 16 == bbits[n, grp]
