@@ -72,6 +72,19 @@ def pass_bytes(cfg, B, K, ctx):
     return w + kv + gathers
 
 
+def q4_pass_bytes(cfg, B, K, ctx):
+    """pass_bytes with the 4-bit matrices counted as their codes (half a byte a
+    weight) and (scale, bias) words (4 bytes a row and group of 64)."""
+    shapes = {n: s for n, s, _ in synth.weight_names(cfg)}
+    out = pass_bytes(cfg, B, K, ctx)
+    for n in synth.q4_names(cfg):
+        if n == "fc":
+            continue  # not read by the pass
+        N, Kin = shapes[n]
+        out += N * Kin // 2 + N * (Kin // 64) * 4 - N * Kin * 2
+    return out
+
+
 def stored_traffic(n_launches):
     """DRAM bytes (read + write) of one replay of the roofline GEMM sequence, from
     the ncu capture recorded in profiles/ -- only while the library's sources are
@@ -310,6 +323,8 @@ def run_gpu(args, rank, world, barrier, allmax):
         res["b32"] = bench_b32(torch, dfl, cfg, Wd, pk, args)
     if "inject" in sections:
         res["inject"] = bench_inject(torch, dfl, cfg, Wd, pk, args)
+    if "q4" in sections:
+        res["q4"] = bench_q4(torch, dfl, cfg, Wh, pk, args)
     return res, Wh
 
 
@@ -454,6 +469,71 @@ def bench_b32(torch, dfl, cfg, Wd, pk, args):
             "hbm_floor_us": t_hbm * 1e6, "tensor_floor_us": t_tc * 1e6,
             "frac_of_tighter_roofline": max(t_hbm, t_tc) / (ms_p2 * 1e-3),
             "ctx_range": [min(ctx2), max(ctx2)], "device_status": status}
+
+
+def bench_q4(torch, dfl, cfg, Wh, pk, args):
+    """The headline workload (B=1, block 8, context 2048) with the 4-bit drafter:
+    fc, QKV, O, gate/up, down and lm_head as 4-bit codes with a (scale, bias) per
+    row and 64 input features (seeded synthetic codes)."""
+    B, K, ctx = 1, 8, [2048]
+    cq = dict(cfg, weight_bits=4)
+    Q = synth.make_q4_weights(cq, seed=0)
+    Wq = dfl.DeviceWeights.from_host(cq, Wh, "cuda", q4=Q)
+    del Q
+    tab_ws = dfl.Workspace(cq, 1, 2, 1)
+    dfl.prepare_selector(cq, Wq, tab_ws)
+    kv, cyc, inp = setup_workload(torch, dfl, cq, Wq, B, K, ctx, 0, 1024)
+
+    def cycle():
+        cyc.run(inp["hidden"], inp["req"], inp["pos"], inp["anchor"], inp["ctx"], inp["target"])
+
+    def dpass():
+        dfl.draft_block(cq, Wq, kv, inp["anchor"], inp["ctx"], K, cyc.ws, cyc.topk_ids,
+                        cyc.topk_logp)
+        dfl.select_path(cq, Wq, inp["anchor"], cyc.topk_ids, cyc.topk_logp, K, cyc.ws, cyc.path,
+                        cyc.score)
+
+    g_cycle = capture(torch, cycle)
+    g_pass = capture(torch, dpass)
+    ms_cycle = event_time(torch, g_cycle.replay, args.steps, args.warmup)
+    torch.cuda.nvtx.range_push("q4_pass")  # lets a profiler select these launches
+    ms_pass = event_time(torch, g_pass.replay, args.steps, args.warmup)
+    torch.cuda.nvtx.range_pop()
+    status = dfl.read_device_status(cyc.ws)
+    # the 4-bit GEMMs of one pass replayed back to back
+    gem = [(N, Kin, T, n) for (N, Kin, T, n) in pass_gemms(cq, B, K)
+           if n.split(".")[-1] in ("wqkv", "wo", "w_gate_up", "w_down", "lm_head")]
+    xs, outs, gbytes = {}, {}, 0
+    for (N, Kin, T, n) in gem:
+        if (T, Kin) not in xs:
+            xs[(T, Kin)] = torch.randn((T, Kin), device="cuda").to(torch.bfloat16)
+        S = dfl.linear_splits(N, T, Kin)
+        while (Kin // 64) % S:
+            S -= 1
+        outs[n] = (torch.empty((S, T, N), device="cuda", dtype=torch.float32), S)
+        gbytes += (N + 127) // 128 * 128 * (Kin // 64) * 2304 // 64 + T * Kin * 2 + S * T * N * 4
+
+    def gemms():
+        for (N, Kin, T, n) in gem:
+            o, S = outs[n]
+            dfl.linear_q4(Wq.t[n + ".q4"], N, xs[(T, Kin)], o, S)
+
+    g_gemm = capture(torch, gemms)
+    torch.cuda.nvtx.range_push("q4_gemm_roofline")
+    ms_gemm = event_time(torch, g_gemm.replay, args.steps, args.warmup)
+    torch.cuda.nvtx.range_pop()
+    pb = q4_pass_bytes(cq, B, K, ctx)
+    del g_cycle, g_pass, g_gemm
+    return {"workload": "B=1, block 8, context 2048, 4-bit fc/QKV/O/gate-up/down/lm_head "
+                        "(codes + bf16 scale and bias per 64 inputs)",
+            "cycle_us": ms_cycle * 1e3, "cycles_per_s": 1e3 / ms_cycle,
+            "draft_pass_us": ms_pass * 1e3, "draft_pass_bytes": pb,
+            "draft_pass_hbm_frac": pb / (ms_pass * 1e-3) / 1e9 / pk["hbm"],
+            "gemm": {"kernel": "k_gemm_q4 (4-bit weights, tcgen05), the pass's 21 shapes",
+                     "bytes_per_pass": gbytes, "us_per_pass": ms_gemm * 1e3,
+                     "achieved_gbs": gbytes / (ms_gemm * 1e-3) / 1e9,
+                     "frac_of_hbm": gbytes / (ms_gemm * 1e-3) / 1e9 / pk["hbm"]},
+            "device_status": status}
 
 
 def inject_flops(cfg, N):
@@ -661,7 +741,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--only", default="",
-                    help="comma list of sections to run: b1 (headline), b32, inject; or "
+                    help="comma list of sections to run: b1 (headline), b32, inject, q4 "
+                         "(the headline workload with 4-bit weights); or "
                          "inject4k alone (a 4096-row injection with only its weights loaded, "
                          "the small profiling case)")
     ap.add_argument("--no-b32", action="store_true")
@@ -671,7 +752,7 @@ def main():
                     help="check the replica barrier / max on CPU (gloo) and exit")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    args.sections = set(x for x in args.only.split(",") if x) or {"b1", "b32", "inject"}
+    args.sections = set(x for x in args.only.split(",") if x) or {"b1", "b32", "inject", "q4"}
     if args.no_b32:
         args.sections.discard("b32")
     if args.no_inject:

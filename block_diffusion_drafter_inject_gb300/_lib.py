@@ -34,7 +34,7 @@ class Config(ctypes.Structure):
 
 
 class Q4(ctypes.Structure):
-    _fields_ = [("codes", vp), ("sb", vp)]
+    _fields_ = [("data", vp)]
 
 
 # the matrices a 4-bit drafter keeps in 4 bits

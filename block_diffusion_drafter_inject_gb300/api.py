@@ -63,8 +63,8 @@ class DeviceWeights:
                 L.conv_base[i] = ptr(p + f"conv_base.{i}")
         if "sel_gate" in tensors:
             w.sel_gate = tensors["sel_gate"].data_ptr()
-        # 4-bit matrices: tensors NAME.codes and NAME.sb (see pack_q4)
-        q4 = lambda q, n: (setattr(q, "codes", ptr(n + ".codes")), setattr(q, "sb", ptr(n + ".sb")))
+        # 4-bit matrices: tensors NAME.q4 (see pack_q4)
+        q4 = lambda q, n: setattr(q, "data", ptr(n + ".q4"))
         for n in _lib.Q4_TOP:
             q4(getattr(w, n + "_q4"), n)
         for l in range(cfg["n_layers"]):
@@ -85,35 +85,41 @@ class DeviceWeights:
                 continue
             t[name] = torch.from_numpy(arr).to(dt).to(device).contiguous()
         for name, (q, sc, bias) in (q4 or {}).items():
-            codes, sb = pack_q4(q, sc, bias)
-            t[name + ".codes"] = codes.to(device)
-            t[name + ".sb"] = sb.to(device)
+            t[name + ".q4"] = pack_q4(q, sc, bias).to(device)
         return cls(cfg, t)
 
 
 def pack_q4(q, scale, bias):
-    """The C ABI's 4-bit layout of one matrix: codes [N, K/2] uint8 with the nibbles
-    of input features 8j..8j+7 in the order 8j, 8j+2, 8j+4, 8j+6, 8j+1, 8j+3, 8j+5,
-    8j+7 from the least significant of their 32-bit word, and (scale, bias) words
-    [K/64, N] int32 (bf16 scale bits low, bf16 bias bits high)."""
+    """The C ABI's 4-bit layout of one matrix (dflash_q4) as a flat uint8 tensor:
+    rows padded to a multiple of 128, cut into 64-row blocks; per block and group
+    of 64 input features one 2304-byte record: the rows' codes (32 bytes a row,
+    the nibbles of features 8j..8j+7 in the order 8j, 8j+2, 8j+4, 8j+6, 8j+1, 8j+3,
+    8j+5, 8j+7 from the least significant of their 32-bit word), then their
+    (scale, bias) words (bf16 scale bits low, bf16 bias bits high)."""
     q = torch.as_tensor(q).to(torch.uint8)
     N, K = q.shape
+    Np = (N + 127) // 128 * 128
+    G = K // 64
     g = q.reshape(N, K // 8, 8)
-    lo = g[:, :, [0, 4, 1, 5]]
-    hi = g[:, :, [2, 6, 3, 7]]
-    codes = (lo | (hi << 4)).reshape(N, K // 2).contiguous()
+    codes = (g[:, :, [0, 4, 1, 5]] | (g[:, :, [2, 6, 3, 7]] << 4)).reshape(N, K // 2)
     bits = lambda a: torch.as_tensor(a).to(torch.bfloat16).view(torch.int16).to(torch.int32) & 0xFFFF
-    sb = (bits(scale) | (bits(bias) << 16)).t().contiguous()
-    return codes, sb
+    words = (bits(scale) | (bits(bias) << 16)).reshape(N, G, 1).view(torch.uint8)  # [N, G, 4]
+    rec = torch.zeros((Np, G, 36), dtype=torch.uint8)
+    rec[:N, :, :32] = codes.reshape(N, G, 32)
+    rec[:N, :, 32:] = words
+    # [row block, 64 rows, group, 36] -> [row block, group, 64 rows x 32 | 64 rows x 4]
+    rec = rec.reshape(Np // 64, 64, G, 36).permute(0, 2, 1, 3)
+    out = torch.cat([rec[..., :32].reshape(Np // 64, G, 2048),
+                     rec[..., 32:].reshape(Np // 64, G, 256)], dim=2)
+    return out.reshape(-1).contiguous()
 
 
-def linear_q4(codes, sb, X, out, splits=1, stream=None):
-    """dflash_linear_q4: out[s] = the s-th K slice of X W^T with W in 4 bits."""
-    N_out, K2 = codes.shape
+def linear_q4(data, N_out, X, out, splits=1, stream=None):
+    """dflash_linear_q4: out[s] = the s-th K slice of X W^T with W [N_out, K] in 4 bits
+    (data from pack_q4)."""
     w = _lib.Q4()
-    w.codes = codes.data_ptr()
-    w.sb = sb.data_ptr()
-    check(lib().dflash_linear_q4(w, int(N_out), int(2 * K2), _ptr(X), int(X.shape[0]),
+    w.data = data.data_ptr()
+    check(lib().dflash_linear_q4(w, int(N_out), int(X.shape[1]), _ptr(X), int(X.shape[0]),
                                  int(splits), _ptr(out), _stream(stream)), "dflash_linear_q4")
 
 

@@ -85,7 +85,6 @@ static int check_cfg(const dflash_config *c) {
   if (!ok) return DFLASH_ERR_DIMS;
   if (c->weight_bits != 0 && c->weight_bits != 4) return DFLASH_ERR_DTYPE;
   if (c->weight_bits == 4 && c->dtype != DFLASH_BF16) return DFLASH_ERR_DTYPE;
-  if (c->weight_bits == 4 && c->vocab % 4) return DFLASH_ERR_DIMS;  // (scale, bias) rows
   return DFLASH_OK;
 }
 
@@ -95,8 +94,8 @@ static bool a16(const void *p) { return ((uintptr_t)p & 15) == 0; }
 // (scale, bias) words.
 static int check_proj(const dflash_config *c, const void *w, const dflash_q4 &q) {
   if (c->weight_bits == 4) {
-    if (!q.codes || !q.sb) return DFLASH_ERR_NULL;
-    return a16(q.codes) && a16(q.sb) ? DFLASH_OK : DFLASH_ERR_ALIGN;
+    if (!q.data) return DFLASH_ERR_NULL;
+    return a16(q.data) ? DFLASH_OK : DFLASH_ERR_ALIGN;
   }
   if (!w) return DFLASH_ERR_NULL;
   return a16(w) ? DFLASH_OK : DFLASH_ERR_ALIGN;
@@ -168,6 +167,11 @@ static GemmPlan reduce_plan(const dflash_config *c, int N_out, int T, int K_in, 
                             int sms) {
   if (c->dtype == DFLASH_F32) return GemmPlan{0, 1};
   GemmPlan p = gemm_plan(N_out, T, K_in, mode, sms, kMaxReduceSplits);
+  if (c->weight_bits == 4 && (p.bn > 128 || p.pair)) {
+    // 4-bit tiles are at most 128 tokens wide
+    p.bn = 128;
+    p.pair = 0;
+  }
   if (gemm_tiles(N_out, T, mode, p.bn) > kTicketInts) p.S = 1, p.chunk = 0;
   return p;
 }
@@ -298,13 +302,10 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   return true;
 }
 
-// The call reads weight matrix rows [row0, row0 + its rows) of a 4-bit matrix
-// with `rows` rows and K_in input features.
-static GemmCall with_q4(GemmCall g, const dflash_q4 &q, int rows, int K_in, int row0 = 0) {
-  g.Wq = (const uint8_t *)q.codes + (size_t)row0 * (K_in / 2);
-  g.Wsb = q.sb;
-  g.sb_rows = rows;
-  g.q_row0 = row0;
+// The call reads rows row0.. (a multiple of 64) of a 4-bit matrix with K_in
+// input features: its records from row block row0 / 64 on.
+static GemmCall with_q4(GemmCall g, const dflash_q4 &q, int K_in, int row0 = 0) {
+  g.Wq = (const uint8_t *)q.data + (size_t)(row0 / 64) * (K_in / 64) * 2304;
   return g;
 }
 
@@ -372,7 +373,7 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
       fit_plan(c, L, D, N, TIN, GEMM_REDUCE, reduce_plan(&c, D, N, TIN, GEMM_REDUCE, sms));
   const bool q4 = c.weight_bits == 4;
   GemmCall gf = reduce_call(c, ws, L, w.fc, D, TIN, gn, N, S_fc, GEMM_REDUCE, nullptr, D, cb, D);
-  if (q4) gf = with_q4(gf, w.fc_q4, D, TIN);
+  if (q4) gf = with_q4(gf, w.fc_q4, TIN);
   TRY(gemm_run(gf, st));
   // the [Wk; Wv] rows of every layer: one grouped launch per kKvGroup layers
   // (layer l's projection -> kvf [l][N][W2])
@@ -389,7 +390,7 @@ static int run_inject(const dflash_config &c, const dflash_weights &w, const dfl
     g.groups = ng;
     g.ostride = (size_t)N * W2;
     for (int j = 1; j < ng; ++j) g.Wg[j] = (const S *)w.layer[l0 + j].wqkv + (size_t)Hq * dh * D;
-    if (q4) g = with_q4(g, w.layer[l0].wqkv_q4, (Hq + 2 * Hkv) * dh, D, Hq * dh);
+    if (q4) g = with_q4(g, w.layer[l0].wqkv_q4, D, Hq * dh);
     TRY(gemm_run(g, st));
   }
   for (int l = 0; l < c.n_layers; ++l) kn.p[l] = w.layer[l].k_norm;
@@ -473,7 +474,7 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     gq.Hkv = Hkv;
     gq.dh = dh;
     gq.eps = eps;
-    if (q4) gq = with_q4(gq, lw.wqkv_q4, QKVW, D);
+    if (q4) gq = with_q4(gq, lw.wqkv_q4, D);
     if (N > 0) {
       gq.T0 = T;
       gq.ctx_slot = slots.slot;
@@ -488,23 +489,23 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   auto o_call = [&](int l) {
     GemmCall g = reduce_call(c, ws, L, w.layer[l].wo, D, Hq * dh, ob, T, L.P_o, GEMM_REDUCE, rf,
                              D, rb, D);
-    return q4 ? with_q4(g, w.layer[l].wo_q4, D, Hq * dh) : g;
+    return q4 ? with_q4(g, w.layer[l].wo_q4, Hq * dh) : g;
   };
   auto gu_call = [&](int l) {
     GemmCall g = reduce_call(c, ws, L, w.layer[l].w_gate_up, F, D, ub, T, L.P_gu, GEMM_SWIGLU,
                              nullptr, 0, hb, F);
-    return q4 ? with_q4(g, w.layer[l].w_gate_up_q4, 2 * F, D) : g;
+    return q4 ? with_q4(g, w.layer[l].w_gate_up_q4, D) : g;
   };
   auto down_call = [&](int l) {
     GemmCall g = reduce_call(c, ws, L, w.layer[l].w_down, D, F, hb, T, L.P_down, GEMM_REDUCE, rf,
                              D, rb, D);
-    return q4 ? with_q4(g, w.layer[l].w_down_q4, D, F) : g;
+    return q4 ? with_q4(g, w.layer[l].w_down_q4, F) : g;
   };
   auto lm_call = [&]() {
     GemmCall gl = reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, GemmPlan{0, 1}, GEMM_REDUCE,
                               logits, V, nullptr, 0);
     gl.stats = tstats;
-    return q4 ? with_q4(gl, w.lm_head_q4, V, D) : gl;
+    return q4 ? with_q4(gl, w.lm_head_q4, D) : gl;
   };
   // A few block rows: each conv is one launch with its gate linear fused (the
   // pre-norm formed inside).  More rows: the gate linear is a tensor-core GEMM
@@ -547,7 +548,7 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
                                  reduce_plan(&c, D, N, TIN, GEMM_REDUCE, device()->num_sms));
     GemmCall gf =
         reduce_call(c, ws, L, w.fc, D, TIN, gn, N, pf, GEMM_REDUCE, nullptr, D, ub + (size_t)T * D, D);
-    if (q4) gf = with_q4(gf, w.fc_q4, D, TIN);
+    if (q4) gf = with_q4(gf, w.fc_q4, TIN);
     TRY(gemm_run(gf, st));
   }
   TRY(launch_embed_norm<S>((const S *)w.embed, anchor, c.mask_token_id, V, B, K, D,
@@ -940,11 +941,11 @@ int dflash_linear(int32_t dtype, const void *W, int32_t N_out, int32_t K_in, con
 
 int dflash_linear_q4(dflash_q4 W, int32_t N_out, int32_t K_in, const void *X, int32_t T,
                      int32_t splits, float *out, void *stream) {
-  if (N_out < 4 || N_out % 4 || T < 0 || K_in < 64 || K_in % 64) return DFLASH_ERR_DIMS;
+  if (N_out < 1 || T < 0 || K_in < 64 || K_in % 64) return DFLASH_ERR_DIMS;
   if (splits < 1 || (K_in / 64) % splits) return DFLASH_ERR_DIMS;
   if (T == 0) return DFLASH_OK;
-  if (!W.codes || !W.sb || !X || !out) return DFLASH_ERR_NULL;
-  if (!a16(W.codes) || !a16(W.sb) || !a16(X)) return DFLASH_ERR_ALIGN;
+  if (!W.data || !X || !out) return DFLASH_ERR_NULL;
+  if (!a16(W.data) || !a16(X)) return DFLASH_ERR_ALIGN;
   if (!device()) return DFLASH_ERR_DEVICE;
   GemmCall g;
   g.dtype = DFLASH_BF16;
@@ -956,7 +957,7 @@ int dflash_linear_q4(dflash_q4 W, int32_t N_out, int32_t K_in, const void *X, in
   g.mode = GEMM_PARTIAL;
   g.out = out;
   g.ld = N_out;
-  g = with_q4(g, W, N_out, K_in);
+  g = with_q4(g, W, K_in);
   return gemm_run(g, (cudaStream_t)stream);
 }
 

@@ -84,9 +84,8 @@ struct GemmParams {
   int stall;
   // two-SM tiles (k_gemm_tc2): work units are over pairs of weight tiles
   int pair;
-  // 4-bit weights (k_gemm_q4): this matrix's rows start at row q_row0 of the
-  // scale/bias matrix
-  int q_row0;
+  // 4-bit weights (k_gemm_q4): records of 64 rows x 64 inputs, row block major
+  const uint8_t *qdata;
 };
 
 // One CTA's share of one tile: k-blocks [kb0, kb0 + nkb), slice `seg` of the
@@ -99,8 +98,9 @@ struct Seg {
 __device__ __forceinline__ void epi_bar(int eg) {
   asm volatile("bar.sync %0, 128;" ::"r"(1 + eg) : "memory");
 }
+template <int NEG = kEpiGroups>
 __device__ __forceinline__ void epi_all_bar() {
-  asm volatile("bar.sync 3, %0;" ::"n"(kEpiGroups * 128) : "memory");
+  asm volatile("bar.sync 3, %0;" ::"n"(NEG * 128) : "memory");
 }
 
 template <int BN>
@@ -333,16 +333,16 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
   }
 }
 
-// Epilogue role (warps 2..9): two groups of four warps (each group covers the
-// four tensor-memory lane quarters); group eg takes the 16-column chunks
-// c = 16*eg + 32*i of each accumulator the MMA issuer hands over.
-template <int BN>
+// Epilogue role (warps 2..2+4*NEG-1): NEG groups of four warps (each group
+// covers the four tensor-memory lane quarters); group eg takes the 16-column
+// chunks c = 16*eg + 16*NEG*i of each accumulator the MMA issuer hands over.
+template <int BN, int NEG = kEpiGroups>
 __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem_base,
                                               uint64_t *tfull, uint64_t *tempty,
                                               volatile int *abort_flag, int warp, int lane) {
   pdl_wait();
-  __shared__ float xbuf[kEpiGroups][128 * 17];
-  __shared__ float xss[kEpiGroups][4 * 16];
+  __shared__ float xbuf[NEG][128 * 17];
+  __shared__ float xss[NEG][4 * 16];
   __shared__ int s_last;
   const int quarter = warp & 3;  // tensor-memory lanes this warp may read
   const int eg = (warp - 2) >> 2;
@@ -361,7 +361,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
       const int n = m_tile * BM + row;
       float *outp = p.out + (size_t)split * p.T * p.ld + n;
 #pragma unroll 1
-      for (int c = 16 * eg; c < BN; c += 32) {
+      for (int c = 16 * eg; c < BN; c += 16 * NEG) {
         float v[16];
         tc_ld16(taddr + c, v);
         const int t0 = tcol0 + c;
@@ -373,7 +373,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
       }
     } else if (sg.nseg == 1) {
 #pragma unroll 1
-      for (int c = 16 * eg; c < BN; c += 32) {
+      for (int c = 16 * eg; c < BN; c += 16 * NEG) {
         if (tcol0 + c >= p.T) break;  // uniform across the group
         float v[16];
         tc_ld16(taddr + c, v);
@@ -386,7 +386,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
       const size_t tile_sz = (size_t)BM * BN;
       float *mine = p.out + (tile * p.nmax + split) * tile_sz + row;
 #pragma unroll 1
-      for (int c = 16 * eg; c < BN; c += 32) {
+      for (int c = 16 * eg; c < BN; c += 16 * NEG) {
         if (tcol0 + c >= p.T) break;
         float v[16];
         tc_ld16(taddr + c, v);
@@ -400,13 +400,13 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
       // the ticket: the barrier orders every epilogue thread's slice stores
       // before one thread's acquire-release atomic (cumulative at GPU scope);
       // in the last CTA the second barrier orders the slice loads after it
-      epi_all_bar();
+      epi_all_bar<NEG>();
       if (threadIdx.x == 64) {
         const int old = atomic_add_acq_rel_gpu(&p.counters[tile], 1);
         s_last = old == sg.nseg - 1;
         if (s_last) p.counters[tile] = 0;
       }
-      epi_all_bar();
+      epi_all_bar<NEG>();
       if (s_last) {
         // sum the slices in slice order, CPI of the group's chunks per pass and
         // four slices (two for wider tiles) per round, so that their loads
@@ -414,7 +414,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
         constexpr int CPI = BN >= 128 ? 4 : BN >= 64 ? 2 : 1;
         const float *base = p.out + tile * p.nmax * tile_sz + row;
 #pragma unroll 1
-        for (int c = 16 * eg; c < BN; c += 32 * CPI) {
+        for (int c = 16 * eg; c < BN; c += 16 * NEG * CPI) {
           if (tcol0 + c >= p.T) break;
           float v[CPI][16];
 #pragma unroll
@@ -425,7 +425,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
           for (int q = 0; q < sg.nseg; ++q) {
 #pragma unroll
             for (int k = 0; k < CPI; ++k) {
-              const int cc = c + 32 * k;
+              const int cc = c + 16 * NEG * k;
               if (cc < BN && tcol0 + cc < p.T) {
                 const float *src = base + (size_t)q * tile_sz + (size_t)cc * BM;
 #pragma unroll
@@ -435,7 +435,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
           }
 #pragma unroll
           for (int k = 0; k < CPI; ++k) {
-            const int cc = c + 32 * k;
+            const int cc = c + 16 * NEG * k;
             if (cc < BN && tcol0 + cc < p.T)  // uniform across the group
               epi_store(p, m_tile, row, tcol0 + cc, v[k], gx, gs, eg);
           }
@@ -622,56 +622,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ---------------------------------------------------------------------------
 // Weights kept as 4-bit codes q with one (scale s, bias b) pair per row and
 // group of 64 input features (one k-block); the MMA multiplies w = bf16(s*q + b).
-// Storage (the C ABI's DFLASH_Q4 format):
-//   codes  [N_out][K_in/2] bytes, row-major.  The 32-bit word holding input
-//          features 8j..8j+7 of a row keeps their codes, from the least
-//          significant nibble up, in the order 8j, 8j+2, 8j+4, 8j+6, 8j+1,
-//          8j+3, 8j+5, 8j+7, so that (word >> 4i) & 0x000F000F is the pair
-//          (8j+2i, 8j+2i+1) in the two halves of a bf16x2
-//   sb     [K_in/64][sb_rows] 32-bit words, the bf16 scale in the low half and
-//          the bf16 bias in the high half: group-major, so one k-block's pairs
-//          for 128 consecutive rows are one 512-byte box
-// Roles (448 threads): warp 0 TMA producer (codes, pairs, activation tile), warp
-// 1 MMA issuer, warps 2-9 the epilogue of k_gemm_tc, warps 10-13 dequantize:
-// thread t turns row t of a k-block's codes into the 64 bf16 weights of row t of
-// the 128-byte-swizzled K-major tile that the MMA reads (the layout a TMA load
-// with 128-byte swizzle writes).  Three rings: code stages (X tile | codes |
-// pairs), released by the dequantizers and the MMA together; dequantized tiles,
-// released by the MMA; accumulators, as in k_gemm_tc.
+// Storage (the C ABI's dflash_q4): records of 2304 bytes, one per 64-row block
+// and k-block, row block major: the 64 rows' codes (32 bytes a row; the 32-bit
+// word of features 8j..8j+7 holds their codes, from the least significant
+// nibble up, in the order 8j, 8j+2, 8j+4, 8j+6, 8j+1, 8j+3, 8j+5, 8j+7, so that
+// (word >> 4i) & 0x000F000F is the pair (8j+2i, 8j+2i+1) in the two halves of
+// a bf16x2), then the rows' (scale, bias) words (bf16 scale low, bias high).
+// A k-block of a 128-row tile is two contiguous records, brought in by two bulk
+// copies.
+// Roles (448 threads): warp 0 bulk-copy producer (records, activation tile),
+// warp 1 MMA issuer, warps 2-5 one epilogue group (the epilogue of k_gemm_tc),
+// warps 6-13 dequantize: the thread on tensor-memory lane r (warp w covers
+// lanes 32*(w%4)..) of half h = (w - 6) / 4 turns inputs 32h..32h+31 of row r
+// of a k-block into bf16 weights and stores them as columns 16h..16h+15 of an
+// A buffer in tensor memory, from which the MMA reads its A operand; each warp
+// overlaps one k-block's store with the next k-block's loads and arithmetic.
+// Shared memory holds only the code stages (activation tile | codes | pairs),
+// released by the dequantizers and the MMA together; tensor memory holds the
+// two accumulators and a ring of A buffers released by the MMA's commits.
+constexpr int kQ4Record = 64 * 32 + 64 * 4;  // codes and pairs of 64 rows x 64 inputs
 template <int BN>
 struct QShape {
+  static_assert(BN <= 128, "4-bit tiles keep A buffers beside the accumulators");
   static constexpr int X_BYTES = BN * BK * 2;
-  static constexpr int W_BYTES = BM * BK / 2;  // codes of 128 rows
-  static constexpr int SB_BYTES = BM * 4;      // their (scale, bias) pairs
   static constexpr int STAGE_BYTES = X_BYTES + 5120;  // 1024-byte aligned stages
-  static constexpr int TX_BYTES = X_BYTES + W_BYTES + SB_BYTES;
-  static constexpr int NQ = BN <= 16 ? 20 : BN <= 32 ? 15 : BN <= 64 ? 10 : BN <= 128 ? 6 : 3;
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int NA = 4;
-  static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int SMEM_BYTES = NQ * STAGE_BYTES + NA * A_BYTES + 1024 + 512;
+  static constexpr int TX_BYTES = X_BYTES + 2 * kQ4Record;
+  static constexpr int NQ = BN <= 16 ? 28 : BN <= 32 ? 22 : BN <= 64 ? 15 : 9;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int A_COL0 = 2 * BN < 32 ? 32 : 2 * BN;  // after the accumulators
+  static constexpr int NA = (TMEM_COLS - A_COL0) / 32 > 14 ? 14 : (TMEM_COLS - A_COL0) / 32;
+  static constexpr int SMEM_BYTES = NQ * STAGE_BYTES + 1024 + 768;
   static_assert(SMEM_BYTES + 18 * 1024 <= 232448, "dynamic + the epilogue's static shared memory");
 };
-constexpr int kQ4Threads = kGemmThreads + 128;
+constexpr int kQ4Epi = 1;  // epilogue groups
+constexpr int kQ4Dq = 8;   // dequantizing warps
+constexpr int kQ4Threads = 64 + kQ4Epi * 128 + kQ4Dq * 32;
 
-struct QMaps {
-  CUtensorMap codes, sb;
-};
-
-// codes and (scale, bias) pairs of weight tile m_tile, k-block kb, into dst
-// (codes [128][32 B], then pairs [128]); GEMM_SWIGLU: gate rows then up rows
-__device__ __forceinline__ void load_wq(uint8_t *dst, const QMaps &m, uint64_t *bar, int kb,
-                                        int m_tile, const GemmParams &p, uint64_t pol) {
-  uint8_t *ds = dst + BM * BK / 2;
-  if (p.mode == 2) {
-    tma_load_2d(dst, &m.codes, bar, kb * 32, m_tile * 64, pol);
-    tma_load_2d(dst + 64 * 32, &m.codes, bar, kb * 32, p.F + m_tile * 64, pol);
-    tma_load_2d(ds, &m.sb, bar, p.q_row0 + m_tile * 64, kb, pol);
-    tma_load_2d(ds + 64 * 4, &m.sb, bar, p.q_row0 + p.F + m_tile * 64, kb, pol);
-  } else {
-    tma_load_2d(dst, &m.codes, bar, kb * 32, m_tile * BM, pol);
-    tma_load_2d(ds, &m.sb, bar, p.q_row0 + m_tile * BM, kb, pol);
-  }
+// the two records of weight tile m_tile, k-block kb, into dst; GEMM_SWIGLU: the
+// gate rows' block m_tile, then the up rows' block F/64 + m_tile
+__device__ __forceinline__ void load_wq(uint8_t *dst, uint64_t *bar, int kb, int m_tile,
+                                        const GemmParams &p, uint64_t pol) {
+  const int rb0 = p.mode == 2 ? m_tile : 2 * m_tile;
+  const int rb1 = p.mode == 2 ? p.F / 64 + m_tile : 2 * m_tile + 1;
+  const size_t per_block = (size_t)p.kb_total * kQ4Record;
+  bulk_load(dst, p.qdata + rb0 * per_block + (size_t)kb * kQ4Record, kQ4Record, bar, pol);
+  bulk_load(dst + kQ4Record, p.qdata + rb1 * per_block + (size_t)kb * kQ4Record, kQ4Record, bar,
+            pol);
 }
 
 // bf16x2 (s*q_lo + b, s*q_hi + b), each rounded once, for the code pair at
@@ -686,14 +682,12 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t w, int shift, uint32_t s2, 
 
 template <int BN>
 __global__ void __launch_bounds__(kQ4Threads, 1)
-    k_gemm_q4(const __grid_constant__ QMaps tmQ, const __grid_constant__ CUtensorMap tmX,
-              GemmParams p) {
+    k_gemm_q4(const __grid_constant__ CUtensorMap tmX, GemmParams p) {
   using QS = QShape<BN>;
   constexpr int NQ = QS::NQ, NA = QS::NA;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t *abuf = smem + NQ * QS::STAGE_BYTES;
-  uint64_t *qfull = (uint64_t *)(abuf + NA * QS::A_BYTES);
+  uint64_t *qfull = (uint64_t *)(smem + NQ * QS::STAGE_BYTES);
   uint64_t *qempty = qfull + NQ;
   uint64_t *afull = qempty + NQ;
   uint64_t *aempty = afull + NA;
@@ -709,21 +703,19 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NQ; ++s) {
       mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], 1 + 4);  // the MMA's commit and the four dequantizing warps
+      mbar_init(&qempty[s], 1 + kQ4Dq);  // the MMA's commit and the dequantizing warps
     }
     for (int a = 0; a < NA; ++a) {
-      mbar_init(&afull[a], 4);
+      mbar_init(&afull[a], kQ4Dq);
       mbar_init(&aempty[a], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4 * kEpiGroups);
+      mbar_init(&tempty[a], 4 * kQ4Epi);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
-    tma_prefetch_desc(&tmQ.codes);
-    tma_prefetch_desc(&tmQ.sb);
     tma_prefetch_desc(&tmX);
   }
   if (warp == 1) {
@@ -755,7 +747,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
         for (int i = 0; cnt < NQ && get_seg(p, i, sg); ++i) {
           for (int kb = 0; kb < sg.nkb && cnt < NQ; ++kb, ++cnt) {
             mbar_expect_tx(&qfull[cnt], QS::TX_BYTES);
-            load_wq(smem + cnt * QS::STAGE_BYTES + QS::X_BYTES, tmQ, &qfull[cnt], sg.kb0 + kb,
+            load_wq(smem + cnt * QS::STAGE_BYTES + QS::X_BYTES, &qfull[cnt], sg.kb0 + kb,
                     sg.m_tile, p, pol_w);
           }
         }
@@ -777,7 +769,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
               break;
             }
             mbar_expect_tx(&qfull[stage], QS::TX_BYTES);
-            load_wq(st + QS::X_BYTES, tmQ, &qfull[stage], sg.kb0 + kb, sg.m_tile, p, pol_w);
+            load_wq(st + QS::X_BYTES, &qfull[stage], sg.kb0 + kb, sg.m_tile, p, pol_w);
             tma_load_2d(st, &tmX, &qfull[stage], kx, sg.t_tile * BN, pol_x);
           }
           issued[stage] = true;
@@ -818,12 +810,12 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = sdesc_k_sw128(smem_u32(abuf + as * QS::A_BYTES));
+          const uint32_t a_tmem = tmem_base + (uint32_t)(QS::A_COL0 + as * 32);
           const uint64_t bdesc = sdesc_k_sw128(smem_u32(smem + qs * QS::STAGE_BYTES));
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            tc_mma_bf16(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc,
-                        (kb | k) != 0);
+          for (int k = 0; k < BK / 16; ++k)  // 16 bf16 of K = 8 tensor-memory columns
+            tc_mma_bf16_ta(d_tmem, a_tmem + (uint32_t)(k * 8), bdesc + (uint64_t)(k * 2), idesc,
+                           (kb | k) != 0);
           tc_commit(&qempty[qs]);
           tc_commit(&aempty[as]);
           if (++qs == NQ) qs = 0, qph ^= 1;
@@ -840,16 +832,29 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 2 + 4 * kEpiGroups) {
-    gemm_epilogue<BN>(p, tmem_base, tfull, tempty, abort_flag, warp, lane);
+  } else if (warp < 2 + 4 * kQ4Epi) {
+    gemm_epilogue<BN, kQ4Epi>(p, tmem_base, tfull, tempty, abort_flag, warp, lane);
   } else {
-    // ---------------- dequantize: warps 10..13, thread t = tile row t ----------------
-    // (codes and pairs are weights: no wait for the previous kernel)
-    const int t = threadIdx.x - kGemmThreads;
-    const int sw = t & 7;
-    int qs = 0, as = 0;
+    // ---------------- dequantize: warps 6..13 ----------------
+    // (records are weights: no wait for the previous kernel)
+    const int quarter = warp & 3, h = (warp - 2 - 4 * kQ4Epi) >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_addr =
+        tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(QS::A_COL0 + 16 * h);
+    const int roff = (r >> 6) * kQ4Record, rrow = r & 63;
+    int qs = 0, as = 0, pq = 0, pa = 0;
     uint32_t qph = 0, aph = 0;
-    bool ok = true;
+    bool ok = true, pending = false;
+    // hand k-block (pq, pa) over once its tensor-memory store has completed
+    auto release = [&]() {
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&afull[pa]);
+        mbar_arrive(&qempty[pq]);
+      }
+    };
     Seg sg;
     for (int i = 0; ok && get_seg(p, i, sg); ++i) {
       for (int kb = 0; kb < sg.nkb; ++kb) {
@@ -859,30 +864,34 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
           ok = false;
           break;
         }
-        const uint8_t *cw = smem + qs * QS::STAGE_BYTES + QS::X_BYTES;
-        const uint4 w0 = *(const uint4 *)(cw + t * 32);
-        const uint4 w1 = *(const uint4 *)(cw + t * 32 + 16);
-        const uint32_t sb = *(const uint32_t *)(cw + QS::W_BYTES + t * 4);
+        tc_fence_after();
+        const uint8_t *rec = smem + qs * QS::STAGE_BYTES + QS::X_BYTES + roff;
+        const uint4 w = *(const uint4 *)(rec + rrow * 32 + 16 * h);
+        const uint32_t sb = *(const uint32_t *)(rec + 64 * 32 + rrow * 4);
         const uint32_t s2 = (sb & 0xFFFFu) * 0x10001u, b2 = (sb >> 16) * 0x10001u;
-        uint8_t *arow = abuf + as * QS::A_BYTES + t * 128;
-        const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+        uint32_t a[16];  // column 16h + j: weights (32h + 2j, 32h + 2j + 1) of the row
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 o;
-          o.x = dq_pair(wd[c], 0, s2, b2);
-          o.y = dq_pair(wd[c], 4, s2, b2);
-          o.z = dq_pair(wd[c], 8, s2, b2);
-          o.w = dq_pair(wd[c], 12, s2, b2);
-          *(uint4 *)(arow + ((c ^ sw) << 4)) = o;
+        for (int c = 0; c < 4; ++c) {
+          a[4 * c + 0] = dq_pair(wd[c], 0, s2, b2);
+          a[4 * c + 1] = dq_pair(wd[c], 4, s2, b2);
+          a[4 * c + 2] = dq_pair(wd[c], 8, s2, b2);
+          a[4 * c + 3] = dq_pair(wd[c], 12, s2, b2);
         }
-        fence_proxy_async();  // the tile's generic writes, before the MMA reads it
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&afull[as]);
-          mbar_arrive(&qempty[qs]);
-        }
+        if (pending) release();  // the previous k-block's store had this long to land
+        tc_st16(lane_addr + (uint32_t)(as * 32), a);
+        pending = true;
+        pq = qs;
+        pa = as;
         if (++qs == NQ) qs = 0, qph ^= 1;
         if (++as == NA) as = 0, aph ^= 1;
+      }
+    }
+    if (pending) {
+      if (ok) {
+        release();
+      } else {
+        tc_wait_st();
       }
     }
   }
@@ -1393,49 +1402,6 @@ bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t cols,
 }
 
 
-// Tensor maps of 4-bit weights (cached): codes [rows][cols_bytes] bytes in boxes of
-// 32 bytes x box_rows rows; (scale, bias) words [groups][ld] in boxes of box_rows
-// words x 1 group, the matrix viewed as [groups][ld] with rows == ld.
-static bool q4_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t cols, uint64_t ld,
-                   uint32_t box_rows, int is_sb, int dev) {
-  static std::mutex mu;
-  static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-  MapKey key{(uintptr_t)ptr ^ ((uintptr_t)is_sb << 63), rows, cols * 1000003ull + ld, box_rows, dev};
-  {
-    std::lock_guard<std::mutex> g(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) {
-      *out = it->second;
-      return true;
-    }
-  }
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  CUresult r;
-  cuuint32_t estr[2] = {1, 1};
-  if (!is_sb) {
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols};
-    cuuint32_t box[2] = {32, box_rows};
-    r = enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  } else {
-    // rows = groups (K_in / 64), cols = words used per group (ld)
-    cuuint64_t dims[2] = {ld, rows};
-    cuuint64_t strides[1] = {ld * 4};
-    cuuint32_t box[2] = {box_rows, 1};
-    r = enc(out, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  }
-  if (r != CUDA_SUCCESS) return false;
-  std::lock_guard<std::mutex> g(mu);
-  if (cache.size() > 8192) cache.clear();
-  cache[key] = *out;
-  return true;
-}
-
 static int token_tile(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
 
 // One k-block of one CTA (microseconds): the slowest of the weight tile from
@@ -1642,7 +1608,7 @@ static int make_params(const GemmCall &g, int BN, int num_sms, dfl::GemmParams &
   p.wait_ns = g.wait_ns > 0 ? g.wait_ns : dfl::kWaitLimitNs;
   p.stall = g.stall;
   p.pair = 0;
-  p.q_row0 = g.q_row0;
+  p.qdata = nullptr;
   int grid = p.num_units < num_sms ? p.num_units : num_sms;
   if (g.chunk > 0) {
     const long total = (long)tiles * p.kb_total;
@@ -1696,21 +1662,14 @@ static int launch_q4(const GemmCall &g, cudaStream_t st, const Dev *d) {
       return DFLASH_ERR_CUDA;
     attr_set_dev[d->id] = 1;
   }
-  const bool swiglu = g.mode == GEMM_SWIGLU;
-  const int w_rows = swiglu ? 2 * g.N_out : g.N_out;
-  const uint32_t box_rows = swiglu ? 64 : dfl::BM;
-  dfl::QMaps mq;
   CUtensorMap mx;
-  memset(&mq, 0, sizeof(mq));
-  if (!q4_map(&mq.codes, g.Wq, (uint64_t)w_rows, (uint64_t)g.K_in / 2, 0, box_rows, 0, d->id) ||
-      !q4_map(&mq.sb, g.Wsb, (uint64_t)g.K_in / 64, 0, (uint64_t)g.sb_rows, box_rows, 1, d->id))
-    return DFLASH_ERR_CUDA;
   if (!bf16_map(&mx, g.X, (uint64_t)g.T, (uint64_t)g.K_in, BN, d->id)) return DFLASH_ERR_CUDA;
   dfl::GemmParams p;
   const int grid = make_params(g, BN, d->num_sms, p);
   if (grid < 0) return DFLASH_ERR_DIMS;
+  p.qdata = (const uint8_t *)g.Wq;
   DFL_CHECK_LAUNCH(launch(dfl::k_gemm_q4<BN>, dim3(grid), dim3(dfl::kQ4Threads),
-                          (size_t)QS::SMEM_BYTES, st, mq, mx, p));
+                          (size_t)QS::SMEM_BYTES, st, mx, p));
   return DFLASH_OK;
 }
 
@@ -1814,13 +1773,11 @@ int gemm_run(const GemmCall &g, cudaStream_t st) {
   }
   if (g.Wq) {
     // 4-bit weights: one weight group, one-SM tiles
-    if (g.dtype != DFLASH_BF16 || g.groups != 1 || g.stall || !g.Wsb) return DFLASH_ERR_DIMS;
-    if (g.sb_rows < 1 || g.sb_rows % 4 || g.q_row0 < 0 || g.q_row0 % 4 ||
-        g.q_row0 + (g.mode == GEMM_SWIGLU ? 2 * g.N_out : g.N_out) > g.sb_rows)
-      return DFLASH_ERR_DIMS;
-    if ((uintptr_t)g.Wq % 16 || (uintptr_t)g.Wsb % 16 || (uintptr_t)g.X % 16) return DFLASH_ERR_ALIGN;
-    if (g.K_in / 2 % 16) return DFLASH_ERR_DIMS;
-    const int qbn = g.bn > 0 && !g.pair ? g.bn : g.pair ? 256 : token_tile(g.T);
+    if (g.dtype != DFLASH_BF16 || g.groups != 1 || g.stall) return DFLASH_ERR_DIMS;
+    if (g.mode == GEMM_SWIGLU && g.N_out % 64) return DFLASH_ERR_DIMS;
+    if ((uintptr_t)g.Wq % 16 || (uintptr_t)g.X % 16) return DFLASH_ERR_ALIGN;
+    int qbn = g.bn > 0 && !g.pair ? g.bn : g.pair ? 256 : token_tile(g.T);
+    if (qbn > 128) qbn = 128;  // the A buffers share tensor memory with the accumulators
     GemmCall gq = g;
     gq.pair = 0;
     switch (qbn) {
@@ -1828,7 +1785,6 @@ int gemm_run(const GemmCall &g, cudaStream_t st) {
       case 32: return launch_q4<32>(gq, st, d);
       case 64: return launch_q4<64>(gq, st, d);
       case 128: return launch_q4<128>(gq, st, d);
-      case 256: return launch_q4<256>(gq, st, d);
       default: return DFLASH_ERR_DIMS;
     }
   }

@@ -84,11 +84,9 @@ struct GemmCall {
   // two-SM tiles (bf16, uniform schedule, an even number of weight tiles per
   // group): clusters of two CTAs compute 256-row x 256-token tiles
   int pair = 0;
-  // 4-bit weights (DFLASH_Q4 storage; W unused): Wq = codes [N_out][K_in/2] of
-  // this matrix, Wsb = the whole (scale, bias) matrix [K_in/64][sb_rows] whose
-  // rows q_row0.. belong to this matrix; one group, no two-SM tiles
-  const void *Wq = nullptr, *Wsb = nullptr;
-  int sb_rows = 0, q_row0 = 0;
+  // 4-bit weights (W unused): Wq = the 2304-byte records of this matrix, its
+  // row block 0 first (dflash_q4); one group, no two-SM tiles
+  const void *Wq = nullptr;
 };
 
 // Floats of slice scratch a reduce-mode GEMM needs (0 when S == 1 and chunk == 0).

@@ -108,16 +108,18 @@ typedef struct dflash_config {
  * and, per row and group of 64 consecutive input features, a bf16 scale s and
  * bias b; the products use w = bf16(s*q + b) (s*q + b rounded once, to
  * nearest even), activations stay bf16.
- *   codes  device [N][K/2] bytes, 16-byte aligned.  The 32-bit little-endian
- *          word holding input features 8j..8j+7 of a row keeps their codes,
- *          from the least significant nibble up, in the order 8j, 8j+2, 8j+4,
- *          8j+6, 8j+1, 8j+3, 8j+5, 8j+7.
- *   sb     device [K/64][N] 32-bit words, 16-byte aligned, N % 4 == 0: word
- *          (g, n) holds the bf16 scale of row n, group g in its low 16 bits and
- *          the bf16 bias in its high 16 bits.                              */
+ *   data   device, 16-byte aligned: ceil(N/128)*2 row blocks of 64 rows, each
+ *          cut into K/64 records of 2304 bytes, records ordered (row block,
+ *          group): record (r, g) is the codes of rows 64r..64r+63 for input
+ *          features 64g..64g+63 (64 rows x 32 bytes), then their (scale, bias)
+ *          words (64 x 4 bytes: bf16 scale in the low 16 bits, bf16 bias in
+ *          the high 16 bits).  In a row's 32 bytes, the 32-bit little-endian
+ *          word holding features 64g+8j..64g+8j+7 keeps their codes, from the
+ *          least significant nibble up, in the order 8j, 8j+2, 8j+4, 8j+6,
+ *          8j+1, 8j+3, 8j+5, 8j+7.  Rows past N (padding) may hold anything.
+ * One k-block of a 128-row weight tile is then two contiguous records. */
 typedef struct dflash_q4 {
-  const void *codes;
-  const void *sb;
+  const void *data;
 } dflash_q4;
 
 /* One draft layer.  All device pointers, dtype of the config. */
@@ -390,9 +392,8 @@ int dflash_accept_greedy_noalloc(const int32_t *path, const void *target_logits,
 int dflash_linear(int32_t dtype, const void *W, int32_t N_out, int32_t K_in, const void *X,
                   int32_t T, int32_t splits, float *out, void *stream);
 /* The same product with W in the 4-bit format (w = bf16(s*q + b)) and bf16 X:
- * tensor-core GEMM whose weight tiles are dequantized in shared memory.
- *   W       codes / (scale, bias) words of W [N_out, K_in]; N_out % 4 == 0,
- *           K_in a multiple of 64
+ * tensor-core GEMM whose weight tiles are dequantized into tensor memory.
+ *   W       the records of W [N_out, K_in]; K_in a multiple of 64
  *   X, splits, out   as dflash_linear                                       */
 int dflash_linear_q4(dflash_q4 W, int32_t N_out, int32_t K_in, const void *X, int32_t T,
                      int32_t splits, float *out, void *stream);

@@ -190,16 +190,25 @@ class FullCase:
 
     _weights = {}
 
-    def __init__(self, B, K, ctx, seed=0, oracle_requests=None, sel_scale=0.3, wseed=0):
-        self.cfg = synth.preset("full")
+    def __init__(self, B, K, ctx, seed=0, oracle_requests=None, sel_scale=0.3, wseed=0,
+                 q4=False):
+        self.cfg = synth.preset("full", **({"weight_bits": 4} if q4 else {}))
         self.B, self.K = B, K
         self.ctx = np.asarray(ctx, dtype=np.int32)
         self.seed = seed
-        key = (wseed, sel_scale)
+        key = (wseed, sel_scale, q4)
         if key not in FullCase._weights:
             FullCase._weights.clear()
-            FullCase._weights[key] = synth.make_weights(self.cfg, seed=wseed, sel_scale=sel_scale)
-        self.W = FullCase._weights[key]
+            W = synth.make_weights(self.cfg, seed=wseed, sel_scale=sel_scale)
+            Q = None
+            if q4:
+                # the oracle reads the weights the codes stand for (bf16 values, kept
+                # as float32 like the other weights)
+                Q = synth.make_q4_weights(self.cfg, seed=wseed)
+                for n, (q, sc, b) in Q.items():
+                    W[n] = oracle.dequantize_affine(q, sc, b, 64).astype(np.float32)
+            FullCase._weights[key] = (W, Q)
+        self.W, self.Q = FullCase._weights[key]
         Wn, P = self.cfg["window"], self.cfg["page_size"]
         self.lo = np.maximum(0, self.ctx - Wn)
         self.req = np.concatenate([np.full(c - l, b, np.int32)
@@ -258,7 +267,7 @@ class FullCase:
         import torch
         import block_diffusion_drafter_inject_gb300 as dfl
         self.Wd = None
-        self.Wd = dfl.DeviceWeights.from_host(self.cfg, self.W, "cuda")
+        self.Wd = dfl.DeviceWeights.from_host(self.cfg, self.W, "cuda", q4=self.Q)
         self.kv = dfl.PagedKV(self.cfg, self.table, self.num_pages, "cuda")
         self.cyc = dfl.DraftCycle(self.cfg, self.Wd, self.kv, self.B, self.K, max_inject, "cuda")
         if sel_table:

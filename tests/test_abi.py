@@ -227,8 +227,8 @@ def test_launch_counter_resets(dfl):
 
 def test_q4_host_checks(dfl):
     """4-bit weights: the config's weight_bits (0 or 4, bf16 storage only), the
-    codes / (scale, bias) pointers of every projection, dflash_linear_q4's shape
-    rules; all refused before any launch."""
+    record pointer of every projection, dflash_linear_q4's shape rules; all
+    refused before any launch."""
     L = dfl.lib()
     P = ctypes.c_void_p
     a = P(1 << 24)
@@ -248,55 +248,55 @@ def test_q4_host_checks(dfl):
     assert draft(cfg, w) == -1
     base = 1 << 26
     for n in dfl._lib.Q4_TOP:
-        q = getattr(w, n + "_q4")
-        q.codes, q.sb = base, base + 4096
+        getattr(w, n + "_q4").data = base
         base += 8192
     for l in range(cfg.n_layers):
         for n in dfl._lib.Q4_LAYER:
-            q = getattr(w.layer[l], n + "_q4")
-            q.codes, q.sb = base, base + 4096
+            getattr(w.layer[l], n + "_q4").data = base
             base += 8192
-    w.layer[1].w_down_q4.sb = base + 8                      # misaligned
+    w.layer[1].w_down_q4.data = base + 8                    # misaligned
     assert draft(cfg, w) == -7
-    w.layer[1].w_down_q4.sb = base
-    w.layer[0].wo_q4.codes = 0
+    w.layer[1].w_down_q4.data = base
+    w.layer[0].wo_q4.data = 0
     assert draft(cfg, w) == -1
     # the 4-bit product
     q = dfl._lib.Q4()
-    q.codes, q.sb = 1 << 24, 1 << 25
-    assert L.dflash_linear_q4(q, 130, 512, a, 8, 1, a, None) == -2     # rows % 4
+    q.data = 1 << 24
     assert L.dflash_linear_q4(q, 128, 500, a, 8, 1, a, None) == -2     # K % 64
     assert L.dflash_linear_q4(q, 128, 512, a, 8, 3, a, None) == -2     # splits must divide
     assert L.dflash_linear_q4(q, 128, 512, a, 0, 1, a, None) == 0      # no tokens
     assert L.dflash_linear_q4(q, 128, 512, P(0), 8, 1, a, None) == -1
-    q.sb = (1 << 25) + 4
+    q.data = (1 << 24) + 4
     assert L.dflash_linear_q4(q, 128, 512, a, 8, 1, a, None) == -7
 
 
 def test_pack_q4_layout(dfl):
-    """The binding's 4-bit packing follows the header: in the word of input features
-    8j..8j+7, (word >> 4i) & 0xF and (word >> (16 + 4i)) & 0xF are the codes of
-    features 8j+2i and 8j+2i+1; the (scale, bias) words are group-major."""
+    """The binding's 4-bit packing follows the header: rows padded to 128, one
+    2304-byte record per (64-row block, group of 64 inputs), row block major; in
+    a record, row i's 32 code bytes then its (scale, bias) word at 2048 + 4i; in
+    the word of features 8j..8j+7, (word >> 4k) & 0xF and (word >> (16 + 4k)) & 0xF
+    are the codes of features 8j+2k and 8j+2k+1."""
     import numpy as np
     import torch
     g = np.random.default_rng(0)
-    N, K = 6, 128
+    N, K = 70, 192
     q = g.integers(0, 16, (N, K)).astype(np.uint8)
     s = torch.tensor(g.uniform(0.001, 1.0, (N, K // 64)), dtype=torch.float32).to(torch.bfloat16)
     b = torch.tensor(g.standard_normal((N, K // 64)), dtype=torch.float32).to(torch.bfloat16)
-    codes, sb = dfl.pack_q4(q, s.float().numpy(), b.float().numpy())
-    assert codes.shape == (N, K // 2) and sb.shape == (K // 64, N)
-    words = codes.numpy().view("<u4")
-    for n in range(N):
-        for j in range(K // 8):
-            w = int(words[n, j])
-            for i in range(4):
-                assert (w >> (4 * i)) & 15 == q[n, 8 * j + 2 * i]
-                assert (w >> (16 + 4 * i)) & 15 == q[n, 8 * j + 2 * i + 1]
+    data = dfl.pack_q4(q, s.float().numpy(), b.float().numpy()).numpy()
+    G = K // 64
+    assert data.shape == (2 * G * 2304,)                   # 70 rows -> 128 -> 2 blocks
     sbits = s.view(torch.int16).numpy().astype(np.uint16)
     bbits = b.view(torch.int16).numpy().astype(np.uint16)
-    sbw = sb.numpy().view("<u4")
     for n in range(N):
-        for grp in range(K // 64):
-            assert sbw[grp, n] & 0xFFFF == sbits[n, grp]
-            assert sbw[grp, n] >> 16 == bbits[n, grp]
+        for grp in range(G):
+            rec = data[((n // 64) * G + grp) * 2304:][:2304]
+            i = n % 64
+            words = rec[32 * i:32 * i + 32].view("<u4")
+            for j in range(8):
+                w = int(words[j])
+                for k in range(4):
+                    assert (w >> (4 * k)) & 15 == q[n, 64 * grp + 8 * j + 2 * k]
+                    assert (w >> (16 + 4 * k)) & 15 == q[n, 64 * grp + 8 * j + 2 * k + 1]
+            sw = int(rec[2048 + 4 * i:2052 + 4 * i].view("<u4")[0])
+            assert sw & 0xFFFF == sbits[n, grp] and sw >> 16 == bbits[n, grp]

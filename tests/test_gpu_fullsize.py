@@ -109,6 +109,16 @@ def test_full_b1_k8_ctx2048():
     _check_request(case, 0)
 
 
+def test_full_q4_b1_k8_ctx2048():
+    """The 4-bit drafter at full size (fc, QKV, O, gate/up, down, lm_head as codes
+    with a bf16 scale and bias per 64 inputs): the serving cycle, the last 8
+    context rows injected by the pass, against the oracle on the weights the codes
+    stand for."""
+    case = FullCase(1, 8, [2048], seed=3, q4=True).device(tail=[8])
+    assert case.status == 0 and case.n_fused == 8
+    _check_request(case, 0)
+
+
 def test_full_b1_unaligned_window_with_selector_table():
     """Context 2100: the window starts mid-page, so it spans 17 cache pages and
     the last of the 16 key splits takes three tiles (two context pages and the

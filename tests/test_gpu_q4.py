@@ -33,21 +33,20 @@ def _q4(N, K, seed):
 
 def _run(q, s, b, X, splits):
     import block_diffusion_drafter_inject_gb300 as dfl
-    codes, sb = dfl.pack_q4(q, s, b)
-    codes, sb = codes.cuda(), sb.cuda()
+    data = dfl.pack_q4(q, s, b).cuda()
     T = X.shape[0]
     out = torch.zeros((splits, T, q.shape[0]), dtype=torch.float32, device="cuda")
-    dfl.linear_q4(codes, sb, X, out, splits)
+    dfl.linear_q4(data, q.shape[0], X, out, splits)
     torch.cuda.synchronize()
     return out.double().sum(0).cpu().numpy()
 
 
 @pytest.mark.parametrize("N,K,T,splits", [
     (384, 512, 1, 1), (384, 512, 7, 2), (260, 512, 16, 4), (512, 1024, 33, 2),
-    (384, 256, 64, 1), (256, 512, 200, 2), (128, 512, 300, 1),
+    (384, 256, 64, 1), (256, 512, 200, 2), (128, 512, 300, 1), (70, 192, 20, 3),
 ])
 def test_linear_q4_matches_dequantized_product(N, K, T, splits):
-    """Token tiles 16..256, K slices, a weight tail (260 rows): within fp32
+    """Token tiles 16..128, K slices, weight tails (260, 70 rows): within fp32
     accumulation of the bf16 products of the oracle's dequantized weights."""
     q, s, b = _q4(N, K, seed=N + K + T)
     Xh = np.random.default_rng(T).standard_normal((T, K)).astype(np.float32)
