@@ -297,6 +297,24 @@ def bench_inject_rows(torch, dfl, cfg, pk, args, N=4096):
             "device_status": dfl.read_device_status(ws)}
 
 
+def bench_q4_lm_head(torch, dfl, cfg, pk, args, T=7):
+    """The 4-bit lm_head GEMM alone (vocab x d_model, T tokens) with only its records
+    on the device (350 MB of random bytes: the time does not depend on the values):
+    the small case on which the 4-bit GEMM is profiled."""
+    V, D = cfg["vocab"], cfg["d_model"]
+    nbytes = (V + 127) // 128 * 2 * (D // 64) * 2304
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4)
+    rec = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda", generator=gen)
+    X = torch.randn((T, D), device="cuda", generator=gen).to(torch.bfloat16)
+    S = dfl.linear_splits(V, T, D)
+    out = torch.empty((S, T, V), device="cuda", dtype=torch.float32)
+    steps = max(3, min(args.steps, 20))
+    ms = event_time(torch, lambda: dfl.linear_q4(rec, V, X, out, S), steps, args.warmup)
+    return {"shape": [V, D, T], "us": ms * 1e3, "record_bytes": nbytes,
+            "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / pk["hbm"]}
+
+
 def run_gpu(args, rank, world, barrier, allmax):
     import torch
     import block_diffusion_drafter_inject_gb300 as dfl
@@ -307,6 +325,8 @@ def run_gpu(args, rank, world, barrier, allmax):
     pk = peaks()
     if args.sections == {"inject4k"}:
         return {"inject4k": bench_inject_rows(torch, dfl, cfg, pk, args)}, None
+    if args.sections == {"q4lm"}:
+        return {"q4lm": bench_q4_lm_head(torch, dfl, cfg, pk, args)}, None
     t0 = time.time()
     Wh = synth.make_weights(cfg, seed=0)
     Wd = dfl.DeviceWeights.from_host(cfg, Wh, "cuda")
@@ -746,9 +766,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--only", default="",
                     help="comma list of sections to run: b1 (headline), b32, inject, q4 "
-                         "(the headline workload with 4-bit weights); or "
-                         "inject4k alone (a 4096-row injection with only its weights loaded, "
-                         "the small profiling case)")
+                         "(the headline workload with 4-bit weights); or, alone, a small "
+                         "profiling case: inject4k (a 4096-row injection with only its weights "
+                         "loaded) or q4lm (the 4-bit lm_head GEMM with only its records)")
     ap.add_argument("--no-b32", action="store_true")
     ap.add_argument("--no-inject", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
