@@ -630,7 +630,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // a bf16x2), then the rows' (scale, bias) words (bf16 scale low, bias high).
 // A k-block of a 128-row tile is two contiguous records, brought in by two bulk
 // copies.
-// Roles (448 threads): warp 0 bulk-copy producer (records, activation tile),
+// Roles (448 threads): warp 0 bulk-copy producer (records, activation tiles),
 // warp 1 MMA issuer, warps 2-5 one epilogue group (the epilogue of k_gemm_tc),
 // warps 6-13 dequantize: the thread on tensor-memory lane r (warp w covers
 // lanes 32*(w%4)..) of half h = (w - 6) / 4 turns inputs 32h..32h+31 of row r
@@ -641,18 +641,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // released by the dequantizers and the MMA together; tensor memory holds the
 // two accumulators and a ring of A buffers released by the MMA's commits.
 constexpr int kQ4Record = 64 * 32 + 64 * 4;  // codes and pairs of 64 rows x 64 inputs
+// A stage carries KPS consecutive k-blocks of a segment (fewer at a segment's
+// end): the MMA issuer's barrier waits, fence and commits, which cost more than
+// its four MMAs per k-block, are paid once per stage.
 template <int BN>
 struct QShape {
   static_assert(BN <= 128, "4-bit tiles keep A buffers beside the accumulators");
+  static constexpr int KPS = BN <= 64 ? 4 : 2;
   static constexpr int X_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = X_BYTES + 5120;  // 1024-byte aligned stages
-  static constexpr int TX_BYTES = X_BYTES + 2 * kQ4Record;
-  static constexpr int NQ = BN <= 16 ? 28 : BN <= 32 ? 22 : BN <= 64 ? 15 : 9;
+  static constexpr int KB_TX = X_BYTES + 2 * kQ4Record;  // bytes one k-block brings in
+  // KPS activation tiles (1024-byte aligned), then KPS pairs of records
+  static constexpr int STAGE_BYTES = (KPS * KB_TX + 1023) / 1024 * 1024;
+  static constexpr int NQ = (232448 - 18 * 1024 - 1024 - 768) / STAGE_BYTES;
   static constexpr int TMEM_COLS = 512;
   static constexpr int A_COL0 = 2 * BN < 32 ? 32 : 2 * BN;  // after the accumulators
-  static constexpr int NA = (TMEM_COLS - A_COL0) / 32 > 14 ? 14 : (TMEM_COLS - A_COL0) / 32;
+  static constexpr int A_COLS = 32 * KPS;                    // one stage's A buffer
+  static constexpr int NA = (TMEM_COLS - A_COL0) / A_COLS;
   static constexpr int SMEM_BYTES = NQ * STAGE_BYTES + 1024 + 768;
+  static_assert(NA >= 2 && NQ >= 2, "rings");
   static_assert(SMEM_BYTES + 18 * 1024 <= 232448, "dynamic + the epilogue's static shared memory");
+  static_assert(2 * NQ + 2 * NA + 5 <= 768 / 8 - 1, "barriers");
 };
 constexpr int kQ4Epi = 1;  // epilogue groups
 constexpr int kQ4Dq = 8;   // dequantizing warps
@@ -684,7 +692,7 @@ template <int BN>
 __global__ void __launch_bounds__(kQ4Threads, 1)
     k_gemm_q4(const __grid_constant__ CUtensorMap tmX, GemmParams p) {
   using QS = QShape<BN>;
-  constexpr int NQ = QS::NQ, NA = QS::NA;
+  constexpr int NQ = QS::NQ, NA = QS::NA, KPS = QS::KPS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *qfull = (uint64_t *)(smem + NQ * QS::STAGE_BYTES);
@@ -699,6 +707,11 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // stage layout: activation tile k at k * X_BYTES, records of k-block k after the tiles
+  auto xtile = [&](int st, int k) { return smem + st * QS::STAGE_BYTES + k * QS::X_BYTES; };
+  auto recs = [&](int st, int k) {
+    return smem + st * QS::STAGE_BYTES + KPS * QS::X_BYTES + k * 2 * kQ4Record;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NQ; ++s) {
@@ -730,7 +743,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- bulk-copy producer ----------------
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
       int stage = 0;
@@ -738,40 +751,39 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
       uint32_t last_phase[NQ];
       bool issued[NQ];
       for (int s = 0; s < NQ; ++s) issued[s] = false, last_phase[s] = 0;
-      // codes and pairs do not depend on the previous kernel: the first stages'
-      // start before waiting for it, the activation tiles after
+      // records do not depend on the previous kernel: the first stages' start
+      // before waiting for it, the activation tiles after
       int pre = 0;
       {
-        int cnt = 0;
         Seg sg;
-        for (int i = 0; cnt < NQ && get_seg(p, i, sg); ++i) {
-          for (int kb = 0; kb < sg.nkb && cnt < NQ; ++kb, ++cnt) {
-            mbar_expect_tx(&qfull[cnt], QS::TX_BYTES);
-            load_wq(smem + cnt * QS::STAGE_BYTES + QS::X_BYTES, &qfull[cnt], sg.kb0 + kb,
-                    sg.m_tile, p, pol_w);
+        for (int i = 0; pre < NQ && get_seg(p, i, sg); ++i) {
+          for (int kb = 0; kb < sg.nkb && pre < NQ; kb += KPS, ++pre) {
+            const int nk = min(KPS, sg.nkb - kb);
+            mbar_expect_tx(&qfull[pre], nk * QS::KB_TX);
+            for (int k = 0; k < nk; ++k)
+              load_wq(recs(pre, k), &qfull[pre], sg.kb0 + kb + k, sg.m_tile, p, pol_w);
           }
         }
-        pre = cnt;
       }
       pdl_wait();
       bool ok = true;
       int n = 0;
       Seg sg;
       for (int i = 0; ok && get_seg(p, i, sg); ++i) {
-        for (int kb = 0; kb < sg.nkb; ++kb, ++n) {
-          uint8_t *st = smem + stage * QS::STAGE_BYTES;
-          const int kx = (sg.kb0 + kb) * BK;
-          if (n < pre) {
-            tma_load_2d(st, &tmX, &qfull[stage], kx, sg.t_tile * BN, pol_x);
-          } else {
+        for (int kb = 0; kb < sg.nkb; kb += KPS, ++n) {
+          const int nk = min(KPS, sg.nkb - kb);
+          if (n >= pre) {
             if (!mbar_wait(&qempty[stage], phase ^ 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
-            mbar_expect_tx(&qfull[stage], QS::TX_BYTES);
-            load_wq(st + QS::X_BYTES, &qfull[stage], sg.kb0 + kb, sg.m_tile, p, pol_w);
-            tma_load_2d(st, &tmX, &qfull[stage], kx, sg.t_tile * BN, pol_x);
+            mbar_expect_tx(&qfull[stage], nk * QS::KB_TX);
+            for (int k = 0; k < nk; ++k)
+              load_wq(recs(stage, k), &qfull[stage], sg.kb0 + kb + k, sg.m_tile, p, pol_w);
           }
+          for (int k = 0; k < nk; ++k)
+            tma_load_2d(xtile(stage, k), &tmX, &qfull[stage], (sg.kb0 + kb + k) * BK,
+                        sg.t_tile * BN, pol_x);
           issued[stage] = true;
           last_phase[stage] = phase;
           if (++stage == NQ) stage = 0, phase ^= 1;
@@ -803,19 +815,22 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < sg.nkb; ++kb) {
+        for (int kb = 0; kb < sg.nkb; kb += KPS) {
+          const int nk = min(KPS, sg.nkb - kb);
           if (!mbar_wait(&afull[as], aph, abort_flag, p.wait_ns) ||
               !mbar_wait(&qfull[qs], qph, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_tmem = tmem_base + (uint32_t)(QS::A_COL0 + as * 32);
-          const uint64_t bdesc = sdesc_k_sw128(smem_u32(smem + qs * QS::STAGE_BYTES));
+          const uint32_t a_tmem = tmem_base + (uint32_t)(QS::A_COL0 + as * QS::A_COLS);
+          for (int k = 0; k < nk; ++k) {
+            const uint64_t bdesc = sdesc_k_sw128(smem_u32(xtile(qs, k)));
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)  // 16 bf16 of K = 8 tensor-memory columns
-            tc_mma_bf16_ta(d_tmem, a_tmem + (uint32_t)(k * 8), bdesc + (uint64_t)(k * 2), idesc,
-                           (kb | k) != 0);
+            for (int j = 0; j < BK / 16; ++j)  // 16 bf16 of K = 8 tensor-memory columns
+              tc_mma_bf16_ta(d_tmem, a_tmem + (uint32_t)(k * 32 + j * 8),
+                             bdesc + (uint64_t)(j * 2), idesc, (kb | k | j) != 0);
+          }
           tc_commit(&qempty[qs]);
           tc_commit(&aempty[as]);
           if (++qs == NQ) qs = 0, qph ^= 1;
@@ -845,7 +860,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
     int qs = 0, as = 0, pq = 0, pa = 0;
     uint32_t qph = 0, aph = 0;
     bool ok = true, pending = false;
-    // hand k-block (pq, pa) over once its tensor-memory store has completed
+    // hand stage (pq, pa) over once its tensor-memory stores have completed
     auto release = [&]() {
       tc_wait_st();
       tc_fence_before();
@@ -857,7 +872,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
     };
     Seg sg;
     for (int i = 0; ok && get_seg(p, i, sg); ++i) {
-      for (int kb = 0; kb < sg.nkb; ++kb) {
+      for (int kb = 0; kb < sg.nkb; kb += KPS) {
+        const int nk = min(KPS, sg.nkb - kb);
         const bool got = mbar_wait(&qfull[qs], qph, abort_flag, p.wait_ns) &&
                          mbar_wait(&aempty[as], aph ^ 1, abort_flag, p.wait_ns);
         if (!__all_sync(0xffffffffu, got)) {  // the warp gives up together
@@ -865,21 +881,23 @@ __global__ void __launch_bounds__(kQ4Threads, 1)
           break;
         }
         tc_fence_after();
-        const uint8_t *rec = smem + qs * QS::STAGE_BYTES + QS::X_BYTES + roff;
-        const uint4 w = *(const uint4 *)(rec + rrow * 32 + 16 * h);
-        const uint32_t sb = *(const uint32_t *)(rec + 64 * 32 + rrow * 4);
-        const uint32_t s2 = (sb & 0xFFFFu) * 0x10001u, b2 = (sb >> 16) * 0x10001u;
-        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
-        uint32_t a[16];  // column 16h + j: weights (32h + 2j, 32h + 2j + 1) of the row
+        for (int k = 0; k < nk; ++k) {
+          const uint8_t *rec = recs(qs, k) + roff;
+          const uint4 w = *(const uint4 *)(rec + rrow * 32 + 16 * h);
+          const uint32_t sb = *(const uint32_t *)(rec + 64 * 32 + rrow * 4);
+          const uint32_t s2 = (sb & 0xFFFFu) * 0x10001u, b2 = (sb >> 16) * 0x10001u;
+          const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+          uint32_t a[16];  // column 16h + j: weights (32h + 2j, 32h + 2j + 1) of the row
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          a[4 * c + 0] = dq_pair(wd[c], 0, s2, b2);
-          a[4 * c + 1] = dq_pair(wd[c], 4, s2, b2);
-          a[4 * c + 2] = dq_pair(wd[c], 8, s2, b2);
-          a[4 * c + 3] = dq_pair(wd[c], 12, s2, b2);
+          for (int c = 0; c < 4; ++c) {
+            a[4 * c + 0] = dq_pair(wd[c], 0, s2, b2);
+            a[4 * c + 1] = dq_pair(wd[c], 4, s2, b2);
+            a[4 * c + 2] = dq_pair(wd[c], 8, s2, b2);
+            a[4 * c + 3] = dq_pair(wd[c], 12, s2, b2);
+          }
+          if (k == 0 && pending) release();  // the previous stage's stores had this long
+          tc_st16(lane_addr + (uint32_t)(as * QS::A_COLS + k * 32), a);
         }
-        if (pending) release();  // the previous k-block's store had this long to land
-        tc_st16(lane_addr + (uint32_t)(as * 32), a);
         pending = true;
         pq = qs;
         pa = as;
