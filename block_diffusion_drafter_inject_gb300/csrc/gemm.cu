@@ -107,10 +107,15 @@ template <int BN>
 struct GemmShape {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN <= 16 ? 11 : BN <= 32 ? 10 : BN <= 64 ? 8 : BN <= 128 ? 6 : 4;
+  static constexpr int KB_BYTES = A_BYTES + B_BYTES;  // one k-block: weight tile, token tile
+  // a stage carries KPS consecutive k-blocks of a segment (fewer at its end), so the
+  // MMA issuer's barrier wait, fence and commit are paid once per KPS k-blocks
+  static constexpr int KPS = BN <= 128 ? 2 : 1;
+  static constexpr int STAGE_BYTES = KPS * KB_BYTES;
+  static constexpr int STAGES = (232448 - 18 * 1024 - 1024 - 256) / STAGE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(STAGES >= 3 && 2 * STAGES + 6 <= 256 / 8 - 1, "ring and barriers");
 };
 
 // Tile index -> (weight tile, token tile).  Token tile fastest, so that the CTAs
@@ -510,36 +515,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // stages' weight tiles before waiting for it, then add activations.
       int pre = 0;
       {
-        int cnt = 0;
         Seg sg;
-        for (int i = 0; cnt < STAGES && get_seg(p, i, sg); ++i) {
-          for (int kb = 0; kb < sg.nkb && cnt < STAGES; ++kb, ++cnt) {
-            mbar_expect_tx(&full[cnt], SH::STAGE_BYTES);
-            load_w(smem + cnt * SH::STAGE_BYTES, tmW, &full[cnt], (sg.kb0 + kb) * BK, sg.m_tile,
-                   p, pol_w);
+        for (int i = 0; pre < STAGES && get_seg(p, i, sg); ++i) {
+          for (int kb = 0; kb < sg.nkb && pre < STAGES; kb += SH::KPS, ++pre) {
+            const int nk = min(SH::KPS, sg.nkb - kb);
+            mbar_expect_tx(&full[pre], nk * SH::KB_BYTES);
+            for (int k = 0; k < nk; ++k)
+              load_w(smem + pre * SH::STAGE_BYTES + k * SH::KB_BYTES, tmW, &full[pre],
+                     (sg.kb0 + kb + k) * BK, sg.m_tile, p, pol_w);
           }
         }
-        pre = cnt;
       }
       pdl_wait();
       bool ok = true;
       int n = 0;  // fill counter across segments
       Seg sg;
       for (int i = 0; ok && get_seg(p, i, sg); ++i) {
-        for (int kb = 0; kb < sg.nkb; ++kb, ++n) {
+        for (int kb = 0; kb < sg.nkb; kb += SH::KPS, ++n) {
           uint8_t *sa = smem + stage * SH::STAGE_BYTES;
-          const int kx = (sg.kb0 + kb) * BK;
-          if (n < pre) {
-            tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, sg.t_tile * BN, pol_x);
-          } else {
+          const int nk = min(SH::KPS, sg.nkb - kb);
+          if (n >= pre) {
             if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
-            mbar_expect_tx(&full[stage], SH::STAGE_BYTES);
-            load_w(sa, tmW, &full[stage], kx, sg.m_tile, p, pol_w);
-            tma_load_2d(sa + SH::A_BYTES, &tmX, &full[stage], kx, sg.t_tile * BN, pol_x);
+            mbar_expect_tx(&full[stage], nk * SH::KB_BYTES);
+            for (int k = 0; k < nk; ++k)
+              load_w(sa + k * SH::KB_BYTES, tmW, &full[stage], (sg.kb0 + kb + k) * BK, sg.m_tile,
+                     p, pol_w);
           }
+          for (int k = 0; k < nk; ++k)
+            tma_load_2d(sa + k * SH::KB_BYTES + SH::A_BYTES, &tmX, &full[stage],
+                        (sg.kb0 + kb + k) * BK, sg.t_tile * BN, pol_x);
           issued[stage] = true;
           last_phase[stage] = phase;
           if (++stage == STAGES) stage = 0, phase ^= 1;
@@ -573,20 +580,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < sg.nkb; ++kb) {
+        for (int kb = 0; kb < sg.nkb; kb += SH::KPS) {
+          const int nk = min(SH::KPS, sg.nkb - kb);
           if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * SH::STAGE_BYTES);
-          const uint64_t adesc = sdesc_k_sw128(sa);
-          const uint64_t bdesc = sdesc_k_sw128(sa + SH::A_BYTES);
+          for (int k = 0; k < nk; ++k) {
+            const uint32_t sa = smem_u32(smem + stage * SH::STAGE_BYTES + k * SH::KB_BYTES);
+            const uint64_t adesc = sdesc_k_sw128(sa);
+            const uint64_t bdesc = sdesc_k_sw128(sa + SH::A_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            // advance 16 bf16 = 32 bytes along K inside the swizzled row
-            tc_mma_bf16(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc,
-                        (kb | k) != 0);
+            for (int j = 0; j < BK / 16; ++j) {
+              // advance 16 bf16 = 32 bytes along K inside the swizzled row
+              tc_mma_bf16(d_tmem, adesc + (uint64_t)(j * 2), bdesc + (uint64_t)(j * 2), idesc,
+                          (kb | k | j) != 0);
+            }
           }
           tc_commit(&empty[stage]);
           if (++stage == STAGES) stage = 0, phase ^= 1;
