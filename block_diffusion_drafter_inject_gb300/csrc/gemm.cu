@@ -956,8 +956,10 @@ constexpr int kPairBN = 256;
 struct PairShape {
   static constexpr int A_BYTES = BM * BK * 2;             // this CTA's 128 weight rows
   static constexpr int B_BYTES = (kPairBN / 2) * BK * 2;  // this CTA's 128 tokens
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 6;
+  static constexpr int KB_BYTES = A_BYTES + B_BYTES;      // one k-block
+  static constexpr int KPS = 2;                            // k-blocks a stage
+  static constexpr int STAGE_BYTES = KPS * KB_BYTES;
+  static constexpr int STAGES = 3;
   static constexpr int TMEM_COLS = 2 * kPairBN;  // two accumulators of 256 columns
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 512 /*barriers*/;
 };
@@ -1060,37 +1062,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; s < STAGES; ++s) issued[s] = false, last_phase[s] = 0;
       int pre = 0;
       {
-        int cnt = 0;
         Seg sg;
-        for (int i = 0; cnt < STAGES && get_seg_pair(p, i, rank, sg); ++i) {
-          for (int kb = 0; kb < sg.nkb && cnt < STAGES; ++kb, ++cnt) {
-            if (even) mbar_expect_tx(&full[cnt], 2 * SH::STAGE_BYTES);
-            load_w_pair(smem + cnt * SH::STAGE_BYTES, tmW, full0 + (uint32_t)(cnt * 8),
-                        (sg.kb0 + kb) * BK, sg.m_tile, p, pol_w);
+        for (int i = 0; pre < STAGES && get_seg_pair(p, i, rank, sg); ++i) {
+          for (int kb = 0; kb < sg.nkb && pre < STAGES; kb += SH::KPS, ++pre) {
+            const int nk = min(SH::KPS, sg.nkb - kb);
+            if (even) mbar_expect_tx(&full[pre], 2 * nk * SH::KB_BYTES);
+            for (int k = 0; k < nk; ++k)
+              load_w_pair(smem + pre * SH::STAGE_BYTES + k * SH::KB_BYTES, tmW,
+                          full0 + (uint32_t)(pre * 8), (sg.kb0 + kb + k) * BK, sg.m_tile, p,
+                          pol_w);
           }
         }
-        pre = cnt;
       }
       pdl_wait();
       bool ok = true;
       int n = 0;
       Seg sg;
       for (int i = 0; ok && get_seg_pair(p, i, rank, sg); ++i) {
-        for (int kb = 0; kb < sg.nkb; ++kb, ++n) {
+        for (int kb = 0; kb < sg.nkb; kb += SH::KPS, ++n) {
           uint8_t *sa = smem + stage * SH::STAGE_BYTES;
-          const int kx = (sg.kb0 + kb) * BK;
+          const int nk = min(SH::KPS, sg.nkb - kb);
           const uint32_t fb = full0 + (uint32_t)(stage * 8);
-          if (n < pre) {
-            tma_load_2d_pair(sa + SH::A_BYTES, &tmX, fb, kx, sg.t_tile * BN + xrow, pol_x);
-          } else {
+          if (n >= pre) {
             if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
-            if (even) mbar_expect_tx(&full[stage], 2 * SH::STAGE_BYTES);
-            load_w_pair(sa, tmW, fb, kx, sg.m_tile, p, pol_w);
-            tma_load_2d_pair(sa + SH::A_BYTES, &tmX, fb, kx, sg.t_tile * BN + xrow, pol_x);
+            if (even) mbar_expect_tx(&full[stage], 2 * nk * SH::KB_BYTES);
+            for (int k = 0; k < nk; ++k)
+              load_w_pair(sa + k * SH::KB_BYTES, tmW, fb, (sg.kb0 + kb + k) * BK, sg.m_tile, p,
+                          pol_w);
           }
+          for (int k = 0; k < nk; ++k)
+            tma_load_2d_pair(sa + k * SH::KB_BYTES + SH::A_BYTES, &tmX, fb, (sg.kb0 + kb + k) * BK,
+                             sg.t_tile * BN + xrow, pol_x);
           issued[stage] = true;
           last_phase[stage] = phase;
           if (++stage == STAGES) stage = 0, phase ^= 1;
@@ -1119,19 +1124,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-          for (int kb = 0; kb < sg.nkb; ++kb) {
+          for (int kb = 0; kb < sg.nkb; kb += SH::KPS) {
+            const int nk = min(SH::KPS, sg.nkb - kb);
             if (!mbar_wait<true>(&full[stage], phase, abort_flag, p.wait_ns)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t sa = smem_u32(smem + stage * SH::STAGE_BYTES);
-            const uint64_t adesc = sdesc_k_sw128(sa);
-            const uint64_t bdesc = sdesc_k_sw128(sa + SH::A_BYTES);
+            for (int k = 0; k < nk; ++k) {
+              const uint32_t sa = smem_u32(smem + stage * SH::STAGE_BYTES + k * SH::KB_BYTES);
+              const uint64_t adesc = sdesc_k_sw128(sa);
+              const uint64_t bdesc = sdesc_k_sw128(sa + SH::A_BYTES);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-              tc2_mma_bf16(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), idesc,
-                           (kb | k) != 0);
+              for (int j = 0; j < BK / 16; ++j)
+                tc2_mma_bf16(d_tmem, adesc + (uint64_t)(j * 2), bdesc + (uint64_t)(j * 2), idesc,
+                             (kb | k | j) != 0);
+            }
             any = true;
             tc2_commit_mc(&empty[stage], 0x3);
             if (++stage == STAGES) stage = 0, phase ^= 1;
