@@ -1441,12 +1441,17 @@ bool bf16_map(CUtensorMap *out, const void *ptr, uint64_t rows, uint64_t cols,
 static int token_tile(int T) { return T <= 16 ? 16 : T <= 32 ? 32 : T <= 64 ? 64 : T <= 128 ? 128 : 256; }
 
 // One k-block of one CTA (microseconds): the slowest of the weight tile from
-// HBM (~46 GB/s per CTA, measured with per-CTA timestamps), both tiles through
-// TMA (~110 GB/s per CTA, the activation tile mostly from L2) and the tensor
-// pipe (~11 TFLOP/s per CTA).
-static double stage_us(int bn) {
+// HBM (~46 GB/s per CTA, measured with per-CTA timestamps; a weight tile shared
+// by several token tiles is streamed by the CTAs of those tiles together, mostly
+// from L2), both tiles through TMA (~110 GB/s per CTA, the activation tile mostly
+// from L2) and the MMA issuer: ~0.25 us of barrier wait, fence and commit per
+// pipeline stage, shared by the stage's k-blocks, plus the tensor pipe's time
+// (~11 TFLOP/s per CTA).
+static double stage_us(int bn, bool shared_w) {
   const double a = 128.0 * 64 * 2, b = (double)bn * 64 * 2;
-  return std::max(std::max(a / 46e3, (a + b) / 110e3), 2.0 * 128 * bn * 64 / 11e6);
+  const int kps = bn <= 128 ? 2 : 1;  // k-blocks a stage (GemmShape::KPS)
+  const double issue = 0.25 / kps + 2.0 * 128 * bn * 64 / 11e6;
+  return std::max(std::max(shared_w ? 0.0 : a / 46e3, (a + b) / 110e3), issue);
 }
 
 // Epilogue of one tile (microseconds): per 16-column chunk a tensor-memory
@@ -1477,7 +1482,7 @@ static double gemm_cost(int N_out, int T, int K_in, int S, int bn, int mode, int
   const int m_tiles = (N_out + dfl::BM - 1) / dfl::BM;
   const double kbps = kb / S;
   const double uA = 128.0 * 64 * 2 * kbps;
-  const double t_unit = kbps * stage_us(bn) + 0.15;
+  const double t_unit = kbps * stage_us(bn, t_tiles > 1) + 0.15;
   const long U = (long)m_tiles * t_tiles * S;
   const double wbytes = 2.0 * N_out * K_in;
   const double hbm_share = wbytes > 48e6 ? 1.0 : 1.0 / t_tiles;  // re-read per token tile?
@@ -1513,7 +1518,7 @@ static double gemm_cost_balanced(int N_out, int T, int K_in, int bn, int mode, i
   *chunk_out = (int)chunk;
   if (chunk < 2 || total > (1L << 30)) return 1e300;
   const int segs = (int)((chunk + kb - 1) / kb) + 1;
-  const double t_cta = chunk * stage_us(bn) + 0.15 * segs;
+  const double t_cta = chunk * stage_us(bn, t_tiles > 1) + 0.15 * segs;
   const double wbytes = 2.0 * N_out * K_in;
   const double hbm = wbytes * (wbytes > 48e6 ? t_tiles : 1) / 6.5e6;
   double tot = std::max(t_cta, hbm);
