@@ -418,10 +418,37 @@ def bench_b1(torch, dfl, cfg, Wd, pk, args, world, barrier, allmax, dev):
     h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = out_acc.numel() * 4 + out_tok.numel() * 4
 
+    # The target's logits are read only by acceptance: the serving loop copies them
+    # on a side stream while the pass runs (once the previous step's acceptance has
+    # been issued, so that the buffer it reads is not overwritten); the rest of the
+    # inputs go first on the main stream.
+    def front():
+        dfl.draft_block_inject(cfg, Wd, kv, inp["hidden"], inp["req"], inp["pos"],
+                               inp["anchor"], inp["ctx"], K, cyc.ws, cyc.topk_ids, cyc.topk_logp)
+        dfl.select_path(cfg, Wd, inp["anchor"], cyc.topk_ids, cyc.topk_logp, K, cyc.ws, cyc.path,
+                        cyc.score)
+
+    def back():
+        dfl.accept_greedy(cyc.path, inp["target"], cyc.ws, cyc.accept_len, cyc.tokens)
+
+    g_front = capture(torch, front)
+    g_back = capture(torch, back)
+    side = torch.cuda.Stream()
+    ev_free, ev_copied = torch.cuda.Event(), torch.cuda.Event()
+
     def e2e_step():
+        main = torch.cuda.current_stream()
         for k in inp:
-            inp[k].copy_(pin[k], non_blocking=True)
-        g_cycle.replay()
+            if k != "target":
+                inp[k].copy_(pin[k], non_blocking=True)
+        ev_free.record(main)
+        side.wait_event(ev_free)
+        with torch.cuda.stream(side):
+            inp["target"].copy_(pin["target"], non_blocking=True)
+            ev_copied.record(side)
+        g_front.replay()
+        main.wait_event(ev_copied)
+        g_back.replay()
         out_acc.copy_(cyc.accept_len, non_blocking=True)
         out_tok.copy_(cyc.tokens, non_blocking=True)
 
@@ -448,7 +475,9 @@ def bench_b1(torch, dfl, cfg, Wd, pk, args, world, barrier, allmax, dev):
                      "algorithmic_bytes_per_pass": gem_bytes, "us_per_pass": ms_gemm * 1e3,
                      "peak_source": pk["src"]},
         "e2e": {"value": whole_job_value(world, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "note": "target logits copied on a side stream during the pass, joined before "
+                        "acceptance; the other inputs before the pass"},
         "gpu_launches": launches_per_cycle * args.steps,
         "launches_per_cycle": launches_per_cycle,
         "clocks": clocks,
