@@ -348,6 +348,15 @@ def run_gpu(args, rank, world, barrier, allmax):
     return res, Wh
 
 
+def headline_config(cfg, world):
+    """The `config` of the headline line, shared by both arms."""
+    return {"workload": WORKLOAD, "B": 1, "K": 8, "ctx": 2048, "window": cfg["window"],
+            "cycle": "draft_block_inject (K new context rows injected inside the pass) + "
+                     "select_path + accept_greedy, one CUDA graph",
+            "l2": "inputs larger than L2: 3.5 GB of weights streamed per step, no flush",
+            "parallelism": f"replicas x{world}"}
+
+
 def bench_b1(torch, dfl, cfg, Wd, pk, args, world, barrier, allmax, dev):
     """The headline: one draft cycle at B=1, K=8, context 2048 (one CUDA graph)."""
     B, K, ctx = 1, 8, [2048]
@@ -460,11 +469,7 @@ def bench_b1(torch, dfl, cfg, Wd, pk, args, world, barrier, allmax, dev):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_cycle,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) target hiddens, N(0,3) target logits)",
-        "config": {"workload": WORKLOAD, "B": B, "K": K, "ctx": ctx[0], "window": cfg["window"],
-                   "cycle": "draft_block_inject (K new context rows injected inside the pass) + "
-                            "select_path + accept_greedy, one CUDA graph",
-                   "l2": "inputs larger than L2: 3.5 GB of weights streamed per step, no flush",
-                   "parallelism": f"replicas x{world}"},
+        "config": headline_config(cfg, world),
         "draft_pass_us": ms_pass * 1e3,
         "cycle_two_calls_us": ms_two * 1e3,
         "draft_pass_bytes": pb1,
@@ -716,7 +721,8 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD, "B": 1, "K": 8, "ctx": 2048},
+            "data": "synthetic",
+            "config": headline_config(cfg, int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores(), "kind": "oracle",
                              "sample": f"each step: oracle on layer 0 + 1/5 of lm_head rows + "
                                        f"inject + select + accept = {frac:.3f} of a cycle's weights"},
