@@ -2,19 +2,22 @@
 
 Headline workload: the full-size drafter (5 layers, width 4096, vocab 151936),
 one request, block K=8, 2048 context tokens with a 1024-token window.  One
-step = one draft cycle: inject K target-hidden rows (the most accepted tokens a
-cycle can add) -> drafter pass + top-16 -> Viterbi selector -> greedy accept.
+step = one draft cycle in one CUDA graph: the drafter pass injecting K
+target-hidden rows (the most accepted tokens a cycle can add; their K/V formed
+inside the pass) + top-16 -> Viterbi selector -> greedy accept.
 value = draft cycles per second over all ranks (each GPU runs its own replica).
 
-Also reported: the draft pass alone (draft_block + select_path) at B=1 and at
-B=32 (ragged contexts in [512, 8192], paged 64-token pages), each as a
-fraction of the HBM roofline for its algorithmic bytes; the roofline of the
-dominant kernel (the tcgen05 projection GEMM) over the pass's GEMM shapes;
-an end-to-end figure through the C ABI with host buffers; and the CPU oracle
-timed on a bounded sample of the same workload.
+Also reported: the same cycle with the injection as its own call; the draft
+pass alone (draft_block + select_path) at B=1 and at B=32 (ragged contexts in
+[512, 8192], paged 64-token pages), each as a fraction of its roofline; the
+roofline of the dominant kernel (the tcgen05 projection GEMM) over the pass's
+GEMM shapes; the bulk injection of 8 x 4096 rows against the bf16 tensor
+roofline; the 4-bit drafter; an end-to-end figure through the C ABI with host
+buffers; and the CPU oracle timed on a bounded sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--only b1,b32,inject] [--no-b32] [--no-inject] [--no-cpu-baseline]
+                  [--only b1,b32,inject,q4 | inject4k | q4lm] [--no-b32] [--no-inject]
+                  [--no-cpu-baseline]
 """
 
 import argparse
