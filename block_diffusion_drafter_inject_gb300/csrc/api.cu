@@ -208,7 +208,10 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
     off += (bytes + 255) & ~(size_t)255;
     return o;
   };
-  L->P_gate = reduce_plan(c, GW, T, D, GEMM_REDUCE, sms);
+  // the conv gate linears (row path): bf16 writes K slices that the conv sums
+  // itself, so the GEMM has no reduction tail; float32 one slice
+  L->P_gate = c->dtype == DFLASH_BF16 ? gemm_plan(GW, T, D, GEMM_PARTIAL, sms, kMaxReduceSplits)
+                                     : reduce_plan(c, GW, T, D, GEMM_REDUCE, sms);
   L->P_qkv = reduce_plan(c, QKVW, T, D, c->dtype == DFLASH_BF16 ? GEMM_QKV : GEMM_REDUCE, sms);
   L->P_o = reduce_plan(c, D, T, Hq * dh, GEMM_REDUCE, sms);
   L->P_gu = reduce_plan(c, F, T, D, GEMM_SWIGLU, sms);
@@ -219,7 +222,6 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->ap = attn_plan(B, K, Hq, Hkv, dh, c->window, sms);
   // slice scratch shared by every reduce-mode GEMM (they run one after another)
   size_t sc = 0;
-  sc = std::max(sc, reduce_scratch(c, GW, T, D, L->P_gate, GEMM_REDUCE));
   sc = std::max(sc, reduce_scratch(c, QKVW, T, D, L->P_qkv,
                                     c->dtype == DFLASH_BF16 ? GEMM_QKV : GEMM_REDUCE));
   sc = std::max(sc, reduce_scratch(c, D, T, Hq * dh, L->P_o, GEMM_REDUCE));
@@ -269,7 +271,7 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->un = take((size_t)T * D * es);
   L->rf = take((size_t)T * D * 4);
   L->rb = take((size_t)T * D * es);
-  L->gates = take((size_t)T * GW * 4);
+  L->gates = take((size_t)L->P_gate.S * T * GW * 4);
   L->qkv = take((size_t)T * QKVW * 4);
   L->qb = take((size_t)T * Hq * dh * es);
   L->kb = take((size_t)T * Hkv * dh * es);
@@ -426,7 +428,16 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   float *logits = logits_opt ? logits_opt : (float *)(ws + L.logits);
   float *attnp = (float *)(ws + L.attn), *topkp = (float *)(ws + L.topk);
   const RopeTable rope = rope_table(c.rope_theta, dh);
+  // the conv gate linear of the row path -> gates: nsl_gate K slices (bf16) or
+  // the reduced rows (float32)
+  const int nsl_gate = c.dtype == DFLASH_BF16 ? L.P_gate.S : 1;
   auto gate_gemm = [&](const void *Wg, const S *X) {
+    if (c.dtype == DFLASH_BF16) {
+      GemmCall gc = reduce_call(c, ws, L, Wg, GW, D, X, T, L.P_gate, GEMM_PARTIAL, nullptr, GW,
+                                nullptr, 0);
+      gc.out = gates;
+      return gemm_run(gc, st);
+    }
     return gemm_run(
         reduce_call(c, ws, L, Wg, GW, D, X, T, L.P_gate, GEMM_REDUCE, gates, GW, nullptr, 0), st);
   };
@@ -518,7 +529,8 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
                                  (const S *)lw.conv_base[i], (const S *)gain, eps, ub, st);
     int rc = gate_gemm(lw.conv_w[i], un);
     if (rc != DFLASH_OK) return rc;
-    return launch_conv_pre<S>(un, gates, T, K, D, g, (const S *)lw.conv_base[i], ub, st);
+    return launch_conv_pre<S>(un, gates, nsl_gate, T, K, D, g, (const S *)lw.conv_base[i], ub,
+                              st);
   };
   // conv after a sublayer + residual; then the next pre-norm (row path) or,
   // after the last layer, the final norm into zf
@@ -533,8 +545,9 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     }
     rc = gate_gemm(lw.conv_w[i], rb);
     if (rc != DFLASH_OK) return rc;
-    return launch_conv_post_norm<S>(rf, gates, T, K, D, g, (const S *)lw.conv_base[i], x,
-                                    (const S *)next_gain, eps, un, last ? zf : (S *)nullptr, st);
+    return launch_conv_post_norm<S>(rf, gates, nsl_gate, T, K, D, g, (const S *)lw.conv_base[i],
+                                    x, (const S *)next_gain, eps, un, last ? zf : (S *)nullptr,
+                                    st);
   };
 
   if (N > 0) {

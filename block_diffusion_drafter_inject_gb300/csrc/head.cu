@@ -196,20 +196,28 @@ __global__ void __launch_bounds__(256) k_topk_rows(const float *__restrict__ log
   const int nt = (V + 127) / 128;
   float *sm_m = tk_sm, *sm_s = tk_sm + nt;
   const float *z = logits + (size_t)row * V;
+  constexpr int LB = 8;  // loads in flight per thread in the staging loops
   if (tid == 0) n_tiles = 0, n_cand = 0;
-  for (int i = tid; i < nt; i += blockDim.x) {
-    float m, sum;
-    if (stats) {
-      const float2 st = stats[(size_t)row * nt + i];
-      m = st.x, sum = st.y;
-    } else {
+  if (stats) {
+    const float2 *st = stats + (size_t)row * nt;
+    for (int i0 = 0; i0 < nt; i0 += LB * 256) {
+      float2 q[LB];
+#pragma unroll
+      for (int j = 0; j < LB; ++j)
+        if (i0 + j * 256 + tid < nt) q[j] = st[i0 + j * 256 + tid];
+#pragma unroll
+      for (int j = 0; j < LB; ++j)
+        if (i0 + j * 256 + tid < nt) sm_m[i0 + j * 256 + tid] = q[j].x, sm_s[i0 + j * 256 + tid] = q[j].y;
+    }
+  } else {
+    for (int i = tid; i < nt; i += blockDim.x) {
       const int e1 = min(V, 128 * i + 128);
-      m = -INFINITY, sum = 0.f;
+      float m = -INFINITY, sum = 0.f;
       for (int e = 128 * i; e < e1; ++e) m = fmaxf(m, z[e]);
       for (int e = 128 * i; e < e1; ++e) sum += expf(z[e] - m);
+      sm_m[i] = m;
+      sm_s[i] = sum;
     }
-    sm_m[i] = m;
-    sm_s[i] = sum;
   }
   __syncthreads();
   float mm = -INFINITY;
@@ -262,19 +270,24 @@ __global__ void __launch_bounds__(256) k_topk_rows(const float *__restrict__ log
   __syncthreads();
   bool direct = n_tiles <= kTopkCandTiles;
   if (direct) {
-    for (int q = w; q < n_tiles; q += 8) {
-      const int e0 = 128 * ctile[q];
+    // the candidate tiles' entries, flattened over the threads (entry f of
+    // the list is entry f % 128 of tile ctile[f / 128]), LB loads in flight
+    const int nf = n_tiles * 128;
+    for (int f0 = 0; f0 < nf; f0 += LB * 256) {
+      float x[LB];
+      int e[LB];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = e0 + 32 * j + lane;
-        if (e < V) {
-          const float x = z[e];
-          if (x >= thr) {
-            const int pos = atomicAdd(&n_cand, 1);
-            if (pos < kTopkCand) cv[pos] = x, ci[pos] = e;
-          }
-        }
+      for (int j = 0; j < LB; ++j) {
+        const int f = f0 + j * 256 + tid;
+        e[j] = f < nf ? 128 * ctile[f >> 7] + (f & 127) : V;
+        if (e[j] < V) x[j] = z[e[j]];
       }
+#pragma unroll
+      for (int j = 0; j < LB; ++j)
+        if (e[j] < V && x[j] >= thr) {
+          const int pos = atomicAdd(&n_cand, 1);
+          if (pos < kTopkCand) cv[pos] = x[j], ci[pos] = e[j];
+        }
     }
     __syncthreads();
     direct = n_cand <= kTopkCand;
@@ -401,6 +414,7 @@ __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
   __shared__ float delta[DFLASH_MAX_TOPK];
   __shared__ int bp[DFLASH_MAX_BLOCK][DFLASH_MAX_TOPK];
   __shared__ int s_last;
+  __shared__ const float *s_src[2 * DFLASH_MAX_TOPK];
   pdl_launch();
   pdl_wait();
   const int t = blockIdx.x, b = blockIdx.y;
@@ -408,9 +422,11 @@ __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
   const int np = t == 0 ? 1 : k;
   const size_t ubase = (size_t)b * R + (t == 0 ? 0 : 1 + (size_t)(t - 1) * k);
   const size_t vbase = (size_t)b * R + 1 + (size_t)t * k;
-  const int r4 = r / 4;
-  for (int e = threadIdx.x; e < (np + k) * r4; e += blockDim.x) {
-    const int row = e / r4, c = e % r4;
+  const int r4 = r / 4, nrow = np + k;
+  // the source row of every staged row first (one round trip for the tokens),
+  // then all of a thread's row loads in flight at once
+  if (threadIdx.x < nrow) {
+    const int row = threadIdx.x;
     const float *src;
     if (tab) {
       // the rows' tokens: the anchor or position t-1's candidates (P_u side),
@@ -418,16 +434,33 @@ __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
       int tok = row < np ? (t == 0 ? anchor[b] : topk_ids[((size_t)b * (K - 1) + t - 1) * k + row])
                          : topk_ids[((size_t)b * (K - 1) + t) * k + (row - np)];
       if (tok < 0 || tok >= V) {
-        if (c == 0) set_err(err, DFLASH_DEV_TOKEN_RANGE);
+        set_err(err, DFLASH_DEV_TOKEN_RANGE);
         tok = tok < 0 ? 0 : V - 1;
       }
       src = tab + ((row < np ? 0 : (size_t)V) + (size_t)tok) * r;
     } else {
       src = row < np ? U + (ubase + row) * r : Vp + (vbase + row - np) * r;
     }
-    const float4 q = ((const float4 *)src)[c];
-    float *dst = (row < np ? su + (size_t)row * LDR : sv + (size_t)(row - np) * LDR) + 4 * c;
-    dst[0] = q.x, dst[1] = q.y, dst[2] = q.z, dst[3] = q.w;
+    s_src[row] = src;
+  }
+  __syncthreads();
+  constexpr int SB = 8;  // 16-byte loads in flight per thread
+  for (int e0 = 0; e0 < nrow * r4; e0 += SB * 256) {
+    float4 q[SB];
+#pragma unroll
+    for (int j = 0; j < SB; ++j) {
+      const int e = e0 + j * 256 + threadIdx.x;
+      if (e < nrow * r4) q[j] = ((const float4 *)s_src[e / r4])[e % r4];
+    }
+#pragma unroll
+    for (int j = 0; j < SB; ++j) {
+      const int e = e0 + j * 256 + threadIdx.x;
+      if (e < nrow * r4) {
+        const int row = e / r4, c = e % r4;
+        float *dst = (row < np ? su + (size_t)row * LDR : sv + (size_t)(row - np) * LDR) + 4 * c;
+        dst[0] = q[j].x, dst[1] = q[j].y, dst[2] = q[j].z, dst[3] = q[j].w;
+      }
+    }
   }
   __syncthreads();
   float *out = pair + ((size_t)b * (K - 1) + t) * k * k;
@@ -499,19 +532,48 @@ __global__ void __launch_bounds__(256) k_sel_pairs(const float *__restrict__ U,
 }
 
 // argmax of one chunk of one target-logit row -> partial (value, id); NaN ranks
-// above every number (better_nan_max)
+// above every number (better_nan_max).  better_nan_max is a total order on
+// (value, id), so the visiting order does not change the result: a 16-byte
+// aligned row is read as 16-byte words, all of a thread's words issued before
+// the first comparison (one memory round trip per chunk), the ragged end of
+// the chunk element by element.
 template <typename L>
 __global__ void __launch_bounds__(256) k_argmax_partial(const L *__restrict__ logits, int V,
                                                         float *__restrict__ partial) {
+  constexpr int NT = 256, VW = 16 / sizeof(L), NV = dflh::kArgmaxChunk / (NT * VW);
+  static_assert(dflh::kArgmaxChunk % (NT * VW) == 0, "chunk is whole 16-byte words per thread");
   __shared__ float redv[32];
   __shared__ int redi[32];
   pdl_launch();
   pdl_wait();
-  const int chunk = blockIdx.x, row = blockIdx.y, nch = gridDim.x;
+  const int chunk = blockIdx.x, row = blockIdx.y, nch = gridDim.x, tid = threadIdx.x;
   const int c0 = chunk * dflh::kArgmaxChunk, c1 = min(V, c0 + dflh::kArgmaxChunk);
   const L *z = logits + (size_t)row * V;
   VI best{-INFINITY, 0x7fffffff};
-  for (int i = c0 + threadIdx.x; i < c1; i += blockDim.x) {
+  int tail = c0;  // first element left to the element-wise loop
+  if ((reinterpret_cast<uintptr_t>(z + c0) & 15) == 0) {
+    const int nw = (c1 - c0) / VW;  // whole words in the chunk
+    const uint4 *zw = reinterpret_cast<const uint4 *>(z + c0);
+    uint4 r[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+      if (j * NT + tid < nw) r[j] = __ldg(zw + j * NT + tid);
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const int q = j * NT + tid;
+      if (q < nw) {
+        const L *e = reinterpret_cast<const L *>(&r[j]);
+#pragma unroll
+        for (int u = 0; u < VW; ++u) {
+          const float v = ldf(e + u);
+          const int i = c0 + q * VW + u;
+          if (better_nan_max(v, i, best.v, best.i)) best.v = v, best.i = i;
+        }
+      }
+    }
+    tail = c0 + nw * VW;
+  }
+  for (int i = tail + tid; i < c1; i += NT) {
     const float v = ldf(z + i);
     if (better_nan_max(v, i, best.v, best.i)) best.v = v, best.i = i;
   }

@@ -35,6 +35,10 @@ __device__ __forceinline__ void rope_row(float2 *__restrict__ cs, int pos,
   }
 }
 
+// 8-element chunks of a row a thread keeps in registers between the two
+// passes of a row norm
+constexpr int kNormCache = 4;
+
 template <typename S>
 __global__ void __launch_bounds__(512) k_embed_norm(const S *__restrict__ E,
                                                     const int32_t *__restrict__ anchor,
@@ -51,34 +55,63 @@ __global__ void __launch_bounds__(512) k_embed_norm(const S *__restrict__ E,
   // K/V above all) has completed, and may read the caches before its own wait.
   pdl_wait();
   const int r = blockIdx.x, b = r / K, i = r % K;
-  rope_row(rope_cs + (size_t)r * half, ctx_len[b] + i, rope, half);
   int tok = i == 0 ? anchor[b] : mask_id;
   if (tok < 0 || tok >= V) {
     if (threadIdx.x == 0) set_err(err, DFLASH_DEV_TOKEN_RANGE);
     tok = tok < 0 ? 0 : V - 1;
   }
+  // the thread's first kNormCache chunks of the embedding row stay in
+  // registers for the normed output; the RoPE row is formed while they load
   const S *e = E + (size_t)tok * D;
-  float ss = 0.f;
-  for (int c = threadIdx.x * 8; c < D; c += blockDim.x * 8) {
-    float v[8];
-    load8(e + c, v);
-    store8(x + (size_t)r * D + c, v);
+  const int step = blockDim.x * 8, c0 = threadIdx.x * 8;
+  float v[kNormCache][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) ss += v[j] * v[j];
+  for (int q = 0; q < kNormCache; ++q)
+    if (c0 + q * step < D) load8(e + c0 + q * step, v[q]);
+  rope_row(rope_cs + (size_t)r * half, ctx_len[b] + i, rope, half);
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < kNormCache; ++q)
+    if (c0 + q * step < D) {
+      store8(x + (size_t)r * D + c0 + q * step, v[q]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss += v[q][j] * v[q][j];
+    }
+  for (int c = c0 + kNormCache * step; c < D; c += step) {
+    float w[8];
+    load8(e + c, w);
+    store8(x + (size_t)r * D + c, w);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += w[j] * w[j];
   }
   const float inv = rsqrtf(block_sum(ss, red) / D + eps);
   if (!un) return;
-  for (int c = threadIdx.x * 8; c < D; c += blockDim.x * 8) {
-    float v[8], g[8];
-    load8(e + c, v);
+#pragma unroll
+  for (int q = 0; q < kNormCache; ++q) {
+    const int c = c0 + q * step;
+    if (c < D) {
+      float g[8];
+      load8(gain + c, g);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[q][j] = v[q][j] * inv * g[j];
+      store8(un + (size_t)r * D + c, v[q]);
+    }
+  }
+  for (int c = c0 + kNormCache * step; c < D; c += step) {
+    float w[8], g[8];
+    load8(e + c, w);
     load8(gain + c, g);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = v[j] * inv * g[j];
-    store8(un + (size_t)r * D + c, v);
+    for (int j = 0; j < 8; ++j) w[j] = w[j] * inv * g[j];
+    store8(un + (size_t)r * D + c, w);
   }
 }
 
 // out[r] = gain * in[r] / rms(in[r]); cols % 8 == 0, 16-byte aligned rows.
+// A thread's first few 8-element chunks of the row (kNormCache, two for
+// float32 rows) are loaded at once and kept in registers for the output pass (the chunks past them, if any, are
+// read again); the RoPE row and the cache-slot lookup run while those loads
+// are in flight, the slot's page-table read after the row is written.
 template <typename S>
 __global__ void __launch_bounds__(1024) k_rows_norm(const S *__restrict__ in, int cols,
                                                     const S *__restrict__ gain, float eps,
@@ -90,59 +123,104 @@ __global__ void __launch_bounds__(1024) k_rows_norm(const S *__restrict__ in, in
   __shared__ float red[32];
   pdl_launch();
   pdl_wait();
+  const S *row = in + (size_t)blockIdx.x * cols;
+  // float32 rows: two cached chunks (64 registers a thread at 1024 threads)
+  constexpr int NC = sizeof(S) == 2 ? kNormCache : 2;
+  const int step = blockDim.x * 8, c0 = threadIdx.x * 8;
+  float v[NC][8];
+#pragma unroll
+  for (int q = 0; q < NC; ++q)
+    if (c0 + q * step < cols) load8(row + c0 + q * step, v[q]);
+  int srow = 0, spos = 0;
+  const bool slot_thread = cs.slot && threadIdx.x == 0;
+  if (slot_thread) srow = cs.req[blockIdx.x], spos = pos[blockIdx.x];
   if (rope_cs) rope_row(rope_cs + (size_t)blockIdx.x * half, pos[blockIdx.x], rope, half);
-  if (cs.slot && threadIdx.x == 0) {
-    const int row = cs.req[blockIdx.x], p = pos[blockIdx.x];
-    long long s = -1;
-    if (row < 0 || row >= cs.num_rows) {
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < NC; ++q)
+    if (c0 + q * step < cols) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss += v[q][j] * v[q][j];
+    }
+  for (int c = c0 + NC * step; c < cols; c += step) {
+    float w[8];
+    load8(row + c, w);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += w[j] * w[j];
+  }
+  const float inv = rsqrtf(block_sum(ss, red) / cols + eps);
+  S *o = out + (size_t)blockIdx.x * cols;
+#pragma unroll
+  for (int q = 0; q < NC; ++q) {
+    const int c = c0 + q * step;
+    if (c < cols) {
+      float g[8];
+      load8(gain + c, g);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[q][j] = v[q][j] * inv * g[j];
+      store8(o + c, v[q]);
+    }
+  }
+  for (int c = c0 + NC * step; c < cols; c += step) {
+    float w[8], g[8];
+    load8(row + c, w);
+    load8(gain + c, g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = w[j] * inv * g[j];
+    store8(o + c, w);
+  }
+  if (slot_thread) {
+    long long sl = -1;
+    if (srow < 0 || srow >= cs.num_rows) {
       set_err(cs.err, DFLASH_DEV_REQ_RANGE);
-    } else if (p < 0 || p / cs.P >= cs.max_pages) {
+    } else if (spos < 0 || spos / cs.P >= cs.max_pages) {
       set_err(cs.err, DFLASH_DEV_POS_RANGE);
     } else {
-      const int page = cs.table[(size_t)row * cs.max_pages + p / cs.P];
+      const int page = cs.table[(size_t)srow * cs.max_pages + spos / cs.P];
       if (page < 0 || page >= cs.num_pages)
         set_err(cs.err, DFLASH_DEV_PAGE_RANGE);
       else
-        s = ((long long)page * cs.Hkv * cs.P + p % cs.P) * cs.dh;
+        sl = ((long long)page * cs.Hkv * cs.P + spos % cs.P) * cs.dh;
     }
-    cs.slot[blockIdx.x] = s;
+    cs.slot[blockIdx.x] = sl;
   }
-  const S *row = in + (size_t)blockIdx.x * cols;
-  float ss = 0.f;
-  for (int c = threadIdx.x * 8; c < cols; c += blockDim.x * 8) {
-    float v[8];
-    load8(row + c, v);
+}
+
+// Sum of the nsl K slices p[0], p[stride], ... in slice order; the first
+// kGateSlices loads are all issued before the first add (one round trip).
+constexpr int kGateSlices = 16;
+__device__ __forceinline__ float sum_slices(const float *p, int nsl, size_t stride) {
+  float t[kGateSlices];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) ss += v[j] * v[j];
-  }
-  const float inv = rsqrtf(block_sum(ss, red) / cols + eps);
-  for (int c = threadIdx.x * 8; c < cols; c += blockDim.x * 8) {
-    float v[8], g[8];
-    load8(row + c, v);
-    load8(gain + c, g);
+  for (int q = 0; q < kGateSlices; ++q)
+    if (q < nsl) t[q] = p[(size_t)q * stride];
+  float v = t[0];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = v[j] * inv * g[j];
-    store8(out + (size_t)blockIdx.x * cols + c, v);
-  }
+  for (int q = 1; q < kGateSlices; ++q)
+    if (q < nsl) v += t[q];
+  for (int q = kGateSlices; q < nsl; ++q) v += p[(size_t)q * stride];
+  return v;
 }
 
 // Pre-sublayer conv: ub[r] = a(r) * un[r] + b(r) * un[r-1] (zero before slot 0),
 //   a_c(r) = sigmoid(base[c] + gate[r][c/g]),  b_c(r) = sigmoid(base[D+c] + gate[r][D/g + c/g])
-// gate: the conv's gate linear of row r, fp32 [rows, 2D/g].  grid (rows, D/chunk).
+// gate: the conv's gate linear of row r as nsl K slices, fp32 [nsl][rows][2D/g],
+// summed here in slice order.  grid (rows, D/chunk); dynamic shared: the
+// summed gates of the chunk's groups.
 template <typename S>
 __global__ void __launch_bounds__(256) k_conv_pre(const S *__restrict__ un,
-                                                  const float *__restrict__ gate, int K, int D,
-                                                  int group, int chunk, const S *__restrict__ base,
-                                                  S *__restrict__ ub) {
+                                                  const float *__restrict__ gate, int nsl, int K,
+                                                  int D, int group, int chunk,
+                                                  const S *__restrict__ base, S *__restrict__ ub) {
+  extern __shared__ float sg[];  // [2][ng]: the a gates, then the b gates
   pdl_launch();
   pdl_wait();
-  const int r = blockIdx.x;
+  const int r = blockIdx.x, rows = gridDim.x;
   const int c0 = blockIdx.y * chunk, c1 = min(D, c0 + chunk);
-  const float *ga = gate + (size_t)r * (2 * D / group);
-  const float *gb = ga + D / group;
+  const int GW = 2 * D / group, gl0 = c0 / group, ng = (c1 - 1) / group - gl0 + 1;
   const bool first = (r % K) == 0;
-  for (int c = c0 + threadIdx.x * 8; c < c1; c += blockDim.x * 8) {
-    float cur[8], prev[8], ba[8], bb[8], y[8];
+  float cur[8], prev[8], ba[8], bb[8];
+  auto load_at = [&](int c) {
     load8(un + (size_t)r * D + c, cur);
     if (first) {
 #pragma unroll
@@ -152,6 +230,17 @@ __global__ void __launch_bounds__(256) k_conv_pre(const S *__restrict__ un,
     }
     load8(base + c, ba);
     load8(base + D + c, bb);
+  };
+  const int cA = c0 + threadIdx.x * 8;
+  for (int i = threadIdx.x; i < 2 * ng; i += blockDim.x) {
+    const int col = i < ng ? gl0 + i : D / group + gl0 + (i - ng);
+    sg[i] = sum_slices(gate + (size_t)r * GW + col, nsl, (size_t)rows * GW);
+  }
+  __syncthreads();
+  const float *ga = sg - gl0, *gb = sg + ng - gl0;
+  for (int c = cA; c < c1; c += blockDim.x * 8) {
+    float y[8];
+    load_at(c);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int g = (c + j) / group;
@@ -167,23 +256,22 @@ __global__ void __launch_bounds__(256) k_conv_pre(const S *__restrict__ un,
 //   x[r] += a(r) * rf[r] + b(r) * rf[r-1];  un[r] = gain * x[r] / rms(x[r]).
 // With zf != nullptr (after the last layer) the normed rows of slots 1..K-1
 // are written compactly to zf[b*(K-1) + i-1] instead of un.
-// One CTA per row; dynamic shared: D floats.
+// gate: as for the pre-sublayer conv, nsl K slices [nsl][rows][2D/g].
+// One CTA per row; dynamic shared: D + 2D/g floats.
 template <typename S>
 __global__ void __launch_bounds__(512) k_conv_post_norm(
-    const float *__restrict__ rf, const float *__restrict__ gate, int K, int D, int group,
-    const S *__restrict__ base, float *__restrict__ x, const S *__restrict__ gain, float eps,
-    S *__restrict__ un, S *__restrict__ zf) {
-  extern __shared__ float xrow[];
+    const float *__restrict__ rf, const float *__restrict__ gate, int nsl, int K, int D,
+    int group, const S *__restrict__ base, float *__restrict__ x, const S *__restrict__ gain,
+    float eps, S *__restrict__ un, S *__restrict__ zf) {
+  extern __shared__ float xrow[];  // [D] the updated row, then [2D/g] the summed gates
   __shared__ float red[32];
   pdl_launch();
   pdl_wait();
-  const int r = blockIdx.x;
-  const float *ga = gate + (size_t)r * (2 * D / group);
-  const float *gb = ga + D / group;
+  const int r = blockIdx.x, rows = gridDim.x, GW = 2 * D / group;
+  float *sg = xrow + D;
   const bool first = (r % K) == 0;
-  float ss = 0.f;
-  for (int c = threadIdx.x * 8; c < D; c += blockDim.x * 8) {
-    float cur[8], prev[8], ba[8], bb[8], xv[8];
+  float cur[8], prev[8], ba[8], bb[8], xv[8];
+  auto load_at = [&](int c) {
     load8(rf + (size_t)r * D + c, cur);
     if (first) {
 #pragma unroll
@@ -194,6 +282,17 @@ __global__ void __launch_bounds__(512) k_conv_post_norm(
     load8(base + c, ba);
     load8(base + D + c, bb);
     load8(x + (size_t)r * D + c, xv);
+  };
+  // the thread's first chunk is in flight while the gates are summed
+  const int cA = threadIdx.x * 8;
+  for (int i = threadIdx.x; i < GW; i += blockDim.x) {
+    sg[i] = sum_slices(gate + (size_t)r * GW + i, nsl, (size_t)rows * GW);
+  }
+  __syncthreads();
+  const float *ga = sg, *gb = sg + D / group;
+  float ss = 0.f;
+  for (int c = cA; c < D; c += blockDim.x * 8) {
+    load_at(c);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int g = (c + j) / group;
@@ -214,7 +313,7 @@ __global__ void __launch_bounds__(512) k_conv_post_norm(
   } else {
     o = un + (size_t)r * D;
   }
-  for (int c = threadIdx.x * 8; c < D; c += blockDim.x * 8) {
+  for (int c = cA; c < D; c += blockDim.x * 8) {
     float g[8], y[8];
     load8(gain + c, g);
 #pragma unroll
@@ -737,18 +836,20 @@ int launch_rows_norm(const S *in, int rows, int cols, const S *gain, float eps, 
   return DFLASH_OK;
 }
 template <typename S>
-int launch_conv_pre(const S *un, const float *gate, int rows, int K, int D, int group,
+int launch_conv_pre(const S *un, const float *gate, int nsl, int rows, int K, int D, int group,
                     const S *base, S *ub, cudaStream_t st) {
   const int chunk = D >= 2048 ? 1024 : D;
-  DFL_CHECK_LAUNCH(launch(dfl::k_conv_pre<S>, dim3(rows, (D + chunk - 1) / chunk), dim3(128), 0,
-                          st, un, gate, K, D, group, chunk, base, ub));
+  const size_t smem = (size_t)2 * ((chunk + group - 1) / group + 1) * sizeof(float);
+  if (smem > 48 * 1024) return DFLASH_ERR_DIMS;
+  DFL_CHECK_LAUNCH(launch(dfl::k_conv_pre<S>, dim3(rows, (D + chunk - 1) / chunk), dim3(128),
+                          smem, st, un, gate, nsl, K, D, group, chunk, base, ub));
   return DFLASH_OK;
 }
 template <typename S>
-int launch_conv_post_norm(const float *rf, const float *gate, int rows, int K, int D, int group,
-                          const S *base, float *x, const S *gain, float eps, S *un, S *zf,
-                          cudaStream_t st) {
-  const size_t smem = (size_t)D * sizeof(float);
+int launch_conv_post_norm(const float *rf, const float *gate, int nsl, int rows, int K, int D,
+                          int group, const S *base, float *x, const S *gain, float eps, S *un,
+                          S *zf, cudaStream_t st) {
+  const size_t smem = (size_t)(D + 2 * D / group) * sizeof(float);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(dfl::k_conv_post_norm<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
@@ -756,7 +857,7 @@ int launch_conv_post_norm(const float *rf, const float *gate, int rows, int K, i
   }
   const int threads = D >= 4096 ? 512 : D >= 1024 ? 128 : 32;
   DFL_CHECK_LAUNCH(launch(dfl::k_conv_post_norm<S>, dim3(rows), dim3(threads), smem, st, rf, gate,
-                          K, D, group, base, x, gain, eps, un, zf));
+                          nsl, K, D, group, base, x, gain, eps, un, zf));
   return DFLASH_OK;
 }
 template <typename S>
@@ -906,9 +1007,9 @@ int launch_final_norm(const float *x, int B, int K, int D, const S *gain, float 
   template int launch_rows_norm<S>(const S *, int, int, const S *, float, S *, const int32_t *,  \
                                    const RopeTable &, int, float2 *, cudaStream_t,               \
                                    const CacheSlots &);                                          \
-  template int launch_conv_pre<S>(const S *, const float *, int, int, int, int, const S *, S *,  \
-                                  cudaStream_t);                                                 \
-  template int launch_conv_post_norm<S>(const float *, const float *, int, int, int, int,        \
+  template int launch_conv_pre<S>(const S *, const float *, int, int, int, int, int, const S *,  \
+                                  S *, cudaStream_t);                                            \
+  template int launch_conv_post_norm<S>(const float *, const float *, int, int, int, int, int,   \
                                         const S *, float *, const S *, float, S *, S *,          \
                                         cudaStream_t);                                           \
   template int launch_qkv_post<S>(const float *, int, int, int, int, int, const S *, const S *,  \

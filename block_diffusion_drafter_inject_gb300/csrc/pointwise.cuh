@@ -36,14 +36,15 @@ template <typename S>
 int launch_rows_norm(const S *in, int rows, int cols, const S *gain, float eps, S *out,
                      const int32_t *pos, const RopeTable &rope, int half, float2 *rope_cs,
                      cudaStream_t st, const CacheSlots &slots = CacheSlots());
-// gate: the conv's gate linear, fp32 [rows, 2D/group]
+// gate: the conv's gate linear as nsl K slices, fp32 [nsl][rows][2D/group],
+// summed by the conv in slice order
 template <typename S>
-int launch_conv_pre(const S *un, const float *gate, int rows, int K, int D, int group,
+int launch_conv_pre(const S *un, const float *gate, int nsl, int rows, int K, int D, int group,
                     const S *base, S *ub, cudaStream_t st);
 template <typename S>
-int launch_conv_post_norm(const float *rf, const float *gate, int rows, int K, int D, int group,
-                          const S *base, float *x, const S *gain, float eps, S *un, S *zf,
-                          cudaStream_t st);
+int launch_conv_post_norm(const float *rf, const float *gate, int nsl, int rows, int K, int D,
+                          int group, const S *base, float *x, const S *gain, float eps, S *un,
+                          S *zf, cudaStream_t st);
 // Two-tap conv with its gate linear fused, for T <= kGconvMaxT block rows
 // (one launch per conv).  PRE: ub = conv(u) with u = R(rmsnorm(x, gain)) formed
 // here from the fp32 residual x.  POST: x += conv(rf) with the gates of gin.
