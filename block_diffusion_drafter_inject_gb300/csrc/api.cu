@@ -154,7 +154,7 @@ constexpr size_t kHeaderBytes = 256 + kTicketInts * 4 + kTopkTicketInts * 4;
 struct Layout {
   size_t status, tickets, scratch;
   size_t x, un, ub, rf, rb, gates, qkv, qb, kb, vb, ob, hb, zf, logits, attn, topk, topk_tickets;
-  size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf, rope, rope_inj, selgate, slots;
+  size_t selrows, U, Vp, pairs, argmax, gn, cb, kvf, rope, rope_inj, selgate, slots, ssq;
   size_t total, sc_floats;
   GemmPlan P_gate, P_qkv, P_o, P_gu, P_down, P_sel, P_sel2, P_hgate;
   AttnPlan ap;
@@ -288,6 +288,8 @@ static bool make_layout(const dflash_config *c, int B, int K, int Nmax, Layout *
   L->pairs = take((size_t)B * (K - 1) * k * k * 4);
   L->argmax = take((size_t)T * argmax_chunks(V) * 2 * 4);
   L->selgate = take((size_t)TL * r * 4);
+  // the fused convs' row sums of squares, [slots][16]
+  L->ssq = take((size_t)std::max(1, gconv_ssq_slots(T, D, c->conv_group, c->dtype)) * 16 * 4);
   // then the ones sized by it: the QKV operand and the RoPE table hold the block
   // rows followed by up to N injected rows
   L->rope = take((size_t)(T + N) * (dh / 2) * 8);
@@ -522,11 +524,22 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   // pre-norm formed inside).  More rows: the gate linear is a tensor-core GEMM
   // and the conv a row kernel.
   const bool fused = gconv_fits(T, D, g, c.dtype);
+  // The fused path hands each row's sum of squares from the kernel that
+  // updates the residual stream (the embedding kernel, the post-sublayer conv)
+  // to the next pre-sublayer conv: ssq_n partials a row wait in ssq (0: none,
+  // the conv forms them itself).
+  const int ssq_slots = fused ? gconv_ssq_slots(T, D, g, c.dtype) : 0;
+  float *ssq = ssq_slots > 0 ? (float *)(ws + L.ssq) : nullptr;
+  int ssq_n = 0;
   auto conv_pre = [&](int l, int i, const void *gain) -> int {
     const dflash_layer_weights &lw = w.layer[l];
-    if (fused)
+    if (fused) {
+      const int n = ssq_n;
+      ssq_n = 0;
       return launch_gconv_pre<S>(x, T, K, D, g, (const S *)lw.conv_w[i],
-                                 (const S *)lw.conv_base[i], (const S *)gain, eps, ub, st);
+                                 (const S *)lw.conv_base[i], (const S *)gain, eps, ub, st,
+                                 n > 0 ? ssq : nullptr, n);
+    }
     int rc = gate_gemm(lw.conv_w[i], un);
     if (rc != DFLASH_OK) return rc;
     return launch_conv_pre<S>(un, gates, nsl_gate, T, K, D, g, (const S *)lw.conv_base[i], ub,
@@ -539,7 +552,8 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     int rc;
     if (fused) {
       rc = launch_gconv_post<S>(rf, rb, T, K, D, g, (const S *)lw.conv_w[i],
-                                (const S *)lw.conv_base[i], x, st);
+                                (const S *)lw.conv_base[i], x, st, ssq);
+      ssq_n = ssq ? ssq_slots : 0;
       if (rc != DFLASH_OK || !last) return rc;
       return launch_final_norm<S>(x, B, K, D, (const S *)next_gain, eps, zf, st);
     }
@@ -566,7 +580,8 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
   }
   TRY(launch_embed_norm<S>((const S *)w.embed, anchor, c.mask_token_id, V, B, K, D,
                            (const S *)w.layer[0].attn_norm, eps, x, fused ? (S *)nullptr : un, err,
-                           ctx_len, rope, dh / 2, rope_cs, st));
+                           ctx_len, rope, dh / 2, rope_cs, st, ssq));
+  ssq_n = ssq ? 1 : 0;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights &lw = w.layer[l];
     const bool last = l + 1 == c.n_layers;

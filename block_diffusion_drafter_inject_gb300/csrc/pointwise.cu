@@ -47,7 +47,8 @@ __global__ void __launch_bounds__(512) k_embed_norm(const S *__restrict__ E,
                                                     float *__restrict__ x, S *__restrict__ un,
                                                     int *err, const int32_t *__restrict__ ctx_len,
                                                     const dflh::RopeTable rope, int half,
-                                                    float2 *__restrict__ rope_cs) {
+                                                    float2 *__restrict__ rope_cs,
+                                                    float *__restrict__ ssq_out) {
   __shared__ float red[32];
   // The first kernel of a draft pass releases its dependents only when it
   // completes (no early trigger): every later kernel of the pass therefore
@@ -84,7 +85,9 @@ __global__ void __launch_bounds__(512) k_embed_norm(const S *__restrict__ E,
 #pragma unroll
     for (int j = 0; j < 8; ++j) ss += w[j] * w[j];
   }
-  const float inv = rsqrtf(block_sum(ss, red) / D + eps);
+  const float tot = block_sum(ss, red);
+  if (ssq_out && threadIdx.x == 0) ssq_out[r] = tot;  // the row's sum of squares (slot 0)
+  const float inv = rsqrtf(tot / D + eps);
   if (!un) return;
 #pragma unroll
   for (int q = 0; q < kNormCache; ++q) {
@@ -474,6 +477,12 @@ struct GconvArgs {
   S *ub;             // PRE: conv output [T, D]
   const S *gin;      // POST: gate input R(r) [T, D]
   const float *rf;   // POST: conv input r [T, D]
+  // bf16 (cluster kernel): POST writes, per CTA, the sums of squares of the
+  // updated rows over its channels to ssq_out[cta][16]; PRE with ssq_in sums
+  // the n_ssq partials of each row in slot order instead of forming them
+  float *ssq_out;
+  const float *ssq_in;
+  int n_ssq;
 };
 
 // grid (2D/g / (2*NG)), block 256; dynamic shared: (R2 + PRE) * D elements of S.
@@ -588,6 +597,19 @@ __global__ void __launch_bounds__(256) k_gconv(const GconvArgs<S> A) {
   }
 }
 
+// 8 floats (16-byte aligned) whose loads are issued here, ahead of later
+// memory operations (the compiler may not sink them to their first use)
+__device__ __forceinline__ void load8_ordered(const float *p, float *v) {
+  asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+               : "l"(p)
+               : "memory");
+  asm volatile("ld.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+               : "l"(p + 4)
+               : "memory");
+}
+
 // bf16 storage: the same op on tensor cores, one thread-block cluster of C
 // CTAs per NGc (<= 8) channel groups.  CTA rank q takes the channel slice
 // [q*D/C, (q+1)*D/C) of the gate products: it stages its slice of the
@@ -650,7 +672,7 @@ __global__ void __launch_bounds__(256) k_gconv_cl(const GconvArgs<bf16> A, int N
     for (int j = 0; j < MAXI; ++j) {
       const int t = t0 + j * tstep;
       if (t < T) {
-        load8(A.x + (size_t)t * D + d0 + 8 * v, xv[j]);
+        load8_ordered(A.x + (size_t)t * D + d0 + 8 * v, xv[j]);
       } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) xv[j][k] = 0.f;
@@ -662,6 +684,17 @@ __global__ void __launch_bounds__(256) k_gconv_cl(const GconvArgs<bf16> A, int N
 #pragma unroll
       for (int k = 0; k < 8; ++k) ss[j] += xv[j][k] * xv[j][k];
     }
+    if (A.ssq_in) {
+      // the rows' sums of squares from the partials written with x: warp w
+      // sums rows w, w + 8 (each lane its slots in order, then a fixed tree)
+      for (int t = warp; t < T; t += 8) {
+        float a = 0.f;
+        for (int i = lane; i < A.n_ssq; i += 32) a += A.ssq_in[(size_t)i * 16 + t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0) s_inv[t] = rsqrtf(a / D + A.eps);
+      }
+    } else {
     // sum over the lanes that hold the same row (aligned groups of min(nvs, 32))
     const int span = nvs < 32 ? nvs : 32;
     for (int o = span >> 1; o > 0; o >>= 1)
@@ -684,6 +717,7 @@ __global__ void __launch_bounds__(256) k_gconv_cl(const GconvArgs<bf16> A, int N
       float a = 0.f;
       for (int r = 0; r < C; ++r) a += ld_dsmem(smem_u32(&s_ssq[tid]), (uint32_t)r);
       s_inv[tid] = rsqrtf(a / D + A.eps);
+    }
     }
     cp_async_wait<0>();  // the gain slice
     __syncthreads();
@@ -751,6 +785,9 @@ __global__ void __launch_bounds__(256) k_gconv_cl(const GconvArgs<bf16> A, int N
     for (int r = 0; r < C; ++r) a += ld_dsmem(smem_u32(&s_part[tid]), (uint32_t)r);
     s_tot[tid] = a;
   }
+  // this CTA is done reading its peers' shared memory; it waits for theirs
+  // reads of its own only before it exits
+  cluster_arrive_relaxed();
   __syncthreads();
 
   // the conv on this CTA's channels
@@ -769,10 +806,20 @@ __global__ void __launch_bounds__(256) k_gconv_cl(const GconvArgs<bf16> A, int N
       stf(A.ub + o, a * cur + b * prev);
     } else {
       const float cur = A.rf[o], prev = first ? 0.f : A.rf[o - D];
-      A.xo[o] = A.x[o] + (a * cur + b * prev);
+      const float xn = A.x[o] + (a * cur + b * prev);
+      A.xo[o] = xn;
+      if (A.ssq_out) (&red[0][0])[e] = xn * xn;  // free since s_part was formed; T * W <= 2048
     }
   }
-  cluster_sync();  // the peers have read s_part (and s_ssq) before this CTA exits
+  if (!PRE && A.ssq_out) {
+    __syncthreads();
+    if (tid < T) {
+      float a = 0.f;
+      for (int j = 0; j < W; ++j) a += (&red[0][0])[tid * W + j];
+      A.ssq_out[(size_t)blockIdx.x * 16 + tid] = a;
+    }
+  }
+  cluster_wait();  // the peers have read s_part (and s_ssq) before this CTA exits
 }
 
 // zf[b*(K-1) + i-1] = gain * x[b*K + i] / rms(x[b*K + i]) for slots i >= 1.
@@ -819,10 +866,11 @@ RopeTable rope_table(float theta, int head_dim) {
 template <typename S>
 int launch_embed_norm(const S *E, const int32_t *anchor, int mask_id, int V, int B, int K, int D,
                       const S *gain, float eps, float *x, S *un, int *err, const int32_t *ctx_len,
-                      const RopeTable &rope, int half, float2 *rope_cs, cudaStream_t st) {
+                      const RopeTable &rope, int half, float2 *rope_cs, cudaStream_t st,
+                      float *ssq_out) {
   DFL_CHECK_LAUNCH(launch(dfl::k_embed_norm<S>, dim3(B * K), dim3(D >= 4096 ? 512 : 128), 0, st, E,
                           anchor, mask_id, V, K, D, gain, eps, x, un, err, ctx_len, rope, half,
-                          rope_cs));
+                          rope_cs, ssq_out));
   return DFLASH_OK;
 }
 template <typename S>
@@ -968,6 +1016,16 @@ static int launch_gconv(bool pre, const dfl::GconvArgs<S> &a, cudaStream_t st) {
   }
 }
 
+int gconv_ssq_slots(int T, int D, int group, int dtype) {
+  int C, ngc;
+  if (dtype != DFLASH_BF16 || !gconv_fits(T, D, group, dtype) ||
+      !gconv_cluster_shape(D, group, &C, &ngc))
+    return 0;
+  const int W = ngc * group / C;  // channels of one CTA
+  if ((size_t)T * W > 2048) return 0;
+  return (D / group / ngc) * C;
+}
+
 bool gconv_fits(int T, int D, int group, int dtype) {
   if (T < 1 || T > kGconvMaxT) return false;
   int C, ngc;
@@ -977,18 +1035,22 @@ bool gconv_fits(int T, int D, int group, int dtype) {
 
 template <typename S>
 int launch_gconv_pre(const float *x, int T, int K, int D, int group, const S *G, const S *base,
-                     const S *gain, float eps, S *ub, cudaStream_t st) {
+                     const S *gain, float eps, S *ub, cudaStream_t st, const float *ssq_in,
+                     int n_ssq) {
   dfl::GconvArgs<S> a = {};
   a.T = T, a.K = K, a.D = D, a.group = group, a.G = G, a.base = base;
   a.x = x, a.gain = gain, a.eps = eps, a.ub = ub;
+  if (ssq_in && n_ssq > 0) a.ssq_in = ssq_in, a.n_ssq = n_ssq;
   return launch_gconv<S>(true, a, st);
 }
 template <typename S>
 int launch_gconv_post(const float *rf, const S *gin, int T, int K, int D, int group, const S *G,
-                      const S *base, float *x, cudaStream_t st) {
+                      const S *base, float *x, cudaStream_t st, float *ssq_out) {
   dfl::GconvArgs<S> a = {};
   a.T = T, a.K = K, a.D = D, a.group = group, a.G = G, a.base = base;
   a.x = x, a.xo = x, a.gin = gin, a.rf = rf;
+  if (ssq_out && gconv_ssq_slots(T, D, group, sizeof(S) == 2 ? DFLASH_BF16 : DFLASH_F32) > 0)
+    a.ssq_out = ssq_out;
   return launch_gconv<S>(false, a, st);
 }
 template <typename S>
@@ -1003,7 +1065,7 @@ int launch_final_norm(const float *x, int B, int K, int D, const S *gain, float 
 #define DFL_INST(S)                                                                              \
   template int launch_embed_norm<S>(const S *, const int32_t *, int, int, int, int, int, const S *, \
                                     float, float *, S *, int *, const int32_t *,                 \
-                                    const RopeTable &, int, float2 *, cudaStream_t);             \
+                                    const RopeTable &, int, float2 *, cudaStream_t, float *);    \
   template int launch_rows_norm<S>(const S *, int, int, const S *, float, S *, const int32_t *,  \
                                    const RopeTable &, int, float2 *, cudaStream_t,               \
                                    const CacheSlots &);                                          \
@@ -1019,9 +1081,9 @@ int launch_final_norm(const float *x, int B, int K, int D, const S *gain, float 
                                       int, int, int, const float2 *, float, S *, S *, int *,     \
                                       cudaStream_t);                                             \
   template int launch_gconv_pre<S>(const float *, int, int, int, int, const S *, const S *,      \
-                                   const S *, float, S *, cudaStream_t);                         \
+                                   const S *, float, S *, cudaStream_t, const float *, int);     \
   template int launch_gconv_post<S>(const float *, const S *, int, int, int, int, const S *,     \
-                                    const S *, float *, cudaStream_t);                           \
+                                    const S *, float *, cudaStream_t, float *);                  \
   template int launch_final_norm<S>(const float *, int, int, int, const S *, float, S *,         \
                                     cudaStream_t);
 DFL_INST(float)
