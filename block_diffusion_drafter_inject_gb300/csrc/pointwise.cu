@@ -597,6 +597,12 @@ __global__ void __launch_bounds__(256) k_gconv(const GconvArgs<S> A) {
   }
 }
 
+// A float whose load is issued here, ahead of later memory operations
+__device__ __forceinline__ float ld_ordered(const float *p) {
+  float v;
+  asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
 // 8 floats (16-byte aligned) whose loads are issued here, ahead of later
 // memory operations (the compiler may not sink them to their first use)
 __device__ __forceinline__ void load8_ordered(const float *p, float *v) {
@@ -652,7 +658,28 @@ __global__ void __launch_bounds__(256) k_gconv_cl(const GconvArgs<bf16> A, int N
   if (PRE)
     for (int v = tid; v < nvs; v += 256) cp_async16(smem_u32(sGain + 8 * v), A.gain + d0 + 8 * v, 16);
   cp_async_commit();
+  // the conv applies to W channels of the cluster's groups from cb on; this
+  // thread's first element (e = tid): its weights before the wait, its
+  // activations right after it, in flight with the staging loads
+  const int W = NGc * A.group / C;
+  const int cb = j0 * A.group + q * W;
+  const bool pe = tid < T * W;
+  const int pt = pe ? tid / W : 0, pch = cb + (pe ? tid % W : 0);
+  const bool pfirst = (pt % A.K) == 0;
+  const size_t po = (size_t)pt * D + pch;
+  float pba = 0.f, pbb = 0.f, pg = 0.f, pc = 0.f, pp = 0.f, px = 0.f;
+  if (pe) {
+    pba = ldf(A.base + pch);
+    pbb = ldf(A.base + D + pch);
+    if (PRE) pg = ldf(A.gain + pch);
+  }
   pdl_wait();
+  if (pe) {
+    const float *src = PRE ? A.x : A.rf;
+    pc = ld_ordered(src + po);
+    if (!pfirst) pp = ld_ordered(src + po - D);
+    if (!PRE) px = ld_ordered(A.x + po);
+  }
 
   if (!PRE) {
     for (int e = tid; e < 16 * nvs; e += 256) {
@@ -790,23 +817,23 @@ __global__ void __launch_bounds__(256) k_gconv_cl(const GconvArgs<bf16> A, int N
   cluster_arrive_relaxed();
   __syncthreads();
 
-  // the conv on this CTA's channels
-  const int W = NGc * A.group / C;
-  const int cb = j0 * A.group + q * W;
+  // the conv on this CTA's channels (the first element's operands prefetched)
   for (int e = tid; e < T * W; e += 256) {
+    const bool f0 = e == tid;
     const int t = e / W, ch = cb + e % W, gl = ch / A.group - j0;
-    const float a = sigmoidf_(ldf(A.base + ch) + s_tot[t * 16 + gl]);
-    const float b = sigmoidf_(ldf(A.base + D + ch) + s_tot[t * 16 + NGc + gl]);
+    const float a = sigmoidf_((f0 ? pba : ldf(A.base + ch)) + s_tot[t * 16 + gl]);
+    const float b = sigmoidf_((f0 ? pbb : ldf(A.base + D + ch)) + s_tot[t * 16 + NGc + gl]);
     const bool first = (t % A.K) == 0;
     const size_t o = (size_t)t * D + ch;
     if (PRE) {
-      const float g = ldf(A.gain + ch);
-      const float cur = rnd(A.x[o] * s_inv[t] * g, (const bf16 *)nullptr);
-      const float prev = first ? 0.f : rnd(A.x[o - D] * s_inv[t - 1] * g, (const bf16 *)nullptr);
+      const float g = f0 ? pg : ldf(A.gain + ch);
+      const float xc = f0 ? pc : A.x[o], xp = first ? 0.f : (f0 ? pp : A.x[o - D]);
+      const float cur = rnd(xc * s_inv[t] * g, (const bf16 *)nullptr);
+      const float prev = first ? 0.f : rnd(xp * s_inv[t - 1] * g, (const bf16 *)nullptr);
       stf(A.ub + o, a * cur + b * prev);
     } else {
-      const float cur = A.rf[o], prev = first ? 0.f : A.rf[o - D];
-      const float xn = A.x[o] + (a * cur + b * prev);
+      const float cur = f0 ? pc : A.rf[o], prev = first ? 0.f : (f0 ? pp : A.rf[o - D]);
+      const float xn = (f0 ? px : A.x[o]) + (a * cur + b * prev);
       A.xo[o] = xn;
       if (A.ssq_out) (&red[0][0])[e] = xn * xn;  // free since s_part was formed; T * W <= 2048
     }
