@@ -688,18 +688,19 @@ __global__ void __launch_bounds__(128)
   const float *rv = (const float *)pRecv;
   // weights of the splits of each owned row: w_q = e^(m_q - M) / sum_q e^(m_q - M) l_q
   float *wts = (float *)(pRecv + (size_t)A.nsplit * per * RS * 4);  // [per][nsplit]
-  for (int lr = tid; lr < r1 - r0; lr += 128) {
-    float M = -INFINITY;
-    for (int q = 0; q < A.nsplit; ++q) M = fmaxf(M, rv[(q * per + lr) * RS]);
-    float L = 0.f;
-    for (int q = 0; q < A.nsplit; ++q) {
-      const float m = rv[(q * per + lr) * RS];
-      const float w = m == -INFINITY ? 0.f : expf(m - M);
-      wts[lr * A.nsplit + q] = w;
-      L += w * rv[(q * per + lr) * RS + 1];
-    }
-    const float il = 1.f / L;
-    for (int q = 0; q < A.nsplit; ++q) wts[lr * A.nsplit + q] *= il;
+  // one warp per owned row, lane q on split q (at most 16 splits); M and L
+  // over the lanes by a fixed shuffle tree
+  for (int lr = warp; lr < r1 - r0; lr += 4) {
+    const bool has = lane < A.nsplit;
+    const float m = has ? rv[(lane * per + lr) * RS] : -INFINITY;
+    float M = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = m == -INFINITY ? 0.f : expf(m - M);
+    float L = has ? w * rv[(lane * per + lr) * RS + 1] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (has) wts[lr * A.nsplit + lane] = w * (1.f / L);
   }
   __syncthreads();
   for (int e = tid; e < (r1 - r0) * DH; e += 128) {

@@ -112,7 +112,10 @@ struct GemmShape {
   // MMA issuer's barrier wait, fence and commit are paid once per KPS k-blocks
   static constexpr int KPS = BN <= 128 ? 2 : 1;
   static constexpr int STAGE_BYTES = KPS * KB_BYTES;
-  static constexpr int STAGES = (232448 - 18 * 1024 - 1024 - 256) / STAGE_BYTES;
+  // static shared memory of the epilogue: 18 KB, 27 KB with the staged RoPE rows
+  // of a 16-token tile
+  static constexpr int STATIC_BYTES = (BN <= 16 ? 27 : 18) * 1024;
+  static constexpr int STAGES = (232448 - STATIC_BYTES - 1024 - 256) / STAGE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(STAGES >= 3 && 2 * STAGES + 6 <= 256 / 8 - 1, "ring and barriers");
@@ -206,8 +209,12 @@ __device__ __forceinline__ void load_w(uint8_t *dst, const WMaps &maps, uint64_t
 // Final values v[16] of row `row` (0..127) of tile m_tile, columns c0..c0+15.
 // The four warps of epilogue group eg call this in step (SwiGLU and the head
 // norm exchange through the group's xbuf [128][17] and xss [4][16]).
+// srope / sslot (GEMM_QKV, 16-token tiles): the chunk's RoPE rows [16][dh/2]
+// and cache slots [16] staged in shared memory, else nullptr (read from global).
 __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int row, int c0,
-                                          float *v, float *xbuf, float *xss, int eg) {
+                                          float *v, float *xbuf, float *xss, int eg,
+                                          const float2 *srope = nullptr,
+                                          const long long *sslot = nullptr) {
   if (p.mode == 3) {
     // row n of the QKV projection: head h = n / dh, feature d = n % dh; a tile
     // holds 128 / dh whole heads.  q and k heads: y = RMSNorm(x) * gain, then
@@ -233,7 +240,9 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
       float2 cs[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        cs[j] = c0 + j < p.T ? __ldg(&p.rope_cs[(size_t)(c0 + j) * half + di]) : make_float2(1.f, 0.f);
+        cs[j] = c0 + j >= p.T ? make_float2(1.f, 0.f)
+                : srope      ? srope[j * half + di]
+                             : __ldg(&p.rope_cs[(size_t)(c0 + j) * half + di]);
       // the head's sum of squares per token: nw = 2 or 4 warp partials
       const float *s0 = xss + w0 * 16;
       float o[16];
@@ -258,7 +267,7 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
           if (t < p.T0) {
             p.out_bf16[(size_t)t * p.ldb + n] = __float2bfloat16_rn(o[j]);
           } else if (t < p.T && !is_q) {
-            const long long s = __ldg(p.ctx_slot + (t - p.T0));
+            const long long s = sslot ? sslot[j] : __ldg(p.ctx_slot + (t - p.T0));
             if (s >= 0) p.kc[s + hoff] = __float2bfloat16_rn(o[j]);
           }
         }
@@ -271,7 +280,7 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
         if (t < p.T0) {
           p.out_bf16[(size_t)t * p.ldb + n] = __float2bfloat16_rn(v[j]);
         } else if (t < p.T) {
-          const long long s = __ldg(p.ctx_slot + (t - p.T0));
+          const long long s = sslot ? sslot[j] : __ldg(p.ctx_slot + (t - p.T0));
           if (s >= 0) p.vc[s + hoff] = __float2bfloat16_rn(v[j]);
         }
       }
@@ -349,6 +358,16 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
   __shared__ float xbuf[NEG][128 * 17];
   __shared__ float xss[NEG][4 * 16];
   __shared__ int s_last;
+  // GEMM_QKV with 16-token tiles: the tile's RoPE rows and cache slots are
+  // staged in shared memory while its MMAs run (the epilogue reads them
+  // without a trip to global memory)
+  constexpr bool kStage = BN <= 16;
+  __shared__ float2 s_rope[kStage ? 16 * 64 : 1];
+  __shared__ long long s_slot[kStage ? 16 : 1];
+  const bool stage_rope = kStage && p.mode == 3 && p.dh <= 128;
+  const float2 *srope = stage_rope ? s_rope : nullptr;
+  const long long *sslot = stage_rope && p.ctx_slot ? s_slot : nullptr;
+  int staged = -1;
   const int quarter = warp & 3;  // tensor-memory lanes this warp may read
   const int eg = (warp - 2) >> 2;
   const int row = quarter * 32 + lane;
@@ -358,6 +377,20 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
   Seg sg;
   for (int i = 0; get_seg(p, i, sg); ++i) {
     const int m_tile = sg.m_tile, t_tile = sg.t_tile, split = sg.seg;
+    if (stage_rope && t_tile != staged) {
+      epi_all_bar<NEG>();  // the previous tile's rows are no longer read
+      const int et = threadIdx.x - 64, half = p.dh >> 1, tb = t_tile * BN;
+      for (int i = et; i < 16 * half; i += 128 * NEG) {
+        const int tok = tb + i / half;
+        s_rope[i] = tok < p.T ? __ldg(&p.rope_cs[(size_t)tok * half + i % half]) : make_float2(1.f, 0.f);
+      }
+      if (p.ctx_slot && et < 16) {
+        const int tok = tb + et;
+        s_slot[et] = tok >= p.T0 && tok < p.T ? __ldg(p.ctx_slot + (tok - p.T0)) : -1;
+      }
+      epi_all_bar<NEG>();
+      staged = t_tile;
+    }
     if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.wait_ns)) break;
     tc_fence_after();
     const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
@@ -382,7 +415,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
         if (tcol0 + c >= p.T) break;  // uniform across the group
         float v[16];
         tc_ld16(taddr + c, v);
-        epi_store(p, m_tile, row, tcol0 + c, v, gx, gs, eg);
+        epi_store(p, m_tile, row, tcol0 + c, v, gx, gs, eg, srope, sslot);
       }
     } else {
       // slice -> scratch slot (tile, slice) ([column][row] inside: every
@@ -442,7 +475,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
           for (int k = 0; k < CPI; ++k) {
             const int cc = c + 16 * NEG * k;
             if (cc < BN && tcol0 + cc < p.T)  // uniform across the group
-              epi_store(p, m_tile, row, tcol0 + cc, v[k], gx, gs, eg);
+              epi_store(p, m_tile, row, tcol0 + cc, v[k], gx, gs, eg, srope, sslot);
           }
         }
       }
