@@ -209,12 +209,14 @@ __device__ __forceinline__ void load_w(uint8_t *dst, const WMaps &maps, uint64_t
 // Final values v[16] of row `row` (0..127) of tile m_tile, columns c0..c0+15.
 // The four warps of epilogue group eg call this in step (SwiGLU and the head
 // norm exchange through the group's xbuf [128][17] and xss [4][16]).
-// srope / sslot (GEMM_QKV, 16-token tiles): the chunk's RoPE rows [16][dh/2]
-// and cache slots [16] staged in shared memory, else nullptr (read from global).
+// srope / sslot / sgain (GEMM_QKV, 16-token tiles): the chunk's RoPE rows
+// [16][dh/2], cache slots [16] and the q / k norm gains [2][dh] staged in shared
+// memory, else nullptr (read from global).
 __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int row, int c0,
                                           float *v, float *xbuf, float *xss, int eg,
                                           const float2 *srope = nullptr,
-                                          const long long *sslot = nullptr) {
+                                          const long long *sslot = nullptr,
+                                          const float *sgain = nullptr) {
   if (p.mode == 3) {
     // row n of the QKV projection: head h = n / dh, feature d = n % dh; a tile
     // holds 128 / dh whole heads.  q and k heads: y = RMSNorm(x) * gain, then
@@ -235,7 +237,9 @@ __device__ __forceinline__ void epi_store(const GemmParams &p, int m_tile, int r
       const bf16 *gain = is_q ? p.q_norm : p.k_norm;
       const int w0 = (row - d) >> 5, nw = dh >> 5;  // the head's warps
       const int pr = d < half ? row + half : row - half, di = d < half ? d : d - half;
-      const float g = __bfloat162float(gain[d]), gp = __bfloat162float(gain[d < half ? d + half : d - half]);
+      const int dp = d < half ? d + half : d - half;
+      const float g = sgain ? sgain[(is_q ? 0 : dh) + d] : __bfloat162float(gain[d]);
+      const float gp = sgain ? sgain[(is_q ? 0 : dh) + dp] : __bfloat162float(gain[dp]);
       // every load of the chunk before its first store (stores may alias the table)
       float2 cs[16];
 #pragma unroll
@@ -364,9 +368,14 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
   constexpr bool kStage = BN <= 16;
   __shared__ float2 s_rope[kStage ? 16 * 64 : 1];
   __shared__ long long s_slot[kStage ? 16 : 1];
+  __shared__ float s_gain[kStage ? 2 * 128 : 1];  // q then k norm gains
   const bool stage_rope = kStage && p.mode == 3 && p.dh <= 128;
   const float2 *srope = stage_rope ? s_rope : nullptr;
   const long long *sslot = stage_rope && p.ctx_slot ? s_slot : nullptr;
+  const float *sgain = stage_rope ? s_gain : nullptr;
+  if (stage_rope)
+    for (int i = threadIdx.x - 64; i < 2 * p.dh; i += 128 * NEG)
+      s_gain[i] = __bfloat162float(i < p.dh ? p.q_norm[i] : p.k_norm[i - p.dh]);
   int staged = -1;
   const int quarter = warp & 3;  // tensor-memory lanes this warp may read
   const int eg = (warp - 2) >> 2;
@@ -415,7 +424,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
         if (tcol0 + c >= p.T) break;  // uniform across the group
         float v[16];
         tc_ld16(taddr + c, v);
-        epi_store(p, m_tile, row, tcol0 + c, v, gx, gs, eg, srope, sslot);
+        epi_store(p, m_tile, row, tcol0 + c, v, gx, gs, eg, srope, sslot, sgain);
       }
     } else {
       // slice -> scratch slot (tile, slice) ([column][row] inside: every
@@ -475,7 +484,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
           for (int k = 0; k < CPI; ++k) {
             const int cc = c + 16 * NEG * k;
             if (cc < BN && tcol0 + cc < p.T)  // uniform across the group
-              epi_store(p, m_tile, row, tcol0 + cc, v[k], gx, gs, eg, srope, sslot);
+              epi_store(p, m_tile, row, tcol0 + cc, v[k], gx, gs, eg, srope, sslot, sgain);
           }
         }
       }
