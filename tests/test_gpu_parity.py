@@ -39,6 +39,9 @@ CASES = [
     ("tiny_bf16", 1, 8, [64], {"conv_group": 1}),
     ("tiny_bf16", 3, 8, [5, 90, 64], {"conv_group": 1}),
     ("tiny", 1, 8, [64], {"conv_group": 1}),
+    # 256 channels a conv CTA at 16 rows: the post conv writes no sums of squares and
+    # the pre conv forms its own through the cluster
+    ("small_gqa", 2, 8, [200, 129], {"conv_group": 128}),
 ]
 
 
@@ -272,6 +275,40 @@ def test_accept_nan_rows(dtype, noalloc):
     np.testing.assert_array_equal(acc.cpu().numpy(), want_acc)
     np.testing.assert_array_equal(tok.cpu().numpy(), want_tok)
     assert list(want_tok[0][:2]) == [12345, 0] and want_tok[1][0] == 9000
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [20001, 8199, 8192])
+def test_accept_unaligned_rows_and_ties(dtype, V):
+    """Acceptance's argmax on rows that are not 16-byte aligned (V not a multiple
+    of the 16-byte word: those rows take the element-wise path) and on a ragged
+    last chunk, with ties (the lower id wins) and a NaN (it wins), against the
+    oracle's rule."""
+    import block_diffusion_drafter_inject_gb300 as dfl
+    B, K = 2, 5
+    g = np.random.default_rng(V)
+    T = g.standard_normal((B, K, V)).astype(np.float32)
+    T[0, 0, [17, V - 1]] = 9.0               # tie across chunks: id 17
+    T[0, 1, [V - 2, V - 1]] = 9.0            # tie inside the ragged tail: V - 2
+    T[1, 0, 8191] = 9.0                      # last element of the first chunk
+    T[1, 0, 8192 % V] = 9.0                  # ... tied with the next chunk's first (or itself)
+    T[1, 3, V // 2] = np.nan
+    tt = torch.from_numpy(T).cuda()
+    if dtype == "bf16":
+        tt = tt.to(torch.bfloat16)
+        T = tt.float().cpu().numpy()
+    path = np.stack([[int(np.argmax(T[b, i])) for i in range(K - 1)] for b in range(B)])
+    path[1, 2] = (path[1, 2] + 1) % V        # request 1 stops at its third draft
+    want_acc, want_tok = oracle.accept_greedy(path.astype(np.int32), T)
+    acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+    tok = torch.zeros((B, K), dtype=torch.int32, device="cuda")
+    cfg = synth.preset("tiny_bf16")
+    dfl.accept_greedy(torch.from_numpy(path.astype(np.int32)).cuda(), tt,
+                      dfl.Workspace(cfg, B, K, 1), acc, tok)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(acc.cpu().numpy(), want_acc)
+    np.testing.assert_array_equal(tok.cpu().numpy(), want_tok)
+    assert want_tok[0][0] == 17 and want_acc[1] == 3
 
 
 @pytest.mark.parametrize("name,ctx,tail", [
