@@ -362,9 +362,9 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
   __shared__ float xbuf[NEG][128 * 17];
   __shared__ float xss[NEG][4 * 16];
   __shared__ int s_last;
-  // GEMM_QKV with 16-token tiles: the tile's RoPE rows and cache slots are
-  // staged in shared memory while its MMAs run (the epilogue reads them
-  // without a trip to global memory)
+  // GEMM_QKV with 16-token tiles: the tile's RoPE rows and cache slots (and,
+  // once, the head-norm gains) are staged in shared memory while its MMAs run
+  // (the epilogue reads them without a trip to global memory)
   constexpr bool kStage = BN <= 16;
   __shared__ float2 s_rope[kStage ? 16 * 64 : 1];
   __shared__ long long s_slot[kStage ? 16 : 1];
@@ -391,7 +391,8 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams &p, uint32_t tmem
       const int et = threadIdx.x - 64, half = p.dh >> 1, tb = t_tile * BN;
       for (int i = et; i < 16 * half; i += 128 * NEG) {
         const int tok = tb + i / half;
-        s_rope[i] = tok < p.T ? __ldg(&p.rope_cs[(size_t)tok * half + i % half]) : make_float2(1.f, 0.f);
+        s_rope[i] =
+            tok < p.T ? __ldg(&p.rope_cs[(size_t)tok * half + i % half]) : make_float2(1.f, 0.f);
       }
       if (p.ctx_slot && et < 16) {
         const int tok = tb + et;

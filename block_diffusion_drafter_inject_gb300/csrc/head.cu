@@ -207,7 +207,10 @@ __global__ void __launch_bounds__(256) k_topk_rows(const float *__restrict__ log
         if (i0 + j * 256 + tid < nt) q[j] = st[i0 + j * 256 + tid];
 #pragma unroll
       for (int j = 0; j < LB; ++j)
-        if (i0 + j * 256 + tid < nt) sm_m[i0 + j * 256 + tid] = q[j].x, sm_s[i0 + j * 256 + tid] = q[j].y;
+        if (i0 + j * 256 + tid < nt) {
+          sm_m[i0 + j * 256 + tid] = q[j].x;
+          sm_s[i0 + j * 256 + tid] = q[j].y;
+        }
     }
   } else {
     for (int i = tid; i < nt; i += blockDim.x) {

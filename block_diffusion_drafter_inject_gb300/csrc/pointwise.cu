@@ -112,9 +112,10 @@ __global__ void __launch_bounds__(512) k_embed_norm(const S *__restrict__ E,
 
 // out[r] = gain * in[r] / rms(in[r]); cols % 8 == 0, 16-byte aligned rows.
 // A thread's first few 8-element chunks of the row (kNormCache, two for
-// float32 rows) are loaded at once and kept in registers for the output pass (the chunks past them, if any, are
-// read again); the RoPE row and the cache-slot lookup run while those loads
-// are in flight, the slot's page-table read after the row is written.
+// float32 rows) are loaded at once and kept in registers for the output pass
+// (the chunks past them, if any, are read again); the RoPE row and the
+// cache-slot lookup run while those loads are in flight, the slot's page-table
+// read after the row is written.
 template <typename S>
 __global__ void __launch_bounds__(1024) k_rows_norm(const S *__restrict__ in, int cols,
                                                     const S *__restrict__ gain, float eps,
@@ -286,7 +287,6 @@ __global__ void __launch_bounds__(512) k_conv_post_norm(
     load8(base + D + c, bb);
     load8(x + (size_t)r * D + c, xv);
   };
-  // the thread's first chunk is in flight while the gates are summed
   const int cA = threadIdx.x * 8;
   for (int i = threadIdx.x; i < GW; i += blockDim.x) {
     sg[i] = sum_slices(gate + (size_t)r * GW + i, nsl, (size_t)rows * GW);
@@ -812,7 +812,7 @@ __global__ void __launch_bounds__(256) k_gconv_cl(const GconvArgs<bf16> A, int N
     for (int r = 0; r < C; ++r) a += ld_dsmem(smem_u32(&s_part[tid]), (uint32_t)r);
     s_tot[tid] = a;
   }
-  // this CTA is done reading its peers' shared memory; it waits for theirs
+  // this CTA is done reading its peers' shared memory; it waits for their
   // reads of its own only before it exits
   cluster_arrive_relaxed();
   __syncthreads();
