@@ -42,6 +42,9 @@ CASES = [
     # 256 channels a conv CTA at 16 rows: the post conv writes no sums of squares and
     # the pre conv forms its own through the cluster
     ("small_gqa", 2, 8, [200, 129], {"conv_group": 128}),
+    # 80 requests (640 block rows): one key split per (request, kv head), the attention's
+    # single-split form; ragged contexts 5..403 around the 128-token window
+    ("small_gqa", 80, 8, [5 + (37 * i) % 400 for i in range(80)], {}),
 ]
 
 
