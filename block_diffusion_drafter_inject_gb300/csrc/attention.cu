@@ -756,9 +756,10 @@ AttnPlan attn_plan(int B, int K, int Hq, int Hkv, int dh, int window, int num_sm
   const long items = (long)B * Hkv * pl.nqg;
   // smallest key split (multiple of 64) that still gives ~2 CTAs per SM; at
   // most 16 splits (the splits of one item form a thread-block cluster), the
-  // last one taking the keys left over
+  // last one also taking the keys left over, at most another split's worth
   int kps = dfl::kCH;
-  while (kps < n_keys && (long)items * std::min(16, (n_keys + kps - 1) / kps) > 2L * num_sms)
+  while (kps < n_keys && ((long)items * std::min(16, (n_keys + kps - 1) / kps) > 2L * num_sms ||
+                          n_keys - 16 * kps > kps))
     kps += dfl::kCH;
   pl.kps = kps;
   pl.nsplit = std::min(16, (n_keys + kps - 1) / kps);

@@ -179,12 +179,15 @@ def test_topk_heavy_ties(pattern):
         np.testing.assert_array_equal(g["ids"][0, 0], np.arange(k))
 
 
+@pytest.mark.parametrize("window", [1050, 1200])
 @pytest.mark.parametrize("name", ["tiny", "tiny_bf16"])
-def test_long_window_last_split_takes_the_rest(name):
+def test_long_window_leftover_keys(name, window):
     """A window of more than 16 key tiles: the attention's key splits are capped
-    at 16 (one thread-block cluster) and the last split takes every remaining
-    key; logits still match the oracle."""
-    c = Case(name, 1, 8, [1300], seed=5, window=1200).device()
+    at 16 (one thread-block cluster).  1050 + 8 keys: 16 splits of 64 keys and
+    the last also takes the 34 left over; 1200 + 8: more than a split's worth
+    would be left over, so the splits widen instead.  Logits still match the
+    oracle."""
+    c = Case(name, 1, 8, [1300], seed=5, window=window).device()
     g = c.run_device()
     assert g["status"] == 0
     err = rowmax_rel(g["logits"], c.oracle()["logits"])
