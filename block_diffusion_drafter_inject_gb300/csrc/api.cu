@@ -515,8 +515,12 @@ static int run_draft(const dflash_config &c, const dflash_weights &w, const dfla
     return q4 ? with_q4(g, w.layer[l].w_down_q4, F) : g;
   };
   auto lm_call = [&]() {
-    GemmCall gl = reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, GemmPlan{0, 1}, GEMM_REDUCE,
-                              logits, V, nullptr, 0);
+    // more than 128 draft rows: two-SM tiles, each SM taking in half of the
+    // 256-token tile per k-block (one-SM tiles are bound by those bytes)
+    const GemmPlan pl =
+        c.dtype == DFLASH_BF16 && !q4 && TL > 128 ? GemmPlan{256, 1, 0, 1} : GemmPlan{0, 1};
+    GemmCall gl = reduce_call(c, ws, L, w.lm_head, V, D, zf, TL, pl, GEMM_REDUCE, logits, V,
+                              nullptr, 0);
     gl.stats = tstats;
     return q4 ? with_q4(gl, w.lm_head_q4, D) : gl;
   };

@@ -1011,7 +1011,9 @@ struct PairShape {
 __device__ __forceinline__ bool get_seg_pair(const GemmParams &p, int i, uint32_t rank, Seg &s) {
   const int u = (int)(blockIdx.x >> 1) + i * (int)(gridDim.x >> 1);
   if (u >= p.num_units) return false;
-  const int split = u % p.S, tile = u / p.S, mpairs = p.m_tiles >> 1;
+  // an odd tile count: the last pair's odd CTA holds a phantom tile (rows past
+  // the weights: zero-filled loads, nothing stored)
+  const int split = u % p.S, tile = u / p.S, mpairs = (p.m_tiles + 1) >> 1;
   int mp, t;
   if (p.m_fastest) {
     mp = tile % mpairs;
@@ -1037,7 +1039,9 @@ __device__ __forceinline__ void load_w_pair(uint8_t *dst, const WMaps &maps, uin
     tma_load_2d_pair(dst, &maps.m[0], bar_cl, kx, m_tile * 64, pol);
     tma_load_2d_pair(dst + 64 * BK * 2, &maps.m[0], bar_cl, kx, p.F + m_tile * 64, pol);
   } else {
-    const int g = m_tile / p.mtg;
+    // a phantom tile (m_tile == m_tiles, one weight group) reads past the
+    // group's rows: the load fills zeros
+    const int g = min(m_tile / p.mtg, p.m_tiles / p.mtg - 1);
     tma_load_2d_pair(dst, &maps.m[g], bar_cl, kx, (m_tile - g * p.mtg) * BM, pol);
   }
 }
@@ -1227,7 +1231,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       const int tcol0 = t_tile * BN;
-      if (p.mode == 0) {
+      if (m_tile >= p.m_tiles) {
+        // a phantom tile: nothing to store (every CTA of it skips, tickets too)
+      } else if (p.mode == 0) {
         const int n = m_tile * BM + row;
         float *outp = p.out + (size_t)split * p.T * p.ld + n;
 #pragma unroll 1
@@ -1782,7 +1788,7 @@ static int launch_tc2(const GemmCall &g, cudaStream_t st, const Dev *d) {
   dfl::GemmParams p;
   if (make_params(g, dfl::kPairBN, d->num_sms, p) < 0) return DFLASH_ERR_DIMS;
   p.pair = 1;
-  p.num_units = (p.m_tiles / 2) * p.t_tiles * p.S;
+  p.num_units = ((p.m_tiles + 1) / 2) * p.t_tiles * p.S;
   const int clusters = std::min(p.num_units, d->num_sms / 2);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters);
@@ -1804,11 +1810,12 @@ static int launch_tc2(const GemmCall &g, cudaStream_t st, const Dev *d) {
 }
 
 // Whether a call can run on two-SM tiles: bf16, uniform schedule, and weight
-// tiles that pair up inside every weight group.
+// tiles that pair up inside every weight group (an odd count only with one
+// group in reduce mode: the last pair's second tile is a phantom).
 static bool pair_ok(const GemmCall &g) {
   if (g.dtype != DFLASH_BF16 || g.chunk != 0 || g.stall) return false;
   const int mtg = g.mode == GEMM_SWIGLU ? g.N_out / 64 : (g.N_out + dfl::BM - 1) / dfl::BM;
-  return mtg % 2 == 0;
+  return mtg % 2 == 0 || (g.groups == 1 && g.mode == GEMM_REDUCE);
 }
 
 int gemm_run(const GemmCall &g, cudaStream_t st) {

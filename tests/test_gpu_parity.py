@@ -43,8 +43,12 @@ CASES = [
     # the pre conv forms its own through the cluster
     ("small_gqa", 2, 8, [200, 129], {"conv_group": 128}),
     # 80 requests (640 block rows): one key split per (request, kv head), the attention's
-    # single-split form; ragged contexts 5..403 around the 128-token window
+    # single-split form; ragged contexts 5..403 around the 128-token window; the lm_head
+    # over 560 draft rows on two-SM tiles with an odd weight-tile count (71: the last
+    # pair's second tile is a phantom)
     ("small_gqa", 80, 8, [5 + (37 * i) % 400 for i in range(80)], {}),
+    # 140 draft rows: the lm_head on two-SM tiles, 40 weight tiles with a partial last one
+    ("small", 20, 8, [3 + (29 * i) % 150 for i in range(20)], {}),
 ]
 
 
