@@ -50,11 +50,12 @@ __global__ void __launch_bounds__(512) k_embed_norm(const S *__restrict__ E,
                                                     float2 *__restrict__ rope_cs,
                                                     float *__restrict__ ssq_out) {
   __shared__ float red[32];
-  // The first kernel of a draft pass releases its dependents only when it
-  // completes (no early trigger): every later kernel of the pass therefore
-  // starts after all work queued before the pass (the injection of context
-  // K/V above all) has completed, and may read the caches before its own wait.
+  // The first kernel of a draft pass releases its dependents only once its
+  // own wait has returned: every later kernel of the pass therefore starts
+  // after all work queued before the pass (the injection of context K/V above
+  // all) has completed, and may read the caches before its own wait.
   pdl_wait();
+  pdl_launch();
   const int r = blockIdx.x, b = r / K, i = r % K;
   int tok = i == 0 ? anchor[b] : mask_id;
   if (tok < 0 || tok >= V) {
