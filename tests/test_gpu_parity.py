@@ -49,6 +49,9 @@ CASES = [
     ("small_gqa", 80, 8, [5 + (37 * i) % 400 for i in range(80)], {}),
     # 140 draft rows: the lm_head on two-SM tiles, 40 weight tiles with a partial last one
     ("small", 20, 8, [3 + (29 * i) % 150 for i in range(20)], {}),
+    # 129 draft rows, the fewest that take the two-SM lm_head (one 256-token tile, one real
+    # row in its second half)
+    ("tiny_bf16", 43, 4, [(11 * i) % 70 for i in range(43)], {}),
 ]
 
 
