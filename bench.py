@@ -663,10 +663,15 @@ def bench_inject(torch, dfl, cfg, Wd, pk, args):
     g_inj = capture(torch, inject)
     g_cyc = capture(torch, cycle)
     steps = max(3, min(args.steps, 20))
+    # the cycle is timed first, on the context one injection wrote: timed after the
+    # injection's replays it would inherit the clock that seconds of tensor-bound
+    # work leave behind (it moved by ~10 % with the injection's own speed)
+    g_inj.replay()
+    torch.cuda.synchronize()
+    ms_cyc = event_time(torch, g_cyc.replay, max(5, args.steps // 2), args.warmup)
     torch.cuda.nvtx.range_push("inject_32k")  # lets a profiler select these launches
     ms_inj = event_time(torch, g_inj.replay, steps, args.warmup)
     torch.cuda.nvtx.range_pop()
-    ms_cyc = event_time(torch, g_cyc.replay, max(5, args.steps // 2), args.warmup)
     status = dfl.read_device_status(cyc.ws)
     fl = inject_flops(cfg, N)
     t_tc = fl / (pk["bf16_sus"] * 1e12)
